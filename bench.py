@@ -1,0 +1,448 @@
+"""Benchmark of the blockwise-FP8 linear-layer step on GB300.
+
+One step = the whole hot path over one batch: quantise x (1x128 along K) and
+W (128x128 tiles), forward GEMM 1x128 x 128x128; quantise dY (1x128 along N),
+W^T tiles, input-gradient GEMM 1x128 x 128x128; quantise dY^T (1x128 along M)
+and x (128x1 along M), weight-gradient GEMM 1x128 x 128x1.
+
+Default workload: the pages' mid shape M=2048, N=4096, K=4096 (x ~N(0,1) with
+0.1% x100 outliers, W ~N(0,0.02), dY ~N(0,1e-3)), L2 flushed between steps.
+
+value = GEMM FLOPs of the step (3 * 2MNK) / device time of the whole step
+(quantisation included), TFLOP/s.  Per-kernel times come from CUDA events on
+the launching stream.  `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synthetic as S  # noqa: E402
+
+WORKLOADS = {
+    "mid": S.FWD_MID,          # 2048 x 4096 x 4096
+    "square": S.FWD_SQUARE,    # 8192 x 8192 x 8192
+    "mlp_up": S.MLP_UP,        # 16384 x 14336 x 4096
+}
+METRIC = "blockwise FP8 GEMM TFLOPS & quant GB/s at 1 GB300, % of FP8/HBM roofline"
+L2_FLUSH_BYTES = 256 << 20
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+GEMM_SRC = os.path.join(ROOT, "blockwise_scaled_fp8_gb300", "csrc", "gemm.cu")
+QUANT_SRC = os.path.join(ROOT, "blockwise_scaled_fp8_gb300", "csrc", "quant.cu")
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def _sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _profile_traffic(kernel_key: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if its source hash
+    matches the current kernel source; else None."""
+    fname = os.path.join(PROFILE_DIR, f"{kernel_key}_{workload}.md")
+    if not os.path.exists(fname):
+        return None
+    vals = {}
+    with open(fname) as f:
+        for line in f:
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    src = GEMM_SRC if kernel_key.startswith("gemm") else QUANT_SRC
+    if vals.get("source_sha") != _sha(src):
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"bfp8_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "200"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg (the reported baseline; also the whole `--impl reference` arm)
+# ---------------------------------------------------------------------------
+
+def oracle_step_sample(x, w, dy, rows, nrows):
+    """One bounded sample of the step on the CPU oracle: forward and
+    input-gradient outputs for `rows` token rows, weight-gradient outputs for
+    `nrows` output features, each with every quantisation it needs.
+    Returns the GEMM FLOPs the sample covers."""
+    import oracle as O
+    M, K = x.shape
+    N = w.shape[0]
+    qa, sa = O.quant_lhs(np.ascontiguousarray(x[rows]))
+    qw, qwt, sw = O.quant_weight(w, with_t=True)
+    O.gemm(qa, sa, qw, sw, O.SB_TILE, K)
+    qd, sd = O.quant_lhs(np.ascontiguousarray(dy[rows]))
+    O.gemm(qd, sd, qwt, sw, O.SB_TILE_T, N)
+    qdt, sdt = O.quant_lhs(np.ascontiguousarray(dy[:, nrows]), transposed=True)
+    qxt, sxt = O.quant_rhs(x)
+    O.gemm(qdt, sdt, qxt, sxt, O.SB_COL, M)
+    return 2.0 * (len(rows) * N * K + len(rows) * K * N + len(nrows) * K * M)
+
+
+def run_reference(args, wl):
+    import oracle as O
+    O.build()
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    x, w, dy = wl.x(), wl.w(), wl.dy()
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(wl.M, size=args.ref_rows, replace=False))
+    nrows = np.sort(rng.choice(wl.N, size=args.ref_rows, replace=False))
+    for _ in range(args.warmup):
+        oracle_step_sample(x, w, dy, rows, nrows)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(args.steps):
+        flops += oracle_step_sample(x, w, dy, rows, nrows)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    cores = O._threads()
+    sample = (f"{args.ref_rows} of {wl.M} token rows (fwd, dgrad) and {args.ref_rows} of {wl.N} "
+              f"output features (wgrad), with full W and x quantisation, per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU leg
+# ---------------------------------------------------------------------------
+
+class Step:
+    """Preallocated buffers and the kernel sequence of one linear step, each
+    call recorded between CUDA events on the current stream."""
+
+    def __init__(self, wl, torch, B, dev):
+        self.wl, self.torch, self.B = wl, torch, B
+        M, N, K = wl.M, wl.N, wl.K
+        rup = lambda a, b: (a + b - 1) // b * b
+        cd = lambda a: (a + 127) // 128
+        u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
+        e = lambda *s, dt: torch.empty(s, dtype=dt, device=dev)
+        self.qx, self.sx = e(M, rup(K, 16), dt=u8), e(cd(K), rup(M, 4), dt=f32)
+        self.qw, self.sw = e(N, rup(K, 16), dt=u8), e(cd(N), cd(K), dt=f32)
+        self.qdy, self.sdy = e(M, rup(N, 16), dt=u8), e(cd(N), rup(M, 4), dt=f32)
+        self.qwt, self.sw2 = e(K, rup(N, 16), dt=u8), e(cd(N), cd(K), dt=f32)
+        self.qdyt, self.sdyt = e(N, rup(M, 16), dt=u8), e(cd(M), rup(N, 4), dt=f32)
+        self.qxt, self.sxt = e(K, rup(M, 16), dt=u8), e(cd(M), rup(K, 4), dt=f32)
+        self.y, self.dx, self.dw = e(M, N, dt=bf), e(M, K, dt=bf), e(N, K, dt=bf)
+        self.names = ["quant_lhs_x", "quant_weight_w", "gemm_fwd", "quant_lhs_dy", "quant_weight_wt",
+                      "gemm_dgrad", "quant_lhs_dyT", "quant_rhs_x", "gemm_wgrad"]
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(len(self.names) + 1)]
+        self.launches_per_step = len(self.names)
+
+    def run(self, x, w, dy, timed=True):
+        B, wl = self.B, self.wl
+        M, N, K = wl.M, wl.N, wl.K
+        ev = self.events
+        calls = [
+            lambda: B.quant_lhs(x, q=self.qx, s=self.sx),
+            lambda: B.quant_weight(w, with_q=True, with_t=False, q=self.qw, s=self.sw),
+            lambda: B.gemm_1x128_128x128(self.qx, self.sx, self.qw, self.sw, K, out=self.y, M=M, N=N),
+            lambda: B.quant_lhs(dy, q=self.qdy, s=self.sdy),
+            lambda: B.quant_weight(w, with_q=False, with_t=True, qt=self.qwt, s=self.sw2),
+            lambda: B.gemm_1x128_128x128(self.qdy, self.sdy, self.qwt, self.sw2, N, sb_transposed=True,
+                                         out=self.dx, M=M, N=K),
+            lambda: B.quant_lhs(dy, transposed=True, q=self.qdyt, s=self.sdyt),
+            lambda: B.quant_rhs(x, q=self.qxt, s=self.sxt),
+            lambda: B.gemm_1x128_128x1(self.qdyt, self.sdyt, self.qxt, self.sxt, M, out=self.dw, M=N, N=K),
+        ]
+        if timed:
+            ev[0].record()
+        for i, c in enumerate(calls):
+            c()
+            if timed:
+                ev[i + 1].record()
+
+    def kernel_ms(self):
+        ev = self.events
+        return [ev[i].elapsed_time(ev[i + 1]) for i in range(len(self.names))]
+
+
+def algorithmic_units(wl):
+    """Per-launch algorithmic work: FLOPs for the GEMMs, bytes for the quants
+    (read 2 B/elem bf16, write 1 B/elem e4m3, plus 4 B per scale)."""
+    M, N, K = wl.M, wl.N, wl.K
+    cd = lambda a: (a + 127) // 128
+    gem = 2.0 * M * N * K
+    return {
+        "quant_lhs_x": ("GB/s", 3.0 * M * K + 4.0 * M * cd(K)),
+        "quant_weight_w": ("GB/s", 3.0 * N * K + 4.0 * cd(N) * cd(K)),
+        "gemm_fwd": ("TFLOP/s", gem),
+        "quant_lhs_dy": ("GB/s", 3.0 * M * N + 4.0 * M * cd(N)),
+        "quant_weight_wt": ("GB/s", 3.0 * N * K + 4.0 * cd(N) * cd(K)),
+        "gemm_dgrad": ("TFLOP/s", gem),
+        "quant_lhs_dyT": ("GB/s", 3.0 * M * N + 4.0 * N * cd(M)),
+        "quant_rhs_x": ("GB/s", 3.0 * M * K + 4.0 * K * cd(M)),
+        "gemm_wgrad": ("TFLOP/s", gem),
+    }
+
+
+def run_gpu(args, wl):
+    import torch
+
+    import blockwise_scaled_fp8_gb300 as B
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    B.build()
+    dev = torch.device("cuda", local)
+
+    def todev(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    xh, wh, dyh = wl.x(), wl.w(), wl.dy()
+    x, w, dy = todev(xh), todev(wh), todev(dyh)
+    step = Step(wl, torch, B, dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    for _ in range(args.warmup):
+        step.run(x, w, dy, timed=False)
+        flush.fill_(1.0)
+    torch.cuda.synchronize()
+    B.check_device_errors()
+
+    step_ms, per_kernel = [], []
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for _ in range(args.steps):
+            flush.fill_(0.0)  # L2 flush between timed steps (outside the step's events)
+            step.run(x, w, dy, timed=True)
+            torch.cuda.synchronize()
+            per_kernel.append(step.kernel_ms())
+            step_ms.append(step.events[0].elapsed_time(step.events[-1]))
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    B.check_device_errors()
+    clocks = clk.summary()
+
+    total_ms = float(sum(step_ms))
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    flops_step = 3 * wl.gemm_flops
+    value = world * flops_step * args.steps / (total_ms / 1e3) / 1e12
+
+    # per-kernel averages, rooflines
+    units = algorithmic_units(wl)
+    peaks = _peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]  # fp8 dense = 2 x bf16 dense (nominal ratio)
+    avg = np.mean(np.array(per_kernel), axis=0)
+    parts = {}
+    for name, ms in zip(step.names, avg):
+        unit, work = units[name]
+        if unit == "TFLOP/s":
+            ach = work / (ms / 1e3) / 1e12
+            parts[name] = {"ms": round(float(ms), 5), "TFLOP/s": round(ach, 2), "frac_fp8_peak": round(ach / fp8_peak, 4)}
+        else:
+            ach = work / (ms / 1e3) / 1e9
+            parts[name] = {"ms": round(float(ms), 5), "GB/s": round(ach, 1), "frac_hbm": round(ach / peaks["hbm_gbs"], 4)}
+    dom = max(range(len(step.names)), key=lambda i: avg[i])
+    dname = step.names[dom]
+    unit, work = units[dname]
+    if unit == "TFLOP/s":
+        ach = work / (avg[dom] / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": fp8_peak, "unit": "TFLOP/s", "frac": ach / fp8_peak}
+        peak_note = f"{peaks['source']} bf16 burst {peaks['bf16_tflops']} x 2 (fp8/bf16 nominal ratio)"
+    else:
+        ach = work / (avg[dom] / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"]}
+        peak_note = f"{peaks['source']} HBM copy bandwidth"
+    kkey = "gemm_1x128_128x128" if dname in ("gemm_fwd", "gemm_dgrad") else (
+        "gemm_1x128_128x1" if dname == "gemm_wgrad" else dname)
+    roof["traffic"] = _profile_traffic(kkey, wl.name)
+    roof["kernel"] = dname
+    roof["peak_source"] = peak_note
+
+    # end to end through the public API: host (pinned) -> device, fwd + bwd, device -> host
+    e2e = None
+    if not args.no_e2e:
+        hx = torch.from_numpy(xh.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hw = torch.from_numpy(wh.view(np.int16)).view(torch.bfloat16).pin_memory()
+        hdy = torch.from_numpy(dyh.view(np.int16)).view(torch.bfloat16).pin_memory()
+        M, N, K = wl.M, wl.N, wl.K
+        oy = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+        odx = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
+        odw = torch.empty((N, K), dtype=torch.bfloat16).pin_memory()
+        dx_, dw_, dy_ = torch.empty_like(x), torch.empty_like(w), torch.empty_like(dy)
+        ws = torch.empty(B.linear_workspace_size(M, N, K) + 256, dtype=torch.uint8, device=dev)
+        y_ = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        gx, gdx = torch.empty_like(x), torch.empty((M, K), dtype=torch.bfloat16, device=dev)
+        gdw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+
+        def e2e_step():
+            gx.copy_(hx, non_blocking=True)
+            dw_.copy_(hw, non_blocking=True)
+            dy_.copy_(hdy, non_blocking=True)
+            B.linear_fwd(gx, dw_, y=y_, ws=ws)
+            B.linear_bwd(dy_, gx, dw_, dx=gdx, dw=gdw, ws=ws)
+            oy.copy_(y_, non_blocking=True)
+            odx.copy_(gdx, non_blocking=True)
+            odw.copy_(gdw, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        tot = 0.0
+        for _ in range(args.steps):
+            flush.fill_(0.0)
+            s0.record()
+            e2e_step()
+            s1.record()
+            torch.cuda.synchronize()
+            tot += s0.elapsed_time(s1)
+        e2e = {"value": flops_step * args.steps / (tot / 1e3) / 1e12 * world, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(2 * (M * K + N * K + M * N)),
+               "d2h_bytes_per_step": int(2 * (M * N + M * K + N * K)),
+               "ms_per_step": tot / args.steps}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        import oracle as O
+        O.build()
+        rng = np.random.default_rng(0)
+        rows = np.sort(rng.choice(wl.M, size=args.ref_rows, replace=False))
+        nrows = np.sort(rng.choice(wl.N, size=args.ref_rows, replace=False))
+        t0 = time.perf_counter()
+        fl = oracle_step_sample(xh, wh, dyh, rows, nrows)
+        dt = time.perf_counter() - t0
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": O._threads(), "kind": "oracle",
+               "sample": f"{args.ref_rows} token rows (fwd, dgrad) + {args.ref_rows} output features (wgrad) "
+                         f"of the step, with full W and x quantisation; {dt:.1f} s"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)",
+                "data": "synthetic",
+                "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
+                           "step": "quant x,W + fwd GEMM; quant dY,W^T + dgrad GEMM; quant dY^T,x + wgrad GEMM",
+                           "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
+                "gpu_launches": step.launches_per_step * args.steps,
+                "roofline": roof, "parts": parts, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks}
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mid", choices=sorted(WORKLOADS))
+    ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_gpu(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

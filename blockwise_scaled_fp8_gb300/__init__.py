@@ -1,0 +1,273 @@
+"""Python binding of libbfp8 (blockwise-scaled FP8 quantisation and GEMMs, sm_103a).
+
+Argument marshalling only: every step runs in the library's CUDA kernels,
+called through the C ABI declared in ``include/bfp8.h``.  PyTorch provides
+device memory and the current stream.  There is no CPU fallback: if the
+library is missing or the device is not sm_103, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbfp8.so")
+BLOCK = 128
+
+BFP8_OK, BFP8_ERR_INVALID_ARG, BFP8_ERR_UNSUPPORTED, BFP8_ERR_CUDA, BFP8_ERR_TIMEOUT = range(5)
+
+EXPORTS = [
+    "bfp8_last_error", "bfp8_quant_lhs", "bfp8_quant_rhs", "bfp8_quant_weight",
+    "bfp8_gemm_1x128_128x128", "bfp8_gemm_1x128_128x1", "bfp8_linear_workspace_size",
+    "bfp8_linear_fwd", "bfp8_linear_bwd", "bfp8_cast_e4m3", "bfp8_check_device_errors",
+    "bfp8_debug_write_counts",
+]
+
+_lib = None
+
+
+class Bfp8Error(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"bfp8 status {status}: {msg}")
+        self.status = status
+
+
+def build(force: bool = False) -> str:
+    from . import buildlib as _b
+    return _b.build(force=force)
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libbfp8.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with blockwise_scaled_fp8_gb300.build()")
+    L = ctypes.CDLL(LIB_PATH)
+    i64, i32, vp, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
+    L.bfp8_last_error.restype = ctypes.c_char_p
+    L.bfp8_last_error.argtypes = []
+    L.bfp8_quant_lhs.argtypes = [vp, i64, i64, i64, i32, vp, i64, vp, i64, vp]
+    L.bfp8_quant_rhs.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp]
+    L.bfp8_quant_weight.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp]
+    L.bfp8_gemm_1x128_128x128.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, vp, i64, i64, i64, i64, vp]
+    L.bfp8_gemm_1x128_128x1.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, i64, vp]
+    L.bfp8_linear_workspace_size.argtypes = [i64, i64, i64]
+    L.bfp8_linear_workspace_size.restype = sz
+    L.bfp8_linear_fwd.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
+    L.bfp8_linear_bwd.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp, sz, vp]
+    L.bfp8_cast_e4m3.argtypes = [vp, i64, vp, vp]
+    L.bfp8_check_device_errors.argtypes = [vp]
+    L.bfp8_debug_write_counts.argtypes = [i32, i64, i64, i64, i32, vp, vp, ctypes.POINTER(i64)]
+    for name in EXPORTS:
+        if name not in ("bfp8_last_error", "bfp8_linear_workspace_size"):
+            getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _check(status: int) -> None:
+    if status != BFP8_OK:
+        raise Bfp8Error(status, lib().bfp8_last_error().decode(errors="replace"))
+
+
+def _cdiv(a: int, b: int) -> int:
+    return (a + b - 1) // b
+
+
+def _rup(a: int, b: int) -> int:
+    return _cdiv(a, b) * b
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream():
+    return ctypes.c_void_p(_torch().cuda.current_stream().cuda_stream)
+
+
+def _p(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(None)
+
+
+def _need_bf16_2d(t, name):
+    torch = _torch()
+    if t.dtype != torch.bfloat16 or t.dim() != 2 or not t.is_cuda or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D CUDA bf16 tensor with unit column stride")
+
+
+# ---------------------------------------------------------------------------
+# Quantisation
+# ---------------------------------------------------------------------------
+
+def quant_lhs(x, transposed: bool = False, q=None, s=None):
+    """1x128 groups along K of A = x ([M,K]) or A = x^T (x is [K,M]).
+    Returns (q [M, ldq] uint8 e4m3 bytes, s [Kb, lds] float32), where s[kb, m]
+    is the scale of row m's group kb (the column-major [M, Kb] layout)."""
+    torch = _torch()
+    _need_bf16_2d(x, "x")
+    if transposed:
+        K, M = x.shape
+    else:
+        M, K = x.shape
+    Kb = _cdiv(K, BLOCK)
+    if q is None:
+        q = torch.empty((M, _rup(max(K, 1), 16)), dtype=torch.uint8, device=x.device)
+    if s is None:
+        s = torch.empty((Kb, max(M, 1)), dtype=torch.float32, device=x.device)
+    _check(lib().bfp8_quant_lhs(_p(x), M, K, x.stride(0), int(transposed), _p(q), q.stride(0),
+                                _p(s), s.stride(0), _stream()))
+    return q, s
+
+
+def quant_rhs(x, q=None, s=None):
+    """128x1 groups along the rows (reduction dim K) of x [K,N]; bytes written
+    transposed.  Returns (qT [N, ldq] uint8, s [Kb, lds] float32)."""
+    torch = _torch()
+    _need_bf16_2d(x, "x")
+    K, N = x.shape
+    Kb = _cdiv(K, BLOCK)
+    if q is None:
+        q = torch.empty((N, _rup(max(K, 1), 16)), dtype=torch.uint8, device=x.device)
+    if s is None:
+        s = torch.empty((Kb, _rup(max(N, 1), 4)), dtype=torch.float32, device=x.device)
+    _check(lib().bfp8_quant_rhs(_p(x), K, N, x.stride(0), _p(q), q.stride(0), _p(s), s.stride(0), _stream()))
+    return q, s
+
+
+def quant_weight(w, with_q: bool = True, with_t: bool = False, q=None, qt=None, s=None):
+    """128x128 tiles of w [N,K].  Returns (q [N, ldq] or None, qt [K, ldqt] or
+    None, s [Nb, lds] float32)."""
+    torch = _torch()
+    _need_bf16_2d(w, "w")
+    N, K = w.shape
+    Nb, Kb = _cdiv(N, BLOCK), _cdiv(K, BLOCK)
+    if with_q and q is None:
+        q = torch.empty((N, _rup(max(K, 1), 16)), dtype=torch.uint8, device=w.device)
+    if with_t and qt is None:
+        qt = torch.empty((K, _rup(max(N, 1), 16)), dtype=torch.uint8, device=w.device)
+    if s is None:
+        s = torch.empty((max(Nb, 1), max(Kb, 1)), dtype=torch.float32, device=w.device)
+    _check(lib().bfp8_quant_weight(_p(w), N, K, w.stride(0), _p(q), q.stride(0) if q is not None else 0,
+                                   _p(qt), qt.stride(0) if qt is not None else 0, _p(s), s.stride(0),
+                                   _stream()))
+    return q, qt, s
+
+
+def cast_e4m3(x, q=None):
+    """Elementwise RNE fp32 -> e4m3fn with saturation to +-448."""
+    torch = _torch()
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA float32 tensor")
+    if q is None:
+        q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(lib().bfp8_cast_e4m3(_p(x), x.numel(), _p(q), _stream()))
+    return q
+
+
+# ---------------------------------------------------------------------------
+# GEMMs
+# ---------------------------------------------------------------------------
+
+def gemm_1x128_128x128(qa, sa, qb, sb, K: int, sb_transposed: bool = False, out=None, M=None, N=None):
+    """C = A B with A = qa [M, lda] (1x128 scales sa [Kb, ldsa]), B^T = qb
+    [N, ldb] (128x128 tile scales sb, [Nb, ldsb] or transposed [Kb, ldsb]).
+    Returns C [M, N] bf16."""
+    torch = _torch()
+    M = qa.shape[0] if M is None else M
+    N = qb.shape[0] if N is None else N
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
+    _check(lib().bfp8_gemm_1x128_128x128(_p(qa), qa.stride(0), _p(sa), sa.stride(0), _p(qb), qb.stride(0),
+                                         _p(sb), sb.stride(0), int(sb_transposed), _p(out), out.stride(0),
+                                         M, N, K, _stream()))
+    return out
+
+
+def gemm_1x128_128x1(qa, sa, qb, sb, K: int, out=None, M=None, N=None):
+    """C = A B with A = qa [M, lda] (1x128 scales sa [Kb, ldsa]) and B^T = qb
+    [N, ldb] with one scale per column and K-block, sb [Kb, ldsb]."""
+    torch = _torch()
+    M = qa.shape[0] if M is None else M
+    N = qb.shape[0] if N is None else N
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
+    _check(lib().bfp8_gemm_1x128_128x1(_p(qa), qa.stride(0), _p(sa), sa.stride(0), _p(qb), qb.stride(0),
+                                       _p(sb), sb.stride(0), _p(out), out.stride(0), M, N, K, _stream()))
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Linear layer
+# ---------------------------------------------------------------------------
+
+def linear_workspace_size(M: int, N: int, K: int) -> int:
+    return int(lib().bfp8_linear_workspace_size(M, N, K))
+
+
+def _workspace(M, N, K, device, ws):
+    torch = _torch()
+    need = linear_workspace_size(M, N, K)
+    if ws is None:
+        ws = torch.empty(max(need, 256) + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    if ws.numel() - off < need:
+        raise ValueError(f"workspace too small: {ws.numel() - off} < {need}")
+    return ws, ctypes.c_void_p(ws.data_ptr() + off), ws.numel() - off
+
+
+def linear_fwd(x, w, y=None, ws=None):
+    """y = x W^T through blockwise FP8 (x [M,K], w [N,K] bf16 contiguous)."""
+    torch = _torch()
+    M, K = x.shape
+    N = w.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    ws, wp, wn = _workspace(M, N, K, x.device, ws)
+    _check(lib().bfp8_linear_fwd(_p(x), _p(w), _p(y), M, N, K, wp, wn, _stream()))
+    return y
+
+
+def linear_bwd(dy, x, w, dx=None, dw=None, ws=None):
+    """dx = dy W, dw = dy^T x through blockwise FP8."""
+    torch = _torch()
+    M, K = x.shape
+    N = w.shape[0]
+    if dx is None:
+        dx = torch.empty((M, K), dtype=torch.bfloat16, device=x.device)
+    if dw is None:
+        dw = torch.empty((N, K), dtype=torch.bfloat16, device=x.device)
+    ws, wp, wn = _workspace(M, N, K, x.device, ws)
+    _check(lib().bfp8_linear_bwd(_p(dy), _p(x), _p(w), _p(dx), _p(dw), M, N, K, wp, wn, _stream()))
+    return dx, dw
+
+
+def check_device_errors() -> None:
+    """Synchronises the current stream; raises if a GEMM gave up on a bounded wait."""
+    _check(lib().bfp8_check_device_errors(_stream()))
+
+
+# ---------------------------------------------------------------------------
+# Host replay of the kernels' index arithmetic (no GPU)
+# ---------------------------------------------------------------------------
+
+def debug_write_counts(kind: int, M: int, N: int, K: int, flag: int = 0):
+    """Per-element write counts a launch would produce.  Returns
+    (counts [rows, cols], scale_counts or None, out_of_range_writes)."""
+    shapes = {0: ((K, M) if flag else (M, K)), 1: (N, K), 2: (N, K), 3: (M, N), 4: (K, N)}
+    rows, cols = shapes[kind]
+    if kind == 0 and flag:
+        rows, cols = M, K
+    counts = np.zeros((rows, cols), dtype=np.uint32)
+    sshape = {0: (_cdiv(K, BLOCK), M), 1: (_cdiv(K, BLOCK), N), 2: (_cdiv(N, BLOCK), _cdiv(K, BLOCK))}.get(kind)
+    scounts = np.zeros(sshape, dtype=np.uint32) if sshape else None
+    oob = ctypes.c_int64(0)
+    _check(lib().bfp8_debug_write_counts(kind, M, N, K, flag, counts.ctypes.data_as(ctypes.c_void_p),
+                                         scounts.ctypes.data_as(ctypes.c_void_p) if scounts is not None else None,
+                                         ctypes.byref(oob)))
+    return counts, scounts, int(oob.value)

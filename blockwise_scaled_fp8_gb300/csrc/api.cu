@@ -1,0 +1,458 @@
+// C ABI of the library (declared in include/bfp8.h): argument validation,
+// device checks, the linear-layer composition and the host-side index replay.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+#include <vector>
+
+#include "../../include/bfp8.h"
+#include "index.cuh"
+#include "kernels.h"
+
+using namespace bfp8;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+bfp8_status fail(bfp8_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+bfp8_status cuda_fail(cudaError_t e, const char* where) {
+  return fail(BFP8_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+struct DevInfo {
+  int checked = 0;
+  int ok = 0;
+  int sms = 0;
+  int major = 0, minor = 0;
+};
+DevInfo g_dev[64];
+std::mutex g_dev_mu;
+
+// The kernels are built for sm_103a only.  Returns the SM count via *sms.
+bfp8_status check_device(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(BFP8_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.checked) {
+    cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    d.ok = (d.major == 10 && d.minor == 3);
+    d.checked = 1;
+  }
+  if (!d.ok)
+    return fail(BFP8_ERR_UNSUPPORTED, "bfp8 kernels are built for sm_103a (GB300); device %d is sm_%d%d",
+                dev, d.major, d.minor);
+  *sms = d.sms;
+  return BFP8_OK;
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool al4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool al2(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 1u) == 0; }
+constexpr int64_t kMaxDim = (int64_t)1 << 31;  // TMA coordinates are 32-bit signed
+int64_t rup(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+
+#define CHECK_ARG(cond, ...)                                  \
+  do {                                                        \
+    if (!(cond)) return fail(BFP8_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)
+
+bfp8_status check_dims(const char* fn, int64_t a, int64_t b, int64_t c = 1) {
+  CHECK_ARG(a >= 0 && b >= 0 && c >= 0, "%s: negative dimension", fn);
+  CHECK_ARG(a < kMaxDim && b < kMaxDim && c < kMaxDim, "%s: dimension >= 2^31", fn);
+  return BFP8_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* bfp8_last_error(void) { return g_msg; }
+
+bfp8_status bfp8_quant_lhs(const void* x, int64_t M, int64_t K, int64_t ldx, int x_transposed, void* q,
+                           int64_t ldq, float* s, int64_t lds, bfp8_stream_t stream) {
+  bfp8_status st = check_dims("bfp8_quant_lhs", M, K);
+  if (st != BFP8_OK) return st;
+  if (M == 0 || K == 0) return BFP8_OK;
+  CHECK_ARG(x && q && s, "bfp8_quant_lhs: null pointer");
+  CHECK_ARG(al2(x) && al16(q) && al4(s), "bfp8_quant_lhs: x must be 2-byte, q 16-byte, s 4-byte aligned");
+  CHECK_ARG(ldx >= (x_transposed ? M : K), "bfp8_quant_lhs: ldx=%lld < %s=%lld", (long long)ldx,
+            x_transposed ? "M" : "K", (long long)(x_transposed ? M : K));
+  CHECK_ARG(ldq >= K && ldq % 16 == 0, "bfp8_quant_lhs: ldq=%lld must be >= K=%lld and a multiple of 16",
+            (long long)ldq, (long long)K);
+  CHECK_ARG(lds >= M, "bfp8_quant_lhs: lds=%lld < M=%lld", (long long)lds, (long long)M);
+  int sms = 0;
+  if ((st = check_device(&sms)) != BFP8_OK) return st;
+  cudaError_t e;
+  if (x_transposed)
+    e = launch_quant_cols((const uint16_t*)x, K, M, ldx, (uint8_t*)q, ldq, s, lds, (cudaStream_t)stream);
+  else
+    e = launch_quant_rows((const uint16_t*)x, M, K, ldx, (uint8_t*)q, ldq, s, lds, sms, (cudaStream_t)stream);
+  return e == cudaSuccess ? BFP8_OK : cuda_fail(e, "bfp8_quant_lhs launch");
+}
+
+bfp8_status bfp8_quant_rhs(const void* x, int64_t K, int64_t N, int64_t ldx, void* qT, int64_t ldq, float* s,
+                           int64_t lds, bfp8_stream_t stream) {
+  bfp8_status st = check_dims("bfp8_quant_rhs", K, N);
+  if (st != BFP8_OK) return st;
+  if (K == 0 || N == 0) return BFP8_OK;
+  CHECK_ARG(x && qT && s, "bfp8_quant_rhs: null pointer");
+  CHECK_ARG(al2(x) && al16(qT) && al4(s), "bfp8_quant_rhs: x must be 2-byte, qT 16-byte, s 4-byte aligned");
+  CHECK_ARG(ldx >= N, "bfp8_quant_rhs: ldx=%lld < N=%lld", (long long)ldx, (long long)N);
+  CHECK_ARG(ldq >= K && ldq % 16 == 0, "bfp8_quant_rhs: ldq=%lld must be >= K=%lld and a multiple of 16",
+            (long long)ldq, (long long)K);
+  CHECK_ARG(lds >= N, "bfp8_quant_rhs: lds=%lld < N=%lld", (long long)lds, (long long)N);
+  int sms = 0;
+  if ((st = check_device(&sms)) != BFP8_OK) return st;
+  cudaError_t e = launch_quant_cols((const uint16_t*)x, K, N, ldx, (uint8_t*)qT, ldq, s, lds, (cudaStream_t)stream);
+  return e == cudaSuccess ? BFP8_OK : cuda_fail(e, "bfp8_quant_rhs launch");
+}
+
+bfp8_status bfp8_quant_weight(const void* w, int64_t N, int64_t K, int64_t ldw, void* q, int64_t ldq, void* qt,
+                              int64_t ldqt, float* s, int64_t lds, bfp8_stream_t stream) {
+  bfp8_status st = check_dims("bfp8_quant_weight", N, K);
+  if (st != BFP8_OK) return st;
+  if (N == 0 || K == 0) return BFP8_OK;
+  CHECK_ARG(w && s && (q || qt), "bfp8_quant_weight: null pointer (w, s, and one of q/qt are required)");
+  CHECK_ARG(al2(w) && al4(s), "bfp8_quant_weight: w must be 2-byte, s 4-byte aligned");
+  CHECK_ARG(ldw >= K, "bfp8_quant_weight: ldw=%lld < K=%lld", (long long)ldw, (long long)K);
+  if (q) {
+    CHECK_ARG(al16(q), "bfp8_quant_weight: q must be 16-byte aligned");
+    CHECK_ARG(ldq >= K && ldq % 16 == 0, "bfp8_quant_weight: ldq=%lld must be >= K=%lld and a multiple of 16",
+              (long long)ldq, (long long)K);
+  }
+  if (qt) {
+    CHECK_ARG(al16(qt), "bfp8_quant_weight: qt must be 16-byte aligned");
+    CHECK_ARG(ldqt >= N && ldqt % 16 == 0,
+              "bfp8_quant_weight: ldqt=%lld must be >= N=%lld and a multiple of 16", (long long)ldqt, (long long)N);
+  }
+  CHECK_ARG(lds >= cdiv(K, kBlock), "bfp8_quant_weight: lds=%lld < ceil(K/128)=%lld", (long long)lds,
+            (long long)cdiv(K, kBlock));
+  int sms = 0;
+  if ((st = check_device(&sms)) != BFP8_OK) return st;
+  cudaError_t e = launch_quant_weight((const uint16_t*)w, N, K, ldw, (uint8_t*)q, ldq, (uint8_t*)qt, ldqt, s, lds,
+                                      (cudaStream_t)stream);
+  return e == cudaSuccess ? BFP8_OK : cuda_fail(e, "bfp8_quant_weight launch");
+}
+
+static bfp8_status gemm_common(const char* fn, const GemmArgs& a, bfp8_stream_t stream) {
+  bfp8_status st = check_dims(fn, a.M, a.N, a.K);
+  if (st != BFP8_OK) return st;
+  if (a.M == 0 || a.N == 0) return BFP8_OK;
+  CHECK_ARG(a.qa && a.qb && a.sa && a.sb && a.c, "%s: null pointer", fn);
+  if (a.K == 0) {  // empty reduction: C = 0 on the logical [M,N] region
+    CHECK_ARG(a.ldc >= a.N, "%s: ldc=%lld < N=%lld", fn, (long long)a.ldc, (long long)a.N);
+    cudaError_t e = cudaMemset2DAsync(a.c, (size_t)a.ldc * 2, 0, (size_t)a.N * 2, (size_t)a.M,
+                                      (cudaStream_t)stream);
+    return e == cudaSuccess ? BFP8_OK : cuda_fail(e, fn);
+  }
+  CHECK_ARG(al16(a.qa) && al16(a.qb), "%s: qa and qb must be 16-byte aligned", fn);
+  CHECK_ARG(al4(a.sa) && al4(a.sb) && al2(a.c), "%s: sa/sb must be 4-byte and c 2-byte aligned", fn);
+  CHECK_ARG(a.lda >= a.K && a.lda % 16 == 0, "%s: lda=%lld must be >= K=%lld and a multiple of 16", fn,
+            (long long)a.lda, (long long)a.K);
+  CHECK_ARG(a.ldb >= a.K && a.ldb % 16 == 0, "%s: ldb=%lld must be >= K=%lld and a multiple of 16", fn,
+            (long long)a.ldb, (long long)a.K);
+  CHECK_ARG(a.ldsa >= a.M, "%s: ldsa=%lld < M=%lld", fn, (long long)a.ldsa, (long long)a.M);
+  const int64_t Kb = cdiv(a.K, kBlock), Nb = cdiv(a.N, kBlock);
+  if (a.sb_mode == kSbTile)
+    CHECK_ARG(a.ldsb >= Kb, "%s: ldsb=%lld < ceil(K/128)=%lld", fn, (long long)a.ldsb, (long long)Kb);
+  else if (a.sb_mode == kSbTileT)
+    CHECK_ARG(a.ldsb >= Nb, "%s: ldsb=%lld < ceil(N/128)=%lld", fn, (long long)a.ldsb, (long long)Nb);
+  else
+    CHECK_ARG(a.ldsb >= a.N, "%s: ldsb=%lld < N=%lld", fn, (long long)a.ldsb, (long long)a.N);
+  CHECK_ARG(a.ldc >= a.N, "%s: ldc=%lld < N=%lld", fn, (long long)a.ldc, (long long)a.N);
+  int sms = 0;
+  if ((st = check_device(&sms)) != BFP8_OK) return st;
+  const char* msg = nullptr;
+  cudaError_t e = launch_gemm(a, sms, (cudaStream_t)stream, &msg);
+  if (e != cudaSuccess) {
+    if (msg) return fail(BFP8_ERR_INVALID_ARG, "%s: %s", fn, msg);
+    return cuda_fail(e, fn);
+  }
+  return BFP8_OK;
+}
+
+bfp8_status bfp8_gemm_1x128_128x128(const void* qa, int64_t lda, const float* sa, int64_t ldsa, const void* qb,
+                                    int64_t ldb, const float* sb, int64_t ldsb, int sb_transposed, void* c,
+                                    int64_t ldc, int64_t M, int64_t N, int64_t K, bfp8_stream_t stream) {
+  GemmArgs a{qa, lda, sa, ldsa, qb, ldb, sb, ldsb, sb_transposed ? kSbTileT : kSbTile, c, ldc, M, N, K};
+  return gemm_common("bfp8_gemm_1x128_128x128", a, stream);
+}
+
+bfp8_status bfp8_gemm_1x128_128x1(const void* qa, int64_t lda, const float* sa, int64_t ldsa, const void* qb,
+                                  int64_t ldb, const float* sb, int64_t ldsb, void* c, int64_t ldc, int64_t M,
+                                  int64_t N, int64_t K, bfp8_stream_t stream) {
+  GemmArgs a{qa, lda, sa, ldsa, qb, ldb, sb, ldsb, kSbCol, c, ldc, M, N, K};
+  return gemm_common("bfp8_gemm_1x128_128x1", a, stream);
+}
+
+bfp8_status bfp8_cast_e4m3(const float* x, int64_t n, void* q, bfp8_stream_t stream) {
+  CHECK_ARG(n >= 0, "bfp8_cast_e4m3: negative size");
+  if (n == 0) return BFP8_OK;
+  CHECK_ARG(x && q, "bfp8_cast_e4m3: null pointer");
+  CHECK_ARG(al4(x), "bfp8_cast_e4m3: x must be 4-byte aligned");
+  int sms = 0;
+  bfp8_status st = check_device(&sms);
+  if (st != BFP8_OK) return st;
+  cudaError_t e = launch_cast(x, n, (uint8_t*)q, sms, (cudaStream_t)stream);
+  return e == cudaSuccess ? BFP8_OK : cuda_fail(e, "bfp8_cast_e4m3 launch");
+}
+
+bfp8_status bfp8_check_device_errors(bfp8_stream_t stream) {
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "bfp8_check_device_errors: stream synchronize");
+  uint32_t bits = 0;
+  e = gemm_read_errors(&bits);
+  if (e != cudaSuccess) return cuda_fail(e, "bfp8_check_device_errors: read flag");
+  if (bits) {
+    return fail(BFP8_ERR_TIMEOUT,
+                "GEMM kernel gave up on a bounded wait (flags 0x%x: %s%s%s%s%s)", bits,
+                (bits & 1) ? "smem-stage-release " : "", (bits & 2) ? "tma-arrival " : "",
+                (bits & 4) ? "tmem-release " : "", (bits & 8) ? "partial-product " : "",
+                (bits & 16) ? "teardown-drain " : "");
+  }
+  return BFP8_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Linear layer
+// ---------------------------------------------------------------------------
+
+namespace {
+size_t a256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct FwdLayout {
+  size_t qx, sx, qw, sw, total;
+  int64_t ldK, ldsM;
+};
+FwdLayout fwd_layout(int64_t M, int64_t N, int64_t K) {
+  FwdLayout L;
+  L.ldK = rup(K, 16);
+  L.ldsM = rup(M, 4);
+  const int64_t Kb = cdiv(K, kBlock), Nb = cdiv(N, kBlock);
+  size_t o = 0;
+  L.qx = o; o = a256(o + (size_t)M * L.ldK);
+  L.sx = o; o = a256(o + (size_t)Kb * L.ldsM * 4);
+  L.qw = o; o = a256(o + (size_t)N * L.ldK);
+  L.sw = o; o = a256(o + (size_t)Nb * Kb * 4);
+  L.total = o;
+  return L;
+}
+
+struct BwdLayout {
+  size_t qdy, sdy, qwt, sw, qdyt, sdyt, qxt, sxt, total;
+  int64_t ldN, ldM, ldsM, ldsN, ldsK;
+};
+BwdLayout bwd_layout(int64_t M, int64_t N, int64_t K) {
+  BwdLayout L;
+  L.ldN = rup(N, 16);
+  L.ldM = rup(M, 16);
+  L.ldsM = rup(M, 4);
+  L.ldsN = rup(N, 4);
+  L.ldsK = rup(K, 4);
+  const int64_t Kb = cdiv(K, kBlock), Nb = cdiv(N, kBlock), Mb = cdiv(M, kBlock);
+  size_t o = 0;
+  L.qdy = o; o = a256(o + (size_t)M * L.ldN);          // dY, 1x128 along N
+  L.sdy = o; o = a256(o + (size_t)Nb * L.ldsM * 4);
+  L.qwt = o; o = a256(o + (size_t)K * L.ldN);          // W^T bytes
+  L.sw = o; o = a256(o + (size_t)Nb * Kb * 4);
+  L.qdyt = o; o = a256(o + (size_t)N * L.ldM);         // dY^T, 1x128 along M
+  L.sdyt = o; o = a256(o + (size_t)Mb * L.ldsN * 4);
+  L.qxt = o; o = a256(o + (size_t)K * L.ldM);          // X, 128x1 along M, transposed
+  L.sxt = o; o = a256(o + (size_t)Mb * L.ldsK * 4);
+  L.total = o;
+  return L;
+}
+}  // namespace
+
+size_t bfp8_linear_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  const size_t f = fwd_layout(M, N, K).total, b = bwd_layout(M, N, K).total;
+  return f > b ? f : b;
+}
+
+bfp8_status bfp8_linear_fwd(const void* x, const void* w, void* y, int64_t M, int64_t N, int64_t K, void* ws,
+                            size_t ws_bytes, bfp8_stream_t stream) {
+  bfp8_status st = check_dims("bfp8_linear_fwd", M, N, K);
+  if (st != BFP8_OK) return st;
+  if (M == 0 || N == 0 || K == 0) {
+    if (M > 0 && N > 0 && y) {
+      cudaError_t e = cudaMemsetAsync(y, 0, (size_t)M * N * 2, (cudaStream_t)stream);
+      if (e != cudaSuccess) return cuda_fail(e, "bfp8_linear_fwd");
+    }
+    return BFP8_OK;
+  }
+  CHECK_ARG(x && w && y && ws, "bfp8_linear_fwd: null pointer");
+  CHECK_ARG((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "bfp8_linear_fwd: workspace must be 256-byte aligned");
+  const FwdLayout L = fwd_layout(M, N, K);
+  CHECK_ARG(ws_bytes >= bfp8_linear_workspace_size(M, N, K), "bfp8_linear_fwd: workspace too small (%zu < %zu)",
+            ws_bytes, bfp8_linear_workspace_size(M, N, K));
+  uint8_t* base = (uint8_t*)ws;
+  const int64_t Kb = cdiv(K, kBlock);
+  if ((st = bfp8_quant_lhs(x, M, K, K, 0, base + L.qx, L.ldK, (float*)(base + L.sx), L.ldsM, stream)) != BFP8_OK)
+    return st;
+  if ((st = bfp8_quant_weight(w, N, K, K, base + L.qw, L.ldK, nullptr, 0, (float*)(base + L.sw), Kb, stream)) !=
+      BFP8_OK)
+    return st;
+  return bfp8_gemm_1x128_128x128(base + L.qx, L.ldK, (const float*)(base + L.sx), L.ldsM, base + L.qw, L.ldK,
+                                 (const float*)(base + L.sw), Kb, 0, y, N, M, N, K, stream);
+}
+
+bfp8_status bfp8_linear_bwd(const void* dy, const void* x, const void* w, void* dx, void* dw, int64_t M, int64_t N,
+                            int64_t K, void* ws, size_t ws_bytes, bfp8_stream_t stream) {
+  bfp8_status st = check_dims("bfp8_linear_bwd", M, N, K);
+  if (st != BFP8_OK) return st;
+  if (M == 0 || N == 0 || K == 0) {
+    cudaError_t e = cudaSuccess;
+    if (M > 0 && K > 0 && dx) e = cudaMemsetAsync(dx, 0, (size_t)M * K * 2, (cudaStream_t)stream);
+    if (e == cudaSuccess && N > 0 && K > 0 && dw) e = cudaMemsetAsync(dw, 0, (size_t)N * K * 2, (cudaStream_t)stream);
+    return e == cudaSuccess ? BFP8_OK : cuda_fail(e, "bfp8_linear_bwd");
+  }
+  CHECK_ARG(dy && x && w && dx && dw && ws, "bfp8_linear_bwd: null pointer");
+  CHECK_ARG((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "bfp8_linear_bwd: workspace must be 256-byte aligned");
+  CHECK_ARG(ws_bytes >= bfp8_linear_workspace_size(M, N, K), "bfp8_linear_bwd: workspace too small (%zu < %zu)",
+            ws_bytes, bfp8_linear_workspace_size(M, N, K));
+  const BwdLayout L = bwd_layout(M, N, K);
+  uint8_t* base = (uint8_t*)ws;
+  const int64_t Kb = cdiv(K, kBlock), Nb = cdiv(N, kBlock);
+  (void)Nb;
+  // dX = dY W : dY 1x128 along N (reduction), W's tiles read transposed.
+  if ((st = bfp8_quant_lhs(dy, M, N, N, 0, base + L.qdy, L.ldN, (float*)(base + L.sdy), L.ldsM, stream)) != BFP8_OK)
+    return st;
+  if ((st = bfp8_quant_weight(w, N, K, K, nullptr, 0, base + L.qwt, L.ldN, (float*)(base + L.sw), Kb, stream)) !=
+      BFP8_OK)
+    return st;
+  if ((st = bfp8_gemm_1x128_128x128(base + L.qdy, L.ldN, (const float*)(base + L.sdy), L.ldsM, base + L.qwt, L.ldN,
+                                    (const float*)(base + L.sw), Kb, 1, dx, K, M, K, N, stream)) != BFP8_OK)
+    return st;
+  // dW = dY^T X : dY^T 1x128 along M, X 128x1 along M (both written K-major).
+  if ((st = bfp8_quant_lhs(dy, N, M, N, 1, base + L.qdyt, L.ldM, (float*)(base + L.sdyt), L.ldsN, stream)) !=
+      BFP8_OK)
+    return st;
+  if ((st = bfp8_quant_rhs(x, M, K, K, base + L.qxt, L.ldM, (float*)(base + L.sxt), L.ldsK, stream)) != BFP8_OK)
+    return st;
+  return bfp8_gemm_1x128_128x1(base + L.qdyt, L.ldM, (const float*)(base + L.sdyt), L.ldsN, base + L.qxt, L.ldM,
+                               (const float*)(base + L.sxt), L.ldsK, dw, K, N, K, M, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Host replay of the kernels' index arithmetic
+// ---------------------------------------------------------------------------
+
+bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, int flag, uint32_t* counts,
+                                    uint32_t* scale_counts, int64_t* oob) {
+  CHECK_ARG(counts && oob, "bfp8_debug_write_counts: null pointer");
+  CHECK_ARG(M >= 0 && N >= 0 && K >= 0, "bfp8_debug_write_counts: negative size");
+  const int sms = 152;  // GB300
+  *oob = 0;
+  auto hit = [&](uint32_t* arr, int64_t r, int64_t c, int64_t rows, int64_t cols) {
+    if (r < 0 || r >= rows || c < 0 || c >= cols) {
+      ++*oob;
+      return;
+    }
+    if (arr) arr[r * cols + c]++;
+  };
+  if (kind == 0 && !flag) {  // quant_lhs, row-major input [M,K]
+    const int64_t Kb = cdiv(K, kBlock), groups = M * Kb;
+    if (groups == 0) return BFP8_OK;
+    const int64_t grid = quant_rows_grid(M, K, sms);
+    const int64_t nhw = grid * (kRowThreads / 16);
+    const int64_t iters = cdiv(groups, nhw * kRowUnroll);
+    for (int64_t hw = 0; hw < nhw; ++hw)
+      for (int64_t it = 0; it < iters; ++it)
+        for (int u = 0; u < kRowUnroll; ++u) {
+          const int64_t g = row_group(hw, nhw, it, u);
+          if (g >= groups) continue;
+          for (int l16 = 0; l16 < 16; ++l16) {
+            const RowChunk c = row_chunk(g, l16, Kb);
+            for (int b = 0; b < 8; ++b)
+              if (c.k + b < K) hit(counts, c.m, c.k + b, M, K);
+            if (l16 == 0) hit(scale_counts, c.k / kBlock, c.m, Kb, M);
+          }
+        }
+    return BFP8_OK;
+  }
+  if ((kind == 0 && flag) || kind == 1) {  // transposed-read groups: T = grouped dim, C = columns
+    // kind 0 (x is [K,M]): T = K, C = M, logical q [M,K].  kind 1 (x is [K,N]): T = K, C = N, qT [N,K].
+    const int64_t T = K, C = (kind == 0) ? M : N;
+    const int64_t grid = cdiv(T, kColTileT) * cdiv(C, kColTileC);
+    for (int64_t blk = 0; blk < grid; ++blk) {
+      const ColTile tile = col_tile(blk, C);
+      for (int ch = 0; ch < kColTileC * kColTileT / 16; ++ch) {
+        const int64_t c = col_store_c(tile, ch), t = col_store_t(tile, ch);
+        if (c < C)
+          for (int b = 0; b < 16; ++b)
+            if (t + b < T) hit(counts, c, t + b, C, T);
+      }
+      for (int warp = 0; warp < kColThreads / 32; ++warp)
+        for (int j = 0; j < 8; ++j) {
+          const int64_t c = col_elem_c(tile, warp, j);
+          if (c < C) hit(scale_counts, tile.t0 / kBlock, c, cdiv(T, kBlock), C);
+        }
+    }
+    return BFP8_OK;
+  }
+  if (kind == 2 || kind == 4) {  // quant_weight: q (kind 2) or qt (kind 4)
+    const int64_t Kb = cdiv(K, kBlock), grid = cdiv(N, kBlock) * Kb;
+    for (int64_t blk = 0; blk < grid; ++blk) {
+      const WTile tile = w_tile(blk, Kb);
+      if (kind == 2) {
+        for (int warp = 0; warp < kWThreads / 32; ++warp)
+          for (int cc = 0; cc < 2; ++cc)
+            for (int lane = 0; lane < 32; ++lane)
+              for (int i = 0; i < 4; ++i) {
+                const int64_t n = w_elem_n(tile, lane, i), k = w_elem_k(tile, warp + 8 * cc, 0);
+                if (n < N)
+                  for (int b = 0; b < 8; ++b)
+                    if (k + b < K) hit(counts, n, k + b, N, K);
+              }
+        hit(scale_counts, tile.nb, tile.kb, cdiv(N, kBlock), Kb);
+      } else {
+        for (int ch = 0; ch < kBlock * kBlock / 16; ++ch) {
+          const int64_t k = w_tstore_k(tile, ch), n = w_tstore_n(tile, ch);
+          if (k < K)
+            for (int b = 0; b < 16; ++b)
+              if (n + b < N) hit(counts, k, n + b, K, N);
+        }
+      }
+    }
+    return BFP8_OK;
+  }
+  if (kind == 3) {  // GEMM output C [M,N]
+    const int bn = gemm_pick_bn(M, N, sms);
+    const int64_t num_m = cdiv(M, kBM), num_n = cdiv(N, bn), tiles = num_m * num_n;
+    const int64_t grid = gemm_grid(M, N, bn, sms);
+    const int epi_warps = bn / 32;
+    for (int64_t cta = 0; cta < grid; ++cta)
+      for (int64_t t = cta; t < tiles; t += grid) {
+        const GemmTile g = gemm_tile(t, num_m, num_n, bn);
+        for (int e = 0; e < epi_warps; ++e)
+          for (int lane = 0; lane < 32; ++lane) {
+            const int64_t m = g.m0 + epi_row(e, lane);
+            if (m >= M) continue;
+            for (int c = 0; c < 128; ++c) {
+              const int64_t n = g.n0 + epi_col0(e) + c;
+              if (n < N) hit(counts, m, n, M, N);
+            }
+          }
+      }
+    return BFP8_OK;
+  }
+  return fail(BFP8_ERR_INVALID_ARG, "bfp8_debug_write_counts: unknown kind %d", kind);
+}
+
+}  // extern "C"

@@ -1,0 +1,441 @@
+// Blockwise-scaled FP8 GEMMs on the 5th-generation tensor cores (sm_103a).
+//
+// C[m,n] = sum_kb a_s[m,kb] * b_s(n,kb) * P_kb[m,n],  P_kb = the e4m3 x e4m3
+// partial product of one 128-wide K-block ("Mask a_s/b_s scale loads in
+// blockwise FP8 training GEMM kernels", Summary: 1x128 x 128x128 and
+// 1x128 x 128x1 kernels with per-tile a_s/b_s; Fix: scale loads masked to
+// offs_m < M and offs_n < N like every other load and the output store).
+//
+// Design (one persistent CTA per SM, warp-specialised):
+//   warp 0      TMA producer: 128x128-byte A and BNx128-byte B tiles of one
+//               K-block per stage, 128-byte swizzled, into an S-stage ring.
+//   warp 1      MMA issuer: 4 x tcgen05.mma.kind::f8f6f4 (K = 32 each) per
+//               K-block into one of two tensor-memory partial buffers, then
+//               tcgen05.commit to release the smem stage and publish the partial.
+//   warps 2-3   idle (they complete the control warpgroup, which gives its
+//               registers to the promotion warpgroups with setmaxnreg).
+//   warps 4..   promotion/epilogue (BN/32 warps): tcgen05.ld the K-block's
+//               fp32 partial, acc += (a_s*b_s) * partial in registers, release
+//               the tensor-memory buffer; at tile end round to bf16 and store
+//               only rows m < M and columns n < N.
+// The two tensor-memory buffers let the promotion of K-block kb overlap the
+// MMAs of K-block kb+1.  Tails: TMA zero-fills rows/columns outside M, N, K;
+// scale loads are predicated; the epilogue store is masked.
+// Every mbarrier wait is bounded in time; a timeout records an error bit,
+// lets every role leave its loop, waits for its own copies/MMAs in flight and
+// frees tensor memory before the CTA exits.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace bfp8 {
+
+static __device__ uint32_t g_gemm_error;
+
+enum : uint32_t {
+  kErrWaitEmpty = 1u << 0,      // producer: a smem stage was never released
+  kErrWaitFull = 1u << 1,       // MMA: a stage's TMA bytes never landed
+  kErrWaitTmemEmpty = 1u << 2,  // MMA: a tensor-memory buffer was never released
+  kErrWaitTmemFull = 1u << 3,   // epilogue: a partial product never arrived
+  kErrWaitDrain = 1u << 4,      // teardown: MMAs or copies in flight never finished
+};
+
+struct GemmParams {
+  const float* sa;
+  int64_t ldsa;
+  const float* sb;
+  int64_t ldsb;
+  uint16_t* c;
+  int64_t ldc;
+  int64_t M, N, K;
+  int64_t num_m, num_n, num_tiles, Kb, Nb;
+  int c_vec;   // 16-byte output stores allowed (ldc % 8 == 0, c 16-byte aligned)
+  int sb_vec;  // 16-byte column-scale loads allowed (ldsb % 4 == 0, sb 16-byte aligned)
+  uint64_t wait_limit_ns;
+};
+
+template <int BN, int STAGES>
+struct GemmCfg {
+  static constexpr int kEpiWarps = BN / 32;  // 4 warps (128 rows) per 128 columns
+  static constexpr int kThreads = 128 + 32 * kEpiWarps;
+  // Register split (BN = 256: 384 threads launched at 168 registers each):
+  // the control warpgroup drops to 40, the two promotion warpgroups rise to
+  // 224; 128*40 + 256*224 = 62464 <= 384*168 = 64512.
+  static constexpr bool kSplitRegs = (kThreads > 256);
+  static constexpr int kCtrlRegs = 40;
+  static constexpr int kEpiRegs = 224;
+  static constexpr int kABytes = kBM * kBK;
+  static constexpr int kBBytes = BN * kBK;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kTmemCols = 2 * BN;  // two fp32 partial buffers of BN columns
+  static constexpr int kOffB = STAGES * kABytes;
+  static constexpr int kOffSb = kOffB + STAGES * kBBytes;
+  static constexpr int kOffBar = kOffSb + kEpiWarps * 128 * 4;
+  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
+                "tensor-memory allocation must be a power of two in [32, 512]");
+};
+
+__device__ __forceinline__ void gemm_fail(uint32_t code, volatile int* abort_flag) {
+  atomicOr(&g_gemm_error, code);
+  *abort_flag = 1;
+}
+
+template <int BN, int STAGES, int SB_MODE>
+__global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
+    gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tma_a,
+                          const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
+  using Cfg = GemmCfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sA = sbase;
+  const uint32_t sB = sbase + Cfg::kOffB;
+  float* sb_slots = reinterpret_cast<float*>(smem + Cfg::kOffSb);
+  const uint32_t bar0 = sbase + Cfg::kOffBar;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
+  volatile int* never = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
+
+  // barrier addresses: full[S], empty[S], tfull[2], tempty[2], drain
+  auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(STAGES + i); };
+  auto tfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + i); };
+  auto tempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + 2 + i); };
+  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
+
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+  const int lane = (int)(threadIdx.x & 31);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull_bar(i), 1);
+      mbar_init(tempty_bar(i), Cfg::kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    *never = 0;
+    fence_barrier_init();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma_a);
+    tma_prefetch_desc(&tma_b);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  if (warp < 4) {
+    if (Cfg::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kCtrlRegs));
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int64_t it = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        const GemmTile g = gemm_tile(t, p.num_m, p.num_n, BN);
+        for (int64_t kb = 0; kb < p.Kb; ++kb, ++it) {
+          const int st = (int)(it % STAGES);
+          const uint32_t ph = (uint32_t)((it / STAGES) & 1);
+          if (!mbar_wait_bounded(empty_bar(st), ph ^ 1u, p.wait_limit_ns, abort_flag)) {
+            gemm_fail(kErrWaitEmpty, abort_flag);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(st), (uint32_t)Cfg::kStageBytes);
+          tma_load_2d(sA + (uint32_t)(st * Cfg::kABytes), &tma_a, full_bar(st), (int32_t)(kb * kBK),
+                      (int32_t)g.m0);
+          tma_load_2d(sB + (uint32_t)(st * Cfg::kBBytes), &tma_b, full_bar(st), (int32_t)(kb * kBK),
+                      (int32_t)g.n0);
+        }
+      }
+      if (!ok) {
+        // copies already issued must land before this CTA's smem goes away
+        for (int64_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+          if (!mbar_wait_bounded(full_bar((int)(j % STAGES)), (uint32_t)((j / STAGES) & 1),
+                                 p.wait_limit_ns, never))
+            atomicOr(&g_gemm_error, kErrWaitDrain);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
+      int64_t it = 0;
+      bool ok = true;
+      for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+        for (int64_t kb = 0; kb < p.Kb; ++kb, ++it) {
+          const int st = (int)(it % STAGES);
+          const uint32_t ph = (uint32_t)((it / STAGES) & 1);
+          const int buf = (int)(it & 1);
+          const uint32_t tph = (uint32_t)((it >> 1) & 1);
+          if (!mbar_wait_bounded(tempty_bar(buf), tph ^ 1u, p.wait_limit_ns, abort_flag)) {
+            gemm_fail(kErrWaitTmemEmpty, abort_flag);
+            ok = false;
+            break;
+          }
+          if (!mbar_wait_bounded(full_bar(st), ph, p.wait_limit_ns, abort_flag)) {
+            gemm_fail(kErrWaitFull, abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t da = desc_kmajor_sw128(sA + (uint32_t)(st * Cfg::kABytes));
+          const uint64_t db = desc_kmajor_sw128(sB + (uint32_t)(st * Cfg::kBBytes));
+          const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+#pragma unroll
+          for (int k = 0; k < kBK / 32; ++k)  // advance 32 bytes of K inside the swizzled row
+            mma_e4m3(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), idesc, k > 0 ? 1u : 0u);
+          mma_commit(empty_bar(st));
+          mma_commit(tfull_bar(buf));
+        }
+      }
+      // every MMA issued above completes before tensor memory is released
+      mma_commit(drain_bar);
+      if (!mbar_wait_bounded(drain_bar, 0, p.wait_limit_ns, never))
+        gemm_fail(kErrWaitDrain, abort_flag);
+    }
+  }
+  } else {
+    if (Cfg::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::kEpiRegs));
+    // ------------------------------------------------------------ promotion + epilogue
+    const int e = warp - 4;
+    const int row = epi_row(e, lane);
+    const int col0 = epi_col0(e);
+    const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
+    float* slot = sb_slots + e * 128;
+    int64_t it = 0;
+    bool ok = true;
+    for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
+      const GemmTile g = gemm_tile(t, p.num_m, p.num_n, BN);
+      const int64_t m = g.m0 + row;
+      const bool m_ok = m < p.M;
+      const int64_t nb = (g.n0 + col0) / kBlock;  // B tile-scale block of these 128 columns
+      const int64_t ncol = g.n0 + col0 + 4 * lane;  // first of this lane's 4 column scales
+
+      auto load_sa = [&](int64_t kb) -> float { return m_ok ? __ldg(p.sa + kb * p.ldsa + m) : 0.0f; };
+      auto load_sb_tile = [&](int64_t kb) -> float {
+        if (nb >= p.Nb) return 0.0f;
+        return SB_MODE == kSbTile ? __ldg(p.sb + nb * p.ldsb + kb) : __ldg(p.sb + kb * p.ldsb + nb);
+      };
+      auto load_sb_col = [&](int64_t kb) -> float4 {
+        const float* src = p.sb + kb * p.ldsb + ncol;
+        if (p.sb_vec && ncol + 4 <= p.N) return __ldg(reinterpret_cast<const float4*>(src));
+        float4 r;
+        r.x = (ncol + 0 < p.N) ? __ldg(src + 0) : 0.0f;
+        r.y = (ncol + 1 < p.N) ? __ldg(src + 1) : 0.0f;
+        r.z = (ncol + 2 < p.N) ? __ldg(src + 2) : 0.0f;
+        r.w = (ncol + 3 < p.N) ? __ldg(src + 3) : 0.0f;
+        return r;
+      };
+
+      float acc[128];
+#pragma unroll
+      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+
+      float sa_next = load_sa(0);
+      float sb_next = 0.0f;
+      float4 sbc_next = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (SB_MODE == kSbCol) sbc_next = load_sb_col(0);
+      else sb_next = load_sb_tile(0);
+
+      for (int64_t kb = 0; kb < p.Kb; ++kb, ++it) {
+        const float sa_cur = sa_next, sb_cur = sb_next;
+        const float4 sbc_cur = sbc_next;
+        if (kb + 1 < p.Kb) {  // prefetch the next K-block's scales (masked loads)
+          sa_next = load_sa(kb + 1);
+          if (SB_MODE == kSbCol) sbc_next = load_sb_col(kb + 1);
+          else sb_next = load_sb_tile(kb + 1);
+        }
+        const int buf = (int)(it & 1);
+        const uint32_t tph = (uint32_t)((it >> 1) & 1);
+        const bool got = mbar_wait_bounded(tfull_bar(buf), tph, p.wait_limit_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) gemm_fail(kErrWaitTmemFull, abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (SB_MODE == kSbCol) {
+          __syncwarp();
+          reinterpret_cast<float4*>(slot)[lane] = sbc_cur;
+          __syncwarp();
+        }
+        const uint32_t taddr = tmem_base + lane_base + (uint32_t)(buf * BN + col0);
+        const float scale = sa_cur * sb_cur;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(taddr + (uint32_t)(32 * c), r);
+          tmem_ld_wait();
+          if (SB_MODE == kSbCol) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float sc = sa_cur * slot[32 * c + j];
+              acc[32 * c + j] = fmaf(sc, __uint_as_float(r[j]), acc[32 * c + j]);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(scale, __uint_as_float(r[j]), acc[32 * c + j]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(buf));
+      }
+      if (!ok) break;
+
+      if (m_ok) {
+        uint16_t* crow = p.c + m * p.ldc;
+#pragma unroll
+        for (int c8 = 0; c8 < 16; ++c8) {
+          const int64_t n = g.n0 + col0 + 8 * c8;
+          if (n >= p.N) break;
+          uint32_t w[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) w[h] = pack_bf16x2(acc[8 * c8 + 2 * h], acc[8 * c8 + 2 * h + 1]);
+          if (p.c_vec && n + 8 <= p.N) {
+            *reinterpret_cast<uint4*>(crow + n) = make_uint4(w[0], w[1], w[2], w[3]);
+          } else {
+#pragma unroll
+            for (int b = 0; b < 8; ++b)
+              if (n + b < p.N) crow[n + b] = (uint16_t)(w[b >> 1] >> (16 * (b & 1)));
+          }
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// Row-major [rows, inner] uint8 matrix with row stride ld bytes; box of
+// 128 bytes x box_rows rows, 128-byte swizzle, out-of-range reads filled with 0.
+static bool make_tma_u8(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t ld,
+                        int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t elem[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int gemm_pick_bn(int64_t M, int64_t N, int num_sms) {
+  if (N <= 128) return 128;
+  const int64_t tiles256 = cdiv(M, kBM) * cdiv(N, 256);
+  return tiles256 >= num_sms ? 256 : 128;
+}
+
+int64_t gemm_grid(int64_t M, int64_t N, int bn, int num_sms) {
+  const int64_t tiles = cdiv(M, kBM) * cdiv(N, bn);
+  return tiles < num_sms ? tiles : num_sms;
+}
+
+template <int BN, int STAGES, int MODE>
+static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
+                            int64_t grid, cudaStream_t st) {
+  using Cfg = GemmCfg<BN, STAGES>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_blockwise_kernel<BN, STAGES, MODE>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  gemm_blockwise_kernel<BN, STAGES, MODE><<<(unsigned)grid, Cfg::kThreads, Cfg::kSmemBytes, st>>>(ma, mb, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const char** msg) {
+  const int bn = gemm_pick_bn(a.M, a.N, num_sms);
+  CUtensorMap ma, mb;
+  if (!make_tma_u8(&ma, a.qa, a.K, a.M, a.lda, kBM) || !make_tma_u8(&mb, a.qb, a.K, a.N, a.ldb, bn)) {
+    *msg = "cuTensorMapEncodeTiled failed for an operand (alignment, stride or size out of range)";
+    return cudaErrorInvalidValue;
+  }
+  GemmParams p;
+  p.sa = a.sa;
+  p.ldsa = a.ldsa;
+  p.sb = a.sb;
+  p.ldsb = a.ldsb;
+  p.c = reinterpret_cast<uint16_t*>(a.c);
+  p.ldc = a.ldc;
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.num_m = cdiv(a.M, kBM);
+  p.num_n = cdiv(a.N, bn);
+  p.num_tiles = p.num_m * p.num_n;
+  p.Kb = cdiv(a.K, kBK);
+  p.Nb = cdiv(a.N, kBlock);
+  p.c_vec = (a.ldc % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.c) & 15u) == 0);
+  p.sb_vec = (a.ldsb % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.sb) & 15u) == 0);
+  p.wait_limit_ns = 4000000000ull;  // 4 s per wait: far above any legitimate stall
+  const int64_t grid = gemm_grid(a.M, a.N, bn, num_sms);
+  if (bn == 256) {
+    switch (a.sb_mode) {
+      case kSbTile: return run_gemm<256, 4, kSbTile>(ma, mb, p, grid, st);
+      case kSbTileT: return run_gemm<256, 4, kSbTileT>(ma, mb, p, grid, st);
+      default: return run_gemm<256, 4, kSbCol>(ma, mb, p, grid, st);
+    }
+  }
+  switch (a.sb_mode) {
+    case kSbTile: return run_gemm<128, 6, kSbTile>(ma, mb, p, grid, st);
+    case kSbTileT: return run_gemm<128, 6, kSbTileT>(ma, mb, p, grid, st);
+    default: return run_gemm<128, 6, kSbCol>(ma, mb, p, grid, st);
+  }
+}
+
+cudaError_t gemm_read_errors(uint32_t* out) {
+  uint32_t zero = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(out, g_gemm_error, sizeof(uint32_t));
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyToSymbol(g_gemm_error, &zero, sizeof(uint32_t));
+}
+
+}  // namespace bfp8

@@ -1,0 +1,123 @@
+// Launch geometry and index arithmetic of the kernels, as __host__ __device__
+// functions so that the host can replay exactly what a launch would touch
+// (the scale-bounds test idea of "Mask a_s/b_s scale loads in blockwise FP8
+// training GEMM kernels": check the offs -> index arithmetic on tail shapes
+// without running the kernel).
+#pragma once
+
+#include <stdint.h>
+
+#ifndef BFP8_HD
+#define BFP8_HD __host__ __device__ __forceinline__
+#endif
+
+namespace bfp8 {
+
+constexpr int kBlock = 128;            // group / tile edge (block_size = 128)
+constexpr float kE4m3Max = 448.0f;     // FP8_MAX of float8_e4m3fn
+constexpr float kAmaxFloor = 1e-12f;   // keeps an all-zero group's scale finite
+
+BFP8_HD int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------------------
+// quant_lhs, row-major input: 16 threads per 1x128 group, 8 elements each.
+// ---------------------------------------------------------------------------
+constexpr int kRowThreads = 256;       // threads per CTA
+constexpr int kRowUnroll = 4;          // groups per half-warp per iteration
+
+struct RowChunk {
+  int64_t m, k;  // first element of the thread's 8-element chunk
+};
+
+// Group g (row-major over [M, Kb]) and the thread's lane within its half-warp.
+BFP8_HD RowChunk row_chunk(int64_t g, int lane16, int64_t Kb) {
+  RowChunk c;
+  c.m = g / Kb;
+  c.k = (g % Kb) * kBlock + (int64_t)lane16 * 8;
+  return c;
+}
+
+// Group processed by half-warp `hw` (of `nhw`) in iteration `it`, unroll slot `u`.
+BFP8_HD int64_t row_group(int64_t hw, int64_t nhw, int64_t it, int u) {
+  return hw + (it * kRowUnroll + u) * nhw;
+}
+
+// ---------------------------------------------------------------------------
+// Column groups (128 consecutive rows of one column) written transposed:
+// CTA tile of 128 rows x 64 columns; warp w owns columns 8w..8w+7, lane l owns
+// rows 4l..4l+3 of the tile.  Used by quant_lhs(x_transposed) and quant_rhs.
+// ---------------------------------------------------------------------------
+constexpr int kColThreads = 256;
+constexpr int kColTileT = 128;   // rows (the grouped dimension)
+constexpr int kColTileC = 64;    // columns
+
+struct ColTile {
+  int64_t t0, c0;
+};
+BFP8_HD ColTile col_tile(int64_t block, int64_t C) {
+  const int64_t nct = cdiv(C, kColTileC);
+  ColTile t;
+  t.t0 = (block / nct) * kColTileT;
+  t.c0 = (block % nct) * kColTileC;
+  return t;
+}
+// Element (row t, column c) of value (i, j) held by (warp, lane).
+BFP8_HD int64_t col_elem_t(const ColTile& tile, int lane, int i) { return tile.t0 + 4 * lane + i; }
+BFP8_HD int64_t col_elem_c(const ColTile& tile, int warp, int j) { return tile.c0 + 8 * warp + j; }
+// Store phase: 16-byte chunk `ch` (0..511) of the transposed 64 x 128-byte tile.
+BFP8_HD int64_t col_store_c(const ColTile& tile, int ch) { return tile.c0 + ch / 8; }
+BFP8_HD int64_t col_store_t(const ColTile& tile, int ch) { return tile.t0 + (ch % 8) * 16; }
+
+// ---------------------------------------------------------------------------
+// quant_weight: one CTA per 128x128 tile; warp w owns 8-column chunks w and
+// w+8, lane l owns rows 4l..4l+3.
+// ---------------------------------------------------------------------------
+constexpr int kWThreads = 256;
+
+struct WTile {
+  int64_t nb, kb;
+};
+BFP8_HD WTile w_tile(int64_t block, int64_t Kb) {
+  WTile t;
+  t.nb = block / Kb;
+  t.kb = block % Kb;
+  return t;
+}
+BFP8_HD int64_t w_elem_n(const WTile& t, int lane, int i) { return t.nb * kBlock + 4 * lane + i; }
+BFP8_HD int64_t w_elem_k(const WTile& t, int chunk, int j) { return t.kb * kBlock + 8 * chunk + j; }
+// transposed store phase: 16-byte chunk `ch` (0..1023) of the 128 x 128-byte qt tile
+BFP8_HD int64_t w_tstore_k(const WTile& t, int ch) { return t.kb * kBlock + ch / 8; }
+BFP8_HD int64_t w_tstore_n(const WTile& t, int ch) { return t.nb * kBlock + (ch % 8) * 16; }
+
+// ---------------------------------------------------------------------------
+// GEMM: persistent CTAs over BM x BN output tiles.
+// ---------------------------------------------------------------------------
+constexpr int kBM = 128;
+constexpr int kBK = 128;          // one scale block per pipeline stage
+constexpr int kGroupM = 16;       // tile rasterisation: bands of 16 M-blocks
+
+struct GemmTile {
+  int64_t m0, n0;
+};
+
+// Output tile of linear tile index `t`: tiles are walked N-fastest inside
+// bands of kGroupM M-blocks so that concurrently running CTAs share A rows
+// and B columns in L2.
+BFP8_HD GemmTile gemm_tile(int64_t t, int64_t num_m, int64_t num_n, int bn) {
+  const int64_t per_band = (int64_t)kGroupM * num_n;
+  const int64_t band = t / per_band;
+  const int64_t first_m = band * kGroupM;
+  const int64_t rows = (num_m - first_m) < kGroupM ? (num_m - first_m) : kGroupM;
+  const int64_t r = t % per_band;
+  GemmTile g;
+  g.m0 = (first_m + r % rows) * kBM;
+  g.n0 = (r / rows) * bn;
+  return g;
+}
+
+// Epilogue warp e (0-based among the epilogue warps; CTA warp id = e + 4):
+// tensor-memory lane quarter = CTA warp id % 4, column half = e / 4.
+BFP8_HD int epi_row(int e, int lane) { return 32 * ((e + 4) % 4) + lane; }
+BFP8_HD int epi_col0(int e) { return 128 * (e / 4); }
+
+}  // namespace bfp8

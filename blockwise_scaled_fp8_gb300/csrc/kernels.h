@@ -1,0 +1,45 @@
+// Internal launchers (host side) shared by the C-ABI translation unit.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace bfp8 {
+
+cudaError_t launch_quant_rows(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
+                              int64_t ldq, float* s, int64_t lds, int num_sms, cudaStream_t st);
+int64_t quant_rows_grid(int64_t M, int64_t K, int num_sms);
+cudaError_t launch_quant_cols(const uint16_t* x, int64_t T, int64_t C, int64_t ldx, uint8_t* qT,
+                              int64_t ldq, float* s, int64_t lds, cudaStream_t st);
+cudaError_t launch_quant_weight(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
+                                int64_t ldq, uint8_t* qt, int64_t ldqt, float* s, int64_t lds,
+                                cudaStream_t st);
+cudaError_t launch_cast(const float* x, int64_t n, uint8_t* q, int num_sms, cudaStream_t st);
+
+enum SbMode : int { kSbTile = 0, kSbTileT = 1, kSbCol = 2 };
+
+struct GemmArgs {
+  const void* qa;
+  int64_t lda;
+  const float* sa;
+  int64_t ldsa;
+  const void* qb;
+  int64_t ldb;
+  const float* sb;
+  int64_t ldsb;
+  int sb_mode;
+  void* c;
+  int64_t ldc;
+  int64_t M, N, K;
+};
+
+// Returns cudaSuccess or the launch error; *msg gets a static description of
+// a host-side failure (tensor-map encoding) when the return is not success.
+cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const char** msg);
+// Tile width the launcher picks for an M x N output, and the grid it uses.
+int gemm_pick_bn(int64_t M, int64_t N, int num_sms);
+int64_t gemm_grid(int64_t M, int64_t N, int bn, int num_sms);
+// Reads and clears the device error word of the GEMM kernels (synchronous).
+cudaError_t gemm_read_errors(uint32_t* out);
+
+}  // namespace bfp8

@@ -1,0 +1,204 @@
+/*
+ * bfp8 — blockwise-scaled FP8 (e4m3) quantisation and GEMMs for GB300 (sm_103a).
+ *
+ * C ABI of the library libbfp8.so.  Every entry point is asynchronous on the
+ * given CUDA stream, allocates nothing, and never synchronises (except
+ * bfp8_check_device_errors).  The caller owns every buffer.  Pointers named
+ * "device" must be device memory (or managed memory) of the current device.
+ *
+ * The method (pytorch/ao pull-request pages "Enable blockwise FP8 dense
+ * training kernels on ROCm" and "Mask a_s/b_s scale loads in blockwise FP8
+ * training GEMM kernels"):
+ *   - a group of bf16 values (1x128 along the reduction dim, 128x1 along the
+ *     reduction dim, or a 128x128 weight tile) has amax = max |x| over its
+ *     in-range elements; s = max(amax, 1e-12) / 448 (fp32, one IEEE division);
+ *     q = RNE_e4m3fn(clamp(x / s, -448, 448)) with x / s one IEEE division.
+ *   - GEMM: C[m,n] = sum over 128-wide K-blocks kb of
+ *     a_s[m,kb] * b_s(n,kb) * (sum_{k in kb} qA[m,k] * qB[k,n]), partial
+ *     products in fp32 from the tensor cores, promoted per K-block into an
+ *     fp32 running sum, stored as bf16 (round to nearest even) only where
+ *     m < M and n < N; scale loads are masked the same way.
+ *
+ * Layout conventions.  Row-major everywhere; "ld" arguments are row strides
+ * in ELEMENTS of the buffer's type.  e4m3 buffers are bytes.  Kb = ceil(K/128)
+ * for the dimension that is grouped.  Bytes between the logical width and the
+ * row stride (padding) are never read as data and never written.
+ *
+ * Errors.  Each call validates its arguments and returns BFP8_ERR_INVALID_ARG
+ * (nothing launched) on a violation; BFP8_ERR_UNSUPPORTED when the current
+ * device is not sm_103; BFP8_ERR_CUDA when a launch fails.  bfp8_last_error()
+ * returns a message for the calling thread's last failed call.  A zero-sized
+ * problem (any of M, N, K == 0) launches nothing and returns BFP8_OK.
+ * Inputs must be finite; results for Inf/NaN inputs are unspecified.
+ */
+#ifndef BFP8_H_
+#define BFP8_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define BFP8_API __attribute__((visibility("default")))
+#else
+#define BFP8_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream (binary-compatible with cudaStream_t); NULL = legacy default stream. */
+typedef struct CUstream_st *bfp8_stream_t;
+
+typedef enum {
+    BFP8_OK = 0,
+    BFP8_ERR_INVALID_ARG = 1,
+    BFP8_ERR_UNSUPPORTED = 2,
+    BFP8_ERR_CUDA = 3,
+    BFP8_ERR_TIMEOUT = 4
+} bfp8_status;
+
+/* Message describing the calling thread's most recent non-OK status. */
+BFP8_API const char *bfp8_last_error(void);
+
+/*
+ * act_quant_lhs: 1x128 groups along K of A[M,K].
+ * Source: "Enable blockwise FP8 dense training kernels on ROCm" — quantization
+ * kernel correctness table (act_quant_lhs, block_size=128) and the root-cause
+ * comment: the lhs kernel writes its scales into a column-major fp32 tensor and
+ * the store must be masked to rows m < M.
+ *   x            device bf16.  x_transposed == 0: A[m,k] = x[m*ldx + k]
+ *                (x is [M,K], ldx >= K).  x_transposed == 1: A[m,k] =
+ *                x[k*ldx + m] (x is [K,M], ldx >= M) — used to quantise dY^T
+ *                along the token dimension for the weight-gradient GEMM.
+ *   q            device e4m3 [M, ldq], ldq >= K, ldq % 16 == 0, 16-byte aligned.
+ *   s            device fp32 column-major [M, Kb]: s[kb*lds + m], lds >= M.
+ * Writes exactly q[m*ldq + k] (m < M, k < K) and s[kb*lds + m] (m < M, kb < Kb).
+ */
+BFP8_API bfp8_status bfp8_quant_lhs(const void *x, int64_t M, int64_t K, int64_t ldx, int x_transposed,
+                           void *q, int64_t ldq, float *s, int64_t lds, bfp8_stream_t stream);
+
+/*
+ * act_quant_rhs: 128x1 groups along the reduction dimension K of X[K,N]
+ * (one group = one column n and 128 consecutive rows k).
+ * Source: "Enable blockwise FP8 dense training kernels on ROCm" — quantization
+ * kernel correctness table (act_quant_rhs, block_size=128).
+ *   x            device bf16 [K,N], ldx >= N.
+ *   qT           device e4m3 [N, ldq] (the bytes written transposed, K
+ *                contiguous, as the GEMM reads them), ldq >= K, ldq % 16 == 0,
+ *                16-byte aligned.
+ *   s            device fp32 row-major [Kb, N]: s[kb*lds + n], lds >= N.
+ * Writes exactly qT[n*ldq + k] (n < N, k < K) and s[kb*lds + n].
+ */
+BFP8_API bfp8_status bfp8_quant_rhs(const void *x, int64_t K, int64_t N, int64_t ldx,
+                           void *qT, int64_t ldq, float *s, int64_t lds, bfp8_stream_t stream);
+
+/*
+ * weight_quant_rhs: 128x128 tiles of W[N,K], one scale per tile.
+ * Source: "Enable blockwise FP8 dense training kernels on ROCm" — quantization
+ * kernel correctness table (weight_quant_rhs, block_size=128).
+ *   w            device bf16 [N,K], ldw >= K.
+ *   q            device e4m3 [N, ldq] or NULL (not written), ldq >= K,
+ *                ldq % 16 == 0, 16-byte aligned.
+ *   qt           device e4m3 [K, ldqt] or NULL: the same bytes transposed
+ *                (qt[k*ldqt + n] = q[n*ldq + k]) for the input-gradient GEMM;
+ *                ldqt >= N, ldqt % 16 == 0, 16-byte aligned.
+ *   s            device fp32 row-major [Nb, Kb]: s[nb*lds + kb], lds >= Kb.
+ * At least one of q, qt must be non-NULL.
+ */
+BFP8_API bfp8_status bfp8_quant_weight(const void *w, int64_t N, int64_t K, int64_t ldw,
+                              void *q, int64_t ldq, void *qt, int64_t ldqt,
+                              float *s, int64_t lds, bfp8_stream_t stream);
+
+/*
+ * GEMM 1x128 x 128x128 (forward and input gradient).
+ * Source: "Mask a_s/b_s scale loads in blockwise FP8 training GEMM kernels" —
+ * Summary (triton_fp8_gemm_1x128_128x128_kernel, per-tile a_s/b_s) and Fix
+ * (a_s load masked to offs_m < M, b_s load to offs_n < N, output store masked).
+ * C[M,N] = A[M,K] B[K,N] with
+ *   qa           device e4m3 [M, lda], lda >= K, lda % 16 == 0, 16-byte aligned.
+ *   sa           device fp32 column-major 1x128 scales: sa[kb*ldsa + m], ldsa >= M.
+ *   qb           device e4m3 B^T as [N, ldb] (K contiguous), ldb >= K,
+ *                ldb % 16 == 0, 16-byte aligned.
+ *   sb           device fp32 128x128 tile scales of B, nb = n/128:
+ *                sb_transposed == 0: sb[nb*ldsb + kb], ldsb >= Kb
+ *                  (the weight's own [Nb,Kb] scales: forward, y = x W^T);
+ *                sb_transposed == 1: sb[kb*ldsb + nb], ldsb >= ceil(N/128)
+ *                  (the weight's [Nb_out, Kb_in] scales read for dX = dY W).
+ *   c            device bf16 [M, ldc], ldc >= N.  Only m < M, n < N written.
+ */
+BFP8_API bfp8_status bfp8_gemm_1x128_128x128(const void *qa, int64_t lda, const float *sa, int64_t ldsa,
+                                    const void *qb, int64_t ldb, const float *sb, int64_t ldsb,
+                                    int sb_transposed, void *c, int64_t ldc,
+                                    int64_t M, int64_t N, int64_t K, bfp8_stream_t stream);
+
+/*
+ * GEMM 1x128 x 128x1 (weight gradient).
+ * Source: "Mask a_s/b_s scale loads in blockwise FP8 training GEMM kernels" —
+ * Summary (triton_fp8_gemm_1x128_128x1_kernel) and Fix.
+ * As bfp8_gemm_1x128_128x128 except that B has one scale per column and
+ * K-block: sb[kb*ldsb + n], ldsb >= N (the layout bfp8_quant_rhs writes).
+ */
+BFP8_API bfp8_status bfp8_gemm_1x128_128x1(const void *qa, int64_t lda, const float *sa, int64_t ldsa,
+                                  const void *qb, int64_t ldb, const float *sb, int64_t ldsb,
+                                  void *c, int64_t ldc,
+                                  int64_t M, int64_t N, int64_t K, bfp8_stream_t stream);
+
+/*
+ * Blockwise-FP8 linear layer (the Float8BlockwiseLinear computation of the
+ * ROCm enablement page: quantise, then the blockwise GEMMs), y = x W^T.
+ *   x  device bf16 [M,K] contiguous;  w  device bf16 [N,K] contiguous;
+ *   y  device bf16 [M,N] contiguous.
+ *   ws device workspace of at least bfp8_linear_workspace_size(M,N,K) bytes,
+ *      256-byte aligned; its contents on return are the quantised operands
+ *      (scratch for the caller).
+ */
+BFP8_API size_t bfp8_linear_workspace_size(int64_t M, int64_t N, int64_t K);
+BFP8_API bfp8_status bfp8_linear_fwd(const void *x, const void *w, void *y, int64_t M, int64_t N, int64_t K,
+                            void *ws, size_t ws_bytes, bfp8_stream_t stream);
+
+/*
+ * Backward of the linear layer: dx = dy W (GEMM 1x128 x 128x128 with dY
+ * quantised 1x128 along N and W's tiles transposed) and dw = dy^T x (GEMM
+ * 1x128 x 128x1 with dY^T quantised 1x128 along M and x quantised 128x1 along
+ * M).  dy [M,N], x [M,K], w [N,K], dx [M,K], dw [N,K], all contiguous bf16.
+ */
+BFP8_API bfp8_status bfp8_linear_bwd(const void *dy, const void *x, const void *w, void *dx, void *dw,
+                            int64_t M, int64_t N, int64_t K, void *ws, size_t ws_bytes,
+                            bfp8_stream_t stream);
+
+/*
+ * The method's rounding step on its own: q[i] = RNE_e4m3fn(x[i]) with
+ * saturation to +-448 (the clamp).  x device fp32 [n], q device e4m3 [n].
+ */
+BFP8_API bfp8_status bfp8_cast_e4m3(const float *x, int64_t n, void *q, bfp8_stream_t stream);
+
+/*
+ * Synchronises `stream` and reports whether a GEMM kernel gave up on a
+ * bounded wait since the last call (BFP8_ERR_TIMEOUT, with the failing wait
+ * in the message); clears the flag.  Every wait inside the GEMM kernels is
+ * bounded in time, so a broken pipeline ends the kernel with this flag set
+ * instead of hanging the GPU.
+ */
+BFP8_API bfp8_status bfp8_check_device_errors(bfp8_stream_t stream);
+
+/*
+ * Host-side replay of a kernel's index arithmetic (no GPU needed): counts how
+ * many times each logical output element would be written by the kernel that
+ * `kind` names, for the launch configuration the library would use.
+ *   kind 0: bfp8_quant_lhs (rows = M, cols = K), x_transposed = flag
+ *   kind 1: bfp8_quant_rhs as written (rows = N, cols = K of qT)
+ *   kind 2: bfp8_quant_weight q        (rows = N, cols = K)
+ *   kind 3: GEMM output C              (rows = M, cols = N)
+ *   kind 4: bfp8_quant_weight qt       (rows = K, cols = N)
+ * counts is host uint32 [rows*cols] (incremented); *oob receives the number
+ * of writes that would land outside the logical tensor.  Scale writes are
+ * counted in scale_counts (host uint32 [scale_rows*scale_cols], may be NULL).
+ */
+BFP8_API bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, int flag,
+                                    uint32_t *counts, uint32_t *scale_counts, int64_t *oob);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BFP8_H_ */

@@ -1,0 +1,125 @@
+"""Host-side tests of the C ABI (no GPU): the library loads and exports every
+declared symbol, argument validation rejects bad calls before anything is
+launched, and the kernels' own index arithmetic (replayed on the host) writes
+every element of the logical outputs exactly once and nothing outside them —
+the scale-bounds test idea of "Mask a_s/b_s scale loads in blockwise FP8
+training GEMM kernels", generalised from "at least once" to "exactly once"."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import blockwise_scaled_fp8_gb300 as B
+from blockwise_scaled_fp8_gb300 import buildlib as bbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    bbuild.build()
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "bfp8.h")).read()
+    return sorted(set(re.findall(r"\b(bfp8_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = B.lib()
+    declared = _declared_symbols()
+    assert set(declared) == set(B.EXPORTS)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+NULL = ctypes.c_void_p(None)
+P16 = ctypes.c_void_p(0x10000)      # fake, 16-byte aligned; never dereferenced
+P_ODD = ctypes.c_void_p(0x10001)
+
+
+def test_quant_argument_validation():
+    L = B.lib()
+    s = L.bfp8_quant_lhs
+    assert s(NULL, 4, 128, 128, 0, P16, 128, P16, 4, NULL) == B.BFP8_ERR_INVALID_ARG
+    assert s(P16, 4, 128, 100, 0, P16, 128, P16, 4, NULL) == B.BFP8_ERR_INVALID_ARG      # ldx < K
+    assert s(P16, 4, 128, 128, 0, P16, 136, P16, 4, NULL) == B.BFP8_ERR_INVALID_ARG      # ldq % 16
+    assert s(P16, 4, 128, 128, 0, P16, 128, P16, 3, NULL) == B.BFP8_ERR_INVALID_ARG      # lds < M
+    assert s(P16, 4, 128, 128, 0, P_ODD, 128, P16, 4, NULL) == B.BFP8_ERR_INVALID_ARG    # q misaligned
+    assert s(P16, 4, 128, 2, 1, P16, 128, P16, 4, NULL) == B.BFP8_ERR_INVALID_ARG        # transposed: ldx < M
+    assert s(P16, -1, 128, 128, 0, P16, 128, P16, 4, NULL) == B.BFP8_ERR_INVALID_ARG
+    assert s(P16, 0, 128, 128, 0, P16, 128, P16, 4, NULL) == B.BFP8_OK                   # empty: no-op
+    r = L.bfp8_quant_rhs
+    assert r(P16, 256, 64, 32, P16, 256, P16, 64, NULL) == B.BFP8_ERR_INVALID_ARG          # ldx < N
+    assert r(P16, 256, 64, 64, P16, 256, P16, 63, NULL) == B.BFP8_ERR_INVALID_ARG          # lds < N
+    w = L.bfp8_quant_weight
+    assert w(P16, 64, 256, 256, NULL, 0, NULL, 0, P16, 2, NULL) == B.BFP8_ERR_INVALID_ARG  # no output
+    assert w(P16, 64, 256, 256, P16, 256, NULL, 0, P16, 1, NULL) == B.BFP8_ERR_INVALID_ARG # lds < Kb
+    assert w(P16, 64, 256, 256, NULL, 0, P16, 40, P16, 2, NULL) == B.BFP8_ERR_INVALID_ARG  # ldqt < N
+    assert L.bfp8_cast_e4m3(NULL, 5, P16, NULL) == B.BFP8_ERR_INVALID_ARG
+
+
+def test_gemm_argument_validation():
+    L = B.lib()
+    g = L.bfp8_gemm_1x128_128x128
+    ok_args = [P16, 256, P16, 8, P16, 256, P16, 2, 0, P16, 64, 8, 64, 256, NULL]
+
+    def call(**kw):
+        a = list(ok_args)
+        names = ["qa", "lda", "sa", "ldsa", "qb", "ldb", "sb", "ldsb", "t", "c", "ldc", "M", "N", "K", "st"]
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return g(*a)
+
+    assert call(lda=200) == B.BFP8_ERR_INVALID_ARG          # lda < K
+    assert call(lda=264) == B.BFP8_ERR_INVALID_ARG          # not a multiple of 16
+    assert call(ldb=260) == B.BFP8_ERR_INVALID_ARG          # not a multiple of 16
+    assert call(ldsa=7) == B.BFP8_ERR_INVALID_ARG           # ldsa < M
+    assert call(ldsb=1) == B.BFP8_ERR_INVALID_ARG           # ldsb < Kb
+    assert call(t=1, ldsb=0) == B.BFP8_ERR_INVALID_ARG      # transposed: ldsb < Nb
+    assert call(ldc=32) == B.BFP8_ERR_INVALID_ARG           # ldc < N
+    assert call(qa=P_ODD) == B.BFP8_ERR_INVALID_ARG
+    assert call(c=NULL) == B.BFP8_ERR_INVALID_ARG
+    assert call(M=0) == B.BFP8_OK
+    h = L.bfp8_gemm_1x128_128x1
+    assert h(P16, 256, P16, 8, P16, 256, P16, 63, P16, 64, 8, 64, 256, NULL) == B.BFP8_ERR_INVALID_ARG  # ldsb < N
+
+
+def test_linear_workspace_and_validation():
+    L = B.lib()
+    assert L.bfp8_linear_workspace_size(0, 10, 10) == 0
+    M, N, K = 130, 384, 256
+    ws = L.bfp8_linear_workspace_size(M, N, K)
+    assert ws > M * K + N * K
+    assert L.bfp8_linear_fwd(P16, P16, P16, M, N, K, ctypes.c_void_p(0x10010), ws, NULL) == B.BFP8_ERR_INVALID_ARG
+    assert L.bfp8_linear_fwd(P16, P16, P16, M, N, K, ctypes.c_void_p(0x10000), ws - 1, NULL) == B.BFP8_ERR_INVALID_ARG
+
+
+SHAPES = [(1, 1, 1), (2, 512, 128), (4, 3584, 640), (130, 384, 256), (129, 130, 131), (257, 65, 300),
+          (300, 7, 1000), (1, 1000, 8), (128, 256, 128), (640, 5120, 1280)]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_quant_lhs_index_replay_exactly_once(M, N, K):
+    for flag in (0, 1):
+        c, s, oob = B.debug_write_counts(0, M, N, K, flag)
+        assert oob == 0 and c.shape == (M, K) and np.all(c == 1)
+        assert np.all(s == 1)
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_quant_rhs_and_weight_index_replay_exactly_once(M, N, K):
+    c, s, oob = B.debug_write_counts(1, M, N, K)
+    assert oob == 0 and np.all(c == 1) and np.all(s == 1)
+    c, s, oob = B.debug_write_counts(2, M, N, K)
+    assert oob == 0 and np.all(c == 1) and np.all(s == 1)
+    c, _, oob = B.debug_write_counts(4, M, N, K)
+    assert oob == 0 and c.shape == (K, N) and np.all(c == 1)
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES + [(4096, 4096, 128), (2048, 4096, 128), (16384, 1024, 128)])
+def test_gemm_epilogue_index_replay_exactly_once(M, N, K):
+    c, _, oob = B.debug_write_counts(3, M, N, K)
+    assert oob == 0 and np.all(c == 1)

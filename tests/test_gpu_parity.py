@@ -1,0 +1,423 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Quantised bytes and scales must match bit for bit; GEMM outputs must satisfy
+|gpu - oracle| <= 2^-7 |oracle| + 1e-3 rms(oracle) element by element.
+Every output buffer sits inside a guard band pre-filled with a sentinel, with
+padding past the logical width, so a write outside the logical tensor shows
+up as a changed sentinel (the unmasked-store bugs the pages describe).
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+import synthetic as S
+from gpu_util import assert_gemm_close, dev_bf16, host_bf16_as_f64, sqnr_db, torch
+
+import blockwise_scaled_fp8_gb300 as B
+
+pytestmark = pytest.mark.gpu
+
+GUARD = 4096
+SENT_U8 = 0xA5
+SENT_F32_BITS = 0x7FC0DEAD  # a NaN pattern no kernel produces
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _setup():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    B.build()
+    O.build()
+    yield
+    B.check_device_errors()
+
+
+def cdiv(a, b):
+    return (a + b - 1) // b
+
+
+def rup(a, b):
+    return cdiv(a, b) * b
+
+
+class Guarded:
+    """A 2-D device buffer [rows, ld] inside a sentinel-filled guard band."""
+
+    def __init__(self, rows, ld, dtype):
+        self.rows, self.ld, self.dtype = rows, ld, dtype
+        n = rows * ld
+        if dtype == torch.uint8:
+            self.flat = torch.full((n + 2 * GUARD,), SENT_U8, dtype=torch.uint8, device="cuda")
+        else:
+            self.flat = torch.full((n + 2 * GUARD,), SENT_F32_BITS, dtype=torch.int32, device="cuda").view(torch.float32)
+        self.t = self.flat[GUARD:GUARD + n].view(rows, ld)
+
+    def check_outside(self, cols):
+        """Sentinels intact in the guard bands and in columns [cols, ld)."""
+        f = self.flat.view(torch.uint8) if self.dtype == torch.uint8 else self.flat.view(torch.int32)
+        sent = SENT_U8 if self.dtype == torch.uint8 else SENT_F32_BITS
+        h = f.cpu().numpy()
+        assert np.all(h[:GUARD] == sent) and np.all(h[-GUARD:] == sent), "write outside the buffer"
+        body = h[GUARD:GUARD + self.rows * self.ld].reshape(self.rows, self.ld)
+        assert np.all(body[:, cols:] == sent), "write into row padding"
+
+
+def f32_bits(a):
+    return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+
+
+# ------------------------------------------------------------------ the cast
+
+def test_cast_exhaustive_all_fp32_patterns():
+    """The device's rounding step equals the oracle's RNE_e4m3 (with the clamp)
+    on every non-NaN fp32 bit pattern."""
+    n = 1 << 28
+    for c in range(16):
+        start = c << 28
+        lo = start if start < (1 << 31) else start - (1 << 32)   # the same bits as int32
+        x = (torch.arange(n, dtype=torch.int32, device="cuda") + lo).view(torch.float32)
+        q = B.cast_e4m3(x).cpu().numpy()
+        bad, first = O.check_cast_range(start, q)
+        assert bad == 0, f"chunk {c}: {bad} mismatches, first pattern 0x{first:08x}"
+
+
+# ------------------------------------------------------------------ quant_lhs
+
+LHS_SHAPES = [(130, 256), (2, 128), (4, 640), (128, 4096), (512, 1280), (4096, 1024), (300, 1000),
+              (3, 136), (5, 72), (1, 1), (7, 77), (2048, 8192)]
+
+
+def _run_lhs(x, transposed, lds_extra):
+    M, K = (x.shape[1], x.shape[0]) if transposed else x.shape
+    Kb = cdiv(K, 128)
+    ldq, lds = rup(K, 16) + 16, M + lds_extra
+    qg, sg = Guarded(M, ldq, torch.uint8), Guarded(Kb, lds, torch.float32)
+    B.quant_lhs(dev_bf16(x), transposed=transposed, q=qg.t, s=sg.t)
+    torch.cuda.synchronize()
+    return qg, sg, M, K
+
+
+@pytest.mark.parametrize("M,K", LHS_SHAPES)
+@pytest.mark.parametrize("lds_extra", [0, 3])
+def test_quant_lhs_bit_exact(M, K, lds_extra):
+    x = S.normal_bf16((M, K), 1.0, seed=M * 31 + K, outlier_frac=1e-3)
+    qg, sg, _, _ = _run_lhs(x, False, lds_extra)
+    q_ref, s_ref = O.quant_lhs(x)
+    assert np.array_equal(qg.t.cpu().numpy()[:, :K], q_ref)
+    assert np.array_equal(f32_bits(sg.t.cpu().numpy()[:, :M]), f32_bits(s_ref))
+    qg.check_outside(K)
+    sg.check_outside(M)
+
+
+TLHS_SHAPES = [(256, 130), (300, 70), (129, 64), (128, 1), (1000, 9), (8192, 4096), (16, 4100)]
+
+
+@pytest.mark.parametrize("T,C", TLHS_SHAPES)
+def test_quant_lhs_transposed_bit_exact(T, C):
+    """dY^T quantised 1x128 along the token dimension (x is [T, C])."""
+    x = S.normal_bf16((T, C), 1e-3, seed=T + 7 * C)
+    qg, sg, M, K = _run_lhs(x, True, 1)
+    q_ref, s_ref = O.quant_lhs(x, transposed=True)
+    assert np.array_equal(qg.t.cpu().numpy()[:, :K], q_ref)
+    assert np.array_equal(f32_bits(sg.t.cpu().numpy()[:, :M]), f32_bits(s_ref))
+    qg.check_outside(K)
+    sg.check_outside(M)
+
+
+RHS_SHAPES = [(260, 70), (8192, 4096), (128, 8), (1000, 130), (1, 5), (4096, 1024)]
+
+
+@pytest.mark.parametrize("K,N", RHS_SHAPES)
+def test_quant_rhs_bit_exact(K, N):
+    x = S.normal_bf16((K, N), 1.0, seed=K + 3 * N)
+    Kb = cdiv(K, 128)
+    ldq, lds = rup(K, 16) + 32, N + 4
+    qg, sg = Guarded(N, ldq, torch.uint8), Guarded(Kb, lds, torch.float32)
+    B.quant_rhs(dev_bf16(x), q=qg.t, s=sg.t)
+    torch.cuda.synchronize()
+    q_ref, s_ref = O.quant_rhs(x)
+    assert np.array_equal(qg.t.cpu().numpy()[:, :K], q_ref)
+    assert np.array_equal(f32_bits(sg.t.cpu().numpy()[:, :N]), f32_bits(s_ref))
+    qg.check_outside(K)
+    sg.check_outside(N)
+
+
+W_SHAPES = [(384, 256), (300, 260), (4096, 4096), (5120, 1280), (3584, 640), (7, 9), (129, 1000)]
+
+
+@pytest.mark.parametrize("N,K", W_SHAPES)
+def test_quant_weight_bit_exact(N, K):
+    w = S.normal_bf16((N, K), 0.02, seed=N + K)
+    Nb, Kb = cdiv(N, 128), cdiv(K, 128)
+    qg = Guarded(N, rup(K, 16) + 16, torch.uint8)
+    tg = Guarded(K, rup(N, 16) + 16, torch.uint8)
+    sg = Guarded(Nb, Kb + 1, torch.float32)
+    B.quant_weight(dev_bf16(w), with_q=True, with_t=True, q=qg.t, qt=tg.t, s=sg.t)
+    torch.cuda.synchronize()
+    q_ref, qt_ref, s_ref = O.quant_weight(w, with_t=True)
+    assert np.array_equal(qg.t.cpu().numpy()[:, :K], q_ref)
+    assert np.array_equal(tg.t.cpu().numpy()[:, :N], qt_ref)
+    assert np.array_equal(f32_bits(sg.t.cpu().numpy()[:, :Kb]), f32_bits(s_ref))
+    qg.check_outside(K)
+    tg.check_outside(N)
+    sg.check_outside(Kb)
+
+
+def _adversarial_bf16(rows, cols, seed):
+    """Random finite bf16 patterns over the whole exponent range, plus
+    all-zero, signed-zero, all-equal and tie-producing groups."""
+    rng = np.random.default_rng(seed)
+    b = rng.integers(0, 1 << 16, size=(rows, cols), dtype=np.uint32).astype(np.uint16)
+    b[(b & 0x7F80) == 0x7F80] &= 0xBF7F  # no Inf/NaN
+    b[0, :] = 0
+    if rows > 1:
+        b[1, ::2] = 0x8000
+    if rows > 2:
+        b[2, :] = S.f32_to_bf16_bits(np.array([0.3], np.float32))[0]
+    if rows > 3:  # amax 448 -> s = 1 exactly: x/s lands on e4m3 ties
+        v = (np.arange(cols) % 64).astype(np.float32) / 16.0 + 1.0 / 32.0
+        v[0] = 448.0
+        b[3, :] = S.f32_to_bf16_bits(v)
+    if rows > 4:  # tiny magnitudes: subnormal bf16, subnormal scales
+        b[4, :] = rng.integers(1, 0x80, size=cols).astype(np.uint16)
+    return b
+
+
+@pytest.mark.parametrize("M,K", [(8, 128), (64, 1024), (37, 300)])
+def test_quant_adversarial_values_bit_exact(M, K):
+    x = _adversarial_bf16(M, K, seed=M + K)
+    qg, sg, _, _ = _run_lhs(x, False, 0)
+    q_ref, s_ref = O.quant_lhs(x)
+    assert np.array_equal(qg.t.cpu().numpy()[:, :K], q_ref)
+    assert np.array_equal(f32_bits(sg.t.cpu().numpy()[:, :M]), f32_bits(s_ref))
+    # same values through the transposed-read and 128x1 kernels
+    xt = np.ascontiguousarray(x.T)
+    qg2, sg2, _, _ = _run_lhs(xt, True, 0)
+    assert np.array_equal(qg2.t.cpu().numpy()[:, :K], q_ref)
+    assert np.array_equal(f32_bits(sg2.t.cpu().numpy()[:, :M]), f32_bits(s_ref))
+    q3, s3 = B.quant_rhs(dev_bf16(xt))
+    assert np.array_equal(q3.cpu().numpy()[:, :K], q_ref)
+    assert np.array_equal(f32_bits(s3.cpu().numpy()[:, :M]), f32_bits(s_ref))
+    _, _, sw = B.quant_weight(dev_bf16(x))
+    _, _, sw_ref = O.quant_weight(x)
+    assert np.array_equal(f32_bits(sw.cpu().numpy()), f32_bits(sw_ref))
+
+
+# ------------------------------------------------------------------ GEMMs in isolation
+
+def _random_codes(rng, shape):
+    c = rng.integers(0, 256, size=shape, dtype=np.uint8)
+    c[(c & 0x7F) == 0x7F] = 0x00  # no NaN codes
+    return c
+
+
+def _gemm_case(M, N, K, mode, seed, ldc_extra=0):
+    """Random e4m3 codes and random scales fed to both sides."""
+    rng = np.random.default_rng(seed)
+    Kb, Nb = cdiv(K, 128), cdiv(N, 128)
+    lda = ldb = rup(K, 16)
+    qa = _random_codes(rng, (M, lda))
+    qb = _random_codes(rng, (N, ldb))
+    sa = rng.uniform(0.01, 2.0, (Kb, M + 1)).astype(np.float32)
+    if mode == O.SB_TILE:
+        sb = rng.uniform(0.01, 2.0, (Nb, Kb)).astype(np.float32)
+    elif mode == O.SB_TILE_T:
+        sb = rng.uniform(0.01, 2.0, (Kb, Nb + 1)).astype(np.float32)
+    else:
+        sb = rng.uniform(0.01, 2.0, (Kb, rup(N, 4))).astype(np.float32)
+    ref = O.gemm(qa, sa, qb, sb, mode, K)
+    cu = lambda a: torch.from_numpy(a).cuda()
+    ldc = N + ldc_extra
+    flat16 = torch.full((M * ldc + 2 * GUARD,), 0x7FC1, dtype=torch.int16, device="cuda")
+    out = flat16[GUARD:GUARD + M * ldc].view(torch.bfloat16).view(M, ldc)
+    if mode == O.SB_COL:
+        B.gemm_1x128_128x1(cu(qa), cu(sa), cu(qb), cu(sb), K, out=out, M=M, N=N)
+    else:
+        B.gemm_1x128_128x128(cu(qa), cu(sa), cu(qb), cu(sb), K, sb_transposed=(mode == O.SB_TILE_T),
+                             out=out, M=M, N=N)
+    torch.cuda.synchronize()
+    h = flat16.cpu().numpy()
+    assert np.all(h[:GUARD] == 0x7FC1) and np.all(h[-GUARD:] == 0x7FC1), "write outside C"
+    body = h[GUARD:GUARD + M * ldc].reshape(M, ldc)
+    assert np.all(body[:, N:] == 0x7FC1), "write into C row padding"
+    got = out[:, :N].float().cpu().numpy().astype(np.float64)
+    return got, ref
+
+
+GEMM_SHAPES = [(130, 384, 256), (1, 8, 128), (2, 512, 128), (4, 3584, 640), (128, 256, 128),
+               (129, 257, 1000), (300, 130, 77), (256, 512, 4096), (64, 1000, 200), (513, 384, 384)]
+
+
+@pytest.mark.parametrize("M,N,K", GEMM_SHAPES)
+@pytest.mark.parametrize("mode", [O.SB_TILE, O.SB_TILE_T, O.SB_COL])
+def test_gemm_random_codes_matches_oracle(M, N, K, mode):
+    got, ref = _gemm_case(M, N, K, mode, seed=M * 7 + N * 3 + K + mode, ldc_extra=8)
+    assert_gemm_close(got, ref, f"gemm mode {mode} {M}x{N}x{K}")
+
+
+# ------------------------------------------------------------------ quant + GEMM (linear)
+
+def _dev_linear(M, N, K, seed, x_std=1.0, w_std=0.02, dy_std=1e-3, outliers=0.0):
+    x = S.normal_bf16((M, K), x_std, seed=seed * 16, outlier_frac=outliers)
+    w = S.normal_bf16((N, K), w_std, seed=seed * 16 + 1)
+    dy = S.normal_bf16((M, N), dy_std, seed=seed * 16 + 2)
+    return x, w, dy
+
+
+SMALL_M = [(m, n, k) for m in (2, 4, 128, 512) for (n, k) in ((512, 128), (5120, 1280), (3584, 640), (4096, 4096))]
+
+
+@pytest.mark.parametrize("M,N,K", [(130, 384, 256)] + SMALL_M)
+def test_linear_fwd_matches_oracle(M, N, K):
+    x, w, _ = _dev_linear(M, N, K, seed=3)
+    y = B.linear_fwd(dev_bf16(x), dev_bf16(w))
+    torch.cuda.synchronize()
+    assert_gemm_close(host_bf16_as_f64(y), O.linear_fwd(x, w), f"fwd {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(130, 384, 256), (257, 300, 131), (512, 1024, 640), (1024, 256, 512)])
+def test_linear_bwd_matches_oracle(M, N, K):
+    x, w, dy = _dev_linear(M, N, K, seed=4)
+    dx, dw = B.linear_bwd(dev_bf16(dy), dev_bf16(x), dev_bf16(w))
+    torch.cuda.synchronize()
+    assert_gemm_close(host_bf16_as_f64(dx), O.linear_dgrad(dy, w), f"dgrad {M}x{N}x{K}")
+    assert_gemm_close(host_bf16_as_f64(dw), O.linear_wgrad(dy, x), f"wgrad {M}x{N}x{K}")
+
+
+def _pages_sqnr():
+    import os
+    rows = []
+    with open(os.path.join(os.path.dirname(__file__), "golden", "sqnr_pages.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                m, n, k, db = line.split()
+                rows.append((int(m), int(n), int(k), float(db)))
+    return rows
+
+
+@pytest.mark.parametrize("M,N,K,pages_db", _pages_sqnr())
+def test_gemm_sqnr_vs_pages(M, N, K, pages_db):
+    """SQNR of the device's blockwise FP8 GEMM against an fp64 matmul of the
+    bf16 inputs on N(0,1) data: at least 28 dB and within 0.5 dB of the
+    pages' printed figure for the same shape."""
+    x = S.normal_bf16((M, K), 1.0, seed=11)
+    w = S.normal_bf16((N, K), 1.0, seed=12)
+    y = host_bf16_as_f64(B.linear_fwd(dev_bf16(x), dev_bf16(w)))
+    ref = (torch.from_numpy(S.bf16_bits_to_f32(x)).double().cuda()
+           @ torch.from_numpy(S.bf16_bits_to_f32(w)).double().cuda().T).cpu().numpy()
+    db = sqnr_db(ref, y)
+    assert db >= 28.0 and abs(db - pages_db) <= 0.5, db
+
+
+# ------------------------------------------------------------------ full-size workloads, sampled
+
+def _sample_idx(n, k, seed):
+    rng = np.random.default_rng(seed)
+    idx = set(rng.choice(n, size=min(k, n), replace=False).tolist())
+    idx.update({0, n - 1})
+    return np.array(sorted(idx), dtype=np.int64)
+
+
+def _blocks_of(idx):
+    return np.array(sorted({int(i) // 128 for i in idx}), dtype=np.int64)
+
+
+def _expand_blocks(blocks, n):
+    return np.concatenate([np.arange(b * 128, min(n, b * 128 + 128)) for b in blocks])
+
+
+def _oracle_fwd_sampled(x, w, rows, col_blocks):
+    """Oracle y[rows][:, cols in col_blocks] computed from only the rows of x
+    and the 128-row blocks of W it needs (groups and tiles are local to them)."""
+    cols = _expand_blocks(col_blocks, w.shape[0])
+    qa, sa = O.quant_lhs(np.ascontiguousarray(x[rows]))
+    qb, _, sb = O.quant_weight(np.ascontiguousarray(w[cols]))
+    return O.gemm(qa, sa, qb, sb, O.SB_TILE, x.shape[1]), cols
+
+
+@pytest.mark.parametrize("wl", [S.FWD_MID, S.FWD_SQUARE])
+def test_fwd_full_size_sampled(wl):
+    x, w = wl.x(), wl.w()
+    y = B.linear_fwd(dev_bf16(x), dev_bf16(w))
+    torch.cuda.synchronize()
+    rows = _sample_idx(wl.M, 48, 1)
+    cblk = _sample_idx(wl.N // 128, 3, 2)
+    ref, cols = _oracle_fwd_sampled(x, w, rows, cblk)
+    got = host_bf16_as_f64(y[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()])
+    assert_gemm_close(got, ref, wl.name)
+
+
+def test_wgrad_full_size_sampled():
+    wl = S.WGRAD  # dY [8192,4096], X [8192,4096] -> dW [4096,4096]
+    dy, x = wl.dy(), wl.x()
+    w = wl.w()
+    dx, dw = B.linear_bwd(dev_bf16(dy), dev_bf16(x), dev_bf16(w))
+    torch.cuda.synchronize()
+    rows = _sample_idx(wl.N, 40, 3)     # output-feature rows of dW
+    cols = _sample_idx(wl.K, 300, 4)    # input-feature columns of dW
+    qa, sa = O.quant_lhs(np.ascontiguousarray(dy[:, rows]), transposed=True)
+    qbT, sb = O.quant_rhs(np.ascontiguousarray(x[:, cols]))
+    ref = O.gemm(qa, sa, qbT, sb, O.SB_COL, wl.M)
+    got = host_bf16_as_f64(dw[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()])
+    assert_gemm_close(got, ref, "wgrad 4096x4096x8192")
+    # dgrad of the same step, sampled: dX = dY W
+    r2 = _sample_idx(wl.M, 24, 5)
+    kblk = _sample_idx(wl.K // 128, 2, 6)
+    kcols = _expand_blocks(kblk, wl.K)
+    qa2, sa2 = O.quant_lhs(np.ascontiguousarray(dy[r2]))
+    _, qt, sw = O.quant_weight(np.ascontiguousarray(w[:, kcols]), with_t=True)
+    ref2 = O.gemm(qa2, sa2, qt, sw, O.SB_TILE_T, wl.N)
+    got2 = host_bf16_as_f64(dx[torch.from_numpy(r2).cuda()][:, torch.from_numpy(kcols).cuda()])
+    assert_gemm_close(got2, ref2, "dgrad 8192x4096x4096")
+
+
+def test_mlp_up_step_full_size_sampled():
+    """The full linear step at 16384 x 14336 x 4096: fwd, dgrad and wgrad,
+    each checked on sampled outputs the oracle computes one by one."""
+    wl = S.MLP_UP
+    x, w, dy = wl.x(), wl.w(), wl.dy()
+    xd, wd, dyd = dev_bf16(x), dev_bf16(w), dev_bf16(dy)
+    y = B.linear_fwd(xd, wd)
+    dx, dw = B.linear_bwd(dyd, xd, wd)
+    torch.cuda.synchronize()
+    B.check_device_errors()
+    rows = _sample_idx(wl.M, 16, 7)
+    ref, cols = _oracle_fwd_sampled(x, w, rows, _sample_idx(wl.N // 128, 2, 8))
+    got = host_bf16_as_f64(y[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()])
+    assert_gemm_close(got, ref, "mlp_up fwd")
+    kcols = _expand_blocks(_sample_idx(wl.K // 128, 2, 9), wl.K)
+    qa, sa = O.quant_lhs(np.ascontiguousarray(dy[rows]))
+    _, qt, sw = O.quant_weight(np.ascontiguousarray(w[:, kcols]), with_t=True)
+    ref = O.gemm(qa, sa, qt, sw, O.SB_TILE_T, wl.N)
+    got = host_bf16_as_f64(dx[torch.from_numpy(rows).cuda()][:, torch.from_numpy(kcols).cuda()])
+    assert_gemm_close(got, ref, "mlp_up dgrad")
+    nrows = _sample_idx(wl.N, 12, 10)
+    kc = _sample_idx(wl.K, 200, 11)
+    qa, sa = O.quant_lhs(np.ascontiguousarray(dy[:, nrows]), transposed=True)
+    qbT, sb = O.quant_rhs(np.ascontiguousarray(x[:, kc]))
+    ref = O.gemm(qa, sa, qbT, sb, O.SB_COL, wl.M)
+    got = host_bf16_as_f64(dw[torch.from_numpy(nrows).cuda()][:, torch.from_numpy(kc).cuda()])
+    assert_gemm_close(got, ref, "mlp_up wgrad")
+
+
+def test_repeat_runs_are_deterministic():
+    x, w, dy = _dev_linear(512, 640, 384, seed=9)
+    xd, wd, dyd = dev_bf16(x), dev_bf16(w), dev_bf16(dy)
+    a = [B.linear_fwd(xd, wd) for _ in range(2)]
+    b = [B.linear_bwd(dyd, xd, wd) for _ in range(2)]
+    torch.cuda.synchronize()
+    assert torch.equal(a[0].view(torch.int16), a[1].view(torch.int16))
+    assert torch.equal(b[0][0].view(torch.int16), b[1][0].view(torch.int16))
+    assert torch.equal(b[0][1].view(torch.int16), b[1][1].view(torch.int16))
+
+
+def test_empty_problems_are_noops():
+    e = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    q, s = B.quant_lhs(e)
+    assert q.shape[0] == 0
+    out = torch.full((4, 8), 1.0, dtype=torch.bfloat16, device="cuda")
+    z = torch.zeros((4, 16), dtype=torch.uint8, device="cuda")
+    sc = torch.ones((1, 8), dtype=torch.float32, device="cuda")
+    B.gemm_1x128_128x128(z, sc, torch.zeros((8, 16), dtype=torch.uint8, device="cuda"), sc, 0, out=out)
+    torch.cuda.synchronize()
+    assert torch.all(out.float() == 0)
