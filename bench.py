@@ -100,6 +100,24 @@ class ClockSampler:
             self.proc = None
         return self
 
+    def _lines(self):
+        try:
+            with open(self.path) as f:
+                return sum(1 for _ in f)
+        except OSError:
+            return 0
+
+    def wait_first_sample(self, timeout_s=3.0):
+        t0 = time.time()
+        while self.proc is not None and self._lines() == 0 and time.time() - t0 < timeout_s:
+            time.sleep(0.05)
+
+    def mark_start(self):
+        self.n0 = self._lines()
+
+    def mark_end(self):
+        self.n1 = self._lines()
+
     def __exit__(self, *a):
         if self.proc is not None:
             self.proc.terminate()
@@ -115,18 +133,21 @@ class ClockSampler:
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    mx.append(float(parts[2]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(n)
+            lines = f.readlines()
+        n0, n1 = getattr(self, "n0", 0), getattr(self, "n1", len(lines))
+        # samples taken during the timed region (plus the one in flight at its end)
+        for line in lines[n0:min(len(lines), n1 + 1)]:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
         try:
             os.remove(self.path)
         except OSError:
@@ -141,23 +162,50 @@ class ClockSampler:
 # CPU oracle leg (the reported baseline; also the whole `--impl reference` arm)
 # ---------------------------------------------------------------------------
 
-def oracle_step_sample(x, w, dy, rows, nrows):
-    """One bounded sample of the step on the CPU oracle: forward and
-    input-gradient outputs for `rows` token rows, weight-gradient outputs for
-    `nrows` output features, each with every quantisation it needs.
-    Returns the GEMM FLOPs the sample covers."""
+def oracle_step_sample(x, w, dy, rows, nrows, nblocks, kblocks, parts=("fwd", "dgrad", "wgrad")):
+    """One bounded sample of the step on the CPU oracle: forward outputs
+    y[rows, n in nblocks], input-gradient outputs dx[rows, k in kblocks] and
+    weight-gradient outputs dw[nrows, k in kblocks], each with every
+    quantisation those outputs need (groups and tiles are local to rows,
+    128-row blocks and columns, so the sub-problems quantise exactly as the
+    full tensors would).  Returns the GEMM FLOPs the sample covers."""
     import oracle as O
     M, K = x.shape
     N = w.shape[0]
-    qa, sa = O.quant_lhs(np.ascontiguousarray(x[rows]))
-    qw, qwt, sw = O.quant_weight(w, with_t=True)
-    O.gemm(qa, sa, qw, sw, O.SB_TILE, K)
-    qd, sd = O.quant_lhs(np.ascontiguousarray(dy[rows]))
-    O.gemm(qd, sd, qwt, sw, O.SB_TILE_T, N)
-    qdt, sdt = O.quant_lhs(np.ascontiguousarray(dy[:, nrows]), transposed=True)
-    qxt, sxt = O.quant_rhs(x)
-    O.gemm(qdt, sdt, qxt, sxt, O.SB_COL, M)
-    return 2.0 * (len(rows) * N * K + len(rows) * K * N + len(nrows) * K * M)
+    ncols = np.concatenate([np.arange(b * 128, min(N, b * 128 + 128)) for b in nblocks])
+    kcols = np.concatenate([np.arange(b * 128, min(K, b * 128 + 128)) for b in kblocks])
+    flops = 0.0
+    if "fwd" in parts:
+        qa, sa = O.quant_lhs(np.ascontiguousarray(x[rows]))
+        qw, _, sw = O.quant_weight(np.ascontiguousarray(w[ncols]))
+        O.gemm(qa, sa, qw, sw, O.SB_TILE, K)
+        flops += 2.0 * len(rows) * len(ncols) * K
+    if "dgrad" in parts:
+        qd, sd = O.quant_lhs(np.ascontiguousarray(dy[rows]))
+        _, qwt, swt = O.quant_weight(np.ascontiguousarray(w[:, kcols]), with_t=True)
+        O.gemm(qd, sd, qwt, swt, O.SB_TILE_T, N)
+        flops += 2.0 * len(rows) * len(kcols) * N
+    if "wgrad" in parts:
+        qdt, sdt = O.quant_lhs(np.ascontiguousarray(dy[:, nrows]), transposed=True)
+        qxt, sxt = O.quant_rhs(np.ascontiguousarray(x[:, kcols]))
+        O.gemm(qdt, sdt, qxt, sxt, O.SB_COL, M)
+        flops += 2.0 * len(nrows) * len(kcols) * M
+    return flops
+
+
+def _sample(wl, rows, blocks, seed):
+    rng = np.random.default_rng(seed)
+    r = np.sort(rng.choice(wl.M, size=min(wl.M, rows), replace=False))
+    nr = np.sort(rng.choice(wl.N, size=min(wl.N, rows), replace=False))
+    nb = np.sort(rng.choice((wl.N + 127) // 128, size=min((wl.N + 127) // 128, blocks), replace=False))
+    kb = np.sort(rng.choice((wl.K + 127) // 128, size=min((wl.K + 127) // 128, blocks), replace=False))
+    return r, nr, nb, kb
+
+
+def _sample_text(wl, r, nr, nb, kb):
+    return (f"fwd y[{len(r)} of {wl.M} rows, {len(nb)} of {(wl.N + 127) // 128} 128-col blocks], "
+            f"dgrad dx[{len(r)} rows, {len(kb)} of {(wl.K + 127) // 128} blocks], "
+            f"wgrad dw[{len(nr)} of {wl.N} rows, {len(kb)} blocks], each with the quantisations it needs")
 
 
 def run_reference(args, wl):
@@ -167,20 +215,18 @@ def run_reference(args, wl):
     if rank != 0:
         return 0
     x, w, dy = wl.x(), wl.w(), wl.dy()
-    rng = np.random.default_rng(0)
-    rows = np.sort(rng.choice(wl.M, size=args.ref_rows, replace=False))
-    nrows = np.sort(rng.choice(wl.N, size=args.ref_rows, replace=False))
-    for _ in range(args.warmup):
-        oracle_step_sample(x, w, dy, rows, nrows)
+    r, nr, nb, kb = _sample(wl, args.ref_rows, args.ref_blocks, 0)
+    rot = [("fwd",), ("dgrad",), ("wgrad",)]  # one part of the step per iteration, in rotation
+    for i in range(args.warmup):
+        oracle_step_sample(x, w, dy, r, nr, nb, kb, rot[i % 3])
     t0 = time.perf_counter()
     flops = 0.0
-    for _ in range(args.steps):
-        flops += oracle_step_sample(x, w, dy, rows, nrows)
+    for i in range(args.steps):
+        flops += oracle_step_sample(x, w, dy, r, nr, nb, kb, rot[i % 3])
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
     cores = O._threads()
-    sample = (f"{args.ref_rows} of {wl.M} token rows (fwd, dgrad) and {args.ref_rows} of {wl.N} "
-              f"output features (wgrad), with full W and x quantisation, per step")
+    sample = "per step, one of (in rotation): " + _sample_text(wl, r, nr, nb, kb)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -216,13 +262,15 @@ class Step:
         self.y, self.dx, self.dw = e(M, N, dt=bf), e(M, K, dt=bf), e(N, K, dt=bf)
         self.names = ["quant_lhs_x", "quant_weight_w", "gemm_fwd", "quant_lhs_dy", "quant_weight_wt",
                       "gemm_dgrad", "quant_lhs_dyT", "quant_rhs_x", "gemm_wgrad"]
-        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(len(self.names) + 1)]
         self.launches_per_step = len(self.names)
 
-    def run(self, x, w, dy, timed=True):
+    def new_events(self):
+        return [self.torch.cuda.Event(enable_timing=True) for _ in range(len(self.names) + 1)]
+
+    def run(self, x, w, dy, ev=None):
         B, wl = self.B, self.wl
         M, N, K = wl.M, wl.N, wl.K
-        ev = self.events
+        timed = ev is not None
         calls = [
             lambda: B.quant_lhs(x, q=self.qx, s=self.sx),
             lambda: B.quant_weight(w, with_q=True, with_t=False, q=self.qw, s=self.sw),
@@ -242,8 +290,7 @@ class Step:
             if timed:
                 ev[i + 1].record()
 
-    def kernel_ms(self):
-        ev = self.events
+    def kernel_ms(self, ev):
         return [ev[i].elapsed_time(ev[i + 1]) for i in range(len(self.names))]
 
 
@@ -289,28 +336,29 @@ def run_gpu(args, wl):
     step = Step(wl, torch, B, dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
-    for _ in range(args.warmup):
-        step.run(x, w, dy, timed=False)
-        flush.fill_(1.0)
-    torch.cuda.synchronize()
-    B.check_device_errors()
-
-    step_ms, per_kernel = [], []
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
+    events = [step.new_events() for _ in range(args.steps)]
     with ClockSampler(local) as clk:
-        for _ in range(args.steps):
-            flush.fill_(0.0)  # L2 flush between timed steps (outside the step's events)
-            step.run(x, w, dy, timed=True)
-            torch.cuda.synchronize()
-            per_kernel.append(step.kernel_ms())
-            step_ms.append(step.events[0].elapsed_time(step.events[-1]))
+        for _ in range(args.warmup):
+            step.run(x, w, dy)
+            flush.fill_(1.0)
         torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
+        B.check_device_errors()
+        clk.wait_first_sample()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        clk.mark_start()
+        for i in range(args.steps):
+            flush.fill_(0.0)  # L2 flush between timed steps (outside the step's events)
+            step.run(x, w, dy, events[i])
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        clk.mark_end()
     B.check_device_errors()
     clocks = clk.summary()
+    per_kernel = [step.kernel_ms(ev) for ev in events]
+    step_ms = [ev[0].elapsed_time(ev[-1]) for ev in events]
 
     total_ms = float(sum(step_ms))
     if dist:
@@ -399,15 +447,12 @@ def run_gpu(args, wl):
     if rank == 0 and not args.no_cpu_baseline:
         import oracle as O
         O.build()
-        rng = np.random.default_rng(0)
-        rows = np.sort(rng.choice(wl.M, size=args.ref_rows, replace=False))
-        nrows = np.sort(rng.choice(wl.N, size=args.ref_rows, replace=False))
+        r, nr, nb, kb = _sample(wl, args.cpu_rows, args.cpu_blocks, 1)
         t0 = time.perf_counter()
-        fl = oracle_step_sample(xh, wh, dyh, rows, nrows)
+        fl = oracle_step_sample(xh, wh, dyh, r, nr, nb, kb)
         dt = time.perf_counter() - t0
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": O._threads(), "kind": "oracle",
-               "sample": f"{args.ref_rows} token rows (fwd, dgrad) + {args.ref_rows} output features (wgrad) "
-                         f"of the step, with full W and x quantisation; {dt:.1f} s"}
+               "sample": _sample_text(wl, r, nr, nb, kb) + f"; {dt:.1f} s"}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -428,11 +473,14 @@ def run_gpu(args, wl):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="mid", choices=sorted(WORKLOADS))
-    ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--ref-rows", type=int, default=4, help="oracle sample rows per reference step")
+    ap.add_argument("--ref-blocks", type=int, default=1, help="oracle sample 128-col blocks per reference step")
+    ap.add_argument("--cpu-rows", type=int, default=512, help="oracle sample rows of the cpu_baseline leg")
+    ap.add_argument("--cpu-blocks", type=int, default=32, help="oracle sample 128-col blocks, cpu_baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
