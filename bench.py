@@ -1,9 +1,11 @@
 """Benchmark of the blockwise-FP8 linear-layer step on GB300.
 
-One step = the whole hot path over one batch: quantise x (1x128 along K) and
-W (128x128 tiles), forward GEMM 1x128 x 128x128; quantise dY (1x128 along N),
-W^T tiles, input-gradient GEMM 1x128 x 128x128; quantise dY^T (1x128 along M)
-and x (128x1 along M), weight-gradient GEMM 1x128 x 128x1.
+One step = the whole hot path over one batch, in the library's training form:
+quantise x once into its 1x128 groups along K and its 128x1 groups along M,
+and W once into its 128x128 tiles (as is and transposed); forward GEMM
+1x128 x 128x128; quantise dY once into its 1x128 groups along N and along M
+(of dY^T); input-gradient GEMM 1x128 x 128x128 and weight-gradient GEMM
+1x128 x 128x1.
 
 Default workload: the pages' mid shape M=2048, N=4096, K=4096 (x ~N(0,1) with
 0.1% x100 outliers, W ~N(0,0.02), dY ~N(0,1e-3)), L2 flushed between steps.
@@ -254,14 +256,12 @@ class Step:
         u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
         e = lambda *s, dt: torch.empty(s, dtype=dt, device=dev)
         self.qx, self.sx = e(M, rup(K, 16), dt=u8), e(cd(K), rup(M, 4), dt=f32)
-        self.qw, self.sw = e(N, rup(K, 16), dt=u8), e(cd(N), cd(K), dt=f32)
-        self.qdy, self.sdy = e(M, rup(N, 16), dt=u8), e(cd(N), rup(M, 4), dt=f32)
-        self.qwt, self.sw2 = e(K, rup(N, 16), dt=u8), e(cd(N), cd(K), dt=f32)
-        self.qdyt, self.sdyt = e(N, rup(M, 16), dt=u8), e(cd(M), rup(N, 4), dt=f32)
         self.qxt, self.sxt = e(K, rup(M, 16), dt=u8), e(cd(M), rup(K, 4), dt=f32)
+        self.qw, self.qwt, self.sw = e(N, rup(K, 16), dt=u8), e(K, rup(N, 16), dt=u8), e(cd(N), cd(K), dt=f32)
+        self.qdy, self.sdy = e(M, rup(N, 16), dt=u8), e(cd(N), rup(M, 4), dt=f32)
+        self.qdyt, self.sdyt = e(N, rup(M, 16), dt=u8), e(cd(M), rup(N, 4), dt=f32)
         self.y, self.dx, self.dw = e(M, N, dt=bf), e(M, K, dt=bf), e(N, K, dt=bf)
-        self.names = ["quant_lhs_x", "quant_weight_w", "gemm_fwd", "quant_lhs_dy", "quant_weight_wt",
-                      "gemm_dgrad", "quant_lhs_dyT", "quant_rhs_x", "gemm_wgrad"]
+        self.names = ["quant_dual_x", "quant_weight_w", "gemm_fwd", "quant_dual_dy", "gemm_dgrad", "gemm_wgrad"]
         self.launches_per_step = len(self.names)
 
     def new_events(self):
@@ -272,15 +272,12 @@ class Step:
         M, N, K = wl.M, wl.N, wl.K
         timed = ev is not None
         calls = [
-            lambda: B.quant_lhs(x, q=self.qx, s=self.sx),
-            lambda: B.quant_weight(w, with_q=True, with_t=False, q=self.qw, s=self.sw),
+            lambda: B.quant_dual(x, q_row=self.qx, s_row=self.sx, q_col=self.qxt, s_col=self.sxt),
+            lambda: B.quant_weight(w, with_q=True, with_t=True, q=self.qw, qt=self.qwt, s=self.sw),
             lambda: B.gemm_1x128_128x128(self.qx, self.sx, self.qw, self.sw, K, out=self.y, M=M, N=N),
-            lambda: B.quant_lhs(dy, q=self.qdy, s=self.sdy),
-            lambda: B.quant_weight(w, with_q=False, with_t=True, qt=self.qwt, s=self.sw2),
-            lambda: B.gemm_1x128_128x128(self.qdy, self.sdy, self.qwt, self.sw2, N, sb_transposed=True,
+            lambda: B.quant_dual(dy, q_row=self.qdy, s_row=self.sdy, q_col=self.qdyt, s_col=self.sdyt),
+            lambda: B.gemm_1x128_128x128(self.qdy, self.sdy, self.qwt, self.sw, N, sb_transposed=True,
                                          out=self.dx, M=M, N=K),
-            lambda: B.quant_lhs(dy, transposed=True, q=self.qdyt, s=self.sdyt),
-            lambda: B.quant_rhs(x, q=self.qxt, s=self.sxt),
             lambda: B.gemm_1x128_128x1(self.qdyt, self.sdyt, self.qxt, self.sxt, M, out=self.dw, M=N, N=K),
         ]
         if timed:
@@ -296,19 +293,17 @@ class Step:
 
 def algorithmic_units(wl):
     """Per-launch algorithmic work: FLOPs for the GEMMs, bytes for the quants
-    (read 2 B/elem bf16, write 1 B/elem e4m3, plus 4 B per scale)."""
+    (read 2 B/elem bf16 once, write 1 B/elem e4m3 per output form, plus 4 B
+    per scale)."""
     M, N, K = wl.M, wl.N, wl.K
     cd = lambda a: (a + 127) // 128
     gem = 2.0 * M * N * K
     return {
-        "quant_lhs_x": ("GB/s", 3.0 * M * K + 4.0 * M * cd(K)),
-        "quant_weight_w": ("GB/s", 3.0 * N * K + 4.0 * cd(N) * cd(K)),
+        "quant_dual_x": ("GB/s", 4.0 * M * K + 4.0 * (M * cd(K) + K * cd(M))),
+        "quant_weight_w": ("GB/s", 4.0 * N * K + 4.0 * cd(N) * cd(K)),
         "gemm_fwd": ("TFLOP/s", gem),
-        "quant_lhs_dy": ("GB/s", 3.0 * M * N + 4.0 * M * cd(N)),
-        "quant_weight_wt": ("GB/s", 3.0 * N * K + 4.0 * cd(N) * cd(K)),
+        "quant_dual_dy": ("GB/s", 4.0 * M * N + 4.0 * (M * cd(N) + N * cd(M))),
         "gemm_dgrad": ("TFLOP/s", gem),
-        "quant_lhs_dyT": ("GB/s", 3.0 * M * N + 4.0 * N * cd(M)),
-        "quant_rhs_x": ("GB/s", 3.0 * M * K + 4.0 * K * cd(M)),
         "gemm_wgrad": ("TFLOP/s", gem),
     }
 
@@ -410,19 +405,18 @@ def run_gpu(args, wl):
         oy = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
         odx = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
         odw = torch.empty((N, K), dtype=torch.bfloat16).pin_memory()
-        dx_, dw_, dy_ = torch.empty_like(x), torch.empty_like(w), torch.empty_like(dy)
-        ws = torch.empty(B.linear_workspace_size(M, N, K) + 256, dtype=torch.uint8, device=dev)
-        y_ = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        gx, gdx = torch.empty_like(x), torch.empty((M, K), dtype=torch.bfloat16, device=dev)
-        gdw = torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+        gx, gw, gdy = torch.empty_like(x), torch.empty_like(w), torch.empty_like(dy)
+        ws = B.linear_train_workspace(M, N, K, device=dev)
+        gy = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        gdx, gdw = torch.empty((M, K), dtype=torch.bfloat16, device=dev), torch.empty((N, K), dtype=torch.bfloat16, device=dev)
 
         def e2e_step():
             gx.copy_(hx, non_blocking=True)
-            dw_.copy_(hw, non_blocking=True)
-            dy_.copy_(hdy, non_blocking=True)
-            B.linear_fwd(gx, dw_, y=y_, ws=ws)
-            B.linear_bwd(dy_, gx, dw_, dx=gdx, dw=gdw, ws=ws)
-            oy.copy_(y_, non_blocking=True)
+            gw.copy_(hw, non_blocking=True)
+            gdy.copy_(hdy, non_blocking=True)
+            B.linear_fwd_train(gx, gw, ws, y=gy)
+            B.linear_bwd_saved(gdy, ws, M, N, K, dx=gdx, dw=gdw)
+            oy.copy_(gy, non_blocking=True)
             odx.copy_(gdx, non_blocking=True)
             odw.copy_(gdw, non_blocking=True)
 
@@ -460,7 +454,8 @@ def run_gpu(args, wl):
                 "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)",
                 "data": "synthetic",
                 "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
-                           "step": "quant x,W + fwd GEMM; quant dY,W^T + dgrad GEMM; quant dY^T,x + wgrad GEMM",
+                           "step": "quant x (1x128 + 128x1), W (tiles + transposed); fwd GEMM; "
+                                   "quant dY (1x128 along N and M); dgrad GEMM; wgrad GEMM",
                            "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
                 "gpu_launches": step.launches_per_step * args.steps,
                 "roofline": roof, "parts": parts, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks}

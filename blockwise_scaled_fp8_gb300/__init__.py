@@ -22,7 +22,8 @@ EXPORTS = [
     "bfp8_last_error", "bfp8_quant_lhs", "bfp8_quant_rhs", "bfp8_quant_weight",
     "bfp8_gemm_1x128_128x128", "bfp8_gemm_1x128_128x1", "bfp8_linear_workspace_size",
     "bfp8_linear_fwd", "bfp8_linear_bwd", "bfp8_cast_e4m3", "bfp8_check_device_errors",
-    "bfp8_debug_write_counts",
+    "bfp8_debug_write_counts", "bfp8_debug_gemm_stall", "bfp8_quant_dual",
+    "bfp8_linear_train_workspace_size", "bfp8_linear_fwd_train", "bfp8_linear_bwd_saved",
 ]
 
 _lib = None
@@ -62,8 +63,14 @@ def lib() -> ctypes.CDLL:
     L.bfp8_cast_e4m3.argtypes = [vp, i64, vp, vp]
     L.bfp8_check_device_errors.argtypes = [vp]
     L.bfp8_debug_write_counts.argtypes = [i32, i64, i64, i64, i32, vp, vp, ctypes.POINTER(i64)]
+    L.bfp8_quant_dual.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp]
+    L.bfp8_linear_train_workspace_size.argtypes = [i64, i64, i64]
+    L.bfp8_linear_train_workspace_size.restype = sz
+    L.bfp8_linear_fwd_train.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
+    L.bfp8_linear_bwd_saved.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
+    L.bfp8_debug_gemm_stall.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, i64, i64, vp]
     for name in EXPORTS:
-        if name not in ("bfp8_last_error", "bfp8_linear_workspace_size"):
+        if name not in ("bfp8_last_error", "bfp8_linear_workspace_size", "bfp8_linear_train_workspace_size"):
             getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -159,6 +166,27 @@ def quant_weight(w, with_q: bool = True, with_t: bool = False, q=None, qt=None, 
     return q, qt, s
 
 
+def quant_dual(x, q_row=None, s_row=None, q_col=None, s_col=None):
+    """Both quantisations of x [T,C] from one read: (q_row [T, ldq], s_row
+    [Cb, lds] as quant_lhs(x)) and (q_col [C, ldq'], s_col [Tb, lds'] as
+    quant_rhs(x))."""
+    torch = _torch()
+    _need_bf16_2d(x, "x")
+    T, C = x.shape
+    dev = x.device
+    if q_row is None:
+        q_row = torch.empty((T, _rup(max(C, 1), 16)), dtype=torch.uint8, device=dev)
+    if s_row is None:
+        s_row = torch.empty((_cdiv(C, BLOCK), _rup(max(T, 1), 4)), dtype=torch.float32, device=dev)
+    if q_col is None:
+        q_col = torch.empty((C, _rup(max(T, 1), 16)), dtype=torch.uint8, device=dev)
+    if s_col is None:
+        s_col = torch.empty((_cdiv(T, BLOCK), _rup(max(C, 1), 4)), dtype=torch.float32, device=dev)
+    _check(lib().bfp8_quant_dual(_p(x), T, C, x.stride(0), _p(q_row), q_row.stride(0), _p(s_row), s_row.stride(0),
+                                 _p(q_col), q_col.stride(0), _p(s_col), s_col.stride(0), _stream()))
+    return q_row, s_row, q_col, s_col
+
+
 def cast_e4m3(x, q=None):
     """Elementwise RNE fp32 -> e4m3fn with saturation to +-448."""
     torch = _torch()
@@ -247,6 +275,51 @@ def linear_bwd(dy, x, w, dx=None, dw=None, ws=None):
     return dx, dw
 
 
+def debug_gemm_stall(qa, sa, qb, sb, K: int, out, wait_limit_us: int = 50000):
+    """Test hook: a GEMM launch whose promotion warps wait on a barrier nothing
+    arrives on; returns the launch status (the timeout itself is reported by
+    check_device_errors())."""
+    M, N = out.shape
+    return lib().bfp8_debug_gemm_stall(_p(qa), qa.stride(0), _p(sa), sa.stride(0), _p(qb), qb.stride(0),
+                                       _p(sb), sb.stride(0), _p(out), out.stride(0), M, N, K,
+                                       wait_limit_us, _stream())
+
+
+def linear_train_workspace(M: int, N: int, K: int, device="cuda"):
+    torch = _torch()
+    return torch.empty(int(lib().bfp8_linear_train_workspace_size(M, N, K)) + 256, dtype=torch.uint8, device=device)
+
+
+def _aligned(ws):
+    off = (-ws.data_ptr()) % 256
+    return ctypes.c_void_p(ws.data_ptr() + off), ws.numel() - off
+
+
+def linear_fwd_train(x, w, ws, y=None):
+    """Training forward: y = x W^T, keeping in `ws` the quantised operands the
+    backward needs (see bfp8_linear_fwd_train)."""
+    torch = _torch()
+    M, K = x.shape
+    N = w.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    wp, wn = _aligned(ws)
+    _check(lib().bfp8_linear_fwd_train(_p(x), _p(w), _p(y), M, N, K, wp, wn, _stream()))
+    return y
+
+
+def linear_bwd_saved(dy, ws, M: int, N: int, K: int, dx=None, dw=None):
+    """Backward from the workspace a linear_fwd_train call filled."""
+    torch = _torch()
+    if dx is None:
+        dx = torch.empty((M, K), dtype=torch.bfloat16, device=dy.device)
+    if dw is None:
+        dw = torch.empty((N, K), dtype=torch.bfloat16, device=dy.device)
+    wp, wn = _aligned(ws)
+    _check(lib().bfp8_linear_bwd_saved(_p(dy), _p(dx), _p(dw), M, N, K, wp, wn, _stream()))
+    return dx, dw
+
+
 def check_device_errors() -> None:
     """Synchronises the current stream; raises if a GEMM gave up on a bounded wait."""
     _check(lib().bfp8_check_device_errors(_stream()))
@@ -259,12 +332,11 @@ def check_device_errors() -> None:
 def debug_write_counts(kind: int, M: int, N: int, K: int, flag: int = 0):
     """Per-element write counts a launch would produce.  Returns
     (counts [rows, cols], scale_counts or None, out_of_range_writes)."""
-    shapes = {0: ((K, M) if flag else (M, K)), 1: (N, K), 2: (N, K), 3: (M, N), 4: (K, N)}
+    shapes = {0: (M, K), 1: (N, K), 2: (N, K), 3: (M, N), 4: (K, N), 5: (M, K), 6: (K, M)}
     rows, cols = shapes[kind]
-    if kind == 0 and flag:
-        rows, cols = M, K
     counts = np.zeros((rows, cols), dtype=np.uint32)
-    sshape = {0: (_cdiv(K, BLOCK), M), 1: (_cdiv(K, BLOCK), N), 2: (_cdiv(N, BLOCK), _cdiv(K, BLOCK))}.get(kind)
+    sshape = {0: (_cdiv(K, BLOCK), M), 1: (_cdiv(K, BLOCK), N), 2: (_cdiv(N, BLOCK), _cdiv(K, BLOCK)),
+              5: (_cdiv(K, BLOCK), M), 6: (_cdiv(M, BLOCK), K)}.get(kind)
     scounts = np.zeros(sshape, dtype=np.uint32) if sshape else None
     oob = ctypes.c_int64(0)
     _check(lib().bfp8_debug_write_counts(kind, M, N, K, flag, counts.ctypes.data_as(ctypes.c_void_p),

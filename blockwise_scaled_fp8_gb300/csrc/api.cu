@@ -98,10 +98,19 @@ bfp8_status bfp8_quant_lhs(const void* x, int64_t M, int64_t K, int64_t ldx, int
   int sms = 0;
   if ((st = check_device(&sms)) != BFP8_OK) return st;
   cudaError_t e;
-  if (x_transposed)
-    e = launch_quant_cols((const uint16_t*)x, K, M, ldx, (uint8_t*)q, ldq, s, lds, (cudaStream_t)stream);
-  else
-    e = launch_quant_rows((const uint16_t*)x, M, K, ldx, (uint8_t*)q, ldq, s, lds, sms, (cudaStream_t)stream);
+  const uint16_t* xb = (const uint16_t*)x;
+  if (quant_tile_supported(x, ldx)) {
+    if (x_transposed)  // x is [K, M]: 128x1 groups of x along K are 1x128 groups of A = x^T
+      e = launch_quant_tile(kQuantTileCol, xb, K, M, ldx, nullptr, 0, nullptr, 0, (uint8_t*)q, ldq, s, lds, sms,
+                            (cudaStream_t)stream);
+    else
+      e = launch_quant_tile(kQuantTileRow, xb, M, K, ldx, (uint8_t*)q, ldq, s, lds, nullptr, 0, nullptr, 0, sms,
+                            (cudaStream_t)stream);
+  } else if (x_transposed) {
+    e = launch_quant_cols(xb, K, M, ldx, (uint8_t*)q, ldq, s, lds, (cudaStream_t)stream);
+  } else {
+    e = launch_quant_rows(xb, M, K, ldx, (uint8_t*)q, ldq, s, lds, sms, (cudaStream_t)stream);
+  }
   return e == cudaSuccess ? BFP8_OK : cuda_fail(e, "bfp8_quant_lhs launch");
 }
 
@@ -118,7 +127,12 @@ bfp8_status bfp8_quant_rhs(const void* x, int64_t K, int64_t N, int64_t ldx, voi
   CHECK_ARG(lds >= N, "bfp8_quant_rhs: lds=%lld < N=%lld", (long long)lds, (long long)N);
   int sms = 0;
   if ((st = check_device(&sms)) != BFP8_OK) return st;
-  cudaError_t e = launch_quant_cols((const uint16_t*)x, K, N, ldx, (uint8_t*)qT, ldq, s, lds, (cudaStream_t)stream);
+  cudaError_t e;
+  if (quant_tile_supported(x, ldx))
+    e = launch_quant_tile(kQuantTileCol, (const uint16_t*)x, K, N, ldx, nullptr, 0, nullptr, 0, (uint8_t*)qT, ldq, s,
+                          lds, sms, (cudaStream_t)stream);
+  else
+    e = launch_quant_cols((const uint16_t*)x, K, N, ldx, (uint8_t*)qT, ldq, s, lds, (cudaStream_t)stream);
   return e == cudaSuccess ? BFP8_OK : cuda_fail(e, "bfp8_quant_rhs launch");
 }
 
@@ -144,12 +158,49 @@ bfp8_status bfp8_quant_weight(const void* w, int64_t N, int64_t K, int64_t ldw, 
             (long long)cdiv(K, kBlock));
   int sms = 0;
   if ((st = check_device(&sms)) != BFP8_OK) return st;
-  cudaError_t e = launch_quant_weight((const uint16_t*)w, N, K, ldw, (uint8_t*)q, ldq, (uint8_t*)qt, ldqt, s, lds,
-                                      (cudaStream_t)stream);
+  cudaError_t e;
+  if (quant_tile_supported(w, ldw))
+    e = launch_quant_tile(kQuantTileScale, (const uint16_t*)w, N, K, ldw, (uint8_t*)q, ldq, s, lds, (uint8_t*)qt,
+                          ldqt, nullptr, 0, sms, (cudaStream_t)stream);
+  else
+    e = launch_quant_weight((const uint16_t*)w, N, K, ldw, (uint8_t*)q, ldq, (uint8_t*)qt, ldqt, s, lds,
+                            (cudaStream_t)stream);
   return e == cudaSuccess ? BFP8_OK : cuda_fail(e, "bfp8_quant_weight launch");
 }
 
-static bfp8_status gemm_common(const char* fn, const GemmArgs& a, bfp8_stream_t stream) {
+bfp8_status bfp8_quant_dual(const void* x, int64_t T, int64_t C, int64_t ldx, void* q_row, int64_t ldq_row,
+                            float* s_row, int64_t lds_row, void* q_col, int64_t ldq_col, float* s_col,
+                            int64_t lds_col, bfp8_stream_t stream) {
+  bfp8_status st = check_dims("bfp8_quant_dual", T, C);
+  if (st != BFP8_OK) return st;
+  if (T == 0 || C == 0) return BFP8_OK;
+  CHECK_ARG(x && q_row && s_row && q_col && s_col, "bfp8_quant_dual: null pointer");
+  CHECK_ARG(al2(x) && al16(q_row) && al16(q_col) && al4(s_row) && al4(s_col),
+            "bfp8_quant_dual: x must be 2-byte, q_row/q_col 16-byte, scales 4-byte aligned");
+  CHECK_ARG(ldx >= C, "bfp8_quant_dual: ldx=%lld < C=%lld", (long long)ldx, (long long)C);
+  CHECK_ARG(ldq_row >= C && ldq_row % 16 == 0, "bfp8_quant_dual: ldq_row=%lld must be >= C and a multiple of 16",
+            (long long)ldq_row);
+  CHECK_ARG(ldq_col >= T && ldq_col % 16 == 0, "bfp8_quant_dual: ldq_col=%lld must be >= T and a multiple of 16",
+            (long long)ldq_col);
+  CHECK_ARG(lds_row >= T, "bfp8_quant_dual: lds_row=%lld < T=%lld", (long long)lds_row, (long long)T);
+  CHECK_ARG(lds_col >= C, "bfp8_quant_dual: lds_col=%lld < C=%lld", (long long)lds_col, (long long)C);
+  int sms = 0;
+  if ((st = check_device(&sms)) != BFP8_OK) return st;
+  cudaError_t e;
+  const uint16_t* xb = (const uint16_t*)x;
+  if (quant_tile_supported(x, ldx)) {
+    e = launch_quant_tile(kQuantTileRow | kQuantTileCol, xb, T, C, ldx, (uint8_t*)q_row, ldq_row, s_row, lds_row,
+                          (uint8_t*)q_col, ldq_col, s_col, lds_col, sms, (cudaStream_t)stream);
+  } else {
+    e = launch_quant_rows(xb, T, C, ldx, (uint8_t*)q_row, ldq_row, s_row, lds_row, sms, (cudaStream_t)stream);
+    if (e == cudaSuccess)
+      e = launch_quant_cols(xb, T, C, ldx, (uint8_t*)q_col, ldq_col, s_col, lds_col, (cudaStream_t)stream);
+  }
+  return e == cudaSuccess ? BFP8_OK : cuda_fail(e, "bfp8_quant_dual launch");
+}
+
+static bfp8_status gemm_common(const char* fn, const GemmArgs& a, bfp8_stream_t stream,
+                               uint64_t wait_limit_ns = kWaitLimitNs, int debug_stall = 0) {
   bfp8_status st = check_dims(fn, a.M, a.N, a.K);
   if (st != BFP8_OK) return st;
   if (a.M == 0 || a.N == 0) return BFP8_OK;
@@ -178,7 +229,7 @@ static bfp8_status gemm_common(const char* fn, const GemmArgs& a, bfp8_stream_t 
   int sms = 0;
   if ((st = check_device(&sms)) != BFP8_OK) return st;
   const char* msg = nullptr;
-  cudaError_t e = launch_gemm(a, sms, (cudaStream_t)stream, &msg);
+  cudaError_t e = launch_gemm(a, sms, (cudaStream_t)stream, &msg, wait_limit_ns, debug_stall);
   if (e != cudaSuccess) {
     if (msg) return fail(BFP8_ERR_INVALID_ARG, "%s: %s", fn, msg);
     return cuda_fail(e, fn);
@@ -200,6 +251,15 @@ bfp8_status bfp8_gemm_1x128_128x1(const void* qa, int64_t lda, const float* sa, 
   return gemm_common("bfp8_gemm_1x128_128x1", a, stream);
 }
 
+bfp8_status bfp8_debug_gemm_stall(const void* qa, int64_t lda, const float* sa, int64_t ldsa, const void* qb,
+                                  int64_t ldb, const float* sb, int64_t ldsb, void* c, int64_t ldc, int64_t M,
+                                  int64_t N, int64_t K, int64_t wait_limit_us, bfp8_stream_t stream) {
+  CHECK_ARG(wait_limit_us > 0 && wait_limit_us <= 2000000, "bfp8_debug_gemm_stall: wait limit must be in (0, 2 s]");
+  CHECK_ARG(M > 0 && N > 0 && K > 0, "bfp8_debug_gemm_stall: needs a non-empty problem");
+  GemmArgs a{qa, lda, sa, ldsa, qb, ldb, sb, ldsb, kSbTile, c, ldc, M, N, K};
+  return gemm_common("bfp8_debug_gemm_stall", a, stream, (uint64_t)wait_limit_us * 1000ull, 1);
+}
+
 bfp8_status bfp8_cast_e4m3(const float* x, int64_t n, void* q, bfp8_stream_t stream) {
   CHECK_ARG(n >= 0, "bfp8_cast_e4m3: negative size");
   if (n == 0) return BFP8_OK;
@@ -215,9 +275,12 @@ bfp8_status bfp8_cast_e4m3(const float* x, int64_t n, void* q, bfp8_stream_t str
 bfp8_status bfp8_check_device_errors(bfp8_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "bfp8_check_device_errors: stream synchronize");
-  uint32_t bits = 0;
+  uint32_t bits = 0, qbits = 0;
   e = gemm_read_errors(&bits);
   if (e != cudaSuccess) return cuda_fail(e, "bfp8_check_device_errors: read flag");
+  e = quant_read_errors(&qbits);
+  if (e != cudaSuccess) return cuda_fail(e, "bfp8_check_device_errors: read flag");
+  if (qbits) return fail(BFP8_ERR_TIMEOUT, "quantisation kernel gave up waiting for its TMA tile loads");
   if (bits) {
     return fail(BFP8_ERR_TIMEOUT,
                 "GEMM kernel gave up on a bounded wait (flags 0x%x: %s%s%s%s%s)", bits,
@@ -350,15 +413,100 @@ bfp8_status bfp8_linear_bwd(const void* dy, const void* x, const void* w, void* 
 }
 
 // ---------------------------------------------------------------------------
+// Linear layer, training form: the forward keeps what the backward needs
+// ---------------------------------------------------------------------------
+
+namespace {
+struct TrainLayout {
+  size_t qx, sx, qxt, sxt, qw, qwt, sw, qdy, sdy, qdyt, sdyt, total;
+  int64_t ldK, ldN, ldM, ldsM, ldsN, ldsK;
+};
+TrainLayout train_layout(int64_t M, int64_t N, int64_t K) {
+  TrainLayout L;
+  L.ldK = rup(K, 16);
+  L.ldN = rup(N, 16);
+  L.ldM = rup(M, 16);
+  L.ldsM = rup(M, 4);
+  L.ldsN = rup(N, 4);
+  L.ldsK = rup(K, 4);
+  const int64_t Kb = cdiv(K, kBlock), Nb = cdiv(N, kBlock), Mb = cdiv(M, kBlock);
+  size_t o = 0;
+  L.qx = o; o = a256(o + (size_t)M * L.ldK);            // x, 1x128 along K (forward lhs)
+  L.sx = o; o = a256(o + (size_t)Kb * L.ldsM * 4);
+  L.qxt = o; o = a256(o + (size_t)K * L.ldM);           // x, 128x1 along M, transposed (wgrad rhs)
+  L.sxt = o; o = a256(o + (size_t)Mb * L.ldsK * 4);
+  L.qw = o; o = a256(o + (size_t)N * L.ldK);            // W tiles (forward rhs)
+  L.qwt = o; o = a256(o + (size_t)K * L.ldN);           // W tiles transposed (dgrad rhs)
+  L.sw = o; o = a256(o + (size_t)Nb * Kb * 4);
+  L.qdy = o; o = a256(o + (size_t)M * L.ldN);           // dY, 1x128 along N (dgrad lhs)
+  L.sdy = o; o = a256(o + (size_t)Nb * L.ldsM * 4);
+  L.qdyt = o; o = a256(o + (size_t)N * L.ldM);          // dY^T, 1x128 along M (wgrad lhs)
+  L.sdyt = o; o = a256(o + (size_t)Mb * L.ldsN * 4);
+  L.total = o;
+  return L;
+}
+}  // namespace
+
+size_t bfp8_linear_train_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  return train_layout(M, N, K).total;
+}
+
+bfp8_status bfp8_linear_fwd_train(const void* x, const void* w, void* y, int64_t M, int64_t N, int64_t K, void* ws,
+                                  size_t ws_bytes, bfp8_stream_t stream) {
+  bfp8_status st = check_dims("bfp8_linear_fwd_train", M, N, K);
+  if (st != BFP8_OK) return st;
+  CHECK_ARG(M > 0 && N > 0 && K > 0, "bfp8_linear_fwd_train: dimensions must be positive");
+  CHECK_ARG(x && w && y && ws, "bfp8_linear_fwd_train: null pointer");
+  CHECK_ARG((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "bfp8_linear_fwd_train: workspace must be 256-byte aligned");
+  const TrainLayout L = train_layout(M, N, K);
+  CHECK_ARG(ws_bytes >= L.total, "bfp8_linear_fwd_train: workspace too small (%zu < %zu)", ws_bytes, L.total);
+  uint8_t* b = (uint8_t*)ws;
+  const int64_t Kb = cdiv(K, kBlock);
+  // one read of x: its 1x128 groups (forward) and its 128x1 groups along M (weight gradient)
+  if ((st = bfp8_quant_dual(x, M, K, K, b + L.qx, L.ldK, (float*)(b + L.sx), L.ldsM, b + L.qxt, L.ldM,
+                            (float*)(b + L.sxt), L.ldsK, stream)) != BFP8_OK)
+    return st;
+  // one read of W: its 128x128 tiles, as is (forward) and transposed (input gradient)
+  if ((st = bfp8_quant_weight(w, N, K, K, b + L.qw, L.ldK, b + L.qwt, L.ldN, (float*)(b + L.sw), Kb, stream)) !=
+      BFP8_OK)
+    return st;
+  return bfp8_gemm_1x128_128x128(b + L.qx, L.ldK, (const float*)(b + L.sx), L.ldsM, b + L.qw, L.ldK,
+                                 (const float*)(b + L.sw), Kb, 0, y, N, M, N, K, stream);
+}
+
+bfp8_status bfp8_linear_bwd_saved(const void* dy, void* dx, void* dw, int64_t M, int64_t N, int64_t K, void* ws,
+                                  size_t ws_bytes, bfp8_stream_t stream) {
+  bfp8_status st = check_dims("bfp8_linear_bwd_saved", M, N, K);
+  if (st != BFP8_OK) return st;
+  CHECK_ARG(M > 0 && N > 0 && K > 0, "bfp8_linear_bwd_saved: dimensions must be positive");
+  CHECK_ARG(dy && dx && dw && ws, "bfp8_linear_bwd_saved: null pointer");
+  CHECK_ARG((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "bfp8_linear_bwd_saved: workspace must be 256-byte aligned");
+  const TrainLayout L = train_layout(M, N, K);
+  CHECK_ARG(ws_bytes >= L.total, "bfp8_linear_bwd_saved: workspace too small (%zu < %zu)", ws_bytes, L.total);
+  uint8_t* b = (uint8_t*)ws;
+  const int64_t Kb = cdiv(K, kBlock);
+  // one read of dY: 1x128 along N (input gradient) and 1x128 along M of dY^T (weight gradient)
+  if ((st = bfp8_quant_dual(dy, M, N, N, b + L.qdy, L.ldN, (float*)(b + L.sdy), L.ldsM, b + L.qdyt, L.ldM,
+                            (float*)(b + L.sdyt), L.ldsN, stream)) != BFP8_OK)
+    return st;
+  if ((st = bfp8_gemm_1x128_128x128(b + L.qdy, L.ldN, (const float*)(b + L.sdy), L.ldsM, b + L.qwt, L.ldN,
+                                    (const float*)(b + L.sw), Kb, 1, dx, K, M, K, N, stream)) != BFP8_OK)
+    return st;
+  return bfp8_gemm_1x128_128x1(b + L.qdyt, L.ldM, (const float*)(b + L.sdyt), L.ldsN, b + L.qxt, L.ldM,
+                               (const float*)(b + L.sxt), L.ldsK, dw, K, N, K, M, stream);
+}
+
+// ---------------------------------------------------------------------------
 // Host replay of the kernels' index arithmetic
 // ---------------------------------------------------------------------------
 
-bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, int flag, uint32_t* counts,
-                                    uint32_t* scale_counts, int64_t* oob) {
-  CHECK_ARG(counts && oob, "bfp8_debug_write_counts: null pointer");
-  CHECK_ARG(M >= 0 && N >= 0 && K >= 0, "bfp8_debug_write_counts: negative size");
-  const int sms = 152;  // GB300
-  *oob = 0;
+namespace {
+// Replays the stores of the TMA-staged tile kernel over a [T, C] input.
+// rows_out: q_row [T, C]; cols_out: q_col [C, T]; scale_kind: 0 none,
+// 1 row scales [Cb, T], 2 column scales [Tb, C], 3 tile scales [Tb, Cb].
+void replay_tile(int64_t T, int64_t C, bool rows_out, bool cols_out, int scale_kind, uint32_t* counts,
+                 uint32_t* scounts, int64_t* oob, int sms) {
   auto hit = [&](uint32_t* arr, int64_t r, int64_t c, int64_t rows, int64_t cols) {
     if (r < 0 || r >= rows || c < 0 || c >= cols) {
       ++*oob;
@@ -366,7 +514,71 @@ bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, i
     }
     if (arr) arr[r * cols + c]++;
   };
-  if (kind == 0 && !flag) {  // quant_lhs, row-major input [M,K]
+  const int64_t tiles_c = cdiv(C, 128), num_tiles = cdiv(T, 128) * tiles_c;
+  const int64_t grid = qt_grid(num_tiles, sms), Tb = cdiv(T, 128), Cb = cdiv(C, 128);
+  for (int64_t cta = 0; cta < grid; ++cta)
+    for (int64_t tile = cta; tile < num_tiles; tile += grid) {
+      const int64_t t0 = qt_tile_t0(tile, tiles_c), c0 = qt_tile_c0(tile, tiles_c);
+      if (rows_out || scale_kind == 1)
+        for (int warp = 0; warp < kQtThreads / 32; ++warp)
+          for (int half = 0; half < 2; ++half)
+            for (int l16 = 0; l16 < 16; ++l16)
+              for (int ps = 0; ps < 8; ++ps) {
+                const int64_t t = t0 + qt_rowpass_row(ps, warp, half), c = c0 + qt_rowpass_col(l16);
+                if (t >= T) continue;
+                if (rows_out)
+                  for (int b = 0; b < 8; ++b)
+                    if (c + b < C) hit(counts, t, c + b, T, C);
+                if (scale_kind == 1 && l16 == 0) hit(scounts, c0 / 128, t, Cb, T);
+              }
+      if (cols_out)
+        for (int ch = 0; ch < 128 * 128 / 16; ++ch) {
+          const int64_t cg = c0 + qt_store_col(ch), tg = t0 + qt_store_row(ch);
+          if (cg < C)
+            for (int b = 0; b < 16; ++b)
+              if (tg + b < T) hit(counts, cg, tg + b, C, T);
+        }
+      if (scale_kind == 2)
+        for (int warp = 0; warp < kQtThreads / 32; ++warp)
+          for (int h = 0; h < 2; ++h)
+            for (int lane = 0; lane < 8; ++lane) {
+              const int64_t cg = c0 + 8 * qt_colpass_chunk(warp, h) + lane;
+              if (cg < C) hit(scounts, t0 / 128, cg, Tb, C);
+            }
+      if (scale_kind == 3) hit(scounts, t0 / 128, c0 / 128, Tb, Cb);
+    }
+}
+}  // namespace
+
+bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, int flag, uint32_t* counts,
+                                    uint32_t* scale_counts, int64_t* oob) {
+  CHECK_ARG(counts && oob, "bfp8_debug_write_counts: null pointer");
+  CHECK_ARG(M >= 0 && N >= 0 && K >= 0, "bfp8_debug_write_counts: negative size");
+  const int sms = 152;  // GB300
+  *oob = 0;
+  const bool plain = (flag & 2) != 0;  // replay the untiled fallback kernels instead of the TMA-staged one
+  if (!plain) {
+    switch (kind) {
+      case 0:
+        if (flag & 1) replay_tile(K, M, false, true, 2, counts, scale_counts, oob, sms);   // x is [K, M]
+        else replay_tile(M, K, true, false, 1, counts, scale_counts, oob, sms);
+        return BFP8_OK;
+      case 1: replay_tile(K, N, false, true, 2, counts, scale_counts, oob, sms); return BFP8_OK;
+      case 2: replay_tile(N, K, true, false, 3, counts, scale_counts, oob, sms); return BFP8_OK;
+      case 4: replay_tile(N, K, false, true, 0, counts, nullptr, oob, sms); return BFP8_OK;
+      case 5: replay_tile(M, K, true, false, 1, counts, scale_counts, oob, sms); return BFP8_OK;
+      case 6: replay_tile(M, K, false, true, 2, counts, scale_counts, oob, sms); return BFP8_OK;
+      default: break;
+    }
+  }
+  auto hit = [&](uint32_t* arr, int64_t r, int64_t c, int64_t rows, int64_t cols) {
+    if (r < 0 || r >= rows || c < 0 || c >= cols) {
+      ++*oob;
+      return;
+    }
+    if (arr) arr[r * cols + c]++;
+  };
+  if (kind == 0 && !(flag & 1)) {  // quant_lhs, row-major input [M,K]
     const int64_t Kb = cdiv(K, kBlock), groups = M * Kb;
     if (groups == 0) return BFP8_OK;
     const int64_t grid = quant_rows_grid(M, K, sms);
@@ -386,7 +598,7 @@ bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, i
         }
     return BFP8_OK;
   }
-  if ((kind == 0 && flag) || kind == 1) {  // transposed-read groups: T = grouped dim, C = columns
+  if ((kind == 0 && (flag & 1)) || kind == 1) {  // transposed-read groups: T = grouped dim, C = columns
     // kind 0 (x is [K,M]): T = K, C = M, logical q [M,K].  kind 1 (x is [K,N]): T = K, C = N, qT [N,K].
     const int64_t T = K, C = (kind == 0) ? M : N;
     const int64_t grid = cdiv(T, kColTileT) * cdiv(C, kColTileC);

@@ -20,8 +20,24 @@ __device__ __forceinline__ float group_scale(float amax) {
   return __fdiv_rn(fmaxf(amax, kAmaxFloor), kE4m3Max);
 }
 
-// x / s, one IEEE division rounded to nearest even.
-__device__ __forceinline__ float quotient(float x, float s) { return __fdiv_rn(x, s); }
+// 1/s rounded to nearest even (once per group).
+__device__ __forceinline__ float recip_rn(float s) { return __frcp_rn(s); }
+
+// x / s rounded to nearest even, from y = RN(1/s), by Markstein's correction
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990): q0 = RN(x*y);
+// r = x - s*q (exact with an FMA); q' = RN(q + r*y).  One correction makes q
+// faithful, and from a faithful q the next correction returns RN(x/s) when no
+// intermediate underflows.  Here s >= 1e-12/448 and |x| <= 448 s, so the
+// remainders are normal whenever |x/s| >= 2^-11; smaller quotients can differ
+// from the IEEE quotient by a few ulps but round to the same e4m3 code (+-0).
+__device__ __forceinline__ float quotient(float x, float s, float y) {
+  const float q0 = __fmul_rn(x, y);
+  const float r0 = __fmaf_rn(-s, q0, x);
+  const float q1 = __fmaf_rn(r0, y, q0);
+  const float r1 = __fmaf_rn(-s, q1, x);
+  return __fmaf_rn(r1, y, q1);
+}
 
 // Two fp32 values -> two e4m3fn bytes, RNE, saturating to +-448 (the clamp of
 // the method).  Result byte 0 = lo, byte 1 = hi.
@@ -210,7 +226,9 @@ __device__ __forceinline__ void tmem_ld_wait() {
 
 // Packed fp32x2 arithmetic (one instruction for two lanes of work).
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
-  return ((uint64_t)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
 }
 __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;

@@ -55,6 +55,7 @@ struct GemmParams {
   int c_vec;   // 16-byte output stores allowed (ldc % 8 == 0, c 16-byte aligned)
   int sb_vec;  // 16-byte column-scale loads allowed (ldsb % 4 == 0, sb 16-byte aligned)
   uint64_t wait_limit_ns;
+  int debug_stall;  // test hook: the promotion warps wait on a barrier nothing arrives on
 };
 
 template <int BN, int STAGES>
@@ -74,7 +75,7 @@ struct GemmCfg {
   static constexpr int kOffB = STAGES * kABytes;
   static constexpr int kOffSb = kOffB + STAGES * kBBytes;
   static constexpr int kOffBar = kOffSb + kEpiWarps * 128 * 4;
-  static constexpr int kNumBars = 2 * STAGES + 5;
+  static constexpr int kNumBars = 2 * STAGES + 6;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -104,12 +105,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
   volatile int* never = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
 
-  // barrier addresses: full[S], empty[S], tfull[2], tempty[2], drain
+  // barrier addresses: full[S], empty[S], tfull[2], tempty[2], drain, stall
   auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(STAGES + i); };
   auto tfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + i); };
   auto tempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + 2 + i); };
   const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
+  const uint32_t stall_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 5);  // never arrived on
 
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const int lane = (int)(threadIdx.x & 31);
@@ -124,6 +126,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
       mbar_init(tempty_bar(i), Cfg::kEpiWarps);
     }
     mbar_init(drain_bar, 1);
+    mbar_init(stall_bar, 1);
     *abort_flag = 0;
     *never = 0;
     fence_barrier_init();
@@ -265,7 +268,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
         }
         const int buf = (int)(it & 1);
         const uint32_t tph = (uint32_t)((it >> 1) & 1);
-        const bool got = mbar_wait_bounded(tfull_bar(buf), tph, p.wait_limit_ns, abort_flag);
+        const bool got = mbar_wait_bounded(p.debug_stall ? stall_bar : tfull_bar(buf), tph, p.wait_limit_ns,
+                                           abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
           if (lane == 0) gemm_fail(kErrWaitTmemFull, abort_flag);
           ok = false;
@@ -391,7 +395,8 @@ static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const 
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const char** msg) {
+cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const char** msg,
+                        uint64_t wait_limit_ns, int debug_stall) {
   const int bn = gemm_pick_bn(a.M, a.N, num_sms);
   CUtensorMap ma, mb;
   if (!make_tma_u8(&ma, a.qa, a.K, a.M, a.lda, kBM) || !make_tma_u8(&mb, a.qb, a.K, a.N, a.ldb, bn)) {
@@ -415,7 +420,8 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const c
   p.Nb = cdiv(a.N, kBlock);
   p.c_vec = (a.ldc % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.c) & 15u) == 0);
   p.sb_vec = (a.ldsb % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.sb) & 15u) == 0);
-  p.wait_limit_ns = 4000000000ull;  // 4 s per wait: far above any legitimate stall
+  p.wait_limit_ns = wait_limit_ns;
+  p.debug_stall = debug_stall;
   const int64_t grid = gemm_grid(a.M, a.N, bn, num_sms);
   if (bn == 256) {
     switch (a.sb_mode) {

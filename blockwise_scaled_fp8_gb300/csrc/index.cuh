@@ -90,6 +90,31 @@ BFP8_HD int64_t w_tstore_k(const WTile& t, int ch) { return t.kb * kBlock + ch /
 BFP8_HD int64_t w_tstore_n(const WTile& t, int ch) { return t.nb * kBlock + (ch % 8) * 16; }
 
 // ---------------------------------------------------------------------------
+// TMA-staged tile quantisation: persistent CTAs (two per SM) over 128x128
+// tiles of a [T, C] input, tile index = blockIdx.x + k * gridDim.x, walked
+// C-fastest.  Row pass: 16 threads per tile row, thread lane16 owns columns
+// 8*lane16..+7, pass ps of warp w covers row 16*ps + 2*w + half.  Column pass:
+// warp w owns 8-column chunks w and w+8, lane l owns rows l + 32*i.  The
+// transposed tile is stored as 16-byte chunks: chunk ch -> column ch/8,
+// rows 16*(ch%8)..+15.
+// ---------------------------------------------------------------------------
+constexpr int kQtThreads = 256;
+constexpr int kQtCtasPerSm = 2;
+
+BFP8_HD int64_t qt_grid(int64_t num_tiles, int num_sms) {
+  const int64_t cap = (int64_t)kQtCtasPerSm * num_sms;
+  return num_tiles < cap ? num_tiles : cap;
+}
+BFP8_HD int64_t qt_tile_t0(int64_t tile, int64_t tiles_c) { return (tile / tiles_c) * 128; }
+BFP8_HD int64_t qt_tile_c0(int64_t tile, int64_t tiles_c) { return (tile % tiles_c) * 128; }
+BFP8_HD int qt_rowpass_row(int ps, int warp, int half) { return 16 * ps + 2 * warp + half; }
+BFP8_HD int qt_rowpass_col(int lane16) { return 8 * lane16; }
+BFP8_HD int qt_colpass_chunk(int warp, int h) { return warp + 8 * h; }
+BFP8_HD int qt_colpass_row(int lane, int i) { return lane + 32 * i; }
+BFP8_HD int qt_store_col(int ch) { return ch / 8; }
+BFP8_HD int qt_store_row(int ch) { return 16 * (ch % 8); }
+
+// ---------------------------------------------------------------------------
 // GEMM: persistent CTAs over BM x BN output tiles.
 // ---------------------------------------------------------------------------
 constexpr int kBM = 128;

@@ -6,6 +6,8 @@
 
 namespace bfp8 {
 
+constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s per wait: far above any legitimate stall
+
 cudaError_t launch_quant_rows(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
                               int64_t ldq, float* s, int64_t lds, int num_sms, cudaStream_t st);
 int64_t quant_rows_grid(int64_t M, int64_t K, int num_sms);
@@ -15,6 +17,14 @@ cudaError_t launch_quant_weight(const uint16_t* w, int64_t N, int64_t K, int64_t
                                 int64_t ldq, uint8_t* qt, int64_t ldqt, float* s, int64_t lds,
                                 cudaStream_t st);
 cudaError_t launch_cast(const float* x, int64_t n, uint8_t* q, int num_sms, cudaStream_t st);
+
+// TMA-staged tile quantisation (quant_tile.cu): which outputs one read makes.
+enum : int { kQuantTileRow = 1, kQuantTileCol = 2, kQuantTileScale = 4 };
+bool quant_tile_supported(const void* x, int64_t ldx);
+cudaError_t launch_quant_tile(int mode, const uint16_t* x, int64_t T, int64_t C, int64_t ldx, uint8_t* q_row,
+                              int64_t ldq_row, float* s_row, int64_t lds_row, uint8_t* q_col, int64_t ldq_col,
+                              float* s_col, int64_t lds_col, int num_sms, cudaStream_t st);
+cudaError_t quant_read_errors(uint32_t* out);
 
 enum SbMode : int { kSbTile = 0, kSbTileT = 1, kSbCol = 2 };
 
@@ -35,7 +45,8 @@ struct GemmArgs {
 
 // Returns cudaSuccess or the launch error; *msg gets a static description of
 // a host-side failure (tensor-map encoding) when the return is not success.
-cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const char** msg);
+cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const char** msg,
+                        uint64_t wait_limit_ns = kWaitLimitNs, int debug_stall = 0);
 // Tile width the launcher picks for an M x N output, and the grid it uses.
 int gemm_pick_bn(int64_t M, int64_t N, int num_sms);
 int64_t gemm_grid(int64_t M, int64_t N, int bn, int num_sms);

@@ -8,7 +8,8 @@
 // byte store and scale store is masked to the logical tensor.
 //
 // These kernels are HBM-bound (about 3 bytes moved per element): 16-byte
-// vector loads, packed-bf16 amax, warp-shuffle reductions, packed e4m3 stores.
+// vector loads, packed-bf16 amax, warp-shuffle reductions, one reciprocal per
+// group and a corrected product per element for x/s, packed e4m3 stores.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -69,12 +70,13 @@ __global__ void __launch_bounds__(kRowThreads) quant_rows_kernel(
       for (int off = 8; off >= 1; off >>= 1)
         amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
       const float sc = group_scale(amax);
+      const float rc = recip_rn(sc);
       uint32_t out[2];
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t w0 = v[u][2 * h], w1 = v[u][2 * h + 1];
-        out[h] = cvt_e4m3x2(quotient(bf16_lo(w0), sc), quotient(bf16_hi(w0), sc)) |
-                 (cvt_e4m3x2(quotient(bf16_lo(w1), sc), quotient(bf16_hi(w1), sc)) << 16);
+        out[h] = cvt_e4m3x2(quotient(bf16_lo(w0), sc, rc), quotient(bf16_hi(w0), sc, rc)) |
+                 (cvt_e4m3x2(quotient(bf16_lo(w1), sc, rc), quotient(bf16_hi(w1), sc, rc)) << 16);
       }
       if (gv[u]) {
         uint8_t* dst = q + mm[u] * ldq + kk[u];
@@ -131,12 +133,14 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) m2[p] = __vmaxu2(m2[p], __shfl_xor_sync(0xffffffffu, m2[p], off));
   }
-  float sc[8];
+  float sc[8], rc[8];
 #pragma unroll
   for (int p = 0; p < 4; ++p) {
     sc[2 * p] = group_scale(bf16_lo(m2[p]));
     sc[2 * p + 1] = group_scale(bf16_hi(m2[p]));
   }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) rc[j] = recip_rn(sc[j]);
   // quantise; one 32-bit word per column = the column's 4 rows, in row order
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -144,7 +148,7 @@ __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t w = v[i][j >> 1];
-      r[i] = quotient((j & 1) ? bf16_hi(w) : bf16_lo(w), sc[j]);
+      r[i] = quotient((j & 1) ? bf16_hi(w) : bf16_lo(w), sc[j], rc[j]);
     }
     tout[8 * warp + j][lane] = cvt_e4m3x2(r[0], r[1]) | (cvt_e4m3x2(r[2], r[3]) << 16);
   }
@@ -221,6 +225,7 @@ __global__ void __launch_bounds__(kWThreads) quant_weight_kernel(
 #pragma unroll
   for (int i = 1; i < kWThreads / 32; ++i) amax = fmaxf(amax, red[i]);
   const float sc = group_scale(amax);
+  const float rc = recip_rn(sc);
   if (threadIdx.x == 0) s[tile.nb * lds + tile.kb] = sc;
 
 #pragma unroll
@@ -233,8 +238,8 @@ __global__ void __launch_bounds__(kWThreads) quant_weight_kernel(
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const uint32_t a = v[cc][i][2 * h], b = v[cc][i][2 * h + 1];
-        row_words[i][h] = cvt_e4m3x2(quotient(bf16_lo(a), sc), quotient(bf16_hi(a), sc)) |
-                          (cvt_e4m3x2(quotient(bf16_lo(b), sc), quotient(bf16_hi(b), sc)) << 16);
+        row_words[i][h] = cvt_e4m3x2(quotient(bf16_lo(a), sc, rc), quotient(bf16_hi(a), sc, rc)) |
+                          (cvt_e4m3x2(quotient(bf16_lo(b), sc, rc), quotient(bf16_hi(b), sc, rc)) << 16);
       }
       const int64_t n = w_elem_n(tile, lane, i);
       if (q != nullptr && n < N) {

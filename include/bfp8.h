@@ -28,7 +28,8 @@
  * (nothing launched) on a violation; BFP8_ERR_UNSUPPORTED when the current
  * device is not sm_103; BFP8_ERR_CUDA when a launch fails.  bfp8_last_error()
  * returns a message for the calling thread's last failed call.  A zero-sized
- * problem (any of M, N, K == 0) launches nothing and returns BFP8_OK.
+ * problem launches nothing and returns BFP8_OK (a GEMM with K == 0 and a
+ * linear layer with an empty reduction write zeros into their outputs).
  * Inputs must be finite; results for Inf/NaN inputs are unspecified.
  */
 #ifndef BFP8_H_
@@ -111,6 +112,22 @@ BFP8_API bfp8_status bfp8_quant_weight(const void *w, int64_t N, int64_t K, int6
                               float *s, int64_t lds, bfp8_stream_t stream);
 
 /*
+ * Both 1x128 and 128x1 groups of one bf16 tensor X[T,C] from a single read:
+ *   q_row[t*ldq_row + c], s_row[(c/128)*lds_row + t]   — as bfp8_quant_lhs(X)
+ *   q_col[c*ldq_col + t], s_col[(t/128)*lds_col + c]   — as bfp8_quant_rhs(X),
+ *                                                        = bfp8_quant_lhs(X^T)
+ * Source: the same three quantisations of "Enable blockwise FP8 dense
+ * training kernels on ROCm" (correctness table); fusing them is this
+ * library's choice (a training step needs both forms of x and of dY).
+ *   x  device bf16 [T,C], ldx >= C;  q_row, q_col 16-byte aligned, ld % 16 == 0,
+ *   ldq_row >= C, ldq_col >= T, lds_row >= T, lds_col >= C.
+ */
+BFP8_API bfp8_status bfp8_quant_dual(const void *x, int64_t T, int64_t C, int64_t ldx,
+                                     void *q_row, int64_t ldq_row, float *s_row, int64_t lds_row,
+                                     void *q_col, int64_t ldq_col, float *s_col, int64_t lds_col,
+                                     bfp8_stream_t stream);
+
+/*
  * GEMM 1x128 x 128x128 (forward and input gradient).
  * Source: "Mask a_s/b_s scale loads in blockwise FP8 training GEMM kernels" —
  * Summary (triton_fp8_gemm_1x128_128x128_kernel, per-tile a_s/b_s) and Fix
@@ -168,6 +185,22 @@ BFP8_API bfp8_status bfp8_linear_bwd(const void *dy, const void *x, const void *
                             bfp8_stream_t stream);
 
 /*
+ * Training form of the linear layer: the forward quantises x once into both
+ * of its forms (1x128 along K for y = x W^T, 128x1 along M for dW) and W once
+ * into its tiles as is and transposed, keeping them in `ws`; the backward
+ * quantises dY once into both forms and runs dX = dY W and dW = dY^T x from
+ * what the forward kept.  `ws` (>= bfp8_linear_train_workspace_size(M,N,K)
+ * bytes, 256-byte aligned) must be the one the forward filled, unmodified,
+ * with the same M, N, K.  All tensors contiguous bf16: x [M,K], w [N,K],
+ * y [M,N], dy [M,N], dx [M,K], dw [N,K].
+ */
+BFP8_API size_t bfp8_linear_train_workspace_size(int64_t M, int64_t N, int64_t K);
+BFP8_API bfp8_status bfp8_linear_fwd_train(const void *x, const void *w, void *y, int64_t M, int64_t N,
+                                           int64_t K, void *ws, size_t ws_bytes, bfp8_stream_t stream);
+BFP8_API bfp8_status bfp8_linear_bwd_saved(const void *dy, void *dx, void *dw, int64_t M, int64_t N,
+                                           int64_t K, void *ws, size_t ws_bytes, bfp8_stream_t stream);
+
+/*
  * The method's rounding step on its own: q[i] = RNE_e4m3fn(x[i]) with
  * saturation to +-448 (the clamp).  x device fp32 [n], q device e4m3 [n].
  */
@@ -183,14 +216,33 @@ BFP8_API bfp8_status bfp8_cast_e4m3(const float *x, int64_t n, void *q, bfp8_str
 BFP8_API bfp8_status bfp8_check_device_errors(bfp8_stream_t stream);
 
 /*
+ * Test hook for failure detection (no counterpart on the pages): launches the
+ * 1x128 x 128x128 GEMM with the arguments of bfp8_gemm_1x128_128x128
+ * (sb not transposed) but makes its promotion warps wait on a barrier that
+ * nothing arrives on, with every wait bounded by wait_limit_us (<= 2 s).  The
+ * kernel must give up, record the timeout, release its resources and return;
+ * bfp8_check_device_errors then reports BFP8_ERR_TIMEOUT and the context stays
+ * usable.  C is left unwritten.
+ */
+BFP8_API bfp8_status bfp8_debug_gemm_stall(const void *qa, int64_t lda, const float *sa, int64_t ldsa,
+                                           const void *qb, int64_t ldb, const float *sb, int64_t ldsb,
+                                           void *c, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                           int64_t wait_limit_us, bfp8_stream_t stream);
+
+/*
  * Host-side replay of a kernel's index arithmetic (no GPU needed): counts how
  * many times each logical output element would be written by the kernel that
- * `kind` names, for the launch configuration the library would use.
- *   kind 0: bfp8_quant_lhs (rows = M, cols = K), x_transposed = flag
- *   kind 1: bfp8_quant_rhs as written (rows = N, cols = K of qT)
- *   kind 2: bfp8_quant_weight q        (rows = N, cols = K)
+ * `kind` names, for the launch configuration the library would use on a
+ * 152-SM GB300.  flag bit 0: x_transposed (kind 0); flag bit 1: replay the
+ * untiled fallback kernels (used when the input is not 16-byte aligned or its
+ * row stride is not a multiple of 8) instead of the TMA-staged tile kernel.
+ *   kind 0: bfp8_quant_lhs q           (rows = M, cols = K), scales [Kb, M]
+ *   kind 1: bfp8_quant_rhs qT          (rows = N, cols = K), scales [Kb, N]
+ *   kind 2: bfp8_quant_weight q        (rows = N, cols = K), scales [Nb, Kb]
  *   kind 3: GEMM output C              (rows = M, cols = N)
  *   kind 4: bfp8_quant_weight qt       (rows = K, cols = N)
+ *   kind 5: bfp8_quant_dual q_row      (rows = M, cols = K), scales [Kb, M]  (T = M, C = K)
+ *   kind 6: bfp8_quant_dual q_col      (rows = K, cols = M), scales [Mb, K]
  * counts is host uint32 [rows*cols] (incremented); *oob receives the number
  * of writes that would land outside the logical tensor.  Scale writes are
  * counted in scale_counts (host uint32 [scale_rows*scale_cols], may be NULL).

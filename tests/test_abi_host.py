@@ -102,21 +102,31 @@ SHAPES = [(1, 1, 1), (2, 512, 128), (4, 3584, 640), (130, 384, 256), (129, 130, 
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
-def test_quant_lhs_index_replay_exactly_once(M, N, K):
+@pytest.mark.parametrize("plain", [0, 2])
+def test_quant_lhs_index_replay_exactly_once(M, N, K, plain):
     for flag in (0, 1):
-        c, s, oob = B.debug_write_counts(0, M, N, K, flag)
+        c, s, oob = B.debug_write_counts(0, M, N, K, flag | plain)
         assert oob == 0 and c.shape == (M, K) and np.all(c == 1)
         assert np.all(s == 1)
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
-def test_quant_rhs_and_weight_index_replay_exactly_once(M, N, K):
-    c, s, oob = B.debug_write_counts(1, M, N, K)
+@pytest.mark.parametrize("plain", [0, 2])
+def test_quant_rhs_and_weight_index_replay_exactly_once(M, N, K, plain):
+    c, s, oob = B.debug_write_counts(1, M, N, K, plain)
     assert oob == 0 and np.all(c == 1) and np.all(s == 1)
-    c, s, oob = B.debug_write_counts(2, M, N, K)
+    c, s, oob = B.debug_write_counts(2, M, N, K, plain)
     assert oob == 0 and np.all(c == 1) and np.all(s == 1)
-    c, _, oob = B.debug_write_counts(4, M, N, K)
+    c, _, oob = B.debug_write_counts(4, M, N, K, plain)
     assert oob == 0 and c.shape == (K, N) and np.all(c == 1)
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_quant_dual_index_replay_exactly_once(M, N, K):
+    c, s, oob = B.debug_write_counts(5, M, N, K)
+    assert oob == 0 and c.shape == (M, K) and np.all(c == 1) and np.all(s == 1)
+    c, s, oob = B.debug_write_counts(6, M, N, K)
+    assert oob == 0 and c.shape == (K, M) and np.all(c == 1) and np.all(s == 1)
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES + [(4096, 4096, 128), (2048, 4096, 128), (16384, 1024, 128)])

@@ -203,6 +203,59 @@ def test_quant_adversarial_values_bit_exact(M, K):
     assert np.array_equal(f32_bits(sw.cpu().numpy()), f32_bits(sw_ref))
 
 
+def _padded_dev(x, pad):
+    """Device copy of x [R, C] whose row stride is C + pad (pad not a
+    multiple of 8 forces the untiled fallback kernels)."""
+    R, C = x.shape
+    buf = np.zeros((R, C + pad), dtype=np.uint16)
+    buf[:, :C] = x
+    return dev_bf16(buf)[:, :C]
+
+
+@pytest.mark.parametrize("M,K", [(130, 256), (300, 1000), (2048, 4096)])
+def test_quant_lhs_fallback_path_bit_exact(M, K):
+    """Row stride K+3: the TMA-staged kernel cannot read it; the untiled
+    kernels must give the same bytes."""
+    x = S.normal_bf16((M, K), 1.0, seed=M + 5 * K, outlier_frac=1e-3)
+    q, s = B.quant_lhs(_padded_dev(x, 3))
+    q_ref, s_ref = O.quant_lhs(x)
+    assert np.array_equal(q.cpu().numpy()[:, :K], q_ref)
+    assert np.array_equal(f32_bits(s.cpu().numpy()[:, :M]), f32_bits(s_ref))
+    qt, st = B.quant_lhs(_padded_dev(np.ascontiguousarray(x.T), 5), transposed=True)
+    assert np.array_equal(qt.cpu().numpy()[:, :K], q_ref)
+    assert np.array_equal(f32_bits(st.cpu().numpy()[:, :M]), f32_bits(s_ref))
+    w_q, w_qt, w_s = B.quant_weight(_padded_dev(x, 1), with_q=True, with_t=True)
+    wq_ref, wqt_ref, ws_ref = O.quant_weight(x, with_t=True)
+    assert np.array_equal(w_q.cpu().numpy()[:, :K], wq_ref)
+    assert np.array_equal(w_qt.cpu().numpy()[:, :M], wqt_ref)
+    assert np.array_equal(f32_bits(w_s.cpu().numpy()), f32_bits(ws_ref))
+
+
+DUAL_SHAPES = [(130, 256), (257, 300), (2048, 4096), (8, 1000), (1, 136), (4100, 64)]
+
+
+@pytest.mark.parametrize("T,C", DUAL_SHAPES)
+@pytest.mark.parametrize("pad", [0, 3])
+def test_quant_dual_bit_exact(T, C, pad):
+    """One read of X gives both its 1x128 groups (as quant_lhs) and its 128x1
+    groups written transposed (as quant_rhs)."""
+    x = S.normal_bf16((T, C), 1.0, seed=T + 11 * C, outlier_frac=1e-3)
+    Tb, Cb = cdiv(T, 128), cdiv(C, 128)
+    qr, sr = Guarded(T, rup(C, 16) + 16, torch.uint8), Guarded(Cb, T + 2, torch.float32)
+    qc, sc = Guarded(C, rup(T, 16) + 16, torch.uint8), Guarded(Tb, C + 2, torch.float32)
+    xd = _padded_dev(x, pad) if pad else dev_bf16(x)
+    B.quant_dual(xd, q_row=qr.t, s_row=sr.t, q_col=qc.t, s_col=sc.t)
+    torch.cuda.synchronize()
+    q_ref, s_ref = O.quant_lhs(x)
+    qT_ref, sT_ref = O.quant_rhs(x)
+    assert np.array_equal(qr.t.cpu().numpy()[:, :C], q_ref)
+    assert np.array_equal(f32_bits(sr.t.cpu().numpy()[:, :T]), f32_bits(s_ref))
+    assert np.array_equal(qc.t.cpu().numpy()[:, :T], qT_ref)
+    assert np.array_equal(f32_bits(sc.t.cpu().numpy()[:, :C]), f32_bits(sT_ref))
+    for g, w in ((qr, C), (sr, T), (qc, T), (sc, C)):
+        g.check_outside(w)
+
+
 # ------------------------------------------------------------------ GEMMs in isolation
 
 def _random_codes(rng, shape):
@@ -282,6 +335,32 @@ def test_linear_bwd_matches_oracle(M, N, K):
     torch.cuda.synchronize()
     assert_gemm_close(host_bf16_as_f64(dx), O.linear_dgrad(dy, w), f"dgrad {M}x{N}x{K}")
     assert_gemm_close(host_bf16_as_f64(dw), O.linear_wgrad(dy, x), f"wgrad {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", [(130, 384, 256), (257, 300, 131), (512, 1024, 640), (2048, 4096, 4096)])
+def test_linear_train_form_matches_oracle(M, N, K):
+    """fwd_train keeps the quantised x (both forms) and W (both forms) in the
+    workspace; bwd_saved quantises dY once and runs both gradient GEMMs."""
+    x, w, dy = _dev_linear(M, N, K, seed=6)
+    ws = B.linear_train_workspace(M, N, K)
+    y = B.linear_fwd_train(dev_bf16(x), dev_bf16(w), ws)
+    dx, dw = B.linear_bwd_saved(dev_bf16(dy), ws, M, N, K)
+    torch.cuda.synchronize()
+    if M * N * K <= 1024 ** 3:
+        assert_gemm_close(host_bf16_as_f64(y), O.linear_fwd(x, w), "train fwd")
+        assert_gemm_close(host_bf16_as_f64(dx), O.linear_dgrad(dy, w), "train dgrad")
+        assert_gemm_close(host_bf16_as_f64(dw), O.linear_wgrad(dy, x), "train wgrad")
+    else:
+        rows = _sample_idx(M, 16, 1)
+        ref, cols = _oracle_fwd_sampled(x, w, rows, _sample_idx(N // 128, 2, 2))
+        got = host_bf16_as_f64(y[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()])
+        assert_gemm_close(got, ref, "train fwd sampled")
+        nrows, kc = _sample_idx(N, 16, 3), _sample_idx(K, 128, 4)
+        qa, sa = O.quant_lhs(np.ascontiguousarray(dy[:, nrows]), transposed=True)
+        qbT, sb = O.quant_rhs(np.ascontiguousarray(x[:, kc]))
+        ref = O.gemm(qa, sa, qbT, sb, O.SB_COL, M)
+        got = host_bf16_as_f64(dw[torch.from_numpy(nrows).cuda()][:, torch.from_numpy(kc).cuda()])
+        assert_gemm_close(got, ref, "train wgrad sampled")
 
 
 def _pages_sqnr():
