@@ -30,13 +30,15 @@ __device__ __forceinline__ float recip_rn(float s) { return __frcp_rn(s); }
 // faithful, and from a faithful q the next correction returns RN(x/s) when no
 // intermediate underflows.  Here s >= 1e-12/448 and |x| <= 448 s, so the
 // remainders are normal whenever |x/s| >= 2^-11; smaller quotients can differ
-// from the IEEE quotient by a few ulps but round to the same e4m3 code (+-0).
+// from the IEEE quotient by a few ulps but round to the same e4m3 code.  The
+// corrections can turn a zero quotient's sign positive (-0 + +0 = +0), while
+// x/s for s > 0 always has the sign of x, so the sign of x is copied back.
 __device__ __forceinline__ float quotient(float x, float s, float y) {
   const float q0 = __fmul_rn(x, y);
   const float r0 = __fmaf_rn(-s, q0, x);
   const float q1 = __fmaf_rn(r0, y, q0);
   const float r1 = __fmaf_rn(-s, q1, x);
-  return __fmaf_rn(r1, y, q1);
+  return copysignf(__fmaf_rn(r1, y, q1), x);
 }
 
 // Two fp32 values -> two e4m3fn bytes, RNE, saturating to +-448 (the clamp of
@@ -144,6 +146,25 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// 2-D tiled bulk tensor copy shared -> global (bulk-group completion).
+// Elements outside the tensor's bounds are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map), "r"(src),
+               "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// wait until every committed bulk store of this thread has finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// wait until every committed bulk store of this thread is complete
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// order this thread's generic-proxy shared-memory writes before later async-proxy reads
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------------
 // tcgen05 (5th-generation tensor cores, accumulators in tensor memory)
 // ---------------------------------------------------------------------------
@@ -234,6 +255,10 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
+}
+// copysign on both lanes: magnitude of q, sign of x
+__device__ __forceinline__ uint64_t f2_copysign(uint64_t q, uint64_t x) {
+  return (q & 0x7FFFFFFF7FFFFFFFull) | (x & 0x8000000080000000ull);
 }
 __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   uint64_t d;

@@ -26,6 +26,8 @@
 // frees tensor memory before the CTA exits.
 #include <cudaTypedefs.h>
 
+#include <string.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -53,6 +55,7 @@ struct GemmParams {
   int64_t M, N, K;
   int64_t num_m, num_n, num_tiles, Kb, Nb;
   int c_vec;   // 16-byte output stores allowed (ldc % 8 == 0, c 16-byte aligned)
+  int c_tma;   // C written by TMA stores through shared memory (same conditions)
   int sb_vec;  // 16-byte column-scale loads allowed (ldsb % 4 == 0, sb 16-byte aligned)
   uint64_t wait_limit_ns;
   int debug_stall;  // test hook: the promotion warps wait on a barrier nothing arrives on
@@ -73,8 +76,12 @@ struct GemmCfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;  // two fp32 partial buffers of BN columns
   static constexpr int kOffB = STAGES * kABytes;
+  // per promotion warp: a 4 KiB buffer (32 rows x 64 bf16 columns, 128-byte
+  // swizzled) that stages C for the TMA store at tile end, and holds the
+  // K-block's 128 column scales (128x1 mode) during the K loop
+  static constexpr int kStageC = 32 * 64 * 2;
   static constexpr int kOffSb = kOffB + STAGES * kBBytes;
-  static constexpr int kOffBar = kOffSb + kEpiWarps * 128 * 4;
+  static constexpr int kOffBar = kOffSb + kEpiWarps * kStageC;
   static constexpr int kNumBars = 2 * STAGES + 6;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
@@ -88,10 +95,11 @@ __device__ __forceinline__ void gemm_fail(uint32_t code, volatile int* abort_fla
   *abort_flag = 1;
 }
 
-template <int BN, int STAGES, int SB_MODE>
+template <int BN, int STAGES, int SB_MODE, int LDW>
 __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
     gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tma_a,
-                          const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
+                          const __grid_constant__ CUtensorMap tma_b,
+                          const __grid_constant__ CUtensorMap tma_c, const GemmParams p) {
   using Cfg = GemmCfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -99,7 +107,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sA = sbase;
   const uint32_t sB = sbase + Cfg::kOffB;
-  float* sb_slots = reinterpret_cast<float*>(smem + Cfg::kOffSb);
+  uint8_t* cstage = smem + Cfg::kOffSb;
   const uint32_t bar0 = sbase + Cfg::kOffBar;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
@@ -222,7 +230,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
     const int row = epi_row(e, lane);
     const int col0 = epi_col0(e);
     const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
-    float* slot = sb_slots + e * 128;
+    uint8_t* cbuf = cstage + e * Cfg::kStageC;
+    const uint32_t cbuf_s = smem_u32(cbuf);
+    float* slot = reinterpret_cast<float*>(cbuf);
     int64_t it = 0;
     bool ok = true;
     for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
@@ -251,6 +261,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
       float acc[128];
 #pragma unroll
       for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      if (SB_MODE == kSbCol && p.c_tma) {  // the staging buffer doubles as the scale slot
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+      }
 
       float sa_next = load_sa(0);
       float sb_next = 0.0f;
@@ -283,20 +297,28 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
         }
         const uint32_t taddr = tmem_base + lane_base + (uint32_t)(buf * BN + col0);
         const float scale = sa_cur * sb_cur;
+        // LDW columns of the partial per tensor-memory load round trip (one wait)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(taddr + (uint32_t)(32 * c), r);
+        for (int c = 0; c < 128 / LDW; ++c) {
+          uint32_t r[LDW];
+#pragma unroll
+          for (int h = 0; h < LDW / 32; ++h)
+            tmem_ld_32x32b_x32(taddr + (uint32_t)(LDW * c + 32 * h), *reinterpret_cast<uint32_t(*)[32]>(&r[32 * h]));
           tmem_ld_wait();
           if (SB_MODE == kSbCol) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float sc = sa_cur * slot[32 * c + j];
-              acc[32 * c + j] = fmaf(sc, __uint_as_float(r[j]), acc[32 * c + j]);
+            for (int j4 = 0; j4 < LDW / 4; ++j4) {
+              const float4 sb4 = reinterpret_cast<const float4*>(slot)[LDW / 4 * c + j4];
+              const float sbv[4] = {sb4.x, sb4.y, sb4.z, sb4.w};
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const int j = 4 * j4 + q;
+                acc[LDW * c + j] = fmaf(sa_cur * sbv[q], __uint_as_float(r[j]), acc[LDW * c + j]);
+              }
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) acc[32 * c + j] = fmaf(scale, __uint_as_float(r[j]), acc[32 * c + j]);
+            for (int j = 0; j < LDW; ++j) acc[LDW * c + j] = fmaf(scale, __uint_as_float(r[j]), acc[LDW * c + j]);
           }
         }
         tc_fence_before();
@@ -305,7 +327,33 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
       }
       if (!ok) break;
 
-      if (m_ok) {
+      if (p.c_tma) {
+        // two 32x64 bf16 slices through the swizzled staging buffer, each
+        // written by one TMA store (rows/columns outside [M, N] are dropped)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (lane == 0) bulk_wait_read_all();  // previous store has read the buffer
+          __syncwarp();
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              w[q] = pack_bf16x2(acc[64 * h + 8 * j + 2 * q], acc[64 * h + 8 * j + 2 * q + 1]);
+            const uint32_t addr = cbuf_s + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) << 4));
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                         "r"(w[3])
+                         : "memory");
+          }
+          fence_proxy_async_shared();
+          __syncwarp();
+          const int64_t xs = g.n0 + col0 + 64 * h, ys = g.m0 + 32 * (warp % 4);
+          if (lane == 0 && xs < p.N && ys < p.M) {  // a slice wholly outside C is not issued
+            tma_store_2d(&tma_c, cbuf_s, (int32_t)xs, (int32_t)ys);
+            bulk_commit();
+          }
+        }
+      } else if (m_ok) {
         uint16_t* crow = p.c + m * p.ldc;
 #pragma unroll
         for (int c8 = 0; c8 < 16; ++c8) {
@@ -324,6 +372,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
         }
       }
     }
+    if (p.c_tma && lane == 0) bulk_wait_all();  // stores complete before the CTA exits
   }
 
   __syncwarp();
@@ -369,6 +418,20 @@ static bool make_tma_u8(CUtensorMap* map, const void* base, int64_t inner, int64
   return r == CUDA_SUCCESS;
 }
 
+// Row-major [rows, cols] bf16 output with row stride ld elements; box of
+// 64 columns x 32 rows (one promotion warp's slice), 128-byte swizzle.
+static bool make_tma_bf16_store(CUtensorMap* map, void* base, int64_t cols, int64_t rows, int64_t ld) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t elem[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int gemm_pick_bn(int64_t M, int64_t N, int num_sms) {
   if (N <= 128) return 128;
   const int64_t tiles256 = cdiv(M, kBM) * cdiv(N, 256);
@@ -380,18 +443,18 @@ int64_t gemm_grid(int64_t M, int64_t N, int bn, int num_sms) {
   return tiles < num_sms ? tiles : num_sms;
 }
 
-template <int BN, int STAGES, int MODE>
-static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
-                            int64_t grid, cudaStream_t st) {
+template <int BN, int STAGES, int MODE, int LDW = 32>
+static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
+                            const GemmParams& p, int64_t grid, cudaStream_t st) {
   using Cfg = GemmCfg<BN, STAGES>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_blockwise_kernel<BN, STAGES, MODE>,
+    attr_err = cudaFuncSetAttribute(gemm_blockwise_kernel<BN, STAGES, MODE, LDW>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  gemm_blockwise_kernel<BN, STAGES, MODE><<<(unsigned)grid, Cfg::kThreads, Cfg::kSmemBytes, st>>>(ma, mb, p);
+  gemm_blockwise_kernel<BN, STAGES, MODE, LDW><<<(unsigned)grid, Cfg::kThreads, Cfg::kSmemBytes, st>>>(ma, mb, mc, p);
   return cudaGetLastError();
 }
 
@@ -420,20 +483,23 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const c
   p.Nb = cdiv(a.N, kBlock);
   p.c_vec = (a.ldc % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.c) & 15u) == 0);
   p.sb_vec = (a.ldsb % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.sb) & 15u) == 0);
+  CUtensorMap mc;
+  p.c_tma = p.c_vec && make_tma_bf16_store(&mc, a.c, a.N, a.M, a.ldc);
+  if (!p.c_tma) memset(&mc, 0, sizeof(mc));
   p.wait_limit_ns = wait_limit_ns;
   p.debug_stall = debug_stall;
   const int64_t grid = gemm_grid(a.M, a.N, bn, num_sms);
   if (bn == 256) {
     switch (a.sb_mode) {
-      case kSbTile: return run_gemm<256, 4, kSbTile>(ma, mb, p, grid, st);
-      case kSbTileT: return run_gemm<256, 4, kSbTileT>(ma, mb, p, grid, st);
-      default: return run_gemm<256, 4, kSbCol>(ma, mb, p, grid, st);
+      case kSbTile: return run_gemm<256, 4, kSbTile, 64>(ma, mb, mc, p, grid, st);
+      case kSbTileT: return run_gemm<256, 4, kSbTileT, 64>(ma, mb, mc, p, grid, st);
+      default: return run_gemm<256, 4, kSbCol, 64>(ma, mb, mc, p, grid, st);
     }
   }
   switch (a.sb_mode) {
-    case kSbTile: return run_gemm<128, 6, kSbTile>(ma, mb, p, grid, st);
-    case kSbTileT: return run_gemm<128, 6, kSbTileT>(ma, mb, p, grid, st);
-    default: return run_gemm<128, 6, kSbCol>(ma, mb, p, grid, st);
+    case kSbTile: return run_gemm<128, 6, kSbTile>(ma, mb, mc, p, grid, st);
+    case kSbTileT: return run_gemm<128, 6, kSbTileT>(ma, mb, mc, p, grid, st);
+    default: return run_gemm<128, 6, kSbCol>(ma, mb, mc, p, grid, st);
   }
 }
 

@@ -75,7 +75,7 @@ __device__ __forceinline__ uint32_t quant2(uint32_t w, uint64_t ns2, uint64_t y2
   const uint64_t r0 = f2_fma(ns2, q0, x2);
   const uint64_t q1 = f2_fma(r0, y2, q0);
   const uint64_t r1 = f2_fma(ns2, q1, x2);
-  const uint64_t q2 = f2_fma(r1, y2, q1);
+  const uint64_t q2 = f2_copysign(f2_fma(r1, y2, q1), x2);
   return cvt_e4m3x2(__uint_as_float((uint32_t)q2), __uint_as_float((uint32_t)(q2 >> 32)));
 }
 
@@ -267,7 +267,7 @@ __global__ void __launch_bounds__(kQtThreads, 2)
             const uint64_t r0 = f2_fma(ns2, q0, x2);
             const uint64_t q1 = f2_fma(r0, y2, q0);
             const uint64_t r1 = f2_fma(ns2, q1, x2);
-            const uint64_t q2 = f2_fma(r1, y2, q1);
+            const uint64_t q2 = f2_copysign(f2_fma(r1, y2, q1), x2);
             const uint32_t bb = cvt_e4m3x2(__uint_as_float((uint32_t)q2), __uint_as_float((uint32_t)(q2 >> 32)));
             const uint32_t r = (uint32_t)qt_colpass_row(lane, i);
             asm volatile("st.shared.u8 [%0], %1;" ::"r"(tout + (uint32_t)((8 * chunk + 2 * q) * 128) + r), "r"(bb & 0xFF));
