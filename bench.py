@@ -327,6 +327,21 @@ def algorithmic_units(wl):
     }
 
 
+def aggregate_replicas(local_ms: float, units_per_rank: float, dist=None, device=None):
+    """Whole-job throughput of N independent replicas: every rank processed
+    `units_per_rank` units; the job took the slowest rank's time.
+    Returns (max_ms over ranks, units_total / max_s)."""
+    world = 1
+    ms = float(local_ms)
+    if dist is not None and dist.is_initialized():
+        import torch
+        world = dist.get_world_size()
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * units_per_rank / (ms / 1e3)
+
+
 def run_gpu(args, wl):
     import torch
 
@@ -375,13 +390,9 @@ def run_gpu(args, wl):
     per_kernel = [step.kernel_ms(ev) for ev in events]
     step_ms = [ev[0].elapsed_time(ev[-1]) for ev in events]
 
-    total_ms = float(sum(step_ms))
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     flops_step = 3 * wl.gemm_flops
-    value = world * flops_step * args.steps / (total_ms / 1e3) / 1e12
+    total_ms, flops_per_s = aggregate_replicas(float(sum(step_ms)), flops_step * args.steps, dist, dev)
+    value = flops_per_s / 1e12
 
     # per-kernel averages, rooflines
     units = algorithmic_units(wl)
