@@ -196,12 +196,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
           const uint32_t ph = (uint32_t)((it / STAGES) & 1);
           const int buf = (int)(it & 1);
           const uint32_t tph = (uint32_t)((it >> 1) & 1);
-          if (!mbar_wait_bounded(tempty_bar(buf), tph ^ 1u, p.wait_limit_ns, abort_flag)) {
+          if (!mbar_spin_bounded(tempty_bar(buf), tph ^ 1u, p.wait_limit_ns, abort_flag)) {
             gemm_fail(kErrWaitTmemEmpty, abort_flag);
             ok = false;
             break;
           }
-          if (!mbar_wait_bounded(full_bar(st), ph, p.wait_limit_ns, abort_flag)) {
+          if (!mbar_spin_bounded(full_bar(st), ph, p.wait_limit_ns, abort_flag)) {
             gemm_fail(kErrWaitFull, abort_flag);
             ok = false;
             break;
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
         }
         const int buf = (int)(it & 1);
         const uint32_t tph = (uint32_t)((it >> 1) & 1);
-        const bool got = mbar_wait_bounded(p.debug_stall ? stall_bar : tfull_bar(buf), tph, p.wait_limit_ns,
+        const bool got = mbar_spin_bounded(p.debug_stall ? stall_bar : tfull_bar(buf), tph, p.wait_limit_ns,
                                            abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
           if (lane == 0) gemm_fail(kErrWaitTmemFull, abort_flag);
@@ -305,15 +305,25 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
           for (int h = 0; h < LDW / 32; ++h)
             tmem_ld_32x32b_x32(taddr + (uint32_t)(LDW * c + 32 * h), *reinterpret_cast<uint32_t(*)[32]>(&r[32 * h]));
           tmem_ld_wait();
+          if (c == 128 / LDW - 1) {
+            // the whole partial is in registers: hand the buffer back to the MMA warp now
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(buf));
+          }
           if (SB_MODE == kSbCol) {
+            // acc[n] += (a_s * b_s[n]) * P[n] on fp32x2 lanes (two columns per instruction)
+            const uint64_t sa2 = f2_pack(sa_cur, sa_cur);
 #pragma unroll
             for (int j4 = 0; j4 < LDW / 4; ++j4) {
               const float4 sb4 = reinterpret_cast<const float4*>(slot)[LDW / 4 * c + j4];
-              const float sbv[4] = {sb4.x, sb4.y, sb4.z, sb4.w};
+              const uint64_t t2[2] = {f2_mul(sa2, f2_pack(sb4.x, sb4.y)), f2_mul(sa2, f2_pack(sb4.z, sb4.w))};
 #pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const int j = 4 * j4 + q;
-                acc[LDW * c + j] = fmaf(sa_cur * sbv[q], __uint_as_float(r[j]), acc[LDW * c + j]);
+              for (int h = 0; h < 2; ++h) {
+                const int j = LDW * c + 4 * j4 + 2 * h;
+                const uint64_t p2 =
+                    f2_pack(__uint_as_float(r[4 * j4 + 2 * h]), __uint_as_float(r[4 * j4 + 2 * h + 1]));
+                f2_unpack(f2_fma(t2[h], p2, f2_pack(acc[j], acc[j + 1])), acc[j], acc[j + 1]);
               }
             }
           } else {
@@ -321,9 +331,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
             for (int j = 0; j < LDW; ++j) acc[LDW * c + j] = fmaf(scale, __uint_as_float(r[j]), acc[LDW * c + j]);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(buf));
       }
       if (!ok) break;
 

@@ -68,23 +68,31 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int q) {
 }
 
 // x/s for the two bf16 values of `w` (Markstein-corrected product, as
-// quotient()), on packed fp32x2 lanes; returns the two e4m3 bytes.
+// quotient()), on packed fp32x2 lanes; returns the two e4m3 bytes.  The
+// sign of a zero result may come out positive; sign_bytes() restores it.
 __device__ __forceinline__ uint32_t quant2(uint32_t w, uint64_t ns2, uint64_t y2) {
   const uint64_t x2 = f2_pack(bf16_lo(w), bf16_hi(w));
   const uint64_t q0 = f2_mul(x2, y2);
   const uint64_t r0 = f2_fma(ns2, q0, x2);
   const uint64_t q1 = f2_fma(r0, y2, q0);
   const uint64_t r1 = f2_fma(ns2, q1, x2);
-  const uint64_t q2 = f2_copysign(f2_fma(r1, y2, q1), x2);
+  const uint64_t q2 = f2_fma(r1, y2, q1);
   return cvt_e4m3x2(__uint_as_float((uint32_t)q2), __uint_as_float((uint32_t)(q2 >> 32)));
+}
+
+// The four e4m3 sign bits of the bf16 values in words a (values 0, 1) and b
+// (values 2, 3), placed at bit 7 of bytes 0..3: x/s keeps the sign of x, so
+// ORing these into the codes fixes zero codes and leaves the others as they are.
+__device__ __forceinline__ uint32_t sign_bytes(uint32_t a, uint32_t b) {
+  return __byte_perm(a, b, 0x7531) & 0x80808080u;
 }
 
 // eight values (one 16-byte chunk) -> eight bytes, as two words
 __device__ __forceinline__ uint2 quant8(const uint4& v, float sc, float rc) {
   const uint64_t ns2 = f2_pack(-sc, -sc), y2 = f2_pack(rc, rc);
   uint2 o;
-  o.x = quant2(v.x, ns2, y2) | (quant2(v.y, ns2, y2) << 16);
-  o.y = quant2(v.z, ns2, y2) | (quant2(v.w, ns2, y2) << 16);
+  o.x = (quant2(v.x, ns2, y2) | (quant2(v.y, ns2, y2) << 16)) | sign_bytes(v.x, v.y);
+  o.y = (quant2(v.z, ns2, y2) | (quant2(v.w, ns2, y2) << 16)) | sign_bytes(v.z, v.w);
   return o;
 }
 
