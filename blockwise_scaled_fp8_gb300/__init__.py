@@ -24,6 +24,7 @@ EXPORTS = [
     "bfp8_linear_fwd", "bfp8_linear_bwd", "bfp8_cast_e4m3", "bfp8_check_device_errors",
     "bfp8_debug_write_counts", "bfp8_debug_gemm_stall", "bfp8_quant_dual",
     "bfp8_linear_train_workspace_size", "bfp8_linear_fwd_train", "bfp8_linear_bwd_saved",
+    "bfp8_linear_fwd_static",
 ]
 
 _lib = None
@@ -68,6 +69,7 @@ def lib() -> ctypes.CDLL:
     L.bfp8_linear_train_workspace_size.restype = sz
     L.bfp8_linear_fwd_train.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
     L.bfp8_linear_bwd_saved.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
+    L.bfp8_linear_fwd_static.argtypes = [vp, vp, vp, i64, i64, i64, vp]
     L.bfp8_debug_gemm_stall.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, i64, i64, vp]
     for name in EXPORTS:
         if name not in ("bfp8_last_error", "bfp8_linear_workspace_size", "bfp8_linear_train_workspace_size"):
@@ -283,6 +285,18 @@ def debug_gemm_stall(qa, sa, qb, sb, K: int, out, wait_limit_us: int = 50000):
     return lib().bfp8_debug_gemm_stall(_p(qa), qa.stride(0), _p(sa), sa.stride(0), _p(qb), qb.stride(0),
                                        _p(sb), sb.stride(0), _p(out), out.stride(0), M, N, K,
                                        wait_limit_us, _stream())
+
+
+def linear_fwd_static(x, w, y=None):
+    """y = x W^T through blockwise FP8 without a caller workspace (the
+    library's fixed 32 MiB scratch; see bfp8_linear_fwd_static)."""
+    torch = _torch()
+    M, K = x.shape
+    N = w.shape[0]
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(lib().bfp8_linear_fwd_static(_p(x), _p(w), _p(y), M, N, K, _stream()))
+    return y
 
 
 def linear_train_workspace(M: int, N: int, K: int, device="cuda"):

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbfp8.so")
-SOURCES = ["quant.cu", "quant_tile.cu", "gemm.cu", "api.cu"]
+SOURCES = ["quant.cu", "quant_tile.cu", "gemm.cu", "api.cu", "noalloc.cu"]
 HEADERS = ["common.cuh", "index.cuh", "kernels.h"]
 
 NVCC_FLAGS = [

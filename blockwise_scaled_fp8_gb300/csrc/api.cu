@@ -79,6 +79,8 @@ bfp8_status check_dims(const char* fn, int64_t a, int64_t b, int64_t c = 1) {
 
 }  // namespace
 
+void bfp8::set_last_error(const char* msg) { snprintf(g_msg, sizeof g_msg, "%s", msg); }
+
 extern "C" {
 
 const char* bfp8_last_error(void) { return g_msg; }

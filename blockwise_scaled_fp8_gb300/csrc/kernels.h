@@ -8,6 +8,9 @@ namespace bfp8 {
 
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s per wait: far above any legitimate stall
 
+// Sets the message bfp8_last_error() returns on the calling thread.
+void set_last_error(const char* msg);
+
 cudaError_t launch_quant_rows(const uint16_t* x, int64_t M, int64_t K, int64_t ldx, uint8_t* q,
                               int64_t ldq, float* s, int64_t lds, int num_sms, cudaStream_t st);
 int64_t quant_rows_grid(int64_t M, int64_t K, int num_sms);

@@ -201,6 +201,23 @@ BFP8_API bfp8_status bfp8_linear_bwd_saved(const void *dy, void *dx, void *dw, i
                                            int64_t K, void *ws, size_t ws_bytes, bfp8_stream_t stream);
 
 /*
+ * Linear forward without caller-provided scratch (no counterpart on the pages:
+ * an addition for callers that cannot allocate device memory — code running
+ * inside a CUDA stream capture, where cudaMalloc is not permitted, or plugins
+ * whose host owns all allocations and exposes no allocator).  Same inputs and
+ * output as bfp8_linear_fwd; the quantised x and W and their scales live in
+ * one 32 MiB array that the library reserves on every GPU that loads it, for
+ * the life of the process.  Problems needing more than 32 MiB of quantised
+ * operands (about M*K + N*K bytes plus scales) return BFP8_ERR_INVALID_ARG.
+ * All calls share that array: calls whose work overlaps on the GPU race, so
+ * order them (one stream, or events).  Nothing in it needs clearing between
+ * calls.  The first call on each device looks the array up with that device
+ * current; make it before any stream capture.  Allocates nothing.
+ */
+BFP8_API bfp8_status bfp8_linear_fwd_static(const void *x, const void *w, void *y, int64_t M, int64_t N,
+                                            int64_t K, bfp8_stream_t stream);
+
+/*
  * The method's rounding step on its own: q[i] = RNE_e4m3fn(x[i]) with
  * saturation to +-448 (the clamp).  x device fp32 [n], q device e4m3 [n].
  */
