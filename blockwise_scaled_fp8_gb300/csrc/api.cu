@@ -253,6 +253,37 @@ bfp8_status bfp8_gemm_1x128_128x1(const void* qa, int64_t lda, const float* sa, 
   return gemm_common("bfp8_gemm_1x128_128x1", a, stream);
 }
 
+size_t bfp8_gemm_workspace_size(void) {
+  int sms = 0;
+  if (check_device(&sms) != BFP8_OK) return 0;
+  return gemm_workspace_bytes(sms);
+}
+
+static bfp8_status check_gemm_ws(const char* fn, void* ws, size_t ws_bytes) {
+  if (ws == nullptr) return BFP8_OK;
+  CHECK_ARG((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "%s: workspace must be 256-byte aligned", fn);
+  return BFP8_OK;
+}
+
+bfp8_status bfp8_gemm_1x128_128x128_ws(const void* qa, int64_t lda, const float* sa, int64_t ldsa, const void* qb,
+                                       int64_t ldb, const float* sb, int64_t ldsb, int sb_transposed, void* c,
+                                       int64_t ldc, int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes,
+                                       bfp8_stream_t stream) {
+  bfp8_status st = check_gemm_ws("bfp8_gemm_1x128_128x128_ws", ws, ws_bytes);
+  if (st != BFP8_OK) return st;
+  GemmArgs a{qa, lda, sa, ldsa, qb, ldb, sb, ldsb, sb_transposed ? kSbTileT : kSbTile, c, ldc, M, N, K, ws, ws_bytes};
+  return gemm_common("bfp8_gemm_1x128_128x128_ws", a, stream);
+}
+
+bfp8_status bfp8_gemm_1x128_128x1_ws(const void* qa, int64_t lda, const float* sa, int64_t ldsa, const void* qb,
+                                     int64_t ldb, const float* sb, int64_t ldsb, void* c, int64_t ldc, int64_t M,
+                                     int64_t N, int64_t K, void* ws, size_t ws_bytes, bfp8_stream_t stream) {
+  bfp8_status st = check_gemm_ws("bfp8_gemm_1x128_128x1_ws", ws, ws_bytes);
+  if (st != BFP8_OK) return st;
+  GemmArgs a{qa, lda, sa, ldsa, qb, ldb, sb, ldsb, kSbCol, c, ldc, M, N, K, ws, ws_bytes};
+  return gemm_common("bfp8_gemm_1x128_128x1_ws", a, stream);
+}
+
 bfp8_status bfp8_debug_gemm_stall(const void* qa, int64_t lda, const float* sa, int64_t ldsa, const void* qb,
                                   int64_t ldb, const float* sb, int64_t ldsb, void* c, int64_t ldc, int64_t M,
                                   int64_t N, int64_t K, int64_t wait_limit_us, bfp8_stream_t stream) {
@@ -419,8 +450,10 @@ bfp8_status bfp8_linear_bwd(const void* dy, const void* x, const void* w, void* 
 // ---------------------------------------------------------------------------
 
 namespace {
+constexpr int kMaxSmsForLayout = 256;  // the layout reserves stream-K space for up to 256 SMs
 struct TrainLayout {
-  size_t qx, sx, qxt, sxt, qw, qwt, sw, qdy, sdy, qdyt, sdyt, total;
+  size_t gws, qx, sx, qxt, sxt, qw, qwt, sw, qdy, sdy, qdyt, sdyt, total;
+  size_t gws_bytes;
   int64_t ldK, ldN, ldM, ldsM, ldsN, ldsK;
 };
 TrainLayout train_layout(int64_t M, int64_t N, int64_t K) {
@@ -433,6 +466,8 @@ TrainLayout train_layout(int64_t M, int64_t N, int64_t K) {
   L.ldsK = rup(K, 4);
   const int64_t Kb = cdiv(K, kBlock), Nb = cdiv(N, kBlock), Mb = cdiv(M, kBlock);
   size_t o = 0;
+  L.gws_bytes = gemm_workspace_bytes(kMaxSmsForLayout);
+  L.gws = o; o = a256(o + L.gws_bytes);                 // GEMM stream-K flags + partial tiles
   L.qx = o; o = a256(o + (size_t)M * L.ldK);            // x, 1x128 along K (forward lhs)
   L.sx = o; o = a256(o + (size_t)Kb * L.ldsM * 4);
   L.qxt = o; o = a256(o + (size_t)K * L.ldM);           // x, 128x1 along M, transposed (wgrad rhs)
@@ -473,8 +508,8 @@ bfp8_status bfp8_linear_fwd_train(const void* x, const void* w, void* y, int64_t
   if ((st = bfp8_quant_weight(w, N, K, K, b + L.qw, L.ldK, b + L.qwt, L.ldN, (float*)(b + L.sw), Kb, stream)) !=
       BFP8_OK)
     return st;
-  return bfp8_gemm_1x128_128x128(b + L.qx, L.ldK, (const float*)(b + L.sx), L.ldsM, b + L.qw, L.ldK,
-                                 (const float*)(b + L.sw), Kb, 0, y, N, M, N, K, stream);
+  return bfp8_gemm_1x128_128x128_ws(b + L.qx, L.ldK, (const float*)(b + L.sx), L.ldsM, b + L.qw, L.ldK,
+                                    (const float*)(b + L.sw), Kb, 0, y, N, M, N, K, b + L.gws, L.gws_bytes, stream);
 }
 
 bfp8_status bfp8_linear_bwd_saved(const void* dy, void* dx, void* dw, int64_t M, int64_t N, int64_t K, void* ws,
@@ -492,11 +527,12 @@ bfp8_status bfp8_linear_bwd_saved(const void* dy, void* dx, void* dw, int64_t M,
   if ((st = bfp8_quant_dual(dy, M, N, N, b + L.qdy, L.ldN, (float*)(b + L.sdy), L.ldsM, b + L.qdyt, L.ldM,
                             (float*)(b + L.sdyt), L.ldsN, stream)) != BFP8_OK)
     return st;
-  if ((st = bfp8_gemm_1x128_128x128(b + L.qdy, L.ldN, (const float*)(b + L.sdy), L.ldsM, b + L.qwt, L.ldN,
-                                    (const float*)(b + L.sw), Kb, 1, dx, K, M, K, N, stream)) != BFP8_OK)
+  if ((st = bfp8_gemm_1x128_128x128_ws(b + L.qdy, L.ldN, (const float*)(b + L.sdy), L.ldsM, b + L.qwt, L.ldN,
+                                       (const float*)(b + L.sw), Kb, 1, dx, K, M, K, N, b + L.gws, L.gws_bytes,
+                                       stream)) != BFP8_OK)
     return st;
-  return bfp8_gemm_1x128_128x1(b + L.qdyt, L.ldM, (const float*)(b + L.sdyt), L.ldsN, b + L.qxt, L.ldM,
-                               (const float*)(b + L.sxt), L.ldsK, dw, K, N, K, M, stream);
+  return bfp8_gemm_1x128_128x1_ws(b + L.qdyt, L.ldM, (const float*)(b + L.sdyt), L.ldsN, b + L.qxt, L.ldM,
+                                  (const float*)(b + L.sxt), L.ldsK, dw, K, N, K, M, b + L.gws, L.gws_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -525,7 +561,7 @@ void replay_tile(int64_t T, int64_t C, bool rows_out, bool cols_out, int scale_k
         for (int warp = 0; warp < kQtThreads / 32; ++warp)
           for (int half = 0; half < 2; ++half)
             for (int l16 = 0; l16 < 16; ++l16)
-              for (int ps = 0; ps < 8; ++ps) {
+              for (int ps = 0; ps < kQtRowPasses; ++ps) {
                 const int64_t t = t0 + qt_rowpass_row(ps, warp, half), c = c0 + qt_rowpass_col(l16);
                 if (t >= T) continue;
                 if (rows_out)
@@ -542,7 +578,7 @@ void replay_tile(int64_t T, int64_t C, bool rows_out, bool cols_out, int scale_k
         }
       if (scale_kind == 2)
         for (int warp = 0; warp < kQtThreads / 32; ++warp)
-          for (int h = 0; h < 2; ++h)
+          for (int h = 0; h < kQtColChunks; ++h)
             for (int lane = 0; lane < 8; ++lane) {
               const int64_t cg = c0 + 8 * qt_colpass_chunk(warp, h) + lane;
               if (cg < C) hit(scounts, t0 / 128, cg, Tb, C);
@@ -646,14 +682,19 @@ bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, i
     }
     return BFP8_OK;
   }
-  if (kind == 3) {  // GEMM output C [M,N]
+  if (kind == 3) {  // GEMM output C [M,N]; flag bit 2: launched with a stream-K workspace
     const int bn = gemm_pick_bn(M, N, sms);
     const int64_t num_m = cdiv(M, kBM), num_n = cdiv(N, bn), tiles = num_m * num_n;
-    const int64_t grid = gemm_grid(M, N, bn, sms);
+    const int64_t grid = gemm_grid(M, N, bn, sms), Kb = cdiv(K, kBK);
+    const bool sk = (flag & 4) && gemm_use_stream_k(M, N, K, bn, sms);
     const int epi_warps = bn / 32;
-    for (int64_t cta = 0; cta < grid; ++cta)
-      for (int64_t t = cta; t < tiles; t += grid) {
-        const GemmTile g = gemm_tile(t, num_m, num_n, bn);
+    for (int64_t cta = 0; cta < grid; ++cta) {
+      GemmWork work;
+      work.init(sk, cta, grid, tiles, Kb > 0 ? Kb : 1);
+      GemmSeg seg;
+      while (work.next(seg, Kb > 0 ? Kb : 1)) {
+        if (seg.kb1 == Kb && seg.kb0 > 0) continue;  // hands its partial to the tile's owner; no store
+        const GemmTile g = gemm_tile(seg.tile, num_m, num_n, bn);
         for (int e = 0; e < epi_warps; ++e)
           for (int lane = 0; lane < 32; ++lane) {
             const int64_t m = g.m0 + epi_row(e, lane);
@@ -664,6 +705,7 @@ bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, i
             }
           }
       }
+    }
     return BFP8_OK;
   }
   return fail(BFP8_ERR_INVALID_ARG, "bfp8_debug_write_counts: unknown kind %d", kind);

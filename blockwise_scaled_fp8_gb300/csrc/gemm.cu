@@ -43,6 +43,7 @@ enum : uint32_t {
   kErrWaitTmemEmpty = 1u << 2,  // MMA: a tensor-memory buffer was never released
   kErrWaitTmemFull = 1u << 3,   // epilogue: a partial product never arrived
   kErrWaitDrain = 1u << 4,      // teardown: MMAs or copies in flight never finished
+  kErrWaitPartial = 1u << 5,    // stream-K: a neighbouring CTA's partial tile never arrived
 };
 
 struct GemmParams {
@@ -59,6 +60,9 @@ struct GemmParams {
   int sb_vec;  // 16-byte column-scale loads allowed (ldsb % 4 == 0, sb 16-byte aligned)
   uint64_t wait_limit_ns;
   int debug_stall;  // test hook: the promotion warps wait on a barrier nothing arrives on
+  int stream_k;     // split the (tile, K-block) units evenly over the CTAs
+  float* partials;  // stream-K: one BM x BN fp32 partial tile per CTA
+  uint32_t* flags;  // stream-K: flags[cta] = 1 once CTA cta's partial is written
 };
 
 template <int BN, int STAGES>
@@ -82,7 +86,7 @@ struct GemmCfg {
   static constexpr int kStageC = 32 * 64 * 2;
   static constexpr int kOffSb = kOffB + STAGES * kBBytes;
   static constexpr int kOffBar = kOffSb + kEpiWarps * kStageC;
-  static constexpr int kNumBars = 2 * STAGES + 6;
+  static constexpr int kNumBars = 2 * STAGES + 8;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -120,6 +124,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
   auto tempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + 2 + i); };
   const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
   const uint32_t stall_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 5);  // never arrived on
+  // stream-K hand-offs among the promotion warps (each used at most once per CTA)
+  const uint32_t skc_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 6);  // partial written
+  const uint32_t sko_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 7);  // neighbour's partial consumed
 
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const int lane = (int)(threadIdx.x & 31);
@@ -135,6 +142,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
     }
     mbar_init(drain_bar, 1);
     mbar_init(stall_bar, 1);
+    mbar_init(skc_bar, Cfg::kEpiWarps);
+    mbar_init(sko_bar, Cfg::kEpiWarps);
     *abort_flag = 0;
     *never = 0;
     fence_barrier_init();
@@ -159,9 +168,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
     if (lane == 0) {
       int64_t it = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        const GemmTile g = gemm_tile(t, p.num_m, p.num_n, BN);
-        for (int64_t kb = 0; kb < p.Kb; ++kb, ++it) {
+      GemmWork work;
+      work.init(p.stream_k, blockIdx.x, gridDim.x, p.num_tiles, p.Kb);
+      GemmSeg seg;
+      while (ok && work.next(seg, p.Kb)) {
+        const GemmTile g = gemm_tile(seg.tile, p.num_m, p.num_n, BN);
+        for (int64_t kb = seg.kb0; kb < seg.kb1; ++kb, ++it) {
           const int st = (int)(it % STAGES);
           const uint32_t ph = (uint32_t)((it / STAGES) & 1);
           if (!mbar_wait_bounded(empty_bar(st), ph ^ 1u, p.wait_limit_ns, abort_flag)) {
@@ -190,8 +202,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
       constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
       int64_t it = 0;
       bool ok = true;
-      for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-        for (int64_t kb = 0; kb < p.Kb; ++kb, ++it) {
+      GemmWork work;
+      work.init(p.stream_k, blockIdx.x, gridDim.x, p.num_tiles, p.Kb);
+      GemmSeg seg;
+      while (ok && work.next(seg, p.Kb)) {
+        for (int64_t kb = seg.kb0; kb < seg.kb1; ++kb, ++it) {
           const int st = (int)(it % STAGES);
           const uint32_t ph = (uint32_t)((it / STAGES) & 1);
           const int buf = (int)(it & 1);
@@ -235,8 +250,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
     float* slot = reinterpret_cast<float*>(cbuf);
     int64_t it = 0;
     bool ok = true;
-    for (int64_t t = blockIdx.x; t < p.num_tiles && ok; t += gridDim.x) {
-      const GemmTile g = gemm_tile(t, p.num_m, p.num_n, BN);
+    GemmWork work;
+    work.init(p.stream_k, blockIdx.x, gridDim.x, p.num_tiles, p.Kb);
+    GemmSeg seg;
+    while (ok && work.next(seg, p.Kb)) {
+      const GemmTile g = gemm_tile(seg.tile, p.num_m, p.num_n, BN);
       const int64_t m = g.m0 + row;
       const bool m_ok = m < p.M;
       const int64_t nb = (g.n0 + col0) / kBlock;  // B tile-scale block of these 128 columns
@@ -266,23 +284,23 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
         __syncwarp();
       }
 
-      float sa_next = load_sa(0);
+      float sa_next = load_sa(seg.kb0);
       float sb_next = 0.0f;
       float4 sbc_next = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (SB_MODE == kSbCol) sbc_next = load_sb_col(0);
-      else sb_next = load_sb_tile(0);
+      if (SB_MODE == kSbCol) sbc_next = load_sb_col(seg.kb0);
+      else sb_next = load_sb_tile(seg.kb0);
 
-      for (int64_t kb = 0; kb < p.Kb; ++kb, ++it) {
+      for (int64_t kb = seg.kb0; kb < seg.kb1; ++kb, ++it) {
         const float sa_cur = sa_next, sb_cur = sb_next;
         const float4 sbc_cur = sbc_next;
-        if (kb + 1 < p.Kb) {  // prefetch the next K-block's scales (masked loads)
+        if (kb + 1 < seg.kb1) {  // prefetch the next K-block's scales (masked loads)
           sa_next = load_sa(kb + 1);
           if (SB_MODE == kSbCol) sbc_next = load_sb_col(kb + 1);
           else sb_next = load_sb_tile(kb + 1);
         }
         const int buf = (int)(it & 1);
         const uint32_t tph = (uint32_t)((it >> 1) & 1);
-        const bool got = mbar_spin_bounded(p.debug_stall ? stall_bar : tfull_bar(buf), tph, p.wait_limit_ns,
+        const bool got = mbar_wait_bounded(p.debug_stall ? stall_bar : tfull_bar(buf), tph, p.wait_limit_ns,
                                            abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
           if (lane == 0) gemm_fail(kErrWaitTmemFull, abort_flag);
@@ -333,6 +351,51 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
         }
       }
       if (!ok) break;
+
+      if (seg.kb1 == p.Kb && seg.kb0 > 0) {
+        // stream-K, this CTA finished the tile's last K-blocks first: leave the
+        // partial sums for the CTA that computes its first K-blocks, then move on
+        float* dst = p.partials + (size_t)blockIdx.x * (kBM * BN) + (size_t)row * BN + col0;
+#pragma unroll
+        for (int j = 0; j < 128; j += 4)
+          *reinterpret_cast<float4*>(dst + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(skc_bar);
+        if (e == 0 && lane == 0) {  // publish once every promotion warp has written its rows
+          if (mbar_wait_bounded(skc_bar, 0, p.wait_limit_ns, abort_flag)) st_release_gpu(p.flags + blockIdx.x, 1u);
+          else gemm_fail(kErrWaitPartial, abort_flag);
+        }
+        continue;
+      }
+      if (seg.kb0 == 0 && seg.kb1 < p.Kb) {
+        // stream-K, this CTA computed the tile's first K-blocks last: add the
+        // next CTA's partial sums (written at that CTA's start) before storing
+        const uint32_t* flag = p.flags + blockIdx.x + 1;
+        bool got = true;
+        if (lane == 0) got = spin_flag_bounded(flag, p.wait_limit_ns, abort_flag);
+        if (!__shfl_sync(0xffffffffu, (int)got, 0)) {
+          if (lane == 0) gemm_fail(kErrWaitPartial, abort_flag);
+          ok = false;
+          break;
+        }
+        (void)ld_acquire_gpu(flag);  // order this lane's loads after the flag
+        const float* src = p.partials + (size_t)(blockIdx.x + 1) * (kBM * BN) + (size_t)row * BN + col0;
+#pragma unroll
+        for (int j = 0; j < 128; j += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(src + j);
+          acc[j] += v.x;
+          acc[j + 1] += v.y;
+          acc[j + 2] += v.z;
+          acc[j + 3] += v.w;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sko_bar);
+        if (e == 0 && lane == 0) {  // every promotion warp has read it: clear for the next launch
+          if (mbar_wait_bounded(sko_bar, 0, p.wait_limit_ns, abort_flag)) st_relaxed_gpu(const_cast<uint32_t*>(flag), 0u);
+          else gemm_fail(kErrWaitPartial, abort_flag);
+        }
+      }
 
       if (p.c_tma) {
         // two 32x64 bf16 slices through the swizzled staging buffer, each
@@ -465,6 +528,19 @@ static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const 
   return cudaGetLastError();
 }
 
+bool gemm_use_stream_k(int64_t M, int64_t N, int64_t K, int bn, int num_sms) {
+  const int64_t tiles = cdiv(M, kBM) * cdiv(N, bn), Kb = cdiv(K, kBK);
+  const int64_t grid = gemm_grid(M, N, bn, num_sms);
+  if (grid < num_sms) return false;                       // fewer tiles than SMs: nothing to balance
+  if (tiles * Kb / grid < Kb) return false;               // a tile would span three CTAs
+  const double eff = (double)tiles / (double)(cdiv(tiles, grid) * grid);
+  return eff < 0.95;
+}
+
+size_t gemm_workspace_bytes(int num_sms) {
+  return kGemmFlagBytes + (size_t)num_sms * kBM * 256 * sizeof(float);
+}
+
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const char** msg,
                         uint64_t wait_limit_ns, int debug_stall) {
   const int bn = gemm_pick_bn(a.M, a.N, num_sms);
@@ -495,6 +571,10 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const c
   if (!p.c_tma) memset(&mc, 0, sizeof(mc));
   p.wait_limit_ns = wait_limit_ns;
   p.debug_stall = debug_stall;
+  p.stream_k = a.ws != nullptr && a.ws_bytes >= gemm_workspace_bytes(num_sms) &&
+               gemm_use_stream_k(a.M, a.N, a.K, bn, num_sms);
+  p.flags = reinterpret_cast<uint32_t*>(a.ws);
+  p.partials = a.ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(a.ws) + kGemmFlagBytes) : nullptr;
   const int64_t grid = gemm_grid(a.M, a.N, bn, num_sms);
   if (bn == 256) {
     switch (a.sb_mode) {

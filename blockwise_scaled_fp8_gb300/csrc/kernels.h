@@ -44,12 +44,18 @@ struct GemmArgs {
   void* c;
   int64_t ldc;
   int64_t M, N, K;
+  void* ws = nullptr;   // optional stream-K workspace (flags zeroed before first use)
+  size_t ws_bytes = 0;
 };
 
 // Returns cudaSuccess or the launch error; *msg gets a static description of
 // a host-side failure (tensor-map encoding) when the return is not success.
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const char** msg,
                         uint64_t wait_limit_ns = kWaitLimitNs, int debug_stall = 0);
+// Whether a launch with a workspace splits its (tile, K-block) units evenly
+// over the CTAs (stream-K), and the workspace that needs.
+bool gemm_use_stream_k(int64_t M, int64_t N, int64_t K, int bn, int num_sms);
+size_t gemm_workspace_bytes(int num_sms);
 // Tile width the launcher picks for an M x N output, and the grid it uses.
 int gemm_pick_bn(int64_t M, int64_t N, int num_sms);
 int64_t gemm_grid(int64_t M, int64_t N, int bn, int num_sms);

@@ -33,7 +33,7 @@ constexpr int kQtBoxBytes = 128 * 128;               // 64 bf16 columns x 128 ro
 constexpr int kQtStageBytes = 2 * kQtBoxBytes;       // one 128x128 bf16 tile
 constexpr int kQtOffTout = 2 * kQtStageBytes;        // transposed byte tile, 128 x 128
 constexpr int kQtOffBar = kQtOffTout + 128 * 128;
-constexpr int kQtSmemBytes = kQtOffBar + 64 + 1024;  // + alignment slack
+constexpr int kQtSmemBytes = kQtOffBar + 64 + 4 * (kQtThreads / 32) + 1024;  // + alignment slack
 
 struct TileQuantParams {
   int64_t T, C;
@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kQtThreads, 2)
   const uint32_t tout = sbase + kQtOffTout;
   const uint32_t bar0 = sbase + kQtOffBar;
   volatile int* never = reinterpret_cast<volatile int*>(smem + kQtOffBar + 16);
-  float* red = reinterpret_cast<float*>(smem + kQtOffBar + 32);  // 8 warp partials
+  float* red = reinterpret_cast<float*>(smem + kQtOffBar + 64);  // one partial per warp
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
@@ -155,33 +155,33 @@ __global__ void __launch_bounds__(kQtThreads, 2)
     // ------------------------------------------------------------ row pass
     if (MODE & (kTileRow | kTileScale)) {
       const int lane16 = lane & 15, half = lane >> 4;
-      uint4 v[8];
+      uint4 v[kQtRowPasses];
 #pragma unroll
-      for (int ps = 0; ps < 8; ++ps) v[ps] = lds128(tile_chunk_addr(stage, qt_rowpass_row(ps, warp, half), lane16));
-      float sc[8], rc[8];
+      for (int ps = 0; ps < kQtRowPasses; ++ps) v[ps] = lds128(tile_chunk_addr(stage, qt_rowpass_row(ps, warp, half), lane16));
+      float sc[kQtRowPasses], rc[kQtRowPasses];
       if (MODE & kTileRow) {
-        float a[8];
+        float a[kQtRowPasses];
 #pragma unroll
-        for (int ps = 0; ps < 8; ++ps) {
+        for (int ps = 0; ps < kQtRowPasses; ++ps) {
           const uint32_t m2 = absmax2(absmax2(absmax2(absmax2(0u, v[ps].x), v[ps].y), v[ps].z), v[ps].w);
           a[ps] = fmaxf(bf16_lo(m2), bf16_hi(m2));
 #pragma unroll
           for (int off = 8; off >= 1; off >>= 1) a[ps] = fmaxf(a[ps], __shfl_xor_sync(0xffffffffu, a[ps], off));
         }
-        // lane (half*16 + j), j < 8, computes the scale of pass j; then broadcast
+        // lane (half*16 + j), j < kQtRowPasses, computes the scale of pass j; then broadcast
         float amine = a[0];
 #pragma unroll
-        for (int ps = 1; ps < 8; ++ps) amine = (lane16 == ps) ? a[ps] : amine;
+        for (int ps = 1; ps < kQtRowPasses; ++ps) amine = (lane16 == ps) ? a[ps] : amine;
         const float scm = group_scale(amine), rcm = recip_rn(scm);
 #pragma unroll
-        for (int ps = 0; ps < 8; ++ps) {
+        for (int ps = 0; ps < kQtRowPasses; ++ps) {
           sc[ps] = __shfl_sync(0xffffffffu, scm, half * 16 + ps);
           rc[ps] = __shfl_sync(0xffffffffu, rcm, half * 16 + ps);
         }
       } else {
         uint32_t m2 = 0;
 #pragma unroll
-        for (int ps = 0; ps < 8; ++ps)
+        for (int ps = 0; ps < kQtRowPasses; ++ps)
           m2 = absmax2(absmax2(absmax2(absmax2(m2, v[ps].x), v[ps].y), v[ps].z), v[ps].w);
         float a = fmaxf(bf16_lo(m2), bf16_hi(m2));
 #pragma unroll
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kQtThreads, 2)
         tile_sc = group_scale(a);
         tile_rc = recip_rn(tile_sc);
 #pragma unroll
-        for (int ps = 0; ps < 8; ++ps) {
+        for (int ps = 0; ps < kQtRowPasses; ++ps) {
           sc[ps] = tile_sc;
           rc[ps] = tile_rc;
         }
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kQtThreads, 2)
       if ((MODE & kTileRow) || p.q_row != nullptr) {
         const int64_t c = c0 + qt_rowpass_col(lane16);
 #pragma unroll
-        for (int ps = 0; ps < 8; ++ps) {
+        for (int ps = 0; ps < kQtRowPasses; ++ps) {
           const int64_t t = t0 + qt_rowpass_row(ps, warp, half);
           const uint2 o = quant8(v[ps], sc[ps], rc[ps]);
           if (t < p.T) {
@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kQtThreads, 2)
     // ------------------------------------------------------------ column pass
     if ((MODE & kTileCol) || ((MODE & kTileScale) && p.q_col != nullptr)) {
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < kQtColChunks; ++h) {
         const int chunk = qt_colpass_chunk(warp, h);
         uint4 v[4];
 #pragma unroll

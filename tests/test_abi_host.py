@@ -129,7 +129,10 @@ def test_quant_dual_index_replay_exactly_once(M, N, K):
     assert oob == 0 and c.shape == (K, M) and np.all(c == 1) and np.all(s == 1)
 
 
-@pytest.mark.parametrize("M,N,K", SHAPES + [(4096, 4096, 128), (2048, 4096, 128), (16384, 1024, 128)])
-def test_gemm_epilogue_index_replay_exactly_once(M, N, K):
-    c, _, oob = B.debug_write_counts(3, M, N, K)
+@pytest.mark.parametrize("M,N,K", SHAPES + [(4096, 4096, 128), (2048, 4096, 128), (16384, 1024, 128),
+                                             (2048, 4096, 4096), (2000, 4000, 520), (4096, 4096, 8192)])
+@pytest.mark.parametrize("ws", [0, 4])
+def test_gemm_epilogue_index_replay_exactly_once(M, N, K, ws):
+    """Tile-parallel and stream-K schedules store each output element once."""
+    c, _, oob = B.debug_write_counts(3, M, N, K, ws)
     assert oob == 0 and np.all(c == 1)

@@ -264,7 +264,7 @@ def _random_codes(rng, shape):
     return c
 
 
-def _gemm_case(M, N, K, mode, seed, ldc_extra=0):
+def _gemm_case(M, N, K, mode, seed, ldc_extra=0, ws=None, repeats=1):
     """Random e4m3 codes and random scales fed to both sides."""
     rng = np.random.default_rng(seed)
     Kb, Nb = cdiv(K, 128), cdiv(N, 128)
@@ -283,11 +283,13 @@ def _gemm_case(M, N, K, mode, seed, ldc_extra=0):
     ldc = N + ldc_extra
     flat16 = torch.full((M * ldc + 2 * GUARD,), 0x7FC1, dtype=torch.int16, device="cuda")
     out = flat16[GUARD:GUARD + M * ldc].view(torch.bfloat16).view(M, ldc)
-    if mode == O.SB_COL:
-        B.gemm_1x128_128x1(cu(qa), cu(sa), cu(qb), cu(sb), K, out=out, M=M, N=N)
-    else:
-        B.gemm_1x128_128x128(cu(qa), cu(sa), cu(qb), cu(sb), K, sb_transposed=(mode == O.SB_TILE_T),
-                             out=out, M=M, N=N)
+    for _ in range(repeats):
+        out[:, :N].zero_()
+        if mode == O.SB_COL:
+            B.gemm_1x128_128x1(cu(qa), cu(sa), cu(qb), cu(sb), K, out=out, M=M, N=N, ws=ws)
+        else:
+            B.gemm_1x128_128x128(cu(qa), cu(sa), cu(qb), cu(sb), K, sb_transposed=(mode == O.SB_TILE_T),
+                                 out=out, M=M, N=N, ws=ws)
     torch.cuda.synchronize()
     h = flat16.cpu().numpy()
     assert np.all(h[:GUARD] == 0x7FC1) and np.all(h[-GUARD:] == 0x7FC1), "write outside C"
@@ -306,6 +308,25 @@ GEMM_SHAPES = [(130, 384, 256), (1, 8, 128), (2, 512, 128), (4, 3584, 640), (128
 def test_gemm_random_codes_matches_oracle(M, N, K, mode):
     got, ref = _gemm_case(M, N, K, mode, seed=M * 7 + N * 3 + K + mode, ldc_extra=8)
     assert_gemm_close(got, ref, f"gemm mode {mode} {M}x{N}x{K}")
+
+
+# shapes whose whole-tile schedule would leave the last wave partly idle on a
+# 152-SM GB300, so a launch with a workspace splits K-blocks across CTAs
+SK_SHAPES = [(2048, 4096, 512), (2000, 4000, 520), (1200, 4096, 384), (2048, 4096, 4096)]
+
+
+@pytest.mark.parametrize("M,N,K", SK_SHAPES)
+@pytest.mark.parametrize("mode", [O.SB_TILE, O.SB_TILE_T, O.SB_COL])
+def test_gemm_stream_k_matches_oracle(M, N, K, mode):
+    """Stream-K schedule: partial tiles handed between CTAs through the
+    workspace; three launches in a row reuse its flags (each launch must leave
+    them clear)."""
+    ws = B.gemm_workspace()
+    got, ref = _gemm_case(M, N, K, mode, seed=M + N + K + mode, ldc_extra=8, ws=ws, repeats=3)
+    assert_gemm_close(got, ref, f"stream-K gemm mode {mode} {M}x{N}x{K}")
+    off = (-ws.data_ptr()) % 256
+    assert int(ws[off:off + 4096].count_nonzero()) == 0  # flags left clear
+    B.check_device_errors()
 
 
 # ------------------------------------------------------------------ quant + GEMM (linear)
