@@ -261,7 +261,6 @@ class Step:
         self.qdy, self.sdy = e(M, rup(N, 16), dt=u8), e(cd(N), rup(M, 4), dt=f32)
         self.qdyt, self.sdyt = e(N, rup(M, 16), dt=u8), e(cd(M), rup(N, 4), dt=f32)
         self.y, self.dx, self.dw = e(M, N, dt=bf), e(M, K, dt=bf), e(N, K, dt=bf)
-        self.gws = B.gemm_workspace(dev)  # stream-K workspace shared by the three GEMMs (one stream)
         self.names = ["quant_dual_x", "quant_weight_w", "gemm_fwd", "quant_dual_dy", "gemm_dgrad", "gemm_wgrad"]
         self.launches_per_step = len(self.names)
 
@@ -274,12 +273,11 @@ class Step:
         return [
             lambda: B.quant_dual(x, q_row=self.qx, s_row=self.sx, q_col=self.qxt, s_col=self.sxt),
             lambda: B.quant_weight(w, with_q=True, with_t=True, q=self.qw, qt=self.qwt, s=self.sw),
-            lambda: B.gemm_1x128_128x128(self.qx, self.sx, self.qw, self.sw, K, out=self.y, M=M, N=N, ws=self.gws),
+            lambda: B.gemm_1x128_128x128(self.qx, self.sx, self.qw, self.sw, K, out=self.y, M=M, N=N),
             lambda: B.quant_dual(dy, q_row=self.qdy, s_row=self.sdy, q_col=self.qdyt, s_col=self.sdyt),
             lambda: B.gemm_1x128_128x128(self.qdy, self.sdy, self.qwt, self.sw, N, sb_transposed=True,
-                                         out=self.dx, M=M, N=K, ws=self.gws),
-            lambda: B.gemm_1x128_128x1(self.qdyt, self.sdyt, self.qxt, self.sxt, M, out=self.dw, M=N, N=K,
-                                       ws=self.gws),
+                                         out=self.dx, M=M, N=K),
+            lambda: B.gemm_1x128_128x1(self.qdyt, self.sdyt, self.qxt, self.sxt, M, out=self.dw, M=N, N=K),
         ]
 
     def capture(self, x, w, dy):

@@ -24,8 +24,7 @@ EXPORTS = [
     "bfp8_linear_fwd", "bfp8_linear_bwd", "bfp8_cast_e4m3", "bfp8_check_device_errors",
     "bfp8_debug_write_counts", "bfp8_debug_gemm_stall", "bfp8_quant_dual",
     "bfp8_linear_train_workspace_size", "bfp8_linear_fwd_train", "bfp8_linear_bwd_saved",
-    "bfp8_linear_fwd_static", "bfp8_gemm_workspace_size", "bfp8_gemm_1x128_128x128_ws",
-    "bfp8_gemm_1x128_128x1_ws",
+    "bfp8_linear_fwd_static",
 ]
 
 _lib = None
@@ -71,15 +70,9 @@ def lib() -> ctypes.CDLL:
     L.bfp8_linear_fwd_train.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
     L.bfp8_linear_bwd_saved.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
     L.bfp8_linear_fwd_static.argtypes = [vp, vp, vp, i64, i64, i64, vp]
-    L.bfp8_gemm_workspace_size.argtypes = []
-    L.bfp8_gemm_workspace_size.restype = sz
-    L.bfp8_gemm_1x128_128x128_ws.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, vp, i64, i64, i64, i64,
-                                             vp, sz, vp]
-    L.bfp8_gemm_1x128_128x1_ws.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, i64, vp, sz, vp]
     L.bfp8_debug_gemm_stall.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, i64, i64, vp]
     for name in EXPORTS:
-        if name not in ("bfp8_last_error", "bfp8_linear_workspace_size", "bfp8_linear_train_workspace_size",
-                        "bfp8_gemm_workspace_size"):
+        if name not in ("bfp8_last_error", "bfp8_linear_workspace_size", "bfp8_linear_train_workspace_size"):
             getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -211,35 +204,22 @@ def cast_e4m3(x, q=None):
 # GEMMs
 # ---------------------------------------------------------------------------
 
-def gemm_workspace(device="cuda"):
-    """A zeroed workspace for the stream-K GEMM schedule (see bfp8_gemm_*_ws)."""
-    torch = _torch()
-    return torch.zeros(int(lib().bfp8_gemm_workspace_size()) + 256, dtype=torch.uint8, device=device)
-
-
-def _ws_args(ws):
-    if ws is None:
-        return ctypes.c_void_p(None), 0
-    return _aligned(ws)
-
-
-def gemm_1x128_128x128(qa, sa, qb, sb, K: int, sb_transposed: bool = False, out=None, M=None, N=None, ws=None):
+def gemm_1x128_128x128(qa, sa, qb, sb, K: int, sb_transposed: bool = False, out=None, M=None, N=None):
     """C = A B with A = qa [M, lda] (1x128 scales sa [Kb, ldsa]), B^T = qb
     [N, ldb] (128x128 tile scales sb, [Nb, ldsb] or transposed [Kb, ldsb]).
-    Returns C [M, N] bf16.  `ws` (from gemm_workspace()) enables stream-K."""
+    Returns C [M, N] bf16."""
     torch = _torch()
     M = qa.shape[0] if M is None else M
     N = qb.shape[0] if N is None else N
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
-    wp, wn = _ws_args(ws)
-    _check(lib().bfp8_gemm_1x128_128x128_ws(_p(qa), qa.stride(0), _p(sa), sa.stride(0), _p(qb), qb.stride(0),
-                                            _p(sb), sb.stride(0), int(sb_transposed), _p(out), out.stride(0),
-                                            M, N, K, wp, wn, _stream()))
+    _check(lib().bfp8_gemm_1x128_128x128(_p(qa), qa.stride(0), _p(sa), sa.stride(0), _p(qb), qb.stride(0),
+                                         _p(sb), sb.stride(0), int(sb_transposed), _p(out), out.stride(0),
+                                         M, N, K, _stream()))
     return out
 
 
-def gemm_1x128_128x1(qa, sa, qb, sb, K: int, out=None, M=None, N=None, ws=None):
+def gemm_1x128_128x1(qa, sa, qb, sb, K: int, out=None, M=None, N=None):
     """C = A B with A = qa [M, lda] (1x128 scales sa [Kb, ldsa]) and B^T = qb
     [N, ldb] with one scale per column and K-block, sb [Kb, ldsb]."""
     torch = _torch()
@@ -247,10 +227,8 @@ def gemm_1x128_128x1(qa, sa, qb, sb, K: int, out=None, M=None, N=None, ws=None):
     N = qb.shape[0] if N is None else N
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
-    wp, wn = _ws_args(ws)
-    _check(lib().bfp8_gemm_1x128_128x1_ws(_p(qa), qa.stride(0), _p(sa), sa.stride(0), _p(qb), qb.stride(0),
-                                          _p(sb), sb.stride(0), _p(out), out.stride(0), M, N, K, wp, wn,
-                                          _stream()))
+    _check(lib().bfp8_gemm_1x128_128x1(_p(qa), qa.stride(0), _p(sa), sa.stride(0), _p(qb), qb.stride(0),
+                                       _p(sb), sb.stride(0), _p(out), out.stride(0), M, N, K, _stream()))
     return out
 
 
@@ -322,10 +300,10 @@ def linear_fwd_static(x, w, y=None):
 
 
 def linear_train_workspace(M: int, N: int, K: int, device="cuda"):
-    """Workspace for linear_fwd_train / linear_bwd_saved (zeroed: its first
-    4 KiB are the GEMMs' stream-K flags)."""
+    """Workspace for linear_fwd_train / linear_bwd_saved (256 bytes of slack
+    for alignment)."""
     torch = _torch()
-    return torch.zeros(int(lib().bfp8_linear_train_workspace_size(M, N, K)) + 256, dtype=torch.uint8, device=device)
+    return torch.empty(int(lib().bfp8_linear_train_workspace_size(M, N, K)) + 256, dtype=torch.uint8, device=device)
 
 
 def _aligned(ws):

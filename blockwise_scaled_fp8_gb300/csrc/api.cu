@@ -101,7 +101,7 @@ bfp8_status bfp8_quant_lhs(const void* x, int64_t M, int64_t K, int64_t ldx, int
   if ((st = check_device(&sms)) != BFP8_OK) return st;
   cudaError_t e;
   const uint16_t* xb = (const uint16_t*)x;
-  if (quant_tile_supported(x, ldx)) {
+  if (x_transposed ? quant_tile_supported(x, ldx, nullptr, 0, q, ldq) : quant_tile_supported(x, ldx, q, ldq, nullptr, 0)) {
     if (x_transposed)  // x is [K, M]: 128x1 groups of x along K are 1x128 groups of A = x^T
       e = launch_quant_tile(kQuantTileCol, xb, K, M, ldx, nullptr, 0, nullptr, 0, (uint8_t*)q, ldq, s, lds, sms,
                             (cudaStream_t)stream);
@@ -130,7 +130,7 @@ bfp8_status bfp8_quant_rhs(const void* x, int64_t K, int64_t N, int64_t ldx, voi
   int sms = 0;
   if ((st = check_device(&sms)) != BFP8_OK) return st;
   cudaError_t e;
-  if (quant_tile_supported(x, ldx))
+  if (quant_tile_supported(x, ldx, nullptr, 0, qT, ldq))
     e = launch_quant_tile(kQuantTileCol, (const uint16_t*)x, K, N, ldx, nullptr, 0, nullptr, 0, (uint8_t*)qT, ldq, s,
                           lds, sms, (cudaStream_t)stream);
   else
@@ -161,7 +161,7 @@ bfp8_status bfp8_quant_weight(const void* w, int64_t N, int64_t K, int64_t ldw, 
   int sms = 0;
   if ((st = check_device(&sms)) != BFP8_OK) return st;
   cudaError_t e;
-  if (quant_tile_supported(w, ldw))
+  if (quant_tile_supported(w, ldw, q, ldq, qt, ldqt))
     e = launch_quant_tile(kQuantTileScale, (const uint16_t*)w, N, K, ldw, (uint8_t*)q, ldq, s, lds, (uint8_t*)qt,
                           ldqt, nullptr, 0, sms, (cudaStream_t)stream);
   else
@@ -190,7 +190,7 @@ bfp8_status bfp8_quant_dual(const void* x, int64_t T, int64_t C, int64_t ldx, vo
   if ((st = check_device(&sms)) != BFP8_OK) return st;
   cudaError_t e;
   const uint16_t* xb = (const uint16_t*)x;
-  if (quant_tile_supported(x, ldx)) {
+  if (quant_tile_supported(x, ldx, q_row, ldq_row, q_col, ldq_col)) {
     e = launch_quant_tile(kQuantTileRow | kQuantTileCol, xb, T, C, ldx, (uint8_t*)q_row, ldq_row, s_row, lds_row,
                           (uint8_t*)q_col, ldq_col, s_col, lds_col, sms, (cudaStream_t)stream);
   } else {
@@ -251,37 +251,6 @@ bfp8_status bfp8_gemm_1x128_128x1(const void* qa, int64_t lda, const float* sa, 
                                   int64_t N, int64_t K, bfp8_stream_t stream) {
   GemmArgs a{qa, lda, sa, ldsa, qb, ldb, sb, ldsb, kSbCol, c, ldc, M, N, K};
   return gemm_common("bfp8_gemm_1x128_128x1", a, stream);
-}
-
-size_t bfp8_gemm_workspace_size(void) {
-  int sms = 0;
-  if (check_device(&sms) != BFP8_OK) return 0;
-  return gemm_workspace_bytes(sms);
-}
-
-static bfp8_status check_gemm_ws(const char* fn, void* ws, size_t ws_bytes) {
-  if (ws == nullptr) return BFP8_OK;
-  CHECK_ARG((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "%s: workspace must be 256-byte aligned", fn);
-  return BFP8_OK;
-}
-
-bfp8_status bfp8_gemm_1x128_128x128_ws(const void* qa, int64_t lda, const float* sa, int64_t ldsa, const void* qb,
-                                       int64_t ldb, const float* sb, int64_t ldsb, int sb_transposed, void* c,
-                                       int64_t ldc, int64_t M, int64_t N, int64_t K, void* ws, size_t ws_bytes,
-                                       bfp8_stream_t stream) {
-  bfp8_status st = check_gemm_ws("bfp8_gemm_1x128_128x128_ws", ws, ws_bytes);
-  if (st != BFP8_OK) return st;
-  GemmArgs a{qa, lda, sa, ldsa, qb, ldb, sb, ldsb, sb_transposed ? kSbTileT : kSbTile, c, ldc, M, N, K, ws, ws_bytes};
-  return gemm_common("bfp8_gemm_1x128_128x128_ws", a, stream);
-}
-
-bfp8_status bfp8_gemm_1x128_128x1_ws(const void* qa, int64_t lda, const float* sa, int64_t ldsa, const void* qb,
-                                     int64_t ldb, const float* sb, int64_t ldsb, void* c, int64_t ldc, int64_t M,
-                                     int64_t N, int64_t K, void* ws, size_t ws_bytes, bfp8_stream_t stream) {
-  bfp8_status st = check_gemm_ws("bfp8_gemm_1x128_128x1_ws", ws, ws_bytes);
-  if (st != BFP8_OK) return st;
-  GemmArgs a{qa, lda, sa, ldsa, qb, ldb, sb, ldsb, kSbCol, c, ldc, M, N, K, ws, ws_bytes};
-  return gemm_common("bfp8_gemm_1x128_128x1_ws", a, stream);
 }
 
 bfp8_status bfp8_debug_gemm_stall(const void* qa, int64_t lda, const float* sa, int64_t ldsa, const void* qb,
@@ -450,10 +419,8 @@ bfp8_status bfp8_linear_bwd(const void* dy, const void* x, const void* w, void* 
 // ---------------------------------------------------------------------------
 
 namespace {
-constexpr int kMaxSmsForLayout = 256;  // the layout reserves stream-K space for up to 256 SMs
 struct TrainLayout {
-  size_t gws, qx, sx, qxt, sxt, qw, qwt, sw, qdy, sdy, qdyt, sdyt, total;
-  size_t gws_bytes;
+  size_t qx, sx, qxt, sxt, qw, qwt, sw, qdy, sdy, qdyt, sdyt, total;
   int64_t ldK, ldN, ldM, ldsM, ldsN, ldsK;
 };
 TrainLayout train_layout(int64_t M, int64_t N, int64_t K) {
@@ -466,8 +433,6 @@ TrainLayout train_layout(int64_t M, int64_t N, int64_t K) {
   L.ldsK = rup(K, 4);
   const int64_t Kb = cdiv(K, kBlock), Nb = cdiv(N, kBlock), Mb = cdiv(M, kBlock);
   size_t o = 0;
-  L.gws_bytes = gemm_workspace_bytes(kMaxSmsForLayout);
-  L.gws = o; o = a256(o + L.gws_bytes);                 // GEMM stream-K flags + partial tiles
   L.qx = o; o = a256(o + (size_t)M * L.ldK);            // x, 1x128 along K (forward lhs)
   L.sx = o; o = a256(o + (size_t)Kb * L.ldsM * 4);
   L.qxt = o; o = a256(o + (size_t)K * L.ldM);           // x, 128x1 along M, transposed (wgrad rhs)
@@ -508,8 +473,8 @@ bfp8_status bfp8_linear_fwd_train(const void* x, const void* w, void* y, int64_t
   if ((st = bfp8_quant_weight(w, N, K, K, b + L.qw, L.ldK, b + L.qwt, L.ldN, (float*)(b + L.sw), Kb, stream)) !=
       BFP8_OK)
     return st;
-  return bfp8_gemm_1x128_128x128_ws(b + L.qx, L.ldK, (const float*)(b + L.sx), L.ldsM, b + L.qw, L.ldK,
-                                    (const float*)(b + L.sw), Kb, 0, y, N, M, N, K, b + L.gws, L.gws_bytes, stream);
+  return bfp8_gemm_1x128_128x128(b + L.qx, L.ldK, (const float*)(b + L.sx), L.ldsM, b + L.qw, L.ldK,
+                                 (const float*)(b + L.sw), Kb, 0, y, N, M, N, K, stream);
 }
 
 bfp8_status bfp8_linear_bwd_saved(const void* dy, void* dx, void* dw, int64_t M, int64_t N, int64_t K, void* ws,
@@ -527,12 +492,11 @@ bfp8_status bfp8_linear_bwd_saved(const void* dy, void* dx, void* dw, int64_t M,
   if ((st = bfp8_quant_dual(dy, M, N, N, b + L.qdy, L.ldN, (float*)(b + L.sdy), L.ldsM, b + L.qdyt, L.ldM,
                             (float*)(b + L.sdyt), L.ldsN, stream)) != BFP8_OK)
     return st;
-  if ((st = bfp8_gemm_1x128_128x128_ws(b + L.qdy, L.ldN, (const float*)(b + L.sdy), L.ldsM, b + L.qwt, L.ldN,
-                                       (const float*)(b + L.sw), Kb, 1, dx, K, M, K, N, b + L.gws, L.gws_bytes,
-                                       stream)) != BFP8_OK)
+  if ((st = bfp8_gemm_1x128_128x128(b + L.qdy, L.ldN, (const float*)(b + L.sdy), L.ldsM, b + L.qwt, L.ldN,
+                                    (const float*)(b + L.sw), Kb, 1, dx, K, M, K, N, stream)) != BFP8_OK)
     return st;
-  return bfp8_gemm_1x128_128x1_ws(b + L.qdyt, L.ldM, (const float*)(b + L.sdyt), L.ldsN, b + L.qxt, L.ldM,
-                                  (const float*)(b + L.sxt), L.ldsK, dw, K, N, K, M, b + L.gws, L.gws_bytes, stream);
+  return bfp8_gemm_1x128_128x1(b + L.qdyt, L.ldM, (const float*)(b + L.sdyt), L.ldsN, b + L.qxt, L.ldM,
+                               (const float*)(b + L.sxt), L.ldsK, dw, K, N, K, M, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -545,6 +509,8 @@ namespace {
 // 1 row scales [Cb, T], 2 column scales [Tb, C], 3 tile scales [Tb, Cb].
 void replay_tile(int64_t T, int64_t C, bool rows_out, bool cols_out, int scale_kind, uint32_t* counts,
                  uint32_t* scounts, int64_t* oob, int sms) {
+  // scale_kind: 0 none, 1 row scales s_row[c/128][t], 2 column scales
+  // s_col[t/128][c], 3 tile scales s_row[t/128][c/128]
   auto hit = [&](uint32_t* arr, int64_t r, int64_t c, int64_t rows, int64_t cols) {
     if (r < 0 || r >= rows || c < 0 || c >= cols) {
       ++*oob;
@@ -557,32 +523,29 @@ void replay_tile(int64_t T, int64_t C, bool rows_out, bool cols_out, int scale_k
   for (int64_t cta = 0; cta < grid; ++cta)
     for (int64_t tile = cta; tile < num_tiles; tile += grid) {
       const int64_t t0 = qt_tile_t0(tile, tiles_c), c0 = qt_tile_c0(tile, tiles_c);
-      if (rows_out || scale_kind == 1)
-        for (int warp = 0; warp < kQtThreads / 32; ++warp)
-          for (int half = 0; half < 2; ++half)
-            for (int l16 = 0; l16 < 16; ++l16)
-              for (int ps = 0; ps < kQtRowPasses; ++ps) {
-                const int64_t t = t0 + qt_rowpass_row(ps, warp, half), c = c0 + qt_rowpass_col(l16);
-                if (t >= T) continue;
-                if (rows_out)
-                  for (int b = 0; b < 8; ++b)
-                    if (c + b < C) hit(counts, t, c + b, T, C);
-                if (scale_kind == 1 && l16 == 0) hit(scounts, c0 / 128, t, Cb, T);
-              }
-      if (cols_out)
-        for (int ch = 0; ch < 128 * 128 / 16; ++ch) {
-          const int64_t cg = c0 + qt_store_col(ch), tg = t0 + qt_store_row(ch);
-          if (cg < C)
-            for (int b = 0; b < 16; ++b)
-              if (tg + b < T) hit(counts, cg, tg + b, C, T);
+      // TMA stores: one 128 x 128 box per output, clipped to the 16-byte-
+      // aligned extent of the inner dimension (C_al for q_row, T_al for q_col)
+      const int64_t C_al = C & ~(int64_t)15, T_al = T & ~(int64_t)15;
+      if (rows_out && c0 < C_al)
+        for (int64_t t = t0; t < t0 + 128 && t < T; ++t)
+          for (int64_t c = c0; c < c0 + 128 && c < C_al; ++c) hit(counts, t, c, T, C);
+      if (cols_out && t0 < T_al)
+        for (int64_t c = c0; c < c0 + 128 && c < C; ++c)
+          for (int64_t t = t0; t < t0 + 128 && t < T_al; ++t) hit(counts, c, t, C, T);
+      for (int tid = 0; tid < kQtThreads; ++tid) {
+        // the ragged bytes past the aligned extents, stored by the threads
+        const int gr = qt_scale_group(tid), b0 = 4 * (tid & 3);
+        for (int b = 0; b < 4; ++b) {
+          if (rows_out && c0 + 128 > C_al && C_al < C && t0 + gr < T && C_al + b0 + b < C)
+            hit(counts, t0 + gr, C_al + b0 + b, T, C);
+          if (cols_out && t0 + 128 > T_al && T_al < T && c0 + gr < C && T_al + b0 + b < T)
+            hit(counts, c0 + gr, T_al + b0 + b, C, T);
         }
-      if (scale_kind == 2)
-        for (int warp = 0; warp < kQtThreads / 32; ++warp)
-          for (int h = 0; h < kQtColChunks; ++h)
-            for (int lane = 0; lane < 8; ++lane) {
-              const int64_t cg = c0 + 8 * qt_colpass_chunk(warp, h) + lane;
-              if (cg < C) hit(scounts, t0 / 128, cg, Tb, C);
-            }
+        if (!qt_scale_writer(tid)) continue;
+        const int g = qt_scale_group(tid);
+        if (scale_kind == 1 && t0 + g < T) hit(scounts, c0 / 128, t0 + g, Cb, T);
+        if (scale_kind == 2 && c0 + g < C) hit(scounts, t0 / 128, c0 + g, Tb, C);
+      }
       if (scale_kind == 3) hit(scounts, t0 / 128, c0 / 128, Tb, Cb);
     }
 }
@@ -682,30 +645,23 @@ bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, i
     }
     return BFP8_OK;
   }
-  if (kind == 3) {  // GEMM output C [M,N]; flag bit 2: launched with a stream-K workspace
+  if (kind == 3) {  // GEMM output C [M,N]
     const int bn = gemm_pick_bn(M, N, sms);
-    const int64_t num_m = cdiv(M, kBM), num_n = cdiv(N, bn), tiles = num_m * num_n;
-    const int64_t grid = gemm_grid(M, N, bn, sms), Kb = cdiv(K, kBK);
-    const bool sk = (flag & 4) && gemm_use_stream_k(M, N, K, bn, sms);
-    const int epi_warps = bn / 32;
-    for (int64_t cta = 0; cta < grid; ++cta) {
-      GemmWork work;
-      work.init(sk, cta, grid, tiles, Kb > 0 ? Kb : 1);
-      GemmSeg seg;
-      while (work.next(seg, Kb > 0 ? Kb : 1)) {
-        if (seg.kb1 == Kb && seg.kb0 > 0) continue;  // hands its partial to the tile's owner; no store
-        const GemmTile g = gemm_tile(seg.tile, num_m, num_n, bn);
-        for (int e = 0; e < epi_warps; ++e)
+    const int num_m = (int)cdiv(M, kBM), num_n = (int)cdiv(N, bn), tiles = num_m * num_n;
+    const int grid = (int)gemm_grid(M, N, bn, sms);
+    for (int cta = 0; cta < grid; ++cta)
+      for (int tile = cta; tile < tiles; tile += grid) {
+        const GemmTile g = gemm_tile(tile, num_m, num_n, bn);
+        for (int e = 0; e < kGemmEpiWarps; ++e)
           for (int lane = 0; lane < 32; ++lane) {
             const int64_t m = g.m0 + epi_row(e, lane);
             if (m >= M) continue;
-            for (int c = 0; c < 128; ++c) {
-              const int64_t n = g.n0 + epi_col0(e) + c;
+            for (int c = 0; c < epi_cols(bn); ++c) {
+              const int64_t n = g.n0 + epi_col0(e, bn) + c;
               if (n < N) hit(counts, m, n, M, N);
             }
           }
       }
-    }
     return BFP8_OK;
   }
   return fail(BFP8_ERR_INVALID_ARG, "bfp8_debug_write_counts: unknown kind %d", kind);

@@ -14,12 +14,15 @@
 //               tcgen05.commit to release the smem stage and publish the partial.
 //   warps 2-3   idle (they complete the control warpgroup, which gives its
 //               registers to the promotion warpgroups with setmaxnreg).
-//   warps 4..   promotion/epilogue (BN/32 warps): tcgen05.ld the K-block's
-//               fp32 partial, acc += (a_s*b_s) * partial in registers, release
-//               the tensor-memory buffer; at tile end round to bf16 and store
-//               only rows m < M and columns n < N.
+//   warps 4..19 promotion/epilogue, four per tensor-memory lane quarter, each
+//               owning 32 rows x BN/4 columns of the tile: tcgen05.ld the
+//               K-block's fp32 partial, release the tensor-memory buffer,
+//               acc += (a_s*b_s) * partial in registers; at tile end round to
+//               bf16 and store only rows m < M and columns n < N.
 // The two tensor-memory buffers let the promotion of K-block kb overlap the
-// MMAs of K-block kb+1.  Tails: TMA zero-fills rows/columns outside M, N, K;
+// MMAs of K-block kb+1.  A warp moves only about 30 bytes per cycle out of
+// tensor memory, so sixteen warps are needed to read a 128 x 256 fp32 partial
+// (128 KiB) in less time than the MMAs of the next K-block take (512 cycles).  Tails: TMA zero-fills rows/columns outside M, N, K;
 // scale loads are predicated; the epilogue store is masked.
 // Every mbarrier wait is bounded in time; a timeout records an error bit,
 // lets every role leave its loop, waits for its own copies/MMAs in flight and
@@ -43,7 +46,6 @@ enum : uint32_t {
   kErrWaitTmemEmpty = 1u << 2,  // MMA: a tensor-memory buffer was never released
   kErrWaitTmemFull = 1u << 3,   // epilogue: a partial product never arrived
   kErrWaitDrain = 1u << 4,      // teardown: MMAs or copies in flight never finished
-  kErrWaitPartial = 1u << 5,    // stream-K: a neighbouring CTA's partial tile never arrived
 };
 
 struct GemmParams {
@@ -54,39 +56,36 @@ struct GemmParams {
   uint16_t* c;
   int64_t ldc;
   int64_t M, N, K;
-  int64_t num_m, num_n, num_tiles, Kb, Nb;
+  int num_m, num_n, num_tiles, Kb, Nb;  // below 2^31, as is num_tiles * Kb (checked by the host)
   int c_vec;   // 16-byte output stores allowed (ldc % 8 == 0, c 16-byte aligned)
   int c_tma;   // C written by TMA stores through shared memory (same conditions)
   int sb_vec;  // 16-byte column-scale loads allowed (ldsb % 4 == 0, sb 16-byte aligned)
   uint64_t wait_limit_ns;
   int debug_stall;  // test hook: the promotion warps wait on a barrier nothing arrives on
-  int stream_k;     // split the (tile, K-block) units evenly over the CTAs
-  float* partials;  // stream-K: one BM x BN fp32 partial tile per CTA
-  uint32_t* flags;  // stream-K: flags[cta] = 1 once CTA cta's partial is written
 };
 
 template <int BN, int STAGES>
 struct GemmCfg {
-  static constexpr int kEpiWarps = BN / 32;  // 4 warps (128 rows) per 128 columns
+  static constexpr int kEpiWarps = kGemmEpiWarps;  // 16: four per tensor-memory lane quarter
+  static constexpr int kCols = BN / 4;             // tile columns per promotion warp
   static constexpr int kThreads = 128 + 32 * kEpiWarps;
-  // Register split (BN = 256: 384 threads launched at 168 registers each):
-  // the control warpgroup drops to 40, the two promotion warpgroups rise to
-  // 224; 128*40 + 256*224 = 62464 <= 384*168 = 64512.
-  static constexpr bool kSplitRegs = (kThreads > 256);
-  static constexpr int kCtrlRegs = 40;
-  static constexpr int kEpiRegs = 224;
+  // Register split: 640 threads launched at 96 registers each (61440); the
+  // control warpgroup drops to 32 and the four promotion warpgroups rise to
+  // 112: 128*32 + 512*112 = 61440.
+  static constexpr int kCtrlRegs = 32;
+  static constexpr int kEpiRegs = 112;
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;  // two fp32 partial buffers of BN columns
   static constexpr int kOffB = STAGES * kABytes;
-  // per promotion warp: a 4 KiB buffer (32 rows x 64 bf16 columns, 128-byte
+  // per promotion warp: a 2 KiB buffer (32 rows x 32 bf16 columns, 64-byte
   // swizzled) that stages C for the TMA store at tile end, and holds the
-  // K-block's 128 column scales (128x1 mode) during the K loop
-  static constexpr int kStageC = 32 * 64 * 2;
+  // K-block's column scales (128x1 mode) during the K loop
+  static constexpr int kStageC = 32 * 32 * 2;
   static constexpr int kOffSb = kOffB + STAGES * kBBytes;
   static constexpr int kOffBar = kOffSb + kEpiWarps * kStageC;
-  static constexpr int kNumBars = 2 * STAGES + 8;
+  static constexpr int kNumBars = 2 * STAGES + 6;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -100,7 +99,7 @@ __device__ __forceinline__ void gemm_fail(uint32_t code, volatile int* abort_fla
 }
 
 template <int BN, int STAGES, int SB_MODE, int LDW>
-__global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tma_a,
                           const __grid_constant__ CUtensorMap tma_b,
                           const __grid_constant__ CUtensorMap tma_c, const GemmParams p) {
@@ -124,9 +123,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
   auto tempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + 2 + i); };
   const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
   const uint32_t stall_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 5);  // never arrived on
-  // stream-K hand-offs among the promotion warps (each used at most once per CTA)
-  const uint32_t skc_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 6);  // partial written
-  const uint32_t sko_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 7);  // neighbour's partial consumed
 
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const int lane = (int)(threadIdx.x & 31);
@@ -142,8 +138,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
     }
     mbar_init(drain_bar, 1);
     mbar_init(stall_bar, 1);
-    mbar_init(skc_bar, Cfg::kEpiWarps);
-    mbar_init(sko_bar, Cfg::kEpiWarps);
     *abort_flag = 0;
     *never = 0;
     fence_barrier_init();
@@ -162,36 +156,31 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   if (warp < 4) {
-    if (Cfg::kSplitRegs) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kCtrlRegs));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kCtrlRegs));
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int64_t it = 0;
+      uint32_t it = 0;
       bool ok = true;
-      GemmWork work;
-      work.init(p.stream_k, blockIdx.x, gridDim.x, p.num_tiles, p.Kb);
-      GemmSeg seg;
-      while (ok && work.next(seg, p.Kb)) {
-        const GemmTile g = gemm_tile(seg.tile, p.num_m, p.num_n, BN);
-        for (int64_t kb = seg.kb0; kb < seg.kb1; ++kb, ++it) {
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+        for (int kb = 0; kb < p.Kb; ++kb, ++it) {
           const int st = (int)(it % STAGES);
-          const uint32_t ph = (uint32_t)((it / STAGES) & 1);
+          const uint32_t ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(empty_bar(st), ph ^ 1u, p.wait_limit_ns, abort_flag)) {
             gemm_fail(kErrWaitEmpty, abort_flag);
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(full_bar(st), (uint32_t)Cfg::kStageBytes);
-          tma_load_2d(sA + (uint32_t)(st * Cfg::kABytes), &tma_a, full_bar(st), (int32_t)(kb * kBK),
-                      (int32_t)g.m0);
-          tma_load_2d(sB + (uint32_t)(st * Cfg::kBBytes), &tma_b, full_bar(st), (int32_t)(kb * kBK),
-                      (int32_t)g.n0);
+          tma_load_2d(sA + (uint32_t)(st * Cfg::kABytes), &tma_a, full_bar(st), kb * kBK, g.m0);
+          tma_load_2d(sB + (uint32_t)(st * Cfg::kBBytes), &tma_b, full_bar(st), kb * kBK, g.n0);
         }
       }
       if (!ok) {
         // copies already issued must land before this CTA's smem goes away
-        for (int64_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
-          if (!mbar_wait_bounded(full_bar((int)(j % STAGES)), (uint32_t)((j / STAGES) & 1),
+        for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+          if (!mbar_wait_bounded(full_bar((int)(j % STAGES)), (j / STAGES) & 1u,
                                  p.wait_limit_ns, never))
             atomicOr(&g_gemm_error, kErrWaitDrain);
       }
@@ -200,17 +189,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
-      int64_t it = 0;
+      uint32_t it = 0;
       bool ok = true;
-      GemmWork work;
-      work.init(p.stream_k, blockIdx.x, gridDim.x, p.num_tiles, p.Kb);
-      GemmSeg seg;
-      while (ok && work.next(seg, p.Kb)) {
-        for (int64_t kb = seg.kb0; kb < seg.kb1; ++kb, ++it) {
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        for (int kb = 0; kb < p.Kb; ++kb, ++it) {
           const int st = (int)(it % STAGES);
-          const uint32_t ph = (uint32_t)((it / STAGES) & 1);
-          const int buf = (int)(it & 1);
-          const uint32_t tph = (uint32_t)((it >> 1) & 1);
+          const uint32_t ph = (it / STAGES) & 1u;
+          const int buf = (int)(it & 1u);
+          const uint32_t tph = (it >> 1) & 1u;
           if (!mbar_spin_bounded(tempty_bar(buf), tph ^ 1u, p.wait_limit_ns, abort_flag)) {
             gemm_fail(kErrWaitTmemEmpty, abort_flag);
             ok = false;
@@ -239,34 +225,33 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
     }
   }
   } else {
-    if (Cfg::kSplitRegs) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::kEpiRegs));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::kEpiRegs));
     // ------------------------------------------------------------ promotion + epilogue
     const int e = warp - 4;
+    constexpr int kCols = Cfg::kCols;
     const int row = epi_row(e, lane);
-    const int col0 = epi_col0(e);
+    const int col0 = epi_col0(e, BN);
     const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
     uint8_t* cbuf = cstage + e * Cfg::kStageC;
     const uint32_t cbuf_s = smem_u32(cbuf);
     float* slot = reinterpret_cast<float*>(cbuf);
-    int64_t it = 0;
+    uint32_t it = 0;
     bool ok = true;
-    GemmWork work;
-    work.init(p.stream_k, blockIdx.x, gridDim.x, p.num_tiles, p.Kb);
-    GemmSeg seg;
-    while (ok && work.next(seg, p.Kb)) {
-      const GemmTile g = gemm_tile(seg.tile, p.num_m, p.num_n, BN);
-      const int64_t m = g.m0 + row;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+      const int m = g.m0 + row;
       const bool m_ok = m < p.M;
-      const int64_t nb = (g.n0 + col0) / kBlock;  // B tile-scale block of these 128 columns
-      const int64_t ncol = g.n0 + col0 + 4 * lane;  // first of this lane's 4 column scales
+      const int nb = (g.n0 + col0) / kBlock;  // B tile-scale block of this warp's columns
+      const int ncol = g.n0 + col0 + 4 * lane;  // first of this lane's 4 column scales
 
-      auto load_sa = [&](int64_t kb) -> float { return m_ok ? __ldg(p.sa + kb * p.ldsa + m) : 0.0f; };
-      auto load_sb_tile = [&](int64_t kb) -> float {
+      auto load_sa = [&](int kb) -> float { return m_ok ? __ldg(p.sa + (int64_t)kb * p.ldsa + m) : 0.0f; };
+      auto load_sb_tile = [&](int kb) -> float {
         if (nb >= p.Nb) return 0.0f;
-        return SB_MODE == kSbTile ? __ldg(p.sb + nb * p.ldsb + kb) : __ldg(p.sb + kb * p.ldsb + nb);
+        return SB_MODE == kSbTile ? __ldg(p.sb + (int64_t)nb * p.ldsb + kb) : __ldg(p.sb + (int64_t)kb * p.ldsb + nb);
       };
-      auto load_sb_col = [&](int64_t kb) -> float4 {
-        const float* src = p.sb + kb * p.ldsb + ncol;
+      auto load_sb_col = [&](int kb) -> float4 {
+        if (lane >= kCols / 4) return make_float4(0.f, 0.f, 0.f, 0.f);  // lanes beyond this warp's columns
+        const float* src = p.sb + (int64_t)kb * p.ldsb + ncol;
         if (p.sb_vec && ncol + 4 <= p.N) return __ldg(reinterpret_cast<const float4*>(src));
         float4 r;
         r.x = (ncol + 0 < p.N) ? __ldg(src + 0) : 0.0f;
@@ -276,30 +261,30 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
         return r;
       };
 
-      float acc[128];
+      float acc[kCols];
 #pragma unroll
-      for (int j = 0; j < 128; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < kCols; ++j) acc[j] = 0.0f;
       if (SB_MODE == kSbCol && p.c_tma) {  // the staging buffer doubles as the scale slot
         if (lane == 0) bulk_wait_read_all();
         __syncwarp();
       }
 
-      float sa_next = load_sa(seg.kb0);
+      float sa_next = load_sa(0);
       float sb_next = 0.0f;
       float4 sbc_next = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (SB_MODE == kSbCol) sbc_next = load_sb_col(seg.kb0);
-      else sb_next = load_sb_tile(seg.kb0);
+      if (SB_MODE == kSbCol) sbc_next = load_sb_col(0);
+      else sb_next = load_sb_tile(0);
 
-      for (int64_t kb = seg.kb0; kb < seg.kb1; ++kb, ++it) {
+      for (int kb = 0; kb < p.Kb; ++kb, ++it) {
         const float sa_cur = sa_next, sb_cur = sb_next;
         const float4 sbc_cur = sbc_next;
-        if (kb + 1 < seg.kb1) {  // prefetch the next K-block's scales (masked loads)
+        if (kb + 1 < p.Kb) {  // prefetch the next K-block's scales (masked loads)
           sa_next = load_sa(kb + 1);
           if (SB_MODE == kSbCol) sbc_next = load_sb_col(kb + 1);
           else sb_next = load_sb_tile(kb + 1);
         }
-        const int buf = (int)(it & 1);
-        const uint32_t tph = (uint32_t)((it >> 1) & 1);
+        const int buf = (int)(it & 1u);
+        const uint32_t tph = (it >> 1) & 1u;
         const bool got = mbar_wait_bounded(p.debug_stall ? stall_bar : tfull_bar(buf), tph, p.wait_limit_ns,
                                            abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
@@ -310,21 +295,23 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
         tc_fence_after();
         if (SB_MODE == kSbCol) {
           __syncwarp();
-          reinterpret_cast<float4*>(slot)[lane] = sbc_cur;
+          if (lane < kCols / 4) reinterpret_cast<float4*>(slot)[lane] = sbc_cur;
           __syncwarp();
         }
         const uint32_t taddr = tmem_base + lane_base + (uint32_t)(buf * BN + col0);
         const float scale = sa_cur * sb_cur;
         // LDW columns of the partial per tensor-memory load round trip (one wait)
 #pragma unroll
-        for (int c = 0; c < 128 / LDW; ++c) {
+        for (int c = 0; c < kCols / LDW; ++c) {
           uint32_t r[LDW];
-#pragma unroll
-          for (int h = 0; h < LDW / 32; ++h)
-            tmem_ld_32x32b_x32(taddr + (uint32_t)(LDW * c + 32 * h), *reinterpret_cast<uint32_t(*)[32]>(&r[32 * h]));
+          if constexpr (LDW == 32)
+            tmem_ld_32x32b_x32(taddr + (uint32_t)(LDW * c), r);
+          else
+            tmem_ld_32x32b_x16(taddr + (uint32_t)(LDW * c), r);
           tmem_ld_wait();
-          if (c == 128 / LDW - 1) {
-            // the whole partial is in registers: hand the buffer back to the MMA warp now
+          tmem_regs_after_wait(r);
+          if (c == kCols / LDW - 1) {
+            // this warp's share of the partial is in registers: release the buffer
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tempty_bar(buf));
@@ -352,82 +339,38 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES>::kThreads, 1)
       }
       if (!ok) break;
 
-      if (seg.kb1 == p.Kb && seg.kb0 > 0) {
-        // stream-K, this CTA finished the tile's last K-blocks first: leave the
-        // partial sums for the CTA that computes its first K-blocks, then move on
-        float* dst = p.partials + (size_t)blockIdx.x * (kBM * BN) + (size_t)row * BN + col0;
-#pragma unroll
-        for (int j = 0; j < 128; j += 4)
-          *reinterpret_cast<float4*>(dst + j) = make_float4(acc[j], acc[j + 1], acc[j + 2], acc[j + 3]);
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(skc_bar);
-        if (e == 0 && lane == 0) {  // publish once every promotion warp has written its rows
-          if (mbar_wait_bounded(skc_bar, 0, p.wait_limit_ns, abort_flag)) st_release_gpu(p.flags + blockIdx.x, 1u);
-          else gemm_fail(kErrWaitPartial, abort_flag);
-        }
-        continue;
-      }
-      if (seg.kb0 == 0 && seg.kb1 < p.Kb) {
-        // stream-K, this CTA computed the tile's first K-blocks last: add the
-        // next CTA's partial sums (written at that CTA's start) before storing
-        const uint32_t* flag = p.flags + blockIdx.x + 1;
-        bool got = true;
-        if (lane == 0) got = spin_flag_bounded(flag, p.wait_limit_ns, abort_flag);
-        if (!__shfl_sync(0xffffffffu, (int)got, 0)) {
-          if (lane == 0) gemm_fail(kErrWaitPartial, abort_flag);
-          ok = false;
-          break;
-        }
-        (void)ld_acquire_gpu(flag);  // order this lane's loads after the flag
-        const float* src = p.partials + (size_t)(blockIdx.x + 1) * (kBM * BN) + (size_t)row * BN + col0;
-#pragma unroll
-        for (int j = 0; j < 128; j += 4) {
-          const float4 v = *reinterpret_cast<const float4*>(src + j);
-          acc[j] += v.x;
-          acc[j + 1] += v.y;
-          acc[j + 2] += v.z;
-          acc[j + 3] += v.w;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sko_bar);
-        if (e == 0 && lane == 0) {  // every promotion warp has read it: clear for the next launch
-          if (mbar_wait_bounded(sko_bar, 0, p.wait_limit_ns, abort_flag)) st_relaxed_gpu(const_cast<uint32_t*>(flag), 0u);
-          else gemm_fail(kErrWaitPartial, abort_flag);
-        }
-      }
-
       if (p.c_tma) {
-        // two 32x64 bf16 slices through the swizzled staging buffer, each
+        // 32x32 bf16 slices through the staging buffer (64-byte swizzle: the
+        // 16-byte chunk k of row r sits at chunk k ^ ((r >> 1) & 3)), each
         // written by one TMA store (rows/columns outside [M, N] are dropped)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
+        for (int h = 0; h < kCols / 32; ++h) {
           if (lane == 0) bulk_wait_read_all();  // previous store has read the buffer
           __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
+          for (int j = 0; j < 4; ++j) {
             uint32_t w[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              w[q] = pack_bf16x2(acc[64 * h + 8 * j + 2 * q], acc[64 * h + 8 * j + 2 * q + 1]);
-            const uint32_t addr = cbuf_s + (uint32_t)(lane * 128 + ((j ^ (lane & 7)) << 4));
+              w[q] = pack_bf16x2(acc[32 * h + 8 * j + 2 * q], acc[32 * h + 8 * j + 2 * q + 1]);
+            const uint32_t addr = cbuf_s + (uint32_t)(lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4));
             asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
                          "r"(w[3])
                          : "memory");
           }
           fence_proxy_async_shared();
           __syncwarp();
-          const int64_t xs = g.n0 + col0 + 64 * h, ys = g.m0 + 32 * (warp % 4);
+          const int xs = g.n0 + col0 + 32 * h, ys = g.m0 + 32 * (warp % 4);
           if (lane == 0 && xs < p.N && ys < p.M) {  // a slice wholly outside C is not issued
-            tma_store_2d(&tma_c, cbuf_s, (int32_t)xs, (int32_t)ys);
+            tma_store_2d(&tma_c, cbuf_s, xs, ys);
             bulk_commit();
           }
         }
       } else if (m_ok) {
-        uint16_t* crow = p.c + m * p.ldc;
+        uint16_t* crow = p.c + (int64_t)m * p.ldc;
 #pragma unroll
-        for (int c8 = 0; c8 < 16; ++c8) {
-          const int64_t n = g.n0 + col0 + 8 * c8;
+        for (int c8 = 0; c8 < kCols / 8; ++c8) {
+          const int n = g.n0 + col0 + 8 * c8;
           if (n >= p.N) break;
           uint32_t w[4];
 #pragma unroll
@@ -489,16 +432,16 @@ static bool make_tma_u8(CUtensorMap* map, const void* base, int64_t inner, int64
 }
 
 // Row-major [rows, cols] bf16 output with row stride ld elements; box of
-// 64 columns x 32 rows (one promotion warp's slice), 128-byte swizzle.
+// 32 columns x 32 rows (one promotion warp's slice), 64-byte swizzle.
 static bool make_tma_bf16_store(CUtensorMap* map, void* base, int64_t cols, int64_t rows, int64_t ld) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {64, 32};
+  cuuint32_t box[2] = {32, 32};
   cuuint32_t elem[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -513,7 +456,7 @@ int64_t gemm_grid(int64_t M, int64_t N, int bn, int num_sms) {
   return tiles < num_sms ? tiles : num_sms;
 }
 
-template <int BN, int STAGES, int MODE, int LDW = 32>
+template <int BN, int STAGES, int MODE, int LDW = 16>
 static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                             const GemmParams& p, int64_t grid, cudaStream_t st) {
   using Cfg = GemmCfg<BN, STAGES>;
@@ -526,19 +469,6 @@ static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const 
   if (attr_err != cudaSuccess) return attr_err;
   gemm_blockwise_kernel<BN, STAGES, MODE, LDW><<<(unsigned)grid, Cfg::kThreads, Cfg::kSmemBytes, st>>>(ma, mb, mc, p);
   return cudaGetLastError();
-}
-
-bool gemm_use_stream_k(int64_t M, int64_t N, int64_t K, int bn, int num_sms) {
-  const int64_t tiles = cdiv(M, kBM) * cdiv(N, bn), Kb = cdiv(K, kBK);
-  const int64_t grid = gemm_grid(M, N, bn, num_sms);
-  if (grid < num_sms) return false;                       // fewer tiles than SMs: nothing to balance
-  if (tiles * Kb / grid < Kb) return false;               // a tile would span three CTAs
-  const double eff = (double)tiles / (double)(cdiv(tiles, grid) * grid);
-  return eff < 0.95;
-}
-
-size_t gemm_workspace_bytes(int num_sms) {
-  return kGemmFlagBytes + (size_t)num_sms * kBM * 256 * sizeof(float);
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const char** msg,
@@ -559,28 +489,32 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const c
   p.M = a.M;
   p.N = a.N;
   p.K = a.K;
-  p.num_m = cdiv(a.M, kBM);
-  p.num_n = cdiv(a.N, bn);
-  p.num_tiles = p.num_m * p.num_n;
-  p.Kb = cdiv(a.K, kBK);
-  p.Nb = cdiv(a.N, kBlock);
+  const int64_t num_m = cdiv(a.M, kBM), num_n = cdiv(a.N, bn), Kb = cdiv(a.K, kBK);
+  if (a.M >= (int64_t)1 << 31 || a.N >= (int64_t)1 << 31 || a.K >= (int64_t)1 << 31 ||
+      num_m * num_n * Kb >= (int64_t)1 << 31) {
+    *msg = "GEMM too large: M, N, K and the number of (tile, K-block) units must stay below 2^31";
+    return cudaErrorInvalidValue;
+  }
+  p.num_m = (int)num_m;
+  p.num_n = (int)num_n;
+  p.num_tiles = (int)(num_m * num_n);
+  p.Kb = (int)Kb;
+  p.Nb = (int)cdiv(a.N, kBlock);
   p.c_vec = (a.ldc % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.c) & 15u) == 0);
   p.sb_vec = (a.ldsb % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.sb) & 15u) == 0);
   CUtensorMap mc;
-  p.c_tma = p.c_vec && make_tma_bf16_store(&mc, a.c, a.N, a.M, a.ldc);
+  // a TMA store clips the inner dimension in 16-byte units: only rows of whole
+  // 16-byte units (N % 8 == 0) keep the padding past N untouched
+  p.c_tma = p.c_vec && a.N % 8 == 0 && make_tma_bf16_store(&mc, a.c, a.N, a.M, a.ldc);
   if (!p.c_tma) memset(&mc, 0, sizeof(mc));
   p.wait_limit_ns = wait_limit_ns;
   p.debug_stall = debug_stall;
-  p.stream_k = a.ws != nullptr && a.ws_bytes >= gemm_workspace_bytes(num_sms) &&
-               gemm_use_stream_k(a.M, a.N, a.K, bn, num_sms);
-  p.flags = reinterpret_cast<uint32_t*>(a.ws);
-  p.partials = a.ws ? reinterpret_cast<float*>(static_cast<uint8_t*>(a.ws) + kGemmFlagBytes) : nullptr;
   const int64_t grid = gemm_grid(a.M, a.N, bn, num_sms);
   if (bn == 256) {
     switch (a.sb_mode) {
-      case kSbTile: return run_gemm<256, 4, kSbTile, 64>(ma, mb, mc, p, grid, st);
-      case kSbTileT: return run_gemm<256, 4, kSbTileT, 64>(ma, mb, mc, p, grid, st);
-      default: return run_gemm<256, 4, kSbCol, 64>(ma, mb, mc, p, grid, st);
+      case kSbTile: return run_gemm<256, 4, kSbTile, 32>(ma, mb, mc, p, grid, st);
+      case kSbTileT: return run_gemm<256, 4, kSbTileT, 32>(ma, mb, mc, p, grid, st);
+      default: return run_gemm<256, 4, kSbCol, 16>(ma, mb, mc, p, grid, st);
     }
   }
   switch (a.sb_mode) {

@@ -92,15 +92,13 @@ BFP8_HD int64_t w_tstore_n(const WTile& t, int ch) { return t.nb * kBlock + (ch 
 // ---------------------------------------------------------------------------
 // TMA-staged tile quantisation: persistent CTAs (two per SM, 16 warps each)
 // over 128x128 tiles of a [T, C] input, tile index = blockIdx.x + k * gridDim.x,
-// walked C-fastest.  Row pass: 16 threads per tile row, thread lane16 owns
-// columns 8*lane16..+7, pass ps (0..3) of warp w covers row 32*ps + 2*w + half.
-// Column pass: warp w owns 8-column chunk w, lane l owns rows l + 32*i.  The
-// transposed tile is stored as 16-byte chunks: chunk ch -> column ch/8,
-// rows 16*(ch%8)..+15.
+// walked C-fastest.  Warp w owns the 8-column chunk w of the tile, lane l the
+// rows 4l..4l+3.  Scales: thread tid joins the maximum of row / column
+// qt_scale_group(tid) of the tile (four threads each), and the thread with
+// qt_scale_writer(tid) stores its scale.  Codes leave by one TMA store per
+// output and tile (a 128 x 128-byte box, clipped to the tensor).
 // ---------------------------------------------------------------------------
 constexpr int kQtThreads = 512;
-constexpr int kQtRowPasses = 4;     // tile rows per thread in the row pass
-constexpr int kQtColChunks = 1;     // 8-column chunks per warp in the column pass
 constexpr int kQtCtasPerSm = 2;
 
 BFP8_HD int64_t qt_grid(int64_t num_tiles, int num_sms) {
@@ -109,12 +107,8 @@ BFP8_HD int64_t qt_grid(int64_t num_tiles, int num_sms) {
 }
 BFP8_HD int64_t qt_tile_t0(int64_t tile, int64_t tiles_c) { return (tile / tiles_c) * 128; }
 BFP8_HD int64_t qt_tile_c0(int64_t tile, int64_t tiles_c) { return (tile % tiles_c) * 128; }
-BFP8_HD int qt_rowpass_row(int ps, int warp, int half) { return 32 * ps + 2 * warp + half; }
-BFP8_HD int qt_rowpass_col(int lane16) { return 8 * lane16; }
-BFP8_HD int qt_colpass_chunk(int warp, int h) { return warp + 16 * h; }
-BFP8_HD int qt_colpass_row(int lane, int i) { return lane + 32 * i; }
-BFP8_HD int qt_store_col(int ch) { return ch / 8; }
-BFP8_HD int qt_store_row(int ch) { return 16 * (ch % 8); }
+BFP8_HD int qt_scale_group(int tid) { return tid >> 2; }
+BFP8_HD bool qt_scale_writer(int tid) { return (tid & 3) == 0; }
 
 // ---------------------------------------------------------------------------
 // GEMM: persistent CTAs over BM x BN output tiles.
@@ -122,75 +116,33 @@ BFP8_HD int qt_store_row(int ch) { return 16 * (ch % 8); }
 constexpr int kBM = 128;
 constexpr int kBK = 128;          // one scale block per pipeline stage
 constexpr int kGroupM = 16;       // tile rasterisation: bands of 16 M-blocks
-constexpr size_t kGemmFlagBytes = 4096;  // stream-K workspace: per-CTA flags, then partial tiles
 
 struct GemmTile {
-  int64_t m0, n0;
+  int m0, n0;
 };
 
 // Output tile of linear tile index `t`: tiles are walked N-fastest inside
 // bands of kGroupM M-blocks so that concurrently running CTAs share A rows
-// and B columns in L2.
-BFP8_HD GemmTile gemm_tile(int64_t t, int64_t num_m, int64_t num_n, int bn) {
-  const int64_t per_band = (int64_t)kGroupM * num_n;
-  const int64_t band = t / per_band;
-  const int64_t first_m = band * kGroupM;
-  const int64_t rows = (num_m - first_m) < kGroupM ? (num_m - first_m) : kGroupM;
-  const int64_t r = t % per_band;
+// and B columns in L2.  (Sizes are below 2^31; the host checks.)
+BFP8_HD GemmTile gemm_tile(int t, int num_m, int num_n, int bn) {
+  const int per_band = kGroupM * num_n;
+  const int band = t / per_band;
+  const int first_m = band * kGroupM;
+  const int rows = (num_m - first_m) < kGroupM ? (num_m - first_m) : kGroupM;
+  const int r = t % per_band;
   GemmTile g;
   g.m0 = (first_m + r % rows) * kBM;
   g.n0 = (r / rows) * bn;
   return g;
 }
 
-// Work of one persistent CTA, as segments (tile, K-blocks [kb0, kb1)).
-// Tile-parallel: tiles cta, cta + grid, ... each with all K-blocks.
-// Stream-K: the units (tile, K-block) in tile-major order are split into
-// `grid` equal contiguous ranges; a CTA's range may begin inside one tile
-// (finishing it: kb0 > 0, kb1 = Kb) and end inside another (starting it:
-// kb0 = 0, kb1 < Kb).  The host enables stream-K only when every range holds
-// at least Kb units, so a tile is split between at most two CTAs.
-struct GemmSeg {
-  int64_t tile;
-  int kb0, kb1;
-};
-struct GemmWork {
-  int64_t a, b, step;  // tile-parallel: next tile, tile count, stride; stream-K: next unit, end, Kb
-  bool sk;
-  BFP8_HD void init(bool stream_k, int64_t cta, int64_t grid, int64_t num_tiles, int64_t Kb) {
-    sk = stream_k;
-    if (sk) {
-      const int64_t units = num_tiles * Kb;
-      a = units * cta / grid;
-      b = units * (cta + 1) / grid;
-      step = Kb;
-    } else {
-      a = cta;
-      b = num_tiles;
-      step = grid;
-    }
-  }
-  BFP8_HD bool next(GemmSeg& s, int64_t Kb) {
-    if (a >= b) return false;
-    if (sk) {
-      s.tile = a / Kb;
-      s.kb0 = (int)(a % Kb);
-      const int64_t left = b - a;
-      s.kb1 = (int)((Kb - s.kb0) < left ? Kb : s.kb0 + left);
-      a += s.kb1 - s.kb0;
-    } else {
-      s.tile = a;
-      s.kb0 = 0;
-      s.kb1 = (int)Kb;
-      a += step;
-    }
-    return true;
-  }
-};
-
-// Epilogue warp e (0-based among the epilogue warps; CTA warp id = e + 4):
-// tensor-memory lane quarter = CTA warp id % 4, column half = e / 4.
-BFP8_HD int epi_row(int e, int lane) { return 32 * ((e + 4) % 4) + lane; }
-BFP8_HD int epi_col0(int e) { return 128 * (e / 4); }
+// Promotion / epilogue warp e (0-based, CTA warp id = e + 4): tensor-memory
+// lane quarter e % 4 (the quarter a warp may access is its CTA warp id % 4),
+// column block e / 4 of BN/4 columns.
+constexpr int kGemmEpiWarps = 16;
+constexpr int kGemmThreads = 128 + 32 * kGemmEpiWarps;
+BFP8_HD int epi_row(int e, int lane) { return 32 * (e % 4) + lane; }
+BFP8_HD int epi_cols(int bn) { return bn / 4; }
+BFP8_HD int epi_col0(int e, int bn) { return epi_cols(bn) * (e / 4); }
 
 }  // namespace bfp8

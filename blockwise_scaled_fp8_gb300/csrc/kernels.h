@@ -23,7 +23,9 @@ cudaError_t launch_cast(const float* x, int64_t n, uint8_t* q, int num_sms, cuda
 
 // TMA-staged tile quantisation (quant_tile.cu): which outputs one read makes.
 enum : int { kQuantTileRow = 1, kQuantTileCol = 2, kQuantTileScale = 4 };
-bool quant_tile_supported(const void* x, int64_t ldx);
+// x: 16-byte aligned, ldx % 8 == 0; each non-null output: 16-byte aligned, ld % 16 == 0
+bool quant_tile_supported(const void* x, int64_t ldx, const void* q_row, int64_t ldq_row, const void* q_col,
+                          int64_t ldq_col);
 cudaError_t launch_quant_tile(int mode, const uint16_t* x, int64_t T, int64_t C, int64_t ldx, uint8_t* q_row,
                               int64_t ldq_row, float* s_row, int64_t lds_row, uint8_t* q_col, int64_t ldq_col,
                               float* s_col, int64_t lds_col, int num_sms, cudaStream_t st);
@@ -44,18 +46,12 @@ struct GemmArgs {
   void* c;
   int64_t ldc;
   int64_t M, N, K;
-  void* ws = nullptr;   // optional stream-K workspace (flags zeroed before first use)
-  size_t ws_bytes = 0;
 };
 
 // Returns cudaSuccess or the launch error; *msg gets a static description of
 // a host-side failure (tensor-map encoding) when the return is not success.
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const char** msg,
                         uint64_t wait_limit_ns = kWaitLimitNs, int debug_stall = 0);
-// Whether a launch with a workspace splits its (tile, K-block) units evenly
-// over the CTAs (stream-K), and the workspace that needs.
-bool gemm_use_stream_k(int64_t M, int64_t N, int64_t K, int bn, int num_sms);
-size_t gemm_workspace_bytes(int num_sms);
 // Tile width the launcher picks for an M x N output, and the grid it uses.
 int gemm_pick_bn(int64_t M, int64_t N, int num_sms);
 int64_t gemm_grid(int64_t M, int64_t N, int bn, int num_sms);

@@ -10,12 +10,32 @@
 //              q_col[c*ldq_col + t], s_col[(t/128)*lds_col + c]
 //   kTileScale one scale per 128x128 tile: q_row and/or q_col (either may
 //              be null), s_row[(t/128)*lds_row + c/128]
-// The input [T, C] (row stride ldx) is read by TMA as two 64-column boxes per
-// tile with 128-byte swizzling into a two-stage ring per CTA; persistent CTAs
-// (two per SM) walk the tiles, so the next tile's load overlaps this tile's
-// arithmetic.  Rows / columns outside [T, C] arrive as zeros (TMA fill) and
-// every store is masked to the logical tensor.
+//
+// Data flow of one tile (persistent CTAs, two per SM, 16 warps each):
+//   1. TMA loads the tile as two 64-column boxes (128-byte swizzle) into one
+//      of two stages.
+//   2. Warp w takes the 8-column chunk w, lane l the four rows 4l..4l+3 (read
+//      in a lane-rotated order so that the 16-byte reads of a quarter-warp hit
+//      eight different bank groups).
+//   3. Group maxima: |x| maxima on packed bf16 pairs inside each thread; the
+//      16 chunk maxima of a row and the 32 lane maxima of a column meet in
+//      shared memory, where four threads per row / column finish them and
+//      compute the scale and the negated reciprocal.
+//   4. Every value is divided by its scale(s) and rounded to e4m3; the codes
+//      are written into the spent input stage, row-major (128-byte swizzled)
+//      and transposed (the four codes of a thread's rows in one column are one
+//      32-bit word, assembled with byte permutes).
+//   5. One TMA store per output writes the tile.  A TMA store clips the
+//      innermost dimension in whole 16-byte units, so the maps cover only the
+//      16-byte-aligned part of each row (q_row: columns < C & ~15, q_col:
+//      rows < T & ~15) and the threads store the last C % 16 (T % 16) bytes of
+//      each row of an edge tile from the staged tile themselves; nothing
+//      outside the logical [T, C] (or [C, T]) region is written.
+// Rows / columns outside [T, C] arrive as zeros (TMA fill) and cannot raise
+// a maximum.  Inputs are finite bf16 values (the method's domain).
 #include <cudaTypedefs.h>
+
+#include <string.h>
 
 #include <mutex>
 
@@ -31,20 +51,28 @@ namespace {
 constexpr int kTileRow = kQuantTileRow, kTileCol = kQuantTileCol, kTileScale = kQuantTileScale;
 constexpr int kQtBoxBytes = 128 * 128;               // 64 bf16 columns x 128 rows
 constexpr int kQtStageBytes = 2 * kQtBoxBytes;       // one 128x128 bf16 tile
-constexpr int kQtOffTout = 2 * kQtStageBytes;        // transposed byte tile, 128 x 128
-constexpr int kQtOffBar = kQtOffTout + 128 * 128;
-constexpr int kQtSmemBytes = kQtOffBar + 64 + 4 * (kQtThreads / 32) + 1024;  // + alignment slack
+// once the tile is in registers its stage holds the outputs:
+constexpr int kQtOutRow = 0;                         // q_row tile: 128 rows x 128 B, 128-byte swizzled
+constexpr int kQtOutCol = 128 * 128;                 // q_col tile: 128 columns x 128 B (input rows)
+constexpr int kQtOffRowRed = 2 * kQtStageBytes;      // [16 chunks][128 rows] bf16x2 row maxima
+constexpr int kQtOffColRed = kQtOffRowRed + 16 * 128 * 4;  // [16 chunks][32 lanes] 4 x bf16x2 column maxima
+constexpr int kQtOffRowSc = kQtOffColRed + 16 * 32 * 16;   // [128 rows] (s, -1/s)
+constexpr int kQtOffColSc = kQtOffRowSc + 128 * 8;         // [64 column pairs] (s0, s1, -1/s0, -1/s1)
+constexpr int kQtOffBar = kQtOffColSc + 64 * 16;
+constexpr int kQtSmemBytes = kQtOffBar + 64 + 1024;        // + alignment slack
 
 struct TileQuantParams {
   int64_t T, C;
-  uint8_t* q_row;
+  uint8_t* q_row;   // for the ragged bytes only; the rest goes through the tensor maps
   int64_t ldq_row;
-  float* s_row;
-  int64_t lds_row;
   uint8_t* q_col;
   int64_t ldq_col;
+  int64_t C_al, T_al;  // C & ~15, T & ~15: extents of the two store maps
+  float* s_row;
+  int64_t lds_row;
   float* s_col;
   int64_t lds_col;
+  int has_q_row, has_q_col;
   int64_t tiles_c, num_tiles;
   uint64_t wait_limit_ns;
 };
@@ -54,79 +82,113 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
   return v;
 }
-
-// 16-byte chunk `chunk` (0..15, 8 columns each) of tile row `r` in a stage
-// written by two 64-column TMA boxes with 128-byte swizzling.
-__device__ __forceinline__ uint32_t tile_chunk_addr(uint32_t stage, int r, int chunk) {
-  return stage + (uint32_t)((chunk >> 3) * kQtBoxBytes + r * 128 + (((chunk & 7) ^ (r & 7)) << 4));
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
 
-__device__ __forceinline__ uint32_t absmax2(uint32_t acc, uint32_t w) { return __vmaxu2(acc, w & 0x7FFF7FFFu); }
+// Packed bf16 pair: per half, a value whose magnitude is max(|a|, |b|) (its
+// sign bit is meaningless and is masked off where the maximum is used).
+__device__ __forceinline__ uint32_t amax2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int q) {
   return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
 }
 
-// x/s for the two bf16 values of `w` (Markstein-corrected product, as
-// quotient()), on packed fp32x2 lanes; returns the two e4m3 bytes.  The
-// sign of a zero result may come out positive; sign_bytes() restores it.
-__device__ __forceinline__ uint32_t quant2(uint32_t w, uint64_t ns2, uint64_t y2) {
+// s = RN(max(amax, 1e-12) / 448).  448 = 7 * 2^6 and a/448 stays a normal
+// float for a >= 1e-12, so s = RN(a/7) * 2^-6 exactly.  RN(a/7) comes from
+// y7 = RN(1/7) with one correction step of Markstein's method (P. Markstein,
+// IBM J. Res. Dev. 34(1), 1990): q0 = RN(a*y7), r = a - 7*q0 (exact), RN(q0 + r*y7).
+// For every bf16 amax this equals the IEEE quotient (checked exhaustively on
+// the CPU; the GPU tests compare every scale bit for bit with the oracle).
+__device__ __forceinline__ float scale_of(float amax) {
+  constexpr float kRcp7 = 1.0f / 7.0f;
+  const float a = fmaxf(amax, kAmaxFloor);
+  const float q0 = __fmul_rn(a, kRcp7);
+  const float r = __fmaf_rn(-7.0f, q0, a);
+  return __fmul_rn(__fmaf_rn(r, kRcp7, q0), 0.015625f);
+}
+
+// -1/s to within one ulp (rcp.approx: at most 1 ulp of error over the whole
+// range; s is normal, so flushing subnormals changes nothing).
+__device__ __forceinline__ float neg_rcp(float s) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(-s));
+  return y;
+}
+
+// The e4m3 codes of -(x/s) for the two bf16 values of `w`, given s2 = (s, s')
+// and ny2 = (-1/s, -1/s') to within an ulp:
+//   q0 = x*(-y), r = x - s*(x*y) (exact), q1 = q0 + r*(-y) = -RN(x/s).
+// With bf16 x, |x| <= 448 s and any such y this one-step quotient rounds to
+// the same e4m3 code as the IEEE quotient, including the sign of zero
+// (checked exhaustively on the CPU over every pair of bf16 (amax, x)).  The
+// caller flips the sign bits of the codes (XOR 0x80).
+__device__ __forceinline__ uint32_t neg_codes2(uint32_t w, uint64_t s2, uint64_t ny2) {
   const uint64_t x2 = f2_pack(bf16_lo(w), bf16_hi(w));
-  const uint64_t q0 = f2_mul(x2, y2);
-  const uint64_t r0 = f2_fma(ns2, q0, x2);
-  const uint64_t q1 = f2_fma(r0, y2, q0);
-  const uint64_t r1 = f2_fma(ns2, q1, x2);
-  const uint64_t q2 = f2_fma(r1, y2, q1);
-  return cvt_e4m3x2(__uint_as_float((uint32_t)q2), __uint_as_float((uint32_t)(q2 >> 32)));
-}
-
-// The four e4m3 sign bits of the bf16 values in words a (values 0, 1) and b
-// (values 2, 3), placed at bit 7 of bytes 0..3: x/s keeps the sign of x, so
-// ORing these into the codes fixes zero codes and leaves the others as they are.
-__device__ __forceinline__ uint32_t sign_bytes(uint32_t a, uint32_t b) {
-  return __byte_perm(a, b, 0x7531) & 0x80808080u;
-}
-
-// eight values (one 16-byte chunk) -> eight bytes, as two words
-__device__ __forceinline__ uint2 quant8(const uint4& v, float sc, float rc) {
-  const uint64_t ns2 = f2_pack(-sc, -sc), y2 = f2_pack(rc, rc);
-  uint2 o;
-  o.x = (quant2(v.x, ns2, y2) | (quant2(v.y, ns2, y2) << 16)) | sign_bytes(v.x, v.y);
-  o.y = (quant2(v.z, ns2, y2) | (quant2(v.w, ns2, y2) << 16)) | sign_bytes(v.z, v.w);
-  return o;
+  const uint64_t q0 = f2_mul(x2, ny2);
+  const uint64_t r = f2_fma(s2, q0, x2);
+  const uint64_t q1 = f2_fma(r, ny2, q0);
+  return cvt_e4m3x2(__uint_as_float((uint32_t)q1), __uint_as_float((uint32_t)(q1 >> 32)));
 }
 
 }  // namespace
 
 template <int MODE>
 __global__ void __launch_bounds__(kQtThreads, 2)
-    quant_tile_kernel(const __grid_constant__ CUtensorMap tmap, const TileQuantParams p) {
+    quant_tile_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ CUtensorMap tmap_qrow,
+                      const __grid_constant__ CUtensorMap tmap_qcol, const TileQuantParams p) {
+  constexpr bool kRow = (MODE & kTileRow) != 0, kCol = (MODE & kTileCol) != 0, kScale = (MODE & kTileScale) != 0;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t tout = sbase + kQtOffTout;
   const uint32_t bar0 = sbase + kQtOffBar;
   volatile int* never = reinterpret_cast<volatile int*>(smem + kQtOffBar + 16);
-  float* red = reinterpret_cast<float*>(smem + kQtOffBar + 64);  // one partial per warp
+  const uint32_t rowred = sbase + kQtOffRowRed;  // also the per-warp tile maxima (kTileScale)
+  const uint32_t colred = sbase + kQtOffColRed;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool out_row = kRow || (kScale && p.has_q_row);
+  const bool out_col = kCol || (kScale && p.has_q_col);
 
   if (tid == 0) {
     mbar_init(bar0, 1);
     mbar_init(bar0 + 8, 1);
     *never = 0;
     fence_barrier_init();
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    tma_prefetch_desc(&tmap);
+    fence_proxy_async_shared();
+    tma_prefetch_desc(&tmap_x);
+    if (out_row && p.C_al > 0) tma_prefetch_desc(&tmap_qrow);
+    if (out_col && p.T_al > 0) tma_prefetch_desc(&tmap_qcol);
   }
   __syncthreads();
+
+  // Lane l reads its rows in the order 4l + rho(i), rho(i) = (i + rot) & 3.
+  const int rot = (lane >> 1) & 3;
+  // Byte selectors that put the codes of rows 4l..4l+3 of one column, in row
+  // order, into one word (see the column store below): in the 8 bytes
+  // (X, Y), slot i's code of the even column sits at {0, 1, 4, 5}[i], of the
+  // odd column at {2, 3, 6, 7}[i].
+  uint32_t sel_e = 0, sel_o = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int i = (k - rot) & 3;
+    sel_e |= (uint32_t)((i & 1) + 4 * (i >> 1)) << (4 * k);
+    sel_o |= (uint32_t)(2 + (i & 1) + 4 * (i >> 1)) << (4 * k);
+  }
 
   auto issue = [&](int64_t tile, int s) {
     const int32_t t0 = (int32_t)qt_tile_t0(tile, p.tiles_c), c0 = (int32_t)qt_tile_c0(tile, p.tiles_c);
     const uint32_t st = sbase + (uint32_t)(s * kQtStageBytes);
     mbar_arrive_expect_tx(bar0 + 8u * s, (uint32_t)kQtStageBytes);
-    tma_load_2d(st, &tmap, bar0 + 8u * s, c0, t0);
-    tma_load_2d(st + kQtBoxBytes, &tmap, bar0 + 8u * s, c0 + 64, t0);
+    tma_load_2d(st, &tmap_x, bar0 + 8u * s, c0, t0);
+    tma_load_2d(st + kQtBoxBytes, &tmap_x, bar0 + 8u * s, c0 + 64, t0);
   };
   if (tid == 0) {
     for (int s = 0; s < 2; ++s) {
@@ -143,172 +205,195 @@ __global__ void __launch_bounds__(kQtThreads, 2)
     if (!__syncthreads_and(ok)) {
       if (tid == 0) {
         atomicOr(&g_quant_error, 1u);
-        // the other stage's copy (if issued) must land before the CTA exits
-        if (tile + gridDim.x < p.num_tiles)
-          mbar_wait_bounded(bar0 + 8u * (s ^ 1), (uint32_t)(((it + 1) >> 1) & 1), p.wait_limit_ns, never);
+        // tile 1's copy, issued at the start, must land before the CTA exits
+        if (it == 0 && tile + gridDim.x < p.num_tiles)
+          mbar_wait_bounded(bar0 + 8u, 0u, p.wait_limit_ns, never);
       }
       break;
     }
     const int64_t t0 = qt_tile_t0(tile, p.tiles_c), c0 = qt_tile_c0(tile, p.tiles_c);
-    float tile_sc = 0.0f, tile_rc = 0.0f;
 
-    // ------------------------------------------------------------ row pass
-    if (MODE & (kTileRow | kTileScale)) {
-      const int lane16 = lane & 15, half = lane >> 4;
-      uint4 v[kQtRowPasses];
+    // ------------------------------------------------ this thread's 4 x 8 values
+    uint4 v[4];
 #pragma unroll
-      for (int ps = 0; ps < kQtRowPasses; ++ps) v[ps] = lds128(tile_chunk_addr(stage, qt_rowpass_row(ps, warp, half), lane16));
-      float sc[kQtRowPasses], rc[kQtRowPasses];
-      if (MODE & kTileRow) {
-        float a[kQtRowPasses];
+    for (int i = 0; i < 4; ++i) {
+      const int r = 4 * lane + ((i + rot) & 3);
+      v[i] = lds128(stage + (uint32_t)((warp >> 3) * kQtBoxBytes + r * 128 + (((warp & 7) ^ (r & 7)) << 4)));
+    }
+    uint32_t rm[4];  // per row: (max |even column|, max |odd column|)
 #pragma unroll
-        for (int ps = 0; ps < kQtRowPasses; ++ps) {
-          const uint32_t m2 = absmax2(absmax2(absmax2(absmax2(0u, v[ps].x), v[ps].y), v[ps].z), v[ps].w);
-          a[ps] = fmaxf(bf16_lo(m2), bf16_hi(m2));
+    for (int i = 0; i < 4; ++i) rm[i] = amax2(amax2(v[i].x, v[i].y), amax2(v[i].z, v[i].w));
+    if (kScale) {
+      uint32_t m = amax2(amax2(rm[0], rm[1]), amax2(rm[2], rm[3]));
 #pragma unroll
-          for (int off = 8; off >= 1; off >>= 1) a[ps] = fmaxf(a[ps], __shfl_xor_sync(0xffffffffu, a[ps], off));
-        }
-        // lane (half*16 + j), j < kQtRowPasses, computes the scale of pass j; then broadcast
-        float amine = a[0];
+      for (int off = 16; off >= 1; off >>= 1) m = amax2(m, __shfl_xor_sync(0xffffffffu, m, off));
+      if (lane == 0) sts32(rowred + 4u * warp, m);
+    } else {
+      if (kRow) {
 #pragma unroll
-        for (int ps = 1; ps < kQtRowPasses; ++ps) amine = (lane16 == ps) ? a[ps] : amine;
-        const float scm = group_scale(amine), rcm = recip_rn(scm);
-#pragma unroll
-        for (int ps = 0; ps < kQtRowPasses; ++ps) {
-          sc[ps] = __shfl_sync(0xffffffffu, scm, half * 16 + ps);
-          rc[ps] = __shfl_sync(0xffffffffu, rcm, half * 16 + ps);
-        }
-      } else {
-        uint32_t m2 = 0;
-#pragma unroll
-        for (int ps = 0; ps < kQtRowPasses; ++ps)
-          m2 = absmax2(absmax2(absmax2(absmax2(m2, v[ps].x), v[ps].y), v[ps].z), v[ps].w);
-        float a = fmaxf(bf16_lo(m2), bf16_hi(m2));
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-        if (lane == 0) red[warp] = a;
-        __syncthreads();
-        a = red[0];
-#pragma unroll
-        for (int w = 1; w < kQtThreads / 32; ++w) a = fmaxf(a, red[w]);
-        tile_sc = group_scale(a);
-        tile_rc = recip_rn(tile_sc);
-#pragma unroll
-        for (int ps = 0; ps < kQtRowPasses; ++ps) {
-          sc[ps] = tile_sc;
-          rc[ps] = tile_rc;
-        }
-        if (tid == 0) p.s_row[(t0 / 128) * p.lds_row + c0 / 128] = tile_sc;
+        for (int i = 0; i < 4; ++i) sts32(rowred + 4u * (uint32_t)(warp * 128 + 4 * lane + ((i + rot) & 3)), rm[i]);
       }
-      if ((MODE & kTileRow) || p.q_row != nullptr) {
-        const int64_t c = c0 + qt_rowpass_col(lane16);
+      if (kCol) {
+        uint32_t cm[4];  // per column pair of the chunk, over this thread's 4 rows
 #pragma unroll
-        for (int ps = 0; ps < kQtRowPasses; ++ps) {
-          const int64_t t = t0 + qt_rowpass_row(ps, warp, half);
-          const uint2 o = quant8(v[ps], sc[ps], rc[ps]);
-          if (t < p.T) {
-            uint8_t* dst = p.q_row + t * p.ldq_row + c;
-            if (c + 8 <= p.C) {
-              *reinterpret_cast<uint2*>(dst) = o;
-            } else {
-#pragma unroll
-              for (int b = 0; b < 8; ++b)
-                if (c + b < p.C) dst[b] = (uint8_t)(((b < 4) ? o.x : o.y) >> (8 * (b & 3)));
-            }
-            if ((MODE & kTileRow) && lane16 == 0) p.s_row[(c0 / 128) * p.lds_row + t] = sc[ps];
-          }
-        }
+        for (int q = 0; q < 4; ++q)
+          cm[q] = amax2(amax2(word_of(v[0], q), word_of(v[1], q)), amax2(word_of(v[2], q), word_of(v[3], q)));
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(colred + 16u * (uint32_t)(warp * 32 + lane)),
+                     "r"(cm[0]), "r"(cm[1]), "r"(cm[2]), "r"(cm[3])
+                     : "memory");
       }
     }
+    __syncthreads();  // partial maxima visible; the input tile is in registers
+    if (tid == 0 && it >= 1) {
+      // the other stage held the previous tile's outputs: once their stores
+      // have read it, it takes the next tile
+      bulk_wait_read_all();
+      const int64_t next = tile + gridDim.x;
+      if (next < p.num_tiles) issue(next, s ^ 1);
+    }
 
-    // ------------------------------------------------------------ column pass
-    if ((MODE & kTileCol) || ((MODE & kTileScale) && p.q_col != nullptr)) {
+    // ------------------------------------------------ scales
+    float tile_s = 0.0f, tile_ny = 0.0f;
+    if (kScale) {
+      uint32_t m = 0;
 #pragma unroll
-      for (int h = 0; h < kQtColChunks; ++h) {
-        const int chunk = qt_colpass_chunk(warp, h);
-        uint4 v[4];
+      for (int k = 0; k < 4; ++k) {
+        const uint4 a = lds128(rowred + 16u * k);
+        m = amax2(m, amax2(amax2(a.x, a.y), amax2(a.z, a.w)));
+      }
+      m = amax2(m, __byte_perm(m, 0, 0x1032));
+      tile_s = scale_of(__uint_as_float(m & 0x7FFF0000u));
+      tile_ny = neg_rcp(tile_s);
+      if (tid == 0) p.s_row[(t0 / 128) * p.lds_row + c0 / 128] = tile_s;
+    } else {
+      const int g = qt_scale_group(tid), qd = tid & 3;  // four threads per row / column g of the tile
+      if (kRow) {
+        uint32_t m = 0;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = lds128(tile_chunk_addr(stage, qt_colpass_row(lane, i), chunk));
-        float sc[8], rc[8];
-        if (MODE & kTileCol) {
-          uint32_t m2[4];
+        for (int j = 0; j < 4; ++j) {
+          uint32_t w;
+          asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(rowred + 4u * (uint32_t)((4 * qd + j) * 128 + g)));
+          m = amax2(m, w);
+        }
+        m = amax2(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = amax2(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        m = amax2(m, __byte_perm(m, 0, 0x1032));
+        const float sc = scale_of(__uint_as_float(m & 0x7FFF0000u));
+        if (qt_scale_writer(tid)) {
+          const float ny = neg_rcp(sc);
+          asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(sbase + kQtOffRowSc + 8u * g), "f"(sc), "f"(ny)
+                       : "memory");
+          if (t0 + g < p.T) p.s_row[(c0 / 128) * p.lds_row + t0 + g] = sc;
+        }
+      }
+      if (kCol) {
+        const int w = g >> 3, q = (g & 7) >> 1;
+        uint32_t m = 0;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            m2[q] = 0;
+        for (int j = 0; j < 8; ++j) {
+          uint32_t x;
+          asm volatile("ld.shared.u32 %0, [%1];"
+                       : "=r"(x)
+                       : "r"(colred + 16u * (uint32_t)(w * 32 + 8 * qd + j) + 4u * q));
+          m = amax2(m, x);
+        }
+        m = amax2(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = amax2(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        const uint32_t bits = (g & 1) ? (m & 0x7FFF0000u) : ((m << 16) & 0x7FFF0000u);
+        const float sc = scale_of(__uint_as_float(bits));
+        if (qt_scale_writer(tid)) {
+          const uint32_t slot = sbase + kQtOffColSc + 16u * (uint32_t)(g >> 1) + 4u * (g & 1);
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(slot), "f"(sc) : "memory");
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(slot + 8u), "f"(neg_rcp(sc)) : "memory");
+          if (c0 + g < p.C) p.s_col[(t0 / 128) * p.lds_col + c0 + g] = sc;
+        }
+      }
+      __syncthreads();  // scales visible
+    }
+
+    // ------------------------------------------------ codes into the spent stage
+    if (out_col) {
+      // column pair q of the chunk: the four rows' codes of each column -> one word
+      const uint32_t dst = stage + kQtOutCol + (uint32_t)(8 * warp * 128 + 4 * lane);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) m2[q] = absmax2(m2[q], word_of(v[i], q));
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) m2[q] = __vmaxu2(m2[q], __shfl_xor_sync(0xffffffffu, m2[q], off));
-          }
-          // lane j < 8 computes the scale of column j of the chunk; then broadcast
-          float amine = 0.0f;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float aj = (j & 1) ? bf16_hi(m2[j >> 1]) : bf16_lo(m2[j >> 1]);
-            amine = ((lane & 7) == j) ? aj : amine;
-          }
-          const float scm = group_scale(amine), rcm = recip_rn(scm);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            sc[j] = __shfl_sync(0xffffffffu, scm, j);
-            rc[j] = __shfl_sync(0xffffffffu, rcm, j);
-          }
-          const int64_t cg = c0 + 8 * chunk + lane;  // lanes 0..7 hold the chunk's 8 column scales
-          if (lane < 8 && cg < p.C) p.s_col[(t0 / 128) * p.lds_col + cg] = scm;
+      for (int q = 0; q < 4; ++q) {
+        uint64_t s2, ny2;
+        if (kScale) {
+          s2 = f2_pack(tile_s, tile_s);
+          ny2 = f2_pack(tile_ny, tile_ny);
         } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            sc[j] = tile_sc;
-            rc[j] = tile_rc;
-          }
+          // (s, s', -1/s, -1/s') of columns 8*warp + 2q, +1
+          asm volatile("ld.shared.v2.u64 {%0, %1}, [%2];"
+                       : "=l"(s2), "=l"(ny2)
+                       : "r"(sbase + kQtOffColSc + 16u * (uint32_t)(4 * warp + q)));
         }
-        // quantise column by column; byte (row r, column j) -> tout[8*chunk + j][r]
+        uint32_t cc[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t wq = word_of(v[i], q);
-            const uint64_t x2 = f2_pack(bf16_lo(wq), bf16_hi(wq));
-            // the two columns of this word have different scales
-            const uint64_t ns2 = f2_pack(-sc[2 * q], -sc[2 * q + 1]), y2 = f2_pack(rc[2 * q], rc[2 * q + 1]);
-            const uint64_t q0 = f2_mul(x2, y2);
-            const uint64_t r0 = f2_fma(ns2, q0, x2);
-            const uint64_t q1 = f2_fma(r0, y2, q0);
-            const uint64_t r1 = f2_fma(ns2, q1, x2);
-            const uint64_t q2 = f2_copysign(f2_fma(r1, y2, q1), x2);
-            const uint32_t bb = cvt_e4m3x2(__uint_as_float((uint32_t)q2), __uint_as_float((uint32_t)(q2 >> 32)));
-            const uint32_t r = (uint32_t)qt_colpass_row(lane, i);
-            asm volatile("st.shared.u8 [%0], %1;" ::"r"(tout + (uint32_t)((8 * chunk + 2 * q) * 128) + r), "r"(bb & 0xFF));
-            asm volatile("st.shared.u8 [%0], %1;" ::"r"(tout + (uint32_t)((8 * chunk + 2 * q + 1) * 128) + r),
-                         "r"(bb >> 8));
-          }
-        }
+        for (int i = 0; i < 4; ++i) cc[i] = neg_codes2(word_of(v[i], q), s2, ny2);
+        const uint32_t X = __byte_perm(cc[0], cc[1], 0x5140), Y = __byte_perm(cc[2], cc[3], 0x5140);
+        sts32(dst + (uint32_t)((2 * q) * 128), __byte_perm(X, Y, sel_e) ^ 0x80808080u);
+        sts32(dst + (uint32_t)((2 * q + 1) * 128), __byte_perm(X, Y, sel_o) ^ 0x80808080u);
       }
-      __syncthreads();
+    }
+    if (out_row) {
 #pragma unroll
-      for (int k = 0; k < (128 * 128 / 16) / kQtThreads; ++k) {
-        const int ch = tid + k * kQtThreads;
-        const int64_t cg = c0 + qt_store_col(ch), tg = t0 + qt_store_row(ch);
-        if (cg < p.C) {
-          const uint4 val = lds128(tout + (uint32_t)(qt_store_col(ch) * 128 + qt_store_row(ch)));
-          uint8_t* dst = p.q_col + cg * p.ldq_col + tg;
-          if (tg + 16 <= p.T) {
-            *reinterpret_cast<uint4*>(dst) = val;
-          } else {
-            const uint32_t w[4] = {val.x, val.y, val.z, val.w};
+      for (int i = 0; i < 4; ++i) {
+        const int r = 4 * lane + ((i + rot) & 3);
+        uint64_t s2, ny2;
+        if (kScale) {
+          s2 = f2_pack(tile_s, tile_s);
+          ny2 = f2_pack(tile_ny, tile_ny);
+        } else {
+          float rs, rny;
+          asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(rs), "=f"(rny) : "r"(sbase + kQtOffRowSc + 8u * r));
+          s2 = f2_pack(rs, rs);
+          ny2 = f2_pack(rny, rny);
+        }
+        const uint32_t c01 = neg_codes2(v[i].x, s2, ny2), c23 = neg_codes2(v[i].y, s2, ny2);
+        const uint32_t c45 = neg_codes2(v[i].z, s2, ny2), c67 = neg_codes2(v[i].w, s2, ny2);
+        const uint32_t lo = __byte_perm(c01, c23, 0x5410) ^ 0x80808080u;
+        const uint32_t hi = __byte_perm(c45, c67, 0x5410) ^ 0x80808080u;
+        sts64(stage + kQtOutRow + (uint32_t)(r * 128 + ((((warp >> 1) ^ (r & 7)) << 4) | ((warp & 1) << 3))), lo, hi);
+      }
+    }
+    fence_proxy_async_shared();
+    __syncthreads();  // the output tiles are complete
+    if (tid == 0) {
+      if (out_row && c0 < p.C_al) tma_store_2d(&tmap_qrow, stage + kQtOutRow, (int32_t)c0, (int32_t)t0);
+      if (out_col && t0 < p.T_al) tma_store_2d(&tmap_qcol, stage + kQtOutCol, (int32_t)t0, (int32_t)c0);
+      bulk_commit();
+    }
+    // ragged bytes past the maps' 16-byte-aligned extents (edge tiles only):
+    // thread tid covers row / column qt_scale_group(tid) of the tile and
+    // four of the (at most 15) trailing positions
+    const int g = qt_scale_group(tid), b0 = 4 * (tid & 3);
+    if (out_row && c0 + 128 > p.C_al && p.C_al < p.C && t0 + g < p.T) {
 #pragma unroll
-            for (int b = 0; b < 16; ++b)
-              if (tg + b < p.T) dst[b] = (uint8_t)(w[b >> 2] >> (8 * (b & 3)));
-          }
+      for (int b = 0; b < 4; ++b) {
+        const int64_t c = p.C_al + b0 + b;
+        if (c < p.C) {
+          const int cl = (int)(c - c0);
+          uint32_t v;
+          asm volatile("ld.shared.u8 %0, [%1];"
+                       : "=r"(v)
+                       : "r"(stage + kQtOutRow + (uint32_t)(g * 128 + ((((cl >> 4) ^ (g & 7)) << 4) | (cl & 15)))));
+          p.q_row[(t0 + g) * p.ldq_row + c] = (uint8_t)v;
         }
       }
     }
-    __syncthreads();  // the stage and the transposed tile are free again
-    if (tid == 0) {
-      const int64_t next = tile + 2 * (int64_t)gridDim.x;
-      if (next < p.num_tiles) issue(next, s);
+    if (out_col && t0 + 128 > p.T_al && p.T_al < p.T && c0 + g < p.C) {
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int64_t t = p.T_al + b0 + b;
+        if (t < p.T) {
+          uint32_t v;
+          asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(stage + kQtOutCol + (uint32_t)(g * 128 + (t - t0))));
+          p.q_col[(c0 + g) * p.ldq_col + t] = (uint8_t)v;
+        }
+      }
     }
   }
+  if (tid == 0) bulk_wait_all();  // stores complete before the CTA exits
 }
 
 // ---------------------------------------------------------------------------
@@ -329,54 +414,82 @@ static PFN_cuTensorMapEncodeTiled_v12000 qt_encode_fn() {
   return fn;
 }
 
-bool quant_tile_supported(const void* x, int64_t ldx) {
-  return ((reinterpret_cast<uintptr_t>(x) & 15u) == 0) && (ldx % 8 == 0) && qt_encode_fn() != nullptr;
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool quant_tile_supported(const void* x, int64_t ldx, const void* q_row, int64_t ldq_row, const void* q_col,
+                          int64_t ldq_col) {
+  if (!aligned16(x) || ldx % 8 != 0 || qt_encode_fn() == nullptr) return false;
+  if (q_row && (!aligned16(q_row) || ldq_row % 16 != 0)) return false;  // TMA store: 16-byte rows
+  if (q_col && (!aligned16(q_col) || ldq_col % 16 != 0)) return false;
+  return true;
+}
+
+// u8 matrix [rows, inner] with row stride ld bytes, written by 128 x 128-byte boxes.
+static bool make_store_map(CUtensorMap* m, void* base, int64_t inner, int64_t rows, int64_t ld, bool swizzle) {
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld};
+  cuuint32_t box[2] = {128, 128};
+  cuuint32_t elem[2] = {1, 1};
+  return qt_encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, elem,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int MODE>
-static cudaError_t run_tile(const CUtensorMap& m, const TileQuantParams& p, int64_t grid, cudaStream_t st) {
+static cudaError_t run_tile(const CUtensorMap& mx, const CUtensorMap& mr, const CUtensorMap& mc,
+                            const TileQuantParams& p, int64_t grid, cudaStream_t st) {
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
   std::call_once(once, [] {
     attr = cudaFuncSetAttribute(quant_tile_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQtSmemBytes);
   });
   if (attr != cudaSuccess) return attr;
-  quant_tile_kernel<MODE><<<(unsigned)grid, kQtThreads, kQtSmemBytes, st>>>(m, p);
+  quant_tile_kernel<MODE><<<(unsigned)grid, kQtThreads, kQtSmemBytes, st>>>(mx, mr, mc, p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_quant_tile(int mode, const uint16_t* x, int64_t T, int64_t C, int64_t ldx, uint8_t* q_row,
                               int64_t ldq_row, float* s_row, int64_t lds_row, uint8_t* q_col, int64_t ldq_col,
                               float* s_col, int64_t lds_col, int num_sms, cudaStream_t st) {
-  CUtensorMap m;
+  CUtensorMap mx, mr, mc;
+  memset(&mr, 0, sizeof(mr));
+  memset(&mc, 0, sizeof(mc));
   cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)T};
   cuuint64_t strides[1] = {(cuuint64_t)ldx * 2};
   cuuint32_t box[2] = {64, 128};
   cuuint32_t elem[2] = {1, 1};
-  if (qt_encode_fn()(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, elem,
+  if (qt_encode_fn()(&mx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims, strides, box, elem,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return cudaErrorInvalidValue;
+  const int64_t C_al = C & ~(int64_t)15, T_al = T & ~(int64_t)15;
+  if (q_row && C_al > 0 && !make_store_map(&mr, q_row, C_al, T, ldq_row, true)) return cudaErrorInvalidValue;
+  if (q_col && T_al > 0 && !make_store_map(&mc, q_col, T_al, C, ldq_col, false)) return cudaErrorInvalidValue;
   TileQuantParams p;
   p.T = T;
   p.C = C;
   p.q_row = q_row;
   p.ldq_row = ldq_row;
-  p.s_row = s_row;
-  p.lds_row = lds_row;
   p.q_col = q_col;
   p.ldq_col = ldq_col;
+  p.C_al = C_al;
+  p.T_al = T_al;
+  p.s_row = s_row;
+  p.lds_row = lds_row;
   p.s_col = s_col;
   p.lds_col = lds_col;
+  p.has_q_row = q_row != nullptr;
+  p.has_q_col = q_col != nullptr;
   p.tiles_c = cdiv(C, 128);
   p.num_tiles = cdiv(T, 128) * p.tiles_c;
   p.wait_limit_ns = kWaitLimitNs;
   const int64_t grid = qt_grid(p.num_tiles, num_sms);
   switch (mode) {
-    case kTileRow: return run_tile<kTileRow>(m, p, grid, st);
-    case kTileCol: return run_tile<kTileCol>(m, p, grid, st);
-    case kTileRow | kTileCol: return run_tile<kTileRow | kTileCol>(m, p, grid, st);
-    case kTileScale: return run_tile<kTileScale>(m, p, grid, st);
+    case kTileRow: return run_tile<kTileRow>(mx, mr, mc, p, grid, st);
+    case kTileCol: return run_tile<kTileCol>(mx, mr, mc, p, grid, st);
+    case kTileRow | kTileCol: return run_tile<kTileRow | kTileCol>(mx, mr, mc, p, grid, st);
+    case kTileScale: return run_tile<kTileScale>(mx, mr, mc, p, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -162,33 +162,6 @@ BFP8_API bfp8_status bfp8_gemm_1x128_128x1(const void *qa, int64_t lda, const fl
                                   int64_t M, int64_t N, int64_t K, bfp8_stream_t stream);
 
 /*
- * The two GEMMs with an optional workspace that lets a launch split its
- * (tile, 128-wide K-block) units evenly over the SMs (stream-K) when whole
- * tiles would leave part of the last wave idle; a tile split between two CTAs
- * is finished by the CTA that computed its first K-blocks, which adds the
- * other CTA's fp32 partial tile from the workspace.  Same arguments and
- * results as bfp8_gemm_1x128_128x128 / bfp8_gemm_1x128_128x1 (up to fp32
- * summation order), plus:
- *   ws         device, 256-byte aligned, at least bfp8_gemm_workspace_size()
- *              bytes, or NULL (tile-parallel schedule).  Its first 4 KiB are
- *              flags that must be zero before the first call; every call
- *              leaves them zero (unless it reports BFP8_ERR_TIMEOUT).  Calls
- *              sharing one workspace must not overlap on the GPU.
- * bfp8_gemm_workspace_size() depends on the current device's SM count
- * (about 20 MB on a 152-SM GB300); it returns 0 if no usable device.
- */
-BFP8_API size_t bfp8_gemm_workspace_size(void);
-BFP8_API bfp8_status bfp8_gemm_1x128_128x128_ws(const void *qa, int64_t lda, const float *sa, int64_t ldsa,
-                                                const void *qb, int64_t ldb, const float *sb, int64_t ldsb,
-                                                int sb_transposed, void *c, int64_t ldc,
-                                                int64_t M, int64_t N, int64_t K,
-                                                void *ws, size_t ws_bytes, bfp8_stream_t stream);
-BFP8_API bfp8_status bfp8_gemm_1x128_128x1_ws(const void *qa, int64_t lda, const float *sa, int64_t ldsa,
-                                              const void *qb, int64_t ldb, const float *sb, int64_t ldsb,
-                                              void *c, int64_t ldc, int64_t M, int64_t N, int64_t K,
-                                              void *ws, size_t ws_bytes, bfp8_stream_t stream);
-
-/*
  * Blockwise-FP8 linear layer (the Float8BlockwiseLinear computation of the
  * ROCm enablement page: quantise, then the blockwise GEMMs), y = x W^T.
  *   x  device bf16 [M,K] contiguous;  w  device bf16 [N,K] contiguous;
@@ -218,8 +191,7 @@ BFP8_API bfp8_status bfp8_linear_bwd(const void *dy, const void *x, const void *
  * quantises dY once into both forms and runs dX = dY W and dW = dY^T x from
  * what the forward kept.  `ws` (>= bfp8_linear_train_workspace_size(M,N,K)
  * bytes, 256-byte aligned) must be the one the forward filled, unmodified,
- * with the same M, N, K.  Its first 4 KiB must be zero before its first use
- * (the GEMMs' stream-K flags; every call leaves them zero).  All tensors contiguous bf16: x [M,K], w [N,K],
+ * with the same M, N, K.  All tensors contiguous bf16: x [M,K], w [N,K],
  * y [M,N], dy [M,N], dx [M,K], dw [N,K].
  */
 BFP8_API size_t bfp8_linear_train_workspace_size(int64_t M, int64_t N, int64_t K);

@@ -264,7 +264,7 @@ def _random_codes(rng, shape):
     return c
 
 
-def _gemm_case(M, N, K, mode, seed, ldc_extra=0, ws=None, repeats=1):
+def _gemm_case(M, N, K, mode, seed, ldc_extra=0, repeats=1):
     """Random e4m3 codes and random scales fed to both sides."""
     rng = np.random.default_rng(seed)
     Kb, Nb = cdiv(K, 128), cdiv(N, 128)
@@ -286,10 +286,10 @@ def _gemm_case(M, N, K, mode, seed, ldc_extra=0, ws=None, repeats=1):
     for _ in range(repeats):
         out[:, :N].zero_()
         if mode == O.SB_COL:
-            B.gemm_1x128_128x1(cu(qa), cu(sa), cu(qb), cu(sb), K, out=out, M=M, N=N, ws=ws)
+            B.gemm_1x128_128x1(cu(qa), cu(sa), cu(qb), cu(sb), K, out=out, M=M, N=N)
         else:
             B.gemm_1x128_128x128(cu(qa), cu(sa), cu(qb), cu(sb), K, sb_transposed=(mode == O.SB_TILE_T),
-                                 out=out, M=M, N=N, ws=ws)
+                                 out=out, M=M, N=N)
     torch.cuda.synchronize()
     h = flat16.cpu().numpy()
     assert np.all(h[:GUARD] == 0x7FC1) and np.all(h[-GUARD:] == 0x7FC1), "write outside C"
@@ -310,23 +310,28 @@ def test_gemm_random_codes_matches_oracle(M, N, K, mode):
     assert_gemm_close(got, ref, f"gemm mode {mode} {M}x{N}x{K}")
 
 
-# shapes whose whole-tile schedule would leave the last wave partly idle on a
-# 152-SM GB300, so a launch with a workspace splits K-blocks across CTAs
-SK_SHAPES = [(2048, 4096, 512), (2000, 4000, 520), (1200, 4096, 384), (2048, 4096, 4096)]
+# shapes with more tiles than SMs on a 152-SM GB300 and a partly idle last
+# wave: persistent CTAs walk several tiles each; launched twice in a row
+MULTIWAVE_SHAPES = [(2048, 4096, 512), (2000, 4000, 520), (1200, 4096, 384), (2048, 4096, 4096)]
 
 
-@pytest.mark.parametrize("M,N,K", SK_SHAPES)
+@pytest.mark.parametrize("M,N,K", MULTIWAVE_SHAPES)
 @pytest.mark.parametrize("mode", [O.SB_TILE, O.SB_TILE_T, O.SB_COL])
-def test_gemm_stream_k_matches_oracle(M, N, K, mode):
-    """Stream-K schedule: partial tiles handed between CTAs through the
-    workspace; three launches in a row reuse its flags (each launch must leave
-    them clear)."""
-    ws = B.gemm_workspace()
-    got, ref = _gemm_case(M, N, K, mode, seed=M + N + K + mode, ldc_extra=8, ws=ws, repeats=3)
-    assert_gemm_close(got, ref, f"stream-K gemm mode {mode} {M}x{N}x{K}")
-    off = (-ws.data_ptr()) % 256
-    assert int(ws[off:off + 4096].count_nonzero()) == 0  # flags left clear
+def test_gemm_multiwave_matches_oracle(M, N, K, mode):
+    got, ref = _gemm_case(M, N, K, mode, seed=M + N + K + mode, ldc_extra=8, repeats=2)
+    assert_gemm_close(got, ref, f"multi-wave gemm mode {mode} {M}x{N}x{K}")
     B.check_device_errors()
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 130, 256), (129, 1001, 384), (64, 2051, 128)])
+@pytest.mark.parametrize("mode", [O.SB_TILE, O.SB_COL])
+def test_gemm_ragged_n_aligned_ldc(M, N, K, mode):
+    """N not a multiple of 8 with a 16-byte-aligned row stride: the C row
+    padding past N must stay untouched (TMA stores clip the inner dimension
+    in 16-byte units, so such shapes take the per-row stores)."""
+    ldc_extra = rup(N, 8) + 8 - N
+    got, ref = _gemm_case(M, N, K, mode, seed=M + 3 * N + K + mode, ldc_extra=ldc_extra)
+    assert_gemm_close(got, ref, f"ragged-N gemm mode {mode} {M}x{N}x{K}")
 
 
 # ------------------------------------------------------------------ quant + GEMM (linear)
