@@ -12,18 +12,20 @@
 //   warp 1      MMA issuer: 4 x tcgen05.mma.kind::f8f6f4 (K = 32 each) per
 //               K-block into one of two tensor-memory partial buffers, then
 //               tcgen05.commit to release the smem stage and publish the partial.
-//   warps 2-3   idle (they complete the control warpgroup, which gives its
-//               registers to the promotion warpgroups with setmaxnreg).
-//   warps 4..19 promotion/epilogue, four per tensor-memory lane quarter, each
-//               owning 32 rows x BN/4 columns of the tile: tcgen05.ld the
+//   warp 2      scale loader: per K-block, a_s of the tile's 128 rows and b_s
+//               (BN column scales, or the tile scales) into a 4-slot shared-
+//               memory ring with cp.async, running ahead of the promotion so
+//               that no promotion warp waits on a global load.
+//   warp 3      idle (completes the control warpgroup, whose registers go to
+//               the promotion warpgroups with setmaxnreg).
+//   warps 4..   promotion/epilogue, EW/4 per tensor-memory lane quarter, each
+//               owning 32 rows x BN/(EW/4) columns of the tile: tcgen05.ld the
 //               K-block's fp32 partial, release the tensor-memory buffer,
 //               acc += (a_s*b_s) * partial in registers; at tile end round to
 //               bf16 and store only rows m < M and columns n < N.
 // The two tensor-memory buffers let the promotion of K-block kb overlap the
-// MMAs of K-block kb+1.  A warp moves only about 30 bytes per cycle out of
-// tensor memory, so sixteen warps are needed to read a 128 x 256 fp32 partial
-// (128 KiB) in less time than the MMAs of the next K-block take (512 cycles).  Tails: TMA zero-fills rows/columns outside M, N, K;
-// scale loads are predicated; the epilogue store is masked.
+// MMAs of K-block kb+1.  Tails: TMA zero-fills rows/columns outside M, N, K;
+// scale copies are zero-filled past M / N; the epilogue store is masked.
 // Every mbarrier wait is bounded in time; a timeout records an error bit,
 // lets every role leave its loop, waits for its own copies/MMAs in flight and
 // frees tensor memory before the CTA exits.
@@ -46,6 +48,7 @@ enum : uint32_t {
   kErrWaitTmemEmpty = 1u << 2,  // MMA: a tensor-memory buffer was never released
   kErrWaitTmemFull = 1u << 3,   // epilogue: a partial product never arrived
   kErrWaitDrain = 1u << 4,      // teardown: MMAs or copies in flight never finished
+  kErrWaitScale = 1u << 5,      // scale ring: a slot was never filled / released
 };
 
 struct GemmParams {
@@ -58,34 +61,42 @@ struct GemmParams {
   int64_t M, N, K;
   int num_m, num_n, num_tiles, Kb, Nb;  // below 2^31, as is num_tiles * Kb (checked by the host)
   int c_vec;   // 16-byte output stores allowed (ldc % 8 == 0, c 16-byte aligned)
-  int c_tma;   // C written by TMA stores through shared memory (same conditions)
-  int sb_vec;  // 16-byte column-scale loads allowed (ldsb % 4 == 0, sb 16-byte aligned)
+  int c_tma;   // C written by TMA stores through shared memory (also N % 8 == 0)
+  int sa_vec;  // 16-byte a_s copies allowed (ldsa % 4 == 0, sa 16-byte aligned)
+  int sb_vec;  // 16-byte b_s copies allowed (ldsb % 4 == 0, sb 16-byte aligned)
   uint64_t wait_limit_ns;
   int debug_stall;  // test hook: the promotion warps wait on a barrier nothing arrives on
 };
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, int EW>
 struct GemmCfg {
-  static constexpr int kEpiWarps = kGemmEpiWarps;  // 16: four per tensor-memory lane quarter
-  static constexpr int kCols = BN / 4;             // tile columns per promotion warp
-  static constexpr int kThreads = 128 + 32 * kEpiWarps;
-  // Register split: 640 threads launched at 96 registers each (61440); the
-  // control warpgroup drops to 32 and the four promotion warpgroups rise to
-  // 112: 128*32 + 512*112 = 61440.
-  static constexpr int kCtrlRegs = 32;
-  static constexpr int kEpiRegs = 112;
+  static constexpr int kEpiWarps = EW;
+  static constexpr int kCols = BN / (EW / 4);  // tile columns per promotion warp
+  static constexpr int kThreads = 128 + 32 * EW;
+  // Register split: the control warpgroup drops to kCtrlRegs and the promotion
+  // warpgroups rise to kEpiRegs, within what the launch holds (threads x
+  // registers per thread at launch, 65536 / threads rounded down to 8):
+  //   EW = 16: 128*40 + 512*104 = 58368 <= 640*96;  EW = 8: 128*40 + 256*224 = 62464 <= 384*168.
+  static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8;
+  static constexpr int kCtrlRegs = 40;
+  static constexpr int kEpiRegs = EW == 16 ? 104 : 224;
+  static_assert(128 * kCtrlRegs + 32 * EW * kEpiRegs <= kThreads * kLaunchRegs, "register split");
   static constexpr int kABytes = kBM * kBK;
   static constexpr int kBBytes = BN * kBK;
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;  // two fp32 partial buffers of BN columns
   static constexpr int kOffB = STAGES * kABytes;
-  // per promotion warp: a 2 KiB buffer (32 rows x 32 bf16 columns, 64-byte
-  // swizzled) that stages C for the TMA store at tile end, and holds the
-  // K-block's column scales (128x1 mode) during the K loop
-  static constexpr int kStageC = 32 * 32 * 2;
-  static constexpr int kOffSb = kOffB + STAGES * kBBytes;
-  static constexpr int kOffBar = kOffSb + kEpiWarps * kStageC;
-  static constexpr int kNumBars = 2 * STAGES + 6;
+  // per promotion warp: two 512-byte slices (32 rows x 8 bf16 columns) that
+  // stage C for the TMA stores at tile end
+  static constexpr int kSliceBytes = 32 * 8 * 2;
+  static constexpr int kOffC = kOffB + STAGES * kBBytes;
+  // scale ring: per K-block a_s[128 rows] then b_s (BN column scales or up to
+  // BN/128 tile scales)
+  static constexpr int kScaleSlots = 4;
+  static constexpr int kScaleBytes = 128 * 4 + BN * 4;
+  static constexpr int kOffScale = kOffC + EW * 2 * kSliceBytes;
+  static constexpr int kOffBar = kOffScale + kScaleSlots * kScaleBytes;
+  static constexpr int kNumBars = 2 * STAGES + 6 + 2 * kScaleSlots;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -98,31 +109,51 @@ __device__ __forceinline__ void gemm_fail(uint32_t code, volatile int* abort_fla
   *abort_flag = 1;
 }
 
-template <int BN, int STAGES, int SB_MODE, int LDW>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+// Four consecutive fp32 scales v[i0 .. i0+3] (of a row of n) into shared
+// memory at dst by cp.async; past n zero-filled.
+__device__ __forceinline__ void copy_scales4(uint32_t dst, const float* v, int i0, int64_t n, bool vec) {
+  if (vec) {
+    const int64_t left = n - i0;
+    const uint32_t bytes = left >= 4 ? 16u : left > 0 ? (uint32_t)left * 4u : 0u;
+    cp_async_16(dst, bytes ? v + i0 : v, bytes);
+  } else {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const bool in = i0 + q < n;
+      cp_async_4(dst + 4u * q, in ? v + i0 + q : v, in ? 4u : 0u);
+    }
+  }
+}
+
+template <int BN, int STAGES, int SB_MODE, int LDW, int EW>
+__global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tma_a,
                           const __grid_constant__ CUtensorMap tma_b,
                           const __grid_constant__ CUtensorMap tma_c, const GemmParams p) {
-  using Cfg = GemmCfg<BN, STAGES>;
+  using Cfg = GemmCfg<BN, STAGES, EW>;
+  constexpr int kCols = Cfg::kCols;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sA = sbase;
   const uint32_t sB = sbase + Cfg::kOffB;
-  uint8_t* cstage = smem + Cfg::kOffSb;
+  const uint32_t sC = sbase + Cfg::kOffC;
+  const uint32_t sScale = sbase + Cfg::kOffScale;
   const uint32_t bar0 = sbase + Cfg::kOffBar;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
   volatile int* never = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
 
-  // barrier addresses: full[S], empty[S], tfull[2], tempty[2], drain, stall
+  // barriers: full[S], empty[S], tfull[2], tempty[2], drain, stall, sfull[4], sempty[4]
   auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(STAGES + i); };
   auto tfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + i); };
   auto tempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + 2 + i); };
   const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
   const uint32_t stall_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 5);  // never arrived on
+  auto sfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + 6 + i); };
+  auto sempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + 6 + Cfg::kScaleSlots + i); };
 
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const int lane = (int)(threadIdx.x & 31);
@@ -138,6 +169,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     mbar_init(drain_bar, 1);
     mbar_init(stall_bar, 1);
+    for (int i = 0; i < Cfg::kScaleSlots; ++i) {
+      mbar_init(sfull_bar(i), 32);  // one cp.async arrival per loader lane
+      mbar_init(sempty_bar(i), Cfg::kEpiWarps);
+    }
     *abort_flag = 0;
     *never = 0;
     fence_barrier_init();
@@ -223,88 +258,87 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!mbar_wait_bounded(drain_bar, 0, p.wait_limit_ns, never))
         gemm_fail(kErrWaitDrain, abort_flag);
     }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ scale loader
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+      for (int kb = 0; kb < p.Kb; ++kb, ++it) {
+        const int sl = (int)(it % Cfg::kScaleSlots);
+        const uint32_t ph = (it / Cfg::kScaleSlots) & 1u;
+        const bool got = mbar_wait_bounded(sempty_bar(sl), ph ^ 1u, p.wait_limit_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) gemm_fail(kErrWaitScale, abort_flag);
+          ok = false;
+          break;
+        }
+        const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes);
+        // a_s of rows m0 + 4*lane .. +3 (zero past M)
+        copy_scales4(slot + 16u * lane, p.sa + (int64_t)kb * p.ldsa, g.m0 + 4 * lane, p.M, p.sa_vec);
+        if (SB_MODE == kSbCol) {  // b_s of columns n0 + 128h + 4*lane .. +3 (zero past N)
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)
+            copy_scales4(slot + 512u + 512u * h + 16u * lane, p.sb + (int64_t)kb * p.ldsb, g.n0 + 128 * h + 4 * lane,
+                         p.N, p.sb_vec);
+        } else if (lane < BN / 128) {  // tile scale of the 128 columns n0 + 128*lane (zero past N)
+          const int nb = g.n0 / kBlock + lane;
+          const bool in = nb < p.Nb;
+          const float* src = SB_MODE == kSbTile ? p.sb + (int64_t)nb * p.ldsb + kb : p.sb + (int64_t)kb * p.ldsb + nb;
+          cp_async_4(slot + 512u + 4u * lane, in ? src : p.sb, in ? 4u : 0u);
+        }
+        cp_async_mbar_arrive(sfull_bar(sl));
+      }
+    }
+    // let this lane's copies land before the CTA can exit
+    asm volatile("cp.async.wait_all;" ::: "memory");
   }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::kEpiRegs));
     // ------------------------------------------------------------ promotion + epilogue
     const int e = warp - 4;
-    constexpr int kCols = Cfg::kCols;
     const int row = epi_row(e, lane);
     const int col0 = epi_col0(e, BN);
     const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
-    uint8_t* cbuf = cstage + e * Cfg::kStageC;
-    const uint32_t cbuf_s = smem_u32(cbuf);
-    float* slot = reinterpret_cast<float*>(cbuf);
+    const uint32_t cbuf_s = sC + (uint32_t)(e * 2 * Cfg::kSliceBytes);
     uint32_t it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
       const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
       const int m = g.m0 + row;
       const bool m_ok = m < p.M;
-      const int nb = (g.n0 + col0) / kBlock;  // B tile-scale block of this warp's columns
-      const int ncol = g.n0 + col0 + 4 * lane;  // first of this lane's 4 column scales
-
-      auto load_sa = [&](int kb) -> float { return m_ok ? __ldg(p.sa + (int64_t)kb * p.ldsa + m) : 0.0f; };
-      auto load_sb_tile = [&](int kb) -> float {
-        if (nb >= p.Nb) return 0.0f;
-        return SB_MODE == kSbTile ? __ldg(p.sb + (int64_t)nb * p.ldsb + kb) : __ldg(p.sb + (int64_t)kb * p.ldsb + nb);
-      };
-      auto load_sb_col = [&](int kb) -> float4 {
-        if (lane >= kCols / 4) return make_float4(0.f, 0.f, 0.f, 0.f);  // lanes beyond this warp's columns
-        const float* src = p.sb + (int64_t)kb * p.ldsb + ncol;
-        if (p.sb_vec && ncol + 4 <= p.N) return __ldg(reinterpret_cast<const float4*>(src));
-        float4 r;
-        r.x = (ncol + 0 < p.N) ? __ldg(src + 0) : 0.0f;
-        r.y = (ncol + 1 < p.N) ? __ldg(src + 1) : 0.0f;
-        r.z = (ncol + 2 < p.N) ? __ldg(src + 2) : 0.0f;
-        r.w = (ncol + 3 < p.N) ? __ldg(src + 3) : 0.0f;
-        return r;
-      };
 
       float acc[kCols];
 #pragma unroll
       for (int j = 0; j < kCols; ++j) acc[j] = 0.0f;
-      if (SB_MODE == kSbCol && p.c_tma) {  // the staging buffer doubles as the scale slot
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
-      }
-
-      float sa_next = load_sa(0);
-      float sb_next = 0.0f;
-      float4 sbc_next = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (SB_MODE == kSbCol) sbc_next = load_sb_col(0);
-      else sb_next = load_sb_tile(0);
 
       for (int kb = 0; kb < p.Kb; ++kb, ++it) {
-        const float sa_cur = sa_next, sb_cur = sb_next;
-        const float4 sbc_cur = sbc_next;
-        if (kb + 1 < p.Kb) {  // prefetch the next K-block's scales (masked loads)
-          sa_next = load_sa(kb + 1);
-          if (SB_MODE == kSbCol) sbc_next = load_sb_col(kb + 1);
-          else sb_next = load_sb_tile(kb + 1);
-        }
+        const int sl = (int)(it % Cfg::kScaleSlots);
+        const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes);
+        const bool sgot = mbar_wait_bounded(sfull_bar(sl), (it / Cfg::kScaleSlots) & 1u, p.wait_limit_ns, abort_flag);
         const int buf = (int)(it & 1u);
         const uint32_t tph = (it >> 1) & 1u;
-        const bool got = mbar_wait_bounded(p.debug_stall ? stall_bar : tfull_bar(buf), tph, p.wait_limit_ns,
-                                           abort_flag);
+        const bool got = sgot && mbar_wait_bounded(p.debug_stall ? stall_bar : tfull_bar(buf), tph, p.wait_limit_ns,
+                                                   abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
-          if (lane == 0) gemm_fail(kErrWaitTmemFull, abort_flag);
+          if (lane == 0) gemm_fail(sgot ? kErrWaitTmemFull : kErrWaitScale, abort_flag);
           ok = false;
           break;
         }
         tc_fence_after();
-        if (SB_MODE == kSbCol) {
-          __syncwarp();
-          if (lane < kCols / 4) reinterpret_cast<float4*>(slot)[lane] = sbc_cur;
-          __syncwarp();
-        }
-        const uint32_t taddr = tmem_base + lane_base + (uint32_t)(buf * BN + col0);
+        float sa_cur, sb_cur = 0.0f;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sa_cur) : "r"(slot + 4u * row));
+        if (SB_MODE != kSbCol)
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sb_cur) : "r"(slot + 512u + 4u * (uint32_t)(col0 >> 7)));
         const float scale = sa_cur * sb_cur;
+        const uint32_t taddr = tmem_base + lane_base + (uint32_t)(buf * BN + col0);
         // LDW columns of the partial per tensor-memory load round trip (one wait)
 #pragma unroll
         for (int c = 0; c < kCols / LDW; ++c) {
           uint32_t r[LDW];
-          if constexpr (LDW == 32)
+          if constexpr (LDW == 64)
+            tmem_ld_32x32b_x64(taddr + (uint32_t)(LDW * c), r);
+          else if constexpr (LDW == 32)
             tmem_ld_32x32b_x32(taddr + (uint32_t)(LDW * c), r);
           else
             tmem_ld_32x32b_x16(taddr + (uint32_t)(LDW * c), r);
@@ -321,7 +355,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             const uint64_t sa2 = f2_pack(sa_cur, sa_cur);
 #pragma unroll
             for (int j4 = 0; j4 < LDW / 4; ++j4) {
-              const float4 sb4 = reinterpret_cast<const float4*>(slot)[LDW / 4 * c + j4];
+              float4 sb4;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(sb4.x), "=f"(sb4.y), "=f"(sb4.z), "=f"(sb4.w)
+                           : "r"(slot + 512u + 4u * (uint32_t)(col0 + LDW * c + 4 * j4)));
               const uint64_t t2[2] = {f2_mul(sa2, f2_pack(sb4.x, sb4.y)), f2_mul(sa2, f2_pack(sb4.z, sb4.w))};
 #pragma unroll
               for (int h = 0; h < 2; ++h) {
@@ -336,33 +373,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int j = 0; j < LDW; ++j) acc[LDW * c + j] = fmaf(scale, __uint_as_float(r[j]), acc[LDW * c + j]);
           }
         }
+        // the slot's scales are no longer needed by this warp
+        __syncwarp();
+        if (lane == 0) mbar_arrive(sempty_bar(sl));
       }
       if (!ok) break;
 
       if (p.c_tma) {
-        // 32x32 bf16 slices through the staging buffer (64-byte swizzle: the
-        // 16-byte chunk k of row r sits at chunk k ^ ((r >> 1) & 3)), each
-        // written by one TMA store (rows/columns outside [M, N] are dropped)
+        // 32x8 bf16 slices through two 512-byte staging buffers, each written
+        // by one TMA store (rows/columns outside [M, N] are dropped); a buffer
+        // is rewritten once the store issued two slices earlier has read it
+        const int ys = g.m0 + 32 * (warp % 4);
 #pragma unroll
-        for (int h = 0; h < kCols / 32; ++h) {
-          if (lane == 0) bulk_wait_read_all();  // previous store has read the buffer
-          __syncwarp();
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            uint32_t w[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              w[q] = pack_bf16x2(acc[32 * h + 8 * j + 2 * q], acc[32 * h + 8 * j + 2 * q + 1]);
-            const uint32_t addr = cbuf_s + (uint32_t)(lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4));
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]), "r"(w[2]),
-                         "r"(w[3])
-                         : "memory");
+        for (int j = 0; j < kCols / 8; ++j) {
+          const int xs = g.n0 + col0 + 8 * j;
+          if (xs >= p.N || ys >= p.M) break;  // this and every later slice lie outside C
+          const uint32_t sbuf = cbuf_s + (uint32_t)((j & 1) * Cfg::kSliceBytes);
+          // the first slice of a tile waits for every earlier store (the previous
+          // tile may have stopped on either buffer), later ones for all but the last
+          if (lane == 0) {
+            if (j == 0) bulk_wait_read_all();
+            else bulk_wait_read_1();
           }
+          __syncwarp();
+          uint32_t w[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) w[q] = pack_bf16x2(acc[8 * j + 2 * q], acc[8 * j + 2 * q + 1]);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sbuf + 16u * lane), "r"(w[0]), "r"(w[1]),
+                       "r"(w[2]), "r"(w[3])
+                       : "memory");
           fence_proxy_async_shared();
           __syncwarp();
-          const int xs = g.n0 + col0 + 32 * h, ys = g.m0 + 32 * (warp % 4);
-          if (lane == 0 && xs < p.N && ys < p.M) {  // a slice wholly outside C is not issued
-            tma_store_2d(&tma_c, cbuf_s, xs, ys);
+          if (lane == 0) {
+            tma_store_2d(&tma_c, sbuf, xs, ys);
             bulk_commit();
           }
         }
@@ -432,16 +475,16 @@ static bool make_tma_u8(CUtensorMap* map, const void* base, int64_t inner, int64
 }
 
 // Row-major [rows, cols] bf16 output with row stride ld elements; box of
-// 32 columns x 32 rows (one promotion warp's slice), 64-byte swizzle.
+// 8 columns x 32 rows (one promotion warp's slice: 16 bytes per row), no swizzle.
 static bool make_tma_bf16_store(CUtensorMap* map, void* base, int64_t cols, int64_t rows, int64_t ld) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {32, 32};
+  cuuint32_t box[2] = {8, 32};
   cuuint32_t elem[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -456,18 +499,27 @@ int64_t gemm_grid(int64_t M, int64_t N, int bn, int num_sms) {
   return tiles < num_sms ? tiles : num_sms;
 }
 
-template <int BN, int STAGES, int MODE, int LDW = 16>
+// Columns per tensor-memory load: one round trip per LDW columns of a warp's
+// share, sized to the promotion warps' registers.
+template <int BN, int MODE>
+constexpr int gemm_ldw() {
+  return kGemmEpiWarps == 16 ? (BN == 256 && MODE != kSbCol ? 32 : 16) : (MODE != kSbCol ? 64 : 32);
+}
+
+template <int BN, int STAGES, int MODE>
 static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
                             const GemmParams& p, int64_t grid, cudaStream_t st) {
-  using Cfg = GemmCfg<BN, STAGES>;
+  constexpr int EW = kGemmEpiWarps, LDW = gemm_ldw<BN, MODE>();
+  using Cfg = GemmCfg<BN, STAGES, EW>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_blockwise_kernel<BN, STAGES, MODE, LDW>,
+    attr_err = cudaFuncSetAttribute(gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  gemm_blockwise_kernel<BN, STAGES, MODE, LDW><<<(unsigned)grid, Cfg::kThreads, Cfg::kSmemBytes, st>>>(ma, mb, mc, p);
+  gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW>
+      <<<(unsigned)grid, Cfg::kThreads, Cfg::kSmemBytes, st>>>(ma, mb, mc, p);
   return cudaGetLastError();
 }
 
@@ -501,6 +553,7 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const c
   p.Kb = (int)Kb;
   p.Nb = (int)cdiv(a.N, kBlock);
   p.c_vec = (a.ldc % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.c) & 15u) == 0);
+  p.sa_vec = (a.ldsa % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.sa) & 15u) == 0);
   p.sb_vec = (a.ldsb % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.sb) & 15u) == 0);
   CUtensorMap mc;
   // a TMA store clips the inner dimension in 16-byte units: only rows of whole
@@ -512,9 +565,9 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const c
   const int64_t grid = gemm_grid(a.M, a.N, bn, num_sms);
   if (bn == 256) {
     switch (a.sb_mode) {
-      case kSbTile: return run_gemm<256, 4, kSbTile, 32>(ma, mb, mc, p, grid, st);
-      case kSbTileT: return run_gemm<256, 4, kSbTileT, 32>(ma, mb, mc, p, grid, st);
-      default: return run_gemm<256, 4, kSbCol, 16>(ma, mb, mc, p, grid, st);
+      case kSbTile: return run_gemm<256, 4, kSbTile>(ma, mb, mc, p, grid, st);
+      case kSbTileT: return run_gemm<256, 4, kSbTileT>(ma, mb, mc, p, grid, st);
+      default: return run_gemm<256, 4, kSbCol>(ma, mb, mc, p, grid, st);
     }
   }
   switch (a.sb_mode) {

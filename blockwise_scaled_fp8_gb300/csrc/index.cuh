@@ -138,11 +138,14 @@ BFP8_HD GemmTile gemm_tile(int t, int num_m, int num_n, int bn) {
 
 // Promotion / epilogue warp e (0-based, CTA warp id = e + 4): tensor-memory
 // lane quarter e % 4 (the quarter a warp may access is its CTA warp id % 4),
-// column block e / 4 of BN/4 columns.
-constexpr int kGemmEpiWarps = 16;
-constexpr int kGemmThreads = 128 + 32 * kGemmEpiWarps;
+// column block e / 4 of epi_cols(BN) columns.
+#ifndef BFP8_GEMM_EPI_WARPS
+#define BFP8_GEMM_EPI_WARPS 16
+#endif
+constexpr int kGemmEpiWarps = BFP8_GEMM_EPI_WARPS;  // 8 or 16 promotion warps
+static_assert(kGemmEpiWarps == 8 || kGemmEpiWarps == 16, "8 or 16 promotion warps");
 BFP8_HD int epi_row(int e, int lane) { return 32 * (e % 4) + lane; }
-BFP8_HD int epi_cols(int bn) { return bn / 4; }
+BFP8_HD int epi_cols(int bn) { return bn / (kGemmEpiWarps / 4); }
 BFP8_HD int epi_col0(int e, int bn) { return epi_cols(bn) * (e / 4); }
 
 }  // namespace bfp8
