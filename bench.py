@@ -42,7 +42,7 @@ METRIC = "blockwise FP8 GEMM TFLOPS & quant GB/s at 1 GB300, % of FP8/HBM roofli
 L2_FLUSH_BYTES = 256 << 20
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 GEMM_SRC = os.path.join(ROOT, "blockwise_scaled_fp8_gb300", "csrc", "gemm.cu")
-QUANT_SRC = os.path.join(ROOT, "blockwise_scaled_fp8_gb300", "csrc", "quant.cu")
+QUANT_SRC = os.path.join(ROOT, "blockwise_scaled_fp8_gb300", "csrc", "quant_tile.cu")
 
 
 def _peaks():

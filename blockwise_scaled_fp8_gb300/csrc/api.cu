@@ -652,15 +652,17 @@ bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, i
     for (int cta = 0; cta < grid; ++cta)
       for (int tile = cta; tile < tiles; tile += grid) {
         const GemmTile g = gemm_tile(tile, num_m, num_n, bn);
+        const int G = epi_group(bn);
         for (int e = 0; e < kGemmEpiWarps; ++e)
-          for (int lane = 0; lane < 32; ++lane) {
-            const int64_t m = g.m0 + epi_row(e, lane);
-            if (m >= M) continue;
-            for (int c = 0; c < epi_cols(bn); ++c) {
-              const int64_t n = g.n0 + epi_col0(e, bn) + c;
-              if (n < N) hit(counts, m, n, M, N);
-            }
-          }
+          for (int lane = 0; lane < 32; ++lane)
+            for (int sg = 0; sg < epi_cols(bn) / (8 * G); ++sg)
+              for (int i = 0; i < G; ++i) {
+                const int64_t m = g.m0 + epi_store_row(e, lane, i, G);
+                const int64_t n0 = g.n0 + epi_store_col(e, lane, sg, G, bn);
+                if (m >= M) continue;
+                for (int b = 0; b < 8; ++b)
+                  if (n0 + b < N) hit(counts, m, n0 + b, M, N);
+              }
       }
     return BFP8_OK;
   }

@@ -217,10 +217,6 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 }
 // wait until every committed bulk store of this thread is complete
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-// wait until at most one committed bulk store group of this thread is still reading shared memory
-__device__ __forceinline__ void bulk_wait_read_1() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
 // Asynchronous global -> shared copies (cp.async); bytes past src_bytes are
 // zero-filled (src_bytes = 0 reads nothing).  16-byte form: both addresses 16-byte aligned.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {

@@ -9,20 +9,23 @@
 // Design (one persistent CTA per SM, warp-specialised):
 //   warp 0      TMA producer: 128x128-byte A and BNx128-byte B tiles of one
 //               K-block per stage, 128-byte swizzled, into an S-stage ring.
-//   warp 1      MMA issuer: 4 x tcgen05.mma.kind::f8f6f4 (K = 32 each) per
+//   warps 1, 3  MMA issuers: 4 x tcgen05.mma.kind::f8f6f4 (K = 32 each) per
 //               K-block into one of two tensor-memory partial buffers, then
 //               tcgen05.commit to release the smem stage and publish the partial.
+//               Warp 1 takes the even K-block steps (buffer 0), warp 3 the odd
+//               ones (buffer 1): a thread issuing MMAs blocks while the tensor
+//               pipe drains its short queue, so with one issuer the pipe sat
+//               idle during every wait for the next buffer and stage.
 //   warp 2      scale loader: per K-block, a_s of the tile's 128 rows and b_s
 //               (BN column scales, or the tile scales) into a 4-slot shared-
 //               memory ring with cp.async, running ahead of the promotion so
 //               that no promotion warp waits on a global load.
-//   warp 3      idle (completes the control warpgroup, whose registers go to
-//               the promotion warpgroups with setmaxnreg).
 //   warps 4..   promotion/epilogue, EW/4 per tensor-memory lane quarter, each
 //               owning 32 rows x BN/(EW/4) columns of the tile: tcgen05.ld the
 //               K-block's fp32 partial, release the tensor-memory buffer,
 //               acc += (a_s*b_s) * partial in registers; at tile end round to
-//               bf16 and store only rows m < M and columns n < N.
+//               bf16, transpose 16-byte chunks across lanes with shuffles and
+//               store whole row segments (only rows m < M, columns n < N).
 // The two tensor-memory buffers let the promotion of K-block kb overlap the
 // MMAs of K-block kb+1.  Tails: TMA zero-fills rows/columns outside M, N, K;
 // scale copies are zero-filled past M / N; the epilogue store is masked.
@@ -61,7 +64,6 @@ struct GemmParams {
   int64_t M, N, K;
   int num_m, num_n, num_tiles, Kb, Nb;  // below 2^31, as is num_tiles * Kb (checked by the host)
   int c_vec;   // 16-byte output stores allowed (ldc % 8 == 0, c 16-byte aligned)
-  int c_tma;   // C written by TMA stores through shared memory (also N % 8 == 0)
   int sa_vec;  // 16-byte a_s copies allowed (ldsa % 4 == 0, sa 16-byte aligned)
   int sb_vec;  // 16-byte b_s copies allowed (ldsb % 4 == 0, sb 16-byte aligned)
   uint64_t wait_limit_ns;
@@ -86,15 +88,12 @@ struct GemmCfg {
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kTmemCols = 2 * BN;  // two fp32 partial buffers of BN columns
   static constexpr int kOffB = STAGES * kABytes;
-  // per promotion warp: two 512-byte slices (32 rows x 8 bf16 columns) that
-  // stage C for the TMA stores at tile end
-  static constexpr int kSliceBytes = 32 * 8 * 2;
   static constexpr int kOffC = kOffB + STAGES * kBBytes;
   // scale ring: per K-block a_s[128 rows] then b_s (BN column scales or up to
   // BN/128 tile scales)
   static constexpr int kScaleSlots = 4;
   static constexpr int kScaleBytes = 128 * 4 + BN * 4;
-  static constexpr int kOffScale = kOffC + EW * 2 * kSliceBytes;
+  static constexpr int kOffScale = kOffC;
   static constexpr int kOffBar = kOffScale + kScaleSlots * kScaleBytes;
   static constexpr int kNumBars = 2 * STAGES + 6 + 2 * kScaleSlots;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -128,8 +127,7 @@ __device__ __forceinline__ void copy_scales4(uint32_t dst, const float* v, int i
 template <int BN, int STAGES, int SB_MODE, int LDW, int EW>
 __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tma_a,
-                          const __grid_constant__ CUtensorMap tma_b,
-                          const __grid_constant__ CUtensorMap tma_c, const GemmParams p) {
+                          const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
   using Cfg = GemmCfg<BN, STAGES, EW>;
   constexpr int kCols = Cfg::kCols;
   extern __shared__ uint8_t smem_raw[];
@@ -138,14 +136,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sA = sbase;
   const uint32_t sB = sbase + Cfg::kOffB;
-  const uint32_t sC = sbase + Cfg::kOffC;
   const uint32_t sScale = sbase + Cfg::kOffScale;
   const uint32_t bar0 = sbase + Cfg::kOffBar;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
   volatile int* never = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
 
-  // barriers: full[S], empty[S], tfull[2], tempty[2], drain, stall, sfull[4], sempty[4]
+  // barriers: full[S], empty[S], tfull[2], tempty[2], drain (both issuers), stall, sfull[4], sempty[4]
   auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(STAGES + i); };
   auto tfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + i); };
@@ -167,7 +164,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
       mbar_init(tfull_bar(i), 1);
       mbar_init(tempty_bar(i), Cfg::kEpiWarps);
     }
-    mbar_init(drain_bar, 1);
+    mbar_init(drain_bar, 2);
     mbar_init(stall_bar, 1);
     for (int i = 0; i < Cfg::kScaleSlots; ++i) {
       mbar_init(sfull_bar(i), 32);  // one cp.async arrival per loader lane
@@ -220,14 +217,16 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
             atomicOr(&g_gemm_error, kErrWaitDrain);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------------ MMA issuers
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
+      const uint32_t mine = warp == 1 ? 0u : 1u;  // the K-block steps (and TMEM buffer) of this issuer
       uint32_t it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
         for (int kb = 0; kb < p.Kb; ++kb, ++it) {
+          if ((it & 1u) != mine) continue;
           const int st = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
           const int buf = (int)(it & 1u);
@@ -253,7 +252,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
           mma_commit(tfull_bar(buf));
         }
       }
-      // every MMA issued above completes before tensor memory is released
+      // every MMA issued by both issuers completes before tensor memory is released
       mma_commit(drain_bar);
       if (!mbar_wait_bounded(drain_bar, 0, p.wait_limit_ns, never))
         gemm_fail(kErrWaitDrain, abort_flag);
@@ -300,14 +299,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     const int row = epi_row(e, lane);
     const int col0 = epi_col0(e, BN);
     const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
-    const uint32_t cbuf_s = sC + (uint32_t)(e * 2 * Cfg::kSliceBytes);
     uint32_t it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
       const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
-      const int m = g.m0 + row;
-      const bool m_ok = m < p.M;
-
       float acc[kCols];
 #pragma unroll
       for (int j = 0; j < kCols; ++j) acc[j] = 0.0f;
@@ -315,7 +310,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
       for (int kb = 0; kb < p.Kb; ++kb, ++it) {
         const int sl = (int)(it % Cfg::kScaleSlots);
         const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes);
-        const bool sgot = mbar_wait_bounded(sfull_bar(sl), (it / Cfg::kScaleSlots) & 1u, p.wait_limit_ns, abort_flag);
+        // the loader runs ahead, so the slot is almost always ready: poll, do not sleep
+        const bool sgot = mbar_spin_bounded(sfull_bar(sl), (it / Cfg::kScaleSlots) & 1u, p.wait_limit_ns, abort_flag);
         const int buf = (int)(it & 1u);
         const uint32_t tph = (it >> 1) & 1u;
         const bool got = sgot && mbar_wait_bounded(p.debug_stall ? stall_bar : tfull_bar(buf), tph, p.wait_limit_ns,
@@ -379,56 +375,54 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
       }
       if (!ok) break;
 
-      if (p.c_tma) {
-        // 32x8 bf16 slices through two 512-byte staging buffers, each written
-        // by one TMA store (rows/columns outside [M, N] are dropped); a buffer
-        // is rewritten once the store issued two slices earlier has read it
-        const int ys = g.m0 + 32 * (warp % 4);
+      // Epilogue: round to bf16, transpose G x G blocks of 16-byte chunks (8
+      // columns) within groups of G lanes (xor shuffles), so that lane pos of a
+      // group holds chunk pos of the group's G rows; each store instruction of
+      // the warp then writes 32/G row segments of 16*G contiguous bytes.  Only
+      // rows < M and columns < N are written.
+      {
+        constexpr int kG = kCols / 8 >= 8 ? 8 : kCols / 8;  // chunks per transposed block (epi_group)
+        const int pos = lane % kG;
 #pragma unroll
-        for (int j = 0; j < kCols / 8; ++j) {
-          const int xs = g.n0 + col0 + 8 * j;
-          if (xs >= p.N || ys >= p.M) break;  // this and every later slice lie outside C
-          const uint32_t sbuf = cbuf_s + (uint32_t)((j & 1) * Cfg::kSliceBytes);
-          // the first slice of a tile waits for every earlier store (the previous
-          // tile may have stopped on either buffer), later ones for all but the last
-          if (lane == 0) {
-            if (j == 0) bulk_wait_read_all();
-            else bulk_wait_read_1();
+        for (int sg = 0; sg < kCols / (8 * kG); ++sg) {
+          uint32_t X[kG][4];
+#pragma unroll
+          for (int j = 0; j < kG; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              X[j][q] = pack_bf16x2(acc[8 * (kG * sg + j) + 2 * q], acc[8 * (kG * sg + j) + 2 * q + 1]);
+#pragma unroll
+          for (int msk = kG / 2; msk >= 1; msk >>= 1) {
+            const bool hi = (pos & msk) != 0;
+#pragma unroll
+            for (int j = 0; j < kG; ++j) {
+              if (j & msk) continue;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint32_t send = hi ? X[j][q] : X[j | msk][q];
+                const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, msk);
+                if (hi) X[j][q] = recv;
+                else X[j | msk][q] = recv;
+              }
+            }
           }
-          __syncwarp();
-          uint32_t w[4];
+          const int n = g.n0 + epi_store_col(e, lane, sg, kG, BN);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) w[q] = pack_bf16x2(acc[8 * j + 2 * q], acc[8 * j + 2 * q + 1]);
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sbuf + 16u * lane), "r"(w[0]), "r"(w[1]),
-                       "r"(w[2]), "r"(w[3])
-                       : "memory");
-          fence_proxy_async_shared();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&tma_c, sbuf, xs, ys);
-            bulk_commit();
-          }
-        }
-      } else if (m_ok) {
-        uint16_t* crow = p.c + (int64_t)m * p.ldc;
+          for (int i = 0; i < kG; ++i) {
+            const int mr = g.m0 + epi_store_row(e, lane, i, kG);
+            if (mr >= p.M || n >= p.N) continue;
+            uint16_t* dst = p.c + (int64_t)mr * p.ldc + n;
+            if (p.c_vec && n + 8 <= p.N) {
+              *reinterpret_cast<uint4*>(dst) = make_uint4(X[i][0], X[i][1], X[i][2], X[i][3]);
+            } else {
 #pragma unroll
-        for (int c8 = 0; c8 < kCols / 8; ++c8) {
-          const int n = g.n0 + col0 + 8 * c8;
-          if (n >= p.N) break;
-          uint32_t w[4];
-#pragma unroll
-          for (int h = 0; h < 4; ++h) w[h] = pack_bf16x2(acc[8 * c8 + 2 * h], acc[8 * c8 + 2 * h + 1]);
-          if (p.c_vec && n + 8 <= p.N) {
-            *reinterpret_cast<uint4*>(crow + n) = make_uint4(w[0], w[1], w[2], w[3]);
-          } else {
-#pragma unroll
-            for (int b = 0; b < 8; ++b)
-              if (n + b < p.N) crow[n + b] = (uint16_t)(w[b >> 1] >> (16 * (b & 1)));
+              for (int b = 0; b < 8; ++b)
+                if (n + b < p.N) dst[b] = (uint16_t)(X[i][b >> 1] >> (16 * (b & 1)));
+            }
           }
         }
       }
     }
-    if (p.c_tma && lane == 0) bulk_wait_all();  // stores complete before the CTA exits
   }
 
   __syncwarp();
@@ -474,20 +468,6 @@ static bool make_tma_u8(CUtensorMap* map, const void* base, int64_t inner, int64
   return r == CUDA_SUCCESS;
 }
 
-// Row-major [rows, cols] bf16 output with row stride ld elements; box of
-// 8 columns x 32 rows (one promotion warp's slice: 16 bytes per row), no swizzle.
-static bool make_tma_bf16_store(CUtensorMap* map, void* base, int64_t cols, int64_t rows, int64_t ld) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
-  cuuint32_t box[2] = {8, 32};
-  cuuint32_t elem[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int gemm_pick_bn(int64_t M, int64_t N, int num_sms) {
   if (N <= 128) return 128;
   const int64_t tiles256 = cdiv(M, kBM) * cdiv(N, 256);
@@ -507,7 +487,7 @@ constexpr int gemm_ldw() {
 }
 
 template <int BN, int STAGES, int MODE>
-static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
+static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb,
                             const GemmParams& p, int64_t grid, cudaStream_t st) {
   constexpr int EW = kGemmEpiWarps, LDW = gemm_ldw<BN, MODE>();
   using Cfg = GemmCfg<BN, STAGES, EW>;
@@ -519,7 +499,7 @@ static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const 
   });
   if (attr_err != cudaSuccess) return attr_err;
   gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW>
-      <<<(unsigned)grid, Cfg::kThreads, Cfg::kSmemBytes, st>>>(ma, mb, mc, p);
+      <<<(unsigned)grid, Cfg::kThreads, Cfg::kSmemBytes, st>>>(ma, mb, p);
   return cudaGetLastError();
 }
 
@@ -555,25 +535,20 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const c
   p.c_vec = (a.ldc % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.c) & 15u) == 0);
   p.sa_vec = (a.ldsa % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.sa) & 15u) == 0);
   p.sb_vec = (a.ldsb % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.sb) & 15u) == 0);
-  CUtensorMap mc;
-  // a TMA store clips the inner dimension in 16-byte units: only rows of whole
-  // 16-byte units (N % 8 == 0) keep the padding past N untouched
-  p.c_tma = p.c_vec && a.N % 8 == 0 && make_tma_bf16_store(&mc, a.c, a.N, a.M, a.ldc);
-  if (!p.c_tma) memset(&mc, 0, sizeof(mc));
   p.wait_limit_ns = wait_limit_ns;
   p.debug_stall = debug_stall;
   const int64_t grid = gemm_grid(a.M, a.N, bn, num_sms);
   if (bn == 256) {
     switch (a.sb_mode) {
-      case kSbTile: return run_gemm<256, 4, kSbTile>(ma, mb, mc, p, grid, st);
-      case kSbTileT: return run_gemm<256, 4, kSbTileT>(ma, mb, mc, p, grid, st);
-      default: return run_gemm<256, 4, kSbCol>(ma, mb, mc, p, grid, st);
+      case kSbTile: return run_gemm<256, 4, kSbTile>(ma, mb, p, grid, st);
+      case kSbTileT: return run_gemm<256, 4, kSbTileT>(ma, mb, p, grid, st);
+      default: return run_gemm<256, 4, kSbCol>(ma, mb, p, grid, st);
     }
   }
   switch (a.sb_mode) {
-    case kSbTile: return run_gemm<128, 6, kSbTile>(ma, mb, mc, p, grid, st);
-    case kSbTileT: return run_gemm<128, 6, kSbTileT>(ma, mb, mc, p, grid, st);
-    default: return run_gemm<128, 6, kSbCol>(ma, mb, mc, p, grid, st);
+    case kSbTile: return run_gemm<128, 6, kSbTile>(ma, mb, p, grid, st);
+    case kSbTileT: return run_gemm<128, 6, kSbTileT>(ma, mb, p, grid, st);
+    default: return run_gemm<128, 6, kSbCol>(ma, mb, p, grid, st);
   }
 }
 

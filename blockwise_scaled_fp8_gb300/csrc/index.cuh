@@ -147,5 +147,12 @@ static_assert(kGemmEpiWarps == 8 || kGemmEpiWarps == 16, "8 or 16 promotion warp
 BFP8_HD int epi_row(int e, int lane) { return 32 * (e % 4) + lane; }
 BFP8_HD int epi_cols(int bn) { return bn / (kGemmEpiWarps / 4); }
 BFP8_HD int epi_col0(int e, int bn) { return epi_cols(bn) * (e / 4); }
+// Epilogue stores: G x G blocks of 16-byte (8-column) chunks are transposed
+// within groups of G lanes, G = min(8, epi_cols / 8); in pass sg, lane (grp =
+// lane / G, pos = lane % G) stores chunk G*sg + pos of tile rows
+// 32*(e%4) + G*grp + i, i < G.
+BFP8_HD int epi_group(int bn) { return epi_cols(bn) / 8 >= 8 ? 8 : epi_cols(bn) / 8; }
+BFP8_HD int epi_store_row(int e, int lane, int i, int G) { return 32 * (e % 4) + G * (lane / G) + i; }
+BFP8_HD int epi_store_col(int e, int lane, int sg, int G, int bn) { return epi_col0(e, bn) + 8 * (G * sg + lane % G); }
 
 }  // namespace bfp8
