@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     // ------------------------------------------------------------ promotion + epilogue
     const int e = warp - 4;
     const int row = epi_row(e, lane);
-    const int col0 = epi_col0(e, BN);
+    const int col0 = epi_col0(e, BN, EW);
     const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
     uint32_t it = 0;
     bool ok = true;
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
               }
             }
           }
-          const int n = g.n0 + epi_store_col(e, lane, sg, kG, BN);
+          const int n = g.n0 + epi_store_col(e, lane, sg, kG, BN, EW);
 #pragma unroll
           for (int i = 0; i < kG; ++i) {
             const int mr = g.m0 + epi_store_row(e, lane, i, kG);
@@ -479,17 +479,22 @@ int64_t gemm_grid(int64_t M, int64_t N, int bn, int num_sms) {
   return tiles < num_sms ? tiles : num_sms;
 }
 
-// Columns per tensor-memory load: one round trip per LDW columns of a warp's
-// share, sized to the promotion warps' registers.
-template <int BN, int MODE>
+// Promotion warps per mode (measured: the tile-scale GEMMs are faster with 8,
+// the column-scale one with 16) and columns per tensor-memory load (one round
+// trip per LDW columns of a warp's share, sized to the promotion warps' registers).
+template <int MODE>
+constexpr int gemm_ew() {
+  return MODE == kSbCol ? 16 : 8;  // = gemm_epi_warps(MODE == kSbCol), which the host replay uses
+}
+template <int BN, int MODE, int EW>
 constexpr int gemm_ldw() {
-  return kGemmEpiWarps == 16 ? (BN == 256 && MODE != kSbCol ? 32 : 16) : (MODE != kSbCol ? 64 : 32);
+  return EW == 16 ? (BN == 256 && MODE != kSbCol ? 32 : 16) : (MODE != kSbCol ? 64 : 32);
 }
 
 template <int BN, int STAGES, int MODE>
 static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb,
                             const GemmParams& p, int64_t grid, cudaStream_t st) {
-  constexpr int EW = kGemmEpiWarps, LDW = gemm_ldw<BN, MODE>();
+  constexpr int EW = gemm_ew<MODE>(), LDW = gemm_ldw<BN, MODE, EW>();
   using Cfg = GemmCfg<BN, STAGES, EW>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;

@@ -136,23 +136,22 @@ BFP8_HD GemmTile gemm_tile(int t, int num_m, int num_n, int bn) {
   return g;
 }
 
-// Promotion / epilogue warp e (0-based, CTA warp id = e + 4): tensor-memory
-// lane quarter e % 4 (the quarter a warp may access is its CTA warp id % 4),
-// column block e / 4 of epi_cols(BN) columns.
-#ifndef BFP8_GEMM_EPI_WARPS
-#define BFP8_GEMM_EPI_WARPS 16
-#endif
-constexpr int kGemmEpiWarps = BFP8_GEMM_EPI_WARPS;  // 8 or 16 promotion warps
-static_assert(kGemmEpiWarps == 8 || kGemmEpiWarps == 16, "8 or 16 promotion warps");
+// Promotion / epilogue warp e (0-based, CTA warp id = e + 4) of `ew` (8 or
+// 16): tensor-memory lane quarter e % 4 (the quarter a warp may access is its
+// CTA warp id % 4), column block e / 4 of epi_cols(bn, ew) columns.  The
+// 1x128 x 128x128 GEMMs use 8 promotion warps, the 1x128 x 128x1 GEMM 16.
+BFP8_HD int gemm_epi_warps(bool col_scales) { return col_scales ? 16 : 8; }
 BFP8_HD int epi_row(int e, int lane) { return 32 * (e % 4) + lane; }
-BFP8_HD int epi_cols(int bn) { return bn / (kGemmEpiWarps / 4); }
-BFP8_HD int epi_col0(int e, int bn) { return epi_cols(bn) * (e / 4); }
+BFP8_HD int epi_cols(int bn, int ew) { return bn / (ew / 4); }
+BFP8_HD int epi_col0(int e, int bn, int ew) { return epi_cols(bn, ew) * (e / 4); }
 // Epilogue stores: G x G blocks of 16-byte (8-column) chunks are transposed
 // within groups of G lanes, G = min(8, epi_cols / 8); in pass sg, lane (grp =
 // lane / G, pos = lane % G) stores chunk G*sg + pos of tile rows
 // 32*(e%4) + G*grp + i, i < G.
-BFP8_HD int epi_group(int bn) { return epi_cols(bn) / 8 >= 8 ? 8 : epi_cols(bn) / 8; }
+BFP8_HD int epi_group(int bn, int ew) { return epi_cols(bn, ew) / 8 >= 8 ? 8 : epi_cols(bn, ew) / 8; }
 BFP8_HD int epi_store_row(int e, int lane, int i, int G) { return 32 * (e % 4) + G * (lane / G) + i; }
-BFP8_HD int epi_store_col(int e, int lane, int sg, int G, int bn) { return epi_col0(e, bn) + 8 * (G * sg + lane % G); }
+BFP8_HD int epi_store_col(int e, int lane, int sg, int G, int bn, int ew) {
+  return epi_col0(e, bn, ew) + 8 * (G * sg + lane % G);
+}
 
 }  // namespace bfp8

@@ -252,7 +252,9 @@ BFP8_API bfp8_status bfp8_debug_gemm_stall(const void *qa, int64_t lda, const fl
  * `kind` names, for the launch configuration the library would use on a
  * 152-SM GB300.  flag bit 0: x_transposed (kind 0); flag bit 1: replay the
  * untiled fallback kernels (used when the input is not 16-byte aligned or its
- * row stride is not a multiple of 8) instead of the TMA-staged tile kernel.
+ * row stride is not a multiple of 8) instead of the TMA-staged tile kernel;
+ * flag bit 3 (kind 3): the 1x128 x 128x1 GEMM (its epilogue has another
+ * warp layout) instead of the 1x128 x 128x128 ones.
  *   kind 0: bfp8_quant_lhs q           (rows = M, cols = K), scales [Kb, M]
  *   kind 1: bfp8_quant_rhs qT          (rows = N, cols = K), scales [Kb, N]
  *   kind 2: bfp8_quant_weight q        (rows = N, cols = K), scales [Nb, Kb]

@@ -131,7 +131,9 @@ def test_quant_dual_index_replay_exactly_once(M, N, K):
 
 @pytest.mark.parametrize("M,N,K", SHAPES + [(4096, 4096, 128), (2048, 4096, 128), (16384, 1024, 128),
                                              (2048, 4096, 4096), (2000, 4000, 520), (4096, 4096, 8192)])
-def test_gemm_epilogue_index_replay_exactly_once(M, N, K):
-    """The persistent tile schedule stores each output element once."""
-    c, _, oob = B.debug_write_counts(3, M, N, K, 0)
+@pytest.mark.parametrize("col_scales", [0, 8])
+def test_gemm_epilogue_index_replay_exactly_once(M, N, K, col_scales):
+    """The persistent tile schedule stores each output element once (both
+    promotion-warp layouts)."""
+    c, _, oob = B.debug_write_counts(3, M, N, K, col_scales)
     assert oob == 0 and np.all(c == 1)
