@@ -17,9 +17,10 @@
 //               pipe drains its short queue, so with one issuer the pipe sat
 //               idle during every wait for the next buffer and stage.
 //   warp 2      scale loader: per K-block, a_s of the tile's 128 rows and b_s
-//               (BN column scales, or the tile scales) into a 4-slot shared-
-//               memory ring with cp.async, running ahead of the promotion so
-//               that no promotion warp waits on a global load.
+//               (BN column scales, or the tile scales) into a shared-memory
+//               ring of two slots of four K-blocks each, with cp.async, running
+//               ahead of the promotion so that no promotion warp waits on a
+//               global load; one wait and one release per four K-blocks.
 //   warps 4..   promotion/epilogue, EW/4 per tensor-memory lane quarter, each
 //               owning 32 rows x BN/(EW/4) columns of the tile: tcgen05.ld the
 //               K-block's fp32 partial, release the tensor-memory buffer,
@@ -89,10 +90,12 @@ struct GemmCfg {
   static constexpr int kTmemCols = 2 * BN;  // two fp32 partial buffers of BN columns
   static constexpr int kOffB = STAGES * kABytes;
   static constexpr int kOffC = kOffB + STAGES * kBBytes;
-  // scale ring: per K-block a_s[128 rows] then b_s (BN column scales or up to
-  // BN/128 tile scales)
-  static constexpr int kScaleSlots = 4;
-  static constexpr int kScaleBytes = 128 * 4 + BN * 4;
+  // scale ring: kScaleSlots slots of kScaleGroup K-blocks, each K-block
+  // a_s[128 rows] then b_s (BN column scales or up to BN/128 tile scales)
+  static constexpr int kScaleSlots = 2;
+  static constexpr int kScaleGroup = 4;
+  static constexpr int kScaleKbBytes = 128 * 4 + BN * 4;
+  static constexpr int kScaleBytes = kScaleGroup * kScaleKbBytes;
   static constexpr int kOffScale = kOffC;
   static constexpr int kOffBar = kOffScale + kScaleSlots * kScaleBytes;
   static constexpr int kNumBars = 2 * STAGES + 6 + 2 * kScaleSlots;
@@ -142,7 +145,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
   volatile int* never = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
 
-  // barriers: full[S], empty[S], tfull[2], tempty[2], drain (both issuers), stall, sfull[4], sempty[4]
+  // barriers: full[S], empty[S], tfull[2], tempty[2], drain (both issuers), stall, sfull[2], sempty[2]
   auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(STAGES + i); };
   auto tfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + i); };
@@ -263,16 +266,20 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
       const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+      const bool last_tile = tile + (int)gridDim.x >= p.num_tiles;
       for (int kb = 0; kb < p.Kb; ++kb, ++it) {
-        const int sl = (int)(it % Cfg::kScaleSlots);
-        const uint32_t ph = (it / Cfg::kScaleSlots) & 1u;
-        const bool got = mbar_wait_bounded(sempty_bar(sl), ph ^ 1u, p.wait_limit_ns, abort_flag);
-        if (!__all_sync(0xffffffffu, got)) {
-          if (lane == 0) gemm_fail(kErrWaitScale, abort_flag);
-          ok = false;
-          break;
+        const uint32_t grp = it / Cfg::kScaleGroup, sub = it % Cfg::kScaleGroup;
+        const int sl = (int)(grp % Cfg::kScaleSlots);
+        if (sub == 0) {
+          const uint32_t ph = (grp / Cfg::kScaleSlots) & 1u;
+          const bool got = mbar_wait_bounded(sempty_bar(sl), ph ^ 1u, p.wait_limit_ns, abort_flag);
+          if (!__all_sync(0xffffffffu, got)) {
+            if (lane == 0) gemm_fail(kErrWaitScale, abort_flag);
+            ok = false;
+            break;
+          }
         }
-        const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes);
+        const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes + sub * Cfg::kScaleKbBytes);
         // a_s of rows m0 + 4*lane .. +3 (zero past M)
         copy_scales4(slot + 16u * lane, p.sa + (int64_t)kb * p.ldsa, g.m0 + 4 * lane, p.M, p.sa_vec);
         if (SB_MODE == kSbCol) {  // b_s of columns n0 + 128h + 4*lane .. +3 (zero past N)
@@ -286,7 +293,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
           const float* src = SB_MODE == kSbTile ? p.sb + (int64_t)nb * p.ldsb + kb : p.sb + (int64_t)kb * p.ldsb + nb;
           cp_async_4(slot + 512u + 4u * lane, in ? src : p.sb, in ? 4u : 0u);
         }
-        cp_async_mbar_arrive(sfull_bar(sl));
+        // the slot is published once its group is complete (or the CTA's K-blocks end)
+        if (sub == Cfg::kScaleGroup - 1 || (last_tile && kb == p.Kb - 1)) cp_async_mbar_arrive(sfull_bar(sl));
       }
     }
     // let this lane's copies land before the CTA can exit
@@ -303,15 +311,18 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
       const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+      const bool last_tile = tile + (int)gridDim.x >= p.num_tiles;
       float acc[kCols];
 #pragma unroll
       for (int j = 0; j < kCols; ++j) acc[j] = 0.0f;
 
       for (int kb = 0; kb < p.Kb; ++kb, ++it) {
-        const int sl = (int)(it % Cfg::kScaleSlots);
-        const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes);
-        // the loader runs ahead, so the slot is almost always ready: poll, do not sleep
-        const bool sgot = mbar_spin_bounded(sfull_bar(sl), (it / Cfg::kScaleSlots) & 1u, p.wait_limit_ns, abort_flag);
+        const uint32_t grp = it / Cfg::kScaleGroup, sub = it % Cfg::kScaleGroup;
+        const int sl = (int)(grp % Cfg::kScaleSlots);
+        const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes + sub * Cfg::kScaleKbBytes);
+        // once per group: the loader runs ahead, so the slot is almost always ready (poll)
+        const bool sgot = sub != 0 || mbar_spin_bounded(sfull_bar(sl), (grp / Cfg::kScaleSlots) & 1u,
+                                                        p.wait_limit_ns, abort_flag);
         const int buf = (int)(it & 1u);
         const uint32_t tph = (it >> 1) & 1u;
         const bool got = sgot && mbar_wait_bounded(p.debug_stall ? stall_bar : tfull_bar(buf), tph, p.wait_limit_ns,
@@ -369,9 +380,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
             for (int j = 0; j < LDW; ++j) acc[LDW * c + j] = fmaf(scale, __uint_as_float(r[j]), acc[LDW * c + j]);
           }
         }
-        // the slot's scales are no longer needed by this warp
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sempty_bar(sl));
+        // the slot's scales are no longer needed by this warp (end of its group)
+        if (sub == Cfg::kScaleGroup - 1 || (last_tile && kb == p.Kb - 1)) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sempty_bar(sl));
+        }
       }
       if (!ok) break;
 
