@@ -441,15 +441,34 @@ def run_gpu(args, wl):
         gy = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
         gdx, gdw = torch.empty((M, K), dtype=torch.bfloat16, device=dev), torch.empty((N, K), dtype=torch.bfloat16, device=dev)
 
+        # copies on their own streams, overlapped with compute as a caller would:
+        # dY goes in while the forward runs, y comes out while the backward runs
+        h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev_xw, ev_dy, ev_y, ev_b = (torch.cuda.Event() for _ in range(4))
+
         def e2e_step():
-            gx.copy_(hx, non_blocking=True)
-            gw.copy_(hw, non_blocking=True)
-            gdy.copy_(hdy, non_blocking=True)
+            main = torch.cuda.current_stream()
+            h2d.wait_stream(main)
+            with torch.cuda.stream(h2d):
+                gx.copy_(hx, non_blocking=True)
+                gw.copy_(hw, non_blocking=True)
+                ev_xw.record(h2d)
+                gdy.copy_(hdy, non_blocking=True)
+                ev_dy.record(h2d)
+            main.wait_event(ev_xw)
             B.linear_fwd_train(gx, gw, ws, y=gy)
+            ev_y.record(main)
+            d2h.wait_event(ev_y)
+            with torch.cuda.stream(d2h):
+                oy.copy_(gy, non_blocking=True)
+            main.wait_event(ev_dy)
             B.linear_bwd_saved(gdy, ws, M, N, K, dx=gdx, dw=gdw)
-            oy.copy_(gy, non_blocking=True)
-            odx.copy_(gdx, non_blocking=True)
-            odw.copy_(gdw, non_blocking=True)
+            ev_b.record(main)
+            d2h.wait_event(ev_b)
+            with torch.cuda.stream(d2h):
+                odx.copy_(gdx, non_blocking=True)
+                odw.copy_(gdw, non_blocking=True)
+            main.wait_stream(d2h)
 
         for _ in range(args.warmup):
             e2e_step()
