@@ -129,7 +129,8 @@ def test_quant_dual_index_replay_exactly_once(M, N, K):
     assert oob == 0 and c.shape == (K, M) and np.all(c == 1) and np.all(s == 1)
 
 
-@pytest.mark.parametrize("M,N,K", SHAPES + [(4096, 4096, 128), (2048, 4096, 128), (16384, 1024, 128),
+@pytest.mark.parametrize("M,N,K", SHAPES + [(128, 2048, 2048), (300, 384, 4096), (2, 5120, 1280), (64, 1000, 2048),
+                                             (4096, 4096, 128), (2048, 4096, 128), (16384, 1024, 128),
                                              (2048, 4096, 4096), (2000, 4000, 520), (4096, 4096, 8192)])
 @pytest.mark.parametrize("col_scales", [0, 8])
 def test_gemm_epilogue_index_replay_exactly_once(M, N, K, col_scales):

@@ -323,6 +323,19 @@ def test_gemm_multiwave_matches_oracle(M, N, K, mode):
     B.check_device_errors()
 
 
+# few output tiles and a deep K: most SMs idle, one CTA walks every K-block of
+# its tile; ragged M and N
+DEEP_K_SHAPES = [(128, 2048, 2048), (300, 384, 4096), (2, 5120, 1280), (64, 1000, 2048)]
+
+
+@pytest.mark.parametrize("M,N,K", DEEP_K_SHAPES)
+@pytest.mark.parametrize("mode", [O.SB_TILE, O.SB_TILE_T, O.SB_COL])
+def test_gemm_few_tiles_deep_k_matches_oracle(M, N, K, mode):
+    got, ref = _gemm_case(M, N, K, mode, seed=5 * M + N + K + mode, ldc_extra=8, repeats=2)
+    assert_gemm_close(got, ref, f"few-tile deep-K gemm mode {mode} {M}x{N}x{K}")
+    B.check_device_errors()
+
+
 @pytest.mark.parametrize("M,N,K", [(300, 130, 256), (129, 1001, 384), (64, 2051, 128)])
 @pytest.mark.parametrize("mode", [O.SB_TILE, O.SB_COL])
 def test_gemm_ragged_n_aligned_ldc(M, N, K, mode):
