@@ -279,3 +279,104 @@ def linear_wgrad(dy: np.ndarray, x: np.ndarray, rows=None, cols=None) -> np.ndar
     qa, sa = quant_lhs(dy, transposed=True)
     qbT, sb = quant_rhs(x)
     return gemm(qa, sa, qbT, sb, SB_COL, T, rows, cols)
+
+
+# ---- grouped (mixture-of-experts) GEMMs -------------------------------------
+#
+# The pages name a mixture-of-experts path beside the dense one ("Enable
+# blockwise FP8 dense training kernels on ROCm", description: the same
+# FP8_MAX fix made for the MoE path) without spelling it out.  Reading taken
+# here: tokens are sorted by expert, expert e owns token rows
+# offs[e] .. offs[e+1] (non-decreasing offsets), and each expert's linear is
+# exactly the dense method on its slice: forward and input gradient are one
+# dense GEMM per expert on its token rows; the weight gradient of expert e
+# reduces over its own tokens only.  So that the 128-token quantisation groups
+# along the token dim never mix two experts, the weight gradient requires every
+# expert to start on a 128-token boundary (offs[e] % 128 == 0 for e < E).
+# Expert weights are stacked as [E*N, K] with N % 128 == 0, so their 128x128
+# tiles never mix two experts either.
+
+def _group_bounds(offs, e):
+    return int(offs[e]), int(offs[e + 1])
+
+
+def moe_gemm_fwd(qa: np.ndarray, sa: np.ndarray, qw: np.ndarray, sw: np.ndarray,
+                 offs, N: int, K: int) -> np.ndarray:
+    """y[offs[e]:offs[e+1]] = (tokens of expert e) W_e^T for every expert:
+    qa [M_total, lda] 1x128 codes, sa [Kb, ldsa] column-major a_s, qw the
+    stacked expert weights' tile codes [E*N, K], sw their tile scales
+    [E*Nb, Kb].  Rows past offs[E] are not defined (NaN)."""
+    E = len(offs) - 1
+    Nb = _cdiv(N, BLOCK)
+    out = np.full((qa.shape[0], N), np.nan)
+    for e in range(E):
+        r0, r1 = _group_bounds(offs, e)
+        if r1 > r0:
+            out[r0:r1] = gemm(qa[r0:r1], sa[:, r0:r1], qw[e * N:(e + 1) * N], sw[e * Nb:(e + 1) * Nb],
+                              SB_TILE, K)
+    return out
+
+
+def moe_gemm_dgrad(qdy: np.ndarray, sdy: np.ndarray, qwt: np.ndarray, sw: np.ndarray,
+                   offs, N: int, K: int) -> np.ndarray:
+    """dx[offs[e]:offs[e+1]] = dY_e W_e: qdy [M_total, N] codes of dY (1x128
+    along N), sdy [Nb, ldsa]; qwt [K, E*N] the stacked weights' transposed
+    tile codes (expert e in columns e*N .. (e+1)*N), sw [E*Nb, Kb] read
+    transposed."""
+    E = len(offs) - 1
+    Nb = _cdiv(N, BLOCK)
+    out = np.full((qdy.shape[0], K), np.nan)
+    for e in range(E):
+        r0, r1 = _group_bounds(offs, e)
+        if r1 > r0:
+            out[r0:r1] = gemm(qdy[r0:r1], sdy[:, r0:r1], qwt[:, e * N:(e + 1) * N],
+                              sw[e * Nb:(e + 1) * Nb], SB_TILE_T, N)
+    return out
+
+
+def moe_gemm_wgrad(qdyt: np.ndarray, sdyt: np.ndarray, qxt: np.ndarray, sxt: np.ndarray,
+                   offs) -> np.ndarray:
+    """dW[e] = dY_e^T X_e, reduced over expert e's tokens only: qdyt [N, ld]
+    codes of dY^T (1x128 along tokens), sdyt [Tb, ldsa] column-major; qxt
+    [K, ld] codes of X (128x1 along tokens, transposed), sxt [Tb, ldsb].
+    Returns dW [E, N, K]; an expert without tokens gets zeros."""
+    E = len(offs) - 1
+    N, K = qdyt.shape[0], qxt.shape[0]
+    out = np.zeros((E, N, K))
+    for e in range(E):
+        t0, t1 = _group_bounds(offs, e)
+        if t1 > t0:
+            assert t0 % BLOCK == 0, "an expert's tokens must start on a 128-token boundary"
+            b0, b1 = t0 // BLOCK, _cdiv(t1, BLOCK)
+            out[e] = gemm(qdyt[:, t0:t1], sdyt[b0:b1], qxt[:, t0:t1], sxt[b0:b1], SB_COL, t1 - t0)
+    return out
+
+
+def moe_linear_fwd(x: np.ndarray, w: np.ndarray, offs) -> np.ndarray:
+    """Per expert, the dense method's forward on its tokens: x [M_total, K]
+    bf16, w [E, N, K] bf16."""
+    out = np.full((x.shape[0], w.shape[1]), np.nan)
+    for e in range(len(offs) - 1):
+        r0, r1 = _group_bounds(offs, e)
+        if r1 > r0:
+            out[r0:r1] = linear_fwd(x[r0:r1], w[e])
+    return out
+
+
+def moe_linear_dgrad(dy: np.ndarray, w: np.ndarray, offs) -> np.ndarray:
+    out = np.full((dy.shape[0], w.shape[2]), np.nan)
+    for e in range(len(offs) - 1):
+        r0, r1 = _group_bounds(offs, e)
+        if r1 > r0:
+            out[r0:r1] = linear_dgrad(dy[r0:r1], w[e])
+    return out
+
+
+def moe_linear_wgrad(dy: np.ndarray, x: np.ndarray, offs) -> np.ndarray:
+    E = len(offs) - 1
+    out = np.zeros((E, dy.shape[1], x.shape[1]))
+    for e in range(E):
+        r0, r1 = _group_bounds(offs, e)
+        if r1 > r0:
+            out[e] = linear_wgrad(dy[r0:r1], x[r0:r1])
+    return out

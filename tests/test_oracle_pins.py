@@ -389,3 +389,121 @@ def test_unmasked_scale_store_regression_is_catastrophic():
                 bad[idx] = tiny
     c = O.gemm(qa, bad.reshape(sa.shape), qb, sb, O.SB_TILE, K)
     assert O.sqnr_db(ref, c) < 12.0
+
+
+# ---------------------------------------------------------------- grouped (MoE)
+
+def _finite_codes(rng, shape, scale=30.0):
+    return O.cast_e4m3(rng.standard_normal(shape).astype(np.float32) * scale)
+
+
+def test_moe_fwd_brute_force_tiny():
+    """Each token row against its own expert's weight, looked up by scanning
+    the offsets, with the scales expanded by hand; an empty expert and rows
+    past the last offset included."""
+    rng = np.random.default_rng(31)
+    E, N, K, M = 3, 128, 200, 11
+    offs = [0, 5, 5, 9]
+    Kb = 2
+    qa = _finite_codes(rng, (M, K))
+    qw = _finite_codes(rng, (E * N, K))
+    sa = rng.uniform(0.5, 2, (Kb, M)).astype(np.float32)
+    sw = rng.uniform(0.5, 2, (E, Kb)).astype(np.float32)       # [E*Nb, Kb], Nb = 1
+    got = O.moe_gemm_fwd(qa, sa, qw, sw, offs, N, K)
+    T = O.e4m3_table()
+    for m in range(M):
+        e = next((g for g in range(E) if offs[g] <= m < offs[g + 1]), None)
+        if e is None:
+            assert np.all(np.isnan(got[m]))
+            continue
+        for n in range(0, N, 17):
+            c = 0.0
+            for kb in range(Kb):
+                ks = slice(128 * kb, min(128 * kb + 128, K))
+                c += float(sa[kb, m]) * float(sw[e, kb]) * float(np.dot(T[qa[m, ks]], T[qw[e * N + n, ks]]))
+            assert abs(got[m, n] - c) <= 1e-12 * max(1.0, abs(c)), (m, n)
+
+
+def test_moe_fwd_is_the_diagonal_blocks_of_one_dense_gemm():
+    """Tokens x (all experts stacked) as one dense GEMM: expert e's block of
+    that product, on e's token rows, is the grouped result."""
+    rng = np.random.default_rng(32)
+    E, N, K, M = 4, 256, 384, 300
+    offs = [0, 70, 70, 200, 300]
+    Kb, Nb = 3, 2
+    qa = _finite_codes(rng, (M, K))
+    qw = _finite_codes(rng, (E * N, K))
+    sa = rng.uniform(0.5, 2, (Kb, M)).astype(np.float32)
+    sw = rng.uniform(0.5, 2, (E * Nb, Kb)).astype(np.float32)
+    full = O.gemm(qa, sa, qw, sw, O.SB_TILE, K)
+    got = O.moe_gemm_fwd(qa, sa, qw, sw, offs, N, K)
+    for e in range(E):
+        r0, r1 = offs[e], offs[e + 1]
+        np.testing.assert_array_equal(got[r0:r1], full[r0:r1, e * N:(e + 1) * N])
+
+
+def test_moe_dgrad_equals_expanded_dequantised_product():
+    """dY_e W_e with W_e's tile scales expanded to every element and the
+    transposed codes un-transposed by hand."""
+    rng = np.random.default_rng(33)
+    E, N, K, M = 3, 256, 200, 50
+    offs = [0, 20, 20, 50]
+    Nb, Kb = 2, 2
+    qdy = _finite_codes(rng, (M, N))
+    qwt = _finite_codes(rng, (K, E * N))
+    sdy = rng.uniform(0.5, 2, (Nb, M)).astype(np.float32)
+    sw = rng.uniform(0.5, 2, (E * Nb, Kb)).astype(np.float32)
+    got = O.moe_gemm_dgrad(qdy, sdy, qwt, sw, offs, N, K)
+    T = O.e4m3_table()
+    A = T[qdy] * sdy[np.arange(N)[None, :] // 128, np.arange(M)[:, None]]
+    for e in range(E):
+        r0, r1 = offs[e], offs[e + 1]
+        We = T[qwt[:, e * N:(e + 1) * N]].T                                  # [N, K]
+        We = We * sw[e * Nb + np.arange(N)[:, None] // 128, np.arange(K)[None, :] // 128]
+        ref = A[r0:r1] @ We
+        if r1 > r0:
+            np.testing.assert_allclose(got[r0:r1], ref, rtol=1e-12, atol=1e-9 * np.abs(ref).max())
+
+
+def test_moe_wgrad_sums_to_the_dense_weight_gradient():
+    """With experts starting on 128-token boundaries the K-blocks of the dense
+    weight gradient split between the experts, so the experts' gradients add
+    up to the dense one; an expert without tokens gets exactly zero."""
+    rng = np.random.default_rng(34)
+    T_, N, K = 700, 130, 200
+    offs = [0, 256, 256, 640, 700]
+    Tb = 6
+    qdyt = _finite_codes(rng, (N, T_))
+    qxt = _finite_codes(rng, (K, T_))
+    sdyt = rng.uniform(0.5, 2, (Tb, N)).astype(np.float32)
+    sxt = rng.uniform(0.5, 2, (Tb, K)).astype(np.float32)
+    got = O.moe_gemm_wgrad(qdyt, sdyt, qxt, sxt, offs)
+    dense = O.gemm(qdyt, sdyt, qxt, sxt, O.SB_COL, T_)
+    assert np.all(got[1] == 0.0)
+    np.testing.assert_allclose(got.sum(axis=0), dense, rtol=1e-11, atol=1e-9 * np.abs(dense).max())
+    # one expert alone is the dense GEMM with the other experts' tokens zeroed
+    Z = O.e4m3_table()
+    keep = np.zeros(T_, bool)
+    keep[256:640] = True
+    ref = (Z[qdyt] * sdyt[np.arange(T_)[None, :] // 128, np.arange(N)[:, None]] * keep) @ \
+          (Z[qxt] * sxt[np.arange(T_)[None, :] // 128, np.arange(K)[:, None]]).T
+    np.testing.assert_allclose(got[2], ref, rtol=1e-11, atol=1e-9 * np.abs(ref).max())
+
+
+def test_moe_linear_with_shared_weights_is_the_dense_linear():
+    """When every expert holds the same weight, grouping the tokens changes
+    nothing: row-wise quantisation does not see the groups, and (experts on
+    128-token boundaries) neither do the token-dim groups of the weight
+    gradient, whose expert sums add up to the dense gradient."""
+    M, N, K = 384, 256, 256
+    offs = [0, 128, 128, 384]
+    x = S.normal_bf16((M, K), 1.0, seed=41)
+    w = S.normal_bf16((N, K), 0.02, seed=42)
+    dy = S.normal_bf16((M, N), 1e-3, seed=43)
+    ws = np.stack([w] * 3)
+    np.testing.assert_array_equal(O.moe_linear_fwd(x, ws, offs), O.linear_fwd(x, w))
+    np.testing.assert_array_equal(O.moe_linear_dgrad(dy, ws, offs), O.linear_dgrad(dy, w))
+    dw = O.moe_linear_wgrad(dy, x, offs)
+    ref = O.linear_wgrad(dy, x)
+    np.testing.assert_allclose(dw.sum(axis=0), ref, rtol=1e-11, atol=1e-12 * np.abs(ref).max())
+    assert np.all(dw[1] == 0.0)
