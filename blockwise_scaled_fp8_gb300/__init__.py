@@ -24,7 +24,7 @@ EXPORTS = [
     "bfp8_linear_fwd", "bfp8_linear_bwd", "bfp8_cast_e4m3", "bfp8_check_device_errors",
     "bfp8_debug_write_counts", "bfp8_debug_gemm_stall", "bfp8_quant_dual",
     "bfp8_linear_train_workspace_size", "bfp8_linear_fwd_train", "bfp8_linear_bwd_saved",
-    "bfp8_linear_fwd_static",
+    "bfp8_linear_fwd_static", "bfp8_gemm_grouped_1x128_128x128", "bfp8_gemm_grouped_1x128_128x1",
 ]
 
 _lib = None
@@ -70,6 +70,10 @@ def lib() -> ctypes.CDLL:
     L.bfp8_linear_fwd_train.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
     L.bfp8_linear_bwd_saved.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
     L.bfp8_linear_fwd_static.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+    L.bfp8_gemm_grouped_1x128_128x128.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, vp, i64, vp, i64,
+                                                  i64, i64, i64, vp]
+    L.bfp8_gemm_grouped_1x128_128x1.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64,
+                                                i64, i64, i64, vp]
     L.bfp8_debug_gemm_stall.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, i64, i64, vp]
     for name in EXPORTS:
         if name not in ("bfp8_last_error", "bfp8_linear_workspace_size", "bfp8_linear_train_workspace_size"):
@@ -230,6 +234,81 @@ def gemm_1x128_128x1(qa, sa, qb, sb, K: int, out=None, M=None, N=None):
     _check(lib().bfp8_gemm_1x128_128x1(_p(qa), qa.stride(0), _p(sa), sa.stride(0), _p(qb), qb.stride(0),
                                        _p(sb), sb.stride(0), _p(out), out.stride(0), M, N, K, _stream()))
     return out
+
+
+# ---------------------------------------------------------------------------
+# Grouped (mixture-of-experts) GEMMs: tokens sorted by expert, expert e owning
+# token rows offs[e] .. offs[e+1] (offs: int32 tensor [E+1] on the device)
+# ---------------------------------------------------------------------------
+
+def _offs(offs):
+    torch = _torch()
+    if offs.dtype != torch.int32 or offs.dim() != 1 or not offs.is_contiguous():
+        raise ValueError("offs must be a contiguous 1-d int32 tensor of E+1 offsets")
+    return offs
+
+
+def gemm_grouped_1x128_128x128(qa, sa, qb, sb, offs, N: int, K: int, sb_transposed: bool = False, out=None):
+    """Per expert e, C[offs[e]:offs[e+1]] = A[offs[e]:offs[e+1]] B_e.  Forward
+    (sb_transposed False): qb [E*N, ldb] stacked weight codes, sb [E*Nb, ldsb]
+    their tile scales.  Input gradient (True, K = the experts' output
+    features): qb [N, ldb] the stacked weight's transposed codes (expert e in
+    columns e*K ..), sb [E*Kb, ldsb].  Returns C [M_total, N] bf16 (rows outside
+    the experts are left as they were in ``out``)."""
+    torch = _torch()
+    offs = _offs(offs)
+    M_total = qa.shape[0]
+    if out is None:
+        out = torch.empty((M_total, N), dtype=torch.bfloat16, device=qa.device)
+    _check(lib().bfp8_gemm_grouped_1x128_128x128(_p(qa), qa.stride(0), _p(sa), sa.stride(0), _p(qb), qb.stride(0),
+                                                 _p(sb), sb.stride(0), int(sb_transposed), _p(offs),
+                                                 offs.numel() - 1, _p(out), out.stride(0), M_total, N, K,
+                                                 _stream()))
+    return out
+
+
+def gemm_grouped_1x128_128x1(qa, sa, qb, sb, offs, T: int, out=None):
+    """Per expert e, dW[e] = A[:, tokens of e] B[tokens of e, :]: qa [M, lda]
+    (1x128 along tokens, sa [Tb, ldsa]), qb [N, ldb] (128x1 along tokens,
+    transposed; sb [Tb, ldsb]).  Every expert starts on a 128-token boundary.
+    Returns dW [E, M, N] bf16."""
+    torch = _torch()
+    offs = _offs(offs)
+    E = offs.numel() - 1
+    M, N = qa.shape[0], qb.shape[0]
+    if out is None:
+        out = torch.empty((E, M, N), dtype=torch.bfloat16, device=qa.device)
+    _check(lib().bfp8_gemm_grouped_1x128_128x1(_p(qa), qa.stride(0), _p(sa), sa.stride(0), _p(qb), qb.stride(0),
+                                               _p(sb), sb.stride(0), _p(offs), E, _p(out), out.stride(1),
+                                               out.stride(0), M, N, T, _stream()))
+    return out
+
+
+def moe_linear_fwd(x, w, offs, y=None):
+    """Mixture-of-experts forward y_e = x_e W_e^T: x [M_total, K] bf16 tokens
+    sorted by expert, w [E, N, K] bf16 (N % 128 == 0, so the stacked weight's
+    128x128 tiles stay inside one expert).  Returns (y, saved) where saved
+    holds the quantised operands the backward reuses."""
+    E, N, K = w.shape
+    if N % 128:
+        raise ValueError("moe_linear_fwd: the experts' output features must be a multiple of 128")
+    qx, sx, qxt, sxt = quant_dual(x)
+    qw, qwt, sw = quant_weight(w.reshape(E * N, K), with_q=True, with_t=True)
+    y = gemm_grouped_1x128_128x128(qx, sx, qw, sw, offs, N, K, out=y)
+    return y, (qxt, sxt, qwt, sw)
+
+
+def moe_linear_bwd(dy, saved, offs, dx=None, dw=None):
+    """Mixture-of-experts backward from moe_linear_fwd's saved operands:
+    dx_e = dy_e W_e, dW_e = dy_e^T x_e (every expert starting on a 128-token
+    boundary).  Returns (dx [M_total, K], dW [E, N, K])."""
+    qxt, sxt, qwt, sw = saved
+    M_total, N = dy.shape
+    K = qxt.shape[0]
+    qdy, sdy, qdyt, sdyt = quant_dual(dy)
+    dx = gemm_grouped_1x128_128x128(qdy, sdy, qwt, sw, offs, K, N, sb_transposed=True, out=dx)
+    dw = gemm_grouped_1x128_128x1(qdyt, sdyt, qxt, sxt, offs, M_total, out=dw)
+    return dx, dw
 
 
 # ---------------------------------------------------------------------------

@@ -253,6 +253,92 @@ bfp8_status bfp8_gemm_1x128_128x1(const void* qa, int64_t lda, const float* sa, 
   return gemm_common("bfp8_gemm_1x128_128x1", a, stream);
 }
 
+// ---------------------------------------------------------------------------
+// Grouped (mixture-of-experts) GEMMs
+// ---------------------------------------------------------------------------
+
+static bfp8_status grouped_common(const char* fn, const GemmGroupArgs& ga, bfp8_stream_t stream) {
+  const GemmArgs& a = ga.g;
+  CHECK_ARG(ga.E >= 1 && ga.E <= kMaxGroups, "%s: E=%lld must be in [1, %d]", fn, (long long)ga.E, kMaxGroups);
+  CHECK_ARG(ga.offs && al4(ga.offs), "%s: offs must be a 4-byte aligned device pointer", fn);
+  const bool rows = ga.kind == kGroupRows;
+  bfp8_status st = check_dims(fn, ga.M_total, a.N, rows ? a.K : a.M);
+  if (st != BFP8_OK) return st;
+  const int64_t K = rows ? a.K : ga.M_total;  // the reduction extent of the maps
+  if ((rows ? ga.M_total : a.M) == 0 || a.N == 0) return BFP8_OK;
+  // (an empty reduction is the kernel's job too: every tile then has no
+  // K-blocks and its outputs are written as zeros)
+  CHECK_ARG(a.qa && a.qb && a.sa && a.sb && a.c, "%s: null pointer", fn);
+  CHECK_ARG(al16(a.qa) && al16(a.qb), "%s: qa and qb must be 16-byte aligned", fn);
+  CHECK_ARG(al4(a.sa) && al4(a.sb) && al2(a.c), "%s: sa/sb must be 4-byte and c 2-byte aligned", fn);
+  // input gradient: expert e's B starts at K column e*K of the map, and a TMA
+  // load must start on a 16-byte boundary
+  CHECK_ARG(!(rows && ga.b_k_step && ga.E > 1 && K % 16 != 0),
+            "%s: the input-gradient form needs K %% 16 == 0 (K=%lld) when E > 1", fn, (long long)K);
+  const int64_t b_inner = rows && ga.b_k_step ? ga.E * K : K;
+  CHECK_ARG(a.lda >= K && a.lda % 16 == 0, "%s: lda=%lld must be >= %lld and a multiple of 16", fn,
+            (long long)a.lda, (long long)K);
+  CHECK_ARG(a.ldb >= b_inner && a.ldb % 16 == 0, "%s: ldb=%lld must be >= %lld and a multiple of 16", fn,
+            (long long)a.ldb, (long long)b_inner);
+  CHECK_ARG(a.ldsa >= (rows ? ga.M_total : a.M), "%s: ldsa=%lld too small", fn, (long long)a.ldsa);
+  const int64_t Kb = cdiv(K, kBlock), Nb = cdiv(a.N, kBlock);
+  if (a.sb_mode == kSbTile)
+    CHECK_ARG(a.ldsb >= Kb, "%s: ldsb=%lld < ceil(K/128)=%lld", fn, (long long)a.ldsb, (long long)Kb);
+  else if (a.sb_mode == kSbTileT)
+    CHECK_ARG(a.ldsb >= Nb, "%s: ldsb=%lld < ceil(N/128)=%lld", fn, (long long)a.ldsb, (long long)Nb);
+  else
+    CHECK_ARG(a.ldsb >= a.N, "%s: ldsb=%lld < N=%lld", fn, (long long)a.ldsb, (long long)a.N);
+  CHECK_ARG(a.ldc >= a.N, "%s: ldc=%lld < N=%lld", fn, (long long)a.ldc, (long long)a.N);
+  if (!rows)
+    CHECK_ARG(ga.c_step >= a.M * a.ldc, "%s: c_expert_stride=%lld < M*ldc=%lld", fn, (long long)ga.c_step,
+              (long long)(a.M * a.ldc));
+  int sms = 0;
+  if ((st = check_device(&sms)) != BFP8_OK) return st;
+  const char* msg = nullptr;
+  cudaError_t e = launch_gemm_grouped(ga, sms, (cudaStream_t)stream, &msg);
+  if (e != cudaSuccess) {
+    if (msg) return fail(BFP8_ERR_INVALID_ARG, "%s: %s", fn, msg);
+    return cuda_fail(e, fn);
+  }
+  return BFP8_OK;
+}
+
+bfp8_status bfp8_gemm_grouped_1x128_128x128(const void* qa, int64_t lda, const float* sa, int64_t ldsa,
+                                            const void* qb, int64_t ldb, const float* sb, int64_t ldsb,
+                                            int sb_transposed, const int32_t* offs, int64_t E, void* c,
+                                            int64_t ldc, int64_t M_total, int64_t N, int64_t K,
+                                            bfp8_stream_t stream) {
+  GemmGroupArgs ga;
+  ga.g = GemmArgs{qa, lda, sa, ldsa, qb, ldb, sb, ldsb, sb_transposed ? kSbTileT : kSbTile, c, ldc, 0, N, K};
+  ga.kind = kGroupRows;
+  ga.offs = offs;
+  ga.E = E;
+  ga.M_total = M_total;
+  // forward: expert e's weight rows e*N ..; input gradient: its K columns e*K ..
+  ga.b_row_step = sb_transposed ? 0 : N;
+  ga.b_k_step = sb_transposed ? K : 0;
+  ga.sb_step = sb_transposed ? cdiv(K, kBlock) * ldsb : cdiv(N, kBlock) * ldsb;
+  ga.c_step = 0;
+  return grouped_common("bfp8_gemm_grouped_1x128_128x128", ga, stream);
+}
+
+bfp8_status bfp8_gemm_grouped_1x128_128x1(const void* qa, int64_t lda, const float* sa, int64_t ldsa,
+                                          const void* qb, int64_t ldb, const float* sb, int64_t ldsb,
+                                          const int32_t* offs, int64_t E, void* c, int64_t ldc,
+                                          int64_t c_expert_stride, int64_t M, int64_t N, int64_t T,
+                                          bfp8_stream_t stream) {
+  GemmGroupArgs ga;
+  ga.g = GemmArgs{qa, lda, sa, ldsa, qb, ldb, sb, ldsb, kSbCol, c, ldc, M, N, 0};
+  ga.kind = kGroupRed;
+  ga.offs = offs;
+  ga.E = E;
+  ga.M_total = T;
+  ga.b_row_step = ga.b_k_step = 0;
+  ga.sb_step = 0;
+  ga.c_step = c_expert_stride;
+  return grouped_common("bfp8_gemm_grouped_1x128_128x1", ga, stream);
+}
+
 bfp8_status bfp8_debug_gemm_stall(const void* qa, int64_t lda, const float* sa, int64_t ldsa, const void* qb,
                                   int64_t ldb, const float* sb, int64_t ldsb, void* c, int64_t ldc, int64_t M,
                                   int64_t N, int64_t K, int64_t wait_limit_us, bfp8_stream_t stream) {
@@ -283,6 +369,10 @@ bfp8_status bfp8_check_device_errors(bfp8_stream_t stream) {
   e = quant_read_errors(&qbits);
   if (e != cudaSuccess) return cuda_fail(e, "bfp8_check_device_errors: read flag");
   if (qbits) return fail(BFP8_ERR_TIMEOUT, "quantisation kernel gave up waiting for its TMA tile loads");
+  if (bits & 64u)  // kErrGroupOffsets
+    return fail(BFP8_ERR_INVALID_ARG,
+                "grouped GEMM: expert offsets decreasing, outside [0, total tokens], or (weight gradient) "
+                "not on a 128-token boundary; the affected experts were computed with clamped offsets");
   if (bits) {
     return fail(BFP8_ERR_TIMEOUT,
                 "GEMM kernel gave up on a bounded wait (flags 0x%x: %s%s%s%s%s)", bits,

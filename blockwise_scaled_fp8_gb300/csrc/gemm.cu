@@ -53,6 +53,7 @@ enum : uint32_t {
   kErrWaitTmemFull = 1u << 3,   // epilogue: a partial product never arrived
   kErrWaitDrain = 1u << 4,      // teardown: MMAs or copies in flight never finished
   kErrWaitScale = 1u << 5,      // scale ring: a slot was never filled / released
+  kErrGroupOffsets = 1u << 6,   // grouped GEMM: expert offsets decreasing, out of range or misaligned
 };
 
 struct GemmParams {
@@ -69,6 +70,27 @@ struct GemmParams {
   int sb_vec;  // 16-byte b_s copies allowed (ldsb % 4 == 0, sb 16-byte aligned)
   uint64_t wait_limit_ns;
   int debug_stall;  // test hook: the promotion warps wait on a barrier nothing arrives on
+  // grouped (mixture-of-experts) forms, unused by the dense GEMM:
+  const int32_t* offs;  // [E+1] token offsets of the experts (device memory)
+  int E;
+  int M_total;          // kGroupRows: token rows of A and C;  kGroupRed: token extent of A and B
+  int b_row_step;       // per expert: first row of its B in the B map (forward)
+  int b_k_step;         // per expert: first K column of its B in the B map (input gradient)
+  int64_t sb_step;      // per expert: offset of its b_s (elements)
+  int64_t c_step;       // per expert: offset of its C (elements; weight gradient)
+};
+
+// One output tile's work: where its operands sit in the two tensor maps, its
+// K-blocks, and where its scales and outputs are.
+struct GemmJob {
+  int a_row, b_row;  // first rows of the tile in the A and B maps
+  int a_k, b_k;      // first K columns (elements) in the A and B maps
+  int kb_s;          // first K-block index in a_s / b_s
+  int kbn;           // K-blocks of the tile (0: the tile is all zeros)
+  int rows;          // valid rows from a_row (>= 1; rows past 128 belong to other tiles)
+  int n0;            // first output column
+  int e;             // expert (b_s at sb + e * sb_step)
+  int64_t c_off;     // element offset of the output C[first row][n0]
 };
 
 template <int BN, int STAGES, int EW>
@@ -101,7 +123,9 @@ struct GemmCfg {
   static constexpr int kNumBars = 2 * STAGES + 6 + 2 * kScaleSlots;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
-  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+  // grouped forms only: the experts' offsets and first tiles
+  static constexpr int kGroupTabBytes = 2 * (kMaxGroups + 1) * 4;
+  static_assert(kSmemBytes + kGroupTabBytes <= 227 * 1024, "shared memory budget");
   static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
                 "tensor-memory allocation must be a power of two in [32, 512]");
 };
@@ -127,7 +151,104 @@ __device__ __forceinline__ void copy_scales4(uint32_t dst, const float* v, int i
   }
 }
 
-template <int BN, int STAGES, int SB_MODE, int LDW, int EW>
+// The experts' clamped offsets o[0..E] (running maximum of offs, within
+// [0, M_total]) and, for kGroupRows, the first tile of each expert, built by
+// one warp into shared memory.  Offsets that had to be clamped, and (kGroupRed)
+// experts not starting on a 128-token boundary, set kErrGroupOffsets.
+template <int GROUP>
+__device__ void gemm_build_groups(const GemmParams& p, int* s_offs, int* s_start, int lane) {
+  const int n = p.E + 1;
+  const int per = (n + 31) / 32;
+  const int i0 = min(lane * per, n), i1 = min(i0 + per, n);
+  int run = 0;
+  for (int i = i0; i < i1; ++i) {
+    run = max(run, min(max(p.offs[i], 0), p.M_total));
+    s_offs[i] = run;
+  }
+  int incl = run;  // running maximum over the chunks of lanes <= this one
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl = max(incl, y);
+  }
+  int excl = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) excl = 0;
+  bool bad = false;
+  for (int i = i0; i < i1; ++i) {
+    const int raw = p.offs[i];
+    const int v = max(s_offs[i], excl);
+    s_offs[i] = v;
+    bad |= raw != v;
+    if (GROUP == kGroupRed && i < p.E) bad |= (v % kBK) != 0;
+  }
+  __syncwarp();
+  if (GROUP == kGroupRows) {
+    int cnt = 0;  // tiles of this lane's experts
+    for (int i = i0; i < i1 && i < p.E; ++i) cnt += (int)cdiv(s_offs[i + 1] - s_offs[i], kBM) * p.num_n;
+    int sum = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, sum, off);
+      if (lane >= off) sum += y;
+    }
+    int acc = sum - cnt;
+    for (int i = i0; i < i1; ++i) {
+      s_start[i] = acc;
+      if (i < p.E) acc += (int)cdiv(s_offs[i + 1] - s_offs[i], kBM) * p.num_n;
+    }
+  }
+  if (__any_sync(0xffffffffu, bad) && lane == 0 && blockIdx.x == 0) atomicOr(&g_gemm_error, kErrGroupOffsets);
+}
+
+template <int GROUP, int BN>
+__device__ __forceinline__ GemmJob gemm_job(int tile, const GemmParams& p, const int* s_offs, const int* s_start) {
+  GemmJob j;
+  if constexpr (GROUP == kGroupRows) {
+    const int e = group_of_tile(s_start, p.E, tile);
+    const int r0 = s_offs[e], re = s_offs[e + 1] - r0;
+    const GemmTile g = gemm_tile(tile - s_start[e], (int)cdiv(re, kBM), p.num_n, BN);
+    j.a_row = r0 + g.m0;
+    j.rows = re - g.m0;
+    j.b_row = e * p.b_row_step + g.n0;
+    j.a_k = 0;
+    j.b_k = e * p.b_k_step;
+    j.kb_s = 0;
+    j.kbn = p.Kb;
+    j.n0 = g.n0;
+    j.e = e;
+    j.c_off = (int64_t)j.a_row * p.ldc + g.n0;
+  } else if constexpr (GROUP == kGroupRed) {
+    const int per = p.num_m * p.num_n;
+    const int e = tile / per;
+    const GemmTile g = gemm_tile(tile - e * per, p.num_m, p.num_n, BN);
+    const int t0 = s_offs[e], t1 = s_offs[e + 1];
+    j.kb_s = t0 / kBK;
+    j.kbn = t1 > t0 ? (int)cdiv(t1, kBK) - j.kb_s : 0;
+    j.a_k = j.kb_s * kBK;
+    j.b_k = j.a_k;
+    j.a_row = g.m0;
+    j.rows = (int)p.M - g.m0;
+    j.b_row = g.n0;
+    j.n0 = g.n0;
+    j.e = e;
+    j.c_off = (int64_t)e * p.c_step + (int64_t)g.m0 * p.ldc + g.n0;
+  } else {
+    const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+    j.a_row = g.m0;
+    j.rows = (int)p.M - g.m0;
+    j.b_row = g.n0;
+    j.a_k = 0;
+    j.b_k = 0;
+    j.kb_s = 0;
+    j.kbn = p.Kb;
+    j.n0 = g.n0;
+    j.e = 0;
+    j.c_off = (int64_t)g.m0 * p.ldc + g.n0;
+  }
+  return j;
+}
+
+template <int BN, int STAGES, int SB_MODE, int LDW, int EW, int GROUP>
 __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tma_a,
                           const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
@@ -144,6 +265,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
   volatile int* never = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
+  // grouped forms: the experts' offsets and first tiles (kGroupTabBytes past the barriers)
+  int* s_offs = reinterpret_cast<int*>(smem + Cfg::kOffMisc + 16);
+  int* s_start = s_offs + (kMaxGroups + 1);
 
   // barriers: full[S], empty[S], tfull[2], tempty[2], drain (both issuers), stall, sfull[2], sempty[2]
   auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -186,10 +310,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     tma_prefetch_desc(&tma_a);
     tma_prefetch_desc(&tma_b);
   }
+  if (GROUP != kGroupNone && warp == 2) gemm_build_groups<GROUP>(p, s_offs, s_start, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  const int num_tiles = GROUP == kGroupRows ? s_start[p.E] : p.num_tiles;
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kCtrlRegs));
   if (warp == 0) {
@@ -197,9 +323,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
-        for (int kb = 0; kb < p.Kb; ++kb, ++it) {
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const GemmJob j = gemm_job<GROUP, BN>(tile, p, s_offs, s_start);
+        for (int kb = 0; kb < j.kbn; ++kb, ++it) {
           const int st = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(empty_bar(st), ph ^ 1u, p.wait_limit_ns, abort_flag)) {
@@ -208,8 +334,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(full_bar(st), (uint32_t)Cfg::kStageBytes);
-          tma_load_2d(sA + (uint32_t)(st * Cfg::kABytes), &tma_a, full_bar(st), kb * kBK, g.m0);
-          tma_load_2d(sB + (uint32_t)(st * Cfg::kBBytes), &tma_b, full_bar(st), kb * kBK, g.n0);
+          tma_load_2d(sA + (uint32_t)(st * Cfg::kABytes), &tma_a, full_bar(st), j.a_k + kb * kBK, j.a_row);
+          tma_load_2d(sB + (uint32_t)(st * Cfg::kBBytes), &tma_b, full_bar(st), j.b_k + kb * kBK, j.b_row);
         }
       }
       if (!ok) {
@@ -227,8 +353,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
       const uint32_t mine = warp == 1 ? 0u : 1u;  // the K-block steps (and TMEM buffer) of this issuer
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-        for (int kb = 0; kb < p.Kb; ++kb, ++it) {
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int kbn = gemm_job<GROUP, BN>(tile, p, s_offs, s_start).kbn;
+        for (int kb = 0; kb < kbn; ++kb, ++it) {
           if ((it & 1u) != mine) continue;
           const int st = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
@@ -262,14 +389,22 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ scale loader
-    uint32_t it = 0;
+    // Scale groups: the dense GEMM's run on over the CTA's consecutive
+    // K-block steps (grp = step / kScaleGroup); a grouped GEMM's tiles have
+    // different K-block counts (some none), so there a group never spans two
+    // tiles and grp counts the groups published so far.
+    uint32_t it = 0, grp = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-      const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
-      const bool last_tile = tile + (int)gridDim.x >= p.num_tiles;
-      for (int kb = 0; kb < p.Kb; ++kb, ++it) {
-        const uint32_t grp = it / Cfg::kScaleGroup, sub = it % Cfg::kScaleGroup;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      const GemmJob j = gemm_job<GROUP, BN>(tile, p, s_offs, s_start);
+      const bool last_tile = tile + (int)gridDim.x >= num_tiles;
+      const bool sa_vec = p.sa_vec && (j.a_row & 3) == 0;
+      const float* sbe = p.sb + (GROUP != kGroupNone ? (int64_t)j.e * p.sb_step : 0);
+      for (int kb = 0; kb < j.kbn; ++kb, ++it) {
+        if (GROUP == kGroupNone) grp = it / Cfg::kScaleGroup;
+        const uint32_t sub = (GROUP == kGroupNone ? it : (uint32_t)kb) % Cfg::kScaleGroup;
         const int sl = (int)(grp % Cfg::kScaleSlots);
+        const int kbs = j.kb_s + kb;
         if (sub == 0) {
           const uint32_t ph = (grp / Cfg::kScaleSlots) & 1u;
           const bool got = mbar_wait_bounded(sempty_bar(sl), ph ^ 1u, p.wait_limit_ns, abort_flag);
@@ -280,21 +415,24 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
           }
         }
         const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes + sub * Cfg::kScaleKbBytes);
-        // a_s of rows m0 + 4*lane .. +3 (zero past M)
-        copy_scales4(slot + 16u * lane, p.sa + (int64_t)kb * p.ldsa, g.m0 + 4 * lane, p.M, p.sa_vec);
+        // a_s of the tile's rows 4*lane .. +3 (zero past its valid rows)
+        copy_scales4(slot + 16u * lane, p.sa + (int64_t)kbs * p.ldsa + j.a_row, 4 * lane, j.rows, sa_vec);
         if (SB_MODE == kSbCol) {  // b_s of columns n0 + 128h + 4*lane .. +3 (zero past N)
 #pragma unroll
           for (int h = 0; h < BN / 128; ++h)
-            copy_scales4(slot + 512u + 512u * h + 16u * lane, p.sb + (int64_t)kb * p.ldsb, g.n0 + 128 * h + 4 * lane,
-                         p.N, p.sb_vec);
+            copy_scales4(slot + 512u + 512u * h + 16u * lane, sbe + (int64_t)kbs * p.ldsb + j.n0, 128 * h + 4 * lane,
+                         p.N - j.n0, p.sb_vec);
         } else if (lane < BN / 128) {  // tile scale of the 128 columns n0 + 128*lane (zero past N)
-          const int nb = g.n0 / kBlock + lane;
+          const int nb = j.n0 / kBlock + lane;
           const bool in = nb < p.Nb;
-          const float* src = SB_MODE == kSbTile ? p.sb + (int64_t)nb * p.ldsb + kb : p.sb + (int64_t)kb * p.ldsb + nb;
+          const float* src = SB_MODE == kSbTile ? sbe + (int64_t)nb * p.ldsb + kbs : sbe + (int64_t)kbs * p.ldsb + nb;
           cp_async_4(slot + 512u + 4u * lane, in ? src : p.sb, in ? 4u : 0u);
         }
-        // the slot is published once its group is complete (or the CTA's K-blocks end)
-        if (sub == Cfg::kScaleGroup - 1 || (last_tile && kb == p.Kb - 1)) cp_async_mbar_arrive(sfull_bar(sl));
+        // the slot is published once its group is complete (or the K-blocks end)
+        if (sub == Cfg::kScaleGroup - 1 || (kb == j.kbn - 1 && (GROUP != kGroupNone || last_tile))) {
+          cp_async_mbar_arrive(sfull_bar(sl));
+          ++grp;
+        }
       }
     }
     // let this lane's copies land before the CTA can exit
@@ -307,17 +445,19 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     const int row = epi_row(e, lane);
     const int col0 = epi_col0(e, BN, EW);
     const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
-    uint32_t it = 0;
+    uint32_t it = 0, grp = 0;  // K-block steps; scale groups as the loader counts them
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-      const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
-      const bool last_tile = tile + (int)gridDim.x >= p.num_tiles;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      // (the rest of the tile's job is recomputed for the epilogue: fewer live registers)
+      const int kbn = GROUP == kGroupNone ? p.Kb : gemm_job<GROUP, BN>(tile, p, s_offs, s_start).kbn;
+      const bool last_tile = tile + (int)gridDim.x >= num_tiles;
       float acc[kCols];
 #pragma unroll
       for (int j = 0; j < kCols; ++j) acc[j] = 0.0f;
 
-      for (int kb = 0; kb < p.Kb; ++kb, ++it) {
-        const uint32_t grp = it / Cfg::kScaleGroup, sub = it % Cfg::kScaleGroup;
+      for (int kb = 0; kb < kbn; ++kb, ++it) {
+        if (GROUP == kGroupNone) grp = it / Cfg::kScaleGroup;
+        const uint32_t sub = (GROUP == kGroupNone ? it : (uint32_t)kb) % Cfg::kScaleGroup;
         const int sl = (int)(grp % Cfg::kScaleSlots);
         const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes + sub * Cfg::kScaleKbBytes);
         // once per group: the loader runs ahead, so the slot is almost always ready (poll)
@@ -381,9 +521,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
           }
         }
         // the slot's scales are no longer needed by this warp (end of its group)
-        if (sub == Cfg::kScaleGroup - 1 || (last_tile && kb == p.Kb - 1)) {
+        if (sub == Cfg::kScaleGroup - 1 || (kb == kbn - 1 && (GROUP != kGroupNone || last_tile))) {
           __syncwarp();
           if (lane == 0) mbar_arrive(sempty_bar(sl));
+          ++grp;
         }
       }
       if (!ok) break;
@@ -394,6 +535,22 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
       // the warp then writes 32/G row segments of 16*G contiguous bytes.  Only
       // rows < M and columns < N are written.
       {
+        // output origin, valid rows / columns from it (the dense GEMM keeps the
+        // plain tile arithmetic: fewer live registers at this point)
+        int64_t c_row0, c_col0, c_rows, c_cols;
+        if constexpr (GROUP == kGroupNone) {
+          const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+          c_row0 = g.m0;
+          c_col0 = g.n0;
+          c_rows = p.M - g.m0;
+          c_cols = p.N - g.n0;
+        } else {
+          const GemmJob job = gemm_job<GROUP, BN>(tile, p, s_offs, s_start);
+          c_row0 = 0;
+          c_col0 = job.c_off;
+          c_rows = job.rows;
+          c_cols = p.N - job.n0;
+        }
         constexpr int kG = kCols / 8 >= 8 ? 8 : kCols / 8;  // chunks per transposed block (epi_group)
         const int pos = lane % kG;
 #pragma unroll
@@ -419,18 +576,18 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
               }
             }
           }
-          const int n = g.n0 + epi_store_col(e, lane, sg, kG, BN, EW);
+          const int n = epi_store_col(e, lane, sg, kG, BN, EW);  // tile-local
 #pragma unroll
           for (int i = 0; i < kG; ++i) {
-            const int mr = g.m0 + epi_store_row(e, lane, i, kG);
-            if (mr >= p.M || n >= p.N) continue;
-            uint16_t* dst = p.c + (int64_t)mr * p.ldc + n;
-            if (p.c_vec && n + 8 <= p.N) {
+            const int mr = epi_store_row(e, lane, i, kG);
+            if (mr >= c_rows || n >= c_cols) continue;
+            uint16_t* dst = p.c + (c_row0 + mr) * p.ldc + c_col0 + n;
+            if (p.c_vec && n + 8 <= c_cols) {
               *reinterpret_cast<uint4*>(dst) = make_uint4(X[i][0], X[i][1], X[i][2], X[i][3]);
             } else {
 #pragma unroll
               for (int b = 0; b < 8; ++b)
-                if (n + b < p.N) dst[b] = (uint16_t)(X[i][b >> 1] >> (16 * (b & 1)));
+                if (n + b < c_cols) dst[b] = (uint16_t)(X[i][b >> 1] >> (16 * (b & 1)));
             }
           }
         }
@@ -504,20 +661,20 @@ constexpr int gemm_ldw() {
   return EW == 16 ? (BN == 256 && MODE != kSbCol ? 32 : 16) : (MODE != kSbCol ? 64 : 32);
 }
 
-template <int BN, int STAGES, int MODE>
+template <int BN, int STAGES, int MODE, int GROUP = kGroupNone>
 static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb,
                             const GemmParams& p, int64_t grid, cudaStream_t st) {
   constexpr int EW = gemm_ew<MODE>(), LDW = gemm_ldw<BN, MODE, EW>();
   using Cfg = GemmCfg<BN, STAGES, EW>;
+  constexpr int kSmem = Cfg::kSmemBytes + (GROUP != kGroupNone ? Cfg::kGroupTabBytes : 0);
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    attr_err = cudaFuncSetAttribute(gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW, GROUP>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW>
-      <<<(unsigned)grid, Cfg::kThreads, Cfg::kSmemBytes, st>>>(ma, mb, p);
+  gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW, GROUP><<<(unsigned)grid, Cfg::kThreads, kSmem, st>>>(ma, mb, p);
   return cudaGetLastError();
 }
 
@@ -555,6 +712,11 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const c
   p.sb_vec = (a.ldsb % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.sb) & 15u) == 0);
   p.wait_limit_ns = wait_limit_ns;
   p.debug_stall = debug_stall;
+  p.offs = nullptr;
+  p.E = 0;
+  p.M_total = 0;
+  p.b_row_step = p.b_k_step = 0;
+  p.sb_step = p.c_step = 0;
   const int64_t grid = gemm_grid(a.M, a.N, bn, num_sms);
   if (bn == 256) {
     switch (a.sb_mode) {
@@ -568,6 +730,76 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const c
     case kSbTileT: return run_gemm<128, 6, kSbTileT>(ma, mb, p, grid, st);
     default: return run_gemm<128, 6, kSbCol>(ma, mb, p, grid, st);
   }
+}
+
+cudaError_t launch_gemm_grouped(const GemmGroupArgs& ga, int num_sms, cudaStream_t st, const char** msg) {
+  const GemmArgs& a = ga.g;
+  const bool rows = ga.kind == kGroupRows;
+  const int64_t E = ga.E;
+  // kGroupRows: A is [M_total, K], B's map is [b_rows, b_inner]; kGroupRed: A is [M, T], B is [N, T]
+  const int64_t a_rows = rows ? ga.M_total : a.M, a_inner = rows ? a.K : ga.M_total;
+  const int64_t b_rows = rows ? (ga.b_row_step ? E * a.N : a.N) : a.N;
+  const int64_t b_inner = rows ? (ga.b_k_step ? E * a.K : a.K) : ga.M_total;
+  const int64_t num_n256 = cdiv(a.N, 256);
+  const int64_t tiles256 = rows ? (cdiv(ga.M_total, kBM) + E) * num_n256 : E * cdiv(a.M, kBM) * num_n256;
+  const int bn = (a.N <= 128 || tiles256 < num_sms) ? 128 : 256;
+  // With an empty reduction no tile loads anything; the maps then only need
+  // to be well formed.
+  const bool empty_k = (rows ? a.K : ga.M_total) == 0;
+  CUtensorMap ma, mb;
+  if (!make_tma_u8(&ma, a.qa, empty_k ? 16 : a_inner, a_rows, empty_k ? 16 : a.lda, kBM) ||
+      !make_tma_u8(&mb, a.qb, empty_k ? 16 : b_inner, b_rows, empty_k ? 16 : a.ldb, bn)) {
+    *msg = "cuTensorMapEncodeTiled failed for an operand (alignment, stride or size out of range)";
+    return cudaErrorInvalidValue;
+  }
+  const int64_t num_n = cdiv(a.N, bn);
+  const int64_t num_m = rows ? 0 : cdiv(a.M, kBM);
+  const int64_t Kb = rows ? cdiv(a.K, kBK) : 0;
+  const int64_t tiles_max = rows ? (cdiv(ga.M_total, kBM) + E) * num_n : E * num_m * num_n;
+  const int64_t kb_max = rows ? Kb : cdiv(ga.M_total, kBK);
+  if (ga.M_total >= (int64_t)1 << 31 || a.M >= (int64_t)1 << 31 || a.N >= (int64_t)1 << 31 ||
+      a.K >= (int64_t)1 << 31 || b_rows >= (int64_t)1 << 31 || b_inner >= (int64_t)1 << 31 ||
+      tiles_max * kb_max >= (int64_t)1 << 31) {
+    *msg = "grouped GEMM too large: sizes and the number of (tile, K-block) units must stay below 2^31";
+    return cudaErrorInvalidValue;
+  }
+  GemmParams p;
+  p.sa = a.sa;
+  p.ldsa = a.ldsa;
+  p.sb = a.sb;
+  p.ldsb = a.ldsb;
+  p.c = reinterpret_cast<uint16_t*>(a.c);
+  p.ldc = a.ldc;
+  p.M = rows ? ga.M_total : a.M;
+  p.N = a.N;
+  p.K = rows ? a.K : ga.M_total;
+  p.num_m = (int)num_m;
+  p.num_n = (int)num_n;
+  p.num_tiles = rows ? 0 : (int)(E * num_m * num_n);
+  p.Kb = (int)Kb;
+  p.Nb = (int)cdiv(a.N, kBlock);
+  p.c_vec = (a.ldc % 8 == 0) && (ga.c_step % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.c) & 15u) == 0);
+  p.sa_vec = (a.ldsa % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.sa) & 15u) == 0);
+  p.sb_vec = (a.ldsb % 4 == 0) && (ga.sb_step % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.sb) & 15u) == 0);
+  p.wait_limit_ns = kWaitLimitNs;
+  p.debug_stall = 0;
+  p.offs = ga.offs;
+  p.E = (int)E;
+  p.M_total = (int)ga.M_total;
+  p.b_row_step = (int)ga.b_row_step;
+  p.b_k_step = (int)ga.b_k_step;
+  p.sb_step = ga.sb_step;
+  p.c_step = ga.c_step;
+  const int64_t grid = tiles_max < num_sms ? (tiles_max > 0 ? tiles_max : 1) : num_sms;
+  if (rows) {
+    if (bn == 256)
+      return a.sb_mode == kSbTile ? run_gemm<256, 4, kSbTile, kGroupRows>(ma, mb, p, grid, st)
+                                  : run_gemm<256, 4, kSbTileT, kGroupRows>(ma, mb, p, grid, st);
+    return a.sb_mode == kSbTile ? run_gemm<128, 6, kSbTile, kGroupRows>(ma, mb, p, grid, st)
+                                : run_gemm<128, 6, kSbTileT, kGroupRows>(ma, mb, p, grid, st);
+  }
+  if (bn == 256) return run_gemm<256, 4, kSbCol, kGroupRed>(ma, mb, p, grid, st);
+  return run_gemm<128, 6, kSbCol, kGroupRed>(ma, mb, p, grid, st);
 }
 
 cudaError_t gemm_read_errors(uint32_t* out) {

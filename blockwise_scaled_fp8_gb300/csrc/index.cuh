@@ -136,6 +136,27 @@ BFP8_HD GemmTile gemm_tile(int t, int num_m, int num_n, int bn) {
   return g;
 }
 
+// Grouped (mixture-of-experts) GEMMs.  kGroupRows (forward, input gradient):
+// expert e owns token rows offs[e] .. offs[e+1] of A and C, and its tiles are
+// gemm_tile(t - start[e], cdiv(rows of e, 128), num_n) for start[e] <= t <
+// start[e+1], start[] the running sum of the experts' tile counts.  kGroupRed
+// (weight gradient): expert e reduces over tokens offs[e] .. offs[e+1]; each
+// expert has num_m x num_n tiles, expert e the tiles e*num_m*num_n onwards.
+enum : int { kGroupNone = 0, kGroupRows = 1, kGroupRed = 2 };
+constexpr int kMaxGroups = 1024;
+
+// The expert holding tile t: the largest e < E with start[e] <= t, given
+// start non-decreasing and start[0] <= t < start[E] (empty experts skipped).
+BFP8_HD int group_of_tile(const int* start, int E, int t) {
+  int lo = 0, hi = E;  // start[lo] <= t < start[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (start[mid] <= t) lo = mid;
+    else hi = mid;
+  }
+  return lo;
+}
+
 // Promotion / epilogue warp e (0-based, CTA warp id = e + 4) of `ew` (8 or
 // 16): tensor-memory lane quarter e % 4 (the quarter a warp may access is its
 // CTA warp id % 4), column block e / 4 of epi_cols(bn, ew) columns.  The

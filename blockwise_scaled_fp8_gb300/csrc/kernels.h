@@ -55,6 +55,26 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const c
 // Tile width the launcher picks for an M x N output, and the grid it uses.
 int gemm_pick_bn(int64_t M, int64_t N, int num_sms);
 int64_t gemm_grid(int64_t M, int64_t N, int bn, int num_sms);
+// Grouped (mixture-of-experts) GEMM, kind kGroupRows or kGroupRed (index.cuh).
+//   kGroupRows: g.qa [M_total, K] token rows, C [M_total, N]; expert e's rows
+//               offs[e] .. offs[e+1] against its B: rows e * b_row_step of the B
+//               map (b_row_step = N: forward) or K columns e * b_k_step
+//               (b_k_step = K: input gradient, B map [N, E*K]); its b_s at
+//               g.sb + e * sb_step.  g.M is unused.
+//   kGroupRed:  g.qa [M, T], g.qb [N, T] (T = M_total tokens), C_e [M, N] at
+//               g.c + e * c_step; expert e reduces over tokens offs[e] ..
+//               offs[e+1] (offs[e] % 128 == 0).  g.K is unused.
+// offs is a device array of E + 1 int32 (1 <= E <= kMaxGroups).
+struct GemmGroupArgs {
+  GemmArgs g;
+  int kind;
+  const int32_t* offs;
+  int64_t E;
+  int64_t M_total;
+  int64_t b_row_step, b_k_step;
+  int64_t sb_step, c_step;
+};
+cudaError_t launch_gemm_grouped(const GemmGroupArgs& a, int num_sms, cudaStream_t st, const char** msg);
 // Reads and clears the device error word of the GEMM kernels (synchronous).
 cudaError_t gemm_read_errors(uint32_t* out);
 

@@ -162,6 +162,56 @@ BFP8_API bfp8_status bfp8_gemm_1x128_128x1(const void *qa, int64_t lda, const fl
                                   int64_t M, int64_t N, int64_t K, bfp8_stream_t stream);
 
 /*
+ * Grouped GEMM 1x128 x 128x128 for a mixture-of-experts layer (forward and
+ * input gradient): token rows grouped by expert.
+ * Source: "Enable blockwise FP8 dense training kernels on ROCm" — its
+ * description names an MoE path beside the dense kernels; reading taken:
+ * each expert's GEMM is exactly bfp8_gemm_1x128_128x128 on its tokens.
+ *   offs   DEVICE int32 [E+1], 1 <= E <= 1024: expert e owns token rows
+ *          offs[e] .. offs[e+1]; non-decreasing, 0 <= offs[e] <= M_total.
+ *          Violations are clamped on the device and reported by
+ *          bfp8_check_device_errors (BFP8_ERR_INVALID_ARG).
+ *   qa, sa as bfp8_gemm_1x128_128x128 with M = M_total (sa[kb*ldsa + m], ldsa >= M_total).
+ *   sb_transposed == 0 (forward, y_e = x_e W_e^T): qb = the experts' weight
+ *          codes stacked [E*N, ldb], ldb >= K; sb = their tile scales stacked
+ *          [E*ceil(N/128), ldsb], ldsb >= ceil(K/128).
+ *   sb_transposed == 1 (input gradient, dx_e = dy_e W_e; here K = the
+ *          experts' output features): qb = the transposed codes [N, ldb],
+ *          ldb >= E*K, expert e in columns e*K .. (e+1)*K (what
+ *          bfp8_quant_weight writes as qt for the stacked weight), K % 16 == 0
+ *          when E > 1 (a TMA load starts on a 16-byte boundary); sb = the
+ *          stacked weight's tile scales [E*ceil(K/128), ldsb], ldsb >= ceil(N/128).
+ *   c      device bf16 [M_total, ldc], ldc >= N.  Rows outside
+ *          [offs[0], offs[E]) and columns >= N are not written.
+ */
+BFP8_API bfp8_status bfp8_gemm_grouped_1x128_128x128(const void *qa, int64_t lda, const float *sa, int64_t ldsa,
+                                    const void *qb, int64_t ldb, const float *sb, int64_t ldsb,
+                                    int sb_transposed, const int32_t *offs, int64_t E,
+                                    void *c, int64_t ldc, int64_t M_total, int64_t N, int64_t K,
+                                    bfp8_stream_t stream);
+
+/*
+ * Grouped GEMM 1x128 x 128x1 for a mixture-of-experts layer (weight
+ * gradient): dW_e = dY_e^T X_e, each expert reducing over its own tokens.
+ * Source and reading as bfp8_gemm_grouped_1x128_128x128; the 128-token
+ * groups along the token dim stay inside one expert only if every expert
+ * starts on a 128-token boundary, so offs[e] % 128 == 0 is required for
+ * e < E (offs[E] <= T may be ragged).
+ *   qa     device e4m3 [M, lda], lda >= T (dY^T codes, 1x128 along tokens);
+ *          sa[tb*ldsa + m], ldsa >= M.
+ *   qb     device e4m3 [N, ldb], ldb >= T (X codes, 128x1 along tokens,
+ *          transposed); sb[tb*ldsb + n], ldsb >= N.
+ *   c      device bf16: expert e's [M, ldc] block at c + e*c_expert_stride
+ *          elements, ldc >= N, c_expert_stride >= M*ldc.  An expert without
+ *          tokens gets zeros.
+ */
+BFP8_API bfp8_status bfp8_gemm_grouped_1x128_128x1(const void *qa, int64_t lda, const float *sa, int64_t ldsa,
+                                    const void *qb, int64_t ldb, const float *sb, int64_t ldsb,
+                                    const int32_t *offs, int64_t E, void *c, int64_t ldc,
+                                    int64_t c_expert_stride, int64_t M, int64_t N, int64_t T,
+                                    bfp8_stream_t stream);
+
+/*
  * Blockwise-FP8 linear layer (the Float8BlockwiseLinear computation of the
  * ROCm enablement page: quantise, then the blockwise GEMMs), y = x W^T.
  *   x  device bf16 [M,K] contiguous;  w  device bf16 [N,K] contiguous;
