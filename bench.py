@@ -37,6 +37,7 @@ WORKLOADS = {
     "mid": S.FWD_MID,          # 2048 x 4096 x 4096
     "square": S.FWD_SQUARE,    # 8192 x 8192 x 8192
     "mlp_up": S.MLP_UP,        # 16384 x 14336 x 4096
+    "moe_up": S.MOE_UP,        # 16384 tokens over 8 experts of 14336 x 4096
 }
 METRIC = "blockwise FP8 GEMM TFLOPS & quant GB/s at 1 GB300, % of FP8/HBM roofline"
 L2_FLUSH_BYTES = 256 << 20
@@ -210,13 +211,28 @@ def _sample_text(wl, r, nr, nb, kb):
             f"wgrad dw[{len(nr)} of {wl.N} rows, {len(kb)} blocks], each with the quantisations it needs")
 
 
+def _oracle_problem(wl, x, w, dy):
+    """The dense problem the oracle samples: the workload itself, or for a
+    mixture-of-experts workload the first expert with tokens (each expert's
+    layer is the dense method on its token slice)."""
+    if not isinstance(wl, S.MoE):
+        return wl, x, w, dy, ""
+    offs = wl.offsets()
+    e = next(i for i in range(wl.E) if offs[i + 1] > offs[i])
+    r0, r1 = int(offs[e]), int(offs[e + 1])
+    sub = S.Linear(f"{wl.name}_expert{e}", M=r1 - r0, N=wl.N, K=wl.K, seed=wl.seed)
+    return (sub, x[r0:r1], w[e * wl.N:(e + 1) * wl.N], dy[r0:r1],
+            f"expert {e} of {wl.E} (tokens {r0}..{r1}): ")
+
+
 def run_reference(args, wl):
     import oracle as O
     O.build()
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    x, w, dy = wl.x(), wl.w(), wl.dy()
+    full = wl
+    wl, x, w, dy, prefix = _oracle_problem(wl, wl.x(), wl.w(), wl.dy())
     r, nr, nb, kb = _sample(wl, args.ref_rows, args.ref_blocks, 0)
     rot = [("fwd",), ("dgrad",), ("wgrad",)]  # one part of the step per iteration, in rotation
     for i in range(args.warmup):
@@ -228,11 +244,11 @@ def run_reference(args, wl):
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
     cores = O._threads()
-    sample = "per step, one of (in rotation): " + _sample_text(wl, r, nr, nb, kb)
+    sample = "per step, one of (in rotation): " + prefix + _sample_text(wl, r, nr, nb, kb)
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K},
+            "data": "synthetic", "config": {"workload": full.name, "M": full.M, "N": full.N, "K": full.K},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -246,21 +262,28 @@ def run_reference(args, wl):
 
 class Step:
     """Preallocated buffers and the kernel sequence of one linear step, each
-    call recorded between CUDA events on the current stream."""
+    call recorded between CUDA events on the current stream.  For a
+    mixture-of-experts workload the weights are the experts' stacked [E*N, K]
+    and the three GEMMs are the grouped ones."""
 
     def __init__(self, wl, torch, B, dev):
         self.wl, self.torch, self.B = wl, torch, B
         M, N, K = wl.M, wl.N, wl.K
+        E = getattr(wl, "E", 1)
+        self.moe = isinstance(wl, S.MoE)
         rup = lambda a, b: (a + b - 1) // b * b
         cd = lambda a: (a + 127) // 128
         u8, f32, bf = torch.uint8, torch.float32, torch.bfloat16
         e = lambda *s, dt: torch.empty(s, dtype=dt, device=dev)
         self.qx, self.sx = e(M, rup(K, 16), dt=u8), e(cd(K), rup(M, 4), dt=f32)
         self.qxt, self.sxt = e(K, rup(M, 16), dt=u8), e(cd(M), rup(K, 4), dt=f32)
-        self.qw, self.qwt, self.sw = e(N, rup(K, 16), dt=u8), e(K, rup(N, 16), dt=u8), e(cd(N), cd(K), dt=f32)
+        self.qw, self.qwt = e(E * N, rup(K, 16), dt=u8), e(K, rup(E * N, 16), dt=u8)
+        self.sw = e(E * cd(N), cd(K), dt=f32)
         self.qdy, self.sdy = e(M, rup(N, 16), dt=u8), e(cd(N), rup(M, 4), dt=f32)
         self.qdyt, self.sdyt = e(N, rup(M, 16), dt=u8), e(cd(M), rup(N, 4), dt=f32)
-        self.y, self.dx, self.dw = e(M, N, dt=bf), e(M, K, dt=bf), e(N, K, dt=bf)
+        self.y, self.dx = e(M, N, dt=bf), e(M, K, dt=bf)
+        self.dw = e(E, N, K, dt=bf) if self.moe else e(N, K, dt=bf)
+        self.offs = torch.from_numpy(wl.offsets()).to(dev) if self.moe else None
         self.names = ["quant_dual_x", "quant_weight_w", "gemm_fwd", "quant_dual_dy", "gemm_dgrad", "gemm_wgrad"]
         self.launches_per_step = len(self.names)
 
@@ -270,6 +293,17 @@ class Step:
     def _calls(self, x, w, dy):
         B, wl = self.B, self.wl
         M, N, K = wl.M, wl.N, wl.K
+        if self.moe:
+            o = self.offs
+            return [
+                lambda: B.quant_dual(x, q_row=self.qx, s_row=self.sx, q_col=self.qxt, s_col=self.sxt),
+                lambda: B.quant_weight(w, with_q=True, with_t=True, q=self.qw, qt=self.qwt, s=self.sw),
+                lambda: B.gemm_grouped_1x128_128x128(self.qx, self.sx, self.qw, self.sw, o, N, K, out=self.y),
+                lambda: B.quant_dual(dy, q_row=self.qdy, s_row=self.sdy, q_col=self.qdyt, s_col=self.sdyt),
+                lambda: B.gemm_grouped_1x128_128x128(self.qdy, self.sdy, self.qwt, self.sw, o, K, N,
+                                                     sb_transposed=True, out=self.dx),
+                lambda: B.gemm_grouped_1x128_128x1(self.qdyt, self.sdyt, self.qxt, self.sxt, o, M, out=self.dw),
+            ]
         return [
             lambda: B.quant_dual(x, q_row=self.qx, s_row=self.sx, q_col=self.qxt, s_col=self.sxt),
             lambda: B.quant_weight(w, with_q=True, with_t=True, q=self.qw, qt=self.qwt, s=self.sw),
@@ -315,11 +349,12 @@ def algorithmic_units(wl):
     (read 2 B/elem bf16 once, write 1 B/elem e4m3 per output form, plus 4 B
     per scale)."""
     M, N, K = wl.M, wl.N, wl.K
+    E = getattr(wl, "E", 1)
     cd = lambda a: (a + 127) // 128
     gem = 2.0 * M * N * K
     return {
         "quant_dual_x": ("GB/s", 4.0 * M * K + 4.0 * (M * cd(K) + K * cd(M))),
-        "quant_weight_w": ("GB/s", 4.0 * N * K + 4.0 * cd(N) * cd(K)),
+        "quant_weight_w": ("GB/s", E * (4.0 * N * K + 4.0 * cd(N) * cd(K))),
         "gemm_fwd": ("TFLOP/s", gem),
         "quant_dual_dy": ("GB/s", 4.0 * M * N + 4.0 * (M * cd(N) + N * cd(M))),
         "gemm_dgrad": ("TFLOP/s", gem),
@@ -422,6 +457,8 @@ def run_gpu(args, wl):
         peak_note = f"{peaks['source']} HBM copy bandwidth"
     kkey = "gemm_1x128_128x128" if dname in ("gemm_fwd", "gemm_dgrad") else (
         "gemm_1x128_128x1" if dname == "gemm_wgrad" else dname)
+    if step.moe and dname.startswith("gemm"):
+        kkey = "gemm_grouped" + kkey[4:]
     roof["traffic"] = _profile_traffic(kkey, wl.name)
     roof["kernel"] = dname
     roof["peak_source"] = peak_note
@@ -433,13 +470,19 @@ def run_gpu(args, wl):
         hw = torch.from_numpy(wh.view(np.int16)).view(torch.bfloat16).pin_memory()
         hdy = torch.from_numpy(dyh.view(np.int16)).view(torch.bfloat16).pin_memory()
         M, N, K = wl.M, wl.N, wl.K
+        E = getattr(wl, "E", 1)
+        dws = (E, N, K) if step.moe else (N, K)
         oy = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
         odx = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
-        odw = torch.empty((N, K), dtype=torch.bfloat16).pin_memory()
+        odw = torch.empty(dws, dtype=torch.bfloat16).pin_memory()
         gx, gw, gdy = torch.empty_like(x), torch.empty_like(w), torch.empty_like(dy)
-        ws = B.linear_train_workspace(M, N, K, device=dev)
+        ws = None if step.moe else B.linear_train_workspace(M, N, K, device=dev)
         gy = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        gdx, gdw = torch.empty((M, K), dtype=torch.bfloat16, device=dev), torch.empty((N, K), dtype=torch.bfloat16, device=dev)
+        gdx, gdw = torch.empty((M, K), dtype=torch.bfloat16, device=dev), torch.empty(dws, dtype=torch.bfloat16, device=dev)
+        if step.moe:
+            hoffs = torch.from_numpy(wl.offsets()).pin_memory()
+            goffs = torch.empty_like(hoffs, device=dev)
+        moe_saved = [None]
 
         # copies on their own streams, overlapped with compute as a caller would:
         # dY goes in while the forward runs, y comes out while the backward runs
@@ -452,17 +495,25 @@ def run_gpu(args, wl):
             with torch.cuda.stream(h2d):
                 gx.copy_(hx, non_blocking=True)
                 gw.copy_(hw, non_blocking=True)
+                if step.moe:
+                    goffs.copy_(hoffs, non_blocking=True)
                 ev_xw.record(h2d)
                 gdy.copy_(hdy, non_blocking=True)
                 ev_dy.record(h2d)
             main.wait_event(ev_xw)
-            B.linear_fwd_train(gx, gw, ws, y=gy)
+            if step.moe:
+                _, moe_saved[0] = B.moe_linear_fwd(gx, gw.view(E, N, K), goffs, y=gy)
+            else:
+                B.linear_fwd_train(gx, gw, ws, y=gy)
             ev_y.record(main)
             d2h.wait_event(ev_y)
             with torch.cuda.stream(d2h):
                 oy.copy_(gy, non_blocking=True)
             main.wait_event(ev_dy)
-            B.linear_bwd_saved(gdy, ws, M, N, K, dx=gdx, dw=gdw)
+            if step.moe:
+                B.moe_linear_bwd(gdy, moe_saved[0], goffs, dx=gdx, dw=gdw)
+            else:
+                B.linear_bwd_saved(gdy, ws, M, N, K, dx=gdx, dw=gdw)
             ev_b.record(main)
             d2h.wait_event(ev_b)
             with torch.cuda.stream(d2h):
@@ -483,20 +534,21 @@ def run_gpu(args, wl):
             torch.cuda.synchronize()
             tot += s0.elapsed_time(s1)
         e2e = {"value": flops_step * args.steps / (tot / 1e3) / 1e12 * world, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(2 * (M * K + N * K + M * N)),
-               "d2h_bytes_per_step": int(2 * (M * N + M * K + N * K)),
+               "h2d_bytes_per_step": int(2 * (M * K + E * N * K + M * N) + (4 * (E + 1) if step.moe else 0)),
+               "d2h_bytes_per_step": int(2 * (M * N + M * K + E * N * K)),
                "ms_per_step": tot / args.steps}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         import oracle as O
         O.build()
-        r, nr, nb, kb = _sample(wl, args.cpu_rows, args.cpu_blocks, 1)
+        owl, ox, ow, ody, prefix = _oracle_problem(wl, xh, wh, dyh)
+        r, nr, nb, kb = _sample(owl, args.cpu_rows, args.cpu_blocks, 1)
         t0 = time.perf_counter()
-        fl = oracle_step_sample(xh, wh, dyh, r, nr, nb, kb)
+        fl = oracle_step_sample(ox, ow, ody, r, nr, nb, kb)
         dt = time.perf_counter() - t0
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": O._threads(), "kind": "oracle",
-               "sample": _sample_text(wl, r, nr, nb, kb) + f"; {dt:.1f} s"}
+               "sample": prefix + _sample_text(owl, r, nr, nb, kb) + f"; {dt:.1f} s"}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -504,6 +556,8 @@ def run_gpu(args, wl):
                 "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3 (fp32 accumulate)",
                 "data": "synthetic",
                 "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
+                           **({"experts": wl.E, "expert_offsets": [int(v) for v in wl.offsets()],
+                               "gemms": "grouped by expert"} if step.moe else {}),
                            "step": "quant x (1x128 + 128x1), W (tiles + transposed); fwd GEMM; "
                                    "quant dY (1x128 along N and M); dgrad GEMM; wgrad GEMM",
                            "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}",

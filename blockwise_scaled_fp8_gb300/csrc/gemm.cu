@@ -70,7 +70,12 @@ struct GemmParams {
   int sb_vec;  // 16-byte b_s copies allowed (ldsb % 4 == 0, sb 16-byte aligned)
   uint64_t wait_limit_ns;
   int debug_stall;  // test hook: the promotion warps wait on a barrier nothing arrives on
-  // grouped (mixture-of-experts) forms, unused by the dense GEMM:
+};
+
+// What the grouped (mixture-of-experts) forms add.  A separate kernel
+// parameter: growing GemmParams alone changed the dense kernels' register
+// allocation (more spills in the weight-gradient form).
+struct GemmGroupParams {
   const int32_t* offs;  // [E+1] token offsets of the experts (device memory)
   int E;
   int M_total;          // kGroupRows: token rows of A and C;  kGroupRed: token extent of A and B
@@ -101,9 +106,10 @@ struct GemmCfg {
   // Register split: the control warpgroup drops to kCtrlRegs and the promotion
   // warpgroups rise to kEpiRegs, within what the launch holds (threads x
   // registers per thread at launch, 65536 / threads rounded down to 8):
-  //   EW = 16: 128*40 + 512*104 = 58368 <= 640*96;  EW = 8: 128*40 + 256*224 = 62464 <= 384*168.
+  //   EW = 16: 128*56 + 512*104 = 60416 <= 640*96;  EW = 8: 128*40 + 256*224 = 62464 <= 384*168.
+  // (With 40 the weight-gradient form's control warps spilled.)
   static constexpr int kLaunchRegs = (65536 / kThreads) / 8 * 8;
-  static constexpr int kCtrlRegs = 40;
+  static constexpr int kCtrlRegs = EW == 16 ? 56 : 40;
   static constexpr int kEpiRegs = EW == 16 ? 104 : 224;
   static_assert(128 * kCtrlRegs + 32 * EW * kEpiRegs <= kThreads * kLaunchRegs, "register split");
   static constexpr int kABytes = kBM * kBK;
@@ -156,13 +162,14 @@ __device__ __forceinline__ void copy_scales4(uint32_t dst, const float* v, int i
 // one warp into shared memory.  Offsets that had to be clamped, and (kGroupRed)
 // experts not starting on a 128-token boundary, set kErrGroupOffsets.
 template <int GROUP>
-__device__ void gemm_build_groups(const GemmParams& p, int* s_offs, int* s_start, int lane) {
-  const int n = p.E + 1;
+__device__ void gemm_build_groups(const GemmParams& p, const GemmGroupParams& gp, int* s_offs, int* s_start,
+                                  int lane) {
+  const int n = gp.E + 1;
   const int per = (n + 31) / 32;
   const int i0 = min(lane * per, n), i1 = min(i0 + per, n);
   int run = 0;
   for (int i = i0; i < i1; ++i) {
-    run = max(run, min(max(p.offs[i], 0), p.M_total));
+    run = max(run, min(max(gp.offs[i], 0), gp.M_total));
     s_offs[i] = run;
   }
   int incl = run;  // running maximum over the chunks of lanes <= this one
@@ -175,16 +182,16 @@ __device__ void gemm_build_groups(const GemmParams& p, int* s_offs, int* s_start
   if (lane == 0) excl = 0;
   bool bad = false;
   for (int i = i0; i < i1; ++i) {
-    const int raw = p.offs[i];
+    const int raw = gp.offs[i];
     const int v = max(s_offs[i], excl);
     s_offs[i] = v;
     bad |= raw != v;
-    if (GROUP == kGroupRed && i < p.E) bad |= (v % kBK) != 0;
+    if (GROUP == kGroupRed && i < gp.E) bad |= (v % kBK) != 0;
   }
   __syncwarp();
   if (GROUP == kGroupRows) {
     int cnt = 0;  // tiles of this lane's experts
-    for (int i = i0; i < i1 && i < p.E; ++i) cnt += (int)cdiv(s_offs[i + 1] - s_offs[i], kBM) * p.num_n;
+    for (int i = i0; i < i1 && i < gp.E; ++i) cnt += (int)cdiv(s_offs[i + 1] - s_offs[i], kBM) * p.num_n;
     int sum = cnt;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -194,30 +201,31 @@ __device__ void gemm_build_groups(const GemmParams& p, int* s_offs, int* s_start
     int acc = sum - cnt;
     for (int i = i0; i < i1; ++i) {
       s_start[i] = acc;
-      if (i < p.E) acc += (int)cdiv(s_offs[i + 1] - s_offs[i], kBM) * p.num_n;
+      if (i < gp.E) acc += (int)cdiv(s_offs[i + 1] - s_offs[i], kBM) * p.num_n;
     }
   }
   if (__any_sync(0xffffffffu, bad) && lane == 0 && blockIdx.x == 0) atomicOr(&g_gemm_error, kErrGroupOffsets);
 }
 
 template <int GROUP, int BN>
-__device__ __forceinline__ GemmJob gemm_job(int tile, const GemmParams& p, const int* s_offs, const int* s_start) {
+__device__ __forceinline__ GemmJob gemm_job(int tile, const GemmParams& p, const GemmGroupParams& gp, const int* s_offs,
+                                            const int* s_start) {
   GemmJob j;
   if constexpr (GROUP == kGroupRows) {
-    const int e = group_of_tile(s_start, p.E, tile);
+    const int e = group_of_tile(s_start, gp.E, tile);
     const int r0 = s_offs[e], re = s_offs[e + 1] - r0;
     const GemmTile g = gemm_tile(tile - s_start[e], (int)cdiv(re, kBM), p.num_n, BN);
     j.a_row = r0 + g.m0;
     j.rows = re - g.m0;
-    j.b_row = e * p.b_row_step + g.n0;
+    j.b_row = e * gp.b_row_step + g.n0;
     j.a_k = 0;
-    j.b_k = e * p.b_k_step;
+    j.b_k = e * gp.b_k_step;
     j.kb_s = 0;
     j.kbn = p.Kb;
     j.n0 = g.n0;
     j.e = e;
     j.c_off = (int64_t)j.a_row * p.ldc + g.n0;
-  } else if constexpr (GROUP == kGroupRed) {
+  } else {  // kGroupRed
     const int per = p.num_m * p.num_n;
     const int e = tile / per;
     const GemmTile g = gemm_tile(tile - e * per, p.num_m, p.num_n, BN);
@@ -231,24 +239,12 @@ __device__ __forceinline__ GemmJob gemm_job(int tile, const GemmParams& p, const
     j.b_row = g.n0;
     j.n0 = g.n0;
     j.e = e;
-    j.c_off = (int64_t)e * p.c_step + (int64_t)g.m0 * p.ldc + g.n0;
-  } else {
-    const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
-    j.a_row = g.m0;
-    j.rows = (int)p.M - g.m0;
-    j.b_row = g.n0;
-    j.a_k = 0;
-    j.b_k = 0;
-    j.kb_s = 0;
-    j.kbn = p.Kb;
-    j.n0 = g.n0;
-    j.e = 0;
-    j.c_off = (int64_t)g.m0 * p.ldc + g.n0;
+    j.c_off = (int64_t)e * gp.c_step + (int64_t)g.m0 * p.ldc + g.n0;
   }
   return j;
 }
 
-template <int BN, int STAGES, int SB_MODE, int LDW, int EW, int GROUP>
+template <int BN, int STAGES, int SB_MODE, int LDW, int EW>
 __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tma_a,
                           const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
@@ -265,9 +261,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
   volatile int* never = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
-  // grouped forms: the experts' offsets and first tiles (kGroupTabBytes past the barriers)
-  int* s_offs = reinterpret_cast<int*>(smem + Cfg::kOffMisc + 16);
-  int* s_start = s_offs + (kMaxGroups + 1);
 
   // barriers: full[S], empty[S], tfull[2], tempty[2], drain (both issuers), stall, sfull[2], sempty[2]
   auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -310,12 +303,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     tma_prefetch_desc(&tma_a);
     tma_prefetch_desc(&tma_b);
   }
-  if (GROUP != kGroupNone && warp == 2) gemm_build_groups<GROUP>(p, s_offs, s_start, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  const int num_tiles = GROUP == kGroupRows ? s_start[p.E] : p.num_tiles;
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kCtrlRegs));
   if (warp == 0) {
@@ -323,9 +314,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const GemmJob j = gemm_job<GROUP, BN>(tile, p, s_offs, s_start);
-        for (int kb = 0; kb < j.kbn; ++kb, ++it) {
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+        for (int kb = 0; kb < p.Kb; ++kb, ++it) {
           const int st = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
           if (!mbar_wait_bounded(empty_bar(st), ph ^ 1u, p.wait_limit_ns, abort_flag)) {
@@ -334,8 +325,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(full_bar(st), (uint32_t)Cfg::kStageBytes);
-          tma_load_2d(sA + (uint32_t)(st * Cfg::kABytes), &tma_a, full_bar(st), j.a_k + kb * kBK, j.a_row);
-          tma_load_2d(sB + (uint32_t)(st * Cfg::kBBytes), &tma_b, full_bar(st), j.b_k + kb * kBK, j.b_row);
+          tma_load_2d(sA + (uint32_t)(st * Cfg::kABytes), &tma_a, full_bar(st), kb * kBK, g.m0);
+          tma_load_2d(sB + (uint32_t)(st * Cfg::kBBytes), &tma_b, full_bar(st), kb * kBK, g.n0);
         }
       }
       if (!ok) {
@@ -353,9 +344,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
       const uint32_t mine = warp == 1 ? 0u : 1u;  // the K-block steps (and TMEM buffer) of this issuer
       uint32_t it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-        const int kbn = gemm_job<GROUP, BN>(tile, p, s_offs, s_start).kbn;
-        for (int kb = 0; kb < kbn; ++kb, ++it) {
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        for (int kb = 0; kb < p.Kb; ++kb, ++it) {
           if ((it & 1u) != mine) continue;
           const int st = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
@@ -389,22 +379,14 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ scale loader
-    // Scale groups: the dense GEMM's run on over the CTA's consecutive
-    // K-block steps (grp = step / kScaleGroup); a grouped GEMM's tiles have
-    // different K-block counts (some none), so there a group never spans two
-    // tiles and grp counts the groups published so far.
-    uint32_t it = 0, grp = 0;
+    uint32_t it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-      const GemmJob j = gemm_job<GROUP, BN>(tile, p, s_offs, s_start);
-      const bool last_tile = tile + (int)gridDim.x >= num_tiles;
-      const bool sa_vec = p.sa_vec && (j.a_row & 3) == 0;
-      const float* sbe = p.sb + (GROUP != kGroupNone ? (int64_t)j.e * p.sb_step : 0);
-      for (int kb = 0; kb < j.kbn; ++kb, ++it) {
-        if (GROUP == kGroupNone) grp = it / Cfg::kScaleGroup;
-        const uint32_t sub = (GROUP == kGroupNone ? it : (uint32_t)kb) % Cfg::kScaleGroup;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+      const bool last_tile = tile + (int)gridDim.x >= p.num_tiles;
+      for (int kb = 0; kb < p.Kb; ++kb, ++it) {
+        const uint32_t grp = it / Cfg::kScaleGroup, sub = it % Cfg::kScaleGroup;
         const int sl = (int)(grp % Cfg::kScaleSlots);
-        const int kbs = j.kb_s + kb;
         if (sub == 0) {
           const uint32_t ph = (grp / Cfg::kScaleSlots) & 1u;
           const bool got = mbar_wait_bounded(sempty_bar(sl), ph ^ 1u, p.wait_limit_ns, abort_flag);
@@ -415,24 +397,21 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
           }
         }
         const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes + sub * Cfg::kScaleKbBytes);
-        // a_s of the tile's rows 4*lane .. +3 (zero past its valid rows)
-        copy_scales4(slot + 16u * lane, p.sa + (int64_t)kbs * p.ldsa + j.a_row, 4 * lane, j.rows, sa_vec);
+        // a_s of rows m0 + 4*lane .. +3 (zero past M)
+        copy_scales4(slot + 16u * lane, p.sa + (int64_t)kb * p.ldsa, g.m0 + 4 * lane, p.M, p.sa_vec);
         if (SB_MODE == kSbCol) {  // b_s of columns n0 + 128h + 4*lane .. +3 (zero past N)
 #pragma unroll
           for (int h = 0; h < BN / 128; ++h)
-            copy_scales4(slot + 512u + 512u * h + 16u * lane, sbe + (int64_t)kbs * p.ldsb + j.n0, 128 * h + 4 * lane,
-                         p.N - j.n0, p.sb_vec);
+            copy_scales4(slot + 512u + 512u * h + 16u * lane, p.sb + (int64_t)kb * p.ldsb, g.n0 + 128 * h + 4 * lane,
+                         p.N, p.sb_vec);
         } else if (lane < BN / 128) {  // tile scale of the 128 columns n0 + 128*lane (zero past N)
-          const int nb = j.n0 / kBlock + lane;
+          const int nb = g.n0 / kBlock + lane;
           const bool in = nb < p.Nb;
-          const float* src = SB_MODE == kSbTile ? sbe + (int64_t)nb * p.ldsb + kbs : sbe + (int64_t)kbs * p.ldsb + nb;
+          const float* src = SB_MODE == kSbTile ? p.sb + (int64_t)nb * p.ldsb + kb : p.sb + (int64_t)kb * p.ldsb + nb;
           cp_async_4(slot + 512u + 4u * lane, in ? src : p.sb, in ? 4u : 0u);
         }
-        // the slot is published once its group is complete (or the K-blocks end)
-        if (sub == Cfg::kScaleGroup - 1 || (kb == j.kbn - 1 && (GROUP != kGroupNone || last_tile))) {
-          cp_async_mbar_arrive(sfull_bar(sl));
-          ++grp;
-        }
+        // the slot is published once its group is complete (or the CTA's K-blocks end)
+        if (sub == Cfg::kScaleGroup - 1 || (last_tile && kb == p.Kb - 1)) cp_async_mbar_arrive(sfull_bar(sl));
       }
     }
     // let this lane's copies land before the CTA can exit
@@ -445,19 +424,17 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     const int row = epi_row(e, lane);
     const int col0 = epi_col0(e, BN, EW);
     const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
-    uint32_t it = 0, grp = 0;  // K-block steps; scale groups as the loader counts them
+    uint32_t it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-      // (the rest of the tile's job is recomputed for the epilogue: fewer live registers)
-      const int kbn = GROUP == kGroupNone ? p.Kb : gemm_job<GROUP, BN>(tile, p, s_offs, s_start).kbn;
-      const bool last_tile = tile + (int)gridDim.x >= num_tiles;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+      const bool last_tile = tile + (int)gridDim.x >= p.num_tiles;
       float acc[kCols];
 #pragma unroll
       for (int j = 0; j < kCols; ++j) acc[j] = 0.0f;
 
-      for (int kb = 0; kb < kbn; ++kb, ++it) {
-        if (GROUP == kGroupNone) grp = it / Cfg::kScaleGroup;
-        const uint32_t sub = (GROUP == kGroupNone ? it : (uint32_t)kb) % Cfg::kScaleGroup;
+      for (int kb = 0; kb < p.Kb; ++kb, ++it) {
+        const uint32_t grp = it / Cfg::kScaleGroup, sub = it % Cfg::kScaleGroup;
         const int sl = (int)(grp % Cfg::kScaleSlots);
         const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes + sub * Cfg::kScaleKbBytes);
         // once per group: the loader runs ahead, so the slot is almost always ready (poll)
@@ -521,10 +498,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
           }
         }
         // the slot's scales are no longer needed by this warp (end of its group)
-        if (sub == Cfg::kScaleGroup - 1 || (kb == kbn - 1 && (GROUP != kGroupNone || last_tile))) {
+        if (sub == Cfg::kScaleGroup - 1 || (last_tile && kb == p.Kb - 1)) {
           __syncwarp();
           if (lane == 0) mbar_arrive(sempty_bar(sl));
-          ++grp;
         }
       }
       if (!ok) break;
@@ -535,22 +511,6 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
       // the warp then writes 32/G row segments of 16*G contiguous bytes.  Only
       // rows < M and columns < N are written.
       {
-        // output origin, valid rows / columns from it (the dense GEMM keeps the
-        // plain tile arithmetic: fewer live registers at this point)
-        int64_t c_row0, c_col0, c_rows, c_cols;
-        if constexpr (GROUP == kGroupNone) {
-          const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
-          c_row0 = g.m0;
-          c_col0 = g.n0;
-          c_rows = p.M - g.m0;
-          c_cols = p.N - g.n0;
-        } else {
-          const GemmJob job = gemm_job<GROUP, BN>(tile, p, s_offs, s_start);
-          c_row0 = 0;
-          c_col0 = job.c_off;
-          c_rows = job.rows;
-          c_cols = p.N - job.n0;
-        }
         constexpr int kG = kCols / 8 >= 8 ? 8 : kCols / 8;  // chunks per transposed block (epi_group)
         const int pos = lane % kG;
 #pragma unroll
@@ -576,18 +536,362 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
               }
             }
           }
-          const int n = epi_store_col(e, lane, sg, kG, BN, EW);  // tile-local
+          const int n = g.n0 + epi_store_col(e, lane, sg, kG, BN, EW);
 #pragma unroll
           for (int i = 0; i < kG; ++i) {
-            const int mr = epi_store_row(e, lane, i, kG);
-            if (mr >= c_rows || n >= c_cols) continue;
-            uint16_t* dst = p.c + (c_row0 + mr) * p.ldc + c_col0 + n;
-            if (p.c_vec && n + 8 <= c_cols) {
+            const int mr = g.m0 + epi_store_row(e, lane, i, kG);
+            if (mr >= p.M || n >= p.N) continue;
+            uint16_t* dst = p.c + (int64_t)mr * p.ldc + n;
+            if (p.c_vec && n + 8 <= p.N) {
               *reinterpret_cast<uint4*>(dst) = make_uint4(X[i][0], X[i][1], X[i][2], X[i][3]);
             } else {
 #pragma unroll
               for (int b = 0; b < 8; ++b)
-                if (n + b < c_cols) dst[b] = (uint16_t)(X[i][b >> 1] >> (16 * (b & 1)));
+                if (n + b < p.N) dst[b] = (uint16_t)(X[i][b >> 1] >> (16 * (b & 1)));
+            }
+          }
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// The grouped (mixture-of-experts) forms: the same pipeline as
+// gemm_blockwise_kernel, with each tile's operands, K-blocks, scales and
+// output found through its GemmJob.  (The dense GEMM keeps its own kernel:
+// its weight-gradient form sits at the register limit of the promotion warps,
+// and the job indirection measured 10-17% slower there.)
+template <int BN, int STAGES, int SB_MODE, int LDW, int EW, int GROUP>
+__global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
+    gemm_grouped_kernel(const __grid_constant__ CUtensorMap tma_a,
+                        const __grid_constant__ CUtensorMap tma_b, const GemmParams p, const GemmGroupParams gp) {
+  static_assert(GROUP == kGroupRows || GROUP == kGroupRed, "a grouped form");
+  using Cfg = GemmCfg<BN, STAGES, EW>;
+  constexpr int kCols = Cfg::kCols;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sA = sbase;
+  const uint32_t sB = sbase + Cfg::kOffB;
+  const uint32_t sScale = sbase + Cfg::kOffScale;
+  const uint32_t bar0 = sbase + Cfg::kOffBar;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
+  volatile int* never = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
+  // grouped forms: the experts' offsets and first tiles (kGroupTabBytes past the barriers)
+  int* s_offs = reinterpret_cast<int*>(smem + Cfg::kOffMisc + 16);
+  int* s_start = s_offs + (kMaxGroups + 1);
+
+  // barriers: full[S], empty[S], tfull[2], tempty[2], drain (both issuers), stall, sfull[2], sempty[2]
+  auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(STAGES + i); };
+  auto tfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + i); };
+  auto tempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + 2 + i); };
+  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
+  const uint32_t stall_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 5);  // never arrived on
+  auto sfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + 6 + i); };
+  auto sempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + 6 + Cfg::kScaleSlots + i); };
+
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+  const int lane = (int)(threadIdx.x & 31);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull_bar(i), 1);
+      mbar_init(tempty_bar(i), Cfg::kEpiWarps);
+    }
+    mbar_init(drain_bar, 2);
+    mbar_init(stall_bar, 1);
+    for (int i = 0; i < Cfg::kScaleSlots; ++i) {
+      mbar_init(sfull_bar(i), 32);  // one cp.async arrival per loader lane
+      mbar_init(sempty_bar(i), Cfg::kEpiWarps);
+    }
+    *abort_flag = 0;
+    *never = 0;
+    fence_barrier_init();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma_a);
+    tma_prefetch_desc(&tma_b);
+  }
+  if (warp == 2) gemm_build_groups<GROUP>(p, gp, s_offs, s_start, lane);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int num_tiles = GROUP == kGroupRows ? s_start[gp.E] : p.num_tiles;
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kCtrlRegs));
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const GemmJob j = gemm_job<GROUP, BN>(tile, p, gp, s_offs, s_start);
+        for (int kb = 0; kb < j.kbn; ++kb, ++it) {
+          const int st = (int)(it % STAGES);
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!mbar_wait_bounded(empty_bar(st), ph ^ 1u, p.wait_limit_ns, abort_flag)) {
+            gemm_fail(kErrWaitEmpty, abort_flag);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(st), (uint32_t)Cfg::kStageBytes);
+          tma_load_2d(sA + (uint32_t)(st * Cfg::kABytes), &tma_a, full_bar(st), j.a_k + kb * kBK, j.a_row);
+          tma_load_2d(sB + (uint32_t)(st * Cfg::kBBytes), &tma_b, full_bar(st), j.b_k + kb * kBK, j.b_row);
+        }
+      }
+      if (!ok) {
+        // copies already issued must land before this CTA's smem goes away
+        for (uint32_t j = (it > STAGES ? it - STAGES : 0); j < it; ++j)
+          if (!mbar_wait_bounded(full_bar((int)(j % STAGES)), (j / STAGES) & 1u,
+                                 p.wait_limit_ns, never))
+            atomicOr(&g_gemm_error, kErrWaitDrain);
+      }
+    }
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------------ MMA issuers
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
+      const uint32_t mine = warp == 1 ? 0u : 1u;  // the K-block steps (and TMEM buffer) of this issuer
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        const int kbn = gemm_job<GROUP, BN>(tile, p, gp, s_offs, s_start).kbn;
+        for (int kb = 0; kb < kbn; ++kb, ++it) {
+          if ((it & 1u) != mine) continue;
+          const int st = (int)(it % STAGES);
+          const uint32_t ph = (it / STAGES) & 1u;
+          const int buf = (int)(it & 1u);
+          const uint32_t tph = (it >> 1) & 1u;
+          if (!mbar_spin_bounded(tempty_bar(buf), tph ^ 1u, p.wait_limit_ns, abort_flag)) {
+            gemm_fail(kErrWaitTmemEmpty, abort_flag);
+            ok = false;
+            break;
+          }
+          if (!mbar_spin_bounded(full_bar(st), ph, p.wait_limit_ns, abort_flag)) {
+            gemm_fail(kErrWaitFull, abort_flag);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t da = desc_kmajor_sw128(sA + (uint32_t)(st * Cfg::kABytes));
+          const uint64_t db = desc_kmajor_sw128(sB + (uint32_t)(st * Cfg::kBBytes));
+          const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+#pragma unroll
+          for (int k = 0; k < kBK / 32; ++k)  // advance 32 bytes of K inside the swizzled row
+            mma_e4m3(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), idesc, k > 0 ? 1u : 0u);
+          mma_commit(empty_bar(st));
+          mma_commit(tfull_bar(buf));
+        }
+      }
+      // every MMA issued by both issuers completes before tensor memory is released
+      mma_commit(drain_bar);
+      if (!mbar_wait_bounded(drain_bar, 0, p.wait_limit_ns, never))
+        gemm_fail(kErrWaitDrain, abort_flag);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ scale loader
+    // Scale groups: the tiles have different K-block counts (some none), so a
+    // group of up to kScaleGroup K-blocks never spans two tiles; grp counts
+    // the groups published so far.
+    uint32_t grp = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      const GemmJob j = gemm_job<GROUP, BN>(tile, p, gp, s_offs, s_start);
+      const bool sa_vec = p.sa_vec && (j.a_row & 3) == 0;
+      const float* sbe = p.sb + (int64_t)j.e * gp.sb_step;
+      for (int kb = 0; kb < j.kbn; ++kb) {
+        const uint32_t sub = (uint32_t)kb % Cfg::kScaleGroup;
+        const int sl = (int)(grp % Cfg::kScaleSlots);
+        const int kbs = j.kb_s + kb;
+        if (sub == 0) {
+          const uint32_t ph = (grp / Cfg::kScaleSlots) & 1u;
+          const bool got = mbar_wait_bounded(sempty_bar(sl), ph ^ 1u, p.wait_limit_ns, abort_flag);
+          if (!__all_sync(0xffffffffu, got)) {
+            if (lane == 0) gemm_fail(kErrWaitScale, abort_flag);
+            ok = false;
+            break;
+          }
+        }
+        const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes + sub * Cfg::kScaleKbBytes);
+        // a_s of the tile's rows 4*lane .. +3 (zero past its valid rows)
+        copy_scales4(slot + 16u * lane, p.sa + (int64_t)kbs * p.ldsa + j.a_row, 4 * lane, j.rows, sa_vec);
+        if (SB_MODE == kSbCol) {  // b_s of columns n0 + 128h + 4*lane .. +3 (zero past N)
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h)
+            copy_scales4(slot + 512u + 512u * h + 16u * lane, sbe + (int64_t)kbs * p.ldsb, j.n0 + 128 * h + 4 * lane,
+                         p.N, p.sb_vec);
+        } else if (lane < BN / 128) {  // tile scale of the 128 columns n0 + 128*lane (zero past N)
+          const int nb = j.n0 / kBlock + lane;
+          const bool in = nb < p.Nb;
+          const float* src = SB_MODE == kSbTile ? sbe + (int64_t)nb * p.ldsb + kbs : sbe + (int64_t)kbs * p.ldsb + nb;
+          cp_async_4(slot + 512u + 4u * lane, in ? src : p.sb, in ? 4u : 0u);
+        }
+        // the slot is published once its group is complete (or the K-blocks end)
+        if (sub == Cfg::kScaleGroup - 1 || kb == j.kbn - 1) {
+          cp_async_mbar_arrive(sfull_bar(sl));
+          ++grp;
+        }
+      }
+    }
+    // let this lane's copies land before the CTA can exit
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::kEpiRegs));
+    // ------------------------------------------------------------ promotion + epilogue
+    const int e = warp - 4;
+    const int row = epi_row(e, lane);
+    const int col0 = epi_col0(e, BN, EW);
+    const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
+    uint32_t it = 0, grp = 0;  // K-block steps; scale groups as the loader counts them
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+      // (the rest of the tile's job is recomputed for the epilogue: fewer live registers)
+      const int kbn = gemm_job<GROUP, BN>(tile, p, gp, s_offs, s_start).kbn;
+      float acc[kCols];
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) acc[j] = 0.0f;
+
+      for (int kb = 0; kb < kbn; ++kb, ++it) {
+        const uint32_t sub = (uint32_t)kb % Cfg::kScaleGroup;
+        const int sl = (int)(grp % Cfg::kScaleSlots);
+        const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes + sub * Cfg::kScaleKbBytes);
+        // once per group: the loader runs ahead, so the slot is almost always ready (poll)
+        const bool sgot = sub != 0 || mbar_spin_bounded(sfull_bar(sl), (grp / Cfg::kScaleSlots) & 1u,
+                                                        p.wait_limit_ns, abort_flag);
+        const int buf = (int)(it & 1u);
+        const uint32_t tph = (it >> 1) & 1u;
+        const bool got = sgot && mbar_wait_bounded(p.debug_stall ? stall_bar : tfull_bar(buf), tph, p.wait_limit_ns,
+                                                   abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) gemm_fail(sgot ? kErrWaitTmemFull : kErrWaitScale, abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float sa_cur, sb_cur = 0.0f;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sa_cur) : "r"(slot + 4u * row));
+        if (SB_MODE != kSbCol)
+          asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sb_cur) : "r"(slot + 512u + 4u * (uint32_t)(col0 >> 7)));
+        const float scale = sa_cur * sb_cur;
+        const uint32_t taddr = tmem_base + lane_base + (uint32_t)(buf * BN + col0);
+        // LDW columns of the partial per tensor-memory load round trip (one wait)
+#pragma unroll
+        for (int c = 0; c < kCols / LDW; ++c) {
+          uint32_t r[LDW];
+          if constexpr (LDW == 64)
+            tmem_ld_32x32b_x64(taddr + (uint32_t)(LDW * c), r);
+          else if constexpr (LDW == 32)
+            tmem_ld_32x32b_x32(taddr + (uint32_t)(LDW * c), r);
+          else
+            tmem_ld_32x32b_x16(taddr + (uint32_t)(LDW * c), r);
+          tmem_ld_wait();
+          tmem_regs_after_wait(r);
+          if (c == kCols / LDW - 1) {
+            // this warp's share of the partial is in registers: release the buffer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(buf));
+          }
+          if (SB_MODE == kSbCol) {
+            // acc[n] += (a_s * b_s[n]) * P[n] on fp32x2 lanes (two columns per instruction)
+            const uint64_t sa2 = f2_pack(sa_cur, sa_cur);
+#pragma unroll
+            for (int j4 = 0; j4 < LDW / 4; ++j4) {
+              float4 sb4;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(sb4.x), "=f"(sb4.y), "=f"(sb4.z), "=f"(sb4.w)
+                           : "r"(slot + 512u + 4u * (uint32_t)(col0 + LDW * c + 4 * j4)));
+              const uint64_t t2[2] = {f2_mul(sa2, f2_pack(sb4.x, sb4.y)), f2_mul(sa2, f2_pack(sb4.z, sb4.w))};
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int j = LDW * c + 4 * j4 + 2 * h;
+                const uint64_t p2 =
+                    f2_pack(__uint_as_float(r[4 * j4 + 2 * h]), __uint_as_float(r[4 * j4 + 2 * h + 1]));
+                f2_unpack(f2_fma(t2[h], p2, f2_pack(acc[j], acc[j + 1])), acc[j], acc[j + 1]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < LDW; ++j) acc[LDW * c + j] = fmaf(scale, __uint_as_float(r[j]), acc[LDW * c + j]);
+          }
+        }
+        // the slot's scales are no longer needed by this warp (end of its group)
+        if (sub == Cfg::kScaleGroup - 1 || kb == kbn - 1) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sempty_bar(sl));
+          ++grp;
+        }
+      }
+      if (!ok) break;
+
+      // Epilogue: round to bf16, transpose G x G blocks of 16-byte chunks (8
+      // columns) within groups of G lanes (xor shuffles), so that lane pos of a
+      // group holds chunk pos of the group's G rows; each store instruction of
+      // the warp then writes 32/G row segments of 16*G contiguous bytes.  Only
+      // rows < M and columns < N are written.
+      {
+        const GemmJob job = gemm_job<GROUP, BN>(tile, p, gp, s_offs, s_start);
+        constexpr int kG = kCols / 8 >= 8 ? 8 : kCols / 8;  // chunks per transposed block (epi_group)
+        const int pos = lane % kG;
+#pragma unroll
+        for (int sg = 0; sg < kCols / (8 * kG); ++sg) {
+          uint32_t X[kG][4];
+#pragma unroll
+          for (int j = 0; j < kG; ++j)
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              X[j][q] = pack_bf16x2(acc[8 * (kG * sg + j) + 2 * q], acc[8 * (kG * sg + j) + 2 * q + 1]);
+#pragma unroll
+          for (int msk = kG / 2; msk >= 1; msk >>= 1) {
+            const bool hi = (pos & msk) != 0;
+#pragma unroll
+            for (int j = 0; j < kG; ++j) {
+              if (j & msk) continue;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const uint32_t send = hi ? X[j][q] : X[j | msk][q];
+                const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, msk);
+                if (hi) X[j][q] = recv;
+                else X[j | msk][q] = recv;
+              }
+            }
+          }
+          const int nl = epi_store_col(e, lane, sg, kG, BN, EW);  // tile-local
+#pragma unroll
+          for (int i = 0; i < kG; ++i) {
+            const int ml = epi_store_row(e, lane, i, kG);
+            const int ncols = (int)p.N - job.n0;
+            if (ml >= job.rows || nl >= ncols) continue;
+            uint16_t* dst = p.c + job.c_off + (int64_t)ml * p.ldc + nl;
+            const int left = ncols - nl;  // valid columns from this chunk's first one
+            if (p.c_vec && left >= 8) {
+              *reinterpret_cast<uint4*>(dst) = make_uint4(X[i][0], X[i][1], X[i][2], X[i][3]);
+            } else {
+#pragma unroll
+              for (int b = 0; b < 8; ++b)
+                if (b < left) dst[b] = (uint16_t)(X[i][b >> 1] >> (16 * (b & 1)));
             }
           }
         }
@@ -662,19 +966,26 @@ constexpr int gemm_ldw() {
 }
 
 template <int BN, int STAGES, int MODE, int GROUP = kGroupNone>
-static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb,
-                            const GemmParams& p, int64_t grid, cudaStream_t st) {
+static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int64_t grid,
+                            cudaStream_t st, const GemmGroupParams* gp = nullptr) {
   constexpr int EW = gemm_ew<MODE>(), LDW = gemm_ldw<BN, MODE, EW>();
   using Cfg = GemmCfg<BN, STAGES, EW>;
   constexpr int kSmem = Cfg::kSmemBytes + (GROUP != kGroupNone ? Cfg::kGroupTabBytes : 0);
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW, GROUP>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if constexpr (GROUP == kGroupNone)
+      attr_err = cudaFuncSetAttribute(gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    else
+      attr_err = cudaFuncSetAttribute(gemm_grouped_kernel<BN, STAGES, MODE, LDW, EW, GROUP>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW, GROUP><<<(unsigned)grid, Cfg::kThreads, kSmem, st>>>(ma, mb, p);
+  if constexpr (GROUP == kGroupNone)
+    gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW><<<(unsigned)grid, Cfg::kThreads, kSmem, st>>>(ma, mb, p);
+  else
+    gemm_grouped_kernel<BN, STAGES, MODE, LDW, EW, GROUP><<<(unsigned)grid, Cfg::kThreads, kSmem, st>>>(ma, mb, p, *gp);
   return cudaGetLastError();
 }
 
@@ -712,11 +1023,6 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const c
   p.sb_vec = (a.ldsb % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.sb) & 15u) == 0);
   p.wait_limit_ns = wait_limit_ns;
   p.debug_stall = debug_stall;
-  p.offs = nullptr;
-  p.E = 0;
-  p.M_total = 0;
-  p.b_row_step = p.b_k_step = 0;
-  p.sb_step = p.c_step = 0;
   const int64_t grid = gemm_grid(a.M, a.N, bn, num_sms);
   if (bn == 256) {
     switch (a.sb_mode) {
@@ -783,23 +1089,24 @@ cudaError_t launch_gemm_grouped(const GemmGroupArgs& ga, int num_sms, cudaStream
   p.sb_vec = (a.ldsb % 4 == 0) && (ga.sb_step % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.sb) & 15u) == 0);
   p.wait_limit_ns = kWaitLimitNs;
   p.debug_stall = 0;
-  p.offs = ga.offs;
-  p.E = (int)E;
-  p.M_total = (int)ga.M_total;
-  p.b_row_step = (int)ga.b_row_step;
-  p.b_k_step = (int)ga.b_k_step;
-  p.sb_step = ga.sb_step;
-  p.c_step = ga.c_step;
+  GemmGroupParams gp;
+  gp.offs = ga.offs;
+  gp.E = (int)E;
+  gp.M_total = (int)ga.M_total;
+  gp.b_row_step = (int)ga.b_row_step;
+  gp.b_k_step = (int)ga.b_k_step;
+  gp.sb_step = ga.sb_step;
+  gp.c_step = ga.c_step;
   const int64_t grid = tiles_max < num_sms ? (tiles_max > 0 ? tiles_max : 1) : num_sms;
   if (rows) {
     if (bn == 256)
-      return a.sb_mode == kSbTile ? run_gemm<256, 4, kSbTile, kGroupRows>(ma, mb, p, grid, st)
-                                  : run_gemm<256, 4, kSbTileT, kGroupRows>(ma, mb, p, grid, st);
-    return a.sb_mode == kSbTile ? run_gemm<128, 6, kSbTile, kGroupRows>(ma, mb, p, grid, st)
-                                : run_gemm<128, 6, kSbTileT, kGroupRows>(ma, mb, p, grid, st);
+      return a.sb_mode == kSbTile ? run_gemm<256, 4, kSbTile, kGroupRows>(ma, mb, p, grid, st, &gp)
+                                  : run_gemm<256, 4, kSbTileT, kGroupRows>(ma, mb, p, grid, st, &gp);
+    return a.sb_mode == kSbTile ? run_gemm<128, 6, kSbTile, kGroupRows>(ma, mb, p, grid, st, &gp)
+                                : run_gemm<128, 6, kSbTileT, kGroupRows>(ma, mb, p, grid, st, &gp);
   }
-  if (bn == 256) return run_gemm<256, 4, kSbCol, kGroupRed>(ma, mb, p, grid, st);
-  return run_gemm<128, 6, kSbCol, kGroupRed>(ma, mb, p, grid, st);
+  if (bn == 256) return run_gemm<256, 4, kSbCol, kGroupRed>(ma, mb, p, grid, st, &gp);
+  return run_gemm<128, 6, kSbCol, kGroupRed>(ma, mb, p, grid, st, &gp);
 }
 
 cudaError_t gemm_read_errors(uint32_t* out) {

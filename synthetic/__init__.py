@@ -84,3 +84,25 @@ WGRAD = Linear("wgrad_tokens8192_4096x4096", M=8192, N=4096, K=4096, seed=2)
 SMALL_M = [Linear(f"small_m{m}_{n}x{k}", M=m, N=n, K=k, seed=3)
            for m in (2, 4, 128, 512) for (n, k) in ((512, 128), (5120, 1280), (3584, 640), (4096, 4096))]
 MLP_UP = Linear("mlp_up_16384x14336x4096", M=16384, N=14336, K=4096, seed=4)
+
+
+@dataclass
+class MoE(Linear):
+    """A mixture-of-experts layer: M tokens sorted by expert, E experts with
+    weights W_e [N, K] stacked as [E*N, K]; expert e owns token rows
+    offsets()[e] .. offsets()[e+1].  Each expert starts on a 128-token
+    boundary; the split is uneven (seeded uniform cut points)."""
+    E: int = 8
+
+    def w(self) -> np.ndarray:
+        return normal_bf16((self.E * self.N, self.K), self.w_std, tensor_seed(self.seed, 1))
+
+    def offsets(self) -> np.ndarray:
+        rng = np.random.Generator(np.random.PCG64(tensor_seed(self.seed, 3)))
+        cuts = np.sort(rng.integers(0, self.M // 128 + 1, size=self.E - 1)) * 128
+        return np.concatenate([[0], cuts, [self.M]]).astype(np.int32)
+
+
+# the MLP-up problem routed over 8 experts: same token count and per-expert
+# weight shape, so its GEMM rates compare with the dense ones
+MOE_UP = MoE("moe_up_8x_16384x14336x4096", M=16384, N=14336, K=4096, seed=5, E=8)
