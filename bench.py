@@ -38,6 +38,7 @@ WORKLOADS = {
     "square": S.FWD_SQUARE,    # 8192 x 8192 x 8192
     "mlp_up": S.MLP_UP,        # 16384 x 14336 x 4096
     "moe_up": S.MOE_UP,        # 16384 tokens over 8 experts of 14336 x 4096
+    "moe_mid": S.MOE_MID,      # 4096 tokens over 8 experts of 4096 x 4096
 }
 METRIC = "blockwise FP8 GEMM TFLOPS & quant GB/s at 1 GB300, % of FP8/HBM roofline"
 L2_FLUSH_BYTES = 256 << 20
@@ -315,9 +316,9 @@ class Step:
         ]
 
     def capture(self, x, w, dy):
-        """One CUDA graph per library call, so that host-side launch work
-        (argument checks, tensor-map encoding) stays off the device timeline
-        between the per-kernel events."""
+        """The whole step as one CUDA graph (the timed step), and one graph per
+        library call (per-kernel events between them); host-side launch work
+        (argument checks, tensor-map encoding) stays off the device timeline."""
         torch = self.torch
         calls = self._calls(x, w, dy)
         for c in calls:  # warm: one-time attribute setup happens outside capture
@@ -329,7 +330,19 @@ class Step:
             with torch.cuda.graph(g):
                 c()
             self.graphs.append(g)
+        self.step_graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.step_graph):
+            for c in calls:
+                c()
         torch.cuda.synchronize()
+
+    def run_step(self, ev=None):
+        """One step as a single graph replay, bracketed by ev = (start, end)."""
+        if ev is not None:
+            ev[0].record()
+        self.step_graph.replay()
+        if ev is not None:
+            ev[1].record()
 
     def run(self, x, w, dy, ev=None):
         timed = ev is not None
@@ -401,9 +414,17 @@ def run_gpu(args, wl):
     step.capture(x, w, dy)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
+    # Timed region: K steps, each the whole step as one graph replay between
+    # two events, the L2 flushed before every step (outside the events).  Then
+    # K more steps with one graph per call and events between the calls, for
+    # the per-kernel times and the roofline of the dominant kernel.
+    step_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
     events = [step.new_events() for _ in range(args.steps)]
     with ClockSampler(local) as clk:
         for _ in range(args.warmup):
+            step.run_step()
+            flush.fill_(1.0)
             step.run(x, w, dy)
             flush.fill_(1.0)
         torch.cuda.synchronize()
@@ -415,15 +436,19 @@ def run_gpu(args, wl):
         clk.mark_start()
         for i in range(args.steps):
             flush.fill_(0.0)  # L2 flush between timed steps (outside the step's events)
-            step.run(x, w, dy, events[i])
+            step.run_step(step_events[i])
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
         clk.mark_end()
+        for i in range(args.steps):
+            flush.fill_(0.0)
+            step.run(x, w, dy, events[i])
+        torch.cuda.synchronize()
     B.check_device_errors()
     clocks = clk.summary()
     per_kernel = [step.kernel_ms(ev) for ev in events]
-    step_ms = [ev[0].elapsed_time(ev[-1]) for ev in events]
+    step_ms = [a.elapsed_time(b) for a, b in step_events]
 
     flops_step = 3 * wl.gemm_flops
     total_ms, flops_per_s = aggregate_replicas(float(sum(step_ms)), flops_step * args.steps, dist, dev)
@@ -561,8 +586,11 @@ def run_gpu(args, wl):
                            "step": "quant x (1x128 + 128x1), W (tiles + transposed); fwd GEMM; "
                                    "quant dY (1x128 along N and M); dgrad GEMM; wgrad GEMM",
                            "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}",
-                           "launch": "each library call replayed as a CUDA graph; events between calls"},
+                           "launch": "timed steps: the whole step replayed as one CUDA graph, events around "
+                                     "each step; parts/roofline: as many steps again with one graph per "
+                                     "library call and events between calls"},
                 "gpu_launches": step.launches_per_step * args.steps,
+                "parts_ms_per_step": round(float(np.sum(avg)), 5),
                 "roofline": roof, "parts": parts, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks}
         print(json.dumps(line), flush=True)
     if dist:

@@ -274,6 +274,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
 
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const int lane = (int)(threadIdx.x & 31);
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -306,6 +307,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  pdl_wait();  // the previous kernel's writes are visible from here on
   const uint32_t tmem_base = *tmem_holder;
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kCtrlRegs));
@@ -603,6 +605,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
 
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const int lane = (int)(threadIdx.x & 31);
+  pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -632,6 +635,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     tma_prefetch_desc(&tma_a);
     tma_prefetch_desc(&tma_b);
   }
+  pdl_wait();  // the previous kernel's writes (the offsets among them) are visible from here on
   if (warp == 2) gemm_build_groups<GROUP>(p, gp, s_offs, s_start, lane);
   tc_fence_before();
   __syncthreads();
@@ -983,10 +987,11 @@ static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const 
   });
   if (attr_err != cudaSuccess) return attr_err;
   if constexpr (GROUP == kGroupNone)
-    gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW><<<(unsigned)grid, Cfg::kThreads, kSmem, st>>>(ma, mb, p);
+    return launch_pdl(gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW>, (unsigned)grid, Cfg::kThreads, kSmem, st, ma,
+                      mb, p);
   else
-    gemm_grouped_kernel<BN, STAGES, MODE, LDW, EW, GROUP><<<(unsigned)grid, Cfg::kThreads, kSmem, st>>>(ma, mb, p, *gp);
-  return cudaGetLastError();
+    return launch_pdl(gemm_grouped_kernel<BN, STAGES, MODE, LDW, EW, GROUP>, (unsigned)grid, Cfg::kThreads, kSmem,
+                      st, ma, mb, p, *gp);
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const char** msg,

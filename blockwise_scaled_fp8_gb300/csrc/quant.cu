@@ -32,6 +32,8 @@ __global__ void __launch_bounds__(kRowThreads) quant_rows_kernel(
     const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t ldx, uint8_t* __restrict__ q,
     int64_t ldq, float* __restrict__ s, int64_t lds, int64_t Kb, int64_t num_groups,
     int64_t iters) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane16 = threadIdx.x & 15;
   const int64_t hw = ((int64_t)blockIdx.x * kRowThreads + threadIdx.x) >> 4;
   const int64_t nhw = ((int64_t)gridDim.x * kRowThreads) >> 4;
@@ -101,6 +103,8 @@ template <bool kVec>
 __global__ void __launch_bounds__(kColThreads) quant_cols_kernel(
     const uint16_t* __restrict__ x, int64_t T, int64_t C, int64_t ldx, uint8_t* __restrict__ qT,
     int64_t ldq, float* __restrict__ s, int64_t lds) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ __align__(16) uint32_t tout[kColTileC][kColTileT / 4];  // 64 rows of 128 bytes
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const ColTile tile = col_tile(blockIdx.x, C);
@@ -186,6 +190,8 @@ __global__ void __launch_bounds__(kWThreads) quant_weight_kernel(
     const uint16_t* __restrict__ w, int64_t N, int64_t K, int64_t ldw, uint8_t* __restrict__ q,
     int64_t ldq, uint8_t* __restrict__ qt, int64_t ldqt, float* __restrict__ s, int64_t lds,
     int64_t Kb) {
+  pdl_launch_dependents();
+  pdl_wait();
   __shared__ __align__(16) uint32_t tout[kBlock][kBlock / 4];  // 128 k-rows of 128 n-bytes
   __shared__ float red[kWThreads / 32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -295,6 +301,8 @@ __global__ void __launch_bounds__(kWThreads) quant_weight_kernel(
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) cast_kernel(const float* __restrict__ x, int64_t n,
                                                    uint8_t* __restrict__ q, int vec) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i * 8 < n; i += stride) {
     const int64_t e = i * 8;
@@ -327,11 +335,8 @@ cudaError_t launch_quant_rows(const uint16_t* x, int64_t M, int64_t K, int64_t l
   const int64_t nhw = grid * (kRowThreads / 16);
   const int64_t iters = cdiv(groups, nhw * kRowUnroll);
   const bool vec = (ldx % 8 == 0) && aligned16(x);
-  if (vec)
-    quant_rows_kernel<true><<<(unsigned)grid, kRowThreads, 0, st>>>(x, M, K, ldx, q, ldq, s, lds, Kb, groups, iters);
-  else
-    quant_rows_kernel<false><<<(unsigned)grid, kRowThreads, 0, st>>>(x, M, K, ldx, q, ldq, s, lds, Kb, groups, iters);
-  return cudaGetLastError();
+  return launch_pdl(vec ? quant_rows_kernel<true> : quant_rows_kernel<false>, (unsigned)grid, kRowThreads, 0, st, x,
+                    M, K, ldx, q, ldq, s, lds, Kb, groups, iters);
 }
 
 int64_t quant_rows_grid(int64_t M, int64_t K, int num_sms) {
@@ -345,11 +350,8 @@ cudaError_t launch_quant_cols(const uint16_t* x, int64_t T, int64_t C, int64_t l
                               int64_t ldq, float* s, int64_t lds, cudaStream_t st) {
   const int64_t grid = cdiv(T, kColTileT) * cdiv(C, kColTileC);
   const bool vec = (ldx % 8 == 0) && aligned16(x);
-  if (vec)
-    quant_cols_kernel<true><<<(unsigned)grid, kColThreads, 0, st>>>(x, T, C, ldx, qT, ldq, s, lds);
-  else
-    quant_cols_kernel<false><<<(unsigned)grid, kColThreads, 0, st>>>(x, T, C, ldx, qT, ldq, s, lds);
-  return cudaGetLastError();
+  return launch_pdl(vec ? quant_cols_kernel<true> : quant_cols_kernel<false>, (unsigned)grid, kColThreads, 0, st, x, T,
+                    C, ldx, qT, ldq, s, lds);
 }
 
 cudaError_t launch_quant_weight(const uint16_t* w, int64_t N, int64_t K, int64_t ldw, uint8_t* q,
@@ -358,11 +360,8 @@ cudaError_t launch_quant_weight(const uint16_t* w, int64_t N, int64_t K, int64_t
   const int64_t Kb = cdiv(K, kBlock);
   const int64_t grid = cdiv(N, kBlock) * Kb;
   const bool vec = (ldw % 8 == 0) && aligned16(w);
-  if (vec)
-    quant_weight_kernel<true><<<(unsigned)grid, kWThreads, 0, st>>>(w, N, K, ldw, q, ldq, qt, ldqt, s, lds, Kb);
-  else
-    quant_weight_kernel<false><<<(unsigned)grid, kWThreads, 0, st>>>(w, N, K, ldw, q, ldq, qt, ldqt, s, lds, Kb);
-  return cudaGetLastError();
+  return launch_pdl(vec ? quant_weight_kernel<true> : quant_weight_kernel<false>, (unsigned)grid, kWThreads, 0, st, w,
+                    N, K, ldw, q, ldq, qt, ldqt, s, lds, Kb);
 }
 
 cudaError_t launch_cast(const float* x, int64_t n, uint8_t* q, int num_sms, cudaStream_t st) {
@@ -371,8 +370,7 @@ cudaError_t launch_cast(const float* x, int64_t n, uint8_t* q, int num_sms, cuda
   if (grid > cap) grid = cap;
   if (grid < 1) grid = 1;
   const int vec = aligned16(x) && aligned16(q);
-  cast_kernel<<<(unsigned)grid, 256, 0, st>>>(x, n, q, vec);
-  return cudaGetLastError();
+  return launch_pdl(cast_kernel, (unsigned)grid, 256, 0, st, x, n, q, vec);
 }
 
 }  // namespace bfp8

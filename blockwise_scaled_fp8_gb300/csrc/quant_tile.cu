@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(kQtThreads, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool out_row = kRow || (kScale && p.has_q_row);
   const bool out_col = kCol || (kScale && p.has_q_col);
+  pdl_launch_dependents();
 
   if (tid == 0) {
     mbar_init(bar0, 1);
@@ -168,6 +169,7 @@ __global__ void __launch_bounds__(kQtThreads, 2)
     if (out_col && p.T_al > 0) tma_prefetch_desc(&tmap_qcol);
   }
   __syncthreads();
+  pdl_wait();  // the previous kernel's writes are visible from here on
 
   // Lane l reads its rows in the order 4l + rho(i), rho(i) = (i + rot) & 3.
   const int rot = (lane >> 1) & 3;
@@ -445,8 +447,7 @@ static cudaError_t run_tile(const CUtensorMap& mx, const CUtensorMap& mr, const 
     attr = cudaFuncSetAttribute(quant_tile_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQtSmemBytes);
   });
   if (attr != cudaSuccess) return attr;
-  quant_tile_kernel<MODE><<<(unsigned)grid, kQtThreads, kQtSmemBytes, st>>>(mx, mr, mc, p);
-  return cudaGetLastError();
+  return launch_pdl(quant_tile_kernel<MODE>, (unsigned)grid, kQtThreads, kQtSmemBytes, st, mx, mr, mc, p);
 }
 
 cudaError_t launch_quant_tile(int mode, const uint16_t* x, int64_t T, int64_t C, int64_t ldx, uint8_t* q_row,

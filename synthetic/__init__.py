@@ -106,3 +106,5 @@ class MoE(Linear):
 # the MLP-up problem routed over 8 experts: same token count and per-expert
 # weight shape, so its GEMM rates compare with the dense ones
 MOE_UP = MoE("moe_up_8x_16384x14336x4096", M=16384, N=14336, K=4096, seed=5, E=8)
+# the mid problem routed over 8 experts (a size a full ncu capture handles)
+MOE_MID = MoE("moe_mid_8x_4096x4096x4096", M=4096, N=4096, K=4096, seed=6, E=8)
