@@ -2,7 +2,8 @@
 
 One step = the whole hot path over one batch, in the library's training form:
 quantise x once into its 1x128 groups along K and its 128x1 groups along M,
-and W once into its 128x128 tiles (as is and transposed); forward GEMM
+and W once into its 128x128 tiles (as is and transposed), both in one launch;
+forward GEMM
 1x128 x 128x128; quantise dY once into its 1x128 groups along N and along M
 (of dY^T); input-gradient GEMM 1x128 x 128x128 and weight-gradient GEMM
 1x128 x 128x1.
@@ -285,7 +286,7 @@ class Step:
         self.y, self.dx = e(M, N, dt=bf), e(M, K, dt=bf)
         self.dw = e(E, N, K, dt=bf) if self.moe else e(N, K, dt=bf)
         self.offs = torch.from_numpy(wl.offsets()).to(dev) if self.moe else None
-        self.names = ["quant_dual_x", "quant_weight_w", "gemm_fwd", "quant_dual_dy", "gemm_dgrad", "gemm_wgrad"]
+        self.names = ["quant_x_w", "gemm_fwd", "quant_dual_dy", "gemm_dgrad", "gemm_wgrad"]
         self.launches_per_step = len(self.names)
 
     def new_events(self):
@@ -297,8 +298,8 @@ class Step:
         if self.moe:
             o = self.offs
             return [
-                lambda: B.quant_dual(x, q_row=self.qx, s_row=self.sx, q_col=self.qxt, s_col=self.sxt),
-                lambda: B.quant_weight(w, with_q=True, with_t=True, q=self.qw, qt=self.qwt, s=self.sw),
+                lambda: B.quant_dual_weight(x, w, q_row=self.qx, s_row=self.sx, q_col=self.qxt, s_col=self.sxt,
+                                            qw=self.qw, qwt=self.qwt, sw=self.sw),
                 lambda: B.gemm_grouped_1x128_128x128(self.qx, self.sx, self.qw, self.sw, o, N, K, out=self.y),
                 lambda: B.quant_dual(dy, q_row=self.qdy, s_row=self.sdy, q_col=self.qdyt, s_col=self.sdyt),
                 lambda: B.gemm_grouped_1x128_128x128(self.qdy, self.sdy, self.qwt, self.sw, o, K, N,
@@ -306,8 +307,8 @@ class Step:
                 lambda: B.gemm_grouped_1x128_128x1(self.qdyt, self.sdyt, self.qxt, self.sxt, o, M, out=self.dw),
             ]
         return [
-            lambda: B.quant_dual(x, q_row=self.qx, s_row=self.sx, q_col=self.qxt, s_col=self.sxt),
-            lambda: B.quant_weight(w, with_q=True, with_t=True, q=self.qw, qt=self.qwt, s=self.sw),
+            lambda: B.quant_dual_weight(x, w, q_row=self.qx, s_row=self.sx, q_col=self.qxt, s_col=self.sxt,
+                                        qw=self.qw, qwt=self.qwt, sw=self.sw),
             lambda: B.gemm_1x128_128x128(self.qx, self.sx, self.qw, self.sw, K, out=self.y, M=M, N=N),
             lambda: B.quant_dual(dy, q_row=self.qdy, s_row=self.sdy, q_col=self.qdyt, s_col=self.sdyt),
             lambda: B.gemm_1x128_128x128(self.qdy, self.sdy, self.qwt, self.sw, N, sb_transposed=True,
@@ -366,8 +367,7 @@ def algorithmic_units(wl):
     cd = lambda a: (a + 127) // 128
     gem = 2.0 * M * N * K
     return {
-        "quant_dual_x": ("GB/s", 4.0 * M * K + 4.0 * (M * cd(K) + K * cd(M))),
-        "quant_weight_w": ("GB/s", E * (4.0 * N * K + 4.0 * cd(N) * cd(K))),
+        "quant_x_w": ("GB/s", 4.0 * M * K + 4.0 * (M * cd(K) + K * cd(M)) + E * (4.0 * N * K + 4.0 * cd(N) * cd(K))),
         "gemm_fwd": ("TFLOP/s", gem),
         "quant_dual_dy": ("GB/s", 4.0 * M * N + 4.0 * (M * cd(N) + N * cd(M))),
         "gemm_dgrad": ("TFLOP/s", gem),
@@ -583,7 +583,7 @@ def run_gpu(args, wl):
                 "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K,
                            **({"experts": wl.E, "expert_offsets": [int(v) for v in wl.offsets()],
                                "gemms": "grouped by expert"} if step.moe else {}),
-                           "step": "quant x (1x128 + 128x1), W (tiles + transposed); fwd GEMM; "
+                           "step": "quant x (1x128 + 128x1) and W (tiles + transposed) in one launch; fwd GEMM; "
                                    "quant dY (1x128 along N and M); dgrad GEMM; wgrad GEMM",
                            "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}",
                            "launch": "timed steps: the whole step replayed as one CUDA graph, events around "

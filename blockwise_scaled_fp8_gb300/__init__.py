@@ -25,6 +25,7 @@ EXPORTS = [
     "bfp8_debug_write_counts", "bfp8_debug_gemm_stall", "bfp8_quant_dual",
     "bfp8_linear_train_workspace_size", "bfp8_linear_fwd_train", "bfp8_linear_bwd_saved",
     "bfp8_linear_fwd_static", "bfp8_gemm_grouped_1x128_128x128", "bfp8_gemm_grouped_1x128_128x1",
+    "bfp8_quant_dual_weight",
 ]
 
 _lib = None
@@ -65,6 +66,8 @@ def lib() -> ctypes.CDLL:
     L.bfp8_check_device_errors.argtypes = [vp]
     L.bfp8_debug_write_counts.argtypes = [i32, i64, i64, i64, i32, vp, vp, ctypes.POINTER(i64)]
     L.bfp8_quant_dual.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp]
+    L.bfp8_quant_dual_weight.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64,
+                                         vp, i64, i64, vp, i64, vp, i64, vp, i64, vp]
     L.bfp8_linear_train_workspace_size.argtypes = [i64, i64, i64]
     L.bfp8_linear_train_workspace_size.restype = sz
     L.bfp8_linear_fwd_train.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
@@ -193,6 +196,32 @@ def quant_dual(x, q_row=None, s_row=None, q_col=None, s_col=None):
     return q_row, s_row, q_col, s_col
 
 
+def quant_dual_weight(x, w, q_row=None, s_row=None, q_col=None, s_col=None, qw=None, qwt=None, sw=None):
+    """quant_dual(x) and quant_weight(w, with_q=True, with_t=True) in one
+    launch (x [T,C], w [N,C]).  Returns ((q_row, s_row, q_col, s_col), (qw, qwt, sw))."""
+    torch = _torch()
+    _need_bf16_2d(x, "x")
+    _need_bf16_2d(w, "w")
+    T, C = x.shape
+    N = w.shape[0]
+    if w.shape[1] != C:
+        raise ValueError("quant_dual_weight: x and w must share their second dimension")
+    dev = x.device
+    e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
+    q_row = e((T, _rup(max(C, 1), 16)), torch.uint8) if q_row is None else q_row
+    s_row = e((_cdiv(C, BLOCK), _rup(max(T, 1), 4)), torch.float32) if s_row is None else s_row
+    q_col = e((C, _rup(max(T, 1), 16)), torch.uint8) if q_col is None else q_col
+    s_col = e((_cdiv(T, BLOCK), _rup(max(C, 1), 4)), torch.float32) if s_col is None else s_col
+    qw = e((N, _rup(max(C, 1), 16)), torch.uint8) if qw is None else qw
+    qwt = e((C, _rup(max(N, 1), 16)), torch.uint8) if qwt is None else qwt
+    sw = e((max(_cdiv(N, BLOCK), 1), max(_cdiv(C, BLOCK), 1)), torch.float32) if sw is None else sw
+    _check(lib().bfp8_quant_dual_weight(_p(x), T, C, x.stride(0), _p(q_row), q_row.stride(0), _p(s_row),
+                                        s_row.stride(0), _p(q_col), q_col.stride(0), _p(s_col), s_col.stride(0),
+                                        _p(w), N, w.stride(0), _p(qw), qw.stride(0), _p(qwt), qwt.stride(0), _p(sw),
+                                        sw.stride(0), _stream()))
+    return (q_row, s_row, q_col, s_col), (qw, qwt, sw)
+
+
 def cast_e4m3(x, q=None):
     """Elementwise RNE fp32 -> e4m3fn with saturation to +-448."""
     torch = _torch()
@@ -292,8 +321,7 @@ def moe_linear_fwd(x, w, offs, y=None):
     E, N, K = w.shape
     if N % 128:
         raise ValueError("moe_linear_fwd: the experts' output features must be a multiple of 128")
-    qx, sx, qxt, sxt = quant_dual(x)
-    qw, qwt, sw = quant_weight(w.reshape(E * N, K), with_q=True, with_t=True)
+    (qx, sx, qxt, sxt), (qw, qwt, sw) = quant_dual_weight(x, w.reshape(E * N, K))
     y = gemm_grouped_1x128_128x128(qx, sx, qw, sw, offs, N, K, out=y)
     return y, (qxt, sxt, qwt, sw)
 

@@ -103,10 +103,10 @@ bfp8_status bfp8_quant_lhs(const void* x, int64_t M, int64_t K, int64_t ldx, int
   const uint16_t* xb = (const uint16_t*)x;
   if (x_transposed ? quant_tile_supported(x, ldx, nullptr, 0, q, ldq) : quant_tile_supported(x, ldx, q, ldq, nullptr, 0)) {
     if (x_transposed)  // x is [K, M]: 128x1 groups of x along K are 1x128 groups of A = x^T
-      e = launch_quant_tile(kQuantTileCol, xb, K, M, ldx, nullptr, 0, nullptr, 0, (uint8_t*)q, ldq, s, lds, sms,
+      e = launch_quant_tile(QuantTileArgs{kQuantTileCol, xb, K, M, ldx, nullptr, 0, nullptr, 0, (uint8_t*)q, ldq, s, lds}, sms,
                             (cudaStream_t)stream);
     else
-      e = launch_quant_tile(kQuantTileRow, xb, M, K, ldx, (uint8_t*)q, ldq, s, lds, nullptr, 0, nullptr, 0, sms,
+      e = launch_quant_tile(QuantTileArgs{kQuantTileRow, xb, M, K, ldx, (uint8_t*)q, ldq, s, lds, nullptr, 0, nullptr, 0}, sms,
                             (cudaStream_t)stream);
   } else if (x_transposed) {
     e = launch_quant_cols(xb, K, M, ldx, (uint8_t*)q, ldq, s, lds, (cudaStream_t)stream);
@@ -131,8 +131,8 @@ bfp8_status bfp8_quant_rhs(const void* x, int64_t K, int64_t N, int64_t ldx, voi
   if ((st = check_device(&sms)) != BFP8_OK) return st;
   cudaError_t e;
   if (quant_tile_supported(x, ldx, nullptr, 0, qT, ldq))
-    e = launch_quant_tile(kQuantTileCol, (const uint16_t*)x, K, N, ldx, nullptr, 0, nullptr, 0, (uint8_t*)qT, ldq, s,
-                          lds, sms, (cudaStream_t)stream);
+    e = launch_quant_tile(QuantTileArgs{kQuantTileCol, (const uint16_t*)x, K, N, ldx, nullptr, 0, nullptr, 0, (uint8_t*)qT, ldq, s,
+                          lds}, sms, (cudaStream_t)stream);
   else
     e = launch_quant_cols((const uint16_t*)x, K, N, ldx, (uint8_t*)qT, ldq, s, lds, (cudaStream_t)stream);
   return e == cudaSuccess ? BFP8_OK : cuda_fail(e, "bfp8_quant_rhs launch");
@@ -162,8 +162,8 @@ bfp8_status bfp8_quant_weight(const void* w, int64_t N, int64_t K, int64_t ldw, 
   if ((st = check_device(&sms)) != BFP8_OK) return st;
   cudaError_t e;
   if (quant_tile_supported(w, ldw, q, ldq, qt, ldqt))
-    e = launch_quant_tile(kQuantTileScale, (const uint16_t*)w, N, K, ldw, (uint8_t*)q, ldq, s, lds, (uint8_t*)qt,
-                          ldqt, nullptr, 0, sms, (cudaStream_t)stream);
+    e = launch_quant_tile(QuantTileArgs{kQuantTileScale, (const uint16_t*)w, N, K, ldw, (uint8_t*)q, ldq, s, lds, (uint8_t*)qt,
+                          ldqt, nullptr, 0}, sms, (cudaStream_t)stream);
   else
     e = launch_quant_weight((const uint16_t*)w, N, K, ldw, (uint8_t*)q, ldq, (uint8_t*)qt, ldqt, s, lds,
                             (cudaStream_t)stream);
@@ -191,14 +191,53 @@ bfp8_status bfp8_quant_dual(const void* x, int64_t T, int64_t C, int64_t ldx, vo
   cudaError_t e;
   const uint16_t* xb = (const uint16_t*)x;
   if (quant_tile_supported(x, ldx, q_row, ldq_row, q_col, ldq_col)) {
-    e = launch_quant_tile(kQuantTileRow | kQuantTileCol, xb, T, C, ldx, (uint8_t*)q_row, ldq_row, s_row, lds_row,
-                          (uint8_t*)q_col, ldq_col, s_col, lds_col, sms, (cudaStream_t)stream);
+    e = launch_quant_tile(QuantTileArgs{kQuantTileRow | kQuantTileCol, xb, T, C, ldx, (uint8_t*)q_row, ldq_row, s_row, lds_row,
+                          (uint8_t*)q_col, ldq_col, s_col, lds_col}, sms, (cudaStream_t)stream);
   } else {
     e = launch_quant_rows(xb, T, C, ldx, (uint8_t*)q_row, ldq_row, s_row, lds_row, sms, (cudaStream_t)stream);
     if (e == cudaSuccess)
       e = launch_quant_cols(xb, T, C, ldx, (uint8_t*)q_col, ldq_col, s_col, lds_col, (cudaStream_t)stream);
   }
   return e == cudaSuccess ? BFP8_OK : cuda_fail(e, "bfp8_quant_dual launch");
+}
+
+bfp8_status bfp8_quant_dual_weight(const void* x, int64_t T, int64_t C, int64_t ldx, void* q_row, int64_t ldq_row,
+                                   float* s_row, int64_t lds_row, void* q_col, int64_t ldq_col, float* s_col,
+                                   int64_t lds_col, const void* w, int64_t N, int64_t ldw, void* qw, int64_t ldqw,
+                                   void* qwt, int64_t ldqwt, float* sw, int64_t ldsw, bfp8_stream_t stream) {
+  bfp8_status st = check_dims("bfp8_quant_dual_weight", T, C, N);
+  if (st != BFP8_OK) return st;
+  CHECK_ARG(x && q_row && s_row && q_col && s_col && w && qw && qwt && sw, "bfp8_quant_dual_weight: null pointer");
+  CHECK_ARG(al2(x) && al2(w) && al16(q_row) && al16(q_col) && al16(qw) && al16(qwt) && al4(s_row) && al4(s_col) &&
+                al4(sw),
+            "bfp8_quant_dual_weight: x, w 2-byte, codes 16-byte, scales 4-byte aligned");
+  CHECK_ARG(ldx >= C && ldw >= C, "bfp8_quant_dual_weight: ldx=%lld / ldw=%lld < C=%lld", (long long)ldx,
+            (long long)ldw, (long long)C);
+  CHECK_ARG(ldq_row >= C && ldq_row % 16 == 0 && ldqw >= C && ldqw % 16 == 0,
+            "bfp8_quant_dual_weight: ldq_row and ldqw must be >= C and multiples of 16");
+  CHECK_ARG(ldq_col >= T && ldq_col % 16 == 0, "bfp8_quant_dual_weight: ldq_col=%lld must be >= T and a multiple of 16",
+            (long long)ldq_col);
+  CHECK_ARG(ldqwt >= N && ldqwt % 16 == 0, "bfp8_quant_dual_weight: ldqwt=%lld must be >= N and a multiple of 16",
+            (long long)ldqwt);
+  CHECK_ARG(lds_row >= T && lds_col >= C && ldsw >= cdiv(C, kBlock), "bfp8_quant_dual_weight: scale stride too small");
+  // one of the inputs empty, or an input the TMA tile path cannot read (not
+  // 16-byte aligned, or rows not of 16-byte multiples): the two calls on their own
+  if (T == 0 || C == 0 || N == 0 || !quant_tile_supported(x, ldx, q_row, ldq_row, q_col, ldq_col) ||
+      !quant_tile_supported(w, ldw, qw, ldqw, qwt, ldqwt)) {
+    if ((st = bfp8_quant_dual(x, T, C, ldx, q_row, ldq_row, s_row, lds_row, q_col, ldq_col, s_col, lds_col, stream)) !=
+        BFP8_OK)
+      return st;
+    return bfp8_quant_weight(w, N, C, ldw, qw, ldqw, qwt, ldqwt, sw, ldsw, stream);
+  }
+  int sms = 0;
+  if ((st = check_device(&sms)) != BFP8_OK) return st;
+  const cudaError_t e = launch_quant_tile_pair(
+      QuantTileArgs{kQuantTileRow | kQuantTileCol, (const uint16_t*)x, T, C, ldx, (uint8_t*)q_row, ldq_row, s_row,
+                    lds_row, (uint8_t*)q_col, ldq_col, s_col, lds_col},
+      QuantTileArgs{kQuantTileScale, (const uint16_t*)w, N, C, ldw, (uint8_t*)qw, ldqw, sw, ldsw, (uint8_t*)qwt, ldqwt,
+                    nullptr, 0},
+      sms, (cudaStream_t)stream);
+  return e == cudaSuccess ? BFP8_OK : cuda_fail(e, "bfp8_quant_dual_weight launch");
 }
 
 static bfp8_status gemm_common(const char* fn, const GemmArgs& a, bfp8_stream_t stream,
@@ -555,13 +594,12 @@ bfp8_status bfp8_linear_fwd_train(const void* x, const void* w, void* y, int64_t
   CHECK_ARG(ws_bytes >= L.total, "bfp8_linear_fwd_train: workspace too small (%zu < %zu)", ws_bytes, L.total);
   uint8_t* b = (uint8_t*)ws;
   const int64_t Kb = cdiv(K, kBlock);
-  // one read of x: its 1x128 groups (forward) and its 128x1 groups along M (weight gradient)
-  if ((st = bfp8_quant_dual(x, M, K, K, b + L.qx, L.ldK, (float*)(b + L.sx), L.ldsM, b + L.qxt, L.ldM,
-                            (float*)(b + L.sxt), L.ldsK, stream)) != BFP8_OK)
-    return st;
-  // one read of W: its 128x128 tiles, as is (forward) and transposed (input gradient)
-  if ((st = bfp8_quant_weight(w, N, K, K, b + L.qw, L.ldK, b + L.qwt, L.ldN, (float*)(b + L.sw), Kb, stream)) !=
-      BFP8_OK)
+  // one launch, one read of x and of W: x's 1x128 groups (forward) and 128x1
+  // groups along M (weight gradient); W's 128x128 tiles as is (forward) and
+  // transposed (input gradient)
+  if ((st = bfp8_quant_dual_weight(x, M, K, K, b + L.qx, L.ldK, (float*)(b + L.sx), L.ldsM, b + L.qxt, L.ldM,
+                                   (float*)(b + L.sxt), L.ldsK, w, N, K, b + L.qw, L.ldK, b + L.qwt, L.ldN,
+                                   (float*)(b + L.sw), Kb, stream)) != BFP8_OK)
     return st;
   return bfp8_gemm_1x128_128x128(b + L.qx, L.ldK, (const float*)(b + L.sx), L.ldsM, b + L.qw, L.ldK,
                                  (const float*)(b + L.sw), Kb, 0, y, N, M, N, K, stream);

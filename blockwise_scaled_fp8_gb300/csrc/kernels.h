@@ -26,9 +26,24 @@ enum : int { kQuantTileRow = 1, kQuantTileCol = 2, kQuantTileScale = 4 };
 // x: 16-byte aligned, ldx % 8 == 0; each non-null output: 16-byte aligned, ld % 16 == 0
 bool quant_tile_supported(const void* x, int64_t ldx, const void* q_row, int64_t ldq_row, const void* q_col,
                           int64_t ldq_col);
-cudaError_t launch_quant_tile(int mode, const uint16_t* x, int64_t T, int64_t C, int64_t ldx, uint8_t* q_row,
-                              int64_t ldq_row, float* s_row, int64_t lds_row, uint8_t* q_col, int64_t ldq_col,
-                              float* s_col, int64_t lds_col, int num_sms, cudaStream_t st);
+// One input of the tile quantisation kernel (quant_tile.cu).
+struct QuantTileArgs {
+  int mode;  // kQuantTileRow, kQuantTileCol, both, or kQuantTileScale
+  const uint16_t* x;
+  int64_t T, C, ldx;
+  uint8_t* q_row;
+  int64_t ldq_row;
+  float* s_row;
+  int64_t lds_row;
+  uint8_t* q_col;
+  int64_t ldq_col;
+  float* s_col;
+  int64_t lds_col;
+};
+cudaError_t launch_quant_tile(const QuantTileArgs& a, int num_sms, cudaStream_t st);
+// Both forms of x (kQuantTileRow | kQuantTileCol) and a weight's tiles
+// (kQuantTileScale) in one launch.
+cudaError_t launch_quant_tile_pair(const QuantTileArgs& x, const QuantTileArgs& w, int num_sms, cudaStream_t st);
 cudaError_t quant_read_errors(uint32_t* out);
 
 enum SbMode : int { kSbTile = 0, kSbTileT = 1, kSbCol = 2 };

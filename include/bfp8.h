@@ -128,6 +128,22 @@ BFP8_API bfp8_status bfp8_quant_dual(const void *x, int64_t T, int64_t C, int64_
                                      bfp8_stream_t stream);
 
 /*
+ * bfp8_quant_dual of x and bfp8_quant_weight of w (with both q and qt) in
+ * one launch: a training step's forward needs both, and at small sizes one
+ * persistent launch over both inputs' tiles beats two.  Same sources as the
+ * two calls.  x device bf16 [T,C], w device bf16 [N,C] (C is the shared
+ * reduction width); arguments and layouts as in bfp8_quant_dual (q_row, s_row,
+ * q_col, s_col) and bfp8_quant_weight (qw = its q, qwt = its qt, sw = its s,
+ * ldsw >= ceil(C/128)).  (x or w not 16-byte aligned, or ldx / ldw not
+ * multiples of 8: the two calls are made instead.)
+ */
+BFP8_API bfp8_status bfp8_quant_dual_weight(const void *x, int64_t T, int64_t C, int64_t ldx,
+                                     void *q_row, int64_t ldq_row, float *s_row, int64_t lds_row,
+                                     void *q_col, int64_t ldq_col, float *s_col, int64_t lds_col,
+                                     const void *w, int64_t N, int64_t ldw, void *qw, int64_t ldqw,
+                                     void *qwt, int64_t ldqwt, float *sw, int64_t ldsw, bfp8_stream_t stream);
+
+/*
  * GEMM 1x128 x 128x128 (forward and input gradient).
  * Source: "Mask a_s/b_s scale loads in blockwise FP8 training GEMM kernels" —
  * Summary (triton_fp8_gemm_1x128_128x128_kernel, per-tile a_s/b_s) and Fix

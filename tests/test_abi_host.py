@@ -87,6 +87,49 @@ def test_gemm_argument_validation():
     assert h(P16, 256, P16, 8, P16, 256, P16, 63, P16, 64, 8, 64, 256, NULL) == B.BFP8_ERR_INVALID_ARG  # ldsb < N
 
 
+def test_grouped_and_fused_argument_validation():
+    """Host-side checks of the grouped GEMMs and of the one-launch
+    quantisation: every rejection happens before anything is launched."""
+    L = B.lib()
+    g = L.bfp8_gemm_grouped_1x128_128x128
+    #       qa   lda  sa   ldsa qb   ldb  sb   ldsb t  offs E  c    ldc Mt   N    K    st
+    ok = [P16, 256, P16, 512, P16, 256, P16, 2, 0, P16, 4, P16, 64, 512, 64, 256, NULL]
+    names = ["qa", "lda", "sa", "ldsa", "qb", "ldb", "sb", "ldsb", "t", "offs", "E", "c", "ldc", "Mt", "N", "K", "st"]
+
+    def call(**kw):
+        a = list(ok)
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return g(*a)
+
+    assert call(E=0) == B.BFP8_ERR_INVALID_ARG             # no expert
+    assert call(E=1025) == B.BFP8_ERR_INVALID_ARG          # more than 1024 experts
+    assert call(offs=NULL) == B.BFP8_ERR_INVALID_ARG
+    assert call(offs=P_ODD) == B.BFP8_ERR_INVALID_ARG       # offsets not 4-byte aligned
+    assert call(lda=200) == B.BFP8_ERR_INVALID_ARG          # lda < K
+    assert call(ldsa=511) == B.BFP8_ERR_INVALID_ARG         # ldsa < M_total
+    assert call(ldc=32) == B.BFP8_ERR_INVALID_ARG           # ldc < N
+    assert call(t=1, K=200, ldb=1024) == B.BFP8_ERR_INVALID_ARG  # input gradient: K % 16 with E > 1
+    assert call(t=1, ldb=512) == B.BFP8_ERR_INVALID_ARG     # input gradient: ldb < E*K
+    assert call(Mt=0) == B.BFP8_OK                          # no tokens: nothing to do
+    r = L.bfp8_gemm_grouped_1x128_128x1
+    #          qa   lda  sa   ldsa qb   ldb  sb   ldsb offs E  c    ldc cstride M   N   T    st
+    assert r(P16, 512, P16, 64, P16, 512, P16, 64, P16, 4, P16, 64, 64 * 64 - 1, 64, 64, 512, NULL) == \
+        B.BFP8_ERR_INVALID_ARG                              # expert stride < M*ldc
+    assert r(P16, 500, P16, 64, P16, 512, P16, 64, P16, 4, P16, 64, 64 * 64, 64, 64, 512, NULL) == \
+        B.BFP8_ERR_INVALID_ARG                              # lda < T
+    f = L.bfp8_quant_dual_weight
+    #            x    T    C    ldx  qr   ldqr sr   ldsr qc   ldqc sc   ldsc w    N   ldw  qw   ldqw qwt  ldqwt sw  ldsw st
+    args = [P16, 128, 256, 256, P16, 256, P16, 128, P16, 128, P16, 256, P16, 64, 256, P16, 256, P16, 64, P16, 2, NULL]
+    assert f(*args[:12], NULL, *args[13:]) == B.BFP8_ERR_INVALID_ARG           # no w
+    bad = list(args); bad[18] = 40
+    assert f(*bad) == B.BFP8_ERR_INVALID_ARG                                   # ldqwt < N
+    bad = list(args); bad[20] = 1
+    assert f(*bad) == B.BFP8_ERR_INVALID_ARG                                   # ldsw < Kb
+    bad = list(args); bad[14] = 200
+    assert f(*bad) == B.BFP8_ERR_INVALID_ARG                                   # ldw < C
+
+
 def test_linear_workspace_and_validation():
     L = B.lib()
     assert L.bfp8_linear_workspace_size(0, 10, 10) == 0

@@ -256,6 +256,35 @@ def test_quant_dual_bit_exact(T, C, pad):
         g.check_outside(w)
 
 
+@pytest.mark.parametrize("T,C,N", [(130, 256, 384), (1, 128, 128), (300, 520, 130), (2048, 4096, 4096),
+                                   (257, 1000, 2051)])
+def test_quant_dual_weight_one_launch_bit_exact(T, C, N):
+    """quant_dual(x) and quant_weight(w) done by one launch over both inputs'
+    tiles give exactly the oracle's bytes and scales of each."""
+    x = S.normal_bf16((T, C), 1.0, seed=T + 3 * C, outlier_frac=1e-3)
+    w = S.normal_bf16((N, C), 0.02, seed=N + 5 * C)
+    Tb, Cb, Nb = cdiv(T, 128), cdiv(C, 128), cdiv(N, 128)
+    qr, sr = Guarded(T, rup(C, 16) + 16, torch.uint8), Guarded(Cb, T + 2, torch.float32)
+    qc, sc = Guarded(C, rup(T, 16) + 16, torch.uint8), Guarded(Tb, C + 2, torch.float32)
+    qw, qwt = Guarded(N, rup(C, 16) + 16, torch.uint8), Guarded(C, rup(N, 16) + 16, torch.uint8)
+    sw = Guarded(Nb, Cb + 1, torch.float32)
+    B.quant_dual_weight(dev_bf16(x), dev_bf16(w), q_row=qr.t, s_row=sr.t, q_col=qc.t, s_col=sc.t,
+                        qw=qw.t, qwt=qwt.t, sw=sw.t)
+    torch.cuda.synchronize()
+    q_ref, s_ref = O.quant_lhs(x)
+    qT_ref, sT_ref = O.quant_rhs(x)
+    qw_ref, qwt_ref, sw_ref = O.quant_weight(w, with_t=True)
+    assert np.array_equal(qr.t.cpu().numpy()[:, :C], q_ref)
+    assert np.array_equal(f32_bits(sr.t.cpu().numpy()[:, :T]), f32_bits(s_ref))
+    assert np.array_equal(qc.t.cpu().numpy()[:, :T], qT_ref)
+    assert np.array_equal(f32_bits(sc.t.cpu().numpy()[:, :C]), f32_bits(sT_ref))
+    assert np.array_equal(qw.t.cpu().numpy()[:, :C], qw_ref)
+    assert np.array_equal(qwt.t.cpu().numpy()[:, :N], qwt_ref)
+    assert np.array_equal(f32_bits(sw.t.cpu().numpy()[:, :Cb]), f32_bits(sw_ref))
+    for g, wd in ((qr, C), (sr, T), (qc, T), (sc, C), (qw, C), (qwt, N), (sw, Cb)):
+        g.check_outside(wd)
+
+
 # ------------------------------------------------------------------ GEMMs in isolation
 
 def _random_codes(rng, shape):
