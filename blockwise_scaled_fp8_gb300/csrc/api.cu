@@ -497,11 +497,25 @@ bfp8_status bfp8_linear_fwd(const void* x, const void* w, void* y, int64_t M, in
             ws_bytes, bfp8_linear_workspace_size(M, N, K));
   uint8_t* base = (uint8_t*)ws;
   const int64_t Kb = cdiv(K, kBlock);
-  if ((st = bfp8_quant_lhs(x, M, K, K, 0, base + L.qx, L.ldK, (float*)(base + L.sx), L.ldsM, stream)) != BFP8_OK)
-    return st;
-  if ((st = bfp8_quant_weight(w, N, K, K, base + L.qw, L.ldK, nullptr, 0, (float*)(base + L.sw), Kb, stream)) !=
-      BFP8_OK)
-    return st;
+  int sms = 0;
+  if ((st = check_device(&sms)) != BFP8_OK) return st;
+  if (quant_tile_supported(x, K, base + L.qx, L.ldK, nullptr, 0) && quant_tile_supported(w, K, base + L.qw, L.ldK,
+                                                                                          nullptr, 0)) {
+    // x's 1x128 groups and W's tiles in one launch
+    const cudaError_t e = launch_quant_tile_pair(
+        QuantTileArgs{kQuantTileRow, (const uint16_t*)x, M, K, K, base + L.qx, L.ldK, (float*)(base + L.sx), L.ldsM,
+                      nullptr, 0, nullptr, 0},
+        QuantTileArgs{kQuantTileScale, (const uint16_t*)w, N, K, K, base + L.qw, L.ldK, (float*)(base + L.sw), Kb,
+                      nullptr, 0, nullptr, 0},
+        sms, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "bfp8_linear_fwd quantisation launch");
+  } else {
+    if ((st = bfp8_quant_lhs(x, M, K, K, 0, base + L.qx, L.ldK, (float*)(base + L.sx), L.ldsM, stream)) != BFP8_OK)
+      return st;
+    if ((st = bfp8_quant_weight(w, N, K, K, base + L.qw, L.ldK, nullptr, 0, (float*)(base + L.sw), Kb, stream)) !=
+        BFP8_OK)
+      return st;
+  }
   return bfp8_gemm_1x128_128x128(base + L.qx, L.ldK, (const float*)(base + L.sx), L.ldsM, base + L.qw, L.ldK,
                                  (const float*)(base + L.sw), Kb, 0, y, N, M, N, K, stream);
 }

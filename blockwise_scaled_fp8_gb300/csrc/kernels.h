@@ -41,8 +41,8 @@ struct QuantTileArgs {
   int64_t lds_col;
 };
 cudaError_t launch_quant_tile(const QuantTileArgs& a, int num_sms, cudaStream_t st);
-// Both forms of x (kQuantTileRow | kQuantTileCol) and a weight's tiles
-// (kQuantTileScale) in one launch.
+// x's 1x128 groups (kQuantTileRow), or both its forms (kQuantTileRow |
+// kQuantTileCol), and a weight's tiles (kQuantTileScale) in one launch.
 cudaError_t launch_quant_tile_pair(const QuantTileArgs& x, const QuantTileArgs& w, int num_sms, cudaStream_t st);
 cudaError_t quant_read_errors(uint32_t* out);
 

@@ -543,12 +543,16 @@ cudaError_t launch_quant_tile(const QuantTileArgs& a, int num_sms, cudaStream_t 
 }
 
 cudaError_t launch_quant_tile_pair(const QuantTileArgs& a, const QuantTileArgs& b, int num_sms, cudaStream_t st) {
-  if (a.mode != (kTileRow | kTileCol) || b.mode != kTileScale) return cudaErrorInvalidValue;
+  if (b.mode != kTileScale) return cudaErrorInvalidValue;
   CUtensorMap ma[3], mb[3];
   TileQuantParams pa, pb;
   if (!prepare_tile(a, ma, &pa) || !prepare_tile(b, mb, &pb)) return cudaErrorInvalidValue;
   const int64_t grid = qt_grid(pa.num_tiles + pb.num_tiles, num_sms);
-  return run_tile<kTileRow | kTileCol, kTileScale>(ma, mb, pa, pb, grid, st);
+  switch (a.mode) {
+    case kTileRow | kTileCol: return run_tile<kTileRow | kTileCol, kTileScale>(ma, mb, pa, pb, grid, st);
+    case kTileRow: return run_tile<kTileRow, kTileScale>(ma, mb, pa, pb, grid, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t quant_read_errors(uint32_t* out) {
