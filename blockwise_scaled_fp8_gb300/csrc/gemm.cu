@@ -33,6 +33,8 @@
 // Every mbarrier wait is bounded in time; a timeout records an error bit,
 // lets every role leave its loop, waits for its own copies/MMAs in flight and
 // frees tensor memory before the CTA exits.
+// gemm_grouped_kernel runs the same pipeline for the mixture-of-experts forms
+// (token rows or the reduction grouped by expert; see GemmJob).
 #include <cudaTypedefs.h>
 
 #include <string.h>

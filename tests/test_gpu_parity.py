@@ -431,6 +431,41 @@ def test_linear_train_form_matches_oracle(M, N, K):
         assert_gemm_close(got, ref, "train wgrad sampled")
 
 
+@pytest.mark.parametrize("M,N,K", [(300, 384, 520), (1024, 2048, 1024)])
+def test_training_step_replayed_as_one_graph(M, N, K):
+    """The whole training step (one quantisation launch for x and W, forward
+    GEMM, dY quantisation, both gradient GEMMs) captured as one CUDA graph and
+    replayed back to back: every kernel starts while the one before it
+    finishes (programmatic dependent launch) and must still read only
+    finished inputs.  New inputs are copied in between replays, so a kernel
+    that read its inputs early would produce the previous replay's results."""
+    ws = B.linear_train_workspace(M, N, K)
+    gx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    gw = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    gdy = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    dw = torch.empty((N, K), dtype=torch.bfloat16, device="cuda")
+    inputs = [_dev_linear(M, N, K, seed=20 + i) for i in range(2)]
+    gx.copy_(dev_bf16(inputs[0][0])); gw.copy_(dev_bf16(inputs[0][1])); gdy.copy_(dev_bf16(inputs[0][2]))
+    step = lambda: (B.linear_fwd_train(gx, gw, ws, y=y), B.linear_bwd_saved(gdy, ws, M, N, K, dx=dx, dw=dw))
+    step()  # one-time attribute set-up outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for rep in range(4):
+        x, w, dy = inputs[rep % 2]
+        gx.copy_(dev_bf16(x)); gw.copy_(dev_bf16(w)); gdy.copy_(dev_bf16(dy))
+        g.replay()
+        g.replay()  # twice in a row: the second replay's kernels overlap the first's tails
+        torch.cuda.synchronize()
+        B.check_device_errors()
+        assert_gemm_close(host_bf16_as_f64(y), O.linear_fwd(x, w), f"graph fwd replay {rep}")
+        assert_gemm_close(host_bf16_as_f64(dx), O.linear_dgrad(dy, w), f"graph dgrad replay {rep}")
+        assert_gemm_close(host_bf16_as_f64(dw), O.linear_wgrad(dy, x), f"graph wgrad replay {rep}")
+
+
 def _pages_sqnr():
     import os
     rows = []
