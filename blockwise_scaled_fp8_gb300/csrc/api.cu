@@ -101,13 +101,17 @@ bfp8_status bfp8_quant_lhs(const void* x, int64_t M, int64_t K, int64_t ldx, int
   if ((st = check_device(&sms)) != BFP8_OK) return st;
   cudaError_t e;
   const uint16_t* xb = (const uint16_t*)x;
-  if (x_transposed ? quant_tile_supported(x, ldx, nullptr, 0, q, ldq) : quant_tile_supported(x, ldx, q, ldq, nullptr, 0)) {
+  const bool tiled = x_transposed ? quant_tile_supported(x, ldx, nullptr, 0, q, ldq)
+                                   : quant_tile_supported(x, ldx, q, ldq, nullptr, 0);
+  if (tiled) {
     if (x_transposed)  // x is [K, M]: 128x1 groups of x along K are 1x128 groups of A = x^T
-      e = launch_quant_tile(QuantTileArgs{kQuantTileCol, xb, K, M, ldx, nullptr, 0, nullptr, 0, (uint8_t*)q, ldq, s, lds}, sms,
-                            (cudaStream_t)stream);
+      e = launch_quant_tile(
+          QuantTileArgs{kQuantTileCol, xb, K, M, ldx, nullptr, 0, nullptr, 0, (uint8_t*)q, ldq, s, lds}, sms,
+          (cudaStream_t)stream);
     else
-      e = launch_quant_tile(QuantTileArgs{kQuantTileRow, xb, M, K, ldx, (uint8_t*)q, ldq, s, lds, nullptr, 0, nullptr, 0}, sms,
-                            (cudaStream_t)stream);
+      e = launch_quant_tile(
+          QuantTileArgs{kQuantTileRow, xb, M, K, ldx, (uint8_t*)q, ldq, s, lds, nullptr, 0, nullptr, 0}, sms,
+          (cudaStream_t)stream);
   } else if (x_transposed) {
     e = launch_quant_cols(xb, K, M, ldx, (uint8_t*)q, ldq, s, lds, (cudaStream_t)stream);
   } else {
@@ -131,8 +135,9 @@ bfp8_status bfp8_quant_rhs(const void* x, int64_t K, int64_t N, int64_t ldx, voi
   if ((st = check_device(&sms)) != BFP8_OK) return st;
   cudaError_t e;
   if (quant_tile_supported(x, ldx, nullptr, 0, qT, ldq))
-    e = launch_quant_tile(QuantTileArgs{kQuantTileCol, (const uint16_t*)x, K, N, ldx, nullptr, 0, nullptr, 0, (uint8_t*)qT, ldq, s,
-                          lds}, sms, (cudaStream_t)stream);
+    e = launch_quant_tile(QuantTileArgs{kQuantTileCol, (const uint16_t*)x, K, N, ldx, nullptr, 0, nullptr, 0,
+                                        (uint8_t*)qT, ldq, s, lds},
+                          sms, (cudaStream_t)stream);
   else
     e = launch_quant_cols((const uint16_t*)x, K, N, ldx, (uint8_t*)qT, ldq, s, lds, (cudaStream_t)stream);
   return e == cudaSuccess ? BFP8_OK : cuda_fail(e, "bfp8_quant_rhs launch");
@@ -162,8 +167,9 @@ bfp8_status bfp8_quant_weight(const void* w, int64_t N, int64_t K, int64_t ldw, 
   if ((st = check_device(&sms)) != BFP8_OK) return st;
   cudaError_t e;
   if (quant_tile_supported(w, ldw, q, ldq, qt, ldqt))
-    e = launch_quant_tile(QuantTileArgs{kQuantTileScale, (const uint16_t*)w, N, K, ldw, (uint8_t*)q, ldq, s, lds, (uint8_t*)qt,
-                          ldqt, nullptr, 0}, sms, (cudaStream_t)stream);
+    e = launch_quant_tile(QuantTileArgs{kQuantTileScale, (const uint16_t*)w, N, K, ldw, (uint8_t*)q, ldq, s, lds,
+                                        (uint8_t*)qt, ldqt, nullptr, 0},
+                          sms, (cudaStream_t)stream);
   else
     e = launch_quant_weight((const uint16_t*)w, N, K, ldw, (uint8_t*)q, ldq, (uint8_t*)qt, ldqt, s, lds,
                             (cudaStream_t)stream);
@@ -191,8 +197,9 @@ bfp8_status bfp8_quant_dual(const void* x, int64_t T, int64_t C, int64_t ldx, vo
   cudaError_t e;
   const uint16_t* xb = (const uint16_t*)x;
   if (quant_tile_supported(x, ldx, q_row, ldq_row, q_col, ldq_col)) {
-    e = launch_quant_tile(QuantTileArgs{kQuantTileRow | kQuantTileCol, xb, T, C, ldx, (uint8_t*)q_row, ldq_row, s_row, lds_row,
-                          (uint8_t*)q_col, ldq_col, s_col, lds_col}, sms, (cudaStream_t)stream);
+    e = launch_quant_tile(QuantTileArgs{kQuantTileRow | kQuantTileCol, xb, T, C, ldx, (uint8_t*)q_row, ldq_row, s_row,
+                                        lds_row, (uint8_t*)q_col, ldq_col, s_col, lds_col},
+                          sms, (cudaStream_t)stream);
   } else {
     e = launch_quant_rows(xb, T, C, ldx, (uint8_t*)q_row, ldq_row, s_row, lds_row, sms, (cudaStream_t)stream);
     if (e == cudaSuccess)

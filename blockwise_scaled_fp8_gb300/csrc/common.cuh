@@ -236,7 +236,9 @@ __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32
 // kernel entry (the next kernel is only scheduled once every CTA of this grid
 // has issued it, so it never takes a slot this grid still needs).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 template <typename... P, typename... A>
 inline cudaError_t launch_pdl(void (*kernel)(P...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
