@@ -582,6 +582,68 @@ def test_mlp_up_step_full_size_sampled():
     assert_gemm_close(got, ref, "mlp_up wgrad")
 
 
+def _bench_step(wl):
+    """The benchmark's own step (its buffers, its calls, the whole step as one
+    CUDA graph), run once on the workload's inputs."""
+    import bench
+    x, w, dy = wl.x(), wl.w(), wl.dy()
+    step = bench.Step(wl, torch, B, torch.device("cuda", 0))
+    step.capture(dev_bf16(x), dev_bf16(w), dev_bf16(dy))
+    step.run_step()
+    torch.cuda.synchronize()
+    B.check_device_errors()
+    return step, x, w, dy
+
+
+def _pick(t, rows, cols):
+    return host_bf16_as_f64(t[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()])
+
+
+def _check_linear_sampled(x, w, dy, y, dx, dw, what, seed):
+    """y, dX and dW of one dense linear on sampled outputs, each computed by
+    the oracle from only the rows / columns it needs."""
+    M, K = x.shape
+    N = w.shape[0]
+    rows = _sample_idx(M, 12, seed)
+    ref, cols = _oracle_fwd_sampled(x, w, rows, _sample_idx(N // 128, 2, seed + 1))
+    assert_gemm_close(_pick(y, rows, cols), ref, f"{what} y")
+    kcols = _expand_blocks(_sample_idx(K // 128, 2, seed + 2), K)
+    qa, sa = O.quant_lhs(np.ascontiguousarray(dy[rows]))
+    _, qt, sw = O.quant_weight(np.ascontiguousarray(w[:, kcols]), with_t=True)
+    assert_gemm_close(_pick(dx, rows, kcols), O.gemm(qa, sa, qt, sw, O.SB_TILE_T, N), f"{what} dx")
+    nrows, kc = _sample_idx(N, 12, seed + 3), _sample_idx(K, 160, seed + 4)
+    qa, sa = O.quant_lhs(np.ascontiguousarray(dy[:, nrows]), transposed=True)
+    qbT, sb = O.quant_rhs(np.ascontiguousarray(x[:, kc]))
+    assert_gemm_close(_pick(dw, nrows, kc), O.gemm(qa, sa, qbT, sb, O.SB_COL, M), f"{what} dW")
+
+
+def test_bench_step_full_size_sampled():
+    """The benchmark's default workload (2048 x 4096 x 4096) in the launch
+    configuration it times: sampled y, dX and dW against the oracle."""
+    step, x, w, dy = _bench_step(S.FWD_MID)
+    _check_linear_sampled(x, w, dy, step.y, step.dx, step.dw, "bench step", seed=30)
+
+
+def test_bench_moe_step_full_size_sampled():
+    """The mixture-of-experts benchmark step (4096 tokens over 8 experts of
+    4096 x 4096, two experts without tokens) in the launch configuration the
+    benchmark times: each expert's sampled y, dX and dW against the oracle on
+    its token slice; the empty experts' gradients are zero."""
+    wl = S.MOE_MID
+    step, x, w, dy = _bench_step(wl)
+    offs = wl.offsets()
+    for e in range(wl.E):
+        t0, t1 = int(offs[e]), int(offs[e + 1])
+        if t1 == t0:
+            assert float(step.dw[e].abs().max()) == 0.0, f"expert {e} without tokens"
+            continue
+        if e not in (0, 3, 5):
+            continue  # three of the experts with tokens, to bound the oracle's time
+        we = w[e * wl.N:(e + 1) * wl.N]
+        _check_linear_sampled(x[t0:t1], we, dy[t0:t1], step.y[t0:t1], step.dx[t0:t1], step.dw[e],
+                              f"moe expert {e}", seed=40 + e)
+
+
 def test_repeat_runs_are_deterministic():
     x, w, dy = _dev_linear(512, 640, 384, seed=9)
     xd, wd, dyd = dev_bf16(x), dev_bf16(w), dev_bf16(dy)
