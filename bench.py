@@ -488,7 +488,8 @@ def run_gpu(args, wl):
     roof["kernel"] = dname
     roof["peak_source"] = peak_note
 
-    # end to end through the public API: host (pinned) -> device, fwd + bwd, device -> host
+    # end to end through the public API: host (pinned) -> device, the step's
+    # five library calls, device -> host
     e2e = None
     if not args.no_e2e:
         hx = torch.from_numpy(xh.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -496,23 +497,19 @@ def run_gpu(args, wl):
         hdy = torch.from_numpy(dyh.view(np.int16)).view(torch.bfloat16).pin_memory()
         M, N, K = wl.M, wl.N, wl.K
         E = getattr(wl, "E", 1)
-        dws = (E, N, K) if step.moe else (N, K)
-        oy = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
-        odx = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
-        odw = torch.empty(dws, dtype=torch.bfloat16).pin_memory()
+        oy = torch.empty(tuple(step.y.shape), dtype=torch.bfloat16).pin_memory()
+        odx = torch.empty(tuple(step.dx.shape), dtype=torch.bfloat16).pin_memory()
+        odw = torch.empty(tuple(step.dw.shape), dtype=torch.bfloat16).pin_memory()
         gx, gw, gdy = torch.empty_like(x), torch.empty_like(w), torch.empty_like(dy)
-        ws = None if step.moe else B.linear_train_workspace(M, N, K, device=dev)
-        gy = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-        gdx, gdw = torch.empty((M, K), dtype=torch.bfloat16, device=dev), torch.empty(dws, dtype=torch.bfloat16, device=dev)
+        calls = step._calls(gx, gw, gdy)  # quant x+W, fwd GEMM, quant dY, dgrad GEMM, wgrad GEMM
         if step.moe:
             hoffs = torch.from_numpy(wl.offsets()).pin_memory()
-            goffs = torch.empty_like(hoffs, device=dev)
-        moe_saved = [None]
 
         # copies on their own streams, overlapped with compute as a caller would:
-        # dY goes in while the forward runs, y comes out while the backward runs
+        # dY goes in while the forward runs, y comes out during the backward,
+        # dX while the weight gradient runs
         h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-        ev_xw, ev_dy, ev_y, ev_b = (torch.cuda.Event() for _ in range(4))
+        ev_xw, ev_dy, ev_y, ev_dx, ev_b = (torch.cuda.Event() for _ in range(5))
 
         def e2e_step():
             main = torch.cuda.current_stream()
@@ -521,29 +518,29 @@ def run_gpu(args, wl):
                 gx.copy_(hx, non_blocking=True)
                 gw.copy_(hw, non_blocking=True)
                 if step.moe:
-                    goffs.copy_(hoffs, non_blocking=True)
+                    step.offs.copy_(hoffs, non_blocking=True)
                 ev_xw.record(h2d)
                 gdy.copy_(hdy, non_blocking=True)
                 ev_dy.record(h2d)
             main.wait_event(ev_xw)
-            if step.moe:
-                _, moe_saved[0] = B.moe_linear_fwd(gx, gw.view(E, N, K), goffs, y=gy)
-            else:
-                B.linear_fwd_train(gx, gw, ws, y=gy)
+            calls[0]()
+            calls[1]()
             ev_y.record(main)
             d2h.wait_event(ev_y)
             with torch.cuda.stream(d2h):
-                oy.copy_(gy, non_blocking=True)
+                oy.copy_(step.y, non_blocking=True)
             main.wait_event(ev_dy)
-            if step.moe:
-                B.moe_linear_bwd(gdy, moe_saved[0], goffs, dx=gdx, dw=gdw)
-            else:
-                B.linear_bwd_saved(gdy, ws, M, N, K, dx=gdx, dw=gdw)
+            calls[2]()
+            calls[3]()
+            ev_dx.record(main)
+            d2h.wait_event(ev_dx)
+            with torch.cuda.stream(d2h):
+                odx.copy_(step.dx, non_blocking=True)
+            calls[4]()
             ev_b.record(main)
             d2h.wait_event(ev_b)
             with torch.cuda.stream(d2h):
-                odx.copy_(gdx, non_blocking=True)
-                odw.copy_(gdw, non_blocking=True)
+                odw.copy_(step.dw, non_blocking=True)
             main.wait_stream(d2h)
 
         for _ in range(args.warmup):
@@ -561,7 +558,9 @@ def run_gpu(args, wl):
         e2e = {"value": flops_step * args.steps / (tot / 1e3) / 1e12 * world, "unit": "TFLOP/s",
                "h2d_bytes_per_step": int(2 * (M * K + E * N * K + M * N) + (4 * (E + 1) if step.moe else 0)),
                "d2h_bytes_per_step": int(2 * (M * N + M * K + E * N * K)),
-               "ms_per_step": tot / args.steps}
+               "ms_per_step": tot / args.steps,
+               "path": "pinned host x, W, dY in; the step's five library calls; y, dX, dW out "
+                       "(copies on two copy streams, overlapped with the calls)"}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
