@@ -68,6 +68,11 @@ def _load():
         lib.ora_quantize_one.argtypes = [f32, f32]
         lib.ora_quantize_one.restype = ctypes.c_uint8
         lib.ora_quant_lhs.argtypes = [vp, i64, i64, i64, i32, vp, i64, vp, i64]
+        lib.ora_mx_exponent.argtypes = [f32]
+        lib.ora_mx_exponent.restype = i32
+        lib.ora_mx_quantize_one.argtypes = [f32, i32]
+        lib.ora_mx_quantize_one.restype = ctypes.c_uint8
+        lib.ora_mx_cast.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64]
         lib.ora_quant_lhs.restype = None
         lib.ora_quant_rhs.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64]
         lib.ora_quant_rhs.restype = None
@@ -210,6 +215,36 @@ def quant_weight(w: np.ndarray, with_t: bool = False, ldq: int | None = None,
     s = np.full((Nb, lds), s_fill, dtype=np.float32)
     _load().ora_quant_weight(_ptr(w), N, K, K, _ptr(q), ldq, _ptr(qt), ldqt, _ptr(s), lds)
     return q, qt, s
+
+
+# ---- MXFP8 casts (reading R14: OCP MX v1.0, FLOOR scale) -------------------
+
+MX_BLOCK = 32
+
+
+def mx_exponent(amax: float) -> int:
+    return _load().ora_mx_exponent(amax)
+
+
+def mx_quantize_one(x: float, e: int) -> int:
+    return _load().ora_mx_quantize_one(x, e)
+
+
+def mx_cast(x: np.ndarray, dim0: bool = True, dim1: bool = True, q_fill: int = 0, e_fill: int = 0):
+    """MXFP8 casts of x [M,K] bf16.  Returns (q0 [M,K], e0 [M,ceil(K/32)]) for
+    dim0 (blocks of 32 along K) and (q1 [K,M], e1 [K,ceil(M/32)]) for dim1
+    (blocks of 32 along M, transposed); None for a cast not asked for.
+    Exponents are the biased E8M0 bytes."""
+    assert x.dtype == np.uint16 and x.ndim == 2
+    x = np.ascontiguousarray(x)
+    M, K = x.shape
+    q0 = np.full((M, K), q_fill, np.uint8) if dim0 else None
+    e0 = np.full((M, max(_cdiv(K, MX_BLOCK), 1)), e_fill, np.uint8) if dim0 else None
+    q1 = np.full((K, M), q_fill, np.uint8) if dim1 else None
+    e1 = np.full((K, max(_cdiv(M, MX_BLOCK), 1)), e_fill, np.uint8) if dim1 else None
+    _load().ora_mx_cast(_ptr(x), M, K, K, _ptr(q0), K, _ptr(e0), e0.shape[1] if dim0 else 0,
+                        _ptr(q1), M, _ptr(e1), e1.shape[1] if dim1 else 0)
+    return (q0, e0), (q1, e1)
 
 
 # ---- GEMM -----------------------------------------------------------------

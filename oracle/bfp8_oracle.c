@@ -36,6 +36,16 @@
  *       to zero gives 0x80.
  *   R5  the GEMM result is kept in double: per K-block partial sums are exact
  *       double sums of exact e4m3 products, then scaled by (double)a_s*b_s.
+ *   R14 MXFP8 ([P3] "Fixes accuracy error for mxfp8 linear": the mxfp8 linear,
+ *       its dim1 cast kernel and ScaleCalculationMode.FLOOR) follows the OCP
+ *       Microscaling Formats v1.0 definition, which the page does not spell
+ *       out: blocks of 32 elements, one E8M0 scale 2^e per block with
+ *       e = floor(log2(amax)) - 8 (8 = the exponent of 448, E4M3's largest
+ *       normal), clamped to [-127, 127] (e = -127 for an all-zero block),
+ *       stored biased as e + 127; codes RNE_e4m3(clamp(fl32(x * 2^-e), +-448)).
+ *       The dim0 cast groups 32 consecutive elements of a row; the dim1 cast
+ *       groups 32 consecutive elements of a column and writes codes and
+ *       scales transposed (the dim0 cast of the transpose).
  *
  * Parity pins (tests/test_oracle_pins.py) tie every function here to facts the
  * pages or the mathematics fix; no function is "parity unpinned".
@@ -309,6 +319,74 @@ float ora_group_scale(float amax) {
 uint8_t ora_quantize_one(float x, float s) {
     float r = x / s;
     return ora_e4m3_rne(r);
+}
+
+/* ---------------------------------------------------------------------- */
+/* MXFP8 casts (reading R14)                                               */
+/* ---------------------------------------------------------------------- */
+
+#define ORA_MX_BLOCK 32
+
+/* e = floor(log2(amax)) - 8 clamped to [-127, 127]; -127 for amax == 0.
+ * frexpf gives amax = f * 2^ex with f in [0.5, 1), so floor(log2(amax)) = ex - 1
+ * for every positive finite amax, subnormals included. */
+int ora_mx_exponent(float amax) {
+    if (!(amax > 0.0f)) return -127;
+    int ex;
+    (void)frexpf(amax, &ex);
+    int e = (ex - 1) - 8;
+    if (e < -127) e = -127;
+    if (e > 127) e = 127;
+    return e;
+}
+
+/* q = RNE_e4m3(clamp(fl32(x * 2^-e), +-448)): one fp32 multiplication by a
+ * power of two (exact unless the product falls below the normal range). */
+uint8_t ora_mx_quantize_one(float x, int e) {
+    return ora_e4m3_rne(x * ldexpf(1.0f, -e));
+}
+
+/*
+ * MXFP8 cast of x [M,K] (bf16, row stride ldx).
+ *   dim0 (q0 != NULL): blocks of 32 along K; q0[m * ldq0 + k], biased
+ *        exponents e0[m * lde0 + k / 32] (lde0 >= ceil(K/32)).
+ *   dim1 (q1 != NULL): blocks of 32 along M, written transposed:
+ *        q1[k * ldq1 + m], e1[k * lde1 + m / 32] (lde1 >= ceil(M/32)).
+ * A tail block takes its amax over its in-range elements; nothing else is written.
+ */
+void ora_mx_cast(const uint16_t *x, int64_t M, int64_t K, int64_t ldx,
+                 uint8_t *q0, int64_t ldq0, uint8_t *e0, int64_t lde0,
+                 uint8_t *q1, int64_t ldq1, uint8_t *e1, int64_t lde1) {
+    if (q0) {
+        for (int64_t m = 0; m < M; ++m)
+            for (int64_t k0 = 0; k0 < K; k0 += ORA_MX_BLOCK) {
+                int64_t k1 = k0 + ORA_MX_BLOCK < K ? k0 + ORA_MX_BLOCK : K;
+                float amax = 0.0f;
+                for (int64_t k = k0; k < k1; ++k) {
+                    float v = fabsf(ora_bf16_to_f32(x[m * ldx + k]));
+                    if (v > amax) amax = v;
+                }
+                int e = ora_mx_exponent(amax);
+                e0[m * lde0 + k0 / ORA_MX_BLOCK] = (uint8_t)(e + 127);
+                for (int64_t k = k0; k < k1; ++k)
+                    q0[m * ldq0 + k] = ora_mx_quantize_one(ora_bf16_to_f32(x[m * ldx + k]), e);
+            }
+    }
+    if (q1) {
+        for (int64_t k = 0; k < K; ++k)
+            for (int64_t m0 = 0; m0 < M; m0 += ORA_MX_BLOCK) {
+                int64_t m1 = m0 + ORA_MX_BLOCK < M ? m0 + ORA_MX_BLOCK : M;
+                float amax = 0.0f;
+                for (int64_t m = m0; m < m1; ++m) {
+                    float v = fabsf(ora_bf16_to_f32(x[m * ldx + k]));
+                    if (v > amax) amax = v;
+                }
+                int e = ora_mx_exponent(amax);
+                e1[k * lde1 + m0 / ORA_MX_BLOCK] = (uint8_t)(e + 127);
+                for (int64_t m = m0; m < m1; ++m)
+                    q1[k * ldq1 + m] = ora_mx_quantize_one(ora_bf16_to_f32(x[m * ldx + k]), e);
+            }
+    }
 }
 
 /*

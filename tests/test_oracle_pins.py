@@ -507,3 +507,79 @@ def test_moe_linear_with_shared_weights_is_the_dense_linear():
     ref = O.linear_wgrad(dy, x)
     np.testing.assert_allclose(dw.sum(axis=0), ref, rtol=1e-11, atol=1e-12 * np.abs(ref).max())
     assert np.all(dw[1] == 0.0)
+
+
+# ---------------------------------------------------------------- MXFP8 casts
+
+def _bf16_exponent_field(a: np.ndarray) -> np.ndarray:
+    return (a.astype(np.int64) >> 7) & 0xFF
+
+
+def test_mx_exponent_is_the_largest_power_of_two_at_or_below_amax_over_all_bf16():
+    """e + 8 is the exponent field of the bf16 amax minus the bias (normal
+    values), clamped at -127 (zero, subnormals and amax < 2^-118): checked for
+    every positive finite bf16 value from its bits, not from a logarithm."""
+    bits = np.arange(1, 0x7F80, dtype=np.uint16)
+    vals = S.bf16_bits_to_f32(bits)
+    E = _bf16_exponent_field(bits)
+    want = np.maximum(E - 127 - 8, -127)
+    got = np.array([O.mx_exponent(float(v)) for v in vals[::7]])
+    assert np.array_equal(got, want[::7])
+    assert O.mx_exponent(0.0) == -127
+
+
+def test_mx_quantize_one_is_the_nearest_code_of_the_scaled_value():
+    """Brute-force nearest-code search (ties to even) on x * 2^-e, clamped."""
+    rng = np.random.default_rng(71)
+    xs = S.bf16_bits_to_f32(S.f32_to_bf16_bits(rng.standard_normal(400).astype(np.float32) * 100))
+    for x in xs:
+        for e in (-9, 0, 3, -127, 60):
+            r = float(np.float32(x) * np.float32(2.0 ** -e))
+            r = max(-448.0, min(448.0, r))
+            assert O.mx_quantize_one(float(x), e) == O.e4m3_nearest(r), (x, e)
+
+
+def test_mx_cast_block_maxima_reach_the_top_binade_and_errors_are_half_ulp():
+    """With e = floor(log2 amax) - 8 the block maximum scales into [256, 512):
+    its code is 256..448 (saturating above 448).  Every other element is
+    within half an e4m3 ulp of x * 2^-e (or saturated at 448)."""
+    x = S.normal_bf16((37, 200), 1.0, seed=72, outlier_frac=0.01)
+    (q0, e0), _ = O.mx_cast(x, dim1=False)
+    T = O.e4m3_table()
+    xf = S.bf16_bits_to_f32(x).astype(np.float64)
+    for m in range(x.shape[0]):
+        for b in range(e0.shape[1]):
+            blk = slice(32 * b, min(32 * b + 32, x.shape[1]))
+            e = int(e0[m, b]) - 127
+            r = xf[m, blk] * 2.0 ** -e
+            d = T[q0[m, blk]]
+            assert 256.0 <= np.abs(d).max() <= 448.0
+            sat = np.abs(r) > 448.0
+            assert np.all(np.abs(d[sat]) == 448.0)
+            ulp = np.where(np.abs(r) >= 2.0 ** -6, 2.0 ** (np.floor(np.log2(np.maximum(np.abs(r), 2.0 ** -6))) - 3),
+                           2.0 ** -9)
+            assert np.all(np.abs(d[~sat] - r[~sat]) <= ulp[~sat] / 2 + 1e-30)
+
+
+def test_mx_dim1_cast_is_the_dim0_cast_of_the_transpose_with_tails():
+    x = S.normal_bf16((70, 45), 1.0, seed=73)
+    (q0, e0), (q1, e1) = O.mx_cast(x)
+    (qt0, et0), _ = O.mx_cast(np.ascontiguousarray(x.T), dim1=False)
+    assert np.array_equal(q1, qt0) and np.array_equal(e1, et0)
+    # tail blocks: the last 32-block of a row holds 45 - 32 = 13 elements, its
+    # exponent comes from those alone
+    xf = np.abs(S.bf16_bits_to_f32(x))
+    for m in range(x.shape[0]):
+        assert int(e0[m, 1]) - 127 == O.mx_exponent(float(xf[m, 32:].max()))
+
+
+def test_mx_cast_power_of_two_invariance_and_zero_blocks():
+    x = S.normal_bf16((8, 64), 1.0, seed=74)
+    (q0, e0), _ = O.mx_cast(x, dim1=False)
+    x4 = S.f32_to_bf16_bits(S.bf16_bits_to_f32(x) * np.float32(16.0))
+    (q4, e4), _ = O.mx_cast(x4, dim1=False)
+    assert np.array_equal(q0, q4) and np.array_equal(e4.astype(int), e0.astype(int) + 4)
+    z = np.zeros((3, 40), np.uint16)
+    z[1] = 0x8000  # -0
+    (qz, ez), _ = O.mx_cast(z, dim1=False)
+    assert np.all(ez == 0) and np.all(qz[0] == 0) and np.all(qz[1] == 0x80)
