@@ -25,7 +25,7 @@ EXPORTS = [
     "bfp8_debug_write_counts", "bfp8_debug_gemm_stall", "bfp8_quant_dual",
     "bfp8_linear_train_workspace_size", "bfp8_linear_fwd_train", "bfp8_linear_bwd_saved",
     "bfp8_linear_fwd_static", "bfp8_gemm_grouped_1x128_128x128", "bfp8_gemm_grouped_1x128_128x1",
-    "bfp8_quant_dual_weight",
+    "bfp8_quant_dual_weight", "bfp8_mx_cast",
 ]
 
 _lib = None
@@ -66,6 +66,7 @@ def lib() -> ctypes.CDLL:
     L.bfp8_check_device_errors.argtypes = [vp]
     L.bfp8_debug_write_counts.argtypes = [i32, i64, i64, i64, i32, vp, vp, ctypes.POINTER(i64)]
     L.bfp8_quant_dual.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp]
+    L.bfp8_mx_cast.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp]
     L.bfp8_quant_dual_weight.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64,
                                          vp, i64, i64, vp, i64, vp, i64, vp, i64, vp]
     L.bfp8_linear_train_workspace_size.argtypes = [i64, i64, i64]
@@ -220,6 +221,27 @@ def quant_dual_weight(x, w, q_row=None, s_row=None, q_col=None, s_col=None, qw=N
                                         _p(w), N, w.stride(0), _p(qw), qw.stride(0), _p(qwt), qwt.stride(0), _p(sw),
                                         sw.stride(0), _stream()))
     return (q_row, s_row, q_col, s_col), (qw, qwt, sw)
+
+
+def mx_cast(x, dim0: bool = True, dim1: bool = True, q0=None, e0=None, q1=None, e1=None):
+    """MXFP8 casts of x [M,K] (E4M3 codes, E8M0 exponents per 32 elements):
+    dim0 -> (q0 [M, ldq0], e0 [M, ceil(K/32)]), dim1 (transposed) -> (q1 [K, ldq1],
+    e1 [K, ceil(M/32)]); None for a cast not asked for."""
+    torch = _torch()
+    _need_bf16_2d(x, "x")
+    M, K = x.shape
+    dev = x.device
+    if dim0:
+        q0 = torch.empty((M, _rup(max(K, 1), 16)), dtype=torch.uint8, device=dev) if q0 is None else q0
+        e0 = torch.empty((M, max(_cdiv(K, 32), 1)), dtype=torch.uint8, device=dev) if e0 is None else e0
+    if dim1:
+        q1 = torch.empty((K, _rup(max(M, 1), 16)), dtype=torch.uint8, device=dev) if q1 is None else q1
+        e1 = torch.empty((K, max(_cdiv(M, 32), 1)), dtype=torch.uint8, device=dev) if e1 is None else e1
+    _check(lib().bfp8_mx_cast(_p(x), M, K, x.stride(0), _p(q0) if dim0 else None, q0.stride(0) if dim0 else 0,
+                              _p(e0) if dim0 else None, e0.stride(0) if dim0 else 0,
+                              _p(q1) if dim1 else None, q1.stride(0) if dim1 else 0,
+                              _p(e1) if dim1 else None, e1.stride(0) if dim1 else 0, _stream()))
+    return (q0 if dim0 else None, e0 if dim0 else None), (q1 if dim1 else None, e1 if dim1 else None)
 
 
 def cast_e4m3(x, q=None):

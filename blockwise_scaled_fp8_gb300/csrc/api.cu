@@ -247,6 +247,35 @@ bfp8_status bfp8_quant_dual_weight(const void* x, int64_t T, int64_t C, int64_t 
   return e == cudaSuccess ? BFP8_OK : cuda_fail(e, "bfp8_quant_dual_weight launch");
 }
 
+bfp8_status bfp8_mx_cast(const void* x, int64_t M, int64_t K, int64_t ldx, void* q0, int64_t ldq0, void* e0,
+                         int64_t lde0, void* q1, int64_t ldq1, void* e1, int64_t lde1, bfp8_stream_t stream) {
+  bfp8_status st = check_dims("bfp8_mx_cast", M, K);
+  if (st != BFP8_OK) return st;
+  if (M == 0 || K == 0) return BFP8_OK;
+  CHECK_ARG(x && (q0 || q1), "bfp8_mx_cast: null input or no output asked for");
+  CHECK_ARG(!q0 == !e0 && !q1 == !e1, "bfp8_mx_cast: each cast needs its codes and its exponents");
+  CHECK_ARG(ldx >= K, "bfp8_mx_cast: ldx=%lld < K=%lld", (long long)ldx, (long long)K);
+  if (q0) {
+    CHECK_ARG(ldq0 >= K && ldq0 % 16 == 0, "bfp8_mx_cast: ldq0=%lld must be >= K and a multiple of 16",
+              (long long)ldq0);
+    CHECK_ARG(lde0 >= cdiv(K, 32), "bfp8_mx_cast: lde0=%lld < ceil(K/32)", (long long)lde0);
+  }
+  if (q1) {
+    CHECK_ARG(ldq1 >= M && ldq1 % 16 == 0, "bfp8_mx_cast: ldq1=%lld must be >= M and a multiple of 16",
+              (long long)ldq1);
+    CHECK_ARG(lde1 >= cdiv(M, 32), "bfp8_mx_cast: lde1=%lld < ceil(M/32)", (long long)lde1);
+  }
+  CHECK_ARG(quant_tile_supported(x, ldx, q0, ldq0, q1, ldq1),
+            "bfp8_mx_cast: x and the codes must be 16-byte aligned, ldx a multiple of 8");
+  int sms = 0;
+  if ((st = check_device(&sms)) != BFP8_OK) return st;
+  QuantTileArgs a{kQuantTileMx | (q0 ? kQuantTileRow : 0) | (q1 ? kQuantTileCol : 0),
+                  (const uint16_t*)x, M, K, ldx, (uint8_t*)q0, ldq0, nullptr, 0, (uint8_t*)q1, ldq1, nullptr, 0,
+                  (uint8_t*)e0, lde0, (uint8_t*)e1, lde1};
+  const cudaError_t e = launch_quant_tile(a, sms, (cudaStream_t)stream);
+  return e == cudaSuccess ? BFP8_OK : cuda_fail(e, "bfp8_mx_cast launch");
+}
+
 static bfp8_status gemm_common(const char* fn, const GemmArgs& a, bfp8_stream_t stream,
                                uint64_t wait_limit_ns = kWaitLimitNs, int debug_stall = 0) {
   bfp8_status st = check_dims(fn, a.M, a.N, a.K);

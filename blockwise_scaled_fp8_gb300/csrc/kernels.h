@@ -22,7 +22,9 @@ cudaError_t launch_quant_weight(const uint16_t* w, int64_t N, int64_t K, int64_t
 cudaError_t launch_cast(const float* x, int64_t n, uint8_t* q, int num_sms, cudaStream_t st);
 
 // TMA-staged tile quantisation (quant_tile.cu): which outputs one read makes.
-enum : int { kQuantTileRow = 1, kQuantTileCol = 2, kQuantTileScale = 4 };
+// kQuantTileMx: MXFP8 instead (blocks of 32, E8M0 exponents): with kQuantTileRow the dim0
+// cast (q_row, e_row), with kQuantTileCol the transposed dim1 cast (q_col, e_col)
+enum : int { kQuantTileRow = 1, kQuantTileCol = 2, kQuantTileScale = 4, kQuantTileMx = 8 };
 // x: 16-byte aligned, ldx % 8 == 0; each non-null output: 16-byte aligned, ld % 16 == 0
 bool quant_tile_supported(const void* x, int64_t ldx, const void* q_row, int64_t ldq_row, const void* q_col,
                           int64_t ldq_col);
@@ -39,6 +41,10 @@ struct QuantTileArgs {
   int64_t ldq_col;
   float* s_col;
   int64_t lds_col;
+  uint8_t* e_row;  // kQuantTileMx: biased exponents, e_row[t * lde_row + c / 32]
+  int64_t lde_row;
+  uint8_t* e_col;  //                                  e_col[c * lde_col + t / 32]
+  int64_t lde_col;
 };
 cudaError_t launch_quant_tile(const QuantTileArgs& a, int num_sms, cudaStream_t st);
 // x's 1x128 groups (kQuantTileRow), or both its forms (kQuantTileRow |

@@ -49,6 +49,7 @@ static __device__ uint32_t g_quant_error;
 namespace {
 
 constexpr int kTileRow = kQuantTileRow, kTileCol = kQuantTileCol, kTileScale = kQuantTileScale;
+constexpr int kTileMx = kQuantTileMx;
 constexpr int kQtBoxBytes = 128 * 128;               // 64 bf16 columns x 128 rows
 constexpr int kQtStageBytes = 2 * kQtBoxBytes;       // one 128x128 bf16 tile
 // once the tile is in registers its stage holds the outputs:
@@ -75,6 +76,10 @@ struct TileQuantParams {
   int has_q_row, has_q_col;
   int64_t tiles_c, num_tiles;
   uint64_t wait_limit_ns;
+  uint8_t* e_row;  // MXFP8: biased exponents of the dim0 and dim1 casts
+  int64_t lde_row;
+  uint8_t* e_col;
+  int64_t lde_col;
 };
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -138,14 +143,35 @@ __device__ __forceinline__ uint32_t neg_codes2(uint32_t w, uint64_t s2, uint64_t
   return cvt_e4m3x2(__uint_as_float((uint32_t)q1), __uint_as_float((uint32_t)(q1 >> 32)));
 }
 
+// MXFP8 (OCP Microscaling v1.0, FLOOR scale): for a block maximum amax (a
+// bf16 value, here its 15 magnitude bits), e = floor(log2(amax)) - 8 clamped
+// to [-127, 127]: amax's exponent field E gives e = max(E - 135, -127) (zero
+// and subnormals included: they clamp).  Returns the biased byte e + 127, and
+// in *mult the fp32 2^-e (a normal float: e <= 119 for bf16 inputs).
+__device__ __forceinline__ uint32_t mx_exponent(uint32_t amax_bits15, float* mult) {
+  const int E = (int)(amax_bits15 >> 7);
+  const int e = max(E - 135, -127);
+  *mult = __uint_as_float((uint32_t)(127 - e) << 23);
+  return (uint32_t)(e + 127);
+}
+
+// e4m3 codes of x * mult for the two bf16 values of `w` (mult2 = (m, m')):
+// one exact power-of-two product per value, rounded to nearest even and
+// saturated at 448 by the conversion.
+__device__ __forceinline__ uint32_t mx_codes2(uint32_t w, uint64_t mult2) {
+  const uint64_t r = f2_mul(f2_pack(bf16_lo(w), bf16_hi(w)), mult2);
+  return cvt_e4m3x2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
+}
+
 }  // namespace
 
 // Phase 1 of a tile: this thread's 4 x 8 input values from the stage into
 // registers, and its partial row / column (or tile) maxima into shared memory.
 template <int MODE>
-__device__ __forceinline__ void qt_load_reduce(uint32_t stage, uint4 (&v)[4], int warp, int lane, int rot,
-                                               uint32_t rowred, uint32_t colred) {
+__device__ __forceinline__ void qt_load_reduce(uint32_t stage, uint4 (&v)[4], uint32_t (&cm)[4], int warp, int lane,
+                                               int rot, uint32_t rowred, uint32_t colred) {
   constexpr bool kRow = (MODE & kTileRow) != 0, kCol = (MODE & kTileCol) != 0, kScale = (MODE & kTileScale) != 0;
+  constexpr bool kMx = (MODE & kTileMx) != 0;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = 4 * lane + ((i + rot) & 3);
@@ -165,13 +191,21 @@ __device__ __forceinline__ void qt_load_reduce(uint32_t stage, uint4 (&v)[4], in
       for (int i = 0; i < 4; ++i) sts32(rowred + 4u * (uint32_t)(warp * 128 + 4 * lane + ((i + rot) & 3)), rm[i]);
     }
     if (kCol) {
-      uint32_t cm[4];  // per column pair of the chunk, over this thread's 4 rows
+      // per column pair of the chunk, over this thread's 4 rows
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         cm[q] = amax2(amax2(word_of(v[0], q), word_of(v[1], q)), amax2(word_of(v[2], q), word_of(v[3], q)));
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(colred + 16u * (uint32_t)(warp * 32 + lane)),
-                   "r"(cm[0]), "r"(cm[1]), "r"(cm[2]), "r"(cm[3])
-                   : "memory");
+      if (kMx) {
+        // MXFP8: a 32-row block is the 4 rows of 8 consecutive lanes
+#pragma unroll
+        for (int off = 1; off <= 4; off <<= 1)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) cm[q] = amax2(cm[q], __shfl_xor_sync(0xffffffffu, cm[q], off));
+      } else {
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(colred + 16u * (uint32_t)(warp * 32 + lane)),
+                     "r"(cm[0]), "r"(cm[1]), "r"(cm[2]), "r"(cm[3])
+                     : "memory");
+      }
     }
   }
 }
@@ -181,13 +215,79 @@ __device__ __forceinline__ void qt_load_reduce(uint32_t stage, uint4 (&v)[4], in
 template <int MODE>
 __device__ __forceinline__ void qt_scale_store(const CUtensorMap* tmap_qrow, const CUtensorMap* tmap_qcol,
                                                const TileQuantParams& p, int64_t tile, uint32_t stage,
-                                               const uint4 (&v)[4], int tid, int warp, int lane, int rot,
-                                               uint32_t sel_e, uint32_t sel_o, uint32_t sbase, uint32_t rowred,
-                                               uint32_t colred) {
+                                               const uint4 (&v)[4], const uint32_t (&cm)[4], int tid, int warp,
+                                               int lane, int rot, uint32_t sel_e, uint32_t sel_o, uint32_t sbase,
+                                               uint32_t rowred, uint32_t colred) {
   constexpr bool kRow = (MODE & kTileRow) != 0, kCol = (MODE & kTileCol) != 0, kScale = (MODE & kTileScale) != 0;
+  constexpr bool kMx = (MODE & kTileMx) != 0;
   const bool out_row = kRow || (kScale && p.has_q_row);
   const bool out_col = kCol || (kScale && p.has_q_col);
   const int64_t t0 = qt_tile_t0(tile, p.tiles_c), c0 = qt_tile_c0(tile, p.tiles_c);
+  if constexpr (kMx) {
+    // ------------------------------------------------ MXFP8 exponents
+    if (kRow) {  // dim0: thread tid takes row tid & 127, 32-column block tid >> 7
+      const int r = tid & 127, g = tid >> 7;
+      uint32_t m = 0;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t w;
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w) : "r"(rowred + 4u * (uint32_t)((4 * g + j) * 128 + r)));
+        m = amax2(m, w);
+      }
+      m = amax2(m, __byte_perm(m, 0, 0x1032));
+      float mult;
+      const uint32_t eb = mx_exponent((m >> 16) & 0x7FFFu, &mult);
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(sbase + kQtOffRowSc + 4u * (uint32_t)(g * 128 + r)), "f"(mult)
+                   : "memory");
+      if (t0 + r < p.T && c0 + 32 * g < p.C) p.e_row[(t0 + r) * p.lde_row + c0 / 32 + g] = (uint8_t)eb;
+    }
+    float cmult[8];  // dim1: the 2^-e of this thread's 8 columns over its lane group's 32 rows
+    if (kCol) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        mx_exponent(cm[q] & 0x7FFFu, &cmult[2 * q]);
+        mx_exponent((cm[q] >> 16) & 0x7FFFu, &cmult[2 * q + 1]);
+      }
+      // lane l of the 8-lane group h = l / 8 stores the exponent of column 8*warp + l % 8
+      const int j = lane & 7, h = lane >> 3;
+      const uint32_t w = j < 2 ? cm[0] : j < 4 ? cm[1] : j < 6 ? cm[2] : cm[3];
+      float unused;
+      const uint32_t eb = mx_exponent(((j & 1) ? (w >> 16) : w) & 0x7FFFu, &unused);
+      if (c0 + 8 * warp + j < p.C && t0 + 32 * h < p.T)
+        p.e_col[(c0 + 8 * warp + j) * p.lde_col + t0 / 32 + h] = (uint8_t)eb;
+    }
+    __syncthreads();  // the row multipliers are visible
+
+    // ------------------------------------------------ codes into the spent stage
+    if (kCol) {
+      const uint32_t dst = stage + kQtOutCol + (uint32_t)(8 * warp * 128 + 4 * lane);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint64_t mult2 = f2_pack(cmult[2 * q], cmult[2 * q + 1]);
+        uint32_t cc[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) cc[i] = mx_codes2(word_of(v[i], q), mult2);
+        const uint32_t X = __byte_perm(cc[0], cc[1], 0x5140), Y = __byte_perm(cc[2], cc[3], 0x5140);
+        sts32(dst + (uint32_t)((2 * q) * 128), __byte_perm(X, Y, sel_e));
+        sts32(dst + (uint32_t)((2 * q + 1) * 128), __byte_perm(X, Y, sel_o));
+      }
+    }
+    if (kRow) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = 4 * lane + ((i + rot) & 3);
+        float mult;
+        asm volatile("ld.shared.f32 %0, [%1];"
+                     : "=f"(mult)
+                     : "r"(sbase + kQtOffRowSc + 4u * (uint32_t)((warp >> 2) * 128 + r)));
+        const uint64_t mult2 = f2_pack(mult, mult);
+        const uint32_t c01 = mx_codes2(v[i].x, mult2), c23 = mx_codes2(v[i].y, mult2);
+        const uint32_t c45 = mx_codes2(v[i].z, mult2), c67 = mx_codes2(v[i].w, mult2);
+        sts64(stage + kQtOutRow + (uint32_t)(r * 128 + ((((warp >> 1) ^ (r & 7)) << 4) | ((warp & 1) << 3))),
+              __byte_perm(c01, c23, 0x5410), __byte_perm(c45, c67, 0x5410));
+      }
+    }
+  } else {
   // ------------------------------------------------ scales
   float tile_s = 0.0f, tile_ny = 0.0f;
   if (kScale) {
@@ -292,6 +392,7 @@ __device__ __forceinline__ void qt_scale_store(const CUtensorMap* tmap_qrow, con
       sts64(stage + kQtOutRow + (uint32_t)(r * 128 + ((((warp >> 1) ^ (r & 7)) << 4) | ((warp & 1) << 3))), lo, hi);
     }
   }
+  }  // blockwise scales
   fence_proxy_async_shared();
   __syncthreads();  // the output tiles are complete
   if (tid == 0) {
@@ -417,8 +518,9 @@ __global__ void __launch_bounds__(kQtThreads, 2)
     }
     const bool in_a = tile < na;
     uint4 v[4];
-    if (in_a) qt_load_reduce<MODE_A>(stage, v, warp, lane, rot, rowred, colred);
-    else qt_load_reduce<MODE_B>(stage, v, warp, lane, rot, rowred, colred);
+    uint32_t cm[4];  // MXFP8: the column maxima of this lane group's 32 rows
+    if (in_a) qt_load_reduce<MODE_A>(stage, v, cm, warp, lane, rot, rowred, colred);
+    else qt_load_reduce<MODE_B>(stage, v, cm, warp, lane, rot, rowred, colred);
     __syncthreads();  // partial maxima visible; the input tile is in registers
     if (tid == 0 && it >= 1) {
       // the other stage held the previous tile's outputs: once their stores
@@ -429,11 +531,11 @@ __global__ void __launch_bounds__(kQtThreads, 2)
     }
 
     if (in_a)
-      qt_scale_store<MODE_A>(&tmap_qrow_a, &tmap_qcol_a, pa, tile, stage, v, tid, warp, lane, rot, sel_e, sel_o,
-                             sbase, rowred, colred);
+      qt_scale_store<MODE_A>(&tmap_qrow_a, &tmap_qcol_a, pa, tile, stage, v, cm, tid, warp, lane, rot, sel_e,
+                             sel_o, sbase, rowred, colred);
     else
-      qt_scale_store<MODE_B>(&tmap_qrow_b, &tmap_qcol_b, pb, tile - na, stage, v, tid, warp, lane, rot, sel_e, sel_o,
-                             sbase, rowred, colred);
+      qt_scale_store<MODE_B>(&tmap_qrow_b, &tmap_qcol_b, pb, tile - na, stage, v, cm, tid, warp, lane, rot, sel_e,
+                             sel_o, sbase, rowred, colred);
   }
   if (tid == 0) bulk_wait_all();  // stores complete before the CTA exits
 }
@@ -523,6 +625,10 @@ static bool prepare_tile(const QuantTileArgs& a, CUtensorMap (&m)[3], TileQuantP
   p->tiles_c = cdiv(a.C, 128);
   p->num_tiles = cdiv(a.T, 128) * p->tiles_c;
   p->wait_limit_ns = kWaitLimitNs;
+  p->e_row = a.e_row;
+  p->lde_row = a.lde_row;
+  p->e_col = a.e_col;
+  p->lde_col = a.lde_col;
   return true;
 }
 
@@ -538,6 +644,10 @@ cudaError_t launch_quant_tile(const QuantTileArgs& a, int num_sms, cudaStream_t 
     case kTileCol: return run_tile<kTileCol, kTileCol>(m, m, p, none, grid, st);
     case kTileRow | kTileCol: return run_tile<kTileRow | kTileCol, kTileRow | kTileCol>(m, m, p, none, grid, st);
     case kTileScale: return run_tile<kTileScale, kTileScale>(m, m, p, none, grid, st);
+    case kTileMx | kTileRow | kTileCol:
+      return run_tile<kTileMx | kTileRow | kTileCol, kTileMx | kTileRow | kTileCol>(m, m, p, none, grid, st);
+    case kTileMx | kTileRow: return run_tile<kTileMx | kTileRow, kTileMx | kTileRow>(m, m, p, none, grid, st);
+    case kTileMx | kTileCol: return run_tile<kTileMx | kTileCol, kTileMx | kTileCol>(m, m, p, none, grid, st);
     default: return cudaErrorInvalidValue;
   }
 }

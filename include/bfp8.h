@@ -144,6 +144,24 @@ BFP8_API bfp8_status bfp8_quant_dual_weight(const void *x, int64_t T, int64_t C,
                                      void *qwt, int64_t ldqwt, float *sw, int64_t ldsw, bfp8_stream_t stream);
 
 /*
+ * MXFP8 casts of x [M,K] (bf16): E4M3 codes with one E8M0 exponent per block
+ * of 32 elements.  Source: "Fixes accuracy error for mxfp8 linear" (the mxfp8
+ * linear, its dim1 cast kernel, ScaleCalculationMode.FLOOR); the page does not
+ * spell the format out, so the OCP Microscaling Formats v1.0 definition is
+ * taken: e = floor(log2(amax)) - 8 clamped to [-127, 127] (-127 for an
+ * all-zero block), stored biased (e + 127); q = RNE_e4m3(clamp(x * 2^-e, +-448)).
+ *   dim0 (q0, e0 non-null): blocks of 32 along K; q0[m*ldq0 + k],
+ *        e0[m*lde0 + k/32], ldq0 >= K, lde0 >= ceil(K/32).
+ *   dim1 (q1, e1 non-null): blocks of 32 along M, written transposed;
+ *        q1[k*ldq1 + m], e1[k*lde1 + m/32], ldq1 >= M, lde1 >= ceil(M/32).
+ *   x and q0 / q1 16-byte aligned, ldx a multiple of 8, ldq0 / ldq1 multiples
+ *   of 16 (BFP8_ERR_INVALID_ARG otherwise).  Either cast or both from one read.
+ */
+BFP8_API bfp8_status bfp8_mx_cast(const void *x, int64_t M, int64_t K, int64_t ldx,
+                                 void *q0, int64_t ldq0, void *e0, int64_t lde0,
+                                 void *q1, int64_t ldq1, void *e1, int64_t lde1, bfp8_stream_t stream);
+
+/*
  * GEMM 1x128 x 128x128 (forward and input gradient).
  * Source: "Mask a_s/b_s scale loads in blockwise FP8 training GEMM kernels" —
  * Summary (triton_fp8_gemm_1x128_128x128_kernel, per-tile a_s/b_s) and Fix

@@ -130,6 +130,26 @@ def test_grouped_and_fused_argument_validation():
     assert f(*bad) == B.BFP8_ERR_INVALID_ARG                                   # ldw < C
 
 
+def test_mx_cast_argument_validation():
+    L = B.lib()
+    f = L.bfp8_mx_cast
+    #          x    M   K    ldx  q0   ldq0 e0   lde0 q1   ldq1 e1   lde1 st
+    ok = [P16, 64, 256, 256, P16, 256, P16, 8, P16, 64, P16, 2, NULL]
+    assert f(*ok[:4], NULL, 0, NULL, 0, NULL, 0, NULL, 0, NULL) == B.BFP8_ERR_INVALID_ARG   # no output
+    bad = list(ok); bad[6] = NULL
+    assert f(*bad) == B.BFP8_ERR_INVALID_ARG                     # codes without exponents
+    bad = list(ok); bad[5] = 264
+    assert f(*bad) == B.BFP8_ERR_INVALID_ARG                     # ldq0 not a multiple of 16
+    bad = list(ok); bad[7] = 7
+    assert f(*bad) == B.BFP8_ERR_INVALID_ARG                     # lde0 < ceil(K/32)
+    bad = list(ok); bad[11] = 1
+    assert f(*bad) == B.BFP8_ERR_INVALID_ARG                     # lde1 < ceil(M/32)
+    bad = list(ok); bad[3] = 260
+    assert f(*bad) == B.BFP8_ERR_INVALID_ARG                     # ldx not a multiple of 8 (no TMA path)
+    bad = list(ok); bad[1] = 0
+    assert f(*bad) == B.BFP8_OK                                  # empty: nothing to do
+
+
 def test_linear_workspace_and_validation():
     L = B.lib()
     assert L.bfp8_linear_workspace_size(0, 10, 10) == 0

@@ -285,6 +285,42 @@ def test_quant_dual_weight_one_launch_bit_exact(T, C, N):
         g.check_outside(wd)
 
 
+MX_SHAPES = [(130, 256, 0), (1, 32, 0), (64, 1000, 0), (300, 520, 8), (2048, 4096, 0), (257, 72, 0),
+             (512, 512, 0), (33, 4104, 0), (4096, 1024, 0), (96, 136, 16)]
+
+
+@pytest.mark.parametrize("M,K,pad", MX_SHAPES)
+@pytest.mark.parametrize("casts", ["both", "dim0", "dim1"])
+def test_mx_cast_bit_exact(M, K, pad, casts):
+    """MXFP8 casts (dim0 along K; dim1 along M, written transposed) give the
+    oracle's codes and E8M0 exponents byte for byte, on tail shapes, padded
+    rows, outliers, zero blocks and subnormal inputs; nothing outside the
+    outputs is written."""
+    x = S.normal_bf16((M, K), 1.0, seed=M + 7 * K, outlier_frac=2e-3)
+    x[:, :min(32, K)][: max(1, M // 7)] = 0                      # all-zero blocks
+    x[-1, -min(16, K):] = 0x0003                                  # bf16 subnormals
+    d0, d1 = casts in ("both", "dim0"), casts in ("both", "dim1")
+    q0 = Guarded(M, rup(K, 16) + 16, torch.uint8) if d0 else None
+    e0 = Guarded(M, cdiv(K, 32) + 3, torch.uint8) if d0 else None
+    q1 = Guarded(K, rup(M, 16) + 16, torch.uint8) if d1 else None
+    e1 = Guarded(K, cdiv(M, 32) + 3, torch.uint8) if d1 else None
+    xd = _padded_dev(x, pad) if pad else dev_bf16(x)
+    B.mx_cast(xd, dim0=d0, dim1=d1, q0=q0.t if d0 else None, e0=e0.t if d0 else None,
+              q1=q1.t if d1 else None, e1=e1.t if d1 else None)
+    torch.cuda.synchronize()
+    (rq0, re0), (rq1, re1) = O.mx_cast(x, dim0=d0, dim1=d1)
+    if d0:
+        assert np.array_equal(q0.t.cpu().numpy()[:, :K], rq0)
+        assert np.array_equal(e0.t.cpu().numpy()[:, :cdiv(K, 32)], re0)
+        q0.check_outside(K)
+        e0.check_outside(cdiv(K, 32))
+    if d1:
+        assert np.array_equal(q1.t.cpu().numpy()[:, :M], rq1)
+        assert np.array_equal(e1.t.cpu().numpy()[:, :cdiv(M, 32)], re1)
+        q1.check_outside(M)
+        e1.check_outside(cdiv(M, 32))
+
+
 # ------------------------------------------------------------------ GEMMs in isolation
 
 def _random_codes(rng, shape):
