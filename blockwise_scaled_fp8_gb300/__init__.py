@@ -488,3 +488,12 @@ def debug_write_counts(kind: int, M: int, N: int, K: int, flag: int = 0):
                                          scounts.ctypes.data_as(ctypes.c_void_p) if scounts is not None else None,
                                          ctypes.byref(oob)))
     return counts, scounts, int(oob.value)
+
+
+def __getattr__(name):
+    # the autograd wrapper lives in its own module (it imports torch at load)
+    if name in ("Float8BlockwiseLinear", "blockwise_fp8_linear"):
+        from . import module
+        return getattr(module, name)
+    raise AttributeError(name)
+

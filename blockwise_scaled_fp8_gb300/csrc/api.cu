@@ -38,11 +38,29 @@ struct DevInfo {
 DevInfo g_dev[64];
 std::mutex g_dev_mu;
 
-// The kernels are built for sm_103a only.  Returns the SM count via *sms.
-bfp8_status check_device(int* sms) {
+// A host thread that never selected a device (an autograd worker, a thread
+// pool) reports device 0 without having its primary context current, and an
+// extensible launch from it fails with "invalid argument".  Selecting the
+// device once per thread makes the context current.
+bfp8_status bind_thread_device(int* dev_out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  thread_local int bound = -1;
+  if (bound != dev) {
+    e = cudaSetDevice(dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+    bound = dev;
+  }
+  *dev_out = dev;
+  return BFP8_OK;
+}
+
+// The kernels are built for sm_103a only.  Returns the SM count via *sms.
+bfp8_status check_device(int* sms) {
+  int dev = 0;
+  bfp8_status st = bind_thread_device(&dev);
+  if (st != BFP8_OK) return st;
   if (dev < 0 || dev >= 64) return fail(BFP8_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
   std::lock_guard<std::mutex> lk(g_dev_mu);
   DevInfo& d = g_dev[dev];
@@ -436,6 +454,9 @@ bfp8_status bfp8_cast_e4m3(const float* x, int64_t n, void* q, bfp8_stream_t str
 }
 
 bfp8_status bfp8_check_device_errors(bfp8_stream_t stream) {
+  int dev = 0;
+  bfp8_status st = bind_thread_device(&dev);
+  if (st != BFP8_OK) return st;
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "bfp8_check_device_errors: stream synchronize");
   uint32_t bits = 0, qbits = 0;

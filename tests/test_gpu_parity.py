@@ -502,6 +502,54 @@ def test_training_step_replayed_as_one_graph(M, N, K):
         assert_gemm_close(host_bf16_as_f64(dw), O.linear_wgrad(dy, x), f"graph wgrad replay {rep}")
 
 
+def test_float8_blockwise_linear_module_forward_and_backward():
+    """The autograd module: y = x W^T forward, dX and dW from y.backward(dY),
+    on a 3-d input (the token dims are flattened), against the oracle."""
+    M0, M1, N, K = 2, 65, 384, 256
+    x, w, dy = _dev_linear(M0 * M1, N, K, seed=60)
+    xd = dev_bf16(x).reshape(M0, M1, K).requires_grad_(True)
+    layer = B.Float8BlockwiseLinear(K, N, device="cuda")
+    with torch.no_grad():
+        layer.weight.copy_(dev_bf16(w))
+    y = layer(xd)
+    assert y.shape == (M0, M1, N) and y.dtype == torch.bfloat16
+    y.backward(dev_bf16(dy).reshape(M0, M1, N))
+    torch.cuda.synchronize()
+    B.check_device_errors()
+    assert_gemm_close(host_bf16_as_f64(y.detach().reshape(-1, N)), O.linear_fwd(x, w), "module y")
+    assert_gemm_close(host_bf16_as_f64(xd.grad.reshape(-1, K)), O.linear_dgrad(dy, w), "module dX")
+    assert_gemm_close(host_bf16_as_f64(layer.weight.grad), O.linear_wgrad(dy, x), "module dW")
+
+
+def test_library_calls_from_a_thread_that_selected_no_device():
+    """Autograd runs backward on a worker thread; a fresh host thread that never
+    selected a device must still be able to launch (the library binds the
+    thread to its current device)."""
+    import threading
+    M, N, K = 256, 256, 384
+    x, w, dy = _dev_linear(M, N, K, seed=61)
+    xd, wd, dyd = dev_bf16(x), dev_bf16(w), dev_bf16(dy)
+    out, errs = {}, []
+
+    def work():
+        try:
+            ws = B.linear_train_workspace(M, N, K, device=xd.device)
+            out["y"] = B.linear_fwd_train(xd, wd, ws)
+            out["dx"], out["dw"] = B.linear_bwd_saved(dyd, ws, M, N, K)
+            torch.cuda.synchronize()
+        except Exception as e:  # reported on the main thread
+            errs.append(e)
+
+    t = threading.Thread(target=work)
+    t.start()
+    t.join()
+    assert not errs, errs
+    B.check_device_errors()
+    assert_gemm_close(host_bf16_as_f64(out["y"]), O.linear_fwd(x, w), "thread y")
+    assert_gemm_close(host_bf16_as_f64(out["dx"]), O.linear_dgrad(dy, w), "thread dX")
+    assert_gemm_close(host_bf16_as_f64(out["dw"]), O.linear_wgrad(dy, x), "thread dW")
+
+
 def _pages_sqnr():
     import os
     rows = []
