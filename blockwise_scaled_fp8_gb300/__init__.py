@@ -25,7 +25,8 @@ EXPORTS = [
     "bfp8_debug_write_counts", "bfp8_debug_gemm_stall", "bfp8_quant_dual",
     "bfp8_linear_train_workspace_size", "bfp8_linear_fwd_train", "bfp8_linear_bwd_saved",
     "bfp8_linear_fwd_static", "bfp8_gemm_grouped_1x128_128x128", "bfp8_gemm_grouped_1x128_128x1",
-    "bfp8_quant_dual_weight", "bfp8_mx_cast",
+    "bfp8_quant_dual_weight", "bfp8_mx_cast", "bfp8_linear_step_host_workspace_size",
+    "bfp8_linear_step_host",
 ]
 
 _lib = None
@@ -73,6 +74,9 @@ def lib() -> ctypes.CDLL:
     L.bfp8_linear_train_workspace_size.restype = sz
     L.bfp8_linear_fwd_train.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
     L.bfp8_linear_bwd_saved.argtypes = [vp, vp, vp, i64, i64, i64, vp, sz, vp]
+    L.bfp8_linear_step_host_workspace_size.argtypes = [i64, i64, i64]
+    L.bfp8_linear_step_host_workspace_size.restype = sz
+    L.bfp8_linear_step_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, sz, vp]
     L.bfp8_linear_fwd_static.argtypes = [vp, vp, vp, i64, i64, i64, vp]
     L.bfp8_gemm_grouped_1x128_128x128.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, vp, i64, vp, i64,
                                                   i64, i64, i64, vp]
@@ -80,7 +84,8 @@ def lib() -> ctypes.CDLL:
                                                 i64, i64, i64, vp]
     L.bfp8_debug_gemm_stall.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, i64, i64, vp]
     for name in EXPORTS:
-        if name not in ("bfp8_last_error", "bfp8_linear_workspace_size", "bfp8_linear_train_workspace_size"):
+        if name not in ("bfp8_last_error", "bfp8_linear_workspace_size", "bfp8_linear_train_workspace_size",
+                        "bfp8_linear_step_host_workspace_size"):
             getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -463,6 +468,42 @@ def linear_bwd_saved(dy, ws, M: int, N: int, K: int, dx=None, dw=None):
     wp, wn = _aligned(ws)
     _check(lib().bfp8_linear_bwd_saved(_p(dy), _p(dx), _p(dw), M, N, K, wp, wn, _stream()))
     return dx, dw
+
+
+def linear_step_host_workspace(M: int, N: int, K: int, device="cuda"):
+    """Device workspace for linear_step_host (256 bytes of slack for alignment)."""
+    torch = _torch()
+    return torch.empty(int(lib().bfp8_linear_step_host_workspace_size(M, N, K)) + 256, dtype=torch.uint8,
+                       device=device)
+
+
+def linear_step_host(x, w, dy, ws, y=None, dx=None, dw=None, chunk_n: int = 0):
+    """One training step from host tensors (see bfp8_linear_step_host): x [M,K],
+    w [N,K], dy [M,N] contiguous bf16 CPU tensors (pinned for overlap); returns
+    host (y, dx, dw), allocated pinned when not given.  Enqueued on the current
+    CUDA stream: synchronise it before reading the outputs."""
+    torch = _torch()
+    for name, t in (("x", x), ("w", w), ("dy", dy)):
+        if t.device.type != "cpu" or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"linear_step_host: {name} must be a contiguous bf16 CPU tensor")
+    M, K = x.shape
+    N = w.shape[0]
+    if tuple(w.shape) != (N, K) or tuple(dy.shape) != (M, N):
+        raise ValueError(f"linear_step_host: shapes x {tuple(x.shape)}, w {tuple(w.shape)}, dy {tuple(dy.shape)}")
+    pin = torch.cuda.is_available()
+    if y is None:
+        y = torch.empty((M, N), dtype=torch.bfloat16, pin_memory=pin)
+    if dx is None:
+        dx = torch.empty((M, K), dtype=torch.bfloat16, pin_memory=pin)
+    if dw is None:
+        dw = torch.empty((N, K), dtype=torch.bfloat16, pin_memory=pin)
+    for name, t, shp in (("y", y, (M, N)), ("dx", dx, (M, K)), ("dw", dw, (N, K))):
+        if t.device.type != "cpu" or t.dtype != torch.bfloat16 or not t.is_contiguous() or tuple(t.shape) != shp:
+            raise ValueError(f"linear_step_host: {name} must be a contiguous bf16 CPU tensor of shape {shp}")
+    wp, wn = _aligned(ws)
+    _check(lib().bfp8_linear_step_host(_p(x), _p(w), _p(dy), _p(y), _p(dx), _p(dw), M, N, K, int(chunk_n),
+                                       wp, wn, _stream()))
+    return y, dx, dw
 
 
 def check_device_errors() -> None:

@@ -699,6 +699,200 @@ bfp8_status bfp8_linear_bwd_saved(const void* dy, void* dx, void* dw, int64_t M,
 }
 
 // ---------------------------------------------------------------------------
+// One training step from host memory, copies overlapped with the kernels
+// ---------------------------------------------------------------------------
+
+namespace {
+struct HostStepLayout {
+  size_t x, w, dy, y, dx, dw, train, total;
+};
+HostStepLayout host_step_layout(int64_t M, int64_t N, int64_t K) {
+  HostStepLayout H;
+  size_t o = 0;
+  H.x = o; o = a256(o + (size_t)M * K * 2);
+  H.w = o; o = a256(o + (size_t)N * K * 2);
+  H.dy = o; o = a256(o + (size_t)M * N * 2);
+  H.y = o; o = a256(o + (size_t)M * N * 2);
+  H.dx = o; o = a256(o + (size_t)M * K * 2);
+  H.dw = o; o = a256(o + (size_t)N * K * 2);
+  H.train = o; o += train_layout(M, N, K).total;
+  H.total = o;
+  return H;
+}
+
+constexpr int kMaxStepChunks = 64;
+constexpr int kMaxDgradPieces = 4;
+
+// Columns of W / dY per pipeline chunk when the caller passes 0: about an
+// eighth of N, at least 512, a multiple of 128 (one weight tile row).
+int64_t step_chunk_n(int64_t N) {
+  const int64_t c = rup(cdiv(N, 8) > 512 ? cdiv(N, 8) : 512, kBlock);
+  return c;
+}
+
+// The copy streams and events of the host step on one device: created on the
+// first call, kept for the life of the process.  Calls on one device enqueue
+// under the mutex; a wait binds to the event's latest record at enqueue time,
+// so reusing the events across calls is safe.
+struct HostStepCtx {
+  std::mutex mu;
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start, x_in, in_end, out_end;
+  cudaEvent_t chunk_in[kMaxStepChunks], y_done[kMaxStepChunks], dw_done[kMaxStepChunks];
+  cudaEvent_t dx_done[kMaxDgradPieces];
+};
+HostStepCtx g_step[64];
+
+cudaError_t host_step_init(HostStepCtx& C) {
+  if (C.ready) return cudaSuccess;
+  cudaError_t e;
+  if ((e = cudaStreamCreateWithFlags(&C.in, cudaStreamNonBlocking)) != cudaSuccess) return e;
+  if ((e = cudaStreamCreateWithFlags(&C.out, cudaStreamNonBlocking)) != cudaSuccess) return e;
+  std::vector<cudaEvent_t*> evs = {&C.start, &C.x_in, &C.in_end, &C.out_end};
+  for (int i = 0; i < kMaxStepChunks; ++i) {
+    evs.push_back(&C.chunk_in[i]);
+    evs.push_back(&C.y_done[i]);
+    evs.push_back(&C.dw_done[i]);
+  }
+  for (int i = 0; i < kMaxDgradPieces; ++i) evs.push_back(&C.dx_done[i]);
+  for (cudaEvent_t* ev : evs)
+    if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
+  C.ready = true;
+  return cudaSuccess;
+}
+}  // namespace
+
+size_t bfp8_linear_step_host_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  return host_step_layout(M, N, K).total;
+}
+
+bfp8_status bfp8_linear_step_host(const void* x, const void* w, const void* dy, void* y, void* dx, void* dw,
+                                  int64_t M, int64_t N, int64_t K, int64_t chunk_n, void* ws, size_t ws_bytes,
+                                  bfp8_stream_t stream) {
+  const char* fn = "bfp8_linear_step_host";
+  bfp8_status st = check_dims(fn, M, N, K);
+  if (st != BFP8_OK) return st;
+  CHECK_ARG(M > 0 && N > 0 && K > 0, "%s: dimensions must be positive", fn);
+  CHECK_ARG(x && w && dy && y && dx && dw && ws, "%s: null pointer", fn);
+  CHECK_ARG((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "%s: workspace must be 256-byte aligned", fn);
+  CHECK_ARG(chunk_n >= 0 && chunk_n % kBlock == 0, "%s: chunk_n=%lld must be 0 (automatic) or a multiple of 128", fn,
+            (long long)chunk_n);
+  const HostStepLayout H = host_step_layout(M, N, K);
+  CHECK_ARG(ws_bytes >= H.total, "%s: workspace too small (%zu < %zu)", fn, ws_bytes, H.total);
+  const int64_t Nc = chunk_n ? chunk_n : step_chunk_n(N);
+  const int64_t nc = cdiv(N, Nc);
+  CHECK_ARG(nc <= kMaxStepChunks, "%s: %lld chunks of %lld columns exceed %d; pass a larger chunk_n", fn,
+            (long long)nc, (long long)Nc, kMaxStepChunks);
+  int sms = 0, dev = 0;
+  if ((st = check_device(&sms)) != BFP8_OK) return st;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  HostStepCtx& C = g_step[dev];
+  std::lock_guard<std::mutex> lk(C.mu);
+  if ((e = host_step_init(C)) != cudaSuccess) return cuda_fail(e, "bfp8_linear_step_host: stream/event creation");
+
+  const cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* base = (uint8_t*)ws;
+  uint16_t *d_x = (uint16_t*)(base + H.x), *d_w = (uint16_t*)(base + H.w), *d_dy = (uint16_t*)(base + H.dy);
+  uint16_t *d_y = (uint16_t*)(base + H.y), *d_dx = (uint16_t*)(base + H.dx), *d_dw = (uint16_t*)(base + H.dw);
+  const TrainLayout L = train_layout(M, N, K);
+  uint8_t* b = base + H.train;
+  const int64_t Kb = cdiv(K, kBlock);
+  const size_t row_x = (size_t)K * 2, row_y = (size_t)N * 2;
+  const char* h_x = (const char*)x;
+  const char* h_w = (const char*)w;
+  const char* h_dy = (const char*)dy;
+
+  // Enqueue everything, stopping at the first failure; the caller's stream
+  // then waits on both copy streams either way, so later work stays ordered.
+  cudaError_t ce = cudaSuccess;
+  const char* what = nullptr;
+  auto cu = [&](cudaError_t r, const char* w_) {
+    if (ce == cudaSuccess && r != cudaSuccess) {
+      ce = r;
+      what = w_;
+    }
+    return ce == cudaSuccess;
+  };
+  auto ok = [&](bfp8_status r) {
+    if (st == BFP8_OK) st = r;
+    return st == BFP8_OK;
+  };
+
+  bool go = cu(cudaEventRecord(C.start, s), "event record") && cu(cudaStreamWaitEvent(C.in, C.start, 0), "wait") &&
+            cu(cudaStreamWaitEvent(C.out, C.start, 0), "wait");
+  // inputs, in the order the kernels need them: x, then W and dY chunk by chunk
+  go = go && cu(cudaMemcpyAsync(d_x, h_x, (size_t)M * row_x, cudaMemcpyDefault, C.in), "copy x in") &&
+       cu(cudaEventRecord(C.x_in, C.in), "event record");
+  for (int64_t j = 0; go && j < nc; ++j) {
+    const int64_t n0 = j * Nc, nj = (N - n0 < Nc) ? N - n0 : Nc;
+    go = cu(cudaMemcpyAsync((char*)d_w + n0 * row_x, h_w + n0 * row_x, (size_t)nj * row_x, cudaMemcpyDefault, C.in),
+            "copy W in") &&
+         cu(cudaMemcpy2DAsync((char*)d_dy + n0 * 2, row_y, h_dy + n0 * 2, row_y, (size_t)nj * 2, (size_t)M,
+                              cudaMemcpyDefault, C.in),
+            "copy dY in") &&
+         cu(cudaEventRecord(C.chunk_in[j], C.in), "event record");
+  }
+
+  // x in both forms: 1x128 along K (forward lhs), 128x1 along M (weight-gradient rhs)
+  go = go && cu(cudaStreamWaitEvent(s, C.x_in, 0), "wait") &&
+       ok(bfp8_quant_dual(d_x, M, K, K, b + L.qx, L.ldK, (float*)(b + L.sx), L.ldsM, b + L.qxt, L.ldM,
+                          (float*)(b + L.sxt), L.ldsK, stream));
+  for (int64_t j = 0; go && j < nc; ++j) {
+    const int64_t n0 = j * Nc, nj = (N - n0 < Nc) ? N - n0 : Nc, nb0 = n0 / kBlock;
+    go = cu(cudaStreamWaitEvent(s, C.chunk_in[j], 0), "wait") &&
+         // W rows n0..n0+nj: tiles as is and transposed, tile scales at tile row nb0
+         ok(bfp8_quant_weight(d_w + n0 * K, nj, K, K, b + L.qw + n0 * L.ldK, L.ldK, b + L.qwt + n0, L.ldN,
+                              (float*)(b + L.sw) + nb0 * Kb, Kb, stream)) &&
+         // y[:, n0..n0+nj] = x W_j^T
+         ok(bfp8_gemm_1x128_128x128(b + L.qx, L.ldK, (const float*)(b + L.sx), L.ldsM, b + L.qw + n0 * L.ldK,
+                                    L.ldK, (const float*)(b + L.sw) + nb0 * Kb, Kb, 0, d_y + n0, N, M, nj, K,
+                                    stream)) &&
+         cu(cudaEventRecord(C.y_done[j], s), "event record") && cu(cudaStreamWaitEvent(C.out, C.y_done[j], 0), "wait") &&
+         cu(cudaMemcpy2DAsync((char*)y + n0 * 2, row_y, (const char*)d_y + n0 * 2, row_y, (size_t)nj * 2, (size_t)M,
+                              cudaMemcpyDefault, C.out),
+            "copy y out") &&
+         // dY[:, n0..n0+nj] in both forms: 1x128 along N (input-gradient lhs), along M of dY^T (weight-gradient lhs)
+         ok(bfp8_quant_dual(d_dy + n0, M, nj, N, b + L.qdy + n0, L.ldN, (float*)(b + L.sdy) + nb0 * L.ldsM, L.ldsM,
+                            b + L.qdyt + n0 * L.ldM, L.ldM, (float*)(b + L.sdyt) + n0, L.ldsN, stream)) &&
+         // dW[n0..n0+nj, :] = dY_j^T x
+         ok(bfp8_gemm_1x128_128x1(b + L.qdyt + n0 * L.ldM, L.ldM, (const float*)(b + L.sdyt) + n0, L.ldsN,
+                                  b + L.qxt, L.ldM, (const float*)(b + L.sxt), L.ldsK, d_dw + n0 * K, K, nj, K, M,
+                                  stream)) &&
+         cu(cudaEventRecord(C.dw_done[j], s), "event record") &&
+         cu(cudaStreamWaitEvent(C.out, C.dw_done[j], 0), "wait") &&
+         cu(cudaMemcpyAsync((char*)dw + n0 * row_x, (const char*)d_dw + n0 * row_x, (size_t)nj * row_x,
+                            cudaMemcpyDefault, C.out),
+            "copy dW out");
+  }
+  // dX = dY W, needing every chunk, in row pieces so that the first pieces
+  // leave while the last ones run
+  const int np = M >= 1024 ? kMaxDgradPieces : (M >= 512 ? 2 : 1);
+  const int64_t Mp = rup(cdiv(M, np), kBlock);
+  for (int p = 0; go && p < np && p * Mp < M; ++p) {
+    const int64_t m0 = p * Mp, mp = (M - m0 < Mp) ? M - m0 : Mp;
+    go = ok(bfp8_gemm_1x128_128x128(b + L.qdy + m0 * L.ldN, L.ldN, (const float*)(b + L.sdy) + m0, L.ldsM,
+                                    b + L.qwt, L.ldN, (const float*)(b + L.sw), Kb, 1, d_dx + m0 * K, K, mp, K, N,
+                                    stream)) &&
+         cu(cudaEventRecord(C.dx_done[p], s), "event record") &&
+         cu(cudaStreamWaitEvent(C.out, C.dx_done[p], 0), "wait") &&
+         cu(cudaMemcpyAsync((char*)dx + m0 * row_x, (const char*)d_dx + m0 * row_x, (size_t)mp * row_x,
+                            cudaMemcpyDefault, C.out),
+            "copy dX out");
+  }
+  // join: the caller's stream continues after every copy of this step
+  cudaEventRecord(C.in_end, C.in);
+  cudaEventRecord(C.out_end, C.out);
+  cudaStreamWaitEvent(s, C.in_end, 0);
+  const cudaError_t je = cudaStreamWaitEvent(s, C.out_end, 0);
+  if (st != BFP8_OK) return st;
+  if (ce != cudaSuccess) return cuda_fail(ce, what);
+  return je == cudaSuccess ? BFP8_OK : cuda_fail(je, "bfp8_linear_step_host: join");
+}
+
+// ---------------------------------------------------------------------------
 // Host replay of the kernels' index arithmetic
 // ---------------------------------------------------------------------------
 

@@ -285,6 +285,44 @@ BFP8_API bfp8_status bfp8_linear_bwd_saved(const void *dy, void *dx, void *dw, i
                                            int64_t K, void *ws, size_t ws_bytes, bfp8_stream_t stream);
 
 /*
+ * One whole training step of the linear layer from HOST memory: copies x, W
+ * and dY in, runs the training form (forward y = x W^T, input gradient
+ * dX = dY W, weight gradient dW = dY^T x, each operand quantised once in the
+ * method's groups — 1x128 for x / dY, 128x128 tiles for W, 128x1 along M
+ * for the weight gradient's right operand; "Enable blockwise FP8 dense
+ * training kernels on ROCm", the Float8BlockwiseLinear forward/backward) and
+ * copies y, dX and dW out.  Results equal those of bfp8_linear_fwd_train +
+ * bfp8_linear_bwd_saved on the same inputs.
+ *
+ * The copies overlap the kernels: W and dY travel in chunks of `chunk_n`
+ * output features (0 = automatic: about N/8, at least 512; otherwise a
+ * multiple of 128, at most 64 chunks); chunk j's forward and weight-gradient
+ * GEMMs run while chunk j+1 arrives, and its y and dW columns leave while
+ * later chunks run; dX is computed in up to four row pieces at the end and
+ * leaves piece by piece.  The copies run on two streams the library creates
+ * per device (once, kept for the process); the caller's `stream` orders the
+ * step: nothing starts before work already on it, and work enqueued on it
+ * afterwards runs after every copy of the step.
+ *
+ *   x [M,K], w [N,K], dy [M,N] (inputs), y [M,N], dx [M,K], dw [N,K]
+ *   (outputs): contiguous row-major bf16 in host memory.  Page-locked memory
+ *   (cudaHostAlloc / cudaHostRegister) lets the copies run asynchronously;
+ *   pageable memory works, with copies that block the host.  (Device
+ *   pointers also work: copies use cudaMemcpyDefault.)  The buffers must stay
+ *   valid and the inputs unmodified until the stream reaches the end of the
+ *   step; the outputs are complete once it has.
+ *   ws: device, >= bfp8_linear_step_host_workspace_size(M,N,K) bytes,
+ *   256-byte aligned; holds the device copies and the quantised operands.
+ * Errors: BFP8_ERR_INVALID_ARG for bad sizes, pointers, chunk_n or workspace
+ * (nothing enqueued); launch or copy failures return their status after the
+ * caller's stream has been joined to the copy streams.
+ */
+BFP8_API size_t bfp8_linear_step_host_workspace_size(int64_t M, int64_t N, int64_t K);
+BFP8_API bfp8_status bfp8_linear_step_host(const void *x, const void *w, const void *dy, void *y, void *dx,
+                                           void *dw, int64_t M, int64_t N, int64_t K, int64_t chunk_n,
+                                           void *ws, size_t ws_bytes, bfp8_stream_t stream);
+
+/*
  * Linear forward without caller-provided scratch (no counterpart on the pages:
  * an addition for callers that cannot allocate device memory — code running
  * inside a CUDA stream capture, where cudaMalloc is not permitted, or plugins

@@ -160,6 +160,37 @@ def test_linear_workspace_and_validation():
     assert L.bfp8_linear_fwd(P16, P16, P16, M, N, K, ctypes.c_void_p(0x10000), ws - 1, NULL) == B.BFP8_ERR_INVALID_ARG
 
 
+def test_linear_step_host_workspace_and_validation():
+    """The host-buffer training step rejects bad arguments before it touches
+    a device or enqueues a copy."""
+    L = B.lib()
+    assert L.bfp8_linear_step_host_workspace_size(0, 10, 10) == 0
+    M, N, K = 256, 1152, 384
+    ws = L.bfp8_linear_step_host_workspace_size(M, N, K)
+    # device copies of x, W, dY, y, dX, dW plus the training form's quantised operands
+    assert ws >= 2 * (2 * M * K + 2 * N * K + 2 * M * N) + L.bfp8_linear_train_workspace_size(M, N, K)
+    W = ctypes.c_void_p(0x100000)  # 256-byte aligned, never dereferenced
+    f = L.bfp8_linear_step_host
+
+    def call(**kw):
+        a = dict(x=P16, w=P16, dy=P16, y=P16, dx=P16, dw=P16, M=M, N=N, K=K, chunk=0, ws=W, n=ws)
+        a.update(kw)
+        return f(a["x"], a["w"], a["dy"], a["y"], a["dx"], a["dw"], a["M"], a["N"], a["K"], a["chunk"],
+                 a["ws"], a["n"], NULL)
+
+    assert call(chunk=100) == B.BFP8_ERR_INVALID_ARG         # not a multiple of 128
+    assert "chunk_n" in L.bfp8_last_error().decode()
+    assert call(chunk=-128) == B.BFP8_ERR_INVALID_ARG
+    assert call(N=128 * 65, chunk=128,
+                n=L.bfp8_linear_step_host_workspace_size(M, 128 * 65, K)) == B.BFP8_ERR_INVALID_ARG  # > 64 chunks
+    assert call(n=ws - 1) == B.BFP8_ERR_INVALID_ARG           # workspace too small
+    assert call(ws=ctypes.c_void_p(0x100010)) == B.BFP8_ERR_INVALID_ARG  # workspace not 256-byte aligned
+    assert call(dy=NULL) == B.BFP8_ERR_INVALID_ARG
+    assert call(dw=NULL) == B.BFP8_ERR_INVALID_ARG
+    assert call(M=0) == B.BFP8_ERR_INVALID_ARG
+    assert call(K=-1) == B.BFP8_ERR_INVALID_ARG
+
+
 SHAPES = [(1, 1, 1), (2, 512, 128), (4, 3584, 640), (130, 384, 256), (129, 130, 131), (257, 65, 300),
           (300, 7, 1000), (1, 1000, 8), (128, 256, 128), (640, 5120, 1280)]
 

@@ -521,6 +521,30 @@ def test_float8_blockwise_linear_module_forward_and_backward():
     assert_gemm_close(host_bf16_as_f64(layer.weight.grad), O.linear_wgrad(dy, x), "module dW")
 
 
+@pytest.mark.parametrize("M,N,K,chunk", [(320, 1152, 384, 256),   # five chunks, the last one 128 wide
+                                         (1100, 1000, 520, 0),    # automatic chunks (512 + 488), three dX pieces
+                                         (130, 384, 256, 0)])     # one chunk, one piece
+def test_linear_step_host_matches_training_form_and_oracle(M, N, K, chunk):
+    """The whole step from pinned host buffers (copies overlapped with the
+    kernels, W and dY in column chunks, dX in row pieces) gives the training
+    form's results bit for bit, and those meet the oracle's bound."""
+    x, w, dy = _dev_linear(M, N, K, seed=62)
+    host = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+    ws = B.linear_step_host_workspace(M, N, K)
+    y, dx, dw = B.linear_step_host(host(x), host(w), host(dy), ws, chunk_n=chunk)
+    torch.cuda.current_stream().synchronize()
+    B.check_device_errors()
+    tws = B.linear_train_workspace(M, N, K)
+    ty = B.linear_fwd_train(dev_bf16(x), dev_bf16(w), tws)
+    tdx, tdw = B.linear_bwd_saved(dev_bf16(dy), tws, M, N, K)
+    torch.cuda.synchronize()
+    for name, a, b in (("y", y, ty), ("dX", dx, tdx), ("dW", dw, tdw)):
+        assert torch.equal(a.view(torch.int16), b.cpu().view(torch.int16)), f"host step {name} differs"
+    assert_gemm_close(y.float().numpy().astype(np.float64), O.linear_fwd(x, w), "host step y")
+    assert_gemm_close(dx.float().numpy().astype(np.float64), O.linear_dgrad(dy, w), "host step dX")
+    assert_gemm_close(dw.float().numpy().astype(np.float64), O.linear_wgrad(dy, x), "host step dW")
+
+
 def test_library_calls_from_a_thread_that_selected_no_device():
     """Autograd runs backward on a worker thread; a fresh host thread that never
     selected a device must still be able to launch (the library binds the
