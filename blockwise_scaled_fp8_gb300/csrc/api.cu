@@ -724,11 +724,9 @@ constexpr int kMaxStepChunks = 64;
 constexpr int kMaxDgradPieces = 4;
 
 // Columns of W / dY per pipeline chunk when the caller passes 0: about an
-// eighth of N, at least 512, a multiple of 128 (one weight tile row).
-int64_t step_chunk_n(int64_t N) {
-  const int64_t c = rup(cdiv(N, 8) > 512 ? cdiv(N, 8) : 512, kBlock);
-  return c;
-}
+// eighth of N, at least 1024 (2-D copies of narrower column chunks move
+// slower, device to host most of all), a multiple of 128 (one weight tile row).
+int64_t step_chunk_n(int64_t N) { return rup(cdiv(N, 8) > 1024 ? cdiv(N, 8) : 1024, kBlock); }
 
 // The copy streams and events of the host step on one device: created on the
 // first call, kept for the life of the process.  Calls on one device enqueue

@@ -295,7 +295,7 @@ BFP8_API bfp8_status bfp8_linear_bwd_saved(const void *dy, void *dx, void *dw, i
  * bfp8_linear_bwd_saved on the same inputs.
  *
  * The copies overlap the kernels: W and dY travel in chunks of `chunk_n`
- * output features (0 = automatic: about N/8, at least 512; otherwise a
+ * output features (0 = automatic: about N/8, at least 1024; otherwise a
  * multiple of 128, at most 64 chunks); chunk j's forward and weight-gradient
  * GEMMs run while chunk j+1 arrives, and its y and dW columns leave while
  * later chunks run; dX is computed in up to four row pieces at the end and
