@@ -459,6 +459,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
         if (SB_MODE != kSbCol)
           asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sb_cur) : "r"(slot + 512u + 4u * (uint32_t)(col0 >> 7)));
         const float scale = sa_cur * sb_cur;
+        const uint64_t scale2 = f2_pack(scale, scale);
         const uint32_t taddr = tmem_base + lane_base + (uint32_t)(buf * BN + col0);
         // LDW columns of the partial per tensor-memory load round trip (one wait)
 #pragma unroll
@@ -498,7 +499,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < LDW; ++j) acc[LDW * c + j] = fmaf(scale, __uint_as_float(r[j]), acc[LDW * c + j]);
+            for (int j = 0; j < LDW; j += 2) {  // acc += (a_s * b_s) * P, two columns per fp32x2 FMA
+              const uint64_t p2 = f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+              f2_unpack(f2_fma(scale2, p2, f2_pack(acc[LDW * c + j], acc[LDW * c + j + 1])), acc[LDW * c + j],
+                        acc[LDW * c + j + 1]);
+            }
           }
         }
         // the slot's scales are no longer needed by this warp (end of its group)
@@ -801,6 +806,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
         if (SB_MODE != kSbCol)
           asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sb_cur) : "r"(slot + 512u + 4u * (uint32_t)(col0 >> 7)));
         const float scale = sa_cur * sb_cur;
+        const uint64_t scale2 = f2_pack(scale, scale);
         const uint32_t taddr = tmem_base + lane_base + (uint32_t)(buf * BN + col0);
         // LDW columns of the partial per tensor-memory load round trip (one wait)
 #pragma unroll
@@ -840,7 +846,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
             }
           } else {
 #pragma unroll
-            for (int j = 0; j < LDW; ++j) acc[LDW * c + j] = fmaf(scale, __uint_as_float(r[j]), acc[LDW * c + j]);
+            for (int j = 0; j < LDW; j += 2) {  // acc += (a_s * b_s) * P, two columns per fp32x2 FMA
+              const uint64_t p2 = f2_pack(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+              f2_unpack(f2_fma(scale2, p2, f2_pack(acc[LDW * c + j], acc[LDW * c + j + 1])), acc[LDW * c + j],
+                        acc[LDW * c + j + 1]);
+            }
           }
         }
         // the slot's scales are no longer needed by this warp (end of its group)
