@@ -546,6 +546,53 @@ def test_linear_step_host_matches_training_form_and_oracle(M, N, K, chunk):
     assert_gemm_close(dw.float().numpy().astype(np.float64), O.linear_wgrad(dy, x), "host step dW")
 
 
+def test_linear_step_host_pageable_memory_and_concurrent_threads():
+    """The host step from pageable (not page-locked) buffers gives the same
+    bits as from pinned ones; two host threads, each with its own workspace
+    and stream, running steps at the same time share the library's copy
+    streams and events safely."""
+    import threading
+    M, N, K = 256, 1280, 384
+    x, w, dy = _dev_linear(M, N, K, seed=63)
+    pinned = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+    pageable = lambda a: torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16)
+    ws = B.linear_step_host_workspace(M, N, K)
+    ref = B.linear_step_host(pinned(x), pinned(w), pinned(dy), ws, chunk_n=512)
+    torch.cuda.synchronize()
+    out = B.linear_step_host(pageable(x), pageable(w), pageable(dy), ws, chunk_n=512,
+                             y=torch.empty(M, N, dtype=torch.bfloat16), dx=torch.empty(M, K, dtype=torch.bfloat16),
+                             dw=torch.empty(N, K, dtype=torch.bfloat16))
+    torch.cuda.synchronize()
+    for a, b in zip(ref, out):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), "pageable host step differs"
+
+    results, errs = [None, None], []
+
+    def work(i):
+        try:
+            st = torch.cuda.Stream()
+            wsi = B.linear_step_host_workspace(M, N, K)
+            hx, hw, hdy = pinned(x), pinned(w), pinned(dy)
+            with torch.cuda.stream(st):
+                for _ in range(5):
+                    r = B.linear_step_host(hx, hw, hdy, wsi, chunk_n=256)
+                st.synchronize()
+            results[i] = r
+        except Exception as e:  # reported on the main thread
+            errs.append(e)
+
+    ts = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errs, errs
+    B.check_device_errors()
+    for r in results:
+        for a, b in zip(ref, r):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16)), "concurrent host step differs"
+
+
 def test_library_calls_from_a_thread_that_selected_no_device():
     """Autograd runs backward on a worker thread; a fresh host thread that never
     selected a device must still be able to launch (the library binds the
