@@ -1038,7 +1038,7 @@ bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, i
   }
   if (kind == 3) {  // GEMM output C [M,N]; flag bit 3: the 1x128 x 128x1 GEMM
     const int bn = gemm_pick_bn(M, N, sms);
-    const int ew = gemm_epi_warps((flag & 8) != 0);
+    const int ew = gemm_epi_warps((flag & 8) != 0, bn);
     const int num_m = (int)cdiv(M, kBM), num_n = (int)cdiv(N, bn), tiles = num_m * num_n;
     const int grid = (int)gemm_grid(M, N, bn, sms);
     for (int cta = 0; cta < grid; ++cta)

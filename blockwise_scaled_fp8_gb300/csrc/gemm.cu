@@ -969,12 +969,16 @@ int64_t gemm_grid(int64_t M, int64_t N, int bn, int num_sms) {
   return tiles < num_sms ? tiles : num_sms;
 }
 
-// Promotion warps per mode (measured: the tile-scale GEMMs are faster with 8,
-// the column-scale one with 16) and columns per tensor-memory load (one round
-// trip per LDW columns of a warp's share, sized to the promotion warps' registers).
-template <int MODE>
+// Promotion warps per tile shape and mode (measured): 16 for the 256-column
+// tiles and for the column-scale mode (more warps read tensor memory faster;
+// the 2048x4096x4096 input gradient 43.0 -> 40.9 us, the 16384x14336x4096
+// forward 818 -> 794 us), 8 for the 128-column tile-scale tiles (few-tile
+// shapes: 16 measured slower there); and columns per tensor-memory load (one
+// round trip per LDW columns of a warp's share, sized to the promotion warps'
+// registers).
+template <int MODE, int BN>
 constexpr int gemm_ew() {
-  return MODE == kSbCol ? 16 : 8;  // = gemm_epi_warps(MODE == kSbCol), which the host replay uses
+  return (MODE == kSbCol || BN == 256) ? 16 : 8;  // = gemm_epi_warps(MODE == kSbCol, BN), which the host replay uses
 }
 template <int BN, int MODE, int EW>
 constexpr int gemm_ldw() {
@@ -984,7 +988,7 @@ constexpr int gemm_ldw() {
 template <int BN, int STAGES, int MODE, int GROUP = kGroupNone>
 static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int64_t grid,
                             cudaStream_t st, const GemmGroupParams* gp = nullptr) {
-  constexpr int EW = gemm_ew<MODE>(), LDW = gemm_ldw<BN, MODE, EW>();
+  constexpr int EW = gemm_ew<MODE, BN>(), LDW = gemm_ldw<BN, MODE, EW>();
   using Cfg = GemmCfg<BN, STAGES, EW>;
   constexpr int kSmem = Cfg::kSmemBytes + (GROUP != kGroupNone ? Cfg::kGroupTabBytes : 0);
   static std::once_flag once;

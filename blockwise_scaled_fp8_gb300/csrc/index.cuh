@@ -161,7 +161,7 @@ BFP8_HD int group_of_tile(const int* start, int E, int t) {
 // 16): tensor-memory lane quarter e % 4 (the quarter a warp may access is its
 // CTA warp id % 4), column block e / 4 of epi_cols(bn, ew) columns.  The
 // 1x128 x 128x128 GEMMs use 8 promotion warps, the 1x128 x 128x1 GEMM 16.
-BFP8_HD int gemm_epi_warps(bool col_scales) { return col_scales ? 16 : 8; }
+BFP8_HD int gemm_epi_warps(bool col_scales, int bn) { return (col_scales || bn == 256) ? 16 : 8; }
 BFP8_HD int epi_row(int e, int lane) { return 32 * (e % 4) + lane; }
 BFP8_HD int epi_cols(int bn, int ew) { return bn / (ew / 4); }
 BFP8_HD int epi_col0(int e, int bn, int ew) { return epi_cols(bn, ew) * (e / 4); }
