@@ -524,7 +524,9 @@ def test_float8_blockwise_linear_module_forward_and_backward():
 @pytest.mark.parametrize("M,N,K,chunk", [(320, 1152, 384, 256),   # five chunks, the last one 128 wide
                                          (1100, 1000, 520, 512),  # chunks of 512 + 488, three dX pieces
                                          (640, 2304, 256, 0),     # automatic: 1024 + 1024 + 256, two pieces
-                                         (130, 384, 256, 0)])     # one chunk, one piece
+                                         (130, 384, 256, 0),      # one chunk, one piece
+                                         (257, 200, 131, 128)])   # ragged everywhere: rows of 131 bf16
+                                                                  # (no TMA path for x), chunks 128 + 72
 def test_linear_step_host_matches_training_form_and_oracle(M, N, K, chunk):
     """The whole step from pinned host buffers (copies overlapped with the
     kernels, W and dY in column chunks, dX in row pieces) gives the training
