@@ -500,15 +500,18 @@ def run_gpu(args, wl):
         oy = torch.empty(tuple(step.y.shape), dtype=torch.bfloat16).pin_memory()
         odx = torch.empty(tuple(step.dx.shape), dtype=torch.bfloat16).pin_memory()
         odw = torch.empty(tuple(step.dw.shape), dtype=torch.bfloat16).pin_memory()
+        # the library's host-buffer steps: W and dY travel in column chunks,
+        # each chunk's GEMMs run while the next arrives, outputs leave as they
+        # are finished (mixture of experts: one such step per expert, two
+        # experts' device buffers in turn, offsets read on the host)
         if step.moe:
-            gx, gw, gdy = torch.empty_like(x), torch.empty_like(w), torch.empty_like(dy)
-            calls = step._calls(gx, gw, gdy)  # quant x+W, fwd GEMM, quant dY, dgrad GEMM, wgrad GEMM
-            hoffs = torch.from_numpy(wl.offsets()).pin_memory()
-            e2e_step = _moe_e2e_step(step, calls, hx, hw, hdy, hoffs, gx, gw, gdy, oy, odx, odw, dev)
+            hoffs = torch.from_numpy(wl.offsets())
+            hw3 = hw.view(E, N, K)
+            hws = B.moe_step_host_workspace(int(np.max(np.diff(wl.offsets()))), N, K, device=dev)
+
+            def e2e_step():
+                B.moe_step_host(hx, hw3, hdy, hoffs, hws, y=oy, dx=odx, dw=odw, chunk_n=args.chunk_n)
         else:
-            # the library's host-buffer step: W and dY travel in column chunks,
-            # each chunk's GEMMs run while the next arrives, outputs leave as
-            # they are finished
             hws = B.linear_step_host_workspace(M, N, K, device=dev)
 
             def e2e_step():
@@ -527,14 +530,13 @@ def run_gpu(args, wl):
             torch.cuda.synchronize()
             tot += s0.elapsed_time(s1)
         e2e = {"value": flops_step * args.steps / (tot / 1e3) / 1e12 * world, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(2 * (M * K + E * N * K + M * N) + (4 * (E + 1) if step.moe else 0)),
+               "h2d_bytes_per_step": int(2 * (M * K + E * N * K + M * N)),
                "d2h_bytes_per_step": int(2 * (M * N + M * K + E * N * K)),
                "ms_per_step": tot / args.steps,
-               "path": ("bfp8_linear_step_host: pinned host x, W, dY in, y, dX, dW out; copies on the "
-                        "library's two copy streams, W and dY in column chunks overlapped with the GEMMs"
-                        if not step.moe else
-                        "pinned host x, W, dY in; the step's five library calls; y, dX, dW out "
-                        "(copies on two copy streams, overlapped with the calls)")}
+               "path": ("bfp8_moe_step_host" if step.moe else "bfp8_linear_step_host") +
+                       ": pinned host x, W, dY in, y, dX, dW out; copies on the library's two copy streams, "
+                       "W and dY in column chunks overlapped with the GEMMs" +
+                       ("; one dense step per expert, offsets on the host" if step.moe else "")}
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -569,49 +571,6 @@ def run_gpu(args, wl):
     if dist:
         dist.destroy_process_group()
     return 0
-
-
-def _moe_e2e_step(step, calls, hx, hw, hdy, hoffs, gx, gw, gdy, oy, odx, odw, dev):
-    """End-to-end step of the mixture-of-experts layer: its copies on two
-    streams, overlapped with the five library calls as a caller would: dY goes
-    in while the forward runs, y comes out during the backward, dX while the
-    weight gradient runs."""
-    import torch
-    h2d, d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    ev_xw, ev_dy, ev_y, ev_dx, ev_b = (torch.cuda.Event() for _ in range(5))
-
-    def e2e_step():
-        main = torch.cuda.current_stream()
-        h2d.wait_stream(main)
-        with torch.cuda.stream(h2d):
-            gx.copy_(hx, non_blocking=True)
-            gw.copy_(hw, non_blocking=True)
-            step.offs.copy_(hoffs, non_blocking=True)
-            ev_xw.record(h2d)
-            gdy.copy_(hdy, non_blocking=True)
-            ev_dy.record(h2d)
-        main.wait_event(ev_xw)
-        calls[0]()
-        calls[1]()
-        ev_y.record(main)
-        d2h.wait_event(ev_y)
-        with torch.cuda.stream(d2h):
-            oy.copy_(step.y, non_blocking=True)
-        main.wait_event(ev_dy)
-        calls[2]()
-        calls[3]()
-        ev_dx.record(main)
-        d2h.wait_event(ev_dx)
-        with torch.cuda.stream(d2h):
-            odx.copy_(step.dx, non_blocking=True)
-        calls[4]()
-        ev_b.record(main)
-        d2h.wait_event(ev_b)
-        with torch.cuda.stream(d2h):
-            odw.copy_(step.dw, non_blocking=True)
-        main.wait_stream(d2h)
-
-    return e2e_step
 
 
 def main():

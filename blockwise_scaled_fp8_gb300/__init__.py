@@ -26,7 +26,7 @@ EXPORTS = [
     "bfp8_linear_train_workspace_size", "bfp8_linear_fwd_train", "bfp8_linear_bwd_saved",
     "bfp8_linear_fwd_static", "bfp8_gemm_grouped_1x128_128x128", "bfp8_gemm_grouped_1x128_128x1",
     "bfp8_quant_dual_weight", "bfp8_mx_cast", "bfp8_linear_step_host_workspace_size",
-    "bfp8_linear_step_host",
+    "bfp8_linear_step_host", "bfp8_moe_step_host_workspace_size", "bfp8_moe_step_host",
 ]
 
 _lib = None
@@ -77,6 +77,9 @@ def lib() -> ctypes.CDLL:
     L.bfp8_linear_step_host_workspace_size.argtypes = [i64, i64, i64]
     L.bfp8_linear_step_host_workspace_size.restype = sz
     L.bfp8_linear_step_host.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, vp, sz, vp]
+    L.bfp8_moe_step_host_workspace_size.argtypes = [i64, i64, i64]
+    L.bfp8_moe_step_host_workspace_size.restype = sz
+    L.bfp8_moe_step_host.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, i64, i64, i64, i64, vp, sz, vp]
     L.bfp8_linear_fwd_static.argtypes = [vp, vp, vp, i64, i64, i64, vp]
     L.bfp8_gemm_grouped_1x128_128x128.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, vp, i64, vp, i64,
                                                   i64, i64, i64, vp]
@@ -85,7 +88,7 @@ def lib() -> ctypes.CDLL:
     L.bfp8_debug_gemm_stall.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, i64, i64, vp]
     for name in EXPORTS:
         if name not in ("bfp8_last_error", "bfp8_linear_workspace_size", "bfp8_linear_train_workspace_size",
-                        "bfp8_linear_step_host_workspace_size"):
+                        "bfp8_linear_step_host_workspace_size", "bfp8_moe_step_host_workspace_size"):
             getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -503,6 +506,42 @@ def linear_step_host(x, w, dy, ws, y=None, dx=None, dw=None, chunk_n: int = 0):
     wp, wn = _aligned(ws)
     _check(lib().bfp8_linear_step_host(_p(x), _p(w), _p(dy), _p(y), _p(dx), _p(dw), M, N, K, int(chunk_n),
                                        wp, wn, _stream()))
+    return y, dx, dw
+
+
+def moe_step_host_workspace(M_max: int, N: int, K: int, device="cuda"):
+    """Device workspace for moe_step_host (M_max: the largest expert's tokens)."""
+    torch = _torch()
+    return torch.empty(int(lib().bfp8_moe_step_host_workspace_size(M_max, N, K)) + 256, dtype=torch.uint8,
+                       device=device)
+
+
+def moe_step_host(x, w, dy, offs, ws, y=None, dx=None, dw=None, chunk_n: int = 0):
+    """Mixture-of-experts training step from host tensors (see
+    bfp8_moe_step_host): x [T,K], w [E,N,K], dy [T,N] contiguous bf16 CPU
+    tensors (pinned for overlap), offs int32 [E+1] on the CPU.  Returns host
+    (y, dx, dw); enqueued on the current CUDA stream."""
+    torch = _torch()
+    for name, t in (("x", x), ("w", w), ("dy", dy)):
+        if t.device.type != "cpu" or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError(f"moe_step_host: {name} must be a contiguous bf16 CPU tensor")
+    if offs.device.type != "cpu" or offs.dtype != torch.int32 or not offs.is_contiguous():
+        raise ValueError("moe_step_host: offs must be a contiguous int32 CPU tensor")
+    T, K = x.shape
+    E, N = w.shape[0], w.shape[1]
+    if tuple(w.shape) != (E, N, K) or tuple(dy.shape) != (T, N) or offs.numel() != E + 1:
+        raise ValueError(f"moe_step_host: shapes x {tuple(x.shape)}, w {tuple(w.shape)}, dy {tuple(dy.shape)}, "
+                         f"offs {tuple(offs.shape)}")
+    pin = torch.cuda.is_available()
+    y = torch.empty((T, N), dtype=torch.bfloat16, pin_memory=pin) if y is None else y
+    dx = torch.empty((T, K), dtype=torch.bfloat16, pin_memory=pin) if dx is None else dx
+    dw = torch.empty((E, N, K), dtype=torch.bfloat16, pin_memory=pin) if dw is None else dw
+    for name, t, shp in (("y", y, (T, N)), ("dx", dx, (T, K)), ("dw", dw, (E, N, K))):
+        if t.device.type != "cpu" or t.dtype != torch.bfloat16 or not t.is_contiguous() or tuple(t.shape) != shp:
+            raise ValueError(f"moe_step_host: {name} must be a contiguous bf16 CPU tensor of shape {shp}")
+    wp, wn = _aligned(ws)
+    _check(lib().bfp8_moe_step_host(_p(x), _p(w), _p(dy), _p(offs), E, _p(y), _p(dx), _p(dw), T, N, K,
+                                    int(chunk_n), wp, wn, _stream()))
     return y, dx, dw
 
 

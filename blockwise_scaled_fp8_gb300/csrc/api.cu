@@ -739,6 +739,7 @@ struct HostStepCtx {
   cudaEvent_t start, x_in, in_end, out_end;
   cudaEvent_t chunk_in[kMaxStepChunks], y_done[kMaxStepChunks], dw_done[kMaxStepChunks];
   cudaEvent_t dx_done[kMaxDgradPieces];
+  cudaEvent_t slot_free[2];  // per-expert steps: a device slot's last copy out
 };
 HostStepCtx g_step[64];
 
@@ -754,6 +755,8 @@ cudaError_t host_step_init(HostStepCtx& C) {
     evs.push_back(&C.dw_done[i]);
   }
   for (int i = 0; i < kMaxDgradPieces; ++i) evs.push_back(&C.dx_done[i]);
+  evs.push_back(&C.slot_free[0]);
+  evs.push_back(&C.slot_free[1]);
   for (cudaEvent_t* ev : evs)
     if ((e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming)) != cudaSuccess) return e;
   C.ready = true;
@@ -761,38 +764,16 @@ cudaError_t host_step_init(HostStepCtx& C) {
 }
 }  // namespace
 
-size_t bfp8_linear_step_host_workspace_size(int64_t M, int64_t N, int64_t K) {
-  if (M <= 0 || N <= 0 || K <= 0) return 0;
-  return host_step_layout(M, N, K).total;
-}
-
-bfp8_status bfp8_linear_step_host(const void* x, const void* w, const void* dy, void* y, void* dx, void* dw,
-                                  int64_t M, int64_t N, int64_t K, int64_t chunk_n, void* ws, size_t ws_bytes,
-                                  bfp8_stream_t stream) {
-  const char* fn = "bfp8_linear_step_host";
-  bfp8_status st = check_dims(fn, M, N, K);
-  if (st != BFP8_OK) return st;
-  CHECK_ARG(M > 0 && N > 0 && K > 0, "%s: dimensions must be positive", fn);
-  CHECK_ARG(x && w && dy && y && dx && dw && ws, "%s: null pointer", fn);
-  CHECK_ARG((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "%s: workspace must be 256-byte aligned", fn);
-  CHECK_ARG(chunk_n >= 0 && chunk_n % kBlock == 0, "%s: chunk_n=%lld must be 0 (automatic) or a multiple of 128", fn,
-            (long long)chunk_n);
+namespace {
+// Enqueues one step (copies on C.in / C.out, kernels on s) into the device
+// buffers at `base` (host_step_layout(M, N, K)).  The caller records the start
+// and joins the streams afterwards, whatever this returns.
+bfp8_status host_step_enqueue(HostStepCtx& C, cudaStream_t s, bfp8_stream_t stream, const void* x, const void* w,
+                              const void* dy, void* y, void* dx, void* dw, int64_t M, int64_t N, int64_t K,
+                              int64_t Nc, uint8_t* base) {
+  bfp8_status st = BFP8_OK;
   const HostStepLayout H = host_step_layout(M, N, K);
-  CHECK_ARG(ws_bytes >= H.total, "%s: workspace too small (%zu < %zu)", fn, ws_bytes, H.total);
-  const int64_t Nc = chunk_n ? chunk_n : step_chunk_n(N);
   const int64_t nc = cdiv(N, Nc);
-  CHECK_ARG(nc <= kMaxStepChunks, "%s: %lld chunks of %lld columns exceed %d; pass a larger chunk_n", fn,
-            (long long)nc, (long long)Nc, kMaxStepChunks);
-  int sms = 0, dev = 0;
-  if ((st = check_device(&sms)) != BFP8_OK) return st;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  HostStepCtx& C = g_step[dev];
-  std::lock_guard<std::mutex> lk(C.mu);
-  if ((e = host_step_init(C)) != cudaSuccess) return cuda_fail(e, "bfp8_linear_step_host: stream/event creation");
-
-  const cudaStream_t s = (cudaStream_t)stream;
-  uint8_t* base = (uint8_t*)ws;
   uint16_t *d_x = (uint16_t*)(base + H.x), *d_w = (uint16_t*)(base + H.w), *d_dy = (uint16_t*)(base + H.dy);
   uint16_t *d_y = (uint16_t*)(base + H.y), *d_dx = (uint16_t*)(base + H.dx), *d_dw = (uint16_t*)(base + H.dw);
   const TrainLayout L = train_layout(M, N, K);
@@ -819,8 +800,7 @@ bfp8_status bfp8_linear_step_host(const void* x, const void* w, const void* dy, 
     return st == BFP8_OK;
   };
 
-  bool go = cu(cudaEventRecord(C.start, s), "event record") && cu(cudaStreamWaitEvent(C.in, C.start, 0), "wait") &&
-            cu(cudaStreamWaitEvent(C.out, C.start, 0), "wait");
+  bool go = true;
   // inputs, in the order the kernels need them: x, then W and dY chunk by chunk
   go = go && cu(cudaMemcpyAsync(d_x, h_x, (size_t)M * row_x, cudaMemcpyDefault, C.in), "copy x in") &&
        cu(cudaEventRecord(C.x_in, C.in), "event record");
@@ -880,14 +860,145 @@ bfp8_status bfp8_linear_step_host(const void* x, const void* w, const void* dy, 
                             cudaMemcpyDefault, C.out),
             "copy dX out");
   }
-  // join: the caller's stream continues after every copy of this step
+  if (st != BFP8_OK) return st;
+  if (ce != cudaSuccess) return cuda_fail(ce, what);
+  return BFP8_OK;
+}
+
+// Records the step's start on the caller's stream for both copy streams.
+cudaError_t host_step_start(HostStepCtx& C, cudaStream_t s) {
+  cudaError_t e = cudaEventRecord(C.start, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(C.in, C.start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(C.out, C.start, 0);
+  return e;
+}
+
+// The caller's stream continues after every copy of the step.
+cudaError_t host_step_join(HostStepCtx& C, cudaStream_t s) {
   cudaEventRecord(C.in_end, C.in);
   cudaEventRecord(C.out_end, C.out);
   cudaStreamWaitEvent(s, C.in_end, 0);
-  const cudaError_t je = cudaStreamWaitEvent(s, C.out_end, 0);
+  return cudaStreamWaitEvent(s, C.out_end, 0);
+}
+}  // namespace
+
+size_t bfp8_linear_step_host_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0) return 0;
+  return host_step_layout(M, N, K).total;
+}
+
+bfp8_status bfp8_linear_step_host(const void* x, const void* w, const void* dy, void* y, void* dx, void* dw,
+                                  int64_t M, int64_t N, int64_t K, int64_t chunk_n, void* ws, size_t ws_bytes,
+                                  bfp8_stream_t stream) {
+  const char* fn = "bfp8_linear_step_host";
+  bfp8_status st = check_dims(fn, M, N, K);
   if (st != BFP8_OK) return st;
-  if (ce != cudaSuccess) return cuda_fail(ce, what);
+  CHECK_ARG(M > 0 && N > 0 && K > 0, "%s: dimensions must be positive", fn);
+  CHECK_ARG(x && w && dy && y && dx && dw && ws, "%s: null pointer", fn);
+  CHECK_ARG((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "%s: workspace must be 256-byte aligned", fn);
+  CHECK_ARG(chunk_n >= 0 && chunk_n % kBlock == 0, "%s: chunk_n=%lld must be 0 (automatic) or a multiple of 128", fn,
+            (long long)chunk_n);
+  const HostStepLayout H = host_step_layout(M, N, K);
+  CHECK_ARG(ws_bytes >= H.total, "%s: workspace too small (%zu < %zu)", fn, ws_bytes, H.total);
+  const int64_t Nc = chunk_n ? chunk_n : step_chunk_n(N);
+  const int64_t nc = cdiv(N, Nc);
+  CHECK_ARG(nc <= kMaxStepChunks, "%s: %lld chunks of %lld columns exceed %d; pass a larger chunk_n", fn,
+            (long long)nc, (long long)Nc, kMaxStepChunks);
+  int sms = 0, dev = 0;
+  if ((st = check_device(&sms)) != BFP8_OK) return st;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  HostStepCtx& C = g_step[dev];
+  std::lock_guard<std::mutex> lk(C.mu);
+  if ((e = host_step_init(C)) != cudaSuccess) return cuda_fail(e, "bfp8_linear_step_host: stream/event creation");
+
+  const cudaStream_t s = (cudaStream_t)stream;
+  if ((e = host_step_start(C, s)) != cudaSuccess) return cuda_fail(e, "bfp8_linear_step_host: start");
+  st = host_step_enqueue(C, s, stream, x, w, dy, y, dx, dw, M, N, K, Nc, (uint8_t*)ws);
+  const cudaError_t je = host_step_join(C, s);
+  if (st != BFP8_OK) return st;
   return je == cudaSuccess ? BFP8_OK : cuda_fail(je, "bfp8_linear_step_host: join");
+}
+
+size_t bfp8_moe_step_host_workspace_size(int64_t M_max, int64_t N, int64_t K) {
+  if (N <= 0 || K <= 0 || M_max < 0) return 0;
+  return 2 * a256(host_step_layout(M_max > 0 ? M_max : 1, N, K).total);
+}
+
+bfp8_status bfp8_moe_step_host(const void* x, const void* w, const void* dy, const int32_t* offs, int64_t E,
+                               void* y, void* dx, void* dw, int64_t T, int64_t N, int64_t K, int64_t chunk_n,
+                               void* ws, size_t ws_bytes, bfp8_stream_t stream) {
+  const char* fn = "bfp8_moe_step_host";
+  bfp8_status st = check_dims(fn, T, N, K);
+  if (st != BFP8_OK) return st;
+  CHECK_ARG(N > 0 && K > 0, "%s: N and K must be positive", fn);
+  CHECK_ARG(E >= 1 && E <= 4096, "%s: E=%lld experts out of [1, 4096]", fn, (long long)E);
+  CHECK_ARG(offs, "%s: null offsets", fn);
+  CHECK_ARG(offs[0] >= 0 && offs[E] <= T, "%s: offsets must lie in [0, T=%lld]", fn, (long long)T);
+  int64_t M_max = 0;
+  for (int64_t e = 0; e < E; ++e) {
+    CHECK_ARG(offs[e + 1] >= offs[e], "%s: offsets decrease at expert %lld", fn, (long long)e);
+    if (offs[e + 1] - offs[e] > M_max) M_max = offs[e + 1] - offs[e];
+  }
+  CHECK_ARG(w && dw && ws, "%s: null pointer", fn);
+  CHECK_ARG(M_max == 0 || (x && dy && y && dx), "%s: null pointer", fn);
+  CHECK_ARG((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "%s: workspace must be 256-byte aligned", fn);
+  CHECK_ARG(chunk_n >= 0 && chunk_n % kBlock == 0, "%s: chunk_n=%lld must be 0 (automatic) or a multiple of 128", fn,
+            (long long)chunk_n);
+  const size_t slot = a256(host_step_layout(M_max > 0 ? M_max : 1, N, K).total);
+  CHECK_ARG(ws_bytes >= 2 * slot, "%s: workspace too small (%zu < %zu)", fn, ws_bytes, 2 * slot);
+  const int64_t Nc = chunk_n ? chunk_n : step_chunk_n(N);
+  CHECK_ARG(cdiv(N, Nc) <= kMaxStepChunks, "%s: %lld chunks of %lld columns exceed %d; pass a larger chunk_n", fn,
+            (long long)cdiv(N, Nc), (long long)Nc, kMaxStepChunks);
+  int sms = 0, dev = 0;
+  if ((st = check_device(&sms)) != BFP8_OK) return st;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  HostStepCtx& C = g_step[dev];
+  std::lock_guard<std::mutex> lk(C.mu);
+  if ((e = host_step_init(C)) != cudaSuccess) return cuda_fail(e, "bfp8_moe_step_host: stream/event creation");
+
+  const cudaStream_t s = (cudaStream_t)stream;
+  if ((e = host_step_start(C, s)) != cudaSuccess) return cuda_fail(e, "bfp8_moe_step_host: start");
+  uint8_t* base = (uint8_t*)ws;
+  const size_t wbytes = (size_t)N * K * 2;
+  // Each expert with tokens is one dense step on its rows, in two device
+  // slots used in turn: expert k's inputs enter slot k % 2 once expert k-2's
+  // outputs have left it, so copies of one expert overlap kernels of another.
+  int64_t k = 0;
+  for (int64_t ex = 0; st == BFP8_OK && ex < E; ++ex) {
+    const int64_t m0 = offs[ex], Me = offs[ex + 1] - offs[ex];
+    if (Me == 0) continue;
+    const int sl = (int)(k & 1);
+    if (k >= 2 && (e = cudaStreamWaitEvent(C.in, C.slot_free[sl], 0)) != cudaSuccess) {
+      st = cuda_fail(e, "bfp8_moe_step_host: wait");
+      break;
+    }
+    st = host_step_enqueue(C, s, stream, (const char*)x + m0 * K * 2, (const char*)w + ex * wbytes,
+                           (const char*)dy + m0 * N * 2, (char*)y + m0 * N * 2, (char*)dx + m0 * K * 2,
+                           (char*)dw + ex * wbytes, Me, N, K, Nc, base + sl * slot);
+    if (st == BFP8_OK && (e = cudaEventRecord(C.slot_free[sl], C.out)) != cudaSuccess)
+      st = cuda_fail(e, "bfp8_moe_step_host: event record");
+    ++k;
+  }
+  // experts without tokens: dW = 0, copied out of a zeroed device region
+  // (slot 0's weight-gradient buffer, after every earlier copy out of it)
+  bool zeroed = false;
+  for (int64_t ex = 0; st == BFP8_OK && ex < E; ++ex) {
+    if (offs[ex + 1] != offs[ex]) continue;
+    const HostStepLayout H = host_step_layout(M_max > 0 ? M_max : 1, N, K);
+    uint8_t* zero = base + H.dw;
+    if (!zeroed && (e = cudaMemsetAsync(zero, 0, wbytes, C.out)) != cudaSuccess) {
+      st = cuda_fail(e, "bfp8_moe_step_host: memset");
+      break;
+    }
+    zeroed = true;
+    if ((e = cudaMemcpyAsync((char*)dw + ex * wbytes, zero, wbytes, cudaMemcpyDefault, C.out)) != cudaSuccess)
+      st = cuda_fail(e, "bfp8_moe_step_host: copy dW out");
+  }
+  const cudaError_t je = host_step_join(C, s);
+  if (st != BFP8_OK) return st;
+  return je == cudaSuccess ? BFP8_OK : cuda_fail(je, "bfp8_moe_step_host: join");
 }
 
 // ---------------------------------------------------------------------------

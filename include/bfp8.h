@@ -323,6 +323,28 @@ BFP8_API bfp8_status bfp8_linear_step_host(const void *x, const void *w, const v
                                            void *ws, size_t ws_bytes, bfp8_stream_t stream);
 
 /*
+ * The mixture-of-experts layer's training step from HOST memory: tokens
+ * sorted by expert, expert e owning token rows offs[e] .. offs[e+1] of x
+ * [T,K], dy [T,N], y [T,N], dx [T,K] and the weight w[e] = w + e*N*K
+ * ([N,K]), gradient dw[e] = dw + e*N*K.  Each expert with tokens runs as one
+ * bfp8_linear_step_host step on its rows (the same per-expert quantisations
+ * and GEMMs as the grouped path when the experts start on 128-token
+ * boundaries; any boundaries work here), two experts' device buffers in turn
+ * so that one expert's copies overlap another's kernels.  Experts without
+ * tokens get dw[e] = 0; rows outside [offs[0], offs[E]) of y and dx are not
+ * written.
+ *   offs: HOST int32 [E+1], non-decreasing, within [0, T] (checked here);
+ *   1 <= E <= 4096.  Other buffers, chunk_n, stream and errors as
+ *   bfp8_linear_step_host.  ws: device, >= bfp8_moe_step_host_workspace_size(
+ *   M_max, N, K) bytes (M_max = the largest expert's token count), 256-byte
+ *   aligned.
+ */
+BFP8_API size_t bfp8_moe_step_host_workspace_size(int64_t M_max, int64_t N, int64_t K);
+BFP8_API bfp8_status bfp8_moe_step_host(const void *x, const void *w, const void *dy, const int32_t *offs,
+                                        int64_t E, void *y, void *dx, void *dw, int64_t T, int64_t N, int64_t K,
+                                        int64_t chunk_n, void *ws, size_t ws_bytes, bfp8_stream_t stream);
+
+/*
  * Linear forward without caller-provided scratch (no counterpart on the pages:
  * an addition for callers that cannot allocate device memory — code running
  * inside a CUDA stream capture, where cudaMalloc is not permitted, or plugins

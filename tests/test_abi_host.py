@@ -160,6 +160,30 @@ def test_linear_workspace_and_validation():
     assert L.bfp8_linear_fwd(P16, P16, P16, M, N, K, ctypes.c_void_p(0x10000), ws - 1, NULL) == B.BFP8_ERR_INVALID_ARG
 
 
+def test_moe_step_host_validation():
+    """The mixture-of-experts host step checks its host offsets and workspace
+    before it touches a device."""
+    L = B.lib()
+    N, K, T = 256, 384, 640
+    ws = L.bfp8_moe_step_host_workspace_size(384, N, K)
+    assert ws == 2 * L.bfp8_linear_step_host_workspace_size(384, N, K)
+    W = ctypes.c_void_p(0x100000)
+    f = L.bfp8_moe_step_host
+
+    def call(offs, E=None, T_=T, n=ws, chunk=0):
+        o = (ctypes.c_int32 * len(offs))(*offs)
+        E = len(offs) - 1 if E is None else E
+        return f(P16, P16, P16, o, E, P16, P16, P16, T_, N, K, chunk, W, n, NULL)
+
+    assert call([0, 384, 384, 640], n=ws - 1) == B.BFP8_ERR_INVALID_ARG         # workspace too small
+    assert call([0, 400, 300, 640]) == B.BFP8_ERR_INVALID_ARG                   # decreasing offsets
+    assert "decrease" in L.bfp8_last_error().decode()
+    assert call([0, 384, 700]) == B.BFP8_ERR_INVALID_ARG                        # past T
+    assert call([-1, 384, 640]) == B.BFP8_ERR_INVALID_ARG                       # negative
+    assert call([0, 384, 640], chunk=100) == B.BFP8_ERR_INVALID_ARG             # chunk not a multiple of 128
+    assert call([0, 640], E=0) == B.BFP8_ERR_INVALID_ARG                        # no expert
+
+
 def test_linear_step_host_workspace_and_validation():
     """The host-buffer training step rejects bad arguments before it touches
     a device or enqueues a copy."""

@@ -228,3 +228,44 @@ def test_moe_linear_matches_oracle(E, T, N, K):
             assert np.all(got_dw[e] == 0.0)
         else:
             assert_gemm_close(got_dw[e], ref_dw[e], f"moe dW expert {e}")
+
+
+@pytest.mark.parametrize("E,offs,T,N,K", [(4, [0, 256, 256, 640, 700], 700, 256, 384),  # an empty expert, ragged end
+                                          (3, [5, 133, 133, 400], 410, 300, 200)])     # unaligned experts
+def test_moe_step_host_matches_oracle(E, offs, T, N, K):
+    """The mixture-of-experts step from host buffers, one dense step per
+    expert with copies overlapped: against the oracle's per-expert forward,
+    input gradient and weight gradient (zeros for an expert without tokens),
+    and bit for bit against the grouped device path when the experts start on
+    128-token boundaries."""
+    offs = np.asarray(offs, np.int32)
+    x = S.normal_bf16((T, K), 1.0, seed=71)
+    w = S.normal_bf16((E * N, K), 0.02, seed=72).reshape(E, N, K)
+    dy = S.normal_bf16((T, N), 1e-3, seed=73)
+    host = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).pin_memory()
+    m_max = int(np.max(np.diff(offs)))
+    ws = B.moe_step_host_workspace(m_max, N, K)
+    y, dx, dw = B.moe_step_host(host(x), host(w), host(dy), torch.from_numpy(offs), ws, chunk_n=128)
+    torch.cuda.current_stream().synchronize()
+    B.check_device_errors()
+    inside = np.zeros(T, bool)
+    inside[offs[0]:offs[-1]] = True
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+    assert_gemm_close(f64(y)[inside], O.moe_linear_fwd(x, w, offs)[inside], "moe host y")
+    assert_gemm_close(f64(dx)[inside], O.moe_linear_dgrad(dy, w, offs)[inside], "moe host dx")
+    ref_dw = O.moe_linear_wgrad(dy, x, offs)
+    got_dw = f64(dw)
+    for e in range(E):
+        if offs[e + 1] == offs[e]:
+            assert np.all(got_dw[e] == 0.0)
+        else:
+            assert_gemm_close(got_dw[e], ref_dw[e], f"moe host dW expert {e}")
+    if np.all(offs[:-1] % 128 == 0):
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).cuda().view(torch.bfloat16)
+        offs_d = _cu(offs)
+        gy, saved = B.moe_linear_fwd(dev(x), dev(w), offs_d)
+        gdx, gdw = B.moe_linear_bwd(dev(dy), saved, offs_d)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16)[inside], gy.cpu().view(torch.int16)[inside])
+        assert torch.equal(dx.view(torch.int16)[inside], gdx.cpu().view(torch.int16)[inside])
+        assert torch.equal(dw.view(torch.int16), gdw.cpu().view(torch.int16))
