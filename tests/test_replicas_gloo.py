@@ -31,7 +31,7 @@ def _rank_main(rank, world, port, out):
 
 def test_replicas_take_the_slowest_rank_and_count_all_work():
     world, port = 2, _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:  # no fork of a multi-threaded process
         out = m.dict()
         mp.spawn(_rank_main, args=(world, port, out), nprocs=world, join=True)
         res = dict(out)
