@@ -582,7 +582,7 @@ def main():
     ap.add_argument("--workload", default="mid", choices=sorted(WORKLOADS))
     ap.add_argument("--ref-rows", type=int, default=4, help="oracle sample rows per reference step")
     ap.add_argument("--ref-blocks", type=int, default=1, help="oracle sample 128-col blocks per reference step")
-    ap.add_argument("--cpu-rows", type=int, default=2048, help="oracle sample rows of the cpu_baseline leg (about 8 s on 16 cores at the default workload)")
+    ap.add_argument("--cpu-rows", type=int, default=2048, help="oracle sample rows of the cpu_baseline leg (about 5 s on 16 Grace cores at the default workload)")
     ap.add_argument("--cpu-blocks", type=int, default=32, help="oracle sample 128-col blocks, cpu_baseline leg")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--chunk-n", type=int, default=0,
