@@ -313,6 +313,8 @@ BFP8_API bfp8_status bfp8_linear_bwd_saved(const void *dy, void *dx, void *dw, i
  *   step; the outputs are complete once it has.
  *   ws: device, >= bfp8_linear_step_host_workspace_size(M,N,K) bytes,
  *   256-byte aligned; holds the device copies and the quantised operands.
+ *   Several host threads may call at once, each with its own workspace:
+ *   their enqueues take turns on the device's copy streams.
  * Errors: BFP8_ERR_INVALID_ARG for bad sizes, pointers, chunk_n or workspace
  * (nothing enqueued); launch or copy failures return their status after the
  * caller's stream has been joined to the copy streams.
