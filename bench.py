@@ -8,12 +8,14 @@ forward GEMM
 (of dY^T); input-gradient GEMM 1x128 x 128x128 and weight-gradient GEMM
 1x128 x 128x1.
 
-Default workload: the pages' mid shape M=2048, N=4096, K=4096 (x ~N(0,1) with
-0.1% x100 outliers, W ~N(0,0.02), dY ~N(0,1e-3)), L2 flushed between steps.
+Default workload: the MLP-up layer M=16384 tokens, N=14336, K=4096 (x ~N(0,1),
+W ~N(0,0.02), dY ~N(0,1e-3)), the largest single-GPU problem; the pages' mid
+shape 2048x4096x4096 is `--workload mid`.  L2 flushed between steps.
 
 value = GEMM FLOPs of the step (3 * 2MNK) / device time of the whole step
 (quantisation included), TFLOP/s.  Per-kernel times come from CUDA events on
 the launching stream.  `--impl reference` times the CPU oracle instead.
+`--only NAME` times one library call of the step by itself (for profilers).
 """
 from __future__ import annotations
 
@@ -36,6 +38,7 @@ import synthetic as S  # noqa: E402
 
 WORKLOADS = {
     "mid": S.FWD_MID,          # 2048 x 4096 x 4096
+    "wgrad": S.WGRAD,          # 8192 tokens, 4096 x 4096 (dW = dY^T X over 8192 tokens)
     "square": S.FWD_SQUARE,    # 8192 x 8192 x 8192
     "mlp_up": S.MLP_UP,        # 16384 x 14336 x 4096
     "moe_up": S.MOE_UP,        # 16384 tokens over 8 experts of 14336 x 4096
@@ -85,82 +88,145 @@ def _profile_traffic(kernel_key: str, workload: str):
 
 
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons while running."""
+    """Samples the GPU's SM clock, its maximum, the power draw and the active
+    clock-event (throttle) reasons every `period_s` on a background thread,
+    through NVML (read-only queries, loaded with ctypes), falling back to an
+    `nvidia-smi -lms` subprocess when NVML cannot be loaded.  summary()
+    reports the samples taken inside the marked region; a region shorter than
+    the period has none, and then the last sample before it and the first
+    after it are reported instead, labelled as bracketing it."""
 
-    def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.path = os.path.join("/tmp", f"bfp8_clocks_{os.getpid()}.csv")
+    # NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, index: int, uuid: str | None = None, period_s: float = 0.01):
+        self.index, self.uuid, self.period_s = index, uuid, period_s
+        self.samples = []  # (perf_counter, sm_mhz, max_mhz, power_w, reasons)
+        self.t0 = self.t1 = None
+        self.source = None
+        self._stop = False
+        self._thread = None
+        self._proc = None
+
+    def _nvml(self):
+        import ctypes
+        lib = None
+        for name in ("libnvidia-ml.so.1", "libnvidia-ml.so"):
+            try:
+                lib = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        if lib is None or lib.nvmlInit_v2() != 0:
+            return None
+        h = ctypes.c_void_p()
+        ok = False
+        if self.uuid:
+            ok = lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) == 0
+        if not ok:
+            ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) == 0
+        if not ok:
+            return None
+        mx = ctypes.c_uint(0)
+        lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # NVML_CLOCK_SM = 1
+
+        def read():
+            clk, pw, rs = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) != 0:
+                return None
+            lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+            lib.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs))
+            return (float(clk.value), float(mx.value), pw.value / 1000.0,
+                    sorted(n for bit, n in self.REASONS.items() if rs.value & bit))
+        return read
+
+    def _run(self, read):
+        while not self._stop:
+            s = read()
+            if s is not None:
+                self.samples.append((time.perf_counter(),) + s)
+            time.sleep(self.period_s)
+
+    def _run_smi(self):
+        q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits", "-i", str(self.index),
+                 "-lms", str(max(20, int(self.period_s * 1000)))],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        for line in self._proc.stdout:
+            p = [v.strip() for v in line.split(",")]
+            try:
+                self.samples.append((time.perf_counter(), float(p[0]), float(p[1]), float(p[2]),
+                                     sorted(n for n, v in zip(names, p[3:7]) if v.lower() == "active")))
+            except (ValueError, IndexError):
+                continue
 
     def __enter__(self):
-        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        import threading
+        read = None
         try:
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
-                                          "-i", str(self.index), "-lms", "200"], stdout=self.f,
-                                         stderr=subprocess.DEVNULL)
-        except (OSError, FileNotFoundError):
-            self.proc = None
+            read = self._nvml()
+        except (OSError, AttributeError):
+            read = None
+        if read is not None:
+            self.source = f"nvml every {self.period_s * 1000:.0f} ms"
+            self._thread = threading.Thread(target=self._run, args=(read,), daemon=True)
+        else:
+            self.source = "nvidia-smi"
+            self._thread = threading.Thread(target=self._run_smi, daemon=True)
+        self._thread.start()
         return self
-
-    def _lines(self):
-        try:
-            with open(self.path) as f:
-                return sum(1 for _ in f)
-        except OSError:
-            return 0
 
     def wait_first_sample(self, timeout_s=3.0):
         t0 = time.time()
-        while self.proc is not None and self._lines() == 0 and time.time() - t0 < timeout_s:
-            time.sleep(0.05)
+        while not self.samples and time.time() - t0 < timeout_s:
+            time.sleep(0.01)
 
     def mark_start(self):
-        self.n0 = self._lines()
+        self.t0 = time.perf_counter()
 
     def mark_end(self):
-        self.n1 = self._lines()
+        self.t1 = time.perf_counter()
+        # let one more sample land after the region, for the bracketing fallback
+        n = len(self.samples)
+        t = time.time()
+        while len(self.samples) == n and time.time() - t < 1.0:
+            time.sleep(0.005)
 
     def __exit__(self, *a):
-        if self.proc is not None:
-            self.proc.terminate()
+        self._stop = True
+        if self._proc is not None:
+            self._proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
-            self.f.close()
+                self._proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
 
     def summary(self):
-        if self.proc is None or not os.path.exists(self.path):
+        if not self.samples or self.t0 is None or self.t1 is None:
             return None
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            lines = f.readlines()
-        n0, n1 = getattr(self, "n0", 0), getattr(self, "n1", len(lines))
-        # samples taken during the timed region (plus the one in flight at its end)
-        for line in lines[n0:min(len(lines), n1 + 1)]:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        try:
-            os.remove(self.path)
-        except OSError:
-            pass
-        if not sm:
+        inside = [s for s in self.samples if self.t0 <= s[0] <= self.t1]
+        window = "timed region"
+        if not inside:
+            before = [s for s in self.samples if s[0] < self.t0][-1:]
+            after = [s for s in self.samples if s[0] > self.t1][:1]
+            inside = before + after
+            window = "bracketing the timed region (no sample fell inside it)"
+        if not inside:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        reasons = sorted({r for s in inside for r in s[4]})
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+                "power_w_max": max(s[3] for s in inside), "samples": len(inside), "reasons": reasons,
+                "window": window, "region_ms": round((self.t1 - self.t0) * 1e3, 2), "source": self.source}
 
 
 # ---------------------------------------------------------------------------
@@ -227,30 +293,39 @@ def _oracle_problem(wl, x, w, dy):
             f"expert {e} of {wl.E} (tokens {r0}..{r1}): ")
 
 
+def cpu_unit_samples(args, wl, x, w, dy, reps, seed0):
+    """`reps` bounded samples of the step on the oracle, each the same shape
+    (--cpu-rows rows, --cpu-blocks 128-column blocks, all three GEMMs with
+    their quantisations) at a different seeded position.  The cpu_baseline
+    leg and the reference arm both time these units, so the two report the
+    same oracle on the same sample shape.  Returns (flops, seconds, text)."""
+    owl, ox, ow, ody, prefix = _oracle_problem(wl, x, w, dy)
+    flops, dt, text = 0.0, 0.0, ""
+    for i in range(reps):
+        r, nr, nb, kb = _sample(owl, args.cpu_rows, args.cpu_blocks, seed0 + i)
+        t0 = time.perf_counter()
+        flops += oracle_step_sample(ox, ow, ody, r, nr, nb, kb)
+        dt += time.perf_counter() - t0
+        text = prefix + _sample_text(owl, r, nr, nb, kb)
+    return flops, dt, text
+
+
 def run_reference(args, wl):
     import oracle as O
     O.build()
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    full = wl
-    wl, x, w, dy, prefix = _oracle_problem(wl, wl.x(), wl.w(), wl.dy())
-    r, nr, nb, kb = _sample(wl, args.ref_rows, args.ref_blocks, 0)
-    rot = [("fwd",), ("dgrad",), ("wgrad",)]  # one part of the step per iteration, in rotation
-    for i in range(args.warmup):
-        oracle_step_sample(x, w, dy, r, nr, nb, kb, rot[i % 3])
-    t0 = time.perf_counter()
-    flops = 0.0
-    for i in range(args.steps):
-        flops += oracle_step_sample(x, w, dy, r, nr, nb, kb, rot[i % 3])
-    dt = time.perf_counter() - t0
+    x, w, dy = wl.x(), wl.w(), wl.dy()
+    cpu_unit_samples(args, wl, x, w, dy, args.warmup, 1000)
+    flops, dt, text = cpu_unit_samples(args, wl, x, w, dy, args.steps, 0)
     value = flops / dt / 1e12
     cores = O._threads()
-    sample = "per step, one of (in rotation): " + prefix + _sample_text(wl, r, nr, nb, kb)
+    sample = "per step, one unit: " + text
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": full.name, "M": full.M, "N": full.N, "K": full.K},
+            "data": "synthetic", "config": {"workload": wl.name, "M": wl.M, "N": wl.N, "K": wl.K},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -390,6 +465,59 @@ def aggregate_replicas(local_ms: float, units_per_rank: float, dist=None, device
     return ms, world * units_per_rank / (ms / 1e3)
 
 
+# the buffers each library call of the step reads or writes (Step attributes)
+ONLY_BUFFERS = {
+    "quant_x_w": ("qx", "sx", "qxt", "sxt", "qw", "qwt", "sw"),
+    "gemm_fwd": ("qx", "sx", "qw", "sw", "y"),
+    "quant_dual_dy": ("qdy", "sdy", "qdyt", "sdyt"),
+    "gemm_dgrad": ("qdy", "sdy", "qwt", "sw", "dx"),
+    "gemm_wgrad": ("qdyt", "sdyt", "qxt", "sxt", "dw"),
+}
+ONLY_INPUTS = {"quant_x_w": ("x", "w"), "quant_dual_dy": ("dy",)}
+
+
+def run_only(args, wl, torch, B, dev, todev, flush):
+    """One library call of the step, by itself: every call of the step runs
+    once (so the call's inputs exist), every buffer the named call does not
+    touch is freed (a profiler that replays the call saves and restores less
+    device memory), then the named call runs --warmup times untimed and
+    --steps times between CUDA events, L2 flushed before each.  Launch order,
+    for a profiler's skip count: the step's five calls (quant_x_w, gemm_fwd,
+    quant_dual_dy, gemm_dgrad, gemm_wgrad), then the repeats of the named one."""
+    step = Step(wl, torch, B, dev)
+    inp = {"x": todev(wl.x()), "w": todev(wl.w()), "dy": todev(wl.dy())}
+    for c in step._calls(inp["x"], inp["w"], inp["dy"]):
+        c()
+    torch.cuda.synchronize()
+    for name in ("qx", "sx", "qxt", "sxt", "qw", "qwt", "sw", "qdy", "sdy", "qdyt", "sdyt", "y", "dx", "dw"):
+        if name not in ONLY_BUFFERS[args.only]:
+            setattr(step, name, None)
+    for name in ("x", "w", "dy"):
+        if name not in ONLY_INPUTS.get(args.only, ()):
+            inp[name] = None
+    torch.cuda.empty_cache()
+    call = step._calls(inp["x"], inp["w"], inp["dy"])[step.names.index(args.only)]
+    for _ in range(args.warmup):
+        flush.fill_(0.0)
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in ev:
+        flush.fill_(0.0)
+        a.record()
+        call()
+        b.record()
+    torch.cuda.synchronize()
+    B.check_device_errors()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    unit, work = algorithmic_units(wl)[args.only]
+    scale = 1e12 if unit == "TFLOP/s" else 1e9
+    print(json.dumps({"only": args.only, "workload": wl.name, "ms": ms, unit: work / (ms / 1e3) / scale,
+                      "steps": args.steps, "warmup": args.warmup,
+                      "device_bytes_held": int(torch.cuda.memory_allocated(dev))}), flush=True)
+    return 0
+
+
 def run_gpu(args, wl):
     import torch
 
@@ -408,11 +536,13 @@ def run_gpu(args, wl):
     def todev(a):
         return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
 
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    if args.only:
+        return run_only(args, wl, torch, B, dev, todev, flush)
     xh, wh, dyh = wl.x(), wl.w(), wl.dy()
     x, w, dy = todev(xh), todev(wh), todev(dyh)
     step = Step(wl, torch, B, dev)
     step.capture(x, w, dy)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
 
     # Timed region: K steps, each the whole step as one graph replay between
     # two events, the L2 flushed before every step (outside the events).  Then
@@ -421,7 +551,9 @@ def run_gpu(args, wl):
     step_events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                    for _ in range(args.steps)]
     events = [step.new_events() for _ in range(args.steps)]
-    with ClockSampler(local) as clk:
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    with ClockSampler(local, uuid=f"GPU-{uuid}" if uuid is not None else None) as clk:
         for _ in range(args.warmup):
             step.run_step()
             flush.fill_(1.0)
@@ -542,13 +674,10 @@ def run_gpu(args, wl):
     if rank == 0 and not args.no_cpu_baseline:
         import oracle as O
         O.build()
-        owl, ox, ow, ody, prefix = _oracle_problem(wl, xh, wh, dyh)
-        r, nr, nb, kb = _sample(owl, args.cpu_rows, args.cpu_blocks, 1)
-        t0 = time.perf_counter()
-        fl = oracle_step_sample(ox, ow, ody, r, nr, nb, kb)
-        dt = time.perf_counter() - t0
+        fl, dt, text = cpu_unit_samples(args, wl, xh, wh, dyh, args.cpu_reps, 0)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": O._threads(), "kind": "oracle",
-               "sample": prefix + _sample_text(owl, r, nr, nb, kb) + f"; {dt:.1f} s"}
+               "sample": f"{args.cpu_reps} units (the reference arm's per-step unit), each: " + text +
+                         f"; {dt:.1f} s in all"}
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -576,14 +705,17 @@ def run_gpu(args, wl):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="mid", choices=sorted(WORKLOADS))
-    ap.add_argument("--ref-rows", type=int, default=4, help="oracle sample rows per reference step")
-    ap.add_argument("--ref-blocks", type=int, default=1, help="oracle sample 128-col blocks per reference step")
-    ap.add_argument("--cpu-rows", type=int, default=2048, help="oracle sample rows of the cpu_baseline leg (about 5 s on 16 Grace cores at the default workload)")
-    ap.add_argument("--cpu-blocks", type=int, default=32, help="oracle sample 128-col blocks, cpu_baseline leg")
+    ap.add_argument("--workload", default="mlp_up", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-rows", type=int, default=512,
+                    help="rows of one oracle sample unit (the reference arm's step; cpu_baseline repeats it)")
+    ap.add_argument("--cpu-blocks", type=int, default=8, help="128-column blocks of one oracle sample unit")
+    ap.add_argument("--cpu-reps", type=int, default=6, help="oracle sample units timed by the cpu_baseline leg")
+    ap.add_argument("--only", default=None,
+                    help="time one library call of the step by itself (quant_x_w, gemm_fwd, quant_dual_dy, "
+                         "gemm_dgrad, gemm_wgrad), for profilers")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--chunk-n", type=int, default=0,
                     help="columns of W / dY per chunk of the host-buffer step (0 = automatic)")

@@ -549,13 +549,26 @@ bfp8_status bfp8_linear_fwd(const void* x, const void* w, void* y, int64_t M, in
   }
   CHECK_ARG(x && w && y && ws, "bfp8_linear_fwd: null pointer");
   CHECK_ARG((reinterpret_cast<uintptr_t>(ws) & 255u) == 0, "bfp8_linear_fwd: workspace must be 256-byte aligned");
-  const FwdLayout L = fwd_layout(M, N, K);
   CHECK_ARG(ws_bytes >= bfp8_linear_workspace_size(M, N, K), "bfp8_linear_fwd: workspace too small (%zu < %zu)",
             ws_bytes, bfp8_linear_workspace_size(M, N, K));
-  uint8_t* base = (uint8_t*)ws;
-  const int64_t Kb = cdiv(K, kBlock);
   int sms = 0;
   if ((st = check_device(&sms)) != BFP8_OK) return st;
+  return bfp8::linear_fwd_into(x, w, y, M, N, K, (uint8_t*)ws, sms, stream);
+}
+
+}  // extern "C"
+
+size_t bfp8::linear_fwd_scratch_bytes(int64_t M, int64_t N, int64_t K) { return fwd_layout(M, N, K).total; }
+
+bfp8_status bfp8::check_current_device(int* sms) { return check_device(sms); }
+
+// The forward's quantisations and GEMM into scratch at base (laid out by
+// fwd_layout, 256-byte aligned), after the caller validated the arguments.
+bfp8_status bfp8::linear_fwd_into(const void* x, const void* w, void* y, int64_t M, int64_t N, int64_t K,
+                                  uint8_t* base, int sms, bfp8_stream_t stream) {
+  bfp8_status st;
+  const FwdLayout L = fwd_layout(M, N, K);
+  const int64_t Kb = cdiv(K, kBlock);
   if (quant_tile_supported(x, K, base + L.qx, L.ldK, nullptr, 0) && quant_tile_supported(w, K, base + L.qw, L.ldK,
                                                                                           nullptr, 0)) {
     // x's 1x128 groups and W's tiles in one launch
@@ -576,6 +589,8 @@ bfp8_status bfp8_linear_fwd(const void* x, const void* w, void* y, int64_t M, in
   return bfp8_gemm_1x128_128x128(base + L.qx, L.ldK, (const float*)(base + L.sx), L.ldsM, base + L.qw, L.ldK,
                                  (const float*)(base + L.sw), Kb, 0, y, N, M, N, K, stream);
 }
+
+extern "C" {
 
 bfp8_status bfp8_linear_bwd(const void* dy, const void* x, const void* w, void* dx, void* dw, int64_t M, int64_t N,
                             int64_t K, void* ws, size_t ws_bytes, bfp8_stream_t stream) {

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/bfp8.h"
+
 namespace bfp8 {
 
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s per wait: far above any legitimate stall
@@ -98,5 +100,15 @@ struct GemmGroupArgs {
 cudaError_t launch_gemm_grouped(const GemmGroupArgs& a, int num_sms, cudaStream_t st, const char** msg);
 // Reads and clears the device error word of the GEMM kernels (synchronous).
 cudaError_t gemm_read_errors(uint32_t* out);
+
+// The linear forward (api.cu), shared with the entry that keeps its scratch
+// in a library-owned array (noalloc.cu): the bytes its scratch needs, the
+// sm_103a check of the current device (SM count via *sms), and the forward's
+// launches into scratch at `base` (256-byte aligned, linear_fwd_scratch_bytes
+// long) once the arguments are validated.
+size_t linear_fwd_scratch_bytes(int64_t M, int64_t N, int64_t K);
+bfp8_status check_current_device(int* sms);
+bfp8_status linear_fwd_into(const void* x, const void* w, void* y, int64_t M, int64_t N, int64_t K, uint8_t* base,
+                            int sms, bfp8_stream_t stream);
 
 }  // namespace bfp8

@@ -348,17 +348,24 @@ BFP8_API bfp8_status bfp8_moe_step_host(const void *x, const void *w, const void
 
 /*
  * Linear forward without caller-provided scratch (no counterpart on the pages:
- * an addition for callers that cannot allocate device memory — code running
- * inside a CUDA stream capture, where cudaMalloc is not permitted, or plugins
- * whose host owns all allocations and exposes no allocator).  Same inputs and
- * output as bfp8_linear_fwd; the quantised x and W and their scales live in
- * one 32 MiB array that the library reserves on every GPU that loads it, for
- * the life of the process.  Problems needing more than 32 MiB of quantised
- * operands (about M*K + N*K bytes plus scales) return BFP8_ERR_INVALID_ARG.
- * All calls share that array: calls whose work overlaps on the GPU race, so
- * order them (one stream, or events).  Nothing in it needs clearing between
- * calls.  The first call on each device looks the array up with that device
- * current; make it before any stream capture.  Allocates nothing.
+ * an addition for callers that cannot allocate device memory — plugins hosted
+ * by a framework that owns every allocation and hands them no allocator, and
+ * latency-critical code that must not enter the driver's allocator, where a
+ * cudaMalloc can synchronise the device).  Same inputs, output and launches as
+ * bfp8_linear_fwd, so the same result bits; the quantised x and W and their
+ * scales live in one 32 MiB array that the library reserves on every GPU that
+ * loads it, for the life of the process.  Problems needing more than 32 MiB
+ * of quantised operands (about M*K + N*K bytes plus scales) return
+ * BFP8_ERR_INVALID_ARG.  All calls share that array: calls whose work
+ * overlaps on the GPU race, so order them (one stream, or events).  Nothing
+ * in it needs clearing between calls.  The first call in each CUDA context
+ * (normally once per device) looks the array's address up with that device
+ * current and keeps it for that context; make that call before any stream
+ * capture.  A new context on the same device (after cudaDeviceReset, or a
+ * driver-API context the caller made current) is looked up again on its
+ * first call.  Allocates nothing.  Errors: BFP8_ERR_INVALID_ARG (sizes,
+ * null pointers), BFP8_ERR_UNSUPPORTED (not sm_103), BFP8_ERR_CUDA (the
+ * lookup or a launch failed).
  */
 BFP8_API bfp8_status bfp8_linear_fwd_static(const void *x, const void *w, void *y, int64_t M, int64_t N,
                                             int64_t K, bfp8_stream_t stream);

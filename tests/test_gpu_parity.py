@@ -776,10 +776,65 @@ def _check_linear_sampled(x, w, dy, y, dx, dw, what, seed):
 
 
 def test_bench_step_full_size_sampled():
-    """The benchmark's default workload (2048 x 4096 x 4096) in the launch
-    configuration it times: sampled y, dX and dW against the oracle."""
+    """The pages' mid shape (2048 x 4096 x 4096) in the launch configuration
+    the benchmark times: sampled y, dX and dW against the oracle."""
     step, x, w, dy = _bench_step(S.FWD_MID)
     _check_linear_sampled(x, w, dy, step.y, step.dx, step.dw, "bench step", seed=30)
+
+
+def _u8_rows(t, rows, ncols):
+    return t[torch.from_numpy(np.asarray(rows)).cuda()][:, :ncols].cpu().numpy()
+
+
+def _f32_cols(t, cols):
+    return f32_bits(t[:, torch.from_numpy(np.asarray(cols)).cuda()].cpu().numpy())
+
+
+def test_bench_mlp_up_step_quant_bytes_bit_exact_and_gemms_sampled():
+    """The benchmark's default workload, the MLP-up layer 16384 x 14336 x 4096,
+    in the launch configuration it times (one graph of the five calls).  Every
+    quantised operand the step makes is compared byte for byte with the
+    oracle -- e4m3 codes and fp32 scale bits -- on sampled rows, columns and
+    128-row weight blocks that include the last tile of each tensor:
+      dY [16384, 14336]: 1x128 groups along N (q_row, s_row) and 1x128 groups
+        along M of dY^T (q_col [14336, 16384], s_col);
+      x [16384, 4096]: 1x128 groups along K and 128x1 groups along M (x^T);
+      W [14336, 4096]: 128x128 tiles as is (q), transposed (qt) and scales.
+    Then y, dX and dW on sampled outputs within the GEMM tolerance."""
+    wl = S.MLP_UP
+    M, N, K = wl.M, wl.N, wl.K
+    step, x, w, dy = _bench_step(wl)
+    mb, nb, kb = cdiv(M, 128), cdiv(N, 128), cdiv(K, 128)
+
+    # dY, 1x128 along N: whole rows, scales column-major [M, Nb]
+    rows = _sample_idx(M, 24, 50)
+    q, s = O.quant_lhs(np.ascontiguousarray(dy[rows]))
+    assert np.array_equal(_u8_rows(step.qdy, rows, N), q), "q(dY) rows"
+    assert np.array_equal(_f32_cols(step.sdy[:nb], rows), f32_bits(s)), "s(dY) rows"
+    # dY^T, 1x128 along M: whole columns of dY (rows of q_col), last column included
+    ncols = _sample_idx(N, 24, 51)
+    q, s = O.quant_lhs(np.ascontiguousarray(dy[:, ncols]), transposed=True)
+    assert np.array_equal(_u8_rows(step.qdyt, ncols, M), q), "q(dY^T) rows"
+    assert np.array_equal(_f32_cols(step.sdyt[:mb], ncols), f32_bits(s)), "s(dY^T)"
+    # x, 1x128 along K
+    q, s = O.quant_lhs(np.ascontiguousarray(x[rows]))
+    assert np.array_equal(_u8_rows(step.qx, rows, K), q), "q(x) rows"
+    assert np.array_equal(_f32_cols(step.sx[:kb], rows), f32_bits(s)), "s(x) rows"
+    # x, 128x1 along M, written transposed [K, M]
+    kcols = _sample_idx(K, 24, 52)
+    q, s = O.quant_rhs(np.ascontiguousarray(x[:, kcols]))
+    assert np.array_equal(_u8_rows(step.qxt, kcols, M), q), "q(x^T) rows"
+    assert np.array_equal(_f32_cols(step.sxt[:mb], kcols), f32_bits(s)), "s(x^T)"
+    # W: 128-row blocks (the last one included), tiles as is and transposed
+    for blk in _sample_idx(nb, 3, 53):
+        r = np.arange(blk * 128, min(N, blk * 128 + 128))
+        q, qt, s = O.quant_weight(np.ascontiguousarray(w[r]), with_t=True)
+        assert np.array_equal(_u8_rows(step.qw, r, K), q), f"q(W) block {blk}"
+        got_t = step.qwt[:, int(r[0]):int(r[-1]) + 1].cpu().numpy()
+        assert np.array_equal(got_t, qt), f"qt(W) block {blk}"
+        assert np.array_equal(f32_bits(step.sw[int(blk)].cpu().numpy()), f32_bits(s[0])), f"s(W) block {blk}"
+    # the GEMM outputs, sampled
+    _check_linear_sampled(x, w, dy, step.y, step.dx, step.dw, "mlp_up bench step", seed=60)
 
 
 def test_bench_moe_step_full_size_sampled():
