@@ -27,6 +27,7 @@ EXPORTS = [
     "bfp8_linear_fwd_static", "bfp8_gemm_grouped_1x128_128x128", "bfp8_gemm_grouped_1x128_128x1",
     "bfp8_quant_dual_weight", "bfp8_mx_cast", "bfp8_linear_step_host_workspace_size",
     "bfp8_linear_step_host", "bfp8_moe_step_host_workspace_size", "bfp8_moe_step_host",
+    "bfp8_gemm_1x128_128x128_xq",
 ]
 
 _lib = None
@@ -81,6 +82,7 @@ def lib() -> ctypes.CDLL:
     L.bfp8_moe_step_host_workspace_size.restype = sz
     L.bfp8_moe_step_host.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, i64, i64, i64, i64, vp, sz, vp]
     L.bfp8_linear_fwd_static.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+    L.bfp8_gemm_1x128_128x128_xq.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, i64, vp]
     L.bfp8_gemm_grouped_1x128_128x128.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, vp, i64, vp, i64,
                                                   i64, i64, i64, vp]
     L.bfp8_gemm_grouped_1x128_128x1.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64,
@@ -292,6 +294,21 @@ def gemm_1x128_128x1(qa, sa, qb, sb, K: int, out=None, M=None, N=None):
         out = torch.empty((M, N), dtype=torch.bfloat16, device=qa.device)
     _check(lib().bfp8_gemm_1x128_128x1(_p(qa), qa.stride(0), _p(sa), sa.stride(0), _p(qb), qb.stride(0),
                                        _p(sb), sb.stride(0), _p(out), out.stride(0), M, N, K, _stream()))
+    return out
+
+
+def gemm_1x128_128x128_xq(x, qb, sb, out=None, N=None):
+    """C = quant_lhs(x) B with x bf16 [M, K] quantised inside the GEMM (one
+    launch), B^T = qb [N, ldb] with its 128x128 tile scales sb [Nb, ldsb]
+    (bfp8_quant_weight's outputs).  Returns C [M, N] bf16."""
+    torch = _torch()
+    _need_bf16_2d(x, "x")
+    M, K = x.shape
+    N = qb.shape[0] if N is None else N
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(lib().bfp8_gemm_1x128_128x128_xq(_p(x), x.stride(0), _p(qb), qb.stride(0), _p(sb), sb.stride(0),
+                                            _p(out), out.stride(0), M, N, K, _stream()))
     return out
 
 

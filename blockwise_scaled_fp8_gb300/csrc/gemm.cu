@@ -924,6 +924,444 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
   }
 }
 
+
+// ---------------------------------------------------------------------------
+// The forward GEMM (1x128 x 128x128) with its A operand quantised inside the
+// kernel: A is the bf16 activation x, read through TMA, and a quantiser
+// warpgroup forms each row's 1x128 group maximum, scale and e4m3 codes for
+// the K-block into the MMA's shared-memory stage, with the same arithmetic as
+// the quantisation kernels (so the bytes, scales and output equal those of
+// quantising x first).  B is a weight already quantised in 128x128 tiles.
+// For small M the separate quantisation launch of x and its HBM round trip go
+// away ("Enable blockwise FP8 dense training kernels on ROCm", perf table:
+// FP8 behind BF16 at M = 128 and 512).
+//
+//   warp 0      producer: raw bf16 x tiles (two 64-column boxes) into a
+//               two-slot ring, B tiles into the stage ring
+//   warps 1, 3  MMA issuers: as the dense kernel, also waiting for the
+//               stage's quantised A
+//   warp 2      b_s of each K-block into the scale ring
+//   warps 4-7   quantisers, two halves taking alternate K-blocks (two
+//               K-blocks quantised at once): thread (row, 16-column chunk);
+//               a row's 8 chunks are 8 lanes of one warp, which combine their
+//               maxima by shuffles; the chunk-0 lane writes a_s into a ring
+//   warps 8-15  promotion + epilogue, as the dense kernel (8 warps)
+// ---------------------------------------------------------------------------
+template <int BN, int STAGES, int RAW_ROWS>
+struct XqCfg {
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kCols = BN / (kEpiWarps / 4);
+  static constexpr int kThreads = 128 + 128 + 32 * kEpiWarps;  // 512
+  // registers: 128 per thread at launch; control 56, quantisers 72, promotion 192
+  static constexpr int kCtrlRegs = 56, kQuantRegs = 72, kEpiRegs = 192;
+  static_assert(128 * kCtrlRegs + 128 * kQuantRegs + 32 * kEpiWarps * kEpiRegs <= kThreads * 128, "register split");
+  static constexpr int kABytes = kBM * kBK;                 // e4m3 A stage: 128 rows x 128 B
+  // With RAW_ROWS == 16 (M <= 16) only the first 16 rows of an A stage are
+  // written, so the stages sit 2 KB apart and the MMA's reads of rows 16..127
+  // fall on neighbouring stages: in-bounds shared memory whose rows only feed
+  // output rows >= M, which are never stored.  That leaves room for more
+  // stages of B, the operand streamed from DRAM.
+  static constexpr int kAStride = RAW_ROWS == 16 ? 16 * kBK : kABytes;
+  static constexpr int kBBytes = BN * kBK;
+  // bf16 x tile of RAW_ROWS rows: two 64-column boxes.  128 rows in two slots,
+  // or (M <= 16) 16 rows in eight, so that small problems keep eight x tiles
+  // in flight against the DRAM latency
+  static constexpr int kRawBytes = RAW_ROWS * kBK * 2;
+  static constexpr int kRawSlots = RAW_ROWS == 16 ? 8 : 2;
+  static constexpr int kOffB = ((STAGES - 1) * kAStride + kABytes + 1023) / 1024 * 1024;
+  static constexpr int kOffRaw = kOffB + STAGES * kBBytes;
+  static constexpr int kOffScale = kOffRaw + kRawSlots * kRawBytes;
+  static constexpr int kScaleSlots = 2, kScaleGroup = 4;
+  static constexpr int kScaleKbBytes = 128 * 4 + BN * 4;
+  static constexpr int kScaleBytes = kScaleGroup * kScaleKbBytes;
+  // a_s of each K-block, written by the quantisers into a ring of kAsSlots
+  // entries: they run at most STAGES units ahead of the MMAs, which run at
+  // most two ahead of the promotion (two tensor-memory buffers), and a
+  // promotion warp reads its a_s before releasing the buffer, so an entry is
+  // never rewritten before it has been read
+  static constexpr int kAsSlots = 16;
+  static_assert(kAsSlots >= STAGES + 2, "a_s ring depth");
+  static constexpr int kOffAs = kOffScale + kScaleSlots * kScaleBytes;
+  static constexpr int kOffBar = kOffAs + kAsSlots * kBM * 4;
+  // full[S] empty[S] afull[S] rfull[R] rempty[R] tfull[2] tempty[2] drain stall sfull[2] sempty[2]
+  static constexpr int kNumBars = 3 * STAGES + 2 * kRawSlots + 4 + 2 + 2 * kScaleSlots;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  static constexpr int kTmemCols = 2 * BN;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+template <int BN, int STAGES, int LDW, int RAW_ROWS>
+__global__ void __launch_bounds__(XqCfg<BN, STAGES, RAW_ROWS>::kThreads, 1)
+    gemm_xq_kernel(const __grid_constant__ CUtensorMap tma_x, const __grid_constant__ CUtensorMap tma_b,
+                   const GemmParams p) {
+  using Cfg = XqCfg<BN, STAGES, RAW_ROWS>;
+  constexpr int NR = Cfg::kRawSlots;
+  constexpr int EW = Cfg::kEpiWarps;
+  constexpr int kCols = Cfg::kCols;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sA = sbase, sB = sbase + Cfg::kOffB, sRaw = sbase + Cfg::kOffRaw;
+  const uint32_t sScale = sbase + Cfg::kOffScale;
+  const uint32_t bar0 = sbase + Cfg::kOffBar;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
+  volatile int* never = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
+
+  auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(STAGES + i); };
+  auto afull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + i); };
+  auto rfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * STAGES + i); };
+  auto rempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * STAGES + NR + i); };
+  auto tfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + i); };
+  auto tempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + 2 + i); };
+  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + 4);
+  const uint32_t stall_bar = bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + 5);  // never arrived on
+  auto sfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + 6 + i); };
+  auto sempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + 8 + i); };
+
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+  const int lane = (int)(threadIdx.x & 31);
+  pdl_launch_dependents();
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), 1);
+      mbar_init(afull_bar(i), 64);  // every thread of the quantiser half that takes the stage
+    }
+    for (int i = 0; i < Cfg::kRawSlots; ++i) {
+      mbar_init(rfull_bar(i), 1);
+      mbar_init(rempty_bar(i), 64);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(tfull_bar(i), 1);
+      mbar_init(tempty_bar(i), EW);
+    }
+    mbar_init(drain_bar, 2);
+    mbar_init(stall_bar, 1);
+    for (int i = 0; i < Cfg::kScaleSlots; ++i) {
+      mbar_init(sfull_bar(i), 32);  // one cp.async arrival per b_s loader lane
+      mbar_init(sempty_bar(i), EW);
+    }
+    *abort_flag = 0;
+    *never = 0;
+    fence_barrier_init();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma_x);
+    tma_prefetch_desc(&tma_b);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();  // the previous kernel's writes are visible from here on
+  const uint32_t tmem_base = *tmem_holder;
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kCtrlRegs));
+    if (warp == 0) {
+      // ---------------------------------------------------------- producer
+      if (lane == 0) {
+        uint32_t it = 0, n_raw = 0, n_b = 0;  // units; raw x and B copies issued
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+          const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+          for (int kb = 0; kb < p.Kb; ++kb, ++it) {
+            const int r = (int)(it % Cfg::kRawSlots);
+            if (!mbar_wait_bounded(rempty_bar(r), ((it / Cfg::kRawSlots) & 1u) ^ 1u, p.wait_limit_ns, abort_flag)) {
+              gemm_fail(kErrWaitEmpty, abort_flag);
+              ok = false;
+              break;
+            }
+            const uint32_t raw = sRaw + (uint32_t)(r * Cfg::kRawBytes);
+            mbar_arrive_expect_tx(rfull_bar(r), (uint32_t)Cfg::kRawBytes);
+            tma_load_2d(raw, &tma_x, rfull_bar(r), kb * kBK, g.m0);
+            tma_load_2d(raw + (uint32_t)(Cfg::kRawBytes / 2), &tma_x, rfull_bar(r), kb * kBK + 64, g.m0);
+            ++n_raw;
+            const int st = (int)(it % STAGES);
+            if (!mbar_wait_bounded(empty_bar(st), ((it / STAGES) & 1u) ^ 1u, p.wait_limit_ns, abort_flag)) {
+              gemm_fail(kErrWaitEmpty, abort_flag);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(full_bar(st), (uint32_t)Cfg::kBBytes);
+            tma_load_2d(sB + (uint32_t)(st * Cfg::kBBytes), &tma_b, full_bar(st), kb * kBK, g.n0);
+            ++n_b;
+          }
+        }
+        if (!ok) {
+          // copies already issued land before this CTA's shared memory goes away
+          for (uint32_t j = (n_raw > Cfg::kRawSlots ? n_raw - Cfg::kRawSlots : 0); j < n_raw; ++j)
+            if (!mbar_wait_bounded(rfull_bar((int)(j % Cfg::kRawSlots)), (j / Cfg::kRawSlots) & 1u, p.wait_limit_ns,
+                                   never))
+              atomicOr(&g_gemm_error, kErrWaitDrain);
+          for (uint32_t j = (n_b > STAGES ? n_b - STAGES : 0); j < n_b; ++j)
+            if (!mbar_wait_bounded(full_bar((int)(j % STAGES)), (j / STAGES) & 1u, p.wait_limit_ns, never))
+              atomicOr(&g_gemm_error, kErrWaitDrain);
+        }
+      }
+    } else if (warp == 1 || warp == 3) {
+      // ---------------------------------------------------------- MMA issuers
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
+        const uint32_t mine = warp == 1 ? 0u : 1u;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+          for (int kb = 0; kb < p.Kb; ++kb, ++it) {
+            if ((it & 1u) != mine) continue;
+            const int st = (int)(it % STAGES);
+            const uint32_t ph = (it / STAGES) & 1u;
+            const int buf = (int)(it & 1u);
+            const uint32_t tph = (it >> 1) & 1u;
+            if (!mbar_spin_bounded(tempty_bar(buf), tph ^ 1u, p.wait_limit_ns, abort_flag)) {
+              gemm_fail(kErrWaitTmemEmpty, abort_flag);
+              ok = false;
+              break;
+            }
+            if (!mbar_spin_bounded(full_bar(st), ph, p.wait_limit_ns, abort_flag) ||
+                !mbar_spin_bounded(afull_bar(st), ph, p.wait_limit_ns, abort_flag)) {
+              gemm_fail(kErrWaitFull, abort_flag);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t da = desc_kmajor_sw128(sA + (uint32_t)(st * Cfg::kAStride));
+            const uint64_t db = desc_kmajor_sw128(sB + (uint32_t)(st * Cfg::kBBytes));
+            const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+#pragma unroll
+            for (int k = 0; k < kBK / 32; ++k)
+              mma_e4m3(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), idesc, k > 0 ? 1u : 0u);
+            mma_commit(empty_bar(st));
+            mma_commit(tfull_bar(buf));
+          }
+        }
+        mma_commit(drain_bar);
+        if (!mbar_wait_bounded(drain_bar, 0, p.wait_limit_ns, never)) gemm_fail(kErrWaitDrain, abort_flag);
+      }
+    } else {
+      // ---------------------------------------------------------- b_s loader (warp 2)
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+        const bool last_tile = tile + (int)gridDim.x >= p.num_tiles;
+        for (int kb = 0; kb < p.Kb; ++kb, ++it) {
+          const uint32_t grp = it / Cfg::kScaleGroup, sub = it % Cfg::kScaleGroup;
+          const int sl = (int)(grp % Cfg::kScaleSlots);
+          if (sub == 0) {
+            const bool got =
+                mbar_wait_bounded(sempty_bar(sl), ((grp / Cfg::kScaleSlots) & 1u) ^ 1u, p.wait_limit_ns, abort_flag);
+            if (!__all_sync(0xffffffffu, got)) {
+              if (lane == 0) gemm_fail(kErrWaitScale, abort_flag);
+              ok = false;
+              break;
+            }
+          }
+          const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes + sub * Cfg::kScaleKbBytes);
+          if (lane < BN / 128) {  // tile scale of the 128 columns n0 + 128*lane (zero past N)
+            const int nb = g.n0 / kBlock + lane;
+            const bool in = nb < p.Nb;
+            cp_async_4(slot + 512u + 4u * lane, in ? p.sb + (int64_t)nb * p.ldsb + kb : p.sb, in ? 4u : 0u);
+          }
+          if (sub == Cfg::kScaleGroup - 1 || (last_tile && kb == p.Kb - 1)) cp_async_mbar_arrive(sfull_bar(sl));
+        }
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    }
+  } else if (warp < 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kQuantRegs));
+    // ------------------------------------------------------------ quantisers
+    const int qt = (int)threadIdx.x - 128;
+    const uint32_t half = (uint32_t)(qt >> 6);  // takes the K-block steps it with it % 2 == half
+    const int hq = qt & 63;
+    const int chunk = hq & 7;          // 16 columns of the K-block
+    const int row0 = hq >> 3;          // rows row0 + 8 i
+    const uint32_t gmask = 0xFFu << (8 * (lane >> 3));  // the 8 lanes of this thread's row
+    const uint32_t sAs = sbase + Cfg::kOffAs;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+      const int rows_valid = (int)min((int64_t)RAW_ROWS, p.M - g.m0);
+      for (int kb = 0; kb < p.Kb; ++kb, ++it) {
+        if ((it & 1u) != half) continue;
+        const int r = (int)(it % Cfg::kRawSlots);
+        const int st = (int)(it % STAGES);
+        const bool got = mbar_wait_bounded(rfull_bar(r), (it / Cfg::kRawSlots) & 1u, p.wait_limit_ns, abort_flag) &&
+                         mbar_wait_bounded(empty_bar(st), ((it / STAGES) & 1u) ^ 1u, p.wait_limit_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) gemm_fail(kErrWaitFull, abort_flag);
+          ok = false;
+          break;
+        }
+        const uint32_t raw = sRaw + (uint32_t)(r * Cfg::kRawBytes);
+        const uint32_t adst = sA + (uint32_t)(st * Cfg::kAStride);
+        const uint32_t as_slot = sAs + (uint32_t)((it % Cfg::kAsSlots) * kBM * 4);
+#pragma unroll 1
+        for (int i = 0; i < RAW_ROWS / 8; ++i) {
+          const int row = row0 + 8 * i;
+          if (row >= rows_valid) continue;  // the 8 lanes of a row agree
+          // 16 bf16 values: 16-byte chunks 2*(chunk%4) and +1 of box chunk/4 (128-byte swizzle)
+          const uint32_t rbase = raw + (uint32_t)((chunk >> 2) * (Cfg::kRawBytes / 2) + row * 128);
+          const int c0 = 2 * (chunk & 3);
+          uint4 v0, v1;
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(v0.x), "=r"(v0.y), "=r"(v0.z), "=r"(v0.w)
+                       : "r"(rbase + (uint32_t)(((c0) ^ (row & 7)) << 4)));
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(v1.x), "=r"(v1.y), "=r"(v1.z), "=r"(v1.w)
+                       : "r"(rbase + (uint32_t)(((c0 + 1) ^ (row & 7)) << 4)));
+          uint32_t m = amax2(amax2(amax2(v0.x, v0.y), amax2(v0.z, v0.w)), amax2(amax2(v1.x, v1.y), amax2(v1.z, v1.w)));
+          m = amax2(m, __shfl_xor_sync(gmask, m, 1));
+          m = amax2(m, __shfl_xor_sync(gmask, m, 2));
+          m = amax2(m, __shfl_xor_sync(gmask, m, 4));
+          m = amax2(m, __byte_perm(m, 0, 0x1032));
+          const float sc = scale_of(__uint_as_float(m & 0x7FFF0000u));
+          const float ny = neg_rcp(sc);
+          const uint64_t s2 = f2_pack(sc, sc), ny2 = f2_pack(ny, ny);
+          const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+          uint32_t q[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            q[k] = __byte_perm(neg_codes2(w[2 * k], s2, ny2), neg_codes2(w[2 * k + 1], s2, ny2), 0x5410) ^ 0x80808080u;
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(adst + (uint32_t)(row * 128) +
+                                                                      (uint32_t)((chunk ^ (row & 7)) << 4)),
+                       "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3])
+                       : "memory");
+          if (chunk == 0) asm volatile("st.shared.f32 [%0], %1;" ::"r"(as_slot + 4u * (uint32_t)row), "f"(sc) : "memory");
+        }
+        fence_proxy_async_shared();  // the codes, for the MMA (async proxy)
+        mbar_arrive(afull_bar(st));
+        mbar_arrive(rempty_bar(r));
+      }
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::kEpiRegs));
+    // ------------------------------------------------------------ promotion + epilogue
+    const int e = warp - 8;
+    const int row = epi_row(e, lane);
+    const int col0 = epi_col0(e, BN, EW);
+    const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+      const bool last_tile = tile + (int)gridDim.x >= p.num_tiles;
+      float acc[kCols];
+#pragma unroll
+      for (int j = 0; j < kCols; ++j) acc[j] = 0.0f;
+      for (int kb = 0; kb < p.Kb; ++kb, ++it) {
+        const uint32_t grp = it / Cfg::kScaleGroup, sub = it % Cfg::kScaleGroup;
+        const int sl = (int)(grp % Cfg::kScaleSlots);
+        const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes + sub * Cfg::kScaleKbBytes);
+        const bool sgot = sub != 0 || mbar_spin_bounded(sfull_bar(sl), (grp / Cfg::kScaleSlots) & 1u,
+                                                        p.wait_limit_ns, abort_flag);
+        const int buf = (int)(it & 1u);
+        const uint32_t tph = (it >> 1) & 1u;
+        const bool got = sgot && mbar_wait_bounded(p.debug_stall ? stall_bar : tfull_bar(buf), tph, p.wait_limit_ns,
+                                                   abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) gemm_fail(sgot ? kErrWaitTmemFull : kErrWaitScale, abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float sa_cur, sb_cur;
+        asm volatile("ld.shared.f32 %0, [%1];"
+                     : "=f"(sa_cur)
+                     : "r"(sbase + Cfg::kOffAs + (uint32_t)((it % Cfg::kAsSlots) * kBM * 4) + 4u * row));
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sb_cur) : "r"(slot + 512u + 4u * (uint32_t)(col0 >> 7)));
+        const float scale = sa_cur * sb_cur;
+        const uint64_t scale2 = f2_pack(scale, scale);
+        const uint32_t taddr = tmem_base + lane_base + (uint32_t)(buf * BN + col0);
+#pragma unroll
+        for (int c = 0; c < kCols / LDW; ++c) {
+          uint32_t rr[LDW];
+          if constexpr (LDW == 64)
+            tmem_ld_32x32b_x64(taddr + (uint32_t)(LDW * c), rr);
+          else
+            tmem_ld_32x32b_x32(taddr + (uint32_t)(LDW * c), rr);
+          tmem_ld_wait();
+          tmem_regs_after_wait(rr);
+          if (c == kCols / LDW - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(buf));
+          }
+#pragma unroll
+          for (int j = 0; j < LDW; j += 2) {  // acc += (a_s * b_s) * P, two columns per fp32x2 FMA
+            const uint64_t p2 = f2_pack(__uint_as_float(rr[j]), __uint_as_float(rr[j + 1]));
+            f2_unpack(f2_fma(scale2, p2, f2_pack(acc[LDW * c + j], acc[LDW * c + j + 1])), acc[LDW * c + j],
+                      acc[LDW * c + j + 1]);
+          }
+        }
+        if (sub == Cfg::kScaleGroup - 1 || (last_tile && kb == p.Kb - 1)) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sempty_bar(sl));
+        }
+      }
+      if (!ok) break;
+      // epilogue (as the dense kernel): rows < M and columns < N only
+      constexpr int kG = kCols / 8 >= 8 ? 8 : kCols / 8;
+      const int pos = lane % kG;
+#pragma unroll
+      for (int sg = 0; sg < kCols / (8 * kG); ++sg) {
+        uint32_t X[kG][4];
+#pragma unroll
+        for (int j = 0; j < kG; ++j)
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            X[j][q] = pack_bf16x2(acc[8 * (kG * sg + j) + 2 * q], acc[8 * (kG * sg + j) + 2 * q + 1]);
+#pragma unroll
+        for (int msk = kG / 2; msk >= 1; msk >>= 1) {
+          const bool hi = (pos & msk) != 0;
+#pragma unroll
+          for (int j = 0; j < kG; ++j) {
+            if (j & msk) continue;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t send = hi ? X[j][q] : X[j | msk][q];
+              const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, msk);
+              if (hi) X[j][q] = recv;
+              else X[j | msk][q] = recv;
+            }
+          }
+        }
+        const int n = g.n0 + epi_store_col(e, lane, sg, kG, BN, EW);
+#pragma unroll
+        for (int i = 0; i < kG; ++i) {
+          const int mr = g.m0 + epi_store_row(e, lane, i, kG);
+          if (mr >= p.M || n >= p.N) continue;
+          uint16_t* dst = p.c + (int64_t)mr * p.ldc + n;
+          if (p.c_vec && n + 8 <= p.N) {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(X[i][0], X[i][1], X[i][2], X[i][3]);
+          } else {
+#pragma unroll
+            for (int b = 0; b < 8; ++b)
+              if (n + b < p.N) dst[b] = (uint16_t)(X[i][b >> 1] >> (16 * (b & 1)));
+          }
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -1130,6 +1568,75 @@ cudaError_t launch_gemm_grouped(const GemmGroupArgs& ga, int num_sms, cudaStream
   }
   if (bn == 256) return run_gemm<256, 3, kSbCol, kGroupRed>(ma, mb, p, grid, st, &gp);
   return run_gemm<128, 6, kSbCol, kGroupRed>(ma, mb, p, grid, st, &gp);
+}
+
+
+// Row-major [rows, inner] bf16 matrix with row stride ld_bytes; 64-column x
+// 128-row boxes, 128-byte swizzle, out-of-range reads filled with 0.
+static bool make_tma_bf16(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t ld_bytes,
+                          int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld_bytes};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t elem[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int RAW_ROWS>
+static cudaError_t run_gemm_xq(const GemmXqArgs& a, int num_sms, cudaStream_t st, const char** msg) {
+  constexpr int BN = 128, STAGES = RAW_ROWS == 16 ? 8 : 4, LDW = 32;
+  using Cfg = XqCfg<BN, STAGES, RAW_ROWS>;
+  CUtensorMap mx, mb;
+  if (!make_tma_bf16(&mx, a.x, a.K, a.M, a.ldx * 2, RAW_ROWS) || !make_tma_u8(&mb, a.qb, a.K, a.N, a.ldb, BN)) {
+    *msg = "cuTensorMapEncodeTiled failed for an operand (alignment, stride or size out of range)";
+    return cudaErrorInvalidValue;
+  }
+  const int64_t num_m = cdiv(a.M, kBM), num_n = cdiv(a.N, BN), Kb = cdiv(a.K, kBK);
+  if (a.M >= (int64_t)1 << 31 || a.N >= (int64_t)1 << 31 || a.K >= (int64_t)1 << 31 ||
+      num_m * num_n * Kb >= (int64_t)1 << 31) {
+    *msg = "GEMM too large: M, N, K and the number of (tile, K-block) units must stay below 2^31";
+    return cudaErrorInvalidValue;
+  }
+  GemmParams p;
+  p.sa = nullptr;
+  p.ldsa = 0;
+  p.sb = a.sb;
+  p.ldsb = a.ldsb;
+  p.c = reinterpret_cast<uint16_t*>(a.c);
+  p.ldc = a.ldc;
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.num_m = (int)num_m;
+  p.num_n = (int)num_n;
+  p.num_tiles = (int)(num_m * num_n);
+  p.Kb = (int)Kb;
+  p.Nb = (int)cdiv(a.N, kBlock);
+  p.c_vec = (a.ldc % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.c) & 15u) == 0);
+  p.sa_vec = 0;
+  p.sb_vec = 0;
+  p.wait_limit_ns = kWaitLimitNs;
+  p.debug_stall = 0;
+  const int64_t grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_xq_kernel<BN, STAGES, LDW, RAW_ROWS>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  return launch_pdl(gemm_xq_kernel<BN, STAGES, LDW, RAW_ROWS>, (unsigned)grid, Cfg::kThreads, Cfg::kSmemBytes, st, mx,
+                    mb, p);
+}
+
+// x tiles of 16 rows (eight in flight) when every row of A fits in them, else of 128.
+cudaError_t launch_gemm_xq(const GemmXqArgs& a, int num_sms, cudaStream_t st, const char** msg) {
+  return a.M <= 16 ? run_gemm_xq<16>(a, num_sms, st, msg) : run_gemm_xq<128>(a, num_sms, st, msg);
 }
 
 cudaError_t gemm_read_errors(uint32_t* out) {

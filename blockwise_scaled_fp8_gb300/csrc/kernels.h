@@ -98,6 +98,23 @@ struct GemmGroupArgs {
   int64_t sb_step, c_step;
 };
 cudaError_t launch_gemm_grouped(const GemmGroupArgs& a, int num_sms, cudaStream_t st, const char** msg);
+// The forward GEMM (1x128 x 128x128) with A quantised inside the kernel: x
+// bf16 [M, K] (ldx elements, ldx % 8 == 0, 16-byte aligned), qb the weight's
+// e4m3 bytes [N, K] (ldb % 16 == 0), sb its tile scales [Nb, Kb] (row-major,
+// ldsb), c bf16 [M, N].
+struct GemmXqArgs {
+  const void* x;
+  int64_t ldx;
+  const void* qb;
+  int64_t ldb;
+  const float* sb;
+  int64_t ldsb;
+  void* c;
+  int64_t ldc;
+  int64_t M, N, K;
+};
+cudaError_t launch_gemm_xq(const GemmXqArgs& a, int num_sms, cudaStream_t st, const char** msg);
+
 // Reads and clears the device error word of the GEMM kernels (synchronous).
 cudaError_t gemm_read_errors(uint32_t* out);
 

@@ -94,53 +94,8 @@ __device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
   asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
 
-// Packed bf16 pair: per half, a value whose magnitude is max(|a|, |b|) (its
-// sign bit is meaningless and is masked off where the maximum is used).
-__device__ __forceinline__ uint32_t amax2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
 __device__ __forceinline__ uint32_t word_of(const uint4& v, int q) {
   return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
-}
-
-// s = RN(max(amax, 1e-12) / 448).  448 = 7 * 2^6 and a/448 stays a normal
-// float for a >= 1e-12, so s = RN(a/7) * 2^-6 exactly.  RN(a/7) comes from
-// y7 = RN(1/7) with one correction step of Markstein's method (P. Markstein,
-// IBM J. Res. Dev. 34(1), 1990): q0 = RN(a*y7), r = a - 7*q0 (exact), RN(q0 + r*y7).
-// For every bf16 amax this equals the IEEE quotient (checked exhaustively on
-// the CPU; the GPU tests compare every scale bit for bit with the oracle).
-__device__ __forceinline__ float scale_of(float amax) {
-  constexpr float kRcp7 = 1.0f / 7.0f;
-  const float a = fmaxf(amax, kAmaxFloor);
-  const float q0 = __fmul_rn(a, kRcp7);
-  const float r = __fmaf_rn(-7.0f, q0, a);
-  return __fmul_rn(__fmaf_rn(r, kRcp7, q0), 0.015625f);
-}
-
-// -1/s to within one ulp (rcp.approx: at most 1 ulp of error over the whole
-// range; s is normal, so flushing subnormals changes nothing).
-__device__ __forceinline__ float neg_rcp(float s) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(-s));
-  return y;
-}
-
-// The e4m3 codes of -(x/s) for the two bf16 values of `w`, given s2 = (s, s')
-// and ny2 = (-1/s, -1/s') to within an ulp:
-//   q0 = x*(-y), r = x - s*(x*y) (exact), q1 = q0 + r*(-y) = -RN(x/s).
-// With bf16 x, |x| <= 448 s and any such y this one-step quotient rounds to
-// the same e4m3 code as the IEEE quotient, including the sign of zero
-// (checked exhaustively on the CPU over every pair of bf16 (amax, x)).  The
-// caller flips the sign bits of the codes (XOR 0x80).
-__device__ __forceinline__ uint32_t neg_codes2(uint32_t w, uint64_t s2, uint64_t ny2) {
-  const uint64_t x2 = f2_pack(bf16_lo(w), bf16_hi(w));
-  const uint64_t q0 = f2_mul(x2, ny2);
-  const uint64_t r = f2_fma(s2, q0, x2);
-  const uint64_t q1 = f2_fma(r, ny2, q0);
-  return cvt_e4m3x2(__uint_as_float((uint32_t)q1), __uint_as_float((uint32_t)(q1 >> 32)));
 }
 
 // MXFP8 (OCP Microscaling v1.0, FLOOR scale): for a block maximum amax (a

@@ -347,6 +347,34 @@ BFP8_API bfp8_status bfp8_moe_step_host(const void *x, const void *w, const void
                                         int64_t chunk_n, void *ws, size_t ws_bytes, bfp8_stream_t stream);
 
 /*
+ * The forward GEMM 1x128 x 128x128 with its A operand quantised inside the
+ * kernel: C = quant_lhs(x) . (the weight's 128x128-tile codes)^T, for an
+ * activation x that has not been quantised yet and a weight that has (e.g.
+ * cached between calls).  The method is that of bfp8_quant_lhs followed by
+ * bfp8_gemm_1x128_128x128 ("Enable blockwise FP8 dense training kernels on
+ * ROCm": act_quant_lhs, the 1x128 x 128x128 GEMM; "Mask a_s/b_s scale loads
+ * in blockwise FP8 training GEMM kernels", Fix: masked loads and stores) and
+ * the result is the same bits: each row's 1x128 group maximum, scale
+ * s = amax/448 and codes RNE_e4m3(clamp(x/s, +-448)) are formed in shared
+ * memory by a quantiser warpgroup with the quantisation kernels' arithmetic,
+ * and never written to global memory.  One launch instead of two, without the
+ * codes' HBM round trip: meant for small M (a few token rows), where the
+ * separate quantisation launch is a large share of the forward.
+ *   x  device bf16 [M, K] row-major, ldx >= K, ldx % 8 == 0, 16-byte aligned;
+ *   qb device e4m3 [N, K] (bfp8_quant_weight's q), ldb >= K, ldb % 16 == 0,
+ *      16-byte aligned; sb device fp32 [ceil(N/128), ceil(K/128)] tile scales,
+ *      ldsb >= ceil(K/128);
+ *   c  device bf16 [M, N], ldc >= N; only the logical [M, N] region is written.
+ * K == 0 sets the [M, N] region of c to zero and reads nothing else.
+ * Errors: BFP8_ERR_INVALID_ARG (sizes, strides, alignment, null pointers),
+ * BFP8_ERR_UNSUPPORTED (not sm_103), BFP8_ERR_CUDA (launch); a bounded wait
+ * that gave up is reported by bfp8_check_device_errors.
+ */
+BFP8_API bfp8_status bfp8_gemm_1x128_128x128_xq(const void *x, int64_t ldx, const void *qb, int64_t ldb,
+                                                const float *sb, int64_t ldsb, void *c, int64_t ldc, int64_t M,
+                                                int64_t N, int64_t K, bfp8_stream_t stream);
+
+/*
  * Linear forward without caller-provided scratch (no counterpart on the pages:
  * an addition for callers that cannot allocate device memory — plugins hosted
  * by a framework that owns every allocation and hands them no allocator, and

@@ -87,6 +87,31 @@ def test_gemm_argument_validation():
     assert h(P16, 256, P16, 8, P16, 256, P16, 63, P16, 64, 8, 64, 256, NULL) == B.BFP8_ERR_INVALID_ARG  # ldsb < N
 
 
+def test_xq_gemm_argument_validation():
+    """The GEMM that quantises its bf16 A itself checks x's row stride (TMA:
+    a multiple of 8 bf16 values, at least K) and alignment before launching."""
+    L = B.lib()
+    g = L.bfp8_gemm_1x128_128x128_xq
+    ok_args = [P16, 256, P16, 256, P16, 2, P16, 64, 8, 64, 256, NULL]
+    names = ["x", "ldx", "qb", "ldb", "sb", "ldsb", "c", "ldc", "M", "N", "K", "st"]
+
+    def call(**kw):
+        a = list(ok_args)
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return g(*a)
+
+    assert call(ldx=200) == B.BFP8_ERR_INVALID_ARG          # ldx < K
+    assert call(ldx=260) == B.BFP8_ERR_INVALID_ARG          # not a multiple of 8 (TMA row stride)
+    assert call(ldb=264) == B.BFP8_ERR_INVALID_ARG          # not a multiple of 16
+    assert call(ldsb=1) == B.BFP8_ERR_INVALID_ARG           # ldsb < Kb
+    assert call(ldc=32) == B.BFP8_ERR_INVALID_ARG           # ldc < N
+    assert call(x=P_ODD) == B.BFP8_ERR_INVALID_ARG          # x not 16-byte aligned
+    assert call(x=NULL) == B.BFP8_ERR_INVALID_ARG
+    assert call(M=-1) == B.BFP8_ERR_INVALID_ARG
+    assert call(M=0) == B.BFP8_OK
+
+
 def test_grouped_and_fused_argument_validation():
     """Host-side checks of the grouped GEMMs and of the one-launch
     quantisation: every rejection happens before anything is launched."""
