@@ -1198,7 +1198,7 @@ bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, i
     return BFP8_OK;
   }
   if (kind == 3) {  // GEMM output C [M,N]; flag bit 3: the 1x128 x 128x1 GEMM
-    const int bn = gemm_pick_bn(M, N, sms);
+    const int bn = gemm_pick_bn(M, N, (flag & 8) != 0, sms);
     const int ew = gemm_epi_warps((flag & 8) != 0, bn);
     const int num_m = (int)cdiv(M, kBM), num_n = (int)cdiv(N, bn), tiles = num_m * num_n;
     const int grid = (int)gemm_grid(M, N, bn, sms);
@@ -1207,7 +1207,7 @@ bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, i
         const GemmTile g = gemm_tile(tile, num_m, num_n, bn);
         const int G = epi_group(bn, ew);
         for (int e = 0; e < ew; ++e)
-          for (int lane = 0; lane < 32; ++lane)
+          for (int lane = 0; lane < 32 && (gemm_a_rows(M, bn) == kBM || e % 4 == 0); ++lane)
             for (int sg = 0; sg < epi_cols(bn, ew) / (8 * G); ++sg)
               for (int i = 0; i < G; ++i) {
                 const int64_t m = g.m0 + epi_store_row(e, lane, i, G);

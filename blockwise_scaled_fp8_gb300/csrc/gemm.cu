@@ -100,7 +100,7 @@ struct GemmJob {
   int64_t c_off;     // element offset of the output C[first row][n0]
 };
 
-template <int BN, int STAGES, int EW>
+template <int BN, int STAGES, int EW, int A_ROWS = 128>
 struct GemmCfg {
   static constexpr int kEpiWarps = EW;
   static constexpr int kCols = BN / (EW / 4);  // tile columns per promotion warp
@@ -114,11 +114,27 @@ struct GemmCfg {
   static constexpr int kCtrlRegs = EW == 16 ? 56 : 40;
   static constexpr int kEpiRegs = EW == 16 ? 104 : 224;
   static_assert(128 * kCtrlRegs + 32 * EW * kEpiRegs <= kThreads * kLaunchRegs, "register split");
-  static constexpr int kABytes = kBM * kBK;
+  static constexpr int kABytes = kBM * kBK;  // what one MMA reads of A: 128 rows x 128 B
+  // A_ROWS = 16 (problems of at most 16 rows): A stages hold 16-row boxes and
+  // sit 2 KiB apart; an MMA still reads 128 rows from its stage's start, and
+  // rows 16..127 (bytes of the following stages) only feed accumulator rows
+  // >= M, which are never read.  The room saved holds more stages of B, the
+  // operand streamed from DRAM.
+  static_assert(A_ROWS == 128 || A_ROWS == 16, "A box rows");
+  static constexpr int kAStride = A_ROWS == 16 ? 16 * kBK : kABytes;
   static constexpr int kBBytes = BN * kBK;
-  static constexpr int kStageBytes = kABytes + kBBytes;
-  static constexpr int kTmemCols = 2 * BN;  // two fp32 partial buffers of BN columns
-  static constexpr int kOffB = STAGES * kABytes;
+  static constexpr int kStageBytes = A_ROWS * kBK + kBBytes;  // what one stage's copies bring
+  // fp32 partial buffers in tensor memory: two of BN >= 128 columns, or (the
+  // narrow tiles of problems that fill few SMs) as many as fit in 512
+  // columns, so that the MMAs run several K-blocks ahead of the promotion
+  static constexpr int kBufs = BN >= 128 ? 2 : 512 / BN;
+  static constexpr int kTmemCols = kBufs * BN;
+  // promotion warps that hold rows of the tile: all, or with A_ROWS = 16 the
+  // EW / 4 warps of tensor-memory lanes 0..31
+  static constexpr int kActiveEpi = A_ROWS == 16 ? EW / 4 : EW;
+  // tile scales (1x128 x 128x128 modes) a K-block needs: one per 128 columns
+  static constexpr int kTileScales = BN >= 128 ? BN / 128 : 1;
+  static constexpr int kOffB = ((STAGES - 1) * kAStride + kABytes + 1023) / 1024 * 1024;
   static constexpr int kOffC = kOffB + STAGES * kBBytes;
   // scale ring: kScaleSlots slots of kScaleGroup K-blocks, each K-block
   // a_s[128 rows] then b_s (BN column scales or up to BN/128 tile scales)
@@ -128,7 +144,7 @@ struct GemmCfg {
   static constexpr int kScaleBytes = kScaleGroup * kScaleKbBytes;
   static constexpr int kOffScale = kOffC;
   static constexpr int kOffBar = kOffScale + kScaleSlots * kScaleBytes;
-  static constexpr int kNumBars = 2 * STAGES + 6 + 2 * kScaleSlots;
+  static constexpr int kNumBars = 2 * STAGES + 2 * kBufs + 2 + 2 * kScaleSlots;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
   // grouped forms only: the experts' offsets and first tiles
@@ -246,12 +262,13 @@ __device__ __forceinline__ GemmJob gemm_job(int tile, const GemmParams& p, const
   return j;
 }
 
-template <int BN, int STAGES, int SB_MODE, int LDW, int EW>
-__global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
+template <int BN, int STAGES, int SB_MODE, int LDW, int EW, int A_ROWS = 128>
+__global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW, A_ROWS>::kThreads, 1)
     gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tma_a,
                           const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
-  using Cfg = GemmCfg<BN, STAGES, EW>;
+  using Cfg = GemmCfg<BN, STAGES, EW, A_ROWS>;
   constexpr int kCols = Cfg::kCols;
+  constexpr int NT = Cfg::kBufs;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -264,15 +281,17 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
   volatile int* never = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
 
-  // barriers: full[S], empty[S], tfull[2], tempty[2], drain (both issuers), stall, sfull[2], sempty[2]
+  // barriers: full[S], empty[S], tfull[NT], tempty[NT], drain (both issuers), stall, sfull[2], sempty[2]
   auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(STAGES + i); };
   auto tfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + i); };
-  auto tempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + 2 + i); };
-  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 4);
-  const uint32_t stall_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 5);  // never arrived on
-  auto sfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + 6 + i); };
-  auto sempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + 6 + Cfg::kScaleSlots + i); };
+  auto tempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + NT + i); };
+  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 2 * NT);
+  const uint32_t stall_bar = bar0 + 8u * (uint32_t)(2 * STAGES + 2 * NT + 1);  // never arrived on
+  auto sfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * STAGES + 2 * NT + 2 + i); };
+  auto sempty_bar = [&](int i) {
+    return bar0 + 8u * (uint32_t)(2 * STAGES + 2 * NT + 2 + Cfg::kScaleSlots + i);
+  };
 
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const int lane = (int)(threadIdx.x & 31);
@@ -283,15 +302,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
       mbar_init(full_bar(i), 1);
       mbar_init(empty_bar(i), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NT; ++i) {
       mbar_init(tfull_bar(i), 1);
-      mbar_init(tempty_bar(i), Cfg::kEpiWarps);
+      mbar_init(tempty_bar(i), Cfg::kActiveEpi);
     }
     mbar_init(drain_bar, 2);
     mbar_init(stall_bar, 1);
     for (int i = 0; i < Cfg::kScaleSlots; ++i) {
       mbar_init(sfull_bar(i), 32);  // one cp.async arrival per loader lane
-      mbar_init(sempty_bar(i), Cfg::kEpiWarps);
+      mbar_init(sempty_bar(i), Cfg::kActiveEpi);
     }
     *abort_flag = 0;
     *never = 0;
@@ -329,7 +348,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(full_bar(st), (uint32_t)Cfg::kStageBytes);
-          tma_load_2d(sA + (uint32_t)(st * Cfg::kABytes), &tma_a, full_bar(st), kb * kBK, g.m0);
+          tma_load_2d(sA + (uint32_t)(st * Cfg::kAStride), &tma_a, full_bar(st), kb * kBK, g.m0);
           tma_load_2d(sB + (uint32_t)(st * Cfg::kBBytes), &tma_b, full_bar(st), kb * kBK, g.n0);
         }
       }
@@ -353,8 +372,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
           if ((it & 1u) != mine) continue;
           const int st = (int)(it % STAGES);
           const uint32_t ph = (it / STAGES) & 1u;
-          const int buf = (int)(it & 1u);
-          const uint32_t tph = (it >> 1) & 1u;
+          const int buf = (int)(it % NT);
+          const uint32_t tph = (it / NT) & 1u;
           if (!mbar_spin_bounded(tempty_bar(buf), tph ^ 1u, p.wait_limit_ns, abort_flag)) {
             gemm_fail(kErrWaitTmemEmpty, abort_flag);
             ok = false;
@@ -366,7 +385,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t da = desc_kmajor_sw128(sA + (uint32_t)(st * Cfg::kABytes));
+          const uint64_t da = desc_kmajor_sw128(sA + (uint32_t)(st * Cfg::kAStride));
           const uint64_t db = desc_kmajor_sw128(sB + (uint32_t)(st * Cfg::kBBytes));
           const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
 #pragma unroll
@@ -408,7 +427,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
           for (int h = 0; h < BN / 128; ++h)
             copy_scales4(slot + 512u + 512u * h + 16u * lane, p.sb + (int64_t)kb * p.ldsb, g.n0 + 128 * h + 4 * lane,
                          p.N, p.sb_vec);
-        } else if (lane < BN / 128) {  // tile scale of the 128 columns n0 + 128*lane (zero past N)
+        } else if (lane < Cfg::kTileScales) {  // tile scale of the 128 columns n0 + 128*lane (zero past N)
           const int nb = g.n0 / kBlock + lane;
           const bool in = nb < p.Nb;
           const float* src = SB_MODE == kSbTile ? p.sb + (int64_t)nb * p.ldsb + kb : p.sb + (int64_t)kb * p.ldsb + nb;
@@ -429,7 +448,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     const int col0 = epi_col0(e, BN, EW);
     const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
     uint32_t it = 0;
-    bool ok = true;
+    // (A_ROWS = 16: warps of lanes 32..127 hold no row of the problem and skip the loop)
+    bool ok = A_ROWS == 128 || warp % 4 == 0;
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
       const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
       const bool last_tile = tile + (int)gridDim.x >= p.num_tiles;
@@ -444,8 +464,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
         // once per group: the loader runs ahead, so the slot is almost always ready (poll)
         const bool sgot = sub != 0 || mbar_spin_bounded(sfull_bar(sl), (grp / Cfg::kScaleSlots) & 1u,
                                                         p.wait_limit_ns, abort_flag);
-        const int buf = (int)(it & 1u);
-        const uint32_t tph = (it >> 1) & 1u;
+        const int buf = (int)(it % NT);
+        const uint32_t tph = (it / NT) & 1u;
         const bool got = sgot && mbar_wait_bounded(p.debug_stall ? stall_bar : tfull_bar(buf), tph, p.wait_limit_ns,
                                                    abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
@@ -584,6 +604,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
                         const __grid_constant__ CUtensorMap tma_b, const GemmParams p, const GemmGroupParams gp) {
   static_assert(GROUP == kGroupRows || GROUP == kGroupRed, "a grouped form");
   using Cfg = GemmCfg<BN, STAGES, EW>;
+  static_assert(Cfg::kBufs == 2 && Cfg::kTileScales == BN / 128, "the grouped forms use tiles of 128 or 256 columns");
   constexpr int kCols = Cfg::kCols;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -974,20 +995,27 @@ struct XqCfg {
   static constexpr int kScaleSlots = 2, kScaleGroup = 4;
   static constexpr int kScaleKbBytes = 128 * 4 + BN * 4;
   static constexpr int kScaleBytes = kScaleGroup * kScaleKbBytes;
+  // fp32 partial buffers in tensor memory: two of 128 columns, or eight of
+  // 64 (the narrow tiles of problems that fill few SMs, as the dense GEMM)
+  static constexpr int kBufs = BN >= 128 ? 2 : 512 / BN;
+  static constexpr int kTmemCols = kBufs * BN;
+  // promotion warps that hold rows of the problem: all, or with M <= 16 the
+  // two of tensor-memory lanes 0..31
+  static constexpr int kActiveEpi = RAW_ROWS == 16 ? kEpiWarps / 4 : kEpiWarps;
+  static constexpr int kTileScales = BN >= 128 ? BN / 128 : 1;
   // a_s of each K-block, written by the quantisers into a ring of kAsSlots
   // entries: they run at most STAGES units ahead of the MMAs, which run at
-  // most two ahead of the promotion (two tensor-memory buffers), and a
-  // promotion warp reads its a_s before releasing the buffer, so an entry is
-  // never rewritten before it has been read
-  static constexpr int kAsSlots = 16;
-  static_assert(kAsSlots >= STAGES + 2, "a_s ring depth");
+  // most kBufs ahead of the promotion, and a promotion warp reads its a_s
+  // before releasing the buffer, so an entry is never rewritten before it has
+  // been read
+  static constexpr int kAsSlots = BN >= 128 ? 16 : 32;
+  static_assert(kAsSlots >= STAGES + kBufs, "a_s ring depth");
   static constexpr int kOffAs = kOffScale + kScaleSlots * kScaleBytes;
   static constexpr int kOffBar = kOffAs + kAsSlots * kBM * 4;
-  // full[S] empty[S] afull[S] rfull[R] rempty[R] tfull[2] tempty[2] drain stall sfull[2] sempty[2]
-  static constexpr int kNumBars = 3 * STAGES + 2 * kRawSlots + 4 + 2 + 2 * kScaleSlots;
+  // full[S] empty[S] afull[S] rfull[R] rempty[R] tfull[T] tempty[T] drain stall sfull[2] sempty[2]
+  static constexpr int kNumBars = 3 * STAGES + 2 * kRawSlots + 2 * kBufs + 2 + 2 * kScaleSlots;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
-  static constexpr int kTmemCols = 2 * BN;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -997,6 +1025,7 @@ __global__ void __launch_bounds__(XqCfg<BN, STAGES, RAW_ROWS>::kThreads, 1)
                    const GemmParams p) {
   using Cfg = XqCfg<BN, STAGES, RAW_ROWS>;
   constexpr int NR = Cfg::kRawSlots;
+  constexpr int NT = Cfg::kBufs;
   constexpr int EW = Cfg::kEpiWarps;
   constexpr int kCols = Cfg::kCols;
   extern __shared__ uint8_t smem_raw[];
@@ -1016,11 +1045,11 @@ __global__ void __launch_bounds__(XqCfg<BN, STAGES, RAW_ROWS>::kThreads, 1)
   auto rfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * STAGES + i); };
   auto rempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * STAGES + NR + i); };
   auto tfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + i); };
-  auto tempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + 2 + i); };
-  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + 4);
-  const uint32_t stall_bar = bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + 5);  // never arrived on
-  auto sfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + 6 + i); };
-  auto sempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + 8 + i); };
+  auto tempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + NT + i); };
+  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + 2 * NT);
+  const uint32_t stall_bar = bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + 2 * NT + 1);  // never arrived on
+  auto sfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + 2 * NT + 2 + i); };
+  auto sempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * STAGES + 2 * NR + 2 * NT + 4 + i); };
 
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const int lane = (int)(threadIdx.x & 31);
@@ -1036,15 +1065,15 @@ __global__ void __launch_bounds__(XqCfg<BN, STAGES, RAW_ROWS>::kThreads, 1)
       mbar_init(rfull_bar(i), 1);
       mbar_init(rempty_bar(i), 64);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < NT; ++i) {
       mbar_init(tfull_bar(i), 1);
-      mbar_init(tempty_bar(i), EW);
+      mbar_init(tempty_bar(i), Cfg::kActiveEpi);
     }
     mbar_init(drain_bar, 2);
     mbar_init(stall_bar, 1);
     for (int i = 0; i < Cfg::kScaleSlots; ++i) {
       mbar_init(sfull_bar(i), 32);  // one cp.async arrival per b_s loader lane
-      mbar_init(sempty_bar(i), EW);
+      mbar_init(sempty_bar(i), Cfg::kActiveEpi);
     }
     *abort_flag = 0;
     *never = 0;
@@ -1119,8 +1148,8 @@ __global__ void __launch_bounds__(XqCfg<BN, STAGES, RAW_ROWS>::kThreads, 1)
             if ((it & 1u) != mine) continue;
             const int st = (int)(it % STAGES);
             const uint32_t ph = (it / STAGES) & 1u;
-            const int buf = (int)(it & 1u);
-            const uint32_t tph = (it >> 1) & 1u;
+            const int buf = (int)(it % NT);
+            const uint32_t tph = (it / NT) & 1u;
             if (!mbar_spin_bounded(tempty_bar(buf), tph ^ 1u, p.wait_limit_ns, abort_flag)) {
               gemm_fail(kErrWaitTmemEmpty, abort_flag);
               ok = false;
@@ -1166,7 +1195,7 @@ __global__ void __launch_bounds__(XqCfg<BN, STAGES, RAW_ROWS>::kThreads, 1)
             }
           }
           const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes + sub * Cfg::kScaleKbBytes);
-          if (lane < BN / 128) {  // tile scale of the 128 columns n0 + 128*lane (zero past N)
+          if (lane < Cfg::kTileScales) {  // tile scale of the 128 columns n0 + 128*lane (zero past N)
             const int nb = g.n0 / kBlock + lane;
             const bool in = nb < p.Nb;
             cp_async_4(slot + 512u + 4u * lane, in ? p.sb + (int64_t)nb * p.ldsb + kb : p.sb, in ? 4u : 0u);
@@ -1251,7 +1280,8 @@ __global__ void __launch_bounds__(XqCfg<BN, STAGES, RAW_ROWS>::kThreads, 1)
     const int col0 = epi_col0(e, BN, EW);
     const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
     uint32_t it = 0;
-    bool ok = true;
+    // (M <= 16: warps of lanes 32..127 hold no row of the problem and skip the loop)
+    bool ok = RAW_ROWS == 128 || warp % 4 == 0;
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
       const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
       const bool last_tile = tile + (int)gridDim.x >= p.num_tiles;
@@ -1264,8 +1294,8 @@ __global__ void __launch_bounds__(XqCfg<BN, STAGES, RAW_ROWS>::kThreads, 1)
         const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes + sub * Cfg::kScaleKbBytes);
         const bool sgot = sub != 0 || mbar_spin_bounded(sfull_bar(sl), (grp / Cfg::kScaleSlots) & 1u,
                                                         p.wait_limit_ns, abort_flag);
-        const int buf = (int)(it & 1u);
-        const uint32_t tph = (it >> 1) & 1u;
+        const int buf = (int)(it % NT);
+        const uint32_t tph = (it / NT) & 1u;
         const bool got = sgot && mbar_wait_bounded(p.debug_stall ? stall_bar : tfull_bar(buf), tph, p.wait_limit_ns,
                                                    abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
@@ -1396,7 +1426,13 @@ static bool make_tma_u8(CUtensorMap* map, const void* base, int64_t inner, int64
   return r == CUDA_SUCCESS;
 }
 
-int gemm_pick_bn(int64_t M, int64_t N, int num_sms) {
+int gemm_pick_bn(int64_t M, int64_t N, bool col_scales, int num_sms) {
+  // Problems whose 128-column tiles would occupy at most half the SMs (small
+  // M: decoding, skinny layers) take 64-column tiles with more tensor-memory
+  // buffers: twice the CTAs streaming B, and MMAs that run ahead of the
+  // promotion.  (1x128 x 128x128 modes only: the column-scale GEMM reduces
+  // over tokens and is not small in both M and N.)
+  if (!col_scales && 2 * cdiv(M, kBM) * cdiv(N, 128) <= num_sms) return 64;
   if (N <= 128) return 128;
   const int64_t tiles256 = cdiv(M, kBM) * cdiv(N, 256);
   return tiles256 >= num_sms ? 256 : 128;
@@ -1410,30 +1446,31 @@ int64_t gemm_grid(int64_t M, int64_t N, int bn, int num_sms) {
 // Promotion warps per tile shape and mode (measured): 16 for the 256-column
 // tiles and for the column-scale mode (more warps read tensor memory faster;
 // the 2048x4096x4096 input gradient 43.0 -> 40.9 us, the 16384x14336x4096
-// forward 818 -> 794 us), 8 for the 128-column tile-scale tiles (few-tile
-// shapes: 16 measured slower there); and columns per tensor-memory load (one
-// round trip per LDW columns of a warp's share, sized to the promotion warps'
-// registers).
+// forward 818 -> 794 us), 8 for the 128- and 64-column tile-scale tiles
+// (few-tile shapes: 16 measured slower there); and columns per tensor-memory
+// load (one round trip per LDW columns of a warp's share, sized to the
+// promotion warps' registers).
 template <int MODE, int BN>
 constexpr int gemm_ew() {
   return (MODE == kSbCol || BN == 256) ? 16 : 8;  // = gemm_epi_warps(MODE == kSbCol, BN), which the host replay uses
 }
 template <int BN, int MODE, int EW>
 constexpr int gemm_ldw() {
-  return EW == 16 ? (BN == 256 && MODE != kSbCol ? 32 : 16) : (MODE != kSbCol ? 64 : 32);
+  return EW == 16 ? (BN == 256 && MODE != kSbCol ? 32 : 16) : (MODE != kSbCol ? (BN >= 128 ? 64 : BN / 2) : 32);
 }
 
-template <int BN, int STAGES, int MODE, int GROUP = kGroupNone>
+template <int BN, int STAGES, int MODE, int GROUP = kGroupNone, int A_ROWS = 128>
 static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int64_t grid,
                             cudaStream_t st, const GemmGroupParams* gp = nullptr) {
   constexpr int EW = gemm_ew<MODE, BN>(), LDW = gemm_ldw<BN, MODE, EW>();
-  using Cfg = GemmCfg<BN, STAGES, EW>;
+  static_assert(GROUP == kGroupNone || A_ROWS == 128, "the grouped forms load 128-row A boxes");
+  using Cfg = GemmCfg<BN, STAGES, EW, A_ROWS>;
   constexpr int kSmem = Cfg::kSmemBytes + (GROUP != kGroupNone ? Cfg::kGroupTabBytes : 0);
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
     if constexpr (GROUP == kGroupNone)
-      attr_err = cudaFuncSetAttribute(gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW>,
+      attr_err = cudaFuncSetAttribute(gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW, A_ROWS>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     else
       attr_err = cudaFuncSetAttribute(gemm_grouped_kernel<BN, STAGES, MODE, LDW, EW, GROUP>,
@@ -1441,8 +1478,8 @@ static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const 
   });
   if (attr_err != cudaSuccess) return attr_err;
   if constexpr (GROUP == kGroupNone)
-    return launch_pdl(gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW>, (unsigned)grid, Cfg::kThreads, kSmem, st, ma,
-                      mb, p);
+    return launch_pdl(gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW, A_ROWS>, (unsigned)grid, Cfg::kThreads,
+                      kSmem, st, ma, mb, p);
   else
     return launch_pdl(gemm_grouped_kernel<BN, STAGES, MODE, LDW, EW, GROUP>, (unsigned)grid, Cfg::kThreads, kSmem,
                       st, ma, mb, p, *gp);
@@ -1450,9 +1487,10 @@ static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const 
 
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const char** msg,
                         uint64_t wait_limit_ns, int debug_stall) {
-  const int bn = gemm_pick_bn(a.M, a.N, num_sms);
+  const int bn = gemm_pick_bn(a.M, a.N, a.sb_mode == kSbCol, num_sms);
+  const int a_rows = gemm_a_rows(a.M, bn);
   CUtensorMap ma, mb;
-  if (!make_tma_u8(&ma, a.qa, a.K, a.M, a.lda, kBM) || !make_tma_u8(&mb, a.qb, a.K, a.N, a.ldb, bn)) {
+  if (!make_tma_u8(&ma, a.qa, a.K, a.M, a.lda, a_rows) || !make_tma_u8(&mb, a.qb, a.K, a.N, a.ldb, bn)) {
     *msg = "cuTensorMapEncodeTiled failed for an operand (alignment, stride or size out of range)";
     return cudaErrorInvalidValue;
   }
@@ -1483,6 +1521,15 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const c
   p.wait_limit_ns = wait_limit_ns;
   p.debug_stall = debug_stall;
   const int64_t grid = gemm_grid(a.M, a.N, bn, num_sms);
+  // 64-column tiles (tile-scale modes): sixteen stages of 2 + 8 KiB with
+  // 16-row A boxes, else eight of 16 + 8 KiB
+  if (bn == 64) {
+    const bool t = a.sb_mode == kSbTile;
+    if (a_rows == 16)
+      return t ? run_gemm<64, 16, kSbTile, kGroupNone, 16>(ma, mb, p, grid, st)
+               : run_gemm<64, 16, kSbTileT, kGroupNone, 16>(ma, mb, p, grid, st);
+    return t ? run_gemm<64, 8, kSbTile>(ma, mb, p, grid, st) : run_gemm<64, 8, kSbTileT>(ma, mb, p, grid, st);
+  }
   // 256-column tiles: three stages of 48 KiB (four measured no faster, and a
   // little slower for the weight gradient)
   if (bn == 256) {
@@ -1587,9 +1634,9 @@ static bool make_tma_bf16(CUtensorMap* map, const void* base, int64_t inner, int
   return r == CUDA_SUCCESS;
 }
 
-template <int RAW_ROWS>
+template <int RAW_ROWS, int BN>
 static cudaError_t run_gemm_xq(const GemmXqArgs& a, int num_sms, cudaStream_t st, const char** msg) {
-  constexpr int BN = 128, STAGES = RAW_ROWS == 16 ? 8 : 4, LDW = 32;
+  constexpr int STAGES = RAW_ROWS == 16 ? (BN == 64 ? 12 : 8) : 4, LDW = 32;
   using Cfg = XqCfg<BN, STAGES, RAW_ROWS>;
   CUtensorMap mx, mb;
   if (!make_tma_bf16(&mx, a.x, a.K, a.M, a.ldx * 2, RAW_ROWS) || !make_tma_u8(&mb, a.qb, a.K, a.N, a.ldb, BN)) {
@@ -1634,9 +1681,14 @@ static cudaError_t run_gemm_xq(const GemmXqArgs& a, int num_sms, cudaStream_t st
                     mb, p);
 }
 
-// x tiles of 16 rows (eight in flight) when every row of A fits in them, else of 128.
+// x tiles of 16 rows (eight in flight) when every row of A fits in them,
+// with the dense GEMM's 64-column tiles where 128-column ones would fill at
+// most half the SMs; else x tiles of 128 rows and 128-column tiles.
 cudaError_t launch_gemm_xq(const GemmXqArgs& a, int num_sms, cudaStream_t st, const char** msg) {
-  return a.M <= 16 ? run_gemm_xq<16>(a, num_sms, st, msg) : run_gemm_xq<128>(a, num_sms, st, msg);
+  if (a.M <= 16)
+    return gemm_pick_bn(a.M, a.N, false, num_sms) == 64 ? run_gemm_xq<16, 64>(a, num_sms, st, msg)
+                                                         : run_gemm_xq<16, 128>(a, num_sms, st, msg);
+  return run_gemm_xq<128, 128>(a, num_sms, st, msg);
 }
 
 cudaError_t gemm_read_errors(uint32_t* out) {

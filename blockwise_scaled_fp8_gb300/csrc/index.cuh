@@ -160,8 +160,13 @@ BFP8_HD int group_of_tile(const int* start, int E, int t) {
 // Promotion / epilogue warp e (0-based, CTA warp id = e + 4) of `ew` (8 or
 // 16): tensor-memory lane quarter e % 4 (the quarter a warp may access is its
 // CTA warp id % 4), column block e / 4 of epi_cols(bn, ew) columns.  The
-// 1x128 x 128x128 GEMMs use 8 promotion warps, the 1x128 x 128x1 GEMM 16.
+// 1x128 x 128x128 GEMMs use 8 promotion warps (16 with 256-column tiles),
+// the 1x128 x 128x1 GEMM 16.
 BFP8_HD int gemm_epi_warps(bool col_scales, int bn) { return (col_scales || bn == 256) ? 16 : 8; }
+// Rows of A one pipeline stage loads: 16 for the 64-column tiles of problems
+// of at most 16 rows, else 128.  With 16, only the promotion warps of lane
+// quarter 0 (e % 4 == 0) hold rows of the problem; the others store nothing.
+BFP8_HD int gemm_a_rows(int64_t M, int bn) { return bn == 64 && M <= 16 ? 16 : kBM; }
 BFP8_HD int epi_row(int e, int lane) { return 32 * (e % 4) + lane; }
 BFP8_HD int epi_cols(int bn, int ew) { return bn / (ew / 4); }
 BFP8_HD int epi_col0(int e, int bn, int ew) { return epi_cols(bn, ew) * (e / 4); }

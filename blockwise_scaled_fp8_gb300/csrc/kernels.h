@@ -75,8 +75,9 @@ struct GemmArgs {
 // a host-side failure (tensor-map encoding) when the return is not success.
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const char** msg,
                         uint64_t wait_limit_ns = kWaitLimitNs, int debug_stall = 0);
-// Tile width the launcher picks for an M x N output, and the grid it uses.
-int gemm_pick_bn(int64_t M, int64_t N, int num_sms);
+// Tile width the launcher picks for an M x N output (col_scales: the 1x128 x
+// 128x1 GEMM), and the grid it uses.
+int gemm_pick_bn(int64_t M, int64_t N, bool col_scales, int num_sms);
 int64_t gemm_grid(int64_t M, int64_t N, int bn, int num_sms);
 // Grouped (mixture-of-experts) GEMM, kind kGroupRows or kGroupRed (index.cuh).
 //   kGroupRows: g.qa [M_total, K] token rows, C [M_total, N]; expert e's rows
