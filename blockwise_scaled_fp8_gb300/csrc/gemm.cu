@@ -958,7 +958,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
 // FP8 behind BF16 at M = 128 and 512).
 //
 //   warp 0      producer: raw bf16 x tiles (two 64-column boxes) into a
-//               two-slot ring, B tiles into the stage ring
+//               ring (two slots of 128 rows, or eight of 16 when M <= 16),
+//               B tiles into the stage ring
 //   warps 1, 3  MMA issuers: as the dense kernel, also waiting for the
 //               stage's quantised A
 //   warp 2      b_s of each K-block into the scale ring
@@ -966,7 +967,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
 //               K-blocks quantised at once): thread (row, 16-column chunk);
 //               a row's 8 chunks are 8 lanes of one warp, which combine their
 //               maxima by shuffles; the chunk-0 lane writes a_s into a ring
-//   warps 8-15  promotion + epilogue, as the dense kernel (8 warps)
+//   warps 8-15  promotion + epilogue, as the dense kernel (8 warps; with
+//               M <= 16 only the two of lanes 0..31 hold rows)
 // ---------------------------------------------------------------------------
 template <int BN, int STAGES, int RAW_ROWS>
 struct XqCfg {

@@ -23,11 +23,10 @@
 //     same call;
 //   - the first call in each CUDA context (normally: once per device) looks up
 //     the array's device address (cudaGetSymbolAddress) with that device
-//     current, and remembers it for that context; make that first call before
-//     any stream capture, since the lookup may not be capturable.  A new
-//     context on the same device (after cudaDeviceReset, or a driver-API
-//     context made current by the caller) loads the library's module again,
-//     possibly at another address, and is looked up again on its first call.
+//     current, and remembers it for that context.  A new context on the same
+//     device (after cudaDeviceReset, or a driver-API context made current by
+//     the caller) loads the library's module again, possibly at another
+//     address, and is looked up again on its first call.
 #include <cudaTypedefs.h>
 
 #include <mutex>

@@ -388,10 +388,9 @@ BFP8_API bfp8_status bfp8_gemm_1x128_128x128_xq(const void *x, int64_t ldx, cons
  * overlaps on the GPU race, so order them (one stream, or events).  Nothing
  * in it needs clearing between calls.  The first call in each CUDA context
  * (normally once per device) looks the array's address up with that device
- * current and keeps it for that context; make that call before any stream
- * capture.  A new context on the same device (after cudaDeviceReset, or a
- * driver-API context the caller made current) is looked up again on its
- * first call.  Allocates nothing.  Errors: BFP8_ERR_INVALID_ARG (sizes,
+ * current and keeps it for that context.  A new context on the same device
+ * (after cudaDeviceReset, or a driver-API context the caller made current) is
+ * looked up again on its first call.  Allocates nothing.  Errors: BFP8_ERR_INVALID_ARG (sizes,
  * null pointers), BFP8_ERR_UNSUPPORTED (not sm_103), BFP8_ERR_CUDA (the
  * lookup or a launch failed).
  */
