@@ -1103,6 +1103,11 @@ void replay_tile(int64_t T, int64_t C, bool rows_out, bool cols_out, int scale_k
 }
 }  // namespace
 
+int bfp8_debug_gemm_pick_bn(int64_t M, int64_t N, int col_scales, int num_sms) {
+  if (M <= 0 || N <= 0 || num_sms <= 0) return 0;
+  return gemm_pick_bn(M, N, col_scales != 0, num_sms);
+}
+
 bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, int flag, uint32_t* counts,
                                     uint32_t* scale_counts, int64_t* oob) {
   CHECK_ARG(counts && oob, "bfp8_debug_write_counts: null pointer");
@@ -1208,8 +1213,8 @@ bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, i
         const int G = epi_group(bn, ew);
         for (int e = 0; e < ew; ++e)
           for (int lane = 0; lane < 32 && (gemm_a_rows(M, bn) == kBM || e % 4 == 0); ++lane)
-            for (int sg = 0; sg < epi_cols(bn, ew) / (8 * G); ++sg)
-              for (int i = 0; i < G; ++i) {
+            for (int sg = 0; sg < epi_passes(bn, ew); ++sg)
+              for (int i = 0; i < G && G * sg + lane % G < epi_chunks(bn, ew); ++i) {
                 const int64_t m = g.m0 + epi_store_row(e, lane, i, G);
                 const int64_t n0 = g.n0 + epi_store_col(e, lane, sg, G, bn, ew);
                 if (m >= M) continue;

@@ -41,6 +41,8 @@
 
 #include <mutex>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -100,6 +102,8 @@ struct GemmJob {
   int64_t c_off;     // element offset of the output C[first row][n0]
 };
 
+constexpr int gcd_c(int a, int b) { return b ? gcd_c(b, a % b) : a; }
+
 template <int BN, int STAGES, int EW, int A_ROWS = 128>
 struct GemmCfg {
   static constexpr int kEpiWarps = EW;
@@ -129,11 +133,16 @@ struct GemmCfg {
   // columns, so that the MMAs run several K-blocks ahead of the promotion
   static constexpr int kBufs = BN >= 128 ? 2 : 512 / BN;
   static constexpr int kTmemCols = kBufs * BN;
+  // the allocation: a power of two of at least kTmemCols columns
+  static constexpr int kTmemAlloc = kTmemCols <= 256 ? 256 : 512;
   // promotion warps that hold rows of the tile: all, or with A_ROWS = 16 the
   // EW / 4 warps of tensor-memory lanes 0..31
   static constexpr int kActiveEpi = A_ROWS == 16 ? EW / 4 : EW;
-  // tile scales (1x128 x 128x128 modes) a K-block needs: one per 128 columns
-  static constexpr int kTileScales = BN >= 128 ? BN / 128 : 1;
+  // tile scales (1x128 x 128x128 modes) a K-block needs: one per 128-column
+  // block its columns touch.  Tiles start on multiples of BN, so a tile starts
+  // at most 128 - gcd(BN, 128) columns into a block (224-column tiles: 96,
+  // three blocks).
+  static constexpr int kTileScales = (128 - gcd_c(BN, 128) + BN + 127) / 128;
   static constexpr int kOffB = ((STAGES - 1) * kAStride + kABytes + 1023) / 1024 * 1024;
   static constexpr int kOffC = kOffB + STAGES * kBBytes;
   // scale ring: kScaleSlots slots of kScaleGroup K-blocks, each K-block
@@ -150,9 +159,27 @@ struct GemmCfg {
   // grouped forms only: the experts' offsets and first tiles
   static constexpr int kGroupTabBytes = 2 * (kMaxGroups + 1) * 4;
   static_assert(kSmemBytes + kGroupTabBytes <= 227 * 1024, "shared memory budget");
-  static_assert(kTmemCols >= 32 && kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0,
-                "tensor-memory allocation must be a power of two in [32, 512]");
+  static_assert(kTmemCols <= kTmemAlloc && kTmemAlloc <= 512, "tensor-memory allocation");
 };
+
+// L consecutive columns of a warp's tensor-memory lanes into r (L a multiple
+// of 8 up to 64; 24 = 16 + 8 and so on, several loads before one wait).
+template <int L>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t* r) {
+  if constexpr (L == 64) {
+    tmem_ld_32x32b_x64(taddr, *reinterpret_cast<uint32_t(*)[64]>(r));
+  } else if constexpr (L == 32) {
+    tmem_ld_32x32b_x32(taddr, *reinterpret_cast<uint32_t(*)[32]>(r));
+  } else if constexpr (L == 16) {
+    tmem_ld_32x32b_x16(taddr, *reinterpret_cast<uint32_t(*)[16]>(r));
+  } else if constexpr (L == 8) {
+    tmem_ld_32x32b_x8(taddr, *reinterpret_cast<uint32_t(*)[8]>(r));
+  } else {
+    static_assert(L % 8 == 0 && L > 16 && L < 64, "tensor-memory load width");
+    tmem_ld_cols<16>(taddr, r);
+    tmem_ld_cols<L - 16>(taddr + 16u, r + 16);
+  }
+}
 
 __device__ __forceinline__ void gemm_fail(uint32_t code, volatile int* abort_flag) {
   atomicOr(&g_gemm_error, code);
@@ -318,7 +345,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW, A_ROWS>::kThreads, 1)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemAlloc);
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -422,11 +449,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW, A_ROWS>::kThreads, 1)
         const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes + sub * Cfg::kScaleKbBytes);
         // a_s of rows m0 + 4*lane .. +3 (zero past M)
         copy_scales4(slot + 16u * lane, p.sa + (int64_t)kb * p.ldsa, g.m0 + 4 * lane, p.M, p.sa_vec);
-        if (SB_MODE == kSbCol) {  // b_s of columns n0 + 128h + 4*lane .. +3 (zero past N)
+        if (SB_MODE == kSbCol) {  // b_s of columns n0 + 128h + 4*lane .. +3 < n0 + BN (zero past N)
 #pragma unroll
-          for (int h = 0; h < BN / 128; ++h)
-            copy_scales4(slot + 512u + 512u * h + 16u * lane, p.sb + (int64_t)kb * p.ldsb, g.n0 + 128 * h + 4 * lane,
-                         p.N, p.sb_vec);
+          for (int h = 0; h < (BN + 127) / 128; ++h)
+            if (128 * h + 4 * lane < BN)
+              copy_scales4(slot + 512u + 512u * h + 16u * lane, p.sb + (int64_t)kb * p.ldsb, g.n0 + 128 * h + 4 * lane,
+                           p.N, p.sb_vec);
         } else if (lane < Cfg::kTileScales) {  // tile scale of the 128 columns n0 + 128*lane (zero past N)
           const int nb = g.n0 / kBlock + lane;
           const bool in = nb < p.Nb;
@@ -481,6 +509,45 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW, A_ROWS>::kThreads, 1)
         const float scale = sa_cur * sb_cur;
         const uint64_t scale2 = f2_pack(scale, scale);
         const uint32_t taddr = tmem_base + lane_base + (uint32_t)(buf * BN + col0);
+        if constexpr (kCols % LDW != 0) {
+          // 224-column tiles (column scales): a warp's 56 columns are
+          // segments of LDW columns and a last one of kCols % LDW, one
+          // tensor-memory round trip each
+          static_assert(kCols == 56 && BN == 224 && SB_MODE == kSbCol, "segmented promotion: 224-column tiles");
+          auto segment = [&](auto len, int c0, bool last) {
+            constexpr int L = decltype(len)::value;
+            uint32_t r[L];
+            tmem_ld_cols<L>(taddr + (uint32_t)c0, r);
+            tmem_ld_wait();
+            tmem_regs_after_wait(r);
+            if (last) {
+              // this warp's share of the partial is in registers: release the buffer
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(tempty_bar(buf));
+            }
+            // acc[n] += (a_s * b_s[n]) * P[n] on fp32x2 lanes, as below
+            const uint64_t sa2 = f2_pack(sa_cur, sa_cur);
+#pragma unroll
+            for (int j4 = 0; j4 < L / 4; ++j4) {
+              float4 sb4;
+              asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                           : "=f"(sb4.x), "=f"(sb4.y), "=f"(sb4.z), "=f"(sb4.w)
+                           : "r"(slot + 512u + 4u * (uint32_t)(col0 + c0 + 4 * j4)));
+              const uint64_t t2[2] = {f2_mul(sa2, f2_pack(sb4.x, sb4.y)), f2_mul(sa2, f2_pack(sb4.z, sb4.w))};
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const int j = c0 + 4 * j4 + 2 * h;
+                const uint64_t p2 =
+                    f2_pack(__uint_as_float(r[4 * j4 + 2 * h]), __uint_as_float(r[4 * j4 + 2 * h + 1]));
+                f2_unpack(f2_fma(t2[h], p2, f2_pack(acc[j], acc[j + 1])), acc[j], acc[j + 1]);
+              }
+            }
+          };
+#pragma unroll
+          for (int c = 0; c < kCols / LDW; ++c) segment(std::integral_constant<int, LDW>{}, LDW * c, false);
+          segment(std::integral_constant<int, kCols % LDW>{}, kCols / LDW * LDW, true);
+        } else {
         // LDW columns of the partial per tensor-memory load round trip (one wait)
 #pragma unroll
         for (int c = 0; c < kCols / LDW; ++c) {
@@ -526,6 +593,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW, A_ROWS>::kThreads, 1)
             }
           }
         }
+        }
         // the slot's scales are no longer needed by this warp (end of its group)
         if (sub == Cfg::kScaleGroup - 1 || (last_tile && kb == p.Kb - 1)) {
           __syncwarp();
@@ -540,16 +608,21 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW, A_ROWS>::kThreads, 1)
       // the warp then writes 32/G row segments of 16*G contiguous bytes.  Only
       // rows < M and columns < N are written.
       {
-        constexpr int kG = kCols / 8 >= 8 ? 8 : kCols / 8;  // chunks per transposed block (epi_group)
+        // chunks per transposed block and passes (epi_group, epi_passes): a
+        // share of 56 columns is 7 chunks in one block of 8, the eighth empty
+        constexpr int kChunks = kCols / 8;
+        constexpr int kG = kChunks > 4 ? 8 : kChunks > 2 ? 4 : kChunks;
         const int pos = lane % kG;
 #pragma unroll
-        for (int sg = 0; sg < kCols / (8 * kG); ++sg) {
+        for (int sg = 0; sg < (kChunks + kG - 1) / kG; ++sg) {
           uint32_t X[kG][4];
 #pragma unroll
           for (int j = 0; j < kG; ++j)
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              X[j][q] = pack_bf16x2(acc[8 * (kG * sg + j) + 2 * q], acc[8 * (kG * sg + j) + 2 * q + 1]);
+              X[j][q] = kG * sg + j < kChunks
+                            ? pack_bf16x2(acc[8 * (kG * sg + j) + 2 * q], acc[8 * (kG * sg + j) + 2 * q + 1])
+                            : 0u;
 #pragma unroll
           for (int msk = kG / 2; msk >= 1; msk >>= 1) {
             const bool hi = (pos & msk) != 0;
@@ -566,10 +639,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW, A_ROWS>::kThreads, 1)
             }
           }
           const int n = g.n0 + epi_store_col(e, lane, sg, kG, BN, EW);
+          const bool has_chunk = kG * sg + pos < kChunks;
 #pragma unroll
           for (int i = 0; i < kG; ++i) {
             const int mr = g.m0 + epi_store_row(e, lane, i, kG);
-            if (mr >= p.M || n >= p.N) continue;
+            if (!has_chunk || mr >= p.M || n >= p.N) continue;
             uint16_t* dst = p.c + (int64_t)mr * p.ldc + n;
             if (p.c_vec && n + 8 <= p.N) {
               *reinterpret_cast<uint4*>(dst) = make_uint4(X[i][0], X[i][1], X[i][2], X[i][3]);
@@ -589,7 +663,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW, A_ROWS>::kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    tmem_dealloc(tmem_base, Cfg::kTmemAlloc);
   }
 }
 
@@ -656,7 +730,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemAlloc);
     tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
@@ -941,7 +1015,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    tmem_dealloc(tmem_base, Cfg::kTmemAlloc);
   }
 }
 
@@ -1437,7 +1511,17 @@ int gemm_pick_bn(int64_t M, int64_t N, bool col_scales, int num_sms) {
   if (!col_scales && 2 * cdiv(M, kBM) * cdiv(N, 128) <= num_sms) return 64;
   if (N <= 128) return 128;
   const int64_t tiles256 = cdiv(M, kBM) * cdiv(N, 256);
-  return tiles256 >= num_sms ? 256 : 128;
+  if (tiles256 < num_sms) return 128;
+  // The 1x128 x 128x1 GEMM takes 224-column tiles where they fill the last
+  // wave of SMs better: a tile's time taken as proportional to its width, 224
+  // is chosen when its waves x width come out at least 5% below 256's (4096 x
+  // 4096: 608 tiles = 4 whole waves of 152 against 3.37 of 256 columns).
+  // (Measured: 4096 x 4096 x 8192 154 vs 164 us.  The 1x128 x 128x128 GEMMs
+  // measured slower with them, 2048 x 4096 x 4096 43.6 vs 41.6 us.)
+  if (!col_scales) return 256;
+  const int64_t tiles224 = cdiv(M, kBM) * cdiv(N, 224);
+  const int64_t cost256 = cdiv(tiles256, num_sms) * 256, cost224 = cdiv(tiles224, num_sms) * 224;
+  return cost224 * 20 <= cost256 * 19 ? 224 : 256;
 }
 
 int64_t gemm_grid(int64_t M, int64_t N, int bn, int num_sms) {
@@ -1454,11 +1538,11 @@ int64_t gemm_grid(int64_t M, int64_t N, int bn, int num_sms) {
 // promotion warps' registers).
 template <int MODE, int BN>
 constexpr int gemm_ew() {
-  return (MODE == kSbCol || BN == 256) ? 16 : 8;  // = gemm_epi_warps(MODE == kSbCol, BN), which the host replay uses
+  return (MODE == kSbCol || BN >= 224) ? 16 : 8;  // = gemm_epi_warps(MODE == kSbCol, BN), which the host replay uses
 }
 template <int BN, int MODE, int EW>
 constexpr int gemm_ldw() {
-  return EW == 16 ? (BN == 256 && MODE != kSbCol ? 32 : 16) : (MODE != kSbCol ? (BN >= 128 ? 64 : BN / 2) : 32);
+  return EW == 16 ? (BN >= 224 && MODE != kSbCol ? 32 : 16) : (MODE != kSbCol ? (BN >= 128 ? 64 : BN / 2) : 32);
 }
 
 template <int BN, int STAGES, int MODE, int GROUP = kGroupNone, int A_ROWS = 128>
@@ -1532,6 +1616,8 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const c
                : run_gemm<64, 16, kSbTileT, kGroupNone, 16>(ma, mb, p, grid, st);
     return t ? run_gemm<64, 8, kSbTile>(ma, mb, p, grid, st) : run_gemm<64, 8, kSbTileT>(ma, mb, p, grid, st);
   }
+  // 224-column tiles (the 1x128 x 128x1 GEMM only): three stages of 44 KiB
+  if (bn == 224) return run_gemm<224, 3, kSbCol>(ma, mb, p, grid, st);
   // 256-column tiles: three stages of 48 KiB (four measured no faster, and a
   // little slower for the weight gradient)
   if (bn == 256) {

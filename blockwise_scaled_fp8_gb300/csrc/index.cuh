@@ -160,9 +160,9 @@ BFP8_HD int group_of_tile(const int* start, int E, int t) {
 // Promotion / epilogue warp e (0-based, CTA warp id = e + 4) of `ew` (8 or
 // 16): tensor-memory lane quarter e % 4 (the quarter a warp may access is its
 // CTA warp id % 4), column block e / 4 of epi_cols(bn, ew) columns.  The
-// 1x128 x 128x128 GEMMs use 8 promotion warps (16 with 256-column tiles),
-// the 1x128 x 128x1 GEMM 16.
-BFP8_HD int gemm_epi_warps(bool col_scales, int bn) { return (col_scales || bn == 256) ? 16 : 8; }
+// 1x128 x 128x128 GEMMs use 8 promotion warps (16 with 224- and 256-column
+// tiles), the 1x128 x 128x1 GEMM 16.
+BFP8_HD int gemm_epi_warps(bool col_scales, int bn) { return (col_scales || bn >= 224) ? 16 : 8; }
 // Rows of A one pipeline stage loads: 16 for the 64-column tiles of problems
 // of at most 16 rows, else 128.  With 16, only the promotion warps of lane
 // quarter 0 (e % 4 == 0) hold rows of the problem; the others store nothing.
@@ -171,10 +171,17 @@ BFP8_HD int epi_row(int e, int lane) { return 32 * (e % 4) + lane; }
 BFP8_HD int epi_cols(int bn, int ew) { return bn / (ew / 4); }
 BFP8_HD int epi_col0(int e, int bn, int ew) { return epi_cols(bn, ew) * (e / 4); }
 // Epilogue stores: G x G blocks of 16-byte (8-column) chunks are transposed
-// within groups of G lanes, G = min(8, epi_cols / 8); in pass sg, lane (grp =
+// within groups of G lanes, G = the warp's chunk count epi_cols / 8 rounded up
+// to a power of two, at most 8; in pass sg (of epi_passes), lane (grp =
 // lane / G, pos = lane % G) stores chunk G*sg + pos of tile rows
-// 32*(e%4) + G*grp + i, i < G.
-BFP8_HD int epi_group(int bn, int ew) { return epi_cols(bn, ew) / 8 >= 8 ? 8 : epi_cols(bn, ew) / 8; }
+// 32*(e%4) + G*grp + i, i < G, if that chunk exists (a share of 56 columns has
+// 7 chunks: the eighth position of each group stores nothing).
+BFP8_HD int epi_chunks(int bn, int ew) { return epi_cols(bn, ew) / 8; }
+BFP8_HD int epi_group(int bn, int ew) {
+  const int c = epi_chunks(bn, ew);
+  return c > 4 ? 8 : c > 2 ? 4 : c;
+}
+BFP8_HD int epi_passes(int bn, int ew) { return (epi_chunks(bn, ew) + epi_group(bn, ew) - 1) / epi_group(bn, ew); }
 BFP8_HD int epi_store_row(int e, int lane, int i, int G) { return 32 * (e % 4) + G * (lane / G) + i; }
 BFP8_HD int epi_store_col(int e, int lane, int sg, int G, int bn, int ew) {
   return epi_col0(e, bn, ew) + 8 * (G * sg + lane % G);

@@ -449,6 +449,14 @@ BFP8_API bfp8_status bfp8_debug_gemm_stall(const void *qa, int64_t lda, const fl
 BFP8_API bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, int flag,
                                     uint32_t *counts, uint32_t *scale_counts, int64_t *oob);
 
+/*
+ * Host test hook: the output tile width (64, 128, 224 or 256 columns) the
+ * GEMM launcher picks for an M x N output on a GPU of num_sms SMs
+ * (col_scales != 0: the 1x128 x 128x1 GEMM).  Pure host arithmetic; returns
+ * the width, or 0 for a non-positive size.
+ */
+BFP8_API int bfp8_debug_gemm_pick_bn(int64_t M, int64_t N, int col_scales, int num_sms);
+
 #ifdef __cplusplus
 }
 #endif

@@ -274,10 +274,26 @@ def test_quant_dual_index_replay_exactly_once(M, N, K):
 
 @pytest.mark.parametrize("M,N,K", SHAPES + [(128, 2048, 2048), (300, 384, 4096), (2, 5120, 1280), (64, 1000, 2048),
                                              (4096, 4096, 128), (2048, 4096, 128), (16384, 1024, 128),
-                                             (2048, 4096, 4096), (2000, 4000, 520), (4096, 4096, 8192)])
+                                             (2048, 4096, 4096), (2000, 4000, 520), (4096, 4096, 8192),
+                                             (2048, 4100, 256), (1900, 4090, 128)])
 @pytest.mark.parametrize("col_scales", [0, 8])
 def test_gemm_epilogue_index_replay_exactly_once(M, N, K, col_scales):
     """The persistent tile schedule stores each output element once (both
     promotion-warp layouts)."""
     c, _, oob = B.debug_write_counts(3, M, N, K, col_scales)
     assert oob == 0 and np.all(c == 1)
+
+
+def test_gemm_tile_width_choice():
+    """Tile widths the launcher picks (host logic, 152 SMs): narrow 64-column
+    tiles for problems that fill few SMs (1x128 x 128x128 only), 224 columns
+    for the 1x128 x 128x1 GEMM where they fill the last wave of SMs better
+    than 256, else 256 or 128."""
+    pick = lambda M, N, col=False: B.lib().bfp8_debug_gemm_pick_bn(M, N, int(col), 152)
+    assert pick(2, 4096) == 64 and pick(128, 5120) == 64       # 32 / 40 tiles of 128: narrow
+    assert pick(2, 4096, True) == 128                          # the 128x1 GEMM never narrows
+    assert pick(2048, 4096) == 256 and pick(2048, 4096, True) == 224   # 256 tiles = 1.68 waves; 304 = 2
+    assert pick(4096, 4096, True) == 224                       # 512 tiles = 3.37 waves; 608 = 4
+    assert pick(16384, 14336) == 256 and pick(14336, 4096, True) == 256   # many waves: 256 kept
+    assert pick(16384, 4096) == 256 and pick(8192, 8192) == 256
+    assert pick(512, 4096) == 128                              # 64 tiles of 256 < 152 SMs
