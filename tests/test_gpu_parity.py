@@ -376,8 +376,10 @@ def test_gemm_random_codes_matches_oracle(M, N, K, mode):
 
 
 # shapes with more tiles than SMs on a 152-SM GB300 and a partly idle last
-# wave: persistent CTAs walk several tiles each; launched twice in a row
-MULTIWAVE_SHAPES = [(2048, 4096, 512), (2000, 4000, 520), (1200, 4096, 384), (2048, 4096, 4096)]
+# wave: persistent CTAs walk several tiles each; launched twice in a row.
+# The 1x128 x 128x1 GEMM takes 224-column tiles at all of them (4052: a last
+# tile of 20 columns, less than one promotion warp's 56)
+MULTIWAVE_SHAPES = [(2048, 4096, 512), (2000, 4000, 520), (1200, 4096, 384), (2048, 4096, 4096), (1600, 4052, 256)]
 
 
 @pytest.mark.parametrize("M,N,K", MULTIWAVE_SHAPES)
