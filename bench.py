@@ -518,6 +518,73 @@ def run_only(args, wl, torch, B, dev, todev, flush):
     return 0
 
 
+def run_ceiling(args, wl, torch, dev, flush):
+    """A measured ceiling, not a result of this library: the vendor library's
+    FP8 GEMM (`torch._scaled_mm`, cuBLASLt) at the workload's three GEMM
+    shapes, tensorwise-scaled (one fp32 scale per operand, no per-block
+    promotion), and block-scaled (1x128 x 128x128 fp32 scales) where this
+    torch build accepts such scales.  Random e4m3 operands; L2 flushed before
+    every call, CUDA events, median of --steps calls after --warmup."""
+    M, N, K = wl.M, wl.N, wl.K
+    shapes = {"gemm_fwd": (M, N, K), "gemm_dgrad": (M, K, N), "gemm_wgrad": (N, K, M)}
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(0)
+    steps = max(5, min(args.steps, 50))
+
+    def timed(f):
+        for _ in range(args.warmup):
+            f()
+        ts = []
+        for _ in range(steps):
+            flush.fill_(1.0)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            f()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ts.sort()
+        return ts[len(ts) // 2] * 1e3
+
+    out = {}
+    for name, (m, n, k) in shapes.items():
+        a = (torch.randn(m, k, device=dev, generator=gen) * 0.5).to(torch.float8_e4m3fn)
+        b = (torch.randn(n, k, device=dev, generator=gen) * 0.5).to(torch.float8_e4m3fn)
+        one = torch.ones((), dtype=torch.float32, device=dev)
+        flops = 2.0 * m * n * k
+        rec = {"M": m, "N": n, "K": k}
+        us = timed(lambda: torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16))
+        rec["tensorwise_us"] = round(us, 1)
+        rec["tensorwise_TFLOP/s"] = round(flops / (us / 1e6) / 1e12, 1)
+        kb, nb = (k + 127) // 128, (n + 127) // 128
+        # candidate layouts for 1x128 (A) and 128x128 (B) scales; the first one this build accepts is timed
+        cands = [("a [M,Kb] outer-major, b [Nb,Kb]",
+                  torch.rand(kb, m, device=dev).t(), torch.rand(nb, kb, device=dev)),
+                 ("a [M,Kb] outer-major, b [Kb,Nb] outer-major",
+                  torch.rand(kb, m, device=dev).t(), torch.rand(nb, kb, device=dev).t()),
+                 ("a [M,Kb], b [Nb,Kb]", torch.rand(m, kb, device=dev), torch.rand(nb, kb, device=dev))]
+        rec["blockwise"] = "not accepted by this build"
+        errors = []
+        for label, sa, sb in cands:
+            try:
+                torch._scaled_mm(a, b.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16)
+                torch.cuda.synchronize()
+            except Exception as e:  # this build rejects the layout (a host-side check)
+                errors.append(f"{label}: {str(e).splitlines()[0][:120]}")
+                continue
+            us = timed(lambda: torch._scaled_mm(a, b.t(), scale_a=sa, scale_b=sb, out_dtype=torch.bfloat16))
+            rec["blockwise"] = {"scales": label, "us": round(us, 1),
+                                "TFLOP/s": round(flops / (us / 1e6) / 1e12, 1)}
+            break
+        if errors and not isinstance(rec["blockwise"], dict):
+            rec["blockwise_errors"] = errors
+        out[name] = rec
+    print(json.dumps({"ceiling": "torch._scaled_mm (cuBLASLt FP8), a measured reference point, not this library",
+                      "workload": wl.name, "torch": torch.__version__, "steps": steps, "warmup": args.warmup,
+                      "gemms": out}), flush=True)
+    return 0
+
+
 def run_gpu(args, wl):
     import torch
 
@@ -537,6 +604,8 @@ def run_gpu(args, wl):
         return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
 
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    if args.ceiling:
+        return run_ceiling(args, wl, torch, dev, flush)
     if args.only:
         return run_only(args, wl, torch, B, dev, todev, flush)
     xh, wh, dyh = wl.x(), wl.w(), wl.dy()
@@ -720,6 +789,9 @@ def main():
     ap.add_argument("--chunk-n", type=int, default=0,
                     help="columns of W / dY per chunk of the host-buffer step (0 = automatic)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ceiling", action="store_true",
+                    help="time the vendor library's FP8 GEMM (torch._scaled_mm) at the workload's GEMM shapes "
+                         "as a measured ceiling, and nothing else")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
