@@ -391,8 +391,9 @@ def test_gemm_multiwave_matches_oracle(M, N, K, mode):
 
 
 # few output tiles and a deep K: most SMs idle, one CTA walks every K-block of
-# its tile; ragged M and N
-DEEP_K_SHAPES = [(128, 2048, 2048), (300, 384, 4096), (2, 5120, 1280), (64, 1000, 2048)]
+# its tile; ragged M and N (the tile-scale GEMMs take 64-column tiles here,
+# with 16-row A boxes for M <= 16; (3, 12288): 128-column tiles, M <= 16)
+DEEP_K_SHAPES = [(128, 2048, 2048), (300, 384, 4096), (2, 5120, 1280), (64, 1000, 2048), (3, 12288, 1024)]
 
 
 @pytest.mark.parametrize("M,N,K", DEEP_K_SHAPES)

@@ -33,6 +33,9 @@ def _setup():
 
 SMALL_M = [(m, n, k) for m in (2, 4, 128, 512) for (n, k) in ((512, 128), (5120, 1280), (3584, 640), (4096, 4096))]
 TAILS = [(1, 130, 256), (3, 384, 136), (130, 300, 520), (257, 1000, 1024), (64, 2051, 128), (300, 640, 4096)]
+# M <= 16 with enough columns that 128-column tiles fill more than half the
+# SMs: 16-row x tiles with 128-column tiles instead of the narrow 64-column ones
+WIDE = [(4, 12288, 256), (16, 9856, 520)]
 
 
 def _guarded_out(M, N, ldc):
@@ -40,7 +43,7 @@ def _guarded_out(M, N, ldc):
     return flat, flat[GUARD:GUARD + M * ldc].view(M, ldc).view(torch.bfloat16)
 
 
-@pytest.mark.parametrize("M,N,K", SMALL_M + TAILS)
+@pytest.mark.parametrize("M,N,K", SMALL_M + TAILS + WIDE)
 def test_xq_forward_bit_exact_with_two_launch_path_and_oracle(M, N, K):
     x = S.normal_bf16((M, K), 1.0, seed=M * 7 + K, outlier_frac=1e-3)
     w = S.normal_bf16((N, K), 0.02, seed=N * 5 + K)
