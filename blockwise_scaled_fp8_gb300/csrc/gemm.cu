@@ -140,8 +140,8 @@ struct GemmCfg {
   static constexpr int kActiveEpi = A_ROWS == 16 ? EW / 4 : EW;
   // tile scales (1x128 x 128x128 modes) a K-block needs: one per 128-column
   // block its columns touch.  Tiles start on multiples of BN, so a tile starts
-  // at most 128 - gcd(BN, 128) columns into a block: 128 and 256 columns
-  // start on a block (one and two blocks), 64 at most 64 in (one block).
+  // at most 128 - gcd(BN, 128) columns into a block (224-column tiles: 96,
+  // three blocks).
   static constexpr int kTileScales = (128 - gcd_c(BN, 128) + BN + 127) / 128;
   static constexpr int kOffB = ((STAGES - 1) * kAStride + kABytes + 1023) / 1024 * 1024;
   static constexpr int kOffC = kOffB + STAGES * kBBytes;
