@@ -27,7 +27,7 @@ EXPORTS = [
     "bfp8_linear_fwd_static", "bfp8_gemm_grouped_1x128_128x128", "bfp8_gemm_grouped_1x128_128x1",
     "bfp8_quant_dual_weight", "bfp8_mx_cast", "bfp8_linear_step_host_workspace_size",
     "bfp8_linear_step_host", "bfp8_moe_step_host_workspace_size", "bfp8_moe_step_host",
-    "bfp8_gemm_1x128_128x128_xq",
+    "bfp8_gemm_1x128_128x128_xq", "bfp8_gemm_1x128_128x1_xq",
 ]
 
 _lib = None
@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
     L.bfp8_moe_step_host.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, i64, i64, i64, i64, vp, sz, vp]
     L.bfp8_linear_fwd_static.argtypes = [vp, vp, vp, i64, i64, i64, vp]
     L.bfp8_gemm_1x128_128x128_xq.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, i64, vp]
+    L.bfp8_gemm_1x128_128x1_xq.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i64, i64, i64, vp]
     L.bfp8_gemm_grouped_1x128_128x128.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, i32, vp, i64, vp, i64,
                                                   i64, i64, i64, vp]
     L.bfp8_gemm_grouped_1x128_128x1.argtypes = [vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp, i64, i64,
@@ -310,6 +311,22 @@ def gemm_1x128_128x128_xq(x, qb, sb, out=None, N=None):
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     _check(lib().bfp8_gemm_1x128_128x128_xq(_p(x), x.stride(0), _p(qb), qb.stride(0), _p(sb), sb.stride(0),
                                             _p(out), out.stride(0), M, N, K, _stream()))
+    return out
+
+
+def gemm_1x128_128x1_xq(qa, sa, x, out=None, M=None):
+    """C = A quant_rhs(x) with A = qa [M, lda] (1x128 scales sa [Kb, ldsa])
+    and x bf16 [K, N] quantised 128x1 inside the GEMM (one launch; the weight
+    gradient dW = dY^T X with qa, sa the transposed 1x128 quantisation of dY).
+    Returns C [M, N] bf16."""
+    torch = _torch()
+    _need_bf16_2d(x, "x")
+    K, N = x.shape
+    M = qa.shape[0] if M is None else M
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _check(lib().bfp8_gemm_1x128_128x1_xq(_p(qa), qa.stride(0), _p(sa), sa.stride(0), _p(x), x.stride(0),
+                                          _p(out), out.stride(0), M, N, K, _stream()))
     return out
 
 

@@ -381,6 +381,40 @@ bfp8_status bfp8_gemm_1x128_128x128_xq(const void* x, int64_t ldx, const void* q
   return BFP8_OK;
 }
 
+bfp8_status bfp8_gemm_1x128_128x1_xq(const void* qa, int64_t lda, const float* sa, int64_t ldsa, const void* x,
+                                     int64_t ldx, void* c, int64_t ldc, int64_t M, int64_t N, int64_t K,
+                                     bfp8_stream_t stream) {
+  const char* fn = "bfp8_gemm_1x128_128x1_xq";
+  bfp8_status st = check_dims(fn, M, N, K);
+  if (st != BFP8_OK) return st;
+  if (M == 0 || N == 0) return BFP8_OK;
+  CHECK_ARG(c, "%s: null pointer", fn);
+  if (K == 0) {  // empty reduction (qa, sa, x are not read): C = 0 on the logical [M,N] region
+    CHECK_ARG(ldc >= N, "%s: ldc=%lld < N=%lld", fn, (long long)ldc, (long long)N);
+    cudaError_t e = cudaMemset2DAsync(c, (size_t)ldc * 2, 0, (size_t)N * 2, (size_t)M, (cudaStream_t)stream);
+    return e == cudaSuccess ? BFP8_OK : cuda_fail(e, fn);
+  }
+  CHECK_ARG(qa && sa && x, "%s: null pointer", fn);
+  CHECK_ARG(al16(qa) && al16(x), "%s: qa and x must be 16-byte aligned", fn);
+  CHECK_ARG(al4(sa) && al2(c), "%s: sa must be 4-byte and c 2-byte aligned", fn);
+  CHECK_ARG(lda >= K && lda % 16 == 0, "%s: lda=%lld must be >= K=%lld and a multiple of 16", fn, (long long)lda,
+            (long long)K);
+  CHECK_ARG(ldsa >= M, "%s: ldsa=%lld < M=%lld", fn, (long long)ldsa, (long long)M);
+  CHECK_ARG(ldx >= N && ldx % 8 == 0, "%s: ldx=%lld must be >= N=%lld and a multiple of 8", fn, (long long)ldx,
+            (long long)N);
+  CHECK_ARG(ldc >= N, "%s: ldc=%lld < N=%lld", fn, (long long)ldc, (long long)N);
+  int sms = 0;
+  if ((st = check_device(&sms)) != BFP8_OK) return st;
+  const char* msg = nullptr;
+  cudaError_t e = launch_gemm_wgrad_xq(GemmWxqArgs{qa, lda, sa, ldsa, x, ldx, c, ldc, M, N, K}, sms,
+                                       (cudaStream_t)stream, &msg);
+  if (e != cudaSuccess) {
+    if (msg) return fail(BFP8_ERR_INVALID_ARG, "%s: %s", fn, msg);
+    return cuda_fail(e, fn);
+  }
+  return BFP8_OK;
+}
+
 // ---------------------------------------------------------------------------
 // Grouped (mixture-of-experts) GEMMs
 // ---------------------------------------------------------------------------

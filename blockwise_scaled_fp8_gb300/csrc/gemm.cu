@@ -1469,6 +1469,476 @@ __global__ void __launch_bounds__(XqCfg<BN, STAGES, RAW_ROWS>::kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// The weight-gradient GEMM (1x128 x 128x1) with its rhs quantised inside the
+// kernel: B arrives as the bf16 activation X[K tokens, N features] and a
+// quantiser warpgroup forms, per K-block, each feature column's 128x1 group
+// maximum over the block's 128 tokens, its scale and the e4m3 codes, written
+// transposed (K-major, the layout the MMA reads) into the stage, with the
+// quantisation kernels' arithmetic: the result equals quant_rhs followed by
+// the 1x128 x 128x1 GEMM bit for bit.  This is the optional fused
+// quantisation in the GEMM prologue for the weight gradient's rhs that the
+// method allows ("Enable blockwise FP8 dense training kernels on ROCm":
+// act_quant_rhs 128x1 and the 1x128 x 128x1 GEMM); every 128-row tile of the
+// output quantises the X columns it reads again, so it trades the separate
+// quantisation's HBM round trip for ceil(M/128)-fold quantisation work.
+//
+//   warp 0      producer: raw X tiles (two 64-feature boxes of 128 tokens)
+//               into a four-slot ring, A tiles (dY^T codes) into the stages
+//   warps 1, 3  MMA issuers on alternate K-blocks, each waiting for the
+//               stage's A bytes and its quantised B
+//   warp 2      a_s of each K-block into the scale ring
+//   warps 4-7   quantisers, two halves taking alternate K-blocks: in a half,
+//               warp w takes features 64w..64w+63, lane (chunk j, token
+//               group g) the 8 features 8j..8j+7 over tokens 32g..32g+31;
+//               the four token groups of a chunk combine their maxima by
+//               shuffles; codes are transposed with byte permutes and stored
+//               16 tokens at a time; b_s goes into a ring the promotion reads
+//   warps 8-15  promotion (per-column scales) + epilogue, as the dense kernel
+// ---------------------------------------------------------------------------
+struct WxqCfg {
+  static constexpr int BN = 128;
+  static constexpr int kStages = 2;   // A and quantised-B stages
+  static constexpr int kRawSlots = 4; // raw X tiles (two per quantiser half)
+  static constexpr int kBufs = 4;     // 128-column fp32 partial buffers in tensor memory
+  static constexpr int kTmemCols = kBufs * BN;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kCols = BN / (kEpiWarps / 4);  // 64 columns per promotion thread
+  static constexpr int kThreads = 128 + 128 + 32 * kEpiWarps;  // 512
+  // registers: 128 per thread at launch; control 56, quantisers 96, promotion 176
+  static constexpr int kCtrlRegs = 56, kQuantRegs = 96, kEpiRegs = 176;
+  static_assert(128 * kCtrlRegs + 128 * kQuantRegs + 32 * kEpiWarps * kEpiRegs <= kThreads * 128, "register split");
+  static constexpr int kABytes = kBM * kBK;      // 16 KiB
+  static constexpr int kBBytes = BN * kBK;       // 16 KiB of codes
+  static constexpr int kRawBytes = kBK * BN * 2; // 128 tokens x 128 features bf16 = 32 KiB
+  static constexpr int kOffB = kStages * kABytes;
+  static constexpr int kOffRaw = kOffB + kStages * kBBytes;
+  static constexpr int kScaleSlots = 2, kScaleGroup = 4;
+  static constexpr int kScaleKbBytes = kBM * 4;  // a_s of the K-block's 128 rows
+  static constexpr int kScaleBytes = kScaleGroup * kScaleKbBytes;
+  static constexpr int kOffScale = kOffRaw + kRawSlots * kRawBytes;
+  // b_s of each K-block, written by the quantisers into a ring of kBsSlots
+  // entries.  A quantiser writes entry `it` after the MMAs of K-block
+  // it - kStages completed; those were issued after the promotion released
+  // the buffer of K-block it - kStages - kBufs, which each promotion warp does
+  // only after its last read of that K-block's b_s.  So the entry's previous
+  // K-block (it - kBsSlots) has been read by then.
+  static constexpr int kBsSlots = 8;
+  static_assert(kBsSlots >= kStages + kBufs, "b_s ring depth");
+  static constexpr int kOffBs = kOffScale + kScaleSlots * kScaleBytes;
+  static constexpr int kOffBar = kOffBs + kBsSlots * BN * 4;
+  // full[S] empty[S] bfull[S] rfull[R] rempty[R] tfull[T] tempty[T] drain stall sfull[2] sempty[2]
+  static constexpr int kNumBars = 3 * kStages + 2 * kRawSlots + 2 * kBufs + 2 + 2 * kScaleSlots;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+__global__ void __launch_bounds__(WxqCfg::kThreads, 1)
+    gemm_wgrad_xq_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_x,
+                         const GemmParams p) {
+  using Cfg = WxqCfg;
+  constexpr int BN = Cfg::BN, S = Cfg::kStages, NR = Cfg::kRawSlots, NT = Cfg::kBufs;
+  constexpr int EW = Cfg::kEpiWarps, kCols = Cfg::kCols, LDW = 32;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sA = sbase, sB = sbase + Cfg::kOffB, sRaw = sbase + Cfg::kOffRaw;
+  const uint32_t sScale = sbase + Cfg::kOffScale, sBs = sbase + Cfg::kOffBs;
+  const uint32_t bar0 = sbase + Cfg::kOffBar;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
+  volatile int* never = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
+
+  auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(S + i); };
+  auto bfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * S + i); };
+  auto rfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * S + i); };
+  auto rempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * S + NR + i); };
+  auto tfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * S + 2 * NR + i); };
+  auto tempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * S + 2 * NR + NT + i); };
+  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(3 * S + 2 * NR + 2 * NT);
+  const uint32_t stall_bar = drain_bar + 8u;  // never arrived on
+  auto sfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * S + 2 * NR + 2 * NT + 2 + i); };
+  auto sempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * S + 2 * NR + 2 * NT + 4 + i); };
+
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+  const int lane = (int)(threadIdx.x & 31);
+  pdl_launch_dependents();
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), 1);
+      mbar_init(bfull_bar(i), 64);  // every thread of the quantiser half that takes the stage
+    }
+    for (int i = 0; i < NR; ++i) {
+      mbar_init(rfull_bar(i), 1);
+      mbar_init(rempty_bar(i), 64);
+    }
+    for (int i = 0; i < NT; ++i) {
+      mbar_init(tfull_bar(i), 1);
+      mbar_init(tempty_bar(i), EW);
+    }
+    mbar_init(drain_bar, 2);
+    mbar_init(stall_bar, 1);
+    for (int i = 0; i < Cfg::kScaleSlots; ++i) {
+      mbar_init(sfull_bar(i), 32);  // one cp.async arrival per a_s loader lane
+      mbar_init(sempty_bar(i), EW);
+    }
+    *abort_flag = 0;
+    *never = 0;
+    fence_barrier_init();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tma_a);
+    tma_prefetch_desc(&tma_x);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  pdl_wait();  // the previous kernel's writes are visible from here on
+  const uint32_t tmem_base = *tmem_holder;
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kCtrlRegs));
+    if (warp == 0) {
+      // ---------------------------------------------------------- producer
+      if (lane == 0) {
+        uint32_t it = 0, n_raw = 0, n_a = 0;  // K-block steps; raw X and A copies issued
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+          const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+          for (int kb = 0; kb < p.Kb; ++kb, ++it) {
+            const int r = (int)(it % NR);
+            if (!mbar_wait_bounded(rempty_bar(r), ((it / NR) & 1u) ^ 1u, p.wait_limit_ns, abort_flag)) {
+              gemm_fail(kErrWaitEmpty, abort_flag);
+              ok = false;
+              break;
+            }
+            const uint32_t raw = sRaw + (uint32_t)(r * Cfg::kRawBytes);
+            mbar_arrive_expect_tx(rfull_bar(r), (uint32_t)Cfg::kRawBytes);
+            tma_load_2d(raw, &tma_x, rfull_bar(r), g.n0, kb * kBK);
+            tma_load_2d(raw + (uint32_t)(Cfg::kRawBytes / 2), &tma_x, rfull_bar(r), g.n0 + 64, kb * kBK);
+            ++n_raw;
+            const int st = (int)(it % S);
+            if (!mbar_wait_bounded(empty_bar(st), ((it / S) & 1u) ^ 1u, p.wait_limit_ns, abort_flag)) {
+              gemm_fail(kErrWaitEmpty, abort_flag);
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(full_bar(st), (uint32_t)Cfg::kABytes);
+            tma_load_2d(sA + (uint32_t)(st * Cfg::kABytes), &tma_a, full_bar(st), kb * kBK, g.m0);
+            ++n_a;
+          }
+        }
+        if (!ok) {
+          // copies already issued land before this CTA's shared memory goes away
+          for (uint32_t j = (n_raw > NR ? n_raw - NR : 0); j < n_raw; ++j)
+            if (!mbar_wait_bounded(rfull_bar((int)(j % NR)), (j / NR) & 1u, p.wait_limit_ns, never))
+              atomicOr(&g_gemm_error, kErrWaitDrain);
+          for (uint32_t j = (n_a > S ? n_a - S : 0); j < n_a; ++j)
+            if (!mbar_wait_bounded(full_bar((int)(j % S)), (j / S) & 1u, p.wait_limit_ns, never))
+              atomicOr(&g_gemm_error, kErrWaitDrain);
+        }
+      }
+    } else if (warp == 1 || warp == 3) {
+      // ---------------------------------------------------------- MMA issuers
+      if (lane == 0) {
+        constexpr uint32_t idesc = idesc_e4m3_f32(kBM, BN);
+        const uint32_t mine = warp == 1 ? 0u : 1u;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+          for (int kb = 0; kb < p.Kb; ++kb, ++it) {
+            if ((it & 1u) != mine) continue;
+            const int st = (int)(it % S);
+            const uint32_t ph = (it / S) & 1u;
+            const int buf = (int)(it % NT);
+            if (!mbar_spin_bounded(tempty_bar(buf), ((it / NT) & 1u) ^ 1u, p.wait_limit_ns, abort_flag)) {
+              gemm_fail(kErrWaitTmemEmpty, abort_flag);
+              ok = false;
+              break;
+            }
+            if (!mbar_spin_bounded(full_bar(st), ph, p.wait_limit_ns, abort_flag) ||
+                !mbar_spin_bounded(bfull_bar(st), ph, p.wait_limit_ns, abort_flag)) {
+              gemm_fail(kErrWaitFull, abort_flag);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint64_t da = desc_kmajor_sw128(sA + (uint32_t)(st * Cfg::kABytes));
+            const uint64_t db = desc_kmajor_sw128(sB + (uint32_t)(st * Cfg::kBBytes));
+            const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+#pragma unroll
+            for (int k = 0; k < kBK / 32; ++k)
+              mma_e4m3(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), idesc, k > 0 ? 1u : 0u);
+            mma_commit(empty_bar(st));
+            mma_commit(tfull_bar(buf));
+          }
+        }
+        mma_commit(drain_bar);
+        if (!mbar_wait_bounded(drain_bar, 0, p.wait_limit_ns, never)) gemm_fail(kErrWaitDrain, abort_flag);
+      }
+    } else {
+      // ---------------------------------------------------------- a_s loader (warp 2)
+      uint32_t it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+        const bool last_tile = tile + (int)gridDim.x >= p.num_tiles;
+        for (int kb = 0; kb < p.Kb; ++kb, ++it) {
+          const uint32_t grp = it / Cfg::kScaleGroup, sub = it % Cfg::kScaleGroup;
+          const int sl = (int)(grp % Cfg::kScaleSlots);
+          if (sub == 0) {
+            const bool got =
+                mbar_wait_bounded(sempty_bar(sl), ((grp / Cfg::kScaleSlots) & 1u) ^ 1u, p.wait_limit_ns, abort_flag);
+            if (!__all_sync(0xffffffffu, got)) {
+              if (lane == 0) gemm_fail(kErrWaitScale, abort_flag);
+              ok = false;
+              break;
+            }
+          }
+          const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes + sub * Cfg::kScaleKbBytes);
+          // a_s of rows m0 + 4*lane .. +3 (zero past M)
+          copy_scales4(slot + 16u * lane, p.sa + (int64_t)kb * p.ldsa, g.m0 + 4 * lane, p.M, p.sa_vec);
+          if (sub == Cfg::kScaleGroup - 1 || (last_tile && kb == p.Kb - 1)) cp_async_mbar_arrive(sfull_bar(sl));
+        }
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
+    }
+  } else if (warp < 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kQuantRegs));
+    // ------------------------------------------------------------ quantisers
+    const int qt = (int)threadIdx.x - 128;
+    const uint32_t half = (uint32_t)(qt >> 6);  // takes the K-block steps it with it % 2 == half
+    const int wq = (qt >> 5) & 1;               // features 64*wq .. +63: raw box wq
+    const int j = lane & 7;                     // features 64*wq + 8j .. +7
+    const int tg = lane >> 3;                   // tokens 32*tg .. +31 of the K-block
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int kb = 0; kb < p.Kb; ++kb, ++it) {
+        if ((it & 1u) != half) continue;
+        const int r = (int)(it % NR);
+        const int st = (int)(it % S);
+        bool got = mbar_wait_bounded(rfull_bar(r), (it / NR) & 1u, p.wait_limit_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) gemm_fail(kErrWaitFull, abort_flag);
+          ok = false;
+          break;
+        }
+        // box wq of the raw tile: token t's 64 features at t*128 bytes, 16-byte chunk c at (c ^ (t & 7))
+        const uint32_t box = sRaw + (uint32_t)(r * Cfg::kRawBytes + wq * (Cfg::kRawBytes / 2));
+        // pass 1: |x| maxima of the 8 features over this lane's 32 tokens (packed bf16 pairs)
+        uint32_t m[4] = {0u, 0u, 0u, 0u};
+#pragma unroll 8
+        for (int i = 0; i < 32; ++i) {
+          const int t = 32 * tg + i;
+          uint4 v;
+          asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                       : "r"(box + (uint32_t)(t * 128) + (uint32_t)((j ^ (t & 7)) << 4)));
+          m[0] = amax2(m[0], v.x);
+          m[1] = amax2(m[1], v.y);
+          m[2] = amax2(m[2], v.z);
+          m[3] = amax2(m[3], v.w);
+        }
+        uint64_t s2[4], ny2[4];  // (s, s') and (-1/s, -1/s') of features 8j + 2q, +1
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          m[q] = amax2(m[q], __shfl_xor_sync(0xffffffffu, m[q], 8));
+          m[q] = amax2(m[q], __shfl_xor_sync(0xffffffffu, m[q], 16));
+          const float s_lo = scale_of(__uint_as_float((m[q] << 16) & 0x7FFF0000u));
+          const float s_hi = scale_of(__uint_as_float(m[q] & 0x7FFF0000u));
+          s2[q] = f2_pack(s_lo, s_hi);
+          ny2[q] = f2_pack(neg_rcp(s_lo), neg_rcp(s_hi));
+        }
+        // the stage (its quantised-B buffer) and the b_s ring entry are free once
+        // the MMAs of K-block it - kStages completed
+        got = mbar_wait_bounded(empty_bar(st), ((it / S) & 1u) ^ 1u, p.wait_limit_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) gemm_fail(kErrWaitEmpty, abort_flag);
+          ok = false;
+          break;
+        }
+        if (tg == 0) {
+          const uint32_t bs = sBs + (uint32_t)((it % Cfg::kBsSlots) * BN * 4 + 4 * (64 * wq + 8 * j));
+          float lo[4], hi[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) f2_unpack(s2[q], lo[q], hi[q]);
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(bs), "f"(lo[0]), "f"(hi[0]), "f"(lo[1]),
+                       "f"(hi[1])
+                       : "memory");
+          asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(bs + 16u), "f"(lo[2]), "f"(hi[2]),
+                       "f"(lo[3]), "f"(hi[3])
+                       : "memory");
+        }
+        // pass 2: codes, 16 tokens at a time; feature f's 16 codes are one 16-byte chunk of row f
+        const uint32_t bdst = sB + (uint32_t)(st * Cfg::kBBytes);
+#pragma unroll 1
+        for (int h16 = 0; h16 < 2; ++h16) {
+          uint32_t o[8][4];
+#pragma unroll
+          for (int i4 = 0; i4 < 4; ++i4) {
+            uint4 v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int t = 32 * tg + 16 * h16 + 4 * i4 + i;
+              asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                           : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w)
+                           : "r"(box + (uint32_t)(t * 128) + (uint32_t)((j ^ (t & 7)) << 4)));
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t cc[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const uint32_t w = q == 0 ? v[i].x : q == 1 ? v[i].y : q == 2 ? v[i].z : v[i].w;
+                cc[i] = neg_codes2(w, s2[q], ny2[q]);  // byte 0: feature 8j+2q, byte 1: 8j+2q+1
+              }
+              // (t0 e, t1 e, t0 o, t1 o) and (t2 e, t3 e, t2 o, t3 o) -> the four tokens of each feature
+              const uint32_t X = __byte_perm(cc[0], cc[1], 0x5140), Y = __byte_perm(cc[2], cc[3], 0x5140);
+              o[2 * q][i4] = __byte_perm(X, Y, 0x5410) ^ 0x80808080u;
+              o[2 * q + 1][i4] = __byte_perm(X, Y, 0x7632) ^ 0x80808080u;
+            }
+          }
+          const int c = 2 * tg + h16;  // 16-byte chunk of the K-block's row
+#pragma unroll
+          for (int fi = 0; fi < 8; ++fi) {
+            const int f = 64 * wq + 8 * j + fi;
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(bdst + (uint32_t)(f * 128) +
+                                                                        (uint32_t)((c ^ (f & 7)) << 4)),
+                         "r"(o[fi][0]), "r"(o[fi][1]), "r"(o[fi][2]), "r"(o[fi][3])
+                         : "memory");
+          }
+        }
+        fence_proxy_async_shared();  // the codes, for the MMA (async proxy)
+        mbar_arrive(bfull_bar(st));
+        mbar_arrive(rempty_bar(r));
+      }
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::kEpiRegs));
+    // ------------------------------------------------------------ promotion + epilogue
+    const int e = warp - 8;
+    const int row = epi_row(e, lane);
+    const int col0 = epi_col0(e, BN, EW);
+    const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+      const bool last_tile = tile + (int)gridDim.x >= p.num_tiles;
+      float acc[kCols];
+#pragma unroll
+      for (int jj = 0; jj < kCols; ++jj) acc[jj] = 0.0f;
+      for (int kb = 0; kb < p.Kb; ++kb, ++it) {
+        const uint32_t grp = it / Cfg::kScaleGroup, sub = it % Cfg::kScaleGroup;
+        const int sl = (int)(grp % Cfg::kScaleSlots);
+        const uint32_t slot = sScale + (uint32_t)(sl * Cfg::kScaleBytes + sub * Cfg::kScaleKbBytes);
+        const bool sgot = sub != 0 || mbar_spin_bounded(sfull_bar(sl), (grp / Cfg::kScaleSlots) & 1u,
+                                                        p.wait_limit_ns, abort_flag);
+        const int buf = (int)(it % NT);
+        const bool got = sgot && mbar_wait_bounded(p.debug_stall ? stall_bar : tfull_bar(buf), (it / NT) & 1u,
+                                                   p.wait_limit_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) gemm_fail(sgot ? kErrWaitTmemFull : kErrWaitScale, abort_flag);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float sa_cur;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sa_cur) : "r"(slot + 4u * row));
+        const uint64_t sa2 = f2_pack(sa_cur, sa_cur);
+        const uint32_t bs = sBs + (uint32_t)((it % Cfg::kBsSlots) * BN * 4);
+        const uint32_t taddr = tmem_base + lane_base + (uint32_t)(buf * BN + col0);
+#pragma unroll
+        for (int c = 0; c < kCols / LDW; ++c) {
+          uint32_t rr[LDW];
+          tmem_ld_32x32b_x32(taddr + (uint32_t)(LDW * c), rr);
+          tmem_ld_wait();
+          tmem_regs_after_wait(rr);
+          // acc[n] += (a_s * b_s[n]) * P[n] on fp32x2 lanes, as the 1x128 x 128x1 GEMM
+#pragma unroll
+          for (int j4 = 0; j4 < LDW / 4; ++j4) {
+            float4 sb4;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(sb4.x), "=f"(sb4.y), "=f"(sb4.z), "=f"(sb4.w)
+                         : "r"(bs + 4u * (uint32_t)(col0 + LDW * c + 4 * j4)));
+            const uint64_t t2[2] = {f2_mul(sa2, f2_pack(sb4.x, sb4.y)), f2_mul(sa2, f2_pack(sb4.z, sb4.w))};
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int jj = LDW * c + 4 * j4 + 2 * h;
+              const uint64_t p2 = f2_pack(__uint_as_float(rr[4 * j4 + 2 * h]), __uint_as_float(rr[4 * j4 + 2 * h + 1]));
+              f2_unpack(f2_fma(t2[h], p2, f2_pack(acc[jj], acc[jj + 1])), acc[jj], acc[jj + 1]);
+            }
+          }
+        }
+        // the partial and this K-block's b_s have been read: release the buffer
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(buf));
+        if (sub == Cfg::kScaleGroup - 1 || (last_tile && kb == p.Kb - 1)) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(sempty_bar(sl));
+        }
+      }
+      if (!ok) break;
+      // epilogue (as the dense kernel): rows < M and columns < N only
+      constexpr int kG = 8;
+      const int pos = lane % kG;
+      uint32_t X[kG][4];
+#pragma unroll
+      for (int jj = 0; jj < kG; ++jj)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) X[jj][q] = pack_bf16x2(acc[8 * jj + 2 * q], acc[8 * jj + 2 * q + 1]);
+#pragma unroll
+      for (int msk = kG / 2; msk >= 1; msk >>= 1) {
+        const bool hi = (pos & msk) != 0;
+#pragma unroll
+        for (int jj = 0; jj < kG; ++jj) {
+          if (jj & msk) continue;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t send = hi ? X[jj][q] : X[jj | msk][q];
+            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, msk);
+            if (hi) X[jj][q] = recv;
+            else X[jj | msk][q] = recv;
+          }
+        }
+      }
+      const int n = g.n0 + epi_store_col(e, lane, 0, kG, BN, EW);
+#pragma unroll
+      for (int i = 0; i < kG; ++i) {
+        const int mr = g.m0 + epi_store_row(e, lane, i, kG);
+        if (mr >= p.M || n >= p.N) continue;
+        uint16_t* dst = p.c + (int64_t)mr * p.ldc + n;
+        if (p.c_vec && n + 8 <= p.N) {
+          *reinterpret_cast<uint4*>(dst) = make_uint4(X[i][0], X[i][1], X[i][2], X[i][3]);
+        } else {
+#pragma unroll
+          for (int b = 0; b < 8; ++b)
+            if (n + b < p.N) dst[b] = (uint16_t)(X[i][b >> 1] >> (16 * (b & 1)));
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 
@@ -1777,6 +2247,51 @@ cudaError_t launch_gemm_xq(const GemmXqArgs& a, int num_sms, cudaStream_t st, co
     return gemm_pick_bn(a.M, a.N, false, num_sms) == 64 ? run_gemm_xq<16, 64>(a, num_sms, st, msg)
                                                          : run_gemm_xq<16, 128>(a, num_sms, st, msg);
   return run_gemm_xq<128, 128>(a, num_sms, st, msg);
+}
+
+cudaError_t launch_gemm_wgrad_xq(const GemmWxqArgs& a, int num_sms, cudaStream_t st, const char** msg) {
+  using Cfg = WxqCfg;
+  CUtensorMap ma, mx;
+  // X [K tokens, N features]: boxes of 64 features x 128 tokens
+  if (!make_tma_u8(&ma, a.qa, a.K, a.M, a.lda, kBM) || !make_tma_bf16(&mx, a.x, a.N, a.K, a.ldx * 2, kBK)) {
+    *msg = "cuTensorMapEncodeTiled failed for an operand (alignment, stride or size out of range)";
+    return cudaErrorInvalidValue;
+  }
+  const int64_t num_m = cdiv(a.M, kBM), num_n = cdiv(a.N, Cfg::BN), Kb = cdiv(a.K, kBK);
+  if (a.M >= (int64_t)1 << 31 || a.N >= (int64_t)1 << 31 || a.K >= (int64_t)1 << 31 ||
+      num_m * num_n * Kb >= (int64_t)1 << 31) {
+    *msg = "GEMM too large: M, N, K and the number of (tile, K-block) units must stay below 2^31";
+    return cudaErrorInvalidValue;
+  }
+  GemmParams p;
+  p.sa = a.sa;
+  p.ldsa = a.ldsa;
+  p.sb = nullptr;
+  p.ldsb = 0;
+  p.c = reinterpret_cast<uint16_t*>(a.c);
+  p.ldc = a.ldc;
+  p.M = a.M;
+  p.N = a.N;
+  p.K = a.K;
+  p.num_m = (int)num_m;
+  p.num_n = (int)num_n;
+  p.num_tiles = (int)(num_m * num_n);
+  p.Kb = (int)Kb;
+  p.Nb = (int)cdiv(a.N, kBlock);
+  p.c_vec = (a.ldc % 8 == 0) && ((reinterpret_cast<uintptr_t>(a.c) & 15u) == 0);
+  p.sa_vec = (a.ldsa % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.sa) & 15u) == 0);
+  p.sb_vec = 0;
+  p.wait_limit_ns = kWaitLimitNs;
+  p.debug_stall = 0;
+  const int64_t grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_wgrad_xq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Cfg::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  return launch_pdl(gemm_wgrad_xq_kernel, (unsigned)grid, Cfg::kThreads, Cfg::kSmemBytes, st, ma, mx, p);
 }
 
 cudaError_t gemm_read_errors(uint32_t* out) {

@@ -115,6 +115,21 @@ struct GemmXqArgs {
   int64_t M, N, K;
 };
 cudaError_t launch_gemm_xq(const GemmXqArgs& a, int num_sms, cudaStream_t st, const char** msg);
+// The weight-gradient GEMM (1x128 x 128x1) with its rhs quantised 128x1 inside
+// the kernel: qa e4m3 [M, K] (lda % 16 == 0), sa its 1x128 scales sa[kb*ldsa + m],
+// x bf16 [K, N] row-major (ldx elements, ldx % 8 == 0, 16-byte aligned), c bf16 [M, N].
+struct GemmWxqArgs {
+  const void* qa;
+  int64_t lda;
+  const float* sa;
+  int64_t ldsa;
+  const void* x;
+  int64_t ldx;
+  void* c;
+  int64_t ldc;
+  int64_t M, N, K;
+};
+cudaError_t launch_gemm_wgrad_xq(const GemmWxqArgs& a, int num_sms, cudaStream_t st, const char** msg);
 
 // Reads and clears the device error word of the GEMM kernels (synchronous).
 cudaError_t gemm_read_errors(uint32_t* out);

@@ -375,6 +375,37 @@ BFP8_API bfp8_status bfp8_gemm_1x128_128x128_xq(const void *x, int64_t ldx, cons
                                                 int64_t N, int64_t K, bfp8_stream_t stream);
 
 /*
+ * Weight-gradient GEMM 1x128 x 128x1 with the rhs quantised inside the
+ * kernel: C[M,N] = A[M,K] quant_rhs(X)[K,N], the optional fused quantisation
+ * in the GEMM prologue for the weight gradient's rhs.  Source: "Enable
+ * blockwise FP8 dense training kernels on ROCm" — quantization kernel
+ * correctness table (act_quant_rhs, block_size=128) and the 1x128 x 128x1
+ * GEMM; "Mask a_s/b_s scale loads in blockwise FP8 training GEMM kernels",
+ * Summary (triton_fp8_gemm_1x128_128x1_kernel) and Fix (masked scale loads
+ * and stores).  The result is the same bits as bfp8_quant_rhs followed by
+ * bfp8_gemm_1x128_128x1: each 128-token block of each column of X gets its
+ * group maximum, scale s = amax/448 and codes RNE_e4m3(clamp(x/s, +-448)),
+ * formed in shared memory by a quantiser warpgroup with the quantisation
+ * kernels' arithmetic and never written to global memory.  Every 128-row
+ * tile of C quantises the columns of X it reads, so the quantisation work is
+ * ceil(M/128)-fold: one launch and no HBM round trip of the codes, at the
+ * cost of recomputation (the two-launch path is faster for large M).
+ *   qa device e4m3 [M, lda] (K contiguous: dY^T for dW = dY^T X), lda >= K,
+ *      lda % 16 == 0, 16-byte aligned; sa device fp32 1x128 scales
+ *      sa[kb*ldsa + m], ldsa >= M (bfp8_quant_lhs's transposed form);
+ *   x  device bf16 [K, N] row-major (K tokens, N features), ldx >= N,
+ *      ldx % 8 == 0, 16-byte aligned;
+ *   c  device bf16 [M, N], ldc >= N; only the logical [M, N] region is written.
+ * K == 0 sets the [M, N] region of c to zero and reads nothing else.
+ * Errors: BFP8_ERR_INVALID_ARG (sizes, strides, alignment, null pointers),
+ * BFP8_ERR_UNSUPPORTED (not sm_103), BFP8_ERR_CUDA (launch); a bounded wait
+ * that gave up is reported by bfp8_check_device_errors.
+ */
+BFP8_API bfp8_status bfp8_gemm_1x128_128x1_xq(const void *qa, int64_t lda, const float *sa, int64_t ldsa,
+                                              const void *x, int64_t ldx, void *c, int64_t ldc, int64_t M,
+                                              int64_t N, int64_t K, bfp8_stream_t stream);
+
+/*
  * Linear forward without caller-provided scratch (no counterpart on the pages:
  * an addition for callers that cannot allocate device memory — plugins hosted
  * by a framework that owns every allocation and hands them no allocator, and

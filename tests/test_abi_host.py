@@ -112,6 +112,35 @@ def test_xq_gemm_argument_validation():
     assert call(M=0) == B.BFP8_OK
 
 
+def test_wgrad_xq_gemm_argument_validation():
+    """The weight-gradient GEMM that quantises its bf16 rhs itself checks x's
+    row stride (TMA: a multiple of 8 bf16 values, at least N), the A operand's
+    stride and alignment before launching."""
+    L = B.lib()
+    g = L.bfp8_gemm_1x128_128x1_xq
+    ok_args = [P16, 256, P16, 64, P16, 512, P16, 512, 64, 512, 256, NULL]
+    names = ["qa", "lda", "sa", "ldsa", "x", "ldx", "c", "ldc", "M", "N", "K", "st"]
+
+    def call(**kw):
+        a = list(ok_args)
+        for k, v in kw.items():
+            a[names.index(k)] = v
+        return g(*a)
+
+    assert call(ldx=500) == B.BFP8_ERR_INVALID_ARG          # ldx < N
+    assert call(ldx=516) == B.BFP8_ERR_INVALID_ARG          # not a multiple of 8 (TMA row stride)
+    assert call(lda=200) == B.BFP8_ERR_INVALID_ARG          # lda < K
+    assert call(lda=264) == B.BFP8_ERR_INVALID_ARG          # not a multiple of 16
+    assert call(ldsa=32) == B.BFP8_ERR_INVALID_ARG          # ldsa < M
+    assert call(ldc=256) == B.BFP8_ERR_INVALID_ARG          # ldc < N
+    assert call(x=P_ODD) == B.BFP8_ERR_INVALID_ARG          # x not 16-byte aligned
+    assert call(qa=P_ODD) == B.BFP8_ERR_INVALID_ARG         # qa not 16-byte aligned
+    assert call(x=NULL) == B.BFP8_ERR_INVALID_ARG
+    assert call(sa=NULL) == B.BFP8_ERR_INVALID_ARG
+    assert call(K=-1) == B.BFP8_ERR_INVALID_ARG
+    assert call(N=0) == B.BFP8_OK
+
+
 def test_grouped_and_fused_argument_validation():
     """Host-side checks of the grouped GEMMs and of the one-launch
     quantisation: every rejection happens before anything is launched."""
