@@ -1470,8 +1470,8 @@ __global__ void __launch_bounds__(XqCfg<BN, STAGES, RAW_ROWS>::kThreads, 1)
 
 // ---------------------------------------------------------------------------
 // The weight-gradient GEMM (1x128 x 128x1) with its rhs quantised inside the
-// kernel: B arrives as the bf16 activation X[K tokens, N features] and a
-// quantiser warpgroup forms, per K-block, each feature column's 128x1 group
+// kernel: B arrives as the bf16 activation X[K tokens, N features] and eight
+// quantiser warps form, per K-block, each feature column's 128x1 group
 // maximum over the block's 128 tokens, its scale and the e4m3 codes, written
 // transposed (K-major, the layout the MMA reads) into the stage, with the
 // quantisation kernels' arithmetic: the result equals quant_rhs followed by
@@ -1482,63 +1482,77 @@ __global__ void __launch_bounds__(XqCfg<BN, STAGES, RAW_ROWS>::kThreads, 1)
 // output quantises the X columns it reads again, so it trades the separate
 // quantisation's HBM round trip for ceil(M/128)-fold quantisation work.
 //
-//   warp 0      producer: raw X tiles (two 64-feature boxes of 128 tokens)
-//               into a four-slot ring, A tiles (dY^T codes) into the stages
-//   warps 1, 3  MMA issuers on alternate K-blocks, each waiting for the
-//               stage's A bytes and its quantised B
-//   warp 2      a_s of each K-block into the scale ring
-//   warps 4-7   quantisers, two halves taking alternate K-blocks: in a half,
-//               warp w takes features 64w..64w+63, lane (chunk j, token
-//               group g) the 8 features 8j..8j+7 over tokens 32g..32g+31;
-//               the four token groups of a chunk combine their maxima by
-//               shuffles; codes are transposed with byte permutes and stored
-//               16 tokens at a time; b_s goes into a ring the promotion reads
-//   warps 8-15  promotion (per-column scales) + epilogue, as the dense kernel
+//   warp 0       producer: raw X tiles (two 64-feature boxes of 128 tokens)
+//                into a ring of three slots, A tiles (dY^T codes) into four
+//                stages
+//   warps 1, 3   MMA issuers on alternate K-blocks, each waiting for the
+//                K-block's A bytes and its quantised B
+//   warp 2       a_s of each K-block into the scale ring
+//   warps 4-11   quantisers, all eight on every K-block: warp w takes the
+//                16 features 16w..16w+15 over the 128 tokens, lane (chunk c,
+//                token group g) the 8 features 16w+8c.. over tokens 8g..8g+7,
+//                read once into registers (in a lane-rotated token order, so
+//                that a warp's 16-byte reads spread over every bank); the
+//                16 token groups combine their maxima by shuffles; the codes
+//                of a feature's 8 tokens are one 8-byte store into the
+//                double-buffered B stage, b_s goes into a ring
+//   warps 12-15  promotion (per-column scales, 128 columns a warp) + epilogue
 // ---------------------------------------------------------------------------
 struct WxqCfg {
   static constexpr int BN = 128;
-  static constexpr int kStages = 2;   // A and quantised-B stages
-  static constexpr int kRawSlots = 4; // raw X tiles (two per quantiser half)
+  static constexpr int kAStages = 4;  // A tiles
+  static constexpr int kBStages = 2;  // quantised B tiles
+  static constexpr int kRawSlots = 3; // raw X tiles
   static constexpr int kBufs = 4;     // 128-column fp32 partial buffers in tensor memory
   static constexpr int kTmemCols = kBufs * BN;
-  static constexpr int kEpiWarps = 8;
-  static constexpr int kCols = BN / (kEpiWarps / 4);  // 64 columns per promotion thread
-  static constexpr int kThreads = 128 + 128 + 32 * kEpiWarps;  // 512
-  // registers: 128 per thread at launch; control 56, quantisers 96, promotion 176
-  static constexpr int kCtrlRegs = 56, kQuantRegs = 96, kEpiRegs = 176;
-  static_assert(128 * kCtrlRegs + 128 * kQuantRegs + 32 * kEpiWarps * kEpiRegs <= kThreads * 128, "register split");
+  static constexpr int kQuantWarps = 8;
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kCols = BN / (kEpiWarps / 4);  // 128 columns per promotion thread
+  static constexpr int kThreads = 128 + 32 * kQuantWarps + 32 * kEpiWarps;  // 512
+  // registers: 128 per thread at launch; control 56, quantisers 88, promotion 248
+  static constexpr int kCtrlRegs = 56, kQuantRegs = 88, kEpiRegs = 248;
+  static_assert(128 * kCtrlRegs + 32 * kQuantWarps * kQuantRegs + 32 * kEpiWarps * kEpiRegs <= kThreads * 128,
+                "register split");
   static constexpr int kABytes = kBM * kBK;      // 16 KiB
   static constexpr int kBBytes = BN * kBK;       // 16 KiB of codes
   static constexpr int kRawBytes = kBK * BN * 2; // 128 tokens x 128 features bf16 = 32 KiB
-  static constexpr int kOffB = kStages * kABytes;
-  static constexpr int kOffRaw = kOffB + kStages * kBBytes;
+  static constexpr int kOffB = kAStages * kABytes;
+  static constexpr int kOffRaw = kOffB + kBStages * kBBytes;
   static constexpr int kScaleSlots = 2, kScaleGroup = 4;
   static constexpr int kScaleKbBytes = kBM * 4;  // a_s of the K-block's 128 rows
   static constexpr int kScaleBytes = kScaleGroup * kScaleKbBytes;
   static constexpr int kOffScale = kOffRaw + kRawSlots * kRawBytes;
   // b_s of each K-block, written by the quantisers into a ring of kBsSlots
-  // entries.  A quantiser writes entry `it` after the MMAs of K-block
-  // it - kStages completed; those were issued after the promotion released
-  // the buffer of K-block it - kStages - kBufs, which each promotion warp does
-  // only after its last read of that K-block's b_s.  So the entry's previous
-  // K-block (it - kBsSlots) has been read by then.
+  // entries.  The quantisers write entry `it` after the MMAs of K-block
+  // it - kBStages completed; those were issued after the promotion released
+  // the buffer of K-block it - kBStages - kBufs, which each promotion warp
+  // does only after its last read of that K-block's b_s.  So the entry's
+  // previous K-block (it - kBsSlots) has been read by then.
   static constexpr int kBsSlots = 8;
-  static_assert(kBsSlots >= kStages + kBufs, "b_s ring depth");
+  static_assert(kBsSlots >= kBStages + kBufs, "b_s ring depth");
   static constexpr int kOffBs = kOffScale + kScaleSlots * kScaleBytes;
   static constexpr int kOffBar = kOffBs + kBsSlots * BN * 4;
-  // full[S] empty[S] bfull[S] rfull[R] rempty[R] tfull[T] tempty[T] drain stall sfull[2] sempty[2]
-  static constexpr int kNumBars = 3 * kStages + 2 * kRawSlots + 2 * kBufs + 2 + 2 * kScaleSlots;
+  // afull[SA] aempty[SA] bfull[SB] bempty[SB] rfull[R] rempty[R] tfull[T] tempty[T] drain stall sfull[2] sempty[2]
+  static constexpr int kNumBars = 2 * kAStages + 2 * kBStages + 2 * kRawSlots + 2 * kBufs + 2 + 2 * kScaleSlots;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
+// 64-bit rotate left by 8*r bits (r in 0..7) of the pair (hi:lo).
+__device__ __forceinline__ void rotl_bytes64(uint32_t& lo, uint32_t& hi, int r) {
+  const uint32_t a = (r & 4) ? hi : lo, b = (r & 4) ? lo : hi;  // rotated by 32 when r >= 4
+  const uint32_t s = 8u * (uint32_t)(r & 3);
+  hi = __funnelshift_l(a, b, s);
+  lo = __funnelshift_l(b, a, s);
+}
+
 __global__ void __launch_bounds__(WxqCfg::kThreads, 1)
     gemm_wgrad_xq_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_x,
                          const GemmParams p) {
   using Cfg = WxqCfg;
-  constexpr int BN = Cfg::BN, S = Cfg::kStages, NR = Cfg::kRawSlots, NT = Cfg::kBufs;
-  constexpr int EW = Cfg::kEpiWarps, kCols = Cfg::kCols, LDW = 32;
+  constexpr int BN = Cfg::BN, SA = Cfg::kAStages, SB = Cfg::kBStages, NR = Cfg::kRawSlots, NT = Cfg::kBufs;
+  constexpr int EW = Cfg::kEpiWarps, QW = Cfg::kQuantWarps, kCols = Cfg::kCols, LDW = 32;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
@@ -1550,31 +1564,35 @@ __global__ void __launch_bounds__(WxqCfg::kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
   volatile int* never = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
 
-  auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
-  auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(S + i); };
-  auto bfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * S + i); };
-  auto rfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * S + i); };
-  auto rempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * S + NR + i); };
-  auto tfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * S + 2 * NR + i); };
-  auto tempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * S + 2 * NR + NT + i); };
-  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(3 * S + 2 * NR + 2 * NT);
+  auto afull_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  auto aempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(SA + i); };
+  auto bfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * SA + i); };
+  auto bempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * SA + SB + i); };
+  auto rfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * SA + 2 * SB + i); };
+  auto rempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * SA + 2 * SB + NR + i); };
+  auto tfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * SA + 2 * SB + 2 * NR + i); };
+  auto tempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * SA + 2 * SB + 2 * NR + NT + i); };
+  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(2 * SA + 2 * SB + 2 * NR + 2 * NT);
   const uint32_t stall_bar = drain_bar + 8u;  // never arrived on
-  auto sfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * S + 2 * NR + 2 * NT + 2 + i); };
-  auto sempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * S + 2 * NR + 2 * NT + 4 + i); };
+  auto sfull_bar = [&](int i) { return drain_bar + 16u + 8u * (uint32_t)i; };
+  auto sempty_bar = [&](int i) { return drain_bar + 32u + 8u * (uint32_t)i; };
 
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const int lane = (int)(threadIdx.x & 31);
   pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(full_bar(i), 1);
-      mbar_init(empty_bar(i), 1);
-      mbar_init(bfull_bar(i), 64);  // every thread of the quantiser half that takes the stage
+    for (int i = 0; i < SA; ++i) {
+      mbar_init(afull_bar(i), 1);
+      mbar_init(aempty_bar(i), 1);
+    }
+    for (int i = 0; i < SB; ++i) {
+      mbar_init(bfull_bar(i), QW);  // one arrival per quantiser warp
+      mbar_init(bempty_bar(i), 1);
     }
     for (int i = 0; i < NR; ++i) {
       mbar_init(rfull_bar(i), 1);
-      mbar_init(rempty_bar(i), 64);
+      mbar_init(rempty_bar(i), QW);
     }
     for (int i = 0; i < NT; ++i) {
       mbar_init(tfull_bar(i), 1);
@@ -1625,14 +1643,14 @@ __global__ void __launch_bounds__(WxqCfg::kThreads, 1)
             tma_load_2d(raw, &tma_x, rfull_bar(r), g.n0, kb * kBK);
             tma_load_2d(raw + (uint32_t)(Cfg::kRawBytes / 2), &tma_x, rfull_bar(r), g.n0 + 64, kb * kBK);
             ++n_raw;
-            const int st = (int)(it % S);
-            if (!mbar_wait_bounded(empty_bar(st), ((it / S) & 1u) ^ 1u, p.wait_limit_ns, abort_flag)) {
+            const int sa = (int)(it % SA);
+            if (!mbar_wait_bounded(aempty_bar(sa), ((it / SA) & 1u) ^ 1u, p.wait_limit_ns, abort_flag)) {
               gemm_fail(kErrWaitEmpty, abort_flag);
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(full_bar(st), (uint32_t)Cfg::kABytes);
-            tma_load_2d(sA + (uint32_t)(st * Cfg::kABytes), &tma_a, full_bar(st), kb * kBK, g.m0);
+            mbar_arrive_expect_tx(afull_bar(sa), (uint32_t)Cfg::kABytes);
+            tma_load_2d(sA + (uint32_t)(sa * Cfg::kABytes), &tma_a, afull_bar(sa), kb * kBK, g.m0);
             ++n_a;
           }
         }
@@ -1641,8 +1659,8 @@ __global__ void __launch_bounds__(WxqCfg::kThreads, 1)
           for (uint32_t j = (n_raw > NR ? n_raw - NR : 0); j < n_raw; ++j)
             if (!mbar_wait_bounded(rfull_bar((int)(j % NR)), (j / NR) & 1u, p.wait_limit_ns, never))
               atomicOr(&g_gemm_error, kErrWaitDrain);
-          for (uint32_t j = (n_a > S ? n_a - S : 0); j < n_a; ++j)
-            if (!mbar_wait_bounded(full_bar((int)(j % S)), (j / S) & 1u, p.wait_limit_ns, never))
+          for (uint32_t j = (n_a > SA ? n_a - SA : 0); j < n_a; ++j)
+            if (!mbar_wait_bounded(afull_bar((int)(j % SA)), (j / SA) & 1u, p.wait_limit_ns, never))
               atomicOr(&g_gemm_error, kErrWaitDrain);
         }
       }
@@ -1656,28 +1674,27 @@ __global__ void __launch_bounds__(WxqCfg::kThreads, 1)
         for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
           for (int kb = 0; kb < p.Kb; ++kb, ++it) {
             if ((it & 1u) != mine) continue;
-            const int st = (int)(it % S);
-            const uint32_t ph = (it / S) & 1u;
-            const int buf = (int)(it % NT);
+            const int sa = (int)(it % SA), sb = (int)(it % SB), buf = (int)(it % NT);
             if (!mbar_spin_bounded(tempty_bar(buf), ((it / NT) & 1u) ^ 1u, p.wait_limit_ns, abort_flag)) {
               gemm_fail(kErrWaitTmemEmpty, abort_flag);
               ok = false;
               break;
             }
-            if (!mbar_spin_bounded(full_bar(st), ph, p.wait_limit_ns, abort_flag) ||
-                !mbar_spin_bounded(bfull_bar(st), ph, p.wait_limit_ns, abort_flag)) {
+            if (!mbar_spin_bounded(afull_bar(sa), (it / SA) & 1u, p.wait_limit_ns, abort_flag) ||
+                !mbar_spin_bounded(bfull_bar(sb), (it / SB) & 1u, p.wait_limit_ns, abort_flag)) {
               gemm_fail(kErrWaitFull, abort_flag);
               ok = false;
               break;
             }
             tc_fence_after();
-            const uint64_t da = desc_kmajor_sw128(sA + (uint32_t)(st * Cfg::kABytes));
-            const uint64_t db = desc_kmajor_sw128(sB + (uint32_t)(st * Cfg::kBBytes));
+            const uint64_t da = desc_kmajor_sw128(sA + (uint32_t)(sa * Cfg::kABytes));
+            const uint64_t db = desc_kmajor_sw128(sB + (uint32_t)(sb * Cfg::kBBytes));
             const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
 #pragma unroll
             for (int k = 0; k < kBK / 32; ++k)
               mma_e4m3(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), idesc, k > 0 ? 1u : 0u);
-            mma_commit(empty_bar(st));
+            mma_commit(aempty_bar(sa));
+            mma_commit(bempty_bar(sb));
             mma_commit(tfull_bar(buf));
           }
         }
@@ -1711,63 +1728,63 @@ __global__ void __launch_bounds__(WxqCfg::kThreads, 1)
       }
       asm volatile("cp.async.wait_all;" ::: "memory");
     }
-  } else if (warp < 8) {
+  } else if (warp < 4 + QW) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Cfg::kQuantRegs));
     // ------------------------------------------------------------ quantisers
-    const int qt = (int)threadIdx.x - 128;
-    const uint32_t half = (uint32_t)(qt >> 6);  // takes the K-block steps it with it % 2 == half
-    const int wq = (qt >> 5) & 1;               // features 64*wq .. +63: raw box wq
-    const int j = lane & 7;                     // features 64*wq + 8j .. +7
-    const int tg = lane >> 3;                   // tokens 32*tg .. +31 of the K-block
+    const int chunk = 2 * (warp - 4) + (lane >> 4);  // features 8*chunk .. +7
+    const int g = lane & 15;                         // tokens 8g .. 8g+7
+    const int rot = g & 7;                           // token order rotation of this lane
+    const int jb = chunk & 7;                        // 16-byte chunk of the features in their box row
     uint32_t it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
       for (int kb = 0; kb < p.Kb; ++kb, ++it) {
-        if ((it & 1u) != half) continue;
-        const int r = (int)(it % NR);
-        const int st = (int)(it % S);
+        const int r = (int)(it % NR), sb = (int)(it % SB);
         bool got = mbar_wait_bounded(rfull_bar(r), (it / NR) & 1u, p.wait_limit_ns, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
           if (lane == 0) gemm_fail(kErrWaitFull, abort_flag);
           ok = false;
           break;
         }
-        // box wq of the raw tile: token t's 64 features at t*128 bytes, 16-byte chunk c at (c ^ (t & 7))
-        const uint32_t box = sRaw + (uint32_t)(r * Cfg::kRawBytes + wq * (Cfg::kRawBytes / 2));
-        // pass 1: |x| maxima of the 8 features over this lane's 32 tokens (packed bf16 pairs)
-        uint32_t m[4] = {0u, 0u, 0u, 0u};
-#pragma unroll 8
-        for (int i = 0; i < 32; ++i) {
-          const int t = 32 * tg + i;
-          uint4 v;
+        // box chunk/8 of the raw tile: token t's 64 features at t*128 bytes, 16-byte chunk c at (c ^ (t & 7)).
+        // Step i reads token 8g + ((i + rot) & 7): the 16 token groups of a warp then hit 8 chunk positions.
+        const uint32_t box = sRaw + (uint32_t)(r * Cfg::kRawBytes + (chunk >> 3) * (Cfg::kRawBytes / 2));
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int ph = (i + rot) & 7;
           asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                       : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                       : "r"(box + (uint32_t)(t * 128) + (uint32_t)((j ^ (t & 7)) << 4)));
-          m[0] = amax2(m[0], v.x);
-          m[1] = amax2(m[1], v.y);
-          m[2] = amax2(m[2], v.z);
-          m[3] = amax2(m[3], v.w);
+                       : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w)
+                       : "r"(box + (uint32_t)((8 * g + ph) * 128) + (uint32_t)((jb ^ ph) << 4)));
         }
-        uint64_t s2[4], ny2[4];  // (s, s') and (-1/s, -1/s') of features 8j + 2q, +1
+        // the values are in registers: the raw slot can be refilled
+        __syncwarp();
+        if (lane == 0) mbar_arrive(rempty_bar(r));
+        // |x| maxima of the 8 features (packed bf16 pairs) over the 128 tokens
+        uint32_t m[4];
+        m[0] = amax2(amax2(amax2(v[0].x, v[1].x), amax2(v[2].x, v[3].x)), amax2(amax2(v[4].x, v[5].x), amax2(v[6].x, v[7].x)));
+        m[1] = amax2(amax2(amax2(v[0].y, v[1].y), amax2(v[2].y, v[3].y)), amax2(amax2(v[4].y, v[5].y), amax2(v[6].y, v[7].y)));
+        m[2] = amax2(amax2(amax2(v[0].z, v[1].z), amax2(v[2].z, v[3].z)), amax2(amax2(v[4].z, v[5].z), amax2(v[6].z, v[7].z)));
+        m[3] = amax2(amax2(amax2(v[0].w, v[1].w), amax2(v[2].w, v[3].w)), amax2(amax2(v[4].w, v[5].w), amax2(v[6].w, v[7].w)));
+        uint64_t s2[4], ny2[4];  // (s, s') and (-1/s, -1/s') of features 8*chunk + 2q, +1
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          m[q] = amax2(m[q], __shfl_xor_sync(0xffffffffu, m[q], 8));
-          m[q] = amax2(m[q], __shfl_xor_sync(0xffffffffu, m[q], 16));
+#pragma unroll
+          for (int d = 1; d < 16; d <<= 1) m[q] = amax2(m[q], __shfl_xor_sync(0xffffffffu, m[q], d));
           const float s_lo = scale_of(__uint_as_float((m[q] << 16) & 0x7FFF0000u));
           const float s_hi = scale_of(__uint_as_float(m[q] & 0x7FFF0000u));
           s2[q] = f2_pack(s_lo, s_hi);
           ny2[q] = f2_pack(neg_rcp(s_lo), neg_rcp(s_hi));
         }
-        // the stage (its quantised-B buffer) and the b_s ring entry are free once
-        // the MMAs of K-block it - kStages completed
-        got = mbar_wait_bounded(empty_bar(st), ((it / S) & 1u) ^ 1u, p.wait_limit_ns, abort_flag);
+        // the B stage and the b_s ring entry are free once the MMAs of K-block it - kBStages completed
+        got = mbar_wait_bounded(bempty_bar(sb), ((it / SB) & 1u) ^ 1u, p.wait_limit_ns, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
           if (lane == 0) gemm_fail(kErrWaitEmpty, abort_flag);
           ok = false;
           break;
         }
-        if (tg == 0) {
-          const uint32_t bs = sBs + (uint32_t)((it % Cfg::kBsSlots) * BN * 4 + 4 * (64 * wq + 8 * j));
+        if (g == 0) {
+          const uint32_t bs = sBs + (uint32_t)((it % Cfg::kBsSlots) * BN * 4 + 4 * (8 * chunk));
           float lo[4], hi[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) f2_unpack(s2[q], lo[q], hi[q]);
@@ -1778,61 +1795,54 @@ __global__ void __launch_bounds__(WxqCfg::kThreads, 1)
                        "f"(lo[3]), "f"(hi[3])
                        : "memory");
         }
-        // pass 2: codes, 16 tokens at a time; feature f's 16 codes are one 16-byte chunk of row f
-        const uint32_t bdst = sB + (uint32_t)(st * Cfg::kBBytes);
-#pragma unroll 1
-        for (int h16 = 0; h16 < 2; ++h16) {
-          uint32_t o[8][4];
+        // codes: per feature pair q, the 8 steps' codes -> one 8-byte word per feature, in step order
+        // (byte i = token 8g + ((i + rot) & 7)), rotated into token order, stored at row f, bytes 8g..8g+7
+        const uint32_t bdst = sB + (uint32_t)(sb * Cfg::kBBytes);
 #pragma unroll
-          for (int i4 = 0; i4 < 4; ++i4) {
-            uint4 v[4];
+        for (int q = 0; q < 4; ++q) {
+          uint32_t fe[2], fo[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t cc[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const int t = 32 * tg + 16 * h16 + 4 * i4 + i;
-              asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                           : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w)
-                           : "r"(box + (uint32_t)(t * 128) + (uint32_t)((j ^ (t & 7)) << 4)));
+              const uint4& w4 = v[4 * h + i];
+              const uint32_t w = q == 0 ? w4.x : q == 1 ? w4.y : q == 2 ? w4.z : w4.w;
+              cc[i] = neg_codes2(w, s2[q], ny2[q]);  // byte 0: feature 8*chunk+2q, byte 1: +1
             }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t cc[4];
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                const uint32_t w = q == 0 ? v[i].x : q == 1 ? v[i].y : q == 2 ? v[i].z : v[i].w;
-                cc[i] = neg_codes2(w, s2[q], ny2[q]);  // byte 0: feature 8j+2q, byte 1: 8j+2q+1
-              }
-              // (t0 e, t1 e, t0 o, t1 o) and (t2 e, t3 e, t2 o, t3 o) -> the four tokens of each feature
-              const uint32_t X = __byte_perm(cc[0], cc[1], 0x5140), Y = __byte_perm(cc[2], cc[3], 0x5140);
-              o[2 * q][i4] = __byte_perm(X, Y, 0x5410) ^ 0x80808080u;
-              o[2 * q + 1][i4] = __byte_perm(X, Y, 0x7632) ^ 0x80808080u;
-            }
+            const uint32_t X = __byte_perm(cc[0], cc[1], 0x5140), Y = __byte_perm(cc[2], cc[3], 0x5140);
+            fe[h] = __byte_perm(X, Y, 0x5410) ^ 0x80808080u;
+            fo[h] = __byte_perm(X, Y, 0x7632) ^ 0x80808080u;
           }
-          const int c = 2 * tg + h16;  // 16-byte chunk of the K-block's row
+          rotl_bytes64(fe[0], fe[1], rot);
+          rotl_bytes64(fo[0], fo[1], rot);
 #pragma unroll
-          for (int fi = 0; fi < 8; ++fi) {
-            const int f = 64 * wq + 8 * j + fi;
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(bdst + (uint32_t)(f * 128) +
-                                                                        (uint32_t)((c ^ (f & 7)) << 4)),
-                         "r"(o[fi][0]), "r"(o[fi][1]), "r"(o[fi][2]), "r"(o[fi][3])
+          for (int h = 0; h < 2; ++h) {
+            const int f = 8 * chunk + 2 * q + h;
+            const uint32_t lo = h ? fo[0] : fe[0], hi = h ? fo[1] : fe[1];
+            asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(bdst + (uint32_t)(f * 128) +
+                                                                 (uint32_t)(((g >> 1) ^ (f & 7)) << 4) +
+                                                                 (uint32_t)(8 * (g & 1))),
+                         "r"(lo), "r"(hi)
                          : "memory");
           }
         }
         fence_proxy_async_shared();  // the codes, for the MMA (async proxy)
-        mbar_arrive(bfull_bar(st));
-        mbar_arrive(rempty_bar(r));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bfull_bar(sb));
       }
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Cfg::kEpiRegs));
     // ------------------------------------------------------------ promotion + epilogue
-    const int e = warp - 8;
+    const int e = warp - 4 - QW;
     const int row = epi_row(e, lane);
     const int col0 = epi_col0(e, BN, EW);
     const uint32_t lane_base = (uint32_t)(32 * (warp % 4)) << 16;
     uint32_t it = 0;
     bool ok = true;
     for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
-      const GemmTile g = gemm_tile(tile, p.num_m, p.num_n, BN);
+      const GemmTile gt = gemm_tile(tile, p.num_m, p.num_n, BN);
       const bool last_tile = tile + (int)gridDim.x >= p.num_tiles;
       float acc[kCols];
 #pragma unroll
@@ -1892,38 +1902,42 @@ __global__ void __launch_bounds__(WxqCfg::kThreads, 1)
       // epilogue (as the dense kernel): rows < M and columns < N only
       constexpr int kG = 8;
       const int pos = lane % kG;
-      uint32_t X[kG][4];
 #pragma unroll
-      for (int jj = 0; jj < kG; ++jj)
+      for (int sg = 0; sg < kCols / (8 * kG); ++sg) {
+        uint32_t X[kG][4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) X[jj][q] = pack_bf16x2(acc[8 * jj + 2 * q], acc[8 * jj + 2 * q + 1]);
+        for (int jj = 0; jj < kG; ++jj)
 #pragma unroll
-      for (int msk = kG / 2; msk >= 1; msk >>= 1) {
-        const bool hi = (pos & msk) != 0;
+          for (int q = 0; q < 4; ++q)
+            X[jj][q] = pack_bf16x2(acc[8 * (kG * sg + jj) + 2 * q], acc[8 * (kG * sg + jj) + 2 * q + 1]);
 #pragma unroll
-        for (int jj = 0; jj < kG; ++jj) {
-          if (jj & msk) continue;
+        for (int msk = kG / 2; msk >= 1; msk >>= 1) {
+          const bool hi = (pos & msk) != 0;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t send = hi ? X[jj][q] : X[jj | msk][q];
-            const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, msk);
-            if (hi) X[jj][q] = recv;
-            else X[jj | msk][q] = recv;
+          for (int jj = 0; jj < kG; ++jj) {
+            if (jj & msk) continue;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t send = hi ? X[jj][q] : X[jj | msk][q];
+              const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, msk);
+              if (hi) X[jj][q] = recv;
+              else X[jj | msk][q] = recv;
+            }
           }
         }
-      }
-      const int n = g.n0 + epi_store_col(e, lane, 0, kG, BN, EW);
+        const int n = gt.n0 + epi_store_col(e, lane, sg, kG, BN, EW);
 #pragma unroll
-      for (int i = 0; i < kG; ++i) {
-        const int mr = g.m0 + epi_store_row(e, lane, i, kG);
-        if (mr >= p.M || n >= p.N) continue;
-        uint16_t* dst = p.c + (int64_t)mr * p.ldc + n;
-        if (p.c_vec && n + 8 <= p.N) {
-          *reinterpret_cast<uint4*>(dst) = make_uint4(X[i][0], X[i][1], X[i][2], X[i][3]);
-        } else {
+        for (int i = 0; i < kG; ++i) {
+          const int mr = gt.m0 + epi_store_row(e, lane, i, kG);
+          if (mr >= p.M || n >= p.N) continue;
+          uint16_t* dst = p.c + (int64_t)mr * p.ldc + n;
+          if (p.c_vec && n + 8 <= p.N) {
+            *reinterpret_cast<uint4*>(dst) = make_uint4(X[i][0], X[i][1], X[i][2], X[i][3]);
+          } else {
 #pragma unroll
-          for (int b = 0; b < 8; ++b)
-            if (n + b < p.N) dst[b] = (uint16_t)(X[i][b >> 1] >> (16 * (b & 1)));
+            for (int b = 0; b < 8; ++b)
+              if (n + b < p.N) dst[b] = (uint16_t)(X[i][b >> 1] >> (16 * (b & 1)));
+          }
         }
       }
     }
