@@ -1237,6 +1237,17 @@ bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int64_t K, i
     return BFP8_OK;
   }
   if (kind == 3) {  // GEMM output C [M,N]; flag bit 3: the 1x128 x 128x1 GEMM
+    if (smallm_eligible(M, N, (flag & 8) != 0, sms)) {
+      // small-M kernel: the leader CTA of tile t, thread nl, stores column 128t + nl of every row
+      for (int64_t t = 0; t < cdiv(N, kBM); ++t)
+        for (int nl = 0; nl < kBM; ++nl) {
+          const int64_t n = t * kBM + nl;
+          if (n >= N) continue;
+          for (int m = 0; m < 16; ++m)
+            if (m < M) hit(counts, m, n, M, N);
+        }
+      return BFP8_OK;
+    }
     const int bn = gemm_pick_bn(M, N, (flag & 8) != 0, sms);
     const int ew = gemm_epi_warps((flag & 8) != 0, bn);
     const int num_m = (int)cdiv(M, kBM), num_n = (int)cdiv(N, bn), tiles = num_m * num_n;

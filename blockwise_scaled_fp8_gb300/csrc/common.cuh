@@ -156,6 +156,98 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 }
 
 // ---------------------------------------------------------------------------
+// Thread-block clusters: distributed shared memory and remote mbarriers
+// ---------------------------------------------------------------------------
+
+// The address in CTA `rank`'s shared memory of the variable at `addr` in this
+// CTA's (a shared::cluster address).
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+
+// One arrival, with release semantics at cluster scope, on the mbarrier at a
+// shared::cluster address (possibly another CTA's).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// One relaxed arrival on a shared::cluster mbarrier: a signal that publishes
+// nothing (here: the signalling CTA no longer reads the target's memory; its
+// loads have completed, since their values were used before the arrival).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// try_wait with acquire semantics at cluster scope: what other CTAs of the
+// cluster wrote before their release arrivals is visible after it succeeds.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded cluster-scope wait: the contract of mbar_wait_bounded, polling
+// (never suspending: a phase completed by another CTA's arrival is seen a few
+// cycles after it, where a suspended try_wait measured about a microsecond late).
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                                          const volatile int* abort) {
+  if (mbar_test_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 256; ++i)
+      if (mbar_test_wait_cluster(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// 16 bytes from a shared::cluster address (another CTA's shared memory).
+__device__ __forceinline__ float4 lds128_cluster(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// The cluster barrier in two halves, each executed by every thread of every
+// CTA at one program point (aligned): the arrival right after the CTA-wide
+// set-up, once the CTA's mbarriers are initialised (their initialisation is
+// published by fence.mbarrier_init.release.cluster, so the arrival itself is
+// relaxed and does not wait for copies in flight), and the wait before the
+// CTA's first signal to a peer.  Every thread arrives unconditionally and the
+// CTAs of a cluster are resident together, so the wait, taken much later,
+// finds every arrival made.
+__device__ __forceinline__ void cluster_arrive_relaxed_all() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_all() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Flags between CTAs of one launch (global memory, GPU scope)
 // ---------------------------------------------------------------------------
 

@@ -1953,6 +1953,390 @@ __global__ void __launch_bounds__(WxqCfg::kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
+// Small-M GEMM (1x128 x 128x128, at most 16 rows of A): the operands swap
+// places in the MMA.  W's 128 rows of a tile are the instruction's A (M = 128)
+// and the (at most) 16 rows of A its B (N = 16), so that every instruction
+// consumes 4 KiB of the weight, the operand streamed from DRAM, and the
+// partial product of a K-block is a 128 x 16 block of tensor memory: lane n,
+// column m.  Each tile's K-blocks are split over the S CTAs of a cluster
+// (contiguous ranges); every CTA promotes its range as the dense kernel does
+// (acc += (a_s * b_s) * P per K-block, the same fp32 operations), the S - 1
+// peers leave their 128 x 16 partial sums in shared memory, and the leader
+// (rank 0) adds them in rank order through distributed shared memory and
+// stores the bf16 tile.  With XQ the rows of A arrive as bf16 x and four
+// quantiser warps form their 1x128 groups in the kernel (the forward that
+// quantises x itself), with the quantisation kernels' arithmetic.
+//
+//   warp 0     producer: W tiles (128 rows) and A tiles (16 rows; bf16 x with
+//              XQ) of the CTA's K-range into an eight-stage ring
+//   warps 1, 3 MMA issuers (M = 128, N = 16) on alternate K-blocks
+//   warp 2     a_s (without XQ) and the tile's b_s of each K-block
+//   warps 4-7  promotion (lane n: the 16 rows of column n), reduction, stores
+//   warps 8-11 (XQ) quantisers: thread (row, 16-column chunk), as the dense
+//              forward's quantiser for 16 rows
+// ---------------------------------------------------------------------------
+template <bool XQ>
+struct SmallCfg {
+  static constexpr int kStages = 8;
+  static constexpr int kRows = 16;  // rows of A: the MMA's N
+  static constexpr int kBufs = 8;   // 16-column partial buffers in tensor memory
+  static constexpr int kTmemCols = 128;
+  static constexpr int kThreads = XQ ? 384 : 256;
+  static constexpr int kWBytes = kBM * kBK;                  // 16 KiB
+  static constexpr int kXBytes = kRows * kBK;                // 2 KiB of codes
+  static constexpr int kRawBytes = XQ ? kRows * kBK * 2 : 0; // 4 KiB of bf16 x (two 64-column boxes)
+  static constexpr int kSlotBytes = 128;                     // a_s[16], then b_s at byte 64
+  static constexpr int kOffX = kStages * kWBytes;
+  static constexpr int kOffRaw = kOffX + kStages * kXBytes;
+  static constexpr int kOffSlot = kOffRaw + kStages * kRawBytes;
+  static constexpr int kOffRed = kOffSlot + kStages * kSlotBytes;  // 128 threads x 16 fp32 partial sums
+  static constexpr int kOffBar = kOffRed + kBM * kRows * 4;
+  // full[S] empty[S] sfull[S] sempty[S] qfull[S] rfull[S] tfull[T] tempty[T] drain red_full red_done stall
+  static constexpr int kNumBars = 6 * kStages + 2 * kBufs + 4;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+};
+
+template <int SB_MODE, bool XQ>
+__global__ void __launch_bounds__(SmallCfg<XQ>::kThreads, 1)
+    gemm_smallm_kernel(const __grid_constant__ CUtensorMap tma_w, const __grid_constant__ CUtensorMap tma_x,
+                       const GemmParams p, const int splits) {
+  using Cfg = SmallCfg<XQ>;
+  static_assert(SB_MODE == kSbTile || SB_MODE == kSbTileT, "tile-scale modes");
+  constexpr int ST = Cfg::kStages, NT = Cfg::kBufs;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sW = sbase, sX = sbase + Cfg::kOffX, sRaw = sbase + Cfg::kOffRaw;
+  const uint32_t sSlot = sbase + Cfg::kOffSlot, sRed = sbase + Cfg::kOffRed;
+  const uint32_t bar0 = sbase + Cfg::kOffBar;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
+  volatile int* never = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
+  auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(ST + i); };
+  auto sfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * ST + i); };
+  auto sempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(3 * ST + i); };
+  auto qfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(4 * ST + i); };
+  auto rfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(5 * ST + i); };
+  auto tfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(6 * ST + i); };
+  auto tempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(6 * ST + NT + i); };
+  const uint32_t drain_bar = bar0 + 8u * (uint32_t)(6 * ST + 2 * NT);
+  const uint32_t red_full_bar = drain_bar + 8u;  // leader: the peers' partial sums are in their shared memory
+  const uint32_t red_done_bar = drain_bar + 16u; // peer: the leader has read this CTA's partial sums
+  const uint32_t stall_bar = drain_bar + 24u;    // never arrived on
+
+  const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
+  const int lane = (int)(threadIdx.x & 31);
+  const int tile = (int)blockIdx.x / splits, split = (int)blockIdx.x % splits;  // split = rank in the cluster
+  const int n0 = tile * kBM;
+  const int kb0 = smallm_kb_lo(split, splits, p.Kb), kbn = smallm_kb_lo(split + 1, splits, p.Kb) - kb0;
+  pdl_launch_dependents();
+  // copy issue of K-block j of the CTA's range (producer thread)
+  auto issue = [&](int j) {
+    const int st = j % ST, kb = kb0 + j;
+    mbar_arrive_expect_tx(full_bar(st), (uint32_t)(Cfg::kWBytes + (XQ ? 0 : Cfg::kXBytes)));
+    tma_load_2d(sW + (uint32_t)(st * Cfg::kWBytes), &tma_w, full_bar(st), kb * kBK, n0);
+    if constexpr (XQ) {
+      const uint32_t raw = sRaw + (uint32_t)(st * Cfg::kRawBytes);
+      mbar_arrive_expect_tx(rfull_bar(st), (uint32_t)Cfg::kRawBytes);
+      tma_load_2d(raw, &tma_x, rfull_bar(st), kb * kBK, 0);
+      tma_load_2d(raw + (uint32_t)(Cfg::kRawBytes / 2), &tma_x, rfull_bar(st), kb * kBK + 64, 0);
+    } else {
+      tma_load_2d(sX + (uint32_t)(st * Cfg::kXBytes), &tma_x, full_bar(st), kb * kBK, 0);
+    }
+  };
+  const int first = kbn < ST ? kbn : ST;  // K-blocks whose stages are fresh
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < ST; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), 1);
+      mbar_init(sfull_bar(i), 32);  // one cp.async arrival per loader lane
+      mbar_init(sempty_bar(i), 4);  // the four promotion warps
+      mbar_init(qfull_bar(i), 128); // the quantiser threads (XQ)
+      mbar_init(rfull_bar(i), 1);
+    }
+    for (int i = 0; i < NT; ++i) {
+      mbar_init(tfull_bar(i), 1);
+      mbar_init(tempty_bar(i), 4);
+    }
+    mbar_init(drain_bar, 2);  // one commit per issuer
+    mbar_init(red_full_bar, splits > 1 ? 4 * (splits - 1) : 1);  // each peer's four promotion warps
+    mbar_init(red_done_bar, 4);                                  // the leader's four promotion warps
+    mbar_init(stall_bar, 1);
+    *abort_flag = 0;
+    *never = 0;
+    fence_barrier_init();
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    // the first stages' copies go out before the CTA-wide set-up completes
+    tma_prefetch_desc(&tma_w);
+    tma_prefetch_desc(&tma_x);
+    pdl_wait();  // the previous kernel's writes are visible from here on
+    for (int j = 0; j < first; ++j) issue(j);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (splits > 1) cluster_arrive_relaxed_all();  // this CTA's barriers exist (waited for before any remote arrival)
+  pdl_wait();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int j = first;
+      bool ok = true;
+      for (; j < kbn; ++j) {
+        if (!mbar_wait_bounded(empty_bar(j % ST), ((j / ST) & 1) ^ 1, p.wait_limit_ns, abort_flag)) {
+          gemm_fail(kErrWaitEmpty, abort_flag);
+          ok = false;
+          break;
+        }
+        issue(j);
+      }
+      if (!ok) {
+        // copies already issued land before this CTA's shared memory goes away
+        for (int i = (j > ST ? j - ST : 0); i < j; ++i) {
+          if (!mbar_wait_bounded(full_bar(i % ST), (i / ST) & 1, p.wait_limit_ns, never))
+            atomicOr(&g_gemm_error, kErrWaitDrain);
+          if (XQ && !mbar_wait_bounded(rfull_bar(i % ST), (i / ST) & 1, p.wait_limit_ns, never))
+            atomicOr(&g_gemm_error, kErrWaitDrain);
+        }
+      }
+    }
+  } else if (warp == 1 || warp == 3) {
+    // ------------------------------------------------------------ MMA issuers (alternate K-blocks)
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_e4m3_f32(kBM, Cfg::kRows);
+      for (int j = warp == 1 ? 0 : 1; j < kbn; j += 2) {
+        const int st = j % ST, buf = j % NT;
+        if (!mbar_spin_bounded(tempty_bar(buf), ((j / NT) & 1) ^ 1, p.wait_limit_ns, abort_flag)) {
+          gemm_fail(kErrWaitTmemEmpty, abort_flag);
+          break;
+        }
+        if (!mbar_spin_bounded(full_bar(st), (j / ST) & 1, p.wait_limit_ns, abort_flag) ||
+            (XQ && !mbar_spin_bounded(qfull_bar(st), (j / ST) & 1, p.wait_limit_ns, abort_flag))) {
+          gemm_fail(kErrWaitFull, abort_flag);
+          break;
+        }
+        tc_fence_after();
+        const uint64_t da = desc_kmajor_sw128(sW + (uint32_t)(st * Cfg::kWBytes));
+        const uint64_t db = desc_kmajor_sw128(sX + (uint32_t)(st * Cfg::kXBytes));
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * Cfg::kRows);
+#pragma unroll
+        for (int k = 0; k < kBK / 32; ++k)
+          mma_e4m3(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), idesc, k > 0 ? 1u : 0u);
+        mma_commit(empty_bar(st));
+        mma_commit(tfull_bar(buf));
+      }
+      // every MMA issued completes before tensor memory is released
+      mma_commit(drain_bar);
+      if (!mbar_wait_bounded(drain_bar, 0, p.wait_limit_ns, never)) gemm_fail(kErrWaitDrain, abort_flag);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ scale loader
+    const int nbk = n0 / kBlock;
+    const bool nin = nbk < p.Nb;
+    for (int j = 0; j < kbn; ++j) {
+      const int st = j % ST, kb = kb0 + j;
+      const bool got = mbar_wait_bounded(sempty_bar(st), ((j / ST) & 1) ^ 1, p.wait_limit_ns, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) gemm_fail(kErrWaitScale, abort_flag);
+        break;
+      }
+      const uint32_t slot = sSlot + (uint32_t)(st * Cfg::kSlotBytes);
+      // a_s of rows 4*lane .. +3 (zero past M)
+      if (!XQ && lane < 4) copy_scales4(slot + 16u * lane, p.sa + (int64_t)kb * p.ldsa, 4 * lane, p.M, p.sa_vec);
+      if (lane == 4) {  // the tile scale of W's 128 x 128 block (nbk, kb)
+        const float* src = SB_MODE == kSbTile ? p.sb + (int64_t)nbk * p.ldsb + kb : p.sb + (int64_t)kb * p.ldsb + nbk;
+        cp_async_4(slot + 64u, nin ? src : p.sb, nin ? 4u : 0u);
+      }
+      cp_async_mbar_arrive(sfull_bar(st));
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ promotion, reduction, stores
+    const int nl = 32 * (warp - 4) + lane;  // tensor-memory lane = column n0 + nl
+    const uint32_t lane_base = (uint32_t)(32 * (warp - 4)) << 16;
+    float acc[Cfg::kRows];
+#pragma unroll
+    for (int m = 0; m < Cfg::kRows; ++m) acc[m] = 0.0f;
+    bool ok = true;
+    for (int j = 0; j < kbn; ++j) {
+      const int st = j % ST, buf = j % NT;
+      const bool sgot = mbar_wait_bounded(sfull_bar(st), (j / ST) & 1, p.wait_limit_ns, abort_flag);
+      const bool got = sgot && mbar_wait_bounded(p.debug_stall ? stall_bar : tfull_bar(buf), (j / NT) & 1,
+                                                 p.wait_limit_ns, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) gemm_fail(sgot ? kErrWaitTmemFull : kErrWaitScale, abort_flag);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t slot = sSlot + (uint32_t)(st * Cfg::kSlotBytes);
+      float as[Cfg::kRows], bsc;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(as[4 * q]), "=f"(as[4 * q + 1]), "=f"(as[4 * q + 2]), "=f"(as[4 * q + 3])
+                     : "r"(slot + 16u * q));
+      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(bsc) : "r"(slot + 64u));
+      uint32_t r[Cfg::kRows];
+      tmem_ld_32x32b_x16(tmem_base + lane_base + (uint32_t)(buf * Cfg::kRows), r);
+      tmem_ld_wait();
+      tmem_regs_after_wait(r);
+      // the partial and the scales are in registers: release the buffer and the slot
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(tempty_bar(buf));
+        mbar_arrive(sempty_bar(st));
+      }
+      // acc[m] += (a_s[m] * b_s) * P[m], two rows per fp32x2 operation
+      const uint64_t b2 = f2_pack(bsc, bsc);
+#pragma unroll
+      for (int m = 0; m < Cfg::kRows; m += 2) {
+        const uint64_t s2 = f2_mul(f2_pack(as[m], as[m + 1]), b2);
+        const uint64_t p2 = f2_pack(__uint_as_float(r[m]), __uint_as_float(r[m + 1]));
+        f2_unpack(f2_fma(s2, p2, f2_pack(acc[m], acc[m + 1])), acc[m], acc[m + 1]);
+      }
+    }
+    bool store = ok;
+    if (splits > 1) {
+      cluster_wait_all();  // every peer's barriers exist
+      // The hand-over runs whether or not this CTA's pipeline succeeded, so
+      // that no CTA leaves while another may still signal it: every peer
+      // arrives on the leader's red_full once (with its partial sums if it
+      // has them), the leader waits for all of them before it signals the
+      // peers' red_done and leaves, and a peer leaves after that signal.
+      // (A pipeline that gave up raised its CTA's abort flag, so it reaches
+      // the hand-over within one wait limit; the hand-over's waits allow
+      // two and three.)
+      const uint32_t red = sRed + (uint32_t)(nl * Cfg::kRows * 4);
+      const int nq = (int)((p.M + 3) / 4);  // 4-row chunks that hold rows of the problem
+      if (split != 0) {
+        if (ok) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (q < nq)
+              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(red + 16u * q), "f"(acc[4 * q]),
+                           "f"(acc[4 * q + 1]), "f"(acc[4 * q + 2]), "f"(acc[4 * q + 3])
+                           : "memory");
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(red_full_bar, 0));
+        const bool done = mbar_wait_cluster_bounded(red_done_bar, 0, 3 * p.wait_limit_ns, never);
+        if (!__all_sync(0xffffffffu, done) && lane == 0) gemm_fail(kErrWaitDrain, abort_flag);
+        store = false;
+      } else {
+        const bool got = mbar_wait_cluster_bounded(red_full_bar, 0, 2 * p.wait_limit_ns, never);
+        if (!__all_sync(0xffffffffu, got && ok && !*abort_flag)) {
+          if (lane == 0 && !got) gemm_fail(kErrWaitDrain, abort_flag);
+          store = false;
+        } else {
+          // the peers' partial sums, added in rank order (each chunk's loads
+          // from every peer issued before the first addition)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (q >= nq) break;
+            float4 v[7];
+#pragma unroll
+            for (int s = 1; s < 8; ++s)
+              if (s < splits) v[s - 1] = lds128_cluster(mapa_shared(red + 16u * q, (uint32_t)s));
+#pragma unroll
+            for (int s = 1; s < 8; ++s)
+              if (s < splits) {
+                acc[4 * q] += v[s - 1].x;
+                acc[4 * q + 1] += v[s - 1].y;
+                acc[4 * q + 2] += v[s - 1].z;
+                acc[4 * q + 3] += v[s - 1].w;
+              }
+          }
+        }
+        // the peers may leave once this warp no longer reads their shared memory
+        __syncwarp();
+        if (lane == 0)
+          for (int s = 1; s < splits; ++s) mbar_arrive_cluster_relaxed(mapa_shared(red_done_bar, (uint32_t)s));
+      }
+    }
+    if (store) {
+      const int64_t n = n0 + nl;
+      if (n < p.N) {
+#pragma unroll
+        for (int m = 0; m < Cfg::kRows; ++m)
+          if (m < p.M) p.c[(int64_t)m * p.ldc + n] = (uint16_t)(pack_bf16x2(acc[m], 0.0f) & 0xFFFFu);
+      }
+    }
+  } else if (XQ && warp >= 8) {
+    // ------------------------------------------------------------ quantisers (XQ)
+    const int qt = (int)threadIdx.x - 256;
+    const int chunk = qt & 7;  // 16 columns of the K-block
+    const int row = qt >> 3;   // 0..15
+    const uint32_t gmask = 0xFFu << (8 * (lane >> 3));  // the 8 lanes of this thread's row
+    for (int j = 0; j < kbn; ++j) {
+      const int st = j % ST;
+      // raw x landed; the stage's codes and a_s were consumed by the MMA and the promotion of K-block j - ST
+      const bool got = mbar_wait_bounded(rfull_bar(st), (j / ST) & 1, p.wait_limit_ns, abort_flag) &&
+                       mbar_wait_bounded(empty_bar(st), ((j / ST) & 1) ^ 1, p.wait_limit_ns, abort_flag) &&
+                       mbar_wait_bounded(sempty_bar(st), ((j / ST) & 1) ^ 1, p.wait_limit_ns, abort_flag);
+      if (!__all_sync(0xffffffffu, got)) {
+        if (lane == 0) gemm_fail(kErrWaitFull, abort_flag);
+        break;
+      }
+      const uint32_t raw = sRaw + (uint32_t)(st * Cfg::kRawBytes);
+      // 16 bf16 values: 16-byte chunks 2*(chunk%4) and +1 of box chunk/4 (128-byte swizzle)
+      const uint32_t rbase = raw + (uint32_t)((chunk >> 2) * (Cfg::kRawBytes / 2) + row * 128);
+      const int c0 = 2 * (chunk & 3);
+      uint4 v0, v1;
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(v0.x), "=r"(v0.y), "=r"(v0.z), "=r"(v0.w)
+                   : "r"(rbase + (uint32_t)(((c0) ^ (row & 7)) << 4)));
+      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                   : "=r"(v1.x), "=r"(v1.y), "=r"(v1.z), "=r"(v1.w)
+                   : "r"(rbase + (uint32_t)(((c0 + 1) ^ (row & 7)) << 4)));
+      uint32_t m = amax2(amax2(amax2(v0.x, v0.y), amax2(v0.z, v0.w)), amax2(amax2(v1.x, v1.y), amax2(v1.z, v1.w)));
+      m = amax2(m, __shfl_xor_sync(gmask, m, 1));
+      m = amax2(m, __shfl_xor_sync(gmask, m, 2));
+      m = amax2(m, __shfl_xor_sync(gmask, m, 4));
+      m = amax2(m, __byte_perm(m, 0, 0x1032));
+      const float sc = scale_of(__uint_as_float(m & 0x7FFF0000u));
+      const float ny = neg_rcp(sc);
+      const uint64_t s2 = f2_pack(sc, sc), ny2 = f2_pack(ny, ny);
+      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      uint32_t q[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        q[k] = __byte_perm(neg_codes2(w[2 * k], s2, ny2), neg_codes2(w[2 * k + 1], s2, ny2), 0x5410) ^ 0x80808080u;
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sX + (uint32_t)(st * Cfg::kXBytes + row * 128) +
+                                                                  (uint32_t)((chunk ^ (row & 7)) << 4)),
+                   "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3])
+                   : "memory");
+      if (chunk == 0)
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(sSlot + (uint32_t)(st * Cfg::kSlotBytes) + 4u * (uint32_t)row),
+                     "f"(sc)
+                     : "memory");
+      fence_proxy_async_shared();  // the codes, for the MMA (async proxy)
+      mbar_arrive(qfull_bar(st));
+    }
+  }
+
+  __syncwarp();
+  if (splits > 1 && !(warp >= 4 && warp < 8)) cluster_wait_all();  // (the promotion warps waited above)
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 
@@ -2055,8 +2439,116 @@ static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const 
                       st, ma, mb, p, *gp);
 }
 
+// Parameters of the small-M kernel (Kb = -1 when a size is out of range).
+static GemmParams smallm_params(const float* sa, int64_t ldsa, const float* sb, int64_t ldsb, void* c, int64_t ldc,
+                                int64_t M, int64_t N, int64_t K, uint64_t wait_limit_ns, int debug_stall) {
+  GemmParams p;
+  p.sa = sa;
+  p.ldsa = ldsa;
+  p.sb = sb;
+  p.ldsb = ldsb;
+  p.c = reinterpret_cast<uint16_t*>(c);
+  p.ldc = ldc;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.num_m = 1;
+  p.num_n = (int)cdiv(N, kBM);
+  p.num_tiles = p.num_n;
+  const int64_t Kb = cdiv(K, kBK);
+  p.Kb = (N >= (int64_t)1 << 31 || K >= (int64_t)1 << 31 || cdiv(N, kBM) * Kb >= (int64_t)1 << 31) ? -1 : (int)Kb;
+  p.Nb = (int)cdiv(N, kBlock);
+  p.c_vec = 0;
+  p.sa_vec = sa && (ldsa % 4 == 0) && ((reinterpret_cast<uintptr_t>(sa) & 15u) == 0);
+  p.sb_vec = 0;
+  p.wait_limit_ns = wait_limit_ns;
+  p.debug_stall = debug_stall;
+  return p;
+}
+
+// The small-M kernel: T = ceil(N/128) tiles, each split over a cluster of S
+// CTAs (at most 8, at least four K-blocks each), S the largest for which the
+// T clusters are resident at once (one wave); S = 1 launches no cluster.
+template <int MODE, bool XQ>
+static int smallm_splits(int tiles, int Kb, int num_sms) {
+  using Cfg = SmallCfg<XQ>;
+  static std::once_flag once;
+  static int max_clusters[9] = {};
+  std::call_once(once, [] {
+    if (cudaFuncSetAttribute(gemm_smallm_kernel<MODE, XQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::kSmemBytes) != cudaSuccess)
+      return;
+    for (int s = 2; s <= 8; ++s) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)(s * 16));
+      cfg.blockDim = dim3(Cfg::kThreads);
+      cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = (unsigned)s;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_smallm_kernel<MODE, XQ>, &cfg) == cudaSuccess) max_clusters[s] = n;
+    }
+    (void)cudaGetLastError();  // a size the device refuses leaves no error behind
+  });
+  // at least four K-blocks a CTA: below that the hand-over of the partial
+  // sums costs more than the K-blocks it spreads (measured)
+  for (int s = Kb / 4 < 8 ? Kb / 4 : 8; s >= 2; --s)
+    if (tiles * s <= num_sms && tiles <= max_clusters[s]) return s;
+  return 1;
+}
+
+template <int MODE, bool XQ>
+static cudaError_t run_gemm_smallm(const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p, int tiles,
+                                   int num_sms, cudaStream_t st) {
+  using Cfg = SmallCfg<XQ>;
+  const int splits = smallm_splits<MODE, XQ>(tiles, p.Kb, num_sms);
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_smallm_kernel<MODE, XQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    Cfg::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(tiles * splits));
+  cfg.blockDim = dim3(Cfg::kThreads);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)splits;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = splits > 1 ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, gemm_smallm_kernel<MODE, XQ>, mw, mx, p, splits);
+}
+
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const char** msg,
                         uint64_t wait_limit_ns, int debug_stall) {
+  if (smallm_eligible(a.M, a.N, a.sb_mode == kSbCol, num_sms)) {
+    // W (B^T, [N, K]) as the MMA's 128-row A; the rows of A as its 16-row B
+    CUtensorMap mw, mx;
+    if (!make_tma_u8(&mw, a.qb, a.K, a.N, a.ldb, kBM) || !make_tma_u8(&mx, a.qa, a.K, a.M, a.lda, 16)) {
+      *msg = "cuTensorMapEncodeTiled failed for an operand (alignment, stride or size out of range)";
+      return cudaErrorInvalidValue;
+    }
+    GemmParams p = smallm_params(a.sa, a.ldsa, a.sb, a.ldsb, a.c, a.ldc, a.M, a.N, a.K, wait_limit_ns, debug_stall);
+    if (p.Kb < 0) {
+      *msg = "GEMM too large: M, N, K and the number of (tile, K-block) units must stay below 2^31";
+      return cudaErrorInvalidValue;
+    }
+    const int tiles = (int)cdiv(a.N, kBM);
+    return a.sb_mode == kSbTile ? run_gemm_smallm<kSbTile, false>(mw, mx, p, tiles, num_sms, st)
+                                : run_gemm_smallm<kSbTileT, false>(mw, mx, p, tiles, num_sms, st);
+  }
   const int bn = gemm_pick_bn(a.M, a.N, a.sb_mode == kSbCol, num_sms);
   const int a_rows = gemm_a_rows(a.M, bn);
   CUtensorMap ma, mb;
@@ -2257,6 +2749,20 @@ static cudaError_t run_gemm_xq(const GemmXqArgs& a, int num_sms, cudaStream_t st
 // with the dense GEMM's 64-column tiles where 128-column ones would fill at
 // most half the SMs; else x tiles of 128 rows and 128-column tiles.
 cudaError_t launch_gemm_xq(const GemmXqArgs& a, int num_sms, cudaStream_t st, const char** msg) {
+  if (smallm_eligible(a.M, a.N, false, num_sms)) {
+    // the small-M kernel with x quantised in it (same splits as the plain GEMM, so the same bits)
+    CUtensorMap mw, mx;
+    if (!make_tma_u8(&mw, a.qb, a.K, a.N, a.ldb, kBM) || !make_tma_bf16(&mx, a.x, a.K, a.M, a.ldx * 2, 16)) {
+      *msg = "cuTensorMapEncodeTiled failed for an operand (alignment, stride or size out of range)";
+      return cudaErrorInvalidValue;
+    }
+    GemmParams p = smallm_params(nullptr, 0, a.sb, a.ldsb, a.c, a.ldc, a.M, a.N, a.K, kWaitLimitNs, 0);
+    if (p.Kb < 0) {
+      *msg = "GEMM too large: M, N, K and the number of (tile, K-block) units must stay below 2^31";
+      return cudaErrorInvalidValue;
+    }
+    return run_gemm_smallm<kSbTile, true>(mw, mx, p, (int)cdiv(a.N, kBM), num_sms, st);
+  }
   if (a.M <= 16)
     return gemm_pick_bn(a.M, a.N, false, num_sms) == 64 ? run_gemm_xq<16, 64>(a, num_sms, st, msg)
                                                          : run_gemm_xq<16, 128>(a, num_sms, st, msg);

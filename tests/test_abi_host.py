@@ -304,7 +304,9 @@ def test_quant_dual_index_replay_exactly_once(M, N, K):
 @pytest.mark.parametrize("M,N,K", SHAPES + [(128, 2048, 2048), (300, 384, 4096), (2, 5120, 1280), (64, 1000, 2048),
                                              (4096, 4096, 128), (2048, 4096, 128), (16384, 1024, 128),
                                              (2048, 4096, 4096), (2000, 4000, 520), (4096, 4096, 8192),
-                                             (2048, 4100, 256), (1900, 4090, 128)])
+                                             (2048, 4100, 256), (1900, 4090, 128),
+                                             (1, 130, 8192), (16, 4096, 4096), (5, 2051, 1100),
+                                             (12, 19456, 256), (2, 19584, 256)])
 @pytest.mark.parametrize("col_scales", [0, 8])
 def test_gemm_epilogue_index_replay_exactly_once(M, N, K, col_scales):
     """The persistent tile schedule stores each output element once (both

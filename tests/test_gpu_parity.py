@@ -404,6 +404,37 @@ def test_gemm_few_tiles_deep_k_matches_oracle(M, N, K, mode):
     B.check_device_errors()
 
 
+# at most 16 rows, tile-scale modes: the operand-swapped kernel whose tiles'
+# K-blocks are split over a cluster of CTAs (152 SMs: 16x4096x4096 4 splits;
+# 1x130x8192 8; 5x2051x1100 8 over 9 K-blocks; 3x512x384 3, one K-block each;
+# 7x18944 148 tiles, 1 split; 12x19456 152 tiles, 1 split; 2x19584 153 tiles:
+# the 64/128-column kernel), launched twice in a row
+SMALLM_SHAPES = [(16, 4096, 4096), (1, 130, 8192), (5, 2051, 1100), (3, 512, 384), (7, 18944, 384),
+                 (12, 19456, 256), (2, 19584, 256)]
+
+
+@pytest.mark.parametrize("M,N,K", SMALLM_SHAPES)
+@pytest.mark.parametrize("mode", [O.SB_TILE, O.SB_TILE_T])
+def test_gemm_small_m_split_k_matches_oracle(M, N, K, mode):
+    got, ref = _gemm_case(M, N, K, mode, seed=11 * M + N + K + mode, ldc_extra=8, repeats=2)
+    assert_gemm_close(got, ref, f"small-M gemm mode {mode} {M}x{N}x{K}")
+    B.check_device_errors()
+
+
+def test_gemm_small_m_repeat_is_bit_identical():
+    """The split sums are added in a fixed order: two calls give the same bits."""
+    rng = np.random.default_rng(3)
+    M, N, K = 9, 3000, 6000
+    qa, qb = _random_codes(rng, (M, rup(K, 16))), _random_codes(rng, (N, rup(K, 16)))
+    sa = rng.uniform(0.01, 2.0, (cdiv(K, 128), M)).astype(np.float32)
+    sb = rng.uniform(0.01, 2.0, (cdiv(N, 128), cdiv(K, 128))).astype(np.float32)
+    cu = lambda a: torch.from_numpy(a).cuda()
+    a = B.gemm_1x128_128x128(cu(qa), cu(sa), cu(qb), cu(sb), K, M=M, N=N)
+    b = B.gemm_1x128_128x128(cu(qa), cu(sa), cu(qb), cu(sb), K, M=M, N=N)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
 @pytest.mark.parametrize("M,N,K", [(300, 130, 256), (129, 1001, 384), (64, 2051, 128)])
 @pytest.mark.parametrize("mode", [O.SB_TILE, O.SB_COL])
 def test_gemm_ragged_n_aligned_ldc(M, N, K, mode):
