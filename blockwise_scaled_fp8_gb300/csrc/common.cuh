@@ -156,7 +156,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 }
 
 // ---------------------------------------------------------------------------
-// Thread-block clusters: distributed shared memory and remote mbarriers
+// Thread-block clusters: distributed shared memory and the cluster barrier
 // ---------------------------------------------------------------------------
 
 // The address in CTA `rank`'s shared memory of the variable at `addr` in this
@@ -167,59 +167,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   return r;
 }
 
-// One arrival, with release semantics at cluster scope, on the mbarrier at a
-// shared::cluster address (possibly another CTA's).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-// One relaxed arrival on a shared::cluster mbarrier: a signal that publishes
-// nothing (here: the signalling CTA no longer reads the target's memory; its
-// loads have completed, since their values were used before the arrival).
-__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-// try_wait with acquire semantics at cluster scope: what other CTAs of the
-// cluster wrote before their release arrivals is visible after it succeeds.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded cluster-scope wait: the contract of mbar_wait_bounded, polling
-// (never suspending: a phase completed by another CTA's arrival is seen a few
-// cycles after it, where a suspended try_wait measured about a microsecond late).
-__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns,
-                                                          const volatile int* abort) {
-  if (mbar_test_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 256; ++i)
-      if (mbar_test_wait_cluster(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
-  }
+// 8 bytes from a shared::cluster address (another CTA's shared memory).
+__device__ __forceinline__ float2 lds64_cluster(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
 }
 
 // 16 bytes from a shared::cluster address (another CTA's shared memory).
@@ -232,19 +184,12 @@ __device__ __forceinline__ float4 lds128_cluster(uint32_t addr) {
   return v;
 }
 
-// The cluster barrier in two halves, each executed by every thread of every
-// CTA at one program point (aligned): the arrival right after the CTA-wide
-// set-up, once the CTA's mbarriers are initialised (their initialisation is
-// published by fence.mbarrier_init.release.cluster, so the arrival itself is
-// relaxed and does not wait for copies in flight), and the wait before the
-// CTA's first signal to a peer.  Every thread arrives unconditionally and the
-// CTAs of a cluster are resident together, so the wait, taken much later,
-// finds every arrival made.
-__device__ __forceinline__ void cluster_arrive_relaxed_all() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait_all() {
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+// Every thread of every CTA of the cluster: arrive (release) and wait
+// (acquire) on the cluster barrier, all at one program point (aligned).  Used
+// where every thread reaches it unconditionally; the CTAs of a cluster are
+// resident together, so it completes.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // ---------------------------------------------------------------------------

@@ -1953,64 +1953,121 @@ __global__ void __launch_bounds__(WxqCfg::kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Small-M GEMM (1x128 x 128x128, at most 16 rows of A): the operands swap
+// Small-M GEMM (1x128 x 128x128, at most 32 rows of A): the operands swap
 // places in the MMA.  W's 128 rows of a tile are the instruction's A (M = 128)
-// and the (at most) 16 rows of A its B (N = 16), so that every instruction
-// consumes 4 KiB of the weight, the operand streamed from DRAM, and the
-// partial product of a K-block is a 128 x 16 block of tensor memory: lane n,
-// column m.  Each tile's K-blocks are split over the S CTAs of a cluster
-// (contiguous ranges); every CTA promotes its range as the dense kernel does
-// (acc += (a_s * b_s) * P per K-block, the same fp32 operations), the S - 1
-// peers leave their 128 x 16 partial sums in shared memory, and the leader
-// (rank 0) adds them in rank order through distributed shared memory and
-// stores the bf16 tile.  With XQ the rows of A arrive as bf16 x and four
-// quantiser warps form their 1x128 groups in the kernel (the forward that
-// quantises x itself), with the quantisation kernels' arithmetic.
+// and the R rows of A (R = 16 or 32, the smaller that holds them) its B
+// (N = R), so that every instruction consumes 4 KiB of the weight, the
+// operand streamed from DRAM, and the partial product of a K-block is a
+// 128 x R block of tensor memory: lane n, column m.  Each tile's K-blocks are
+// split over the S CTAs of a cluster (contiguous ranges); every CTA promotes
+// its range as the dense kernel does (acc += (a_s * b_s) * P per K-block, the
+// same fp32 operations).  With S > 1 every CTA then leaves its 128 x R
+// partial sums in its idle W stages, and CTA s of the cluster adds rows
+// s R/S .. (s+1) R/S - 1 of all S partials in rank order through distributed
+// shared memory and stores them (bf16), between two cluster barriers.  With
+// XQ the rows of A arrive as bf16 x and four quantiser warps form their 1x128
+// groups in the kernel (the forward that quantises x itself), with the
+// quantisation kernels' arithmetic.  (Measured with R = 64 and 128 as well,
+// this form was slower than the dense kernel's tiles beyond 32 rows.)
 //
-//   warp 0     producer: W tiles (128 rows) and A tiles (16 rows; bf16 x with
-//              XQ) of the CTA's K-range into an eight-stage ring
-//   warps 1, 3 MMA issuers (M = 128, N = 16) on alternate K-blocks
-//   warp 2     a_s (without XQ) and the tile's b_s of each K-block
-//   warps 4-7  promotion (lane n: the 16 rows of column n), reduction, stores
-//   warps 8-11 (XQ) quantisers: thread (row, 16-column chunk), as the dense
-//              forward's quantiser for 16 rows
+//   warp 0       producer: W tiles (128 rows) and A tiles (R rows; bf16 x
+//                with XQ) of the CTA's K-range into the stage ring
+//   warps 1, 3   MMA issuers (M = 128, N = R) on alternate K-blocks
+//   warp 2       a_s (without XQ) and the tile's b_s of each K-block
+//   warps 4-7    promotion (lane n: column n of C, its R rows), reduction,
+//                stores
+//   warps 8-11   (XQ) quantisers: thread (row, 16-column chunk) for each group
+//                of 16 rows, as the dense forward's quantiser for 16 rows
 // ---------------------------------------------------------------------------
-template <bool XQ>
+template <bool XQ, int R>
 struct SmallCfg {
-  static constexpr int kStages = 8;
-  static constexpr int kRows = 16;  // rows of A: the MMA's N
-  static constexpr int kBufs = 8;   // 16-column partial buffers in tensor memory
-  static constexpr int kTmemCols = 128;
-  static constexpr int kThreads = XQ ? 384 : 256;
+  static_assert(R == 16 || R == 32, "rows of A");
+  static constexpr int kRows = R;                   // the MMA's N
+  static constexpr int kStages = XQ && R == 32 ? 6 : 8;
+  static constexpr int kBufs = 8;                   // R-column partial buffers in tensor memory
+  static constexpr int kTmemCols = kBufs * R;       // 128 or 256
+  static constexpr int kPromoWarps = 4;
+  static constexpr int kCols = R;                   // rows of A per promotion thread
+  static constexpr int kChunk = R;                  // columns per tensor-memory load
+  static constexpr int kThreads = 128 + 32 * kPromoWarps + (XQ ? 128 : 0);
   static constexpr int kWBytes = kBM * kBK;                  // 16 KiB
-  static constexpr int kXBytes = kRows * kBK;                // 2 KiB of codes
-  static constexpr int kRawBytes = XQ ? kRows * kBK * 2 : 0; // 4 KiB of bf16 x (two 64-column boxes)
-  static constexpr int kSlotBytes = 128;                     // a_s[16], then b_s at byte 64
+  static constexpr int kXBytes = R * kBK;                    // codes of the R rows
+  static constexpr int kRawBytes = XQ ? R * kBK * 2 : 0;     // bf16 x (two 64-column boxes)
+  static constexpr int kSlotBytes = (4 * R + 16 + 127) / 128 * 128;  // a_s[R], then b_s at byte 4R
   static constexpr int kOffX = kStages * kWBytes;
   static constexpr int kOffRaw = kOffX + kStages * kXBytes;
   static constexpr int kOffSlot = kOffRaw + kStages * kRawBytes;
-  static constexpr int kOffRed = kOffSlot + kStages * kSlotBytes;  // 128 threads x 16 fp32 partial sums
-  static constexpr int kOffBar = kOffRed + kBM * kRows * 4;
-  // full[S] empty[S] sfull[S] sempty[S] qfull[S] rfull[S] tfull[T] tempty[T] drain red_full red_done stall
-  static constexpr int kNumBars = 6 * kStages + 2 * kBufs + 4;
+  static constexpr int kOffBar = kOffSlot + kStages * kSlotBytes;
+  // full[S] empty[S] sfull[S] sempty[S] qfull[S] rfull[S] tfull[T] tempty[T] drain stall
+  static constexpr int kNumBars = 6 * kStages + 2 * kBufs + 2;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;
+  // once the K-loop is over, the 128 x R partial sums sit in the W stages
+  static_assert(kBM * R * 4 <= kStages * kWBytes, "partial sums fit in the W stages");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
-template <int SB_MODE, bool XQ>
-__global__ void __launch_bounds__(SmallCfg<XQ>::kThreads, 1)
+// Splits the reduction supports: S = 2, 4 or 8 divides R, and each promotion
+// thread's share of a CTA's rows is at least two values (8-byte loads).
+constexpr int kSmallMaxSplits = 8;
+
+// CTA `rank` of S: rows rank R/S .. of the tile, summed over the S partials
+// (at `part` in every CTA's shared memory, 128 x R fp32, row-major by lane
+// n) in rank order and stored as bf16.  Thread (nl, h): column n0 + nl,
+// rows rank R/S + h CW .. + CW - 1.
+template <int R, int PW, int S>
+__device__ __forceinline__ void smallm_reduce_store(uint32_t part, int rank, int nl, int h, int n0, const GemmParams& p) {
+  constexpr int CW = R / S / (PW / 4);
+  static_assert(CW % 2 == 0, "whole 8-byte loads");
+  const int m0 = rank * (R / S) + h * CW;
+  const uint32_t src = part + (uint32_t)((nl * R + m0) * 4);
+  float v[S][CW];
+#pragma unroll
+  for (int s = 0; s < S; ++s) {
+    const uint32_t a = mapa_shared(src, (uint32_t)s);
+    if constexpr (CW % 4 == 0) {
+#pragma unroll
+      for (int q = 0; q < CW / 4; ++q) {
+        const float4 t = lds128_cluster(a + 16u * q);
+        v[s][4 * q] = t.x;
+        v[s][4 * q + 1] = t.y;
+        v[s][4 * q + 2] = t.z;
+        v[s][4 * q + 3] = t.w;
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < CW / 2; ++q) {
+        const float2 t = lds64_cluster(a + 8u * q);
+        v[s][2 * q] = t.x;
+        v[s][2 * q + 1] = t.y;
+      }
+    }
+  }
+  const int64_t n = n0 + nl;
+  if (n >= p.N) return;
+#pragma unroll
+  for (int j = 0; j < CW; ++j) {
+    float sum = v[0][j];
+#pragma unroll
+    for (int s = 1; s < S; ++s) sum += v[s][j];
+    const int64_t m = m0 + j;
+    if (m < p.M) p.c[m * p.ldc + n] = (uint16_t)(pack_bf16x2(sum, 0.0f) & 0xFFFFu);
+  }
+}
+
+template <int SB_MODE, bool XQ, int R>
+__global__ void __launch_bounds__(SmallCfg<XQ, R>::kThreads, 1)
     gemm_smallm_kernel(const __grid_constant__ CUtensorMap tma_w, const __grid_constant__ CUtensorMap tma_x,
                        const GemmParams p, const int splits) {
-  using Cfg = SmallCfg<XQ>;
+  using Cfg = SmallCfg<XQ, R>;
   static_assert(SB_MODE == kSbTile || SB_MODE == kSbTileT, "tile-scale modes");
-  constexpr int ST = Cfg::kStages, NT = Cfg::kBufs;
+  constexpr int ST = Cfg::kStages, NT = Cfg::kBufs, PW = Cfg::kPromoWarps;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sW = sbase, sX = sbase + Cfg::kOffX, sRaw = sbase + Cfg::kOffRaw;
-  const uint32_t sSlot = sbase + Cfg::kOffSlot, sRed = sbase + Cfg::kOffRed;
+  const uint32_t sSlot = sbase + Cfg::kOffSlot;
   const uint32_t bar0 = sbase + Cfg::kOffBar;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 4);
@@ -2024,9 +2081,7 @@ __global__ void __launch_bounds__(SmallCfg<XQ>::kThreads, 1)
   auto tfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(6 * ST + i); };
   auto tempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(6 * ST + NT + i); };
   const uint32_t drain_bar = bar0 + 8u * (uint32_t)(6 * ST + 2 * NT);
-  const uint32_t red_full_bar = drain_bar + 8u;  // leader: the peers' partial sums are in their shared memory
-  const uint32_t red_done_bar = drain_bar + 16u; // peer: the leader has read this CTA's partial sums
-  const uint32_t stall_bar = drain_bar + 24u;    // never arrived on
+  const uint32_t stall_bar = drain_bar + 8u;  // never arrived on
 
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const int lane = (int)(threadIdx.x & 31);
@@ -2054,17 +2109,15 @@ __global__ void __launch_bounds__(SmallCfg<XQ>::kThreads, 1)
       mbar_init(full_bar(i), 1);
       mbar_init(empty_bar(i), 1);
       mbar_init(sfull_bar(i), 32);  // one cp.async arrival per loader lane
-      mbar_init(sempty_bar(i), 4);  // the four promotion warps
+      mbar_init(sempty_bar(i), PW); // the promotion warps
       mbar_init(qfull_bar(i), 128); // the quantiser threads (XQ)
       mbar_init(rfull_bar(i), 1);
     }
     for (int i = 0; i < NT; ++i) {
       mbar_init(tfull_bar(i), 1);
-      mbar_init(tempty_bar(i), 4);
+      mbar_init(tempty_bar(i), PW);
     }
     mbar_init(drain_bar, 2);  // one commit per issuer
-    mbar_init(red_full_bar, splits > 1 ? 4 * (splits - 1) : 1);  // each peer's four promotion warps
-    mbar_init(red_done_bar, 4);                                  // the leader's four promotion warps
     mbar_init(stall_bar, 1);
     *abort_flag = 0;
     *never = 0;
@@ -2083,9 +2136,9 @@ __global__ void __launch_bounds__(SmallCfg<XQ>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (splits > 1) cluster_arrive_relaxed_all();  // this CTA's barriers exist (waited for before any remote arrival)
   pdl_wait();
   const uint32_t tmem_base = *tmem_holder;
+  const bool promo = warp >= 4 && warp < 4 + PW;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -2113,7 +2166,7 @@ __global__ void __launch_bounds__(SmallCfg<XQ>::kThreads, 1)
   } else if (warp == 1 || warp == 3) {
     // ------------------------------------------------------------ MMA issuers (alternate K-blocks)
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_e4m3_f32(kBM, Cfg::kRows);
+      constexpr uint32_t idesc = idesc_e4m3_f32(kBM, R);
       for (int j = warp == 1 ? 0 : 1; j < kbn; j += 2) {
         const int st = j % ST, buf = j % NT;
         if (!mbar_spin_bounded(tempty_bar(buf), ((j / NT) & 1) ^ 1, p.wait_limit_ns, abort_flag)) {
@@ -2128,7 +2181,7 @@ __global__ void __launch_bounds__(SmallCfg<XQ>::kThreads, 1)
         tc_fence_after();
         const uint64_t da = desc_kmajor_sw128(sW + (uint32_t)(st * Cfg::kWBytes));
         const uint64_t db = desc_kmajor_sw128(sX + (uint32_t)(st * Cfg::kXBytes));
-        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * Cfg::kRows);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * R);
 #pragma unroll
         for (int k = 0; k < kBK / 32; ++k)
           mma_e4m3(d_tmem, da + (uint64_t)(2 * k), db + (uint64_t)(2 * k), idesc, k > 0 ? 1u : 0u);
@@ -2152,21 +2205,23 @@ __global__ void __launch_bounds__(SmallCfg<XQ>::kThreads, 1)
       }
       const uint32_t slot = sSlot + (uint32_t)(st * Cfg::kSlotBytes);
       // a_s of rows 4*lane .. +3 (zero past M)
-      if (!XQ && lane < 4) copy_scales4(slot + 16u * lane, p.sa + (int64_t)kb * p.ldsa, 4 * lane, p.M, p.sa_vec);
-      if (lane == 4) {  // the tile scale of W's 128 x 128 block (nbk, kb)
+      if (!XQ && lane < R / 4) copy_scales4(slot + 16u * lane, p.sa + (int64_t)kb * p.ldsa, 4 * lane, p.M, p.sa_vec);
+      if (lane == 0) {  // the tile scale of W's 128 x 128 block (nbk, kb)
         const float* src = SB_MODE == kSbTile ? p.sb + (int64_t)nbk * p.ldsb + kb : p.sb + (int64_t)kb * p.ldsb + nbk;
-        cp_async_4(slot + 64u, nin ? src : p.sb, nin ? 4u : 0u);
+        cp_async_4(slot + 4u * R, nin ? src : p.sb, nin ? 4u : 0u);
       }
       cp_async_mbar_arrive(sfull_bar(st));
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ promotion, reduction, stores
-    const int nl = 32 * (warp - 4) + lane;  // tensor-memory lane = column n0 + nl
-    const uint32_t lane_base = (uint32_t)(32 * (warp - 4)) << 16;
-    float acc[Cfg::kRows];
+  } else if (promo) {
+    // ------------------------------------------------------------ promotion
+    const int e = warp - 4;
+    const int nl = 32 * (e % 4) + lane;  // tensor-memory lane = column n0 + nl
+    const int h = e / 4;                 // rows h * kCols .. of A
+    const uint32_t lane_base = (uint32_t)(32 * (e % 4)) << 16;
+    float acc[Cfg::kCols];
 #pragma unroll
-    for (int m = 0; m < Cfg::kRows; ++m) acc[m] = 0.0f;
+    for (int m = 0; m < Cfg::kCols; ++m) acc[m] = 0.0f;
     bool ok = true;
     for (int j = 0; j < kbn; ++j) {
       const int st = j % ST, buf = j % NT;
@@ -2179,105 +2234,68 @@ __global__ void __launch_bounds__(SmallCfg<XQ>::kThreads, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t slot = sSlot + (uint32_t)(st * Cfg::kSlotBytes);
-      float as[Cfg::kRows], bsc;
+      const uint32_t slot = sSlot + (uint32_t)(st * Cfg::kSlotBytes) + 4u * (uint32_t)(h * Cfg::kCols);
+      float bsc;
+      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(bsc) : "r"(sSlot + (uint32_t)(st * Cfg::kSlotBytes) + 4u * R));
+      const uint64_t b2 = f2_pack(bsc, bsc);
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(as[4 * q]), "=f"(as[4 * q + 1]), "=f"(as[4 * q + 2]), "=f"(as[4 * q + 3])
-                     : "r"(slot + 16u * q));
-      asm volatile("ld.shared.f32 %0, [%1];" : "=f"(bsc) : "r"(slot + 64u));
-      uint32_t r[Cfg::kRows];
-      tmem_ld_32x32b_x16(tmem_base + lane_base + (uint32_t)(buf * Cfg::kRows), r);
-      tmem_ld_wait();
-      tmem_regs_after_wait(r);
-      // the partial and the scales are in registers: release the buffer and the slot
+      for (int c = 0; c < Cfg::kCols / Cfg::kChunk; ++c) {
+        uint32_t r[Cfg::kChunk];
+        const uint32_t taddr = tmem_base + lane_base + (uint32_t)(buf * R + h * Cfg::kCols + c * Cfg::kChunk);
+        if constexpr (Cfg::kChunk == 32)
+          tmem_ld_32x32b_x32(taddr, r);
+        else
+          tmem_ld_32x32b_x16(taddr, r);
+        tmem_ld_wait();
+        tmem_regs_after_wait(r);
+        // acc[m] += (a_s[m] * b_s) * P[m], two rows per fp32x2 operation
+#pragma unroll
+        for (int q = 0; q < Cfg::kChunk / 4; ++q) {
+          float4 a4;
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(a4.x), "=f"(a4.y), "=f"(a4.z), "=f"(a4.w)
+                       : "r"(slot + 4u * (uint32_t)(c * Cfg::kChunk + 4 * q)));
+          const int m = c * Cfg::kChunk + 4 * q;
+          const uint64_t s01 = f2_mul(f2_pack(a4.x, a4.y), b2), s23 = f2_mul(f2_pack(a4.z, a4.w), b2);
+          f2_unpack(f2_fma(s01, f2_pack(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1])),
+                           f2_pack(acc[m], acc[m + 1])),
+                    acc[m], acc[m + 1]);
+          f2_unpack(f2_fma(s23, f2_pack(__uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])),
+                           f2_pack(acc[m + 2], acc[m + 3])),
+                    acc[m + 2], acc[m + 3]);
+        }
+      }
+      // the partial and the scales have been read: release the buffer and the slot
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(tempty_bar(buf));
         mbar_arrive(sempty_bar(st));
       }
-      // acc[m] += (a_s[m] * b_s) * P[m], two rows per fp32x2 operation
-      const uint64_t b2 = f2_pack(bsc, bsc);
-#pragma unroll
-      for (int m = 0; m < Cfg::kRows; m += 2) {
-        const uint64_t s2 = f2_mul(f2_pack(as[m], as[m + 1]), b2);
-        const uint64_t p2 = f2_pack(__uint_as_float(r[m]), __uint_as_float(r[m + 1]));
-        f2_unpack(f2_fma(s2, p2, f2_pack(acc[m], acc[m + 1])), acc[m], acc[m + 1]);
-      }
     }
-    bool store = ok;
-    if (splits > 1) {
-      cluster_wait_all();  // every peer's barriers exist
-      // The hand-over runs whether or not this CTA's pipeline succeeded, so
-      // that no CTA leaves while another may still signal it: every peer
-      // arrives on the leader's red_full once (with its partial sums if it
-      // has them), the leader waits for all of them before it signals the
-      // peers' red_done and leaves, and a peer leaves after that signal.
-      // (A pipeline that gave up raised its CTA's abort flag, so it reaches
-      // the hand-over within one wait limit; the hand-over's waits allow
-      // two and three.)
-      const uint32_t red = sRed + (uint32_t)(nl * Cfg::kRows * 4);
-      const int nq = (int)((p.M + 3) / 4);  // 4-row chunks that hold rows of the problem
-      if (split != 0) {
-        if (ok) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (q < nq)
-              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(red + 16u * q), "f"(acc[4 * q]),
-                           "f"(acc[4 * q + 1]), "f"(acc[4 * q + 2]), "f"(acc[4 * q + 3])
-                           : "memory");
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(mapa_shared(red_full_bar, 0));
-        const bool done = mbar_wait_cluster_bounded(red_done_bar, 0, 3 * p.wait_limit_ns, never);
-        if (!__all_sync(0xffffffffu, done) && lane == 0) gemm_fail(kErrWaitDrain, abort_flag);
-        store = false;
-      } else {
-        const bool got = mbar_wait_cluster_bounded(red_full_bar, 0, 2 * p.wait_limit_ns, never);
-        if (!__all_sync(0xffffffffu, got && ok && !*abort_flag)) {
-          if (lane == 0 && !got) gemm_fail(kErrWaitDrain, abort_flag);
-          store = false;
-        } else {
-          // the peers' partial sums, added in rank order (each chunk's loads
-          // from every peer issued before the first addition)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            if (q >= nq) break;
-            float4 v[7];
-#pragma unroll
-            for (int s = 1; s < 8; ++s)
-              if (s < splits) v[s - 1] = lds128_cluster(mapa_shared(red + 16u * q, (uint32_t)s));
-#pragma unroll
-            for (int s = 1; s < 8; ++s)
-              if (s < splits) {
-                acc[4 * q] += v[s - 1].x;
-                acc[4 * q + 1] += v[s - 1].y;
-                acc[4 * q + 2] += v[s - 1].z;
-                acc[4 * q + 3] += v[s - 1].w;
-              }
-          }
-        }
-        // the peers may leave once this warp no longer reads their shared memory
-        __syncwarp();
-        if (lane == 0)
-          for (int s = 1; s < splits; ++s) mbar_arrive_cluster_relaxed(mapa_shared(red_done_bar, (uint32_t)s));
-      }
-    }
-    if (store) {
+    if (splits == 1) {
       const int64_t n = n0 + nl;
-      if (n < p.N) {
+      if (ok && n < p.N) {
 #pragma unroll
-        for (int m = 0; m < Cfg::kRows; ++m)
-          if (m < p.M) p.c[(int64_t)m * p.ldc + n] = (uint16_t)(pack_bf16x2(acc[m], 0.0f) & 0xFFFFu);
+        for (int m = 0; m < Cfg::kCols; ++m)
+          if (h * Cfg::kCols + m < p.M)
+            p.c[(int64_t)(h * Cfg::kCols + m) * p.ldc + n] = (uint16_t)(pack_bf16x2(acc[m], 0.0f) & 0xFFFFu);
       }
+    } else if (ok) {
+      // the K-loop is over (every MMA has completed, every copy has landed): the
+      // partial sums go into the W stages, lane n's R rows contiguous
+      const uint32_t part = sW + (uint32_t)((nl * R + h * Cfg::kCols) * 4);
+#pragma unroll
+      for (int q = 0; q < Cfg::kCols / 4; ++q)
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(part + 16u * q), "f"(acc[4 * q]),
+                     "f"(acc[4 * q + 1]), "f"(acc[4 * q + 2]), "f"(acc[4 * q + 3])
+                     : "memory");
     }
-  } else if (XQ && warp >= 8) {
+  } else if (XQ && warp >= 4 + PW) {
     // ------------------------------------------------------------ quantisers (XQ)
-    const int qt = (int)threadIdx.x - 256;
+    const int qt = (int)threadIdx.x - (128 + 32 * PW);
     const int chunk = qt & 7;  // 16 columns of the K-block
-    const int row = qt >> 3;   // 0..15
+    const int row16 = qt >> 3; // rows row16, row16 + 16, ..
     const uint32_t gmask = 0xFFu << (8 * (lane >> 3));  // the 8 lanes of this thread's row
     for (int j = 0; j < kbn; ++j) {
       const int st = j % ST;
@@ -2290,44 +2308,65 @@ __global__ void __launch_bounds__(SmallCfg<XQ>::kThreads, 1)
         break;
       }
       const uint32_t raw = sRaw + (uint32_t)(st * Cfg::kRawBytes);
-      // 16 bf16 values: 16-byte chunks 2*(chunk%4) and +1 of box chunk/4 (128-byte swizzle)
-      const uint32_t rbase = raw + (uint32_t)((chunk >> 2) * (Cfg::kRawBytes / 2) + row * 128);
-      const int c0 = 2 * (chunk & 3);
-      uint4 v0, v1;
-      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                   : "=r"(v0.x), "=r"(v0.y), "=r"(v0.z), "=r"(v0.w)
-                   : "r"(rbase + (uint32_t)(((c0) ^ (row & 7)) << 4)));
-      asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                   : "=r"(v1.x), "=r"(v1.y), "=r"(v1.z), "=r"(v1.w)
-                   : "r"(rbase + (uint32_t)(((c0 + 1) ^ (row & 7)) << 4)));
-      uint32_t m = amax2(amax2(amax2(v0.x, v0.y), amax2(v0.z, v0.w)), amax2(amax2(v1.x, v1.y), amax2(v1.z, v1.w)));
-      m = amax2(m, __shfl_xor_sync(gmask, m, 1));
-      m = amax2(m, __shfl_xor_sync(gmask, m, 2));
-      m = amax2(m, __shfl_xor_sync(gmask, m, 4));
-      m = amax2(m, __byte_perm(m, 0, 0x1032));
-      const float sc = scale_of(__uint_as_float(m & 0x7FFF0000u));
-      const float ny = neg_rcp(sc);
-      const uint64_t s2 = f2_pack(sc, sc), ny2 = f2_pack(ny, ny);
-      const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-      uint32_t q[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        q[k] = __byte_perm(neg_codes2(w[2 * k], s2, ny2), neg_codes2(w[2 * k + 1], s2, ny2), 0x5410) ^ 0x80808080u;
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sX + (uint32_t)(st * Cfg::kXBytes + row * 128) +
-                                                                  (uint32_t)((chunk ^ (row & 7)) << 4)),
-                   "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3])
-                   : "memory");
-      if (chunk == 0)
-        asm volatile("st.shared.f32 [%0], %1;" ::"r"(sSlot + (uint32_t)(st * Cfg::kSlotBytes) + 4u * (uint32_t)row),
-                     "f"(sc)
+      for (int g = 0; g < R / 16; ++g) {
+        const int row = row16 + 16 * g;
+        // 16 bf16 values: 16-byte chunks 2*(chunk%4) and +1 of box chunk/4 (128-byte swizzle)
+        const uint32_t rbase = raw + (uint32_t)((chunk >> 2) * (Cfg::kRawBytes / 2) + row * 128);
+        const int c0 = 2 * (chunk & 3);
+        uint4 v0, v1;
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v0.x), "=r"(v0.y), "=r"(v0.z), "=r"(v0.w)
+                     : "r"(rbase + (uint32_t)(((c0) ^ (row & 7)) << 4)));
+        asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v1.x), "=r"(v1.y), "=r"(v1.z), "=r"(v1.w)
+                     : "r"(rbase + (uint32_t)(((c0 + 1) ^ (row & 7)) << 4)));
+        uint32_t m = amax2(amax2(amax2(v0.x, v0.y), amax2(v0.z, v0.w)), amax2(amax2(v1.x, v1.y), amax2(v1.z, v1.w)));
+        m = amax2(m, __shfl_xor_sync(gmask, m, 1));
+        m = amax2(m, __shfl_xor_sync(gmask, m, 2));
+        m = amax2(m, __shfl_xor_sync(gmask, m, 4));
+        m = amax2(m, __byte_perm(m, 0, 0x1032));
+        const float sc = scale_of(__uint_as_float(m & 0x7FFF0000u));
+        const float ny = neg_rcp(sc);
+        const uint64_t s2 = f2_pack(sc, sc), ny2 = f2_pack(ny, ny);
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint32_t q[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          q[k] = __byte_perm(neg_codes2(w[2 * k], s2, ny2), neg_codes2(w[2 * k + 1], s2, ny2), 0x5410) ^ 0x80808080u;
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(sX + (uint32_t)(st * Cfg::kXBytes + row * 128) +
+                                                                    (uint32_t)((chunk ^ (row & 7)) << 4)),
+                     "r"(q[0]), "r"(q[1]), "r"(q[2]), "r"(q[3])
                      : "memory");
+        if (chunk == 0)
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(sSlot + (uint32_t)(st * Cfg::kSlotBytes) + 4u * (uint32_t)row),
+                       "f"(sc)
+                       : "memory");
+      }
       fence_proxy_async_shared();  // the codes, for the MMA (async proxy)
       mbar_arrive(qfull_bar(st));
     }
   }
 
   __syncwarp();
-  if (splits > 1 && !(warp >= 4 && warp < 8)) cluster_wait_all();  // (the promotion warps waited above)
+  if (splits > 1) {
+    // Every thread of every CTA of the cluster reaches both barriers (no role
+    // leaves the kernel early, and every wait before them is bounded): the
+    // first makes every CTA's partial sums visible, the second keeps each CTA
+    // resident until no peer reads its shared memory any more.  A CTA whose
+    // pipeline gave up has written no partial sums and flagged the error; the
+    // sums stored from it are then not meaningful.
+    cluster_sync_all();
+    if (promo) {
+      const int e = warp - 4;
+      const int nl = 32 * (e % 4) + lane, h = e / 4;
+      if (splits == 2) smallm_reduce_store<R, PW, 2>(sW, split, nl, h, n0, p);
+      else if (splits == 4) smallm_reduce_store<R, PW, 4>(sW, split, nl, h, n0, p);
+      else smallm_reduce_store<R, PW, 8>(sW, split, nl, h, n0, p);
+    }
+    __syncwarp();
+    cluster_sync_all();
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -2467,18 +2506,19 @@ static GemmParams smallm_params(const float* sa, int64_t ldsa, const float* sb, 
 }
 
 // The small-M kernel: T = ceil(N/128) tiles, each split over a cluster of S
-// CTAs (at most 8, at least four K-blocks each), S the largest for which the
-// T clusters are resident at once (one wave); S = 1 launches no cluster.
-template <int MODE, bool XQ>
+// CTAs (S = 8, 4 or 2, at least four K-blocks each, S dividing the rows R),
+// S the largest for which the T clusters are resident at once (one wave);
+// S = 1 launches no cluster.
+template <int MODE, bool XQ, int R>
 static int smallm_splits(int tiles, int Kb, int num_sms) {
-  using Cfg = SmallCfg<XQ>;
+  using Cfg = SmallCfg<XQ, R>;
   static std::once_flag once;
   static int max_clusters[9] = {};
   std::call_once(once, [] {
-    if (cudaFuncSetAttribute(gemm_smallm_kernel<MODE, XQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gemm_smallm_kernel<MODE, XQ, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg::kSmemBytes) != cudaSuccess)
       return;
-    for (int s = 2; s <= 8; ++s) {
+    for (int s = 2; s <= 8; s *= 2) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3((unsigned)(s * 16));
       cfg.blockDim = dim3(Cfg::kThreads);
@@ -2491,26 +2531,27 @@ static int smallm_splits(int tiles, int Kb, int num_sms) {
       cfg.attrs = attr;
       cfg.numAttrs = 1;
       int n = 0;
-      if (cudaOccupancyMaxActiveClusters(&n, gemm_smallm_kernel<MODE, XQ>, &cfg) == cudaSuccess) max_clusters[s] = n;
+      if (cudaOccupancyMaxActiveClusters(&n, gemm_smallm_kernel<MODE, XQ, R>, &cfg) == cudaSuccess)
+        max_clusters[s] = n;
     }
     (void)cudaGetLastError();  // a size the device refuses leaves no error behind
   });
   // at least four K-blocks a CTA: below that the hand-over of the partial
   // sums costs more than the K-blocks it spreads (measured)
-  for (int s = Kb / 4 < 8 ? Kb / 4 : 8; s >= 2; --s)
-    if (tiles * s <= num_sms && tiles <= max_clusters[s]) return s;
+  for (int s = kSmallMaxSplits; s >= 2; s /= 2)
+    if (s <= Kb / 4 && tiles * s <= num_sms && tiles <= max_clusters[s]) return s;
   return 1;
 }
 
-template <int MODE, bool XQ>
+template <int MODE, bool XQ, int R>
 static cudaError_t run_gemm_smallm(const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p, int tiles,
                                    int num_sms, cudaStream_t st) {
-  using Cfg = SmallCfg<XQ>;
-  const int splits = smallm_splits<MODE, XQ>(tiles, p.Kb, num_sms);
+  using Cfg = SmallCfg<XQ, R>;
+  const int splits = smallm_splits<MODE, XQ, R>(tiles, p.Kb, num_sms);
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_smallm_kernel<MODE, XQ>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(gemm_smallm_kernel<MODE, XQ, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     Cfg::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -2528,15 +2569,23 @@ static cudaError_t run_gemm_smallm(const CUtensorMap& mw, const CUtensorMap& mx,
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = splits > 1 ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, gemm_smallm_kernel<MODE, XQ>, mw, mx, p, splits);
+  return cudaLaunchKernelEx(&cfg, gemm_smallm_kernel<MODE, XQ, R>, mw, mx, p, splits);
+}
+
+template <int MODE, bool XQ>
+static cudaError_t run_gemm_smallm_rows(int rows, const CUtensorMap& mw, const CUtensorMap& mx, const GemmParams& p,
+                                        int tiles, int num_sms, cudaStream_t st) {
+  return rows == 16 ? run_gemm_smallm<MODE, XQ, 16>(mw, mx, p, tiles, num_sms, st)
+                    : run_gemm_smallm<MODE, XQ, 32>(mw, mx, p, tiles, num_sms, st);
 }
 
 cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const char** msg,
                         uint64_t wait_limit_ns, int debug_stall) {
   if (smallm_eligible(a.M, a.N, a.sb_mode == kSbCol, num_sms)) {
     // W (B^T, [N, K]) as the MMA's 128-row A; the rows of A as its 16-row B
+    const int rows = smallm_rows(a.M);
     CUtensorMap mw, mx;
-    if (!make_tma_u8(&mw, a.qb, a.K, a.N, a.ldb, kBM) || !make_tma_u8(&mx, a.qa, a.K, a.M, a.lda, 16)) {
+    if (!make_tma_u8(&mw, a.qb, a.K, a.N, a.ldb, kBM) || !make_tma_u8(&mx, a.qa, a.K, a.M, a.lda, rows)) {
       *msg = "cuTensorMapEncodeTiled failed for an operand (alignment, stride or size out of range)";
       return cudaErrorInvalidValue;
     }
@@ -2546,8 +2595,8 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const c
       return cudaErrorInvalidValue;
     }
     const int tiles = (int)cdiv(a.N, kBM);
-    return a.sb_mode == kSbTile ? run_gemm_smallm<kSbTile, false>(mw, mx, p, tiles, num_sms, st)
-                                : run_gemm_smallm<kSbTileT, false>(mw, mx, p, tiles, num_sms, st);
+    return a.sb_mode == kSbTile ? run_gemm_smallm_rows<kSbTile, false>(rows, mw, mx, p, tiles, num_sms, st)
+                                : run_gemm_smallm_rows<kSbTileT, false>(rows, mw, mx, p, tiles, num_sms, st);
   }
   const int bn = gemm_pick_bn(a.M, a.N, a.sb_mode == kSbCol, num_sms);
   const int a_rows = gemm_a_rows(a.M, bn);
@@ -2751,8 +2800,9 @@ static cudaError_t run_gemm_xq(const GemmXqArgs& a, int num_sms, cudaStream_t st
 cudaError_t launch_gemm_xq(const GemmXqArgs& a, int num_sms, cudaStream_t st, const char** msg) {
   if (smallm_eligible(a.M, a.N, false, num_sms)) {
     // the small-M kernel with x quantised in it (same splits as the plain GEMM, so the same bits)
+    const int rows = smallm_rows(a.M);
     CUtensorMap mw, mx;
-    if (!make_tma_u8(&mw, a.qb, a.K, a.N, a.ldb, kBM) || !make_tma_bf16(&mx, a.x, a.K, a.M, a.ldx * 2, 16)) {
+    if (!make_tma_u8(&mw, a.qb, a.K, a.N, a.ldb, kBM) || !make_tma_bf16(&mx, a.x, a.K, a.M, a.ldx * 2, rows)) {
       *msg = "cuTensorMapEncodeTiled failed for an operand (alignment, stride or size out of range)";
       return cudaErrorInvalidValue;
     }
@@ -2761,7 +2811,7 @@ cudaError_t launch_gemm_xq(const GemmXqArgs& a, int num_sms, cudaStream_t st, co
       *msg = "GEMM too large: M, N, K and the number of (tile, K-block) units must stay below 2^31";
       return cudaErrorInvalidValue;
     }
-    return run_gemm_smallm<kSbTile, true>(mw, mx, p, (int)cdiv(a.N, kBM), num_sms, st);
+    return run_gemm_smallm_rows<kSbTile, true>(rows, mw, mx, p, (int)cdiv(a.N, kBM), num_sms, st);
   }
   if (a.M <= 16)
     return gemm_pick_bn(a.M, a.N, false, num_sms) == 64 ? run_gemm_xq<16, 64>(a, num_sms, st, msg)

@@ -167,13 +167,15 @@ BFP8_HD int gemm_epi_warps(bool col_scales, int bn) { return (col_scales || bn >
 // of at most 16 rows, else 128.  With 16, only the promotion warps of lane
 // quarter 0 (e % 4 == 0) hold rows of the problem; the others store nothing.
 BFP8_HD int gemm_a_rows(int64_t M, int bn) { return bn == 64 && M <= 16 ? 16 : kBM; }
-// Small-M GEMMs (at most 16 rows, tile-scale modes) whose 128-column tiles fit
-// in one wave take the operand-swapped kernel: W as the MMA's 128-row A, the
-// rows of A as its 16-row B, and each tile's K-blocks split over a cluster of
-// CTAs.  Split s of S takes K-blocks [smallm_kb_lo(s), smallm_kb_lo(s + 1)).
+// Small-M GEMMs (at most 32 rows, tile-scale modes) whose 128-column tiles
+// fit in one wave take the operand-swapped kernel: W as the MMA's 128-row A,
+// the rows of A as its B (R = 16 or 32 rows: smallm_rows), and each tile's
+// K-blocks split over a cluster of CTAs.  Split s of S takes K-blocks
+// [smallm_kb_lo(s), smallm_kb_lo(s + 1)).
 BFP8_HD bool smallm_eligible(int64_t M, int64_t N, bool col_scales, int num_sms) {
-  return M >= 1 && M <= 16 && !col_scales && (N + kBM - 1) / kBM <= num_sms;
+  return M >= 1 && M <= 32 && !col_scales && (N + kBM - 1) / kBM <= num_sms;
 }
+BFP8_HD int smallm_rows(int64_t M) { return M <= 16 ? 16 : 32; }
 BFP8_HD int smallm_kb_lo(int s, int splits, int Kb) { return (int)((int64_t)s * Kb / splits); }
 BFP8_HD int epi_row(int e, int lane) { return 32 * (e % 4) + lane; }
 BFP8_HD int epi_cols(int bn, int ew) { return bn / (ew / 4); }

@@ -404,13 +404,17 @@ def test_gemm_few_tiles_deep_k_matches_oracle(M, N, K, mode):
     B.check_device_errors()
 
 
-# at most 16 rows, tile-scale modes: the operand-swapped kernel whose tiles'
+# at most 32 rows, tile-scale modes: the operand-swapped kernel whose tiles'
 # K-blocks are split over a cluster of CTAs (152 SMs: 16x4096x4096 4 splits;
-# 1x130x8192 8; 5x2051x1100 8 over 9 K-blocks; 3x512x384 3, one K-block each;
-# 7x18944 148 tiles, 1 split; 12x19456 152 tiles, 1 split; 2x19584 153 tiles:
-# the 64/128-column kernel), launched twice in a row
+# 1x130x8192 2; 5x2051x1100 2 over 9 K-blocks; 3x512x384 one; 7x18944 148
+# tiles, one split; 12x19456 152 tiles, one split; 2x19584 153 tiles: the
+# 64/128-column kernel; 8x1024x8192 8 splits; 17 and 32 rows: its 32-row form),
+# and from 33 rows the dense kernel's tiles at the same kind of shapes;
+# launched twice in a row
 SMALLM_SHAPES = [(16, 4096, 4096), (1, 130, 8192), (5, 2051, 1100), (3, 512, 384), (7, 18944, 384),
-                 (12, 19456, 256), (2, 19584, 256)]
+                 (12, 19456, 256), (2, 19584, 256), (8, 1024, 8192),
+                 (17, 4096, 4096), (32, 512, 2048), (33, 2051, 1100), (64, 4096, 4096), (100, 3000, 2048),
+                 (128, 4096, 4096), (128, 18944, 384), (65, 19456, 256), (128, 1024, 16384)]
 
 
 @pytest.mark.parametrize("M,N,K", SMALLM_SHAPES)

@@ -34,8 +34,10 @@ def _setup():
 SMALL_M = [(m, n, k) for m in (2, 4, 128, 512) for (n, k) in ((512, 128), (5120, 1280), (3584, 640), (4096, 4096))]
 TAILS = [(1, 130, 256), (3, 384, 136), (130, 300, 520), (257, 1000, 1024), (64, 2051, 128), (300, 640, 4096)]
 # M <= 16 with enough columns that 128-column tiles fill more than half the
-# SMs: 16-row x tiles with 128-column tiles instead of the narrow 64-column ones
-WIDE = [(4, 12288, 256), (16, 9856, 520)]
+# SMs; 17..32 rows (the small-M kernel's 32-row form, its quantiser in two
+# passes of 16 rows); 153 tiles of 128 columns (beyond one wave: the dense
+# forward's tiles on both paths)
+WIDE = [(4, 12288, 256), (16, 9856, 520), (24, 4096, 4096), (32, 5120, 1280), (17, 130, 520), (20, 19584, 256)]
 
 
 def _guarded_out(M, N, ldc):
