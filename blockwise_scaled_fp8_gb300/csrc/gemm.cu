@@ -2011,24 +2011,31 @@ struct SmallCfg {
 // thread's share of a CTA's rows is at least two values (8-byte loads).
 constexpr int kSmallMaxSplits = 8;
 
+// The partial sums of lane n: R fp32 in 16-byte chunks, chunk c stored at
+// position c ^ smallm_swz(n), so that a warp's 32 lanes (rows R*4 bytes
+// apart) spread over all eight 16-byte bank groups.
+template <int R>
+__device__ __forceinline__ uint32_t smallm_part_addr(uint32_t part, int n, int m) {
+  const int swz = R >= 32 ? (n & 7) : ((n >> 1) & (R / 4 - 1));
+  return part + (uint32_t)(n * R * 4) + (uint32_t)((((m >> 2) ^ swz) << 4) + (m & 3) * 4);
+}
+
 // CTA `rank` of S: rows rank R/S .. of the tile, summed over the S partials
-// (at `part` in every CTA's shared memory, 128 x R fp32, row-major by lane
-// n) in rank order and stored as bf16.  Thread (nl, h): column n0 + nl,
-// rows rank R/S + h CW .. + CW - 1.
+// (at `part` in every CTA's shared memory, 128 x R fp32 by lane n, chunks
+// swizzled) in rank order and stored as bf16.  Thread (nl, h): column
+// n0 + nl, rows rank R/S + h CW .. + CW - 1.
 template <int R, int PW, int S>
 __device__ __forceinline__ void smallm_reduce_store(uint32_t part, int rank, int nl, int h, int n0, const GemmParams& p) {
   constexpr int CW = R / S / (PW / 4);
   static_assert(CW % 2 == 0, "whole 8-byte loads");
   const int m0 = rank * (R / S) + h * CW;
-  const uint32_t src = part + (uint32_t)((nl * R + m0) * 4);
   float v[S][CW];
 #pragma unroll
   for (int s = 0; s < S; ++s) {
-    const uint32_t a = mapa_shared(src, (uint32_t)s);
     if constexpr (CW % 4 == 0) {
 #pragma unroll
       for (int q = 0; q < CW / 4; ++q) {
-        const float4 t = lds128_cluster(a + 16u * q);
+        const float4 t = lds128_cluster(mapa_shared(smallm_part_addr<R>(part, nl, m0 + 4 * q), (uint32_t)s));
         v[s][4 * q] = t.x;
         v[s][4 * q + 1] = t.y;
         v[s][4 * q + 2] = t.z;
@@ -2037,7 +2044,7 @@ __device__ __forceinline__ void smallm_reduce_store(uint32_t part, int rank, int
     } else {
 #pragma unroll
       for (int q = 0; q < CW / 2; ++q) {
-        const float2 t = lds64_cluster(a + 8u * q);
+        const float2 t = lds64_cluster(mapa_shared(smallm_part_addr<R>(part, nl, m0 + 2 * q), (uint32_t)s));
         v[s][2 * q] = t.x;
         v[s][2 * q + 1] = t.y;
       }
@@ -2283,11 +2290,11 @@ __global__ void __launch_bounds__(SmallCfg<XQ, R>::kThreads, 1)
       }
     } else if (ok) {
       // the K-loop is over (every MMA has completed, every copy has landed): the
-      // partial sums go into the W stages, lane n's R rows contiguous
-      const uint32_t part = sW + (uint32_t)((nl * R + h * Cfg::kCols) * 4);
+      // partial sums go into the W stages
 #pragma unroll
       for (int q = 0; q < Cfg::kCols / 4; ++q)
-        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(part + 16u * q), "f"(acc[4 * q]),
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(smallm_part_addr<R>(sW, nl, h * Cfg::kCols + 4 * q)),
+                     "f"(acc[4 * q]),
                      "f"(acc[4 * q + 1]), "f"(acc[4 * q + 2]), "f"(acc[4 * q + 3])
                      : "memory");
     }
