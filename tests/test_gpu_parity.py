@@ -470,7 +470,8 @@ def test_linear_fwd_matches_oracle(M, N, K):
     assert_gemm_close(host_bf16_as_f64(y), O.linear_fwd(x, w), f"fwd {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("M,N,K", [(130, 384, 256), (257, 300, 131), (512, 1024, 640), (1024, 256, 512)])
+@pytest.mark.parametrize("M,N,K", [(130, 384, 256), (257, 300, 131), (512, 1024, 640), (1024, 256, 512),
+                                   (4, 384, 256), (32, 1024, 1280)])
 def test_linear_bwd_matches_oracle(M, N, K):
     x, w, dy = _dev_linear(M, N, K, seed=4)
     dx, dw = B.linear_bwd(dev_bf16(dy), dev_bf16(x), dev_bf16(w))
@@ -479,7 +480,8 @@ def test_linear_bwd_matches_oracle(M, N, K):
     assert_gemm_close(host_bf16_as_f64(dw), O.linear_wgrad(dy, x), f"wgrad {M}x{N}x{K}")
 
 
-@pytest.mark.parametrize("M,N,K", [(130, 384, 256), (257, 300, 131), (512, 1024, 640), (2048, 4096, 4096)])
+@pytest.mark.parametrize("M,N,K", [(130, 384, 256), (257, 300, 131), (512, 1024, 640), (2048, 4096, 4096),
+                                   (2, 4096, 4096), (24, 640, 1280)])
 def test_linear_train_form_matches_oracle(M, N, K):
     """fwd_train keeps the quantised x (both forms) and W (both forms) in the
     workspace; bwd_saved quantises dY once and runs both gradient GEMMs."""

@@ -31,7 +31,7 @@ def _setup():
 def test_static_scratch_forward_matches_workspace_forward_on_two_calls():
     # two calls in a row with different problems: the second reuses the array
     # (and finds the first call's bytes in it)
-    for (M, N, K, seed) in ((1024, 2048, 1024, 1), (300, 640, 520, 2)):
+    for (M, N, K, seed) in ((1024, 2048, 1024, 1), (300, 640, 520, 2), (4, 4096, 2048, 3)):
         x = S.normal_bf16((M, K), 1.0, seed=seed * 16, outlier_frac=1e-3)
         w = S.normal_bf16((N, K), 0.02, seed=seed * 16 + 1)
         xd, wd = dev_bf16(x), dev_bf16(w)
