@@ -2418,10 +2418,14 @@ static bool make_tma_u8(CUtensorMap* map, const void* base, int64_t inner, int64
 
 int gemm_pick_bn(int64_t M, int64_t N, bool col_scales, int num_sms) {
   // Problems whose 128-column tiles would occupy at most half the SMs (small
-  // M: decoding, skinny layers) take 64-column tiles with more tensor-memory
-  // buffers: twice the CTAs streaming B, and MMAs that run ahead of the
-  // promotion.  (1x128 x 128x128 modes only: the column-scale GEMM reduces
-  // over tokens and is not small in both M and N.)
+  // M: decoding, skinny layers) take narrow tiles with more tensor-memory
+  // buffers: more CTAs streaming B, and MMAs that run ahead of the
+  // promotion.  32 columns where those tiles still fit in one wave of SMs
+  // (every CTA reads all of A through its own L2 port, so a CTA's bytes per
+  // K-block, 16 KiB of A + BN x 128 of B, set its pace), else 64.
+  // (1x128 x 128x128 modes only: the column-scale GEMM reduces over tokens
+  // and is not small in both M and N.)
+  if (!col_scales && cdiv(M, kBM) * cdiv(N, 32) <= num_sms) return 32;
   if (!col_scales && 2 * cdiv(M, kBM) * cdiv(N, 128) <= num_sms) return 64;
   if (N <= 128) return 128;
   const int64_t tiles256 = cdiv(M, kBM) * cdiv(N, 256);
@@ -2639,6 +2643,11 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const c
   p.wait_limit_ns = wait_limit_ns;
   p.debug_stall = debug_stall;
   const int64_t grid = gemm_grid(a.M, a.N, bn, num_sms);
+  // 32-column tiles (tile-scale modes): ten stages of 16 + 4 KiB, sixteen
+  // tensor-memory buffers
+  if (bn == 32)
+    return a.sb_mode == kSbTile ? run_gemm<32, 10, kSbTile>(ma, mb, p, grid, st)
+                                : run_gemm<32, 10, kSbTileT>(ma, mb, p, grid, st);
   // 64-column tiles (tile-scale modes): sixteen stages of 2 + 8 KiB with
   // 16-row A boxes, else eight of 16 + 8 KiB
   if (bn == 64) {
@@ -2821,7 +2830,7 @@ cudaError_t launch_gemm_xq(const GemmXqArgs& a, int num_sms, cudaStream_t st, co
     return run_gemm_smallm_rows<kSbTile, true>(rows, mw, mx, p, (int)cdiv(a.N, kBM), num_sms, st);
   }
   if (a.M <= 16)
-    return gemm_pick_bn(a.M, a.N, false, num_sms) == 64 ? run_gemm_xq<16, 64>(a, num_sms, st, msg)
+    return gemm_pick_bn(a.M, a.N, false, num_sms) <= 64 ? run_gemm_xq<16, 64>(a, num_sms, st, msg)
                                                          : run_gemm_xq<16, 128>(a, num_sms, st, msg);
   return run_gemm_xq<128, 128>(a, num_sms, st, msg);
 }

@@ -316,12 +316,15 @@ def test_gemm_epilogue_index_replay_exactly_once(M, N, K, col_scales):
 
 
 def test_gemm_tile_width_choice():
-    """Tile widths the launcher picks (host logic, 152 SMs): narrow 64-column
-    tiles for problems that fill few SMs (1x128 x 128x128 only), 224 columns
-    for the 1x128 x 128x1 GEMM where they fill the last wave of SMs better
-    than 256, else 256 or 128."""
+    """Tile widths the launcher picks (host logic, 152 SMs): narrow tiles for
+    problems that fill few SMs (1x128 x 128x128 only) -- 32 columns where
+    those tiles fit in one wave, else 64 --, 224 columns for the 1x128 x 128x1
+    GEMM where they fill the last wave of SMs better than 256, else 256 or
+    128."""
     pick = lambda M, N, col=False: B.lib().bfp8_debug_gemm_pick_bn(M, N, int(col), 152)
-    assert pick(2, 4096) == 64 and pick(128, 5120) == 64       # 32 / 40 tiles of 128: narrow
+    assert pick(128, 4096) == 32 and pick(33, 4864) == 32      # 128 / 152 tiles of 32: one wave
+    assert pick(256, 2432) == 32 and pick(128, 512) == 32
+    assert pick(33, 4865) == 64 and pick(128, 5120) == 64      # 153 / 160 tiles of 32; 38 / 40 of 128
     assert pick(2, 4096, True) == 128                          # the 128x1 GEMM never narrows
     assert pick(2048, 4096) == 256 and pick(2048, 4096, True) == 224   # 256 tiles = 1.68 waves; 304 = 2
     assert pick(4096, 4096, True) == 224                       # 512 tiles = 3.37 waves; 608 = 4
