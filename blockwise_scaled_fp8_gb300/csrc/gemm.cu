@@ -74,6 +74,7 @@ struct GemmParams {
   int sb_vec;  // 16-byte b_s copies allowed (ldsb % 4 == 0, sb 16-byte aligned)
   uint64_t wait_limit_ns;
   int debug_stall;  // test hook: the promotion warps wait on a barrier nothing arrives on
+  int c_tma = 0;    // (dense kernel, 256-column tiles) the epilogue stores through the C tensor map
 };
 
 // What the grouped (mixture-of-experts) forms add.  A separate kernel
@@ -156,6 +157,14 @@ struct GemmCfg {
   static constexpr int kNumBars = 2 * STAGES + 2 * kBufs + 2 + 2 * kScaleSlots;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-byte alignment
+  // Dense kernel, 256-column tiles: the epilogue of the tile-scale modes can
+  // leave through TMA stores, each promotion warp staging its 32 rows x 64
+  // columns of bf16 (4 KiB, 128-byte swizzled rows) in a buffer of its own.
+  // (The column-scale mode measured 7% slower with it: its promotion loop,
+  // not its few tiles' epilogues, sets its pace.)
+  static constexpr bool kEpiTma = BN == 256 && EW == 16 && A_ROWS == 128;
+  static constexpr int kOffStage = (kOffMisc + 16 + 1023) / 1024 * 1024;
+  static constexpr int kDenseSmemBytes = kEpiTma ? kOffStage + EW * 4096 + 1024 : kSmemBytes;
   // grouped forms only: the experts' offsets and first tiles
   static constexpr int kGroupTabBytes = 2 * (kMaxGroups + 1) * 4;
   static_assert(kSmemBytes + kGroupTabBytes <= 227 * 1024, "shared memory budget");
@@ -291,8 +300,8 @@ __device__ __forceinline__ GemmJob gemm_job(int tile, const GemmParams& p, const
 
 template <int BN, int STAGES, int SB_MODE, int LDW, int EW, int A_ROWS = 128>
 __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW, A_ROWS>::kThreads, 1)
-    gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tma_a,
-                          const __grid_constant__ CUtensorMap tma_b, const GemmParams p) {
+    gemm_blockwise_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+                          const __grid_constant__ CUtensorMap tma_c, const GemmParams p) {
   using Cfg = GemmCfg<BN, STAGES, EW, A_ROWS>;
   constexpr int kCols = Cfg::kCols;
   constexpr int NT = Cfg::kBufs;
@@ -351,6 +360,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW, A_ROWS>::kThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tma_a);
     tma_prefetch_desc(&tma_b);
+    if (Cfg::kEpiTma && SB_MODE != kSbCol && p.c_tma) tma_prefetch_desc(&tma_c);
   }
   tc_fence_before();
   __syncthreads();
@@ -607,7 +617,29 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW, A_ROWS>::kThreads, 1)
       // group holds chunk pos of the group's G rows; each store instruction of
       // the warp then writes 32/G row segments of 16*G contiguous bytes.  Only
       // rows < M and columns < N are written.
-      {
+      if (Cfg::kEpiTma && SB_MODE != kSbCol && p.c_tma) {
+        // TMA-store epilogue: this warp's 32 rows x 64 columns, rounded to
+        // bf16, into its staging buffer (16-byte chunk c of row r at c ^ (r & 7):
+        // the 128-byte swizzle of the map, and conflict-free for the eight rows
+        // of a quarter-warp), then one store of the box at (n0 + col0, m0 + 32 *
+        // (warp % 4)); the map clips rows >= M and columns >= N (N % 8 == 0).
+        const uint32_t stg = sbase + (uint32_t)(Cfg::kOffStage + e * 4096);
+        if (lane == 0) bulk_wait_read_all();  // the previous tile's store has read the buffer
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(stg + 128u * lane + ((uint32_t)(c ^ (lane & 7)) << 4)),
+                       "r"(pack_bf16x2(acc[8 * c], acc[8 * c + 1])), "r"(pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3])),
+                       "r"(pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5])), "r"(pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]))
+                       : "memory");
+        fence_proxy_async_shared();
+        __syncwarp();
+        const int bm = g.m0 + 32 * (warp % 4), bn0 = g.n0 + col0;
+        if (lane == 0 && bm < p.M && bn0 < p.N) {
+          tma_store_2d(&tma_c, stg, bn0, bm);
+          bulk_commit();
+        }
+      } else {
         // chunks per transposed block and passes (epi_group, epi_passes): a
         // share of 56 columns is 7 chunks in one block of 8, the eighth empty
         constexpr int kChunks = kCols / 8;
@@ -656,6 +688,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW, A_ROWS>::kThreads, 1)
         }
       }
     }
+    // this warp's TMA stores complete before the CTA's shared memory goes away
+    if (Cfg::kEpiTma && SB_MODE != kSbCol && p.c_tma && lane == 0) bulk_wait_all();
   }
 
   __syncwarp();
@@ -2416,6 +2450,9 @@ static bool make_tma_u8(CUtensorMap* map, const void* base, int64_t inner, int64
   return r == CUDA_SUCCESS;
 }
 
+static bool make_tma_bf16(CUtensorMap* map, const void* base, int64_t inner, int64_t rows, int64_t ld_bytes,
+                          int box_rows);
+
 int gemm_pick_bn(int64_t M, int64_t N, bool col_scales, int num_sms) {
   // Problems whose 128-column tiles would occupy at most half the SMs (small
   // M: decoding, skinny layers) take narrow tiles with more tensor-memory
@@ -2465,11 +2502,13 @@ constexpr int gemm_ldw() {
 
 template <int BN, int STAGES, int MODE, int GROUP = kGroupNone, int A_ROWS = 128>
 static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int64_t grid,
-                            cudaStream_t st, const GemmGroupParams* gp = nullptr) {
+                            cudaStream_t st, const GemmGroupParams* gp = nullptr, const CUtensorMap* mc = nullptr) {
   constexpr int EW = gemm_ew<MODE, BN>(), LDW = gemm_ldw<BN, MODE, EW>();
   static_assert(GROUP == kGroupNone || A_ROWS == 128, "the grouped forms load 128-row A boxes");
   using Cfg = GemmCfg<BN, STAGES, EW, A_ROWS>;
-  constexpr int kSmem = Cfg::kSmemBytes + (GROUP != kGroupNone ? Cfg::kGroupTabBytes : 0);
+  constexpr int kSmem = GROUP != kGroupNone ? Cfg::kSmemBytes + Cfg::kGroupTabBytes
+                       : MODE != kSbCol     ? Cfg::kDenseSmemBytes
+                                            : Cfg::kSmemBytes;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -2481,9 +2520,13 @@ static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const 
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  if constexpr (GROUP == kGroupNone)
+  if constexpr (GROUP == kGroupNone) {
+    static_assert(Cfg::kDenseSmemBytes <= 227 * 1024, "shared memory budget (epilogue staging)");
+    CUtensorMap none;  // (no C map: the kernel does not read it)
+    if (!mc) memset(&none, 0, sizeof none);
     return launch_pdl(gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW, A_ROWS>, (unsigned)grid, Cfg::kThreads,
-                      kSmem, st, ma, mb, p);
+                      kSmem, st, ma, mb, mc ? *mc : none, p);
+  }
   else
     return launch_pdl(gemm_grouped_kernel<BN, STAGES, MODE, LDW, EW, GROUP>, (unsigned)grid, Cfg::kThreads, kSmem,
                       st, ma, mb, p, *gp);
@@ -2660,12 +2703,18 @@ cudaError_t launch_gemm(const GemmArgs& a, int num_sms, cudaStream_t st, const c
   // 224-column tiles (the 1x128 x 128x1 GEMM only): three stages of 44 KiB
   if (bn == 224) return run_gemm<224, 3, kSbCol>(ma, mb, p, grid, st);
   // 256-column tiles: three stages of 48 KiB (four measured no faster, and a
-  // little slower for the weight gradient)
+  // little slower for the weight gradient).  Their epilogue stores through a
+  // tensor map of C (32-row x 64-column boxes) in the tile-scale modes, where
+  // the map can clip at exactly N: 16-byte rows of C and N % 8 == 0; else
+  // the warps store.
   if (bn == 256) {
+    CUtensorMap mc;
+    memset(&mc, 0, sizeof mc);
+    p.c_tma = a.sb_mode != kSbCol && p.c_vec && a.N % 8 == 0 && make_tma_bf16(&mc, a.c, a.N, a.M, a.ldc * 2, 32);
     switch (a.sb_mode) {
-      case kSbTile: return run_gemm<256, 3, kSbTile>(ma, mb, p, grid, st);
-      case kSbTileT: return run_gemm<256, 3, kSbTileT>(ma, mb, p, grid, st);
-      default: return run_gemm<256, 3, kSbCol>(ma, mb, p, grid, st);
+      case kSbTile: return run_gemm<256, 3, kSbTile>(ma, mb, p, grid, st, nullptr, &mc);
+      case kSbTileT: return run_gemm<256, 3, kSbTileT>(ma, mb, p, grid, st, nullptr, &mc);
+      default: return run_gemm<256, 3, kSbCol>(ma, mb, p, grid, st, nullptr, &mc);
     }
   }
   switch (a.sb_mode) {
