@@ -404,6 +404,21 @@ def test_gemm_few_tiles_deep_k_matches_oracle(M, N, K, mode):
     B.check_device_errors()
 
 
+# 128-column tiles (fewer 256-column tiles than SMs, too many 32- or
+# 64-column ones for one wave), ragged M, N and K; 512 x 5120 has 160 tiles
+# on 152 SMs, so some CTAs walk a second tile; launched twice in a row
+MID_M_SHAPES = [(512, 4096, 1024), (500, 4000, 1000), (384, 4004, 640), (512, 5120, 1280)]
+
+
+@pytest.mark.parametrize("M,N,K", MID_M_SHAPES)
+@pytest.mark.parametrize("mode", [O.SB_TILE, O.SB_TILE_T])
+def test_gemm_128_column_tiles_match_oracle(M, N, K, mode):
+    assert B.lib().bfp8_debug_gemm_pick_bn(M, N, 0, 152) == 128
+    got, ref = _gemm_case(M, N, K, mode, seed=13 * M + N + K + mode, ldc_extra=8, repeats=2)
+    assert_gemm_close(got, ref, f"128-column-tile gemm mode {mode} {M}x{N}x{K}")
+    B.check_device_errors()
+
+
 # at most 32 rows, tile-scale modes: the operand-swapped kernel whose tiles'
 # K-blocks are split over a cluster of CTAs (152 SMs: 16x4096x4096 4 splits;
 # 1x130x8192 2; 5x2051x1100 2 over 9 K-blocks; 3x512x384 one; 7x18944 148
