@@ -88,6 +88,7 @@ struct GemmGroupParams {
   int b_k_step;         // per expert: first K column of its B in the B map (input gradient)
   int64_t sb_step;      // per expert: offset of its b_s (elements)
   int64_t c_step;       // per expert: offset of its C (elements; weight gradient)
+  int c_rows = 0;       // c_step / ldc where the epilogue stores through the C map (weight gradient)
 };
 
 // One output tile's work: where its operands sit in the two tensor maps, its
@@ -706,12 +707,17 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW, A_ROWS>::kThreads, 1)
 // output found through its GemmJob.  (The dense GEMM keeps its own kernel:
 // its weight-gradient form sits at the register limit of the promotion warps,
 // and the job indirection measured 10-17% slower there.)
-template <int BN, int STAGES, int SB_MODE, int LDW, int EW, int GROUP>
+template <int BN, int STAGES, int SB_MODE, int LDW, int EW, int GROUP, bool STG = false>
 __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
-    gemm_grouped_kernel(const __grid_constant__ CUtensorMap tma_a,
-                        const __grid_constant__ CUtensorMap tma_b, const GemmParams p, const GemmGroupParams gp) {
+    gemm_grouped_kernel(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+                        const __grid_constant__ CUtensorMap tma_c, const GemmParams p, const GemmGroupParams gp) {
   static_assert(GROUP == kGroupRows || GROUP == kGroupRed, "a grouped form");
   using Cfg = GemmCfg<BN, STAGES, EW>;
+  // STG: the epilogue may store through the C map from per-warp staging
+  // buffers placed after an expert table of at most kStageGroups experts
+  static_assert(!STG || Cfg::kEpiTma, "staged epilogue: 64 columns per promotion warp");
+  constexpr int kTab = STG ? kStageGroups : kMaxGroups;
+  constexpr uint32_t kOffStageG = (uint32_t)((Cfg::kOffMisc + 16 + 2 * (kTab + 1) * 4 + 1023) / 1024 * 1024);
   static_assert(Cfg::kBufs == 2 && Cfg::kTileScales == BN / 128, "the grouped forms use tiles of 128 or 256 columns");
   constexpr int kCols = Cfg::kCols;
   extern __shared__ uint8_t smem_raw[];
@@ -727,7 +733,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
   volatile int* never = reinterpret_cast<volatile int*>(smem + Cfg::kOffMisc + 8);
   // grouped forms: the experts' offsets and first tiles (kGroupTabBytes past the barriers)
   int* s_offs = reinterpret_cast<int*>(smem + Cfg::kOffMisc + 16);
-  int* s_start = s_offs + (kMaxGroups + 1);
+  int* s_start = s_offs + (kTab + 1);
 
   // barriers: full[S], empty[S], tfull[2], tempty[2], drain (both issuers), stall, sfull[2], sempty[2]
   auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
@@ -996,8 +1002,28 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
       // group holds chunk pos of the group's G rows; each store instruction of
       // the warp then writes 32/G row segments of 16*G contiguous bytes.  Only
       // rows < M and columns < N are written.
-      {
-        const GemmJob job = gemm_job<GROUP, BN>(tile, p, gp, s_offs, s_start);
+      const GemmJob job = gemm_job<GROUP, BN>(tile, p, gp, s_offs, s_start);
+      if (STG && p.c_tma && 32 * (warp % 4) + 32 <= job.rows) {
+        // all 32 of this warp's rows belong to the job: stage them as bf16
+        // (128-byte swizzled rows) and store the block through the C map at
+        // (n0 + col0, the rows' first row of C); the map clips columns >= N
+        const uint32_t stg = sbase + kOffStageG + (uint32_t)(e * 4096);
+        if (lane == 0) bulk_wait_read_all();  // the previous tile's store has read the buffer
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(stg + 128u * lane + ((uint32_t)(c ^ (lane & 7)) << 4)),
+                       "r"(pack_bf16x2(acc[8 * c], acc[8 * c + 1])), "r"(pack_bf16x2(acc[8 * c + 2], acc[8 * c + 3])),
+                       "r"(pack_bf16x2(acc[8 * c + 4], acc[8 * c + 5])), "r"(pack_bf16x2(acc[8 * c + 6], acc[8 * c + 7]))
+                       : "memory");
+        fence_proxy_async_shared();
+        __syncwarp();
+        const int crow = (GROUP == kGroupRows ? job.a_row : job.e * gp.c_rows + job.a_row) + 32 * (warp % 4);
+        if (lane == 0 && job.n0 + col0 < p.N) {
+          tma_store_2d(&tma_c, stg, job.n0 + col0, crow);
+          bulk_commit();
+        }
+      } else {
         constexpr int kG = kCols / 8 >= 8 ? 8 : kCols / 8;  // chunks per transposed block (epi_group)
         const int pos = lane % kG;
 #pragma unroll
@@ -1042,6 +1068,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
         }
       }
     }
+    // this warp's TMA stores complete before the CTA's shared memory goes away
+    if (STG && p.c_tma && lane == 0) bulk_wait_all();
   }
 
   __syncwarp();
@@ -2500,15 +2528,20 @@ constexpr int gemm_ldw() {
   return EW == 16 ? (BN >= 224 && MODE != kSbCol ? 32 : 16) : (MODE != kSbCol ? (BN >= 128 ? 64 : BN / 2) : 32);
 }
 
-template <int BN, int STAGES, int MODE, int GROUP = kGroupNone, int A_ROWS = 128>
+template <int BN, int STAGES, int MODE, int GROUP = kGroupNone, int A_ROWS = 128, bool STG = false>
 static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, int64_t grid,
                             cudaStream_t st, const GemmGroupParams* gp = nullptr, const CUtensorMap* mc = nullptr) {
   constexpr int EW = gemm_ew<MODE, BN>(), LDW = gemm_ldw<BN, MODE, EW>();
   static_assert(GROUP == kGroupNone || A_ROWS == 128, "the grouped forms load 128-row A boxes");
   using Cfg = GemmCfg<BN, STAGES, EW, A_ROWS>;
-  constexpr int kSmem = GROUP != kGroupNone ? Cfg::kSmemBytes + Cfg::kGroupTabBytes
-                       : MODE != kSbCol     ? Cfg::kDenseSmemBytes
+  // grouped forms with the staged epilogue: the table for kStageGroups
+  // experts, then (1024-aligned) the staging buffers
+  constexpr int kStgSmem = (Cfg::kOffMisc + 16 + 2 * (kStageGroups + 1) * 4 + 1023) / 1024 * 1024 + EW * 4096 + 1024;
+  constexpr int kSmem = GROUP != kGroupNone ? (STG ? kStgSmem : Cfg::kSmemBytes + Cfg::kGroupTabBytes)
+                        : MODE != kSbCol    ? Cfg::kDenseSmemBytes
                                             : Cfg::kSmemBytes;
+  static_assert(!STG || (GROUP != kGroupNone && Cfg::kEpiTma && kStgSmem <= 227 * 1024),
+                "staged grouped epilogue: shared memory budget");
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -2516,7 +2549,7 @@ static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const 
       attr_err = cudaFuncSetAttribute(gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW, A_ROWS>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     else
-      attr_err = cudaFuncSetAttribute(gemm_grouped_kernel<BN, STAGES, MODE, LDW, EW, GROUP>,
+      attr_err = cudaFuncSetAttribute(gemm_grouped_kernel<BN, STAGES, MODE, LDW, EW, GROUP, STG>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -2527,9 +2560,12 @@ static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const 
     return launch_pdl(gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW, A_ROWS>, (unsigned)grid, Cfg::kThreads,
                       kSmem, st, ma, mb, mc ? *mc : none, p);
   }
-  else
-    return launch_pdl(gemm_grouped_kernel<BN, STAGES, MODE, LDW, EW, GROUP>, (unsigned)grid, Cfg::kThreads, kSmem,
-                      st, ma, mb, p, *gp);
+  else {
+    CUtensorMap none;  // (no C map: the kernel does not read it)
+    if (!mc) memset(&none, 0, sizeof none);
+    return launch_pdl(gemm_grouped_kernel<BN, STAGES, MODE, LDW, EW, GROUP, STG>, (unsigned)grid, Cfg::kThreads,
+                      kSmem, st, ma, mb, mc ? *mc : none, p, *gp);
+  }
 }
 
 // Parameters of the small-M kernel (Kb = -1 when a size is out of range).
@@ -2784,14 +2820,35 @@ cudaError_t launch_gemm_grouped(const GemmGroupArgs& ga, int num_sms, cudaStream
   gp.sb_step = ga.sb_step;
   gp.c_step = ga.c_step;
   const int64_t grid = tiles_max < num_sms ? (tiles_max > 0 ? tiles_max : 1) : num_sms;
+  // 256-column tiles of at most kStageGroups experts, with 16-byte rows of C,
+  // N % 8 == 0 and (weight gradient) the experts' outputs whole rows apart:
+  // the staged TMA-store epilogue, through one map over all experts' rows of C
+  // (three stages, to make room for the staging buffers)
+  CUtensorMap mc;
+  memset(&mc, 0, sizeof mc);
+  if (bn == 256 && E <= kStageGroups && p.c_vec && a.N % 8 == 0 &&
+      (rows || (ga.c_step % a.ldc == 0 && ga.c_step / a.ldc >= a.M))) {
+    const int64_t c_rows_total = rows ? ga.M_total : (E - 1) * (ga.c_step / a.ldc) + a.M;
+    gp.c_rows = rows ? 0 : (int)(ga.c_step / a.ldc);
+    p.c_tma = c_rows_total > 0 && c_rows_total < ((int64_t)1 << 31) &&
+              make_tma_bf16(&mc, a.c, a.N, c_rows_total, a.ldc * 2, 32);
+  }
   if (rows) {
-    if (bn == 256)
+    if (bn == 256) {
+      if (p.c_tma)
+        return a.sb_mode == kSbTile
+                   ? run_gemm<256, 3, kSbTile, kGroupRows, 128, true>(ma, mb, p, grid, st, &gp, &mc)
+                   : run_gemm<256, 3, kSbTileT, kGroupRows, 128, true>(ma, mb, p, grid, st, &gp, &mc);
       return a.sb_mode == kSbTile ? run_gemm<256, 4, kSbTile, kGroupRows>(ma, mb, p, grid, st, &gp)
                                   : run_gemm<256, 4, kSbTileT, kGroupRows>(ma, mb, p, grid, st, &gp);
+    }
     return a.sb_mode == kSbTile ? run_gemm<128, 6, kSbTile, kGroupRows>(ma, mb, p, grid, st, &gp)
                                 : run_gemm<128, 6, kSbTileT, kGroupRows>(ma, mb, p, grid, st, &gp);
   }
-  if (bn == 256) return run_gemm<256, 3, kSbCol, kGroupRed>(ma, mb, p, grid, st, &gp);
+  if (bn == 256) {
+    if (p.c_tma) return run_gemm<256, 3, kSbCol, kGroupRed, 128, true>(ma, mb, p, grid, st, &gp, &mc);
+    return run_gemm<256, 3, kSbCol, kGroupRed>(ma, mb, p, grid, st, &gp);
+  }
   return run_gemm<128, 6, kSbCol, kGroupRed>(ma, mb, p, grid, st, &gp);
 }
 

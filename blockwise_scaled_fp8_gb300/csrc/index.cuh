@@ -144,6 +144,9 @@ BFP8_HD GemmTile gemm_tile(int t, int num_m, int num_n, int bn) {
 // expert has num_m x num_n tiles, expert e the tiles e*num_m*num_n onwards.
 enum : int { kGroupNone = 0, kGroupRows = 1, kGroupRed = 2 };
 constexpr int kMaxGroups = 1024;
+// experts a grouped GEMM can have and still take the staged TMA-store epilogue
+// (its expert table shares shared memory with the staging buffers)
+constexpr int kStageGroups = 256;
 
 // The expert holding tile t: the largest e < E with start[e] <= t, given
 // start non-decreasing and start[0] <= t < start[E] (empty experts skipped).

@@ -73,6 +73,7 @@ ROW_CASES = [
     (1, None, 257, 384, 256),                      # one expert = the dense GEMM
     (8, None, 2048, 512, 1024),
     (16, None, 8192, 1024, 512),                   # more tiles than SMs
+    (12, None, 6000, 2056, 256),                   # staged TMA-store epilogue: tiles split at expert ends, 8-column last tile
 ]
 
 
@@ -125,6 +126,7 @@ RED_CASES = [
     (8, None, 4096, 512, 384),
     (3, [0, 0, 4096, 4096], 4096, 384, 1024),      # all tokens in one expert
     (16, None, 8192, 1024, 512),                   # more tiles than SMs
+    (16, None, 8192, 1000, 512),                   # staged TMA-store epilogue with a last row tile of 104 rows
 ]
 
 
