@@ -31,10 +31,11 @@ def _operands(M, N, K, seed):
     return qa, sa, qb, sb
 
 
-@pytest.mark.parametrize("M,N,K", [(256, 512, 384), (256, 4096, 384), (4, 512, 1024)])
+@pytest.mark.parametrize("M,N,K", [(256, 512, 384), (256, 4096, 384), (2048, 4096, 384), (4, 512, 1024)])
 def test_stalled_gemm_times_out_and_context_survives(M, N, K):
     """(256, 512, 384): the dense kernel's 32-column tiles (sixteen partial
-    buffers); (256, 4096, 384): its 64-column tiles; (4, 512, 1024): the
+    buffers); (256, 4096, 384): its 64-column tiles; (2048, 4096, 384): its
+    256-column tiles with the staged TMA-store epilogue; (4, 512, 1024): the
     small-M kernel, each of its 4 tiles split over a cluster of 8 CTAs; every
     CTA gives up and the cluster's hand-over of partial sums still completes
     before any CTA leaves."""
