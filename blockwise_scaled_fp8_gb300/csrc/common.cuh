@@ -262,24 +262,23 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
-// arrive on `bar` once every earlier cp.async of this thread has landed (the
-// arrival is counted in the barrier's expected count: .noinc)
-// Programmatic dependent launch.  Every kernel of this library is launched
-// with launch_pdl, so it may start (set up shared memory, barriers, tensor
-// memory) while the kernel before it in the stream is still finishing; it
-// calls pdl_wait() before its first global-memory access, read or write, and
-// that returns once the previous grid has completed with its writes visible.
-// pdl_launch_dependents() lets the next kernel start early; it is issued at
-// kernel entry (the next kernel is only scheduled once every CTA of this grid
-// has issued it, so it never takes a slot this grid still needs).
+// Programmatic dependent launch.  A kernel of this library launched with it
+// (launch_pdl, or launch_kernel with pdl set) may start (set up shared
+// memory, barriers, tensor memory) while the kernel before it in the stream
+// is still finishing; every kernel calls pdl_wait() before its first
+// global-memory access, read or write, which returns once the previous grid
+// has completed with its writes visible (at once when the kernel was launched
+// without it).  pdl_launch_dependents() lets the next kernel start early; it
+// is issued at kernel entry (the next kernel is only scheduled once every CTA
+// of this grid has issued it, so it never takes a slot this grid still needs).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 template <typename... P, typename... A>
-inline cudaError_t launch_pdl(void (*kernel)(P...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
-                              A&&... args) {
+inline cudaError_t launch_kernel(bool pdl, void (*kernel)(P...), unsigned grid, unsigned block, size_t smem,
+                                 cudaStream_t st, A&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(block);
@@ -289,10 +288,17 @@ inline cudaError_t launch_pdl(void (*kernel)(P...), unsigned grid, unsigned bloc
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
 }
+template <typename... P, typename... A>
+inline cudaError_t launch_pdl(void (*kernel)(P...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                              A&&... args) {
+  return launch_kernel(true, kernel, grid, block, smem, st, static_cast<A&&>(args)...);
+}
 
+// arrive on `bar` once every earlier cp.async of this thread has landed (the
+// arrival is counted in the barrier's expected count: .noinc)
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }

@@ -2557,14 +2557,14 @@ static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const 
     static_assert(Cfg::kDenseSmemBytes <= 227 * 1024, "shared memory budget (epilogue staging)");
     CUtensorMap none;  // (no C map: the kernel does not read it)
     if (!mc) memset(&none, 0, sizeof none);
-    return launch_pdl(gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW, A_ROWS>, (unsigned)grid, Cfg::kThreads,
-                      kSmem, st, ma, mb, mc ? *mc : none, p);
+    return launch_kernel(pdl_for_gemm(p.M, p.N, p.K), gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW, A_ROWS>,
+                         (unsigned)grid, Cfg::kThreads, kSmem, st, ma, mb, mc ? *mc : none, p);
   }
   else {
     CUtensorMap none;  // (no C map: the kernel does not read it)
     if (!mc) memset(&none, 0, sizeof none);
-    return launch_pdl(gemm_grouped_kernel<BN, STAGES, MODE, LDW, EW, GROUP, STG>, (unsigned)grid, Cfg::kThreads,
-                      kSmem, st, ma, mb, mc ? *mc : none, p, *gp);
+    return launch_kernel(pdl_for_gemm(p.M, p.N, p.K), gemm_grouped_kernel<BN, STAGES, MODE, LDW, EW, GROUP, STG>,
+                         (unsigned)grid, Cfg::kThreads, kSmem, st, ma, mb, mc ? *mc : none, p, *gp);
   }
 }
 

@@ -545,8 +545,9 @@ static cudaError_t run_tile(const CUtensorMap (&ma)[3], const CUtensorMap (&mb)[
                                 kQtSmemBytes);
   });
   if (attr != cudaSuccess) return attr;
-  return launch_pdl(quant_tile_kernel<MODE_A, MODE_B>, (unsigned)grid, kQtThreads, kQtSmemBytes, st, ma[0], ma[1],
-                    ma[2], mb[0], mb[1], mb[2], pa, pb);
+  const int64_t bytes_read = 2 * (pa.T * pa.C + (pb.num_tiles > 0 ? pb.T * pb.C : 0));
+  return launch_kernel(pdl_for_quant(bytes_read), quant_tile_kernel<MODE_A, MODE_B>, (unsigned)grid, kQtThreads,
+                       kQtSmemBytes, st, ma[0], ma[1], ma[2], mb[0], mb[1], mb[2], pa, pb);
 }
 
 // Tensor maps (input, q_row store, q_col store) and parameters of one input.
