@@ -75,6 +75,7 @@ struct GemmParams {
   uint64_t wait_limit_ns;
   int debug_stall;  // test hook: the promotion warps wait on a barrier nothing arrives on
   int c_tma = 0;    // (dense kernel, 256-column tiles) the epilogue stores through the C tensor map
+  int pdl = 1;      // launched with programmatic dependent launch: let the next kernel start early
 };
 
 // What the grouped (mixture-of-experts) forms add.  A separate kernel
@@ -332,7 +333,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW, A_ROWS>::kThreads, 1)
 
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const int lane = (int)(threadIdx.x & 31);
-  pdl_launch_dependents();
+  // only a kernel launched with programmatic dependent launch lets the next
+  // one start early; otherwise the next kernel starts once this one completes
+  if (p.pdl) pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -747,7 +750,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, STAGES, EW>::kThreads, 1)
 
   const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x >> 5), 0);
   const int lane = (int)(threadIdx.x & 31);
-  pdl_launch_dependents();
+  // only a kernel launched with programmatic dependent launch lets the next
+  // one start early; otherwise the next kernel starts once this one completes
+  if (p.pdl) pdl_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
@@ -2557,14 +2562,18 @@ static cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const 
     static_assert(Cfg::kDenseSmemBytes <= 227 * 1024, "shared memory budget (epilogue staging)");
     CUtensorMap none;  // (no C map: the kernel does not read it)
     if (!mc) memset(&none, 0, sizeof none);
-    return launch_kernel(pdl_for_gemm(p.M, p.N, p.K), gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW, A_ROWS>,
-                         (unsigned)grid, Cfg::kThreads, kSmem, st, ma, mb, mc ? *mc : none, p);
+    GemmParams q = p;
+    q.pdl = pdl_for_gemm(p.M, p.N, p.K);
+    return launch_kernel(q.pdl != 0, gemm_blockwise_kernel<BN, STAGES, MODE, LDW, EW, A_ROWS>, (unsigned)grid,
+                         Cfg::kThreads, kSmem, st, ma, mb, mc ? *mc : none, q);
   }
   else {
     CUtensorMap none;  // (no C map: the kernel does not read it)
     if (!mc) memset(&none, 0, sizeof none);
-    return launch_kernel(pdl_for_gemm(p.M, p.N, p.K), gemm_grouped_kernel<BN, STAGES, MODE, LDW, EW, GROUP, STG>,
-                         (unsigned)grid, Cfg::kThreads, kSmem, st, ma, mb, mc ? *mc : none, p, *gp);
+    GemmParams q = p;
+    q.pdl = pdl_for_gemm(p.M, p.N, p.K);
+    return launch_kernel(q.pdl != 0, gemm_grouped_kernel<BN, STAGES, MODE, LDW, EW, GROUP, STG>, (unsigned)grid,
+                         Cfg::kThreads, kSmem, st, ma, mb, mc ? *mc : none, q, *gp);
   }
 }
 

@@ -76,6 +76,7 @@ struct TileQuantParams {
   int has_q_row, has_q_col;
   int64_t tiles_c, num_tiles;
   uint64_t wait_limit_ns;
+  int pdl;  // launched with programmatic dependent launch: let the next kernel start early
   uint8_t* e_row;  // MXFP8: biased exponents of the dim0 and dim1 casts
   int64_t lde_row;
   uint8_t* e_col;
@@ -406,7 +407,9 @@ __global__ void __launch_bounds__(kQtThreads, 2)
   const uint32_t colred = sbase + kQtOffColRed;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t na = pa.num_tiles, num_tiles = pa.num_tiles + pb.num_tiles;
-  pdl_launch_dependents();
+  // only a kernel launched with programmatic dependent launch lets the next
+  // one start early; otherwise the next kernel starts once this one completes
+  if (pa.pdl) pdl_launch_dependents();
 
   if (tid == 0) {
     mbar_init(bar0, 1);
@@ -546,8 +549,10 @@ static cudaError_t run_tile(const CUtensorMap (&ma)[3], const CUtensorMap (&mb)[
   });
   if (attr != cudaSuccess) return attr;
   const int64_t bytes_read = 2 * (pa.T * pa.C + (pb.num_tiles > 0 ? pb.T * pb.C : 0));
-  return launch_kernel(pdl_for_quant(bytes_read), quant_tile_kernel<MODE_A, MODE_B>, (unsigned)grid, kQtThreads,
-                       kQtSmemBytes, st, ma[0], ma[1], ma[2], mb[0], mb[1], mb[2], pa, pb);
+  TileQuantParams qa = pa, qb = pb;
+  qa.pdl = qb.pdl = pdl_for_quant(bytes_read);
+  return launch_kernel(qa.pdl != 0, quant_tile_kernel<MODE_A, MODE_B>, (unsigned)grid, kQtThreads, kQtSmemBytes, st,
+                       ma[0], ma[1], ma[2], mb[0], mb[1], mb[2], qa, qb);
 }
 
 // Tensor maps (input, q_row store, q_col store) and parameters of one input.
@@ -581,6 +586,7 @@ static bool prepare_tile(const QuantTileArgs& a, CUtensorMap (&m)[3], TileQuantP
   p->tiles_c = cdiv(a.C, 128);
   p->num_tiles = cdiv(a.T, 128) * p->tiles_c;
   p->wait_limit_ns = kWaitLimitNs;
+  p->pdl = 1;
   p->e_row = a.e_row;
   p->lde_row = a.lde_row;
   p->e_col = a.e_col;

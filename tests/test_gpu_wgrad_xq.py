@@ -95,7 +95,20 @@ def test_wgrad_xq_full_size_sampled():
     got = B.gemm_1x128_128x1_xq(qa, sa, xd)
     torch.cuda.synchronize()
     B.check_device_errors()
-    assert torch.equal(got.view(torch.int16), ref.view(torch.int16)), "bits differ from the two-launch path"
+    diff = got.view(torch.int16) != ref.view(torch.int16)
+    if bool(diff.any()):
+        # say which side is off: both against the oracle at the first differing rows and columns
+        idx = diff.nonzero().cpu().numpy()
+        rows, cols = np.unique(idx[:, 0])[:4], np.unique(idx[:, 1])[:32]
+        qa_o, sa_o = O.quant_lhs(np.ascontiguousarray(dy[:, rows]), transposed=True)
+        qb_o, sb_o = O.quant_rhs(np.ascontiguousarray(x[:, cols]))
+        want = O.gemm(qa_o, sa_o, qb_o, sb_o, O.SB_COL, K)
+        tol = 2.0 ** -7 * np.abs(want) + 1e-3 * np.sqrt(np.mean(want ** 2))
+        sel = lambda t: host_bf16_as_f64(t[torch.from_numpy(rows).cuda()][:, torch.from_numpy(cols).cuda()])
+        ok_ref, ok_got = np.mean(np.abs(sel(ref) - want) <= tol), np.mean(np.abs(sel(got) - want) <= tol)
+        pytest.fail(f"bits differ from the two-launch path at {len(idx)} elements (rows {rows.tolist()}, "
+                    f"columns from {int(cols[0])}); within the oracle bound there: two-launch {ok_ref:.3f}, "
+                    f"fused {ok_got:.3f}")
     rng = np.random.default_rng(5)
     rows = np.sort(rng.choice(M, 16, replace=False))
     cols = np.sort(np.r_[rng.choice(N - 128, 128, replace=False), np.arange(N - 128, N)])
