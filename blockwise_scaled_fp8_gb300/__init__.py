@@ -22,7 +22,7 @@ EXPORTS = [
     "bfp8_last_error", "bfp8_quant_lhs", "bfp8_quant_rhs", "bfp8_quant_weight",
     "bfp8_gemm_1x128_128x128", "bfp8_gemm_1x128_128x1", "bfp8_linear_workspace_size",
     "bfp8_linear_fwd", "bfp8_linear_bwd", "bfp8_cast_e4m3", "bfp8_check_device_errors",
-    "bfp8_debug_write_counts", "bfp8_debug_gemm_stall", "bfp8_debug_gemm_pick_bn", "bfp8_quant_dual",
+    "bfp8_debug_write_counts", "bfp8_debug_gemm_stall", "bfp8_debug_gemm_pick_bn", "bfp8_debug_launch_pdl", "bfp8_quant_dual",
     "bfp8_linear_train_workspace_size", "bfp8_linear_fwd_train", "bfp8_linear_bwd_saved",
     "bfp8_linear_fwd_static", "bfp8_gemm_grouped_1x128_128x128", "bfp8_gemm_grouped_1x128_128x1",
     "bfp8_quant_dual_weight", "bfp8_mx_cast", "bfp8_linear_step_host_workspace_size",
@@ -68,6 +68,7 @@ def lib() -> ctypes.CDLL:
     L.bfp8_check_device_errors.argtypes = [vp]
     L.bfp8_debug_write_counts.argtypes = [i32, i64, i64, i64, i32, vp, vp, ctypes.POINTER(i64)]
     L.bfp8_debug_gemm_pick_bn.argtypes = [i64, i64, i32, i32]
+    L.bfp8_debug_launch_pdl.argtypes = [i32, i64, i64, i64]
     L.bfp8_quant_dual.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp]
     L.bfp8_mx_cast.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64, vp]
     L.bfp8_quant_dual_weight.argtypes = [vp, i64, i64, i64, vp, i64, vp, i64, vp, i64, vp, i64,

@@ -1137,6 +1137,13 @@ void replay_tile(int64_t T, int64_t C, bool rows_out, bool cols_out, int scale_k
 }
 }  // namespace
 
+int bfp8_debug_launch_pdl(int kind, int64_t a, int64_t b, int64_t c) {
+  if (a < 0 || b < 0 || c < 0) return -1;
+  if (kind == 0) return pdl_for_gemm(a, b, c) ? 1 : 0;
+  if (kind == 1) return pdl_for_quant(a) ? 1 : 0;
+  return -1;
+}
+
 int bfp8_debug_gemm_pick_bn(int64_t M, int64_t N, int col_scales, int num_sms) {
   if (M <= 0 || N <= 0 || num_sms <= 0) return 0;
   return gemm_pick_bn(M, N, col_scales != 0, num_sms);

@@ -481,12 +481,23 @@ BFP8_API bfp8_status bfp8_debug_write_counts(int kind, int64_t M, int64_t N, int
                                     uint32_t *counts, uint32_t *scale_counts, int64_t *oob);
 
 /*
- * Host test hook: the output tile width (64, 128, 224 or 256 columns) the
+ * Host test hook: the output tile width (32, 64, 128, 224 or 256 columns) the
  * GEMM launcher picks for an M x N output on a GPU of num_sms SMs
  * (col_scales != 0: the 1x128 x 128x1 GEMM).  Pure host arithmetic; returns
  * the width, or 0 for a non-positive size.
  */
 BFP8_API int bfp8_debug_gemm_pick_bn(int64_t M, int64_t N, int col_scales, int num_sms);
+
+/*
+ * Host test hook: whether a dense or grouped GEMM or a tiled quantisation of
+ * this size is launched with programmatic dependent launch (its set-up
+ * overlapping the end of the kernel before it; long kernels are launched
+ * without it, and then do not let the next kernel start early either).
+ * kind 0: a GEMM of a x b x c (M, N, K); kind 1: a quantisation reading a
+ * bytes of bf16 (b, c unused).  Pure host arithmetic; returns 1 or 0, or -1
+ * for an unknown kind or a negative size.
+ */
+BFP8_API int bfp8_debug_launch_pdl(int kind, int64_t a, int64_t b, int64_t c);
 
 #ifdef __cplusplus
 }

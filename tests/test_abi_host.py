@@ -315,6 +315,22 @@ def test_gemm_epilogue_index_replay_exactly_once(M, N, K, col_scales):
     assert oob == 0 and np.all(c == 1)
 
 
+def test_launch_policy_programmatic_dependent_launch():
+    """Which launches overlap their set-up with the kernel before them (host
+    logic): the short kernels of a 2048 x 4096 x 4096 linear step and of small
+    problems do, the long ones of the 8192-token and 16384 x 14336 x 4096
+    steps do not (measured faster without it)."""
+    pdl = lambda kind, a, b=0, c=0: B.lib().bfp8_debug_launch_pdl(kind, a, b, c)
+    assert pdl(0, 2048, 4096, 4096) == 1 and pdl(0, 2, 4096, 4096) == 1 and pdl(0, 512, 4096, 4096) == 1
+    assert pdl(0, 4096, 4096, 4096) == 0                 # exactly 2^37 FLOPs
+    assert pdl(0, 4096, 4096, 8192) == 0 and pdl(0, 16384, 14336, 4096) == 0 and pdl(0, 14336, 4096, 16384) == 0
+    mib = 1 << 20
+    assert pdl(1, 2 * 2048 * 4096 + 2 * 4096 * 4096) == 1   # x with W, 2048 x 4096 and 4096 x 4096: 48 MiB
+    assert pdl(1, 64 * mib - 2) == 1 and pdl(1, 64 * mib) == 0
+    assert pdl(1, 2 * 16384 * 14336) == 0                 # dY at MLP-up
+    assert pdl(2, 1) == -1 and pdl(0, -1, 1, 1) == -1
+
+
 def test_gemm_tile_width_choice():
     """Tile widths the launcher picks (host logic, 152 SMs): narrow tiles for
     problems that fill few SMs (1x128 x 128x128 only) -- 32 columns where
